@@ -1,0 +1,276 @@
+"""CPU oracle for the NVFP4 paged KV-cache path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and bench.py's ``cpu_baseline`` /
+``--impl reference`` legs may import this package.  The product path (the CUDA
+library ``libnvfp4kv.so`` and its Python binding) never imports, links or
+calls anything here, and this package shares no code with it: the arithmetic
+lives in ``nvfp4_oracle.c`` (plain C, fp64 attention, stated fp32 codec
+steps), and this module only marshals numpy arrays into it.
+
+The readings the oracle takes where the source pages are silent (scale
+formula, rounding, division by the quantized scale, zero blocks, nibble order,
+Q scheme, causal alignment, cache layout) are listed in ``nvfp4_oracle.h``.
+
+Parity status per function:
+  e2m1/e4m3 codec, block quantizer, append, gather/decode, attention,
+  cache_bytes -- pinned by tests/test_oracle_*.py (format definitions, a
+  library cast, brute force, closed forms, the pages' worked byte counts).
+  quantize_rows(mode=PER_ROW), the A4Q Q scheme -- the pages leave the scheme
+  open, so it is pinned only to its stated reading (round trip and error
+  bound), not to any external value: parity unpinned against the pages.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+
+GLOBAL = 0
+PER_ROW = 1
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C, no fused multiply-add)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or force or (
+        os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC),
+                                           os.path.getmtime(os.path.join(_HERE, "nvfp4_oracle.h"))))
+    if stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call([
+            "gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+            "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
+        lib.orc_e2m1_value.restype = f64
+        lib.orc_e2m1_value.argtypes = [ctypes.c_uint]
+        lib.orc_e4m3_value.restype = f64
+        lib.orc_e4m3_value.argtypes = [ctypes.c_uint]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint
+        lib.orc_e4m3_encode.argtypes = [f32]
+        lib.orc_e2m1_encode.restype = ctypes.c_uint
+        lib.orc_e2m1_encode.argtypes = [f32]
+        lib.orc_quantize_block16.argtypes = [P, f32, P, P]
+        lib.orc_quantize_rows.argtypes = [P, i64, i32, i32, f32, P, P, P]
+        lib.orc_dequantize_rows.argtypes = [P, P, i64, i32, P, f32, P]
+        lib.orc_kv_append.restype = i32
+        lib.orc_kv_append.argtypes = [P, P, P, i64, i32, i32, i32, i64, f32, f32, P, P, P, P]
+        lib.orc_gather_decode.restype = i32
+        lib.orc_gather_decode.argtypes = [P, P, P, i32, i32, i32, i32, i32, i64, f32, P]
+        lib.orc_attention_rows.argtypes = [P, P, i32, i32, P, P, i32, i32, i32, f64, P, P]
+        lib.orc_cache_bytes.restype = i64
+        lib.orc_cache_bytes.argtypes = [i64, i32, i32, i32]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+# --- formats -----------------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    return _load().orc_e2m1_value(int(code))
+
+
+def e4m3_value(byte: int) -> float:
+    return _load().orc_e4m3_value(int(byte))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().orc_e4m3_encode(float(np.float32(x))))
+
+
+def e2m1_encode(q: float) -> int:
+    return int(_load().orc_e2m1_encode(float(np.float32(q))))
+
+
+def e4m3_encode_array(x) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.orc_e4m3_encode(float(v)) for v in _f32(x).ravel()], dtype=np.uint8)
+
+
+def e2m1_encode_array(q) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.orc_e2m1_encode(float(v)) for v in _f32(q).ravel()], dtype=np.uint8)
+
+
+# --- codec -------------------------------------------------------------------
+
+def quantize_block16(x, g: float):
+    x = _f32(x)
+    assert x.shape == (16,)
+    packed = np.zeros(8, np.uint8)
+    scale = np.zeros(1, np.uint8)
+    _load().orc_quantize_block16(_ptr(x), float(np.float32(g)), _ptr(packed), _ptr(scale))
+    return packed, int(scale[0])
+
+
+def quantize_rows(x, mode: int = GLOBAL, g: float = 1.0):
+    """x: [rows, D] float32 -> (packed [rows, D/2] u8, scales [rows, D/16] u8,
+    row_g [rows] f32 or None)."""
+    x = _f32(x)
+    rows, D = x.shape
+    packed = np.zeros((rows, D // 2), np.uint8)
+    scales = np.zeros((rows, D // 16), np.uint8)
+    row_g = np.zeros(rows, np.float32) if mode == PER_ROW else None
+    _load().orc_quantize_rows(_ptr(x), rows, D, mode, float(np.float32(g)), _ptr(packed),
+                              _ptr(scales), _ptr(row_g) if row_g is not None else None)
+    return packed, scales, row_g
+
+
+def dequantize_rows(packed, scales, row_g=None, g: float = 1.0) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, half = packed.shape
+    D = half * 2
+    out = np.zeros((rows, D), np.float64)
+    rg = _f32(row_g) if row_g is not None else None
+    _load().orc_dequantize_rows(_ptr(packed), _ptr(scales), rows, D,
+                                _ptr(rg) if rg is not None else None,
+                                float(np.float32(g)), _ptr(out))
+    return out
+
+
+# --- paged cache -------------------------------------------------------------
+
+class Pools:
+    """The four byte pools of one layer's cache, in the stated layout:
+    data [pages][Hkv][page_size][D/2], scales [pages][Hkv][page_size][D/16]."""
+
+    def __init__(self, num_pages: int, Hkv: int, D: int = 128, page_size: int = 16,
+                 fill: int = 0):
+        self.num_pages, self.Hkv, self.D, self.page_size = num_pages, Hkv, D, page_size
+        shp_d = (num_pages, Hkv, page_size, D // 2)
+        shp_s = (num_pages, Hkv, page_size, D // 16)
+        self.k_data = np.full(shp_d, fill, np.uint8)
+        self.k_scale = np.full(shp_s, fill, np.uint8)
+        self.v_data = np.full(shp_d, fill, np.uint8)
+        self.v_scale = np.full(shp_s, fill, np.uint8)
+
+
+def kv_append(pools: Pools, k, v, slot_mapping, k_g: float, v_g: float) -> None:
+    """k, v: [T, Hkv, D] float32 (bf16 values); slot_mapping: [T] int64."""
+    k = _f32(k)
+    v = _f32(v)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T, Hkv, D = k.shape
+    assert Hkv == pools.Hkv and D == pools.D and slots.shape == (T,)
+    rc = _load().orc_kv_append(_ptr(k), _ptr(v), _ptr(slots), T, Hkv, D, pools.page_size,
+                               pools.num_pages, float(np.float32(k_g)), float(np.float32(v_g)),
+                               _ptr(pools.k_data), _ptr(pools.k_scale), _ptr(pools.v_data),
+                               _ptr(pools.v_scale))
+    if rc != 0:
+        raise ValueError("slot out of range")
+
+
+def gather_decode(pools: Pools, which: str, page_row, kv_len: int, head: int, g: float) -> np.ndarray:
+    data = pools.k_data if which == "k" else pools.v_data
+    scale = pools.k_scale if which == "k" else pools.v_scale
+    row = np.ascontiguousarray(page_row, dtype=np.int32)
+    out = np.zeros((kv_len, pools.D), np.float64)
+    rc = _load().orc_gather_decode(_ptr(data), _ptr(scale), _ptr(row), kv_len, head, pools.Hkv,
+                                   pools.D, pools.page_size, pools.num_pages,
+                                   float(np.float32(g)), _ptr(out))
+    if rc != 0:
+        raise ValueError("page id out of range")
+    return out
+
+
+# --- attention ---------------------------------------------------------------
+
+def attention_rows(q, pos, q_len: int, k, v, causal: bool, sm_scale: float):
+    """q: [n, D] float64 decoded queries at positions pos (within the request);
+    k, v: [kv_len, D] float64.  Returns (o [n, D] f64, lse [n] f64)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    n, D = q.shape
+    out = np.zeros((n, D), np.float64)
+    lse = np.zeros(n, np.float64)
+    _load().orc_attention_rows(_ptr(q), _ptr(pos), n, q_len, _ptr(k), _ptr(v), k.shape[0], D,
+                               int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def cache_bytes(num_pages: int, page_size: int, Hkv: int, D: int) -> int:
+    return int(_load().orc_cache_bytes(num_pages, page_size, Hkv, D))
+
+
+def decode_q_a4q(q_rows) -> np.ndarray:
+    """A4Q query as the kernel sees it: per-row dual-level quantization then
+    decode (R6, R5).  q_rows: [n, D] float32 -> [n, D] float64."""
+    packed, scales, row_g = quantize_rows(q_rows, PER_ROW)
+    return dequantize_rows(packed, scales, row_g=row_g)
+
+
+def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_g: float,
+                    v_g: float, causal: bool, sm_scale: float, q_mode: str = "bf16",
+                    rows=None):
+    """Attention of a ragged batch over the paged cache.
+
+    q: [total_q, Hq, D] float32 (bf16 values); q_mode "bf16" uses q as is,
+    "a4q" uses the per-row quantized-then-decoded query.  rows: optional list of
+    (request, position) pairs to evaluate (all rows of every request if None).
+    Returns dict {(request, position): (o [Hq, D], lse [Hq])}.
+    """
+    q = _f32(q)
+    qo = np.asarray(qo_indptr, dtype=np.int64)
+    kvl = np.asarray(kv_lens, dtype=np.int64)
+    pt = np.asarray(page_table, dtype=np.int32)
+    Hkv = pools.Hkv
+    G = Hq // Hkv
+    B = len(kvl)
+    want = {}
+    if rows is None:
+        for b in range(B):
+            for i in range(int(qo[b + 1] - qo[b])):
+                want.setdefault(b, []).append(i)
+    else:
+        for b, i in rows:
+            want.setdefault(int(b), []).append(int(i))
+    result = {}
+    for b, positions in want.items():
+        q_len = int(qo[b + 1] - qo[b])
+        kv_len = int(kvl[b])
+        positions = sorted(set(positions))
+        pos = np.array(positions, np.int32)
+        outs = {i: (np.zeros((Hq, pools.D)), np.zeros(Hq)) for i in positions}
+        for h in range(Hkv):
+            kd = gather_decode(pools, "k", pt[b], kv_len, h, k_g)
+            vd = gather_decode(pools, "v", pt[b], kv_len, h, v_g)
+            for gq in range(G):
+                hq = h * G + gq
+                qr = q[qo[b] + pos, hq, :]
+                qd = decode_q_a4q(qr) if q_mode == "a4q" else qr.astype(np.float64)
+                o, lse = attention_rows(qd, pos, q_len, kd, vd, causal, sm_scale)
+                for r, i in enumerate(positions):
+                    outs[i][0][hq] = o[r]
+                    outs[i][1][hq] = lse[r]
+        for i in positions:
+            result[(b, i)] = outs[i]
+    return result

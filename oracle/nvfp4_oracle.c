@@ -1,0 +1,238 @@
+/*
+ * CPU oracle for the NVFP4 paged KV-cache path.  TEST INFRASTRUCTURE ONLY:
+ * loaded by tests/, the smoke check and bench.py's cpu_baseline/reference
+ * legs, never by the product path.  Plain loops, written for checking by eye
+ * against the definitions; no blocking, fusion or reordering.
+ *
+ * Every function cites the passage it follows; the readings R1..R8 are
+ * stated in nvfp4_oracle.h.  Compile with -ffp-contract=off: each fp32 step
+ * below is one IEEE operation rounded to nearest even.
+ */
+#include "nvfp4_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* E2M1 magnitudes indexed by the 3 low code bits: the value set of a 1-sign,
+ * 2-exponent, 1-mantissa float with exponent bias 1 ([W] "NVFP4 KV cache vs
+ * NVFP4 weights": 4-bit E2M1 values). */
+static const double kE2M1Mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double orc_e2m1_value(unsigned code) {
+  double mag = kE2M1Mag[code & 7u];
+  return (code & 8u) ? -mag : mag;
+}
+
+/* OCP FP8 E4M3FN: sign, 4 exponent bits (bias 7), 3 mantissa bits, no
+ * infinities, S.1111.111 is NaN, max finite 448 ([W]: "an E4M3 scale for
+ * each block of 16 values"). */
+double orc_e4m3_value(unsigned byte) {
+  unsigned s = (byte >> 7) & 1u, e = (byte >> 3) & 15u, m = byte & 7u;
+  double v;
+  if (e == 15u && m == 7u) return NAN;
+  if (e == 0u)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+  return s ? -v : v;
+}
+
+/* R1: nearest non-negative finite E4M3 value, ties to the even code.  The
+ * codes 0x00..0x7E are in increasing value order, so a brute-force search over
+ * them is the definition of round-to-nearest; anything above 448 lands on
+ * 0x7E, which is the saturating behaviour. */
+unsigned orc_e4m3_encode(float x) {
+  double xd = (double)x;
+  /* Saturation first: far above 448 every candidate's distance rounds to the
+   * same double and the search below could not tell them apart. */
+  if (xd >= 448.0) return 0x7Eu;
+  unsigned best = 0;
+  double best_err = fabs(xd - orc_e4m3_value(0));
+  for (unsigned c = 1; c <= 0x7Eu; ++c) {
+    double err = fabs(xd - orc_e4m3_value(c));
+    if (err < best_err || (err == best_err && (c & 1u) == 0u && (best & 1u))) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return best;
+}
+
+/* R2: sign bit of q, then the nearest E2M1 magnitude with ties to the even
+ * code; magnitudes above 6 land on 6 (saturation). */
+unsigned orc_e2m1_encode(float q) {
+  double a = fabs((double)q);
+  if (a >= 6.0) return (signbit(q) ? 8u : 0u) | 7u; /* saturation, as above */
+  unsigned best = 0;
+  double best_err = a;
+  for (unsigned c = 1; c < 8u; ++c) {
+    double err = fabs(a - kE2M1Mag[c]);
+    if (err < best_err || (err == best_err && (c & 1u) == 0u && (best & 1u))) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (signbit(q) ? 8u : 0u) | best;
+}
+
+/* One block ([PD] "NVFP4 stores 4.5 bits per value before padding": one E4M3
+ * scale for each group of 16 elements; packed E2M1 pairs), steps R1..R4. */
+void orc_quantize_block16(const float* x, float g, uint8_t* packed8,
+                          uint8_t* scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  float six_g = 6.0f * g;                 /* fl32(6*g) */
+  float s_real = (amax == 0.0f) ? 0.0f : amax / six_g; /* fl32(amax/(6g)) */
+  unsigned sc = orc_e4m3_encode(s_real);
+  *scale = (uint8_t)sc;
+  unsigned codes[16];
+  double sdec = orc_e4m3_value(sc);
+  if (sdec == 0.0) { /* R3 */
+    for (int i = 0; i < 16; ++i) codes[i] = 0u;
+  } else {
+    float denom = g * (float)sdec;        /* fl32(g * e4m3(s)) */
+    for (int i = 0; i < 16; ++i) {
+      float q = x[i] / denom;             /* fl32(x / denom) */
+      codes[i] = orc_e2m1_encode(q);
+    }
+  }
+  for (int i = 0; i < 8; ++i) /* R4 */
+    packed8[i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));
+}
+
+void orc_quantize_rows(const float* x, int64_t rows, int D, int mode, float g,
+                       uint8_t* packed, uint8_t* scales, float* row_g) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* xr = x + r * (int64_t)D;
+    float gr = g;
+    if (mode == 1) { /* R6: dual level, one fp32 scale per row */
+      float amax = 0.0f;
+      for (int d = 0; d < D; ++d) {
+        float a = fabsf(xr[d]);
+        if (a > amax) amax = a;
+      }
+      gr = amax / 2688.0f; /* 2688 = 6 * 448, the largest FP4 x E4M3 product */
+      if (row_g) row_g[r] = gr;
+      if (gr == 0.0f) {
+        memset(packed + r * (int64_t)(D / 2), 0, (size_t)(D / 2));
+        memset(scales + r * (int64_t)(D / 16), 0, (size_t)(D / 16));
+        continue;
+      }
+    }
+    for (int b = 0; b < D / 16; ++b)
+      orc_quantize_block16(xr + 16 * b, gr,
+                           packed + r * (int64_t)(D / 2) + 8 * b,
+                           scales + r * (int64_t)(D / 16) + b);
+  }
+}
+
+/* R5 ([W]: the FP4 value, its block scale and the second scale). */
+void orc_dequantize_rows(const uint8_t* packed, const uint8_t* scales,
+                         int64_t rows, int D, const float* row_g, float g,
+                         double* out) {
+  for (int64_t r = 0; r < rows; ++r) {
+    double gr = row_g ? (double)row_g[r] : (double)g;
+    for (int d = 0; d < D; ++d) {
+      uint8_t byte = packed[r * (int64_t)(D / 2) + d / 2];
+      unsigned code = (d & 1) ? (byte >> 4) : (byte & 15u);
+      double s = orc_e4m3_value(scales[r * (int64_t)(D / 16) + d / 16]);
+      out[r * (int64_t)D + d] = orc_e2m1_value(code) * s * gr;
+    }
+  }
+}
+
+/* Byte offset of (slot, head) inside a pool whose per-token row is `row`
+ * bytes wide (R8). */
+static int64_t pool_offset(int64_t page, int64_t off, int head, int Hkv,
+                           int page_size, int row) {
+  return ((page * Hkv + head) * page_size + off) * (int64_t)row;
+}
+
+/* [PD] "NVFP4 stores 4.5 bits per value before padding": the cache write
+ * quantizes the new K and V, creates packed FP4 data, writes the block scales
+ * and maps the result into paged cache slots. */
+int orc_kv_append(const float* k, const float* v, const int64_t* slot_mapping,
+                  int64_t T, int Hkv, int D, int page_size, int64_t num_pages,
+                  float k_g, float v_g, uint8_t* k_data, uint8_t* k_scale,
+                  uint8_t* v_data, uint8_t* v_scale) {
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_pages * page_size) return -1;
+    int64_t page = slot / page_size, off = slot % page_size;
+    for (int h = 0; h < Hkv; ++h) {
+      const float* kr = k + (t * Hkv + h) * (int64_t)D;
+      const float* vr = v + (t * Hkv + h) * (int64_t)D;
+      orc_quantize_rows(kr, 1, D, 0, k_g,
+                        k_data + pool_offset(page, off, h, Hkv, page_size, D / 2),
+                        k_scale + pool_offset(page, off, h, Hkv, page_size, D / 16),
+                        NULL);
+      orc_quantize_rows(vr, 1, D, 0, v_g,
+                        v_data + pool_offset(page, off, h, Hkv, page_size, D / 2),
+                        v_scale + pool_offset(page, off, h, Hkv, page_size, D / 16),
+                        NULL);
+    }
+  }
+  return 0;
+}
+
+int orc_gather_decode(const uint8_t* data, const uint8_t* scale,
+                      const int32_t* page_row, int kv_len, int head, int Hkv,
+                      int D, int page_size, int64_t num_pages, float g,
+                      double* out) {
+  for (int j = 0; j < kv_len; ++j) {
+    int64_t page = page_row[j / page_size];
+    int64_t off = j % page_size;
+    if (page < 0 || page >= num_pages) return -1;
+    orc_dequantize_rows(data + pool_offset(page, off, head, Hkv, page_size, D / 2),
+                        scale + pool_offset(page, off, head, Hkv, page_size, D / 16),
+                        1, D, NULL, g, out + (int64_t)j * D);
+  }
+  return 0;
+}
+
+/* Softmax attention from its definition; the causal bound is R7. */
+void orc_attention_rows(const double* q, const int32_t* pos, int n_rows,
+                        int q_len, const double* k, const double* v,
+                        int kv_len, int D, int causal, double sm_scale,
+                        double* out, double* lse) {
+  double* s = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+  for (int r = 0; r < n_rows; ++r) {
+    const double* qr = q + (int64_t)r * D;
+    double* o = out + (int64_t)r * D;
+    int last = causal ? kv_len - q_len + pos[r] : kv_len - 1; /* last key seen */
+    if (last > kv_len - 1) last = kv_len - 1;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (last < 0) { /* no visible key: output 0, lse -inf */
+      if (lse) lse[r] = -INFINITY;
+      continue;
+    }
+    double m = -INFINITY;
+    for (int j = 0; j <= last; ++j) {
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qr[d] * k[(int64_t)j * D + d];
+      s[j] = sm_scale * dot;
+      if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int j = 0; j <= last; ++j) {
+      double p = exp(s[j] - m);
+      l += p;
+      for (int d = 0; d < D; ++d) o[d] += p * v[(int64_t)j * D + d];
+    }
+    for (int d = 0; d < D; ++d) o[d] /= l;
+    if (lse) lse[r] = m + log(l);
+  }
+  free(s);
+}
+
+/* [PD] "A worked per-token cache estimate" and "NVFP4 stores 4.5 bits per
+ * value before padding": K and V each hold D/2 packed bytes and D/16 scale
+ * bytes per (token, kv head). */
+int64_t orc_cache_bytes(int64_t num_pages, int page_size, int Hkv, int D) {
+  return 2 * num_pages * (int64_t)page_size * Hkv * (int64_t)(D / 2 + D / 16);
+}
