@@ -95,8 +95,9 @@ void orc_quantize_block16(const float* x, float g, uint8_t* packed8,
     for (int i = 0; i < 16; ++i) codes[i] = 0u;
   } else {
     float denom = g * (float)sdec;        /* fl32(g * e4m3(s)) */
+    float inv = 1.0f / denom;             /* fl32(1 / denom) */
     for (int i = 0; i < 16; ++i) {
-      float q = x[i] / denom;             /* fl32(x / denom) */
+      float q = x[i] * inv;               /* fl32(x * inv) */
       codes[i] = orc_e2m1_encode(q);
     }
   }

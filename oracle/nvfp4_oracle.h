@@ -28,8 +28,10 @@
  * design notes):
  *   R1 block scale   s = fl32(amax16 / fl32(6*g)), stored as E4M3 with
  *                    round-to-nearest-even, saturating to 448, subnormals kept.
- *   R2 codes         q = fl32(x / fl32(g * e4m3(s))) -- division by the
- *                    QUANTIZED scale -- then E2M1 round-to-nearest-even with
+ *   R2 codes         q = fl32(x * fl32(1 / fl32(g * e4m3(s)))) -- the value
+ *                    times the correctly rounded reciprocal of the QUANTIZED
+ *                    scale, the way NVFP4 quantizers apply a block scale --
+ *                    then E2M1 round-to-nearest-even with
  *                    ties to the even code, saturating to 6.  The sign bit of
  *                    q is kept, so a negative value that rounds to zero is
  *                    code 0x8 (decodes to -0, equal to 0).
