@@ -1,0 +1,199 @@
+/*
+ * nvfp4kv -- NVFP4 paged KV cache: append, A4Q paged prefill, paged decode.
+ * C ABI of libnvfp4kv.so (built for sm_103a only).
+ *
+ * The cache format is the one described on "NVFP4 KV cache prefill vs decode
+ * performance", section "NVFP4 stores 4.5 bits per value before padding"
+ * (packed E2M1 pairs, one E4M3 scale per 16 values) and "NVFP4 KV cache vs
+ * NVFP4 weights", section "NVFP4 KV cache vs NVFP4 weights" (a second,
+ * per-tensor FP32 scale).  Per layer the caller owns four device pools:
+ *
+ *   k_data, v_data   uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
+ *                    two E2M1 codes per byte, element 2i in the low nibble
+ *   k_scale, v_scale uint8 [num_pages][num_kv_heads][page_size][head_dim/16]
+ *                    one E4M3 (FN) block scale per 16 values, linear order
+ *
+ * A stored value decodes as e2m1(code) * e4m3(scale) * global_scale.  A token
+ * lives in slot = page * page_size + offset.  head_dim must be 128 and
+ * page_size 16; 144 bytes per (token, kv head) for K+V scales and codes of
+ * one tensor pair -- 4.5 bits per value, 56.25% of an FP8 cache.
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers unless a comment says HOST.  The
+ *     caller owns every buffer; the library allocates no device memory (the
+ *     prefill and decode calls take a caller-provided workspace).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, passed as void*;
+ *     NULL = legacy default stream) and return before the GPU work finishes.
+ *   - Return 0 (NVFP4KV_OK) or a negative NVFP4KV_ERR_* code.  Argument
+ *     errors are detected on the host before anything is launched.  Errors
+ *     that only the device can see (an out-of-range page id or slot, a causal
+ *     request with q_len > kv_len, a pipeline wait that timed out) are
+ *     recorded in a device status word and reported by
+ *     nvfp4kv_get_device_status(); the offending entries are skipped.
+ *   - Nothing crosses the ABI as an exception; nothing calls exit().
+ *   - Bounds: num_pages * page_size * num_kv_heads < 2^31 token-heads,
+ *     total_q * num_q_heads < 2^31.
+ */
+#ifndef NVFP4KV_H
+#define NVFP4KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVFP4KV_OK 0
+#define NVFP4KV_ERR_ARG (-1)          /* null pointer, bad size, misaligned pool */
+#define NVFP4KV_ERR_SHAPE (-2)        /* device saw q_len > kv_len (causal) or kv_len > table */
+#define NVFP4KV_ERR_WORKSPACE (-3)    /* workspace NULL or smaller than required */
+#define NVFP4KV_ERR_CUDA (-4)         /* a CUDA runtime/driver call failed */
+#define NVFP4KV_ERR_TIMEOUT (-5)      /* a bounded device wait gave up */
+#define NVFP4KV_ERR_DEVICE_INDEX (-6) /* device saw a page id / slot out of range */
+#define NVFP4KV_ERR_UNSUPPORTED (-7)  /* current device is not sm_103 */
+
+#define NVFP4KV_HEAD_DIM 128
+#define NVFP4KV_PAGE_SIZE 16
+
+/* Prefill variants ("NVFP4 KV cache A4Q prefill explained", sections
+ * "Quantize Q instead of expanding K" and "Compare A4Q with dequantize-ahead
+ * repacking"). */
+#define NVFP4KV_VARIANT_A4Q 0      /* Q quantized to NVFP4 in-kernel, QK on block-scaled FP4 MMA */
+#define NVFP4KV_VARIANT_DQ_AHEAD 1 /* K tile dequantized once to BF16, QK on BF16 MMA with BF16 Q */
+
+/* Quantize-rows modes. */
+#define NVFP4KV_QUANT_GLOBAL 0  /* one caller-given global scale for every row */
+#define NVFP4KV_QUANT_PER_ROW 1 /* per-row scale amax/2688 (the A4Q query scheme) */
+
+/* Workspace queries. */
+#define NVFP4KV_OP_PREFILL 0
+#define NVFP4KV_OP_DECODE 1
+
+/* Descriptor of one layer's cache (a HOST struct; the pools are device
+ * memory, each 16-byte aligned). */
+typedef struct nvfp4kv_cache {
+  void* k_data;
+  void* k_scale;
+  void* v_data;
+  void* v_scale;
+  int32_t num_pages;
+  int32_t page_size;    /* must be 16 */
+  int32_t num_kv_heads;
+  int32_t head_dim;     /* must be 128 */
+  float k_global_scale; /* decode multiplier of K (> 0, finite) */
+  float v_global_scale; /* decode multiplier of V (> 0, finite) */
+} nvfp4kv_cache_t;
+
+/* Cache append ("NVFP4 KV cache prefill vs decode performance", section
+ * "NVFP4 stores 4.5 bits per value before padding": the cache write quantizes
+ * BF16 input, creates packed FP4 data, writes block scales and maps the result
+ * into paged cache slots).
+ *
+ * k, v:          bf16 [num_tokens][num_kv_heads][128], row-contiguous.
+ * slot_mapping:  int64 [num_tokens]; token t goes to slot_mapping[t]; a
+ *                negative slot skips the token; a slot >= num_pages*page_size
+ *                is skipped and flagged (NVFP4KV_ERR_DEVICE_INDEX).
+ * Per 16-value block: s = amax/(6*g) rounded to E4M3 (nearest even,
+ * saturating at 448); codes = x * (1/(g*s)) rounded to E2M1 (nearest even,
+ * ties to the even code, saturating at 6); zero scale -> zero codes.
+ * num_tokens == 0 is a no-op. */
+int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                    const nvfp4kv_cache_t* cache, void* stream);
+
+/* Causal (or full) paged prefill attention over the NVFP4 cache
+ * ("NVFP4 KV cache A4Q prefill explained": A4Q quantizes each query tile to
+ * block-scaled FP4 and runs QK on native FP4 MMA against the cache's packed K
+ * and scales; PV stays wide with V dequantized).
+ *
+ * q:          bf16 [total_q][num_q_heads][128] (ragged requests, packed).
+ * qo_indptr:  int32 [batch+1], request b's queries are rows
+ *             qo_indptr[b] .. qo_indptr[b+1]-1 of q (qo_indptr[batch] <= total_q).
+ * kv_lens:    int32 [batch], cached tokens of each request (including the
+ *             new ones, which must already be appended).
+ * page_table: int32 [batch][max_pages_per_req]; entries past a request's
+ *             ceil(kv_len/16) pages are never read.
+ * causal:     1 = query i of a request sees keys j <= kv_len - q_len + i
+ *             (bottom-right alignment); 0 = every query sees all kv_len keys.
+ * sm_scale:   softmax scale applied to q.k (e.g. 1/sqrt(128)).
+ * variant:    NVFP4KV_VARIANT_A4Q or NVFP4KV_VARIANT_DQ_AHEAD.  The A4Q query
+ *             scheme is per (token, head) row: g_row = amax_row/2688, then the
+ *             same 16-value block codec as the cache.
+ * o:          bf16 [total_q][num_q_heads][128] output (rows of q not covered
+ *             by qo_indptr are left untouched).
+ * lse:        optional fp32 [total_q][num_q_heads] natural-log sum-exp of the
+ *             scaled scores; NULL to skip.
+ * workspace:  device buffer of at least
+ *             nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, batch, num_q_heads,
+ *             num_kv_heads, total_q, 0) bytes, 16-byte aligned; its contents
+ *             are overwritten (it holds the work schedule).
+ * num_q_heads must be a multiple of num_kv_heads with a power-of-two ratio
+ * of at most 128.  q_len == 0 requests produce nothing. */
+int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                        const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                        const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
+                        void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Paged decode: one query token per request attends to all kv_lens[b] cached
+ * tokens ("NVFP4 KV cache prefill vs decode performance", section "Decode can
+ * win on fewer bytes read": decode reads the long cache for one new token and
+ * is bandwidth-bound).  The query stays BF16; K and V are dequantized.
+ * q, o:       bf16 [batch][num_q_heads][128].
+ * lse:        optional fp32 [batch][num_q_heads].
+ * workspace:  nvfp4_workspace_bytes(NVFP4KV_OP_DECODE, batch, num_q_heads,
+ *             num_kv_heads, 0, max_pages_per_req*16) bytes (split-KV
+ *             partials).  kv_lens[b] == 0 gives a zero output row. */
+int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t* cache, const int32_t* page_table,
+                       int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o,
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for op (NVFP4KV_OP_PREFILL uses total_q, NVFP4KV_OP_DECODE
+ * uses max_kv_len).  Host-only, no CUDA call.  Returns 0 for bad arguments. */
+size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int64_t total_q,
+                             int32_t max_kv_len);
+
+/* Bytes of one layer's four pools ("NVFP4 KV cache prefill vs decode
+ * performance", section "A worked per-token cache estimate"):
+ * 2 * num_pages * page_size * num_kv_heads * (head_dim/2 + head_dim/16).
+ * Host-only.  Returns 0 for non-positive sizes or head_dim % 16 != 0. */
+size_t nvfp4_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
+
+/* The device quantizer of the cache write and of the A4Q query, exposed for
+ * standalone quantization ("NVFP4 KV cache A4Q prefill explained", section
+ * "Preserve the capacity and decode case": GPU quantize kernels with a linear
+ * block-scale layout).
+ * x:          bf16 [rows][128].
+ * packed:     uint8 [rows][64]; scales: uint8 [rows][8].
+ * mode:       NVFP4KV_QUANT_GLOBAL (uses global_scale > 0) or
+ *             NVFP4KV_QUANT_PER_ROW (writes fp32 row_scales[rows]). */
+int nvfp4_quantize_rows(const void* x, int64_t rows, int32_t mode, float global_scale, void* packed, void* scales,
+                        float* row_scales, void* stream);
+
+/* Inverse of nvfp4_quantize_rows: out bf16 [rows][128] =
+ * e2m1(code) * e4m3(scale) * (row_scales ? row_scales[r] : global_scale),
+ * rounded to bf16 (exact when the product has at most 8 significant bits). */
+int nvfp4_dequantize_rows(const void* packed, const void* scales, int64_t rows, const float* row_scales,
+                          float global_scale, void* out, void* stream);
+
+/* Synchronizes `stream`, then returns and clears the device status word of
+ * the current device: 0, or the NVFP4KV_ERR_* code of the first recorded
+ * condition (TIMEOUT before DEVICE_INDEX before SHAPE). */
+int nvfp4kv_get_device_status(void* stream);
+
+/* Static English text for a status code. */
+const char* nvfp4kv_status_string(int status);
+
+/* Test hook for the failure path: launches one thread that waits on a
+ * shared-memory barrier nothing will ever complete, with a wall-time limit of
+ * limit_ns (clamped to [1 us, 1 s]).  The wait gives up, records
+ * NVFP4KV_ERR_TIMEOUT in the status word and the kernel returns normally:
+ * the context stays usable.  Used to test nvfp4kv_get_device_status(). */
+int nvfp4kv_debug_wait_timeout(uint32_t limit_ns, void* stream);
+
+/* Library version, e.g. "nvfp4kv 0.1 sm_103a". */
+const char* nvfp4kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4KV_H */

@@ -1,0 +1,210 @@
+"""Thin Python binding of libnvfp4kv.so (argument marshalling only).
+
+Every function mirrors one C-ABI entry point of include/nvfp4kv.h and takes
+torch tensors that already live on the current CUDA device; the work runs in
+the library's kernels.  There is no fallback: if the compiled library is
+missing the import of this module raises.  PyTorch provides device memory and
+the current stream, nothing else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+NVFP4KV_OK = 0
+ERR_NAMES = {-1: "ERR_ARG", -2: "ERR_SHAPE", -3: "ERR_WORKSPACE", -4: "ERR_CUDA", -5: "ERR_TIMEOUT",
+             -6: "ERR_DEVICE_INDEX", -7: "ERR_UNSUPPORTED"}
+VARIANT_A4Q = 0
+VARIANT_DQ_AHEAD = 1
+QUANT_GLOBAL = 0
+QUANT_PER_ROW = 1
+OP_PREFILL = 0
+OP_DECODE = 1
+HEAD_DIM = 128
+PAGE_SIZE = 16
+
+EXPORTED = ["nvfp4_kv_append", "nvfp4_paged_prefill", "nvfp4_paged_decode", "nvfp4_workspace_bytes",
+            "nvfp4_cache_bytes", "nvfp4_quantize_rows", "nvfp4_dequantize_rows", "nvfp4kv_get_device_status",
+            "nvfp4kv_status_string", "nvfp4kv_version", "nvfp4kv_debug_wait_timeout"]
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("k_data", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_data", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("k_global_scale", ctypes.c_float), ("v_global_scale", ctypes.c_float)]
+
+
+class NvFp4Error(RuntimeError):
+    def __init__(self, where: str, code: int):
+        super().__init__(f"{where}: {ERR_NAMES.get(code, code)} ({status_string(code)})")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"libnvfp4kv.so has not been built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    D = ctypes.POINTER(CacheDesc)
+    lib.nvfp4_kv_append.argtypes = [P, P, P, i64, D, P]
+    lib.nvfp4_paged_prefill.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, P, P, P, sz, P]
+    lib.nvfp4_paged_decode.argtypes = [P, i32, D, P, i32, P, i32, f32, P, P, P, sz, P]
+    lib.nvfp4_workspace_bytes.argtypes = [i32, i32, i32, i32, i64, i32]
+    lib.nvfp4_workspace_bytes.restype = sz
+    lib.nvfp4_cache_bytes.argtypes = [i32, i32, i32, i32]
+    lib.nvfp4_cache_bytes.restype = sz
+    lib.nvfp4_quantize_rows.argtypes = [P, i64, i32, f32, P, P, P, P]
+    lib.nvfp4_dequantize_rows.argtypes = [P, P, i64, P, f32, P, P]
+    lib.nvfp4kv_get_device_status.argtypes = [P]
+    lib.nvfp4kv_status_string.argtypes = [ctypes.c_int]
+    lib.nvfp4kv_status_string.restype = ctypes.c_char_p
+    lib.nvfp4kv_version.restype = ctypes.c_char_p
+    lib.nvfp4kv_debug_wait_timeout.argtypes = [ctypes.c_uint32, P]
+    lib.nvfp4kv_debug_wait_timeout.restype = ctypes.c_int
+    for name in ("nvfp4_kv_append", "nvfp4_paged_prefill", "nvfp4_paged_decode", "nvfp4_quantize_rows",
+                 "nvfp4_dequantize_rows", "nvfp4kv_get_device_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+def status_string(code: int) -> str:
+    return lib.nvfp4kv_status_string(int(code)).decode()
+
+
+def _check(where: str, rc: int) -> None:
+    if rc != NVFP4KV_OK:
+        raise NvFp4Error(where, rc)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to nvfp4kv must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Cache:
+    """One layer's NVFP4 cache: four caller-owned device pools (uint8 tensors)
+    in the documented layout, plus the two per-tensor scales."""
+
+    def __init__(self, num_pages: int, num_kv_heads: int, k_global_scale: float, v_global_scale: float,
+                 device=None, fill: Optional[int] = 0):
+        dev = device or torch.device("cuda")
+        shp_d = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 2)
+        shp_s = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 16)
+        mk = (lambda s: torch.zeros(s, dtype=torch.uint8, device=dev)) if fill == 0 else \
+            (lambda s: torch.full(s, int(fill), dtype=torch.uint8, device=dev))
+        self.k_data, self.k_scale = mk(shp_d), mk(shp_s)
+        self.v_data, self.v_scale = mk(shp_d), mk(shp_s)
+        self.num_pages, self.num_kv_heads = num_pages, num_kv_heads
+        self.k_global_scale, self.v_global_scale = float(k_global_scale), float(v_global_scale)
+
+    def desc(self) -> CacheDesc:
+        return CacheDesc(self.k_data.data_ptr(), self.k_scale.data_ptr(), self.v_data.data_ptr(),
+                         self.v_scale.data_ptr(), self.num_pages, PAGE_SIZE, self.num_kv_heads, HEAD_DIM,
+                         self.k_global_scale, self.v_global_scale)
+
+
+def nvfp4_cache_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib.nvfp4_cache_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
+def nvfp4_workspace_bytes(op: int, batch: int, num_q_heads: int, num_kv_heads: int, total_q: int = 0,
+                          max_kv_len: int = 0) -> int:
+    return int(lib.nvfp4_workspace_bytes(op, batch, num_q_heads, num_kv_heads, total_q, max_kv_len))
+
+
+def nvfp4_kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, cache: Cache, stream=None) -> None:
+    assert k.dtype == torch.bfloat16 and v.dtype == torch.bfloat16 and slot_mapping.dtype == torch.int64
+    d = cache.desc()
+    _check("nvfp4_kv_append", lib.nvfp4_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
+                                                  ctypes.byref(d), _stream(stream)))
+
+
+def nvfp4_paged_prefill(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, kv_lens: torch.Tensor,
+                        qo_indptr: torch.Tensor, causal: bool = True, sm_scale: Optional[float] = None,
+                        variant: int = VARIANT_A4Q, out: Optional[torch.Tensor] = None,
+                        lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    assert q.dtype == torch.bfloat16 and page_table.dtype == torch.int32
+    assert kv_lens.dtype == torch.int32 and qo_indptr.dtype == torch.int32
+    total_q, hq, _ = q.shape
+    batch = kv_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if sm_scale is None:
+        sm_scale = HEAD_DIM ** -0.5
+    need = nvfp4_workspace_bytes(OP_PREFILL, batch, hq, cache.num_kv_heads, total_q, 0)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    d = cache.desc()
+    _check("nvfp4_paged_prefill", lib.nvfp4_paged_prefill(
+        _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+        _ptr(qo_indptr), batch, int(bool(causal)), float(sm_scale), int(variant), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def nvfp4_paged_decode(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, kv_lens: torch.Tensor,
+                       sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                       lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    assert q.dtype == torch.bfloat16 and page_table.dtype == torch.int32 and kv_lens.dtype == torch.int32
+    batch, hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if sm_scale is None:
+        sm_scale = HEAD_DIM ** -0.5
+    need = nvfp4_workspace_bytes(OP_DECODE, batch, hq, cache.num_kv_heads, 0, page_table.shape[1] * PAGE_SIZE)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    d = cache.desc()
+    _check("nvfp4_paged_decode", lib.nvfp4_paged_decode(
+        _ptr(q), hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens), batch,
+        float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return out
+
+
+def nvfp4_quantize_rows(x: torch.Tensor, mode: int = QUANT_GLOBAL, global_scale: float = 1.0, stream=None):
+    assert x.dtype == torch.bfloat16 and x.shape[-1] == HEAD_DIM
+    rows = x.numel() // HEAD_DIM
+    packed = torch.empty(rows, HEAD_DIM // 2, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(rows, HEAD_DIM // 16, dtype=torch.uint8, device=x.device)
+    row_scales = torch.empty(rows, dtype=torch.float32, device=x.device) if mode == QUANT_PER_ROW else None
+    _check("nvfp4_quantize_rows", lib.nvfp4_quantize_rows(_ptr(x), rows, mode, float(global_scale), _ptr(packed),
+                                                          _ptr(scales), _ptr(row_scales), _stream(stream)))
+    return packed, scales, row_scales
+
+
+def nvfp4_dequantize_rows(packed: torch.Tensor, scales: torch.Tensor, row_scales: Optional[torch.Tensor] = None,
+                          global_scale: float = 1.0, stream=None) -> torch.Tensor:
+    rows = packed.shape[0]
+    out = torch.empty(rows, HEAD_DIM, dtype=torch.bfloat16, device=packed.device)
+    _check("nvfp4_dequantize_rows", lib.nvfp4_dequantize_rows(_ptr(packed), _ptr(scales), rows, _ptr(row_scales),
+                                                              float(global_scale), _ptr(out), _stream(stream)))
+    return out
+
+
+def nvfp4kv_debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check("nvfp4kv_debug_wait_timeout", lib.nvfp4kv_debug_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def nvfp4kv_get_device_status(stream=None) -> int:
+    return int(lib.nvfp4kv_get_device_status(_stream(stream)))

@@ -1,0 +1,365 @@
+// C ABI of libnvfp4kv.so: argument validation on the host, the device status
+// word, TMA descriptors for the K pools, and kernel launches.  No entry point
+// allocates device memory; nothing throws across the boundary.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.cuh"
+#include "nvfp4kv.h"
+
+namespace nvfp4kv {
+size_t prefill_smem_bytes(int variant);
+}
+
+using namespace nvfp4kv;
+
+namespace {
+
+__device__ int g_status_word;  // bit set of kDev* conditions, read + cleared by nvfp4kv_get_device_status
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool init = false;
+  int rc = NVFP4KV_OK;
+  int num_sms = 0;
+  int* status = nullptr;  // device address of g_status_word on this device
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device set-up on first use (device current): capability check, SM
+// count, status word address.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4KV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return NVFP4KV_ERR_CUDA;
+    }
+    d.num_sms = sms;
+    if (major != 10 || minor != 3) {
+      d.rc = NVFP4KV_ERR_UNSUPPORTED;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return NVFP4KV_ERR_CUDA;
+      d.status = static_cast<int*>(p);
+      d.rc = NVFP4KV_OK;
+    }
+    d.init = true;
+  }
+  *out = &d;
+  return d.rc;
+}
+
+int get_encoder() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode) return NVFP4KV_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return NVFP4KV_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return NVFP4KV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool finite_pos(float x) { return std::isfinite(x) && x > 0.0f; }
+
+int check_cache(const nvfp4kv_cache_t* c) {
+  if (!c) return NVFP4KV_ERR_ARG;
+  if (!c->k_data || !c->k_scale || !c->v_data || !c->v_scale) return NVFP4KV_ERR_ARG;
+  if (!aligned16(c->k_data) || !aligned16(c->k_scale) || !aligned16(c->v_data) || !aligned16(c->v_scale))
+    return NVFP4KV_ERR_ARG;
+  if (c->page_size != kPageSize || c->head_dim != kHeadDim) return NVFP4KV_ERR_ARG;
+  if (c->num_pages <= 0 || c->num_kv_heads <= 0 || c->num_kv_heads > 255) return NVFP4KV_ERR_ARG;
+  if (static_cast<int64_t>(c->num_pages) * c->num_kv_heads * kPageSize >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  if (!finite_pos(c->k_global_scale) || !finite_pos(c->v_global_scale)) return NVFP4KV_ERR_ARG;
+  return NVFP4KV_OK;
+}
+
+int log2_exact(int x) {
+  if (x <= 0 || (x & (x - 1)) != 0) return -1;
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+int64_t prefill_max_items(int64_t total_q, int batch, int num_q_heads, int num_kv_heads) {
+  const int64_t group = num_q_heads / num_kv_heads;
+  return (static_cast<int64_t>((total_q * group + kBM - 1) / kBM) + batch) * num_kv_heads;
+}
+
+int launch_rc(cudaError_t e) { return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA; }
+
+// A wait that can only end by its time limit (nothing arrives on `bar`).
+__global__ void nvfp4_debug_wait_kernel(uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  mbar_wait(&bar, 0, status, limit_ns);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nvfp4_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_pages <= 0 || page_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 16 != 0) return 0;
+  return 2ull * static_cast<size_t>(num_pages) * page_size * num_kv_heads * (head_dim / 2 + head_dim / 16);
+}
+
+size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int64_t total_q,
+                             int32_t max_kv_len) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+  if (op == NVFP4KV_OP_PREFILL) {
+    if (total_q < 0) return 0;
+    const int64_t items = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
+    const size_t bytes = 16 + 8 * static_cast<size_t>(items) + 4 * (static_cast<size_t>(batch) + 1);
+    return (bytes + 15) & ~static_cast<size_t>(15);
+  }
+  if (op == NVFP4KV_OP_DECODE) {
+    if (max_kv_len < 0) return 0;
+    const size_t splits = (static_cast<size_t>(max_kv_len) + kDecSplit - 1) / kDecSplit;
+    return static_cast<size_t>(batch) * splits * num_q_heads * (kHeadDim + 1) * sizeof(float);
+  }
+  return 0;
+}
+
+int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                    const nvfp4kv_cache_t* cache, void* stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (num_tokens < 0) return NVFP4KV_ERR_ARG;
+  if (num_tokens == 0) return NVFP4KV_OK;
+  if (!k || !v || !slot_mapping || !aligned16(k) || !aligned16(v)) return NVFP4KV_ERR_ARG;
+  const int64_t rows = num_tokens * cache->num_kv_heads;
+  if (rows * 4 / 256 + 1 >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  AppendArgs a;
+  a.k = k;
+  a.v = v;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.num_slots = static_cast<int64_t>(cache->num_pages) * cache->page_size;
+  a.k_data = static_cast<uint8_t*>(cache->k_data);
+  a.k_scale = static_cast<uint8_t*>(cache->k_scale);
+  a.v_data = static_cast<uint8_t*>(cache->v_data);
+  a.v_scale = static_cast<uint8_t*>(cache->v_scale);
+  a.k_scale_g = cache->k_global_scale;
+  a.v_scale_g = cache->v_global_scale;
+  a.status = d->status;
+  const int64_t threads = rows * 4;
+  dim3 grid(static_cast<unsigned>((threads + 255) / 256), 2);
+  nvfp4_kv_append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_rc(cudaGetLastError());
+}
+
+int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                        const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                        const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
+                        void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (batch < 0 || total_q < 0 || max_pages_per_req <= 0) return NVFP4KV_ERR_ARG;
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return NVFP4KV_ERR_ARG;
+  const int lg = log2_exact(num_q_heads / cache->num_kv_heads);
+  if (lg < 0 || lg > 7) return NVFP4KV_ERR_ARG;
+  if (causal != 0 && causal != 1) return NVFP4KV_ERR_ARG;
+  if (variant != NVFP4KV_VARIANT_A4Q && variant != NVFP4KV_VARIANT_DQ_AHEAD) return NVFP4KV_ERR_ARG;
+  if (!std::isfinite(sm_scale)) return NVFP4KV_ERR_ARG;
+  if (total_q * num_q_heads >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  if (batch == 0 || total_q == 0) return NVFP4KV_OK;
+  if (!q || !o || !page_table || !kv_lens || !qo_indptr || !aligned16(q) || !aligned16(o)) return NVFP4KV_ERR_ARG;
+  const size_t need = nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, batch, num_q_heads, cache->num_kv_heads, total_q, 0);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return NVFP4KV_ERR_WORKSPACE;
+  const int64_t max_items = prefill_max_items(total_q, batch, num_q_heads, cache->num_kv_heads);
+  if (max_items >= (int64_t(1) << 30)) return NVFP4KV_ERR_ARG;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  if ((rc = get_encoder())) return rc;
+
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(cache->num_pages) * cache->num_kv_heads * kPageSize};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, kPageSize};
+  const cuuint32_t estr[2] = {1, 1};
+  if (g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, cache->k_data, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return NVFP4KV_ERR_CUDA;
+
+  PlanArgs plan;
+  plan.kv_lens = kv_lens;
+  plan.qo_indptr = qo_indptr;
+  plan.total_q = total_q;
+  plan.batch = batch;
+  plan.max_pages = max_pages_per_req;
+  plan.num_kv_heads = cache->num_kv_heads;
+  plan.log2_group = lg;
+  plan.causal = causal;
+  plan.work = static_cast<int*>(workspace);
+  plan.max_items = static_cast<int>(max_items);
+  plan.status = d->status;
+
+  PrefillArgs a;
+  a.q = q;
+  a.k_scale = static_cast<const uint8_t*>(cache->k_scale);
+  a.v_data = static_cast<const uint8_t*>(cache->v_data);
+  a.v_scale = static_cast<const uint8_t*>(cache->v_scale);
+  a.page_table = page_table;
+  a.kv_lens = kv_lens;
+  a.qo_indptr = qo_indptr;
+  a.total_q = total_q;
+  a.batch = batch;
+  a.max_pages = max_pages_per_req;
+  a.num_pages = cache->num_pages;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.num_q_heads = num_q_heads;
+  a.group = 1 << lg;
+  a.log2_group = lg;
+  a.causal = causal;
+  a.sm_scale = sm_scale;
+  a.k_g = cache->k_global_scale;
+  a.v_g = cache->v_global_scale;
+  a.o = o;
+  a.lse = lse;
+  a.work = static_cast<const int*>(workspace);
+  a.status = d->status;
+  return launch_rc(launch_prefill(a, plan, tmap, variant, d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t* cache, const int32_t* page_table,
+                       int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o,
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (batch < 0 || max_pages_per_req <= 0) return NVFP4KV_ERR_ARG;
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return NVFP4KV_ERR_ARG;
+  const int lg = log2_exact(num_q_heads / cache->num_kv_heads);
+  if (lg < 0 || lg > 4) return NVFP4KV_ERR_ARG;
+  if (!std::isfinite(sm_scale)) return NVFP4KV_ERR_ARG;
+  if (batch == 0) return NVFP4KV_OK;
+  if (!q || !o || !page_table || !kv_lens || !aligned16(q) || !aligned16(o)) return NVFP4KV_ERR_ARG;
+  const int64_t max_kv = static_cast<int64_t>(max_pages_per_req) * kPageSize;
+  if (max_kv >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  const size_t need = nvfp4_workspace_bytes(NVFP4KV_OP_DECODE, batch, num_q_heads, cache->num_kv_heads, 0,
+                                            static_cast<int32_t>(max_kv));
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return NVFP4KV_ERR_WORKSPACE;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  DecodeArgs a;
+  a.q = q;
+  a.k_data = static_cast<const uint8_t*>(cache->k_data);
+  a.k_scale = static_cast<const uint8_t*>(cache->k_scale);
+  a.v_data = static_cast<const uint8_t*>(cache->v_data);
+  a.v_scale = static_cast<const uint8_t*>(cache->v_scale);
+  a.page_table = page_table;
+  a.kv_lens = kv_lens;
+  a.max_pages = max_pages_per_req;
+  a.num_pages = cache->num_pages;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.num_q_heads = num_q_heads;
+  a.max_splits = static_cast<int>((max_kv + kDecSplit - 1) / kDecSplit);
+  a.k_g = cache->k_global_scale;
+  a.v_g = cache->v_global_scale;
+  a.sm_scale = sm_scale;
+  a.o = o;
+  a.lse = lse;
+  float* ws = static_cast<float*>(workspace);
+  a.part_o = ws;
+  a.part_lse = ws + static_cast<size_t>(batch) * a.max_splits * num_q_heads * kHeadDim;
+  a.status = d->status;
+  return launch_rc(launch_decode(a, batch, static_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4_quantize_rows(const void* x, int64_t rows, int32_t mode, float global_scale, void* packed, void* scales,
+                        float* row_scales, void* stream) {
+  if (rows < 0 || (mode != NVFP4KV_QUANT_GLOBAL && mode != NVFP4KV_QUANT_PER_ROW)) return NVFP4KV_ERR_ARG;
+  if (mode == NVFP4KV_QUANT_GLOBAL && !finite_pos(global_scale)) return NVFP4KV_ERR_ARG;
+  if (rows == 0) return NVFP4KV_OK;
+  if (!x || !packed || !scales || !aligned16(x) || (reinterpret_cast<uintptr_t>(packed) & 7u)) return NVFP4KV_ERR_ARG;
+  if (mode == NVFP4KV_QUANT_PER_ROW && !row_scales) return NVFP4KV_ERR_ARG;
+  if (rows * 32 / 256 + 1 >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  DeviceState* d = nullptr;
+  int rc;
+  if ((rc = device_state(&d))) return rc;
+  QuantArgs a{x, rows, mode, global_scale, static_cast<uint8_t*>(packed), static_cast<uint8_t*>(scales), row_scales};
+  nvfp4_quantize_rows_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_rc(cudaGetLastError());
+}
+
+int nvfp4_dequantize_rows(const void* packed, const void* scales, int64_t rows, const float* row_scales,
+                          float global_scale, void* out, void* stream) {
+  if (rows < 0) return NVFP4KV_ERR_ARG;
+  if (!row_scales && !finite_pos(global_scale)) return NVFP4KV_ERR_ARG;
+  if (rows == 0) return NVFP4KV_OK;
+  if (!packed || !scales || !out || (reinterpret_cast<uintptr_t>(packed) & 3u) || !aligned16(out)) return NVFP4KV_ERR_ARG;
+  if (rows * 16 / 256 + 1 >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  DeviceState* d = nullptr;
+  int rc;
+  if ((rc = device_state(&d))) return rc;
+  DequantArgs a{static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(scales), rows, row_scales,
+                global_scale, out};
+  nvfp4_dequantize_rows_kernel<<<static_cast<unsigned>((rows * 16 + 255) / 256), 256, 0,
+                                 static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_rc(cudaGetLastError());
+}
+
+int nvfp4kv_get_device_status(void* stream) {
+  DeviceState* d = nullptr;
+  int rc;
+  if ((rc = device_state(&d))) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVFP4KV_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NVFP4KV_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return NVFP4KV_ERR_CUDA;
+  if (word & kDevTimeout) return NVFP4KV_ERR_TIMEOUT;
+  if (word & (kDevBadPage | kDevBadSlot)) return NVFP4KV_ERR_DEVICE_INDEX;
+  if (word & kDevBadShape) return NVFP4KV_ERR_SHAPE;
+  return NVFP4KV_OK;
+}
+
+const char* nvfp4kv_status_string(int status) {
+  switch (status) {
+    case NVFP4KV_OK: return "ok";
+    case NVFP4KV_ERR_ARG: return "invalid argument";
+    case NVFP4KV_ERR_SHAPE: return "invalid request shape (q_len > kv_len for causal, or kv_len beyond the page table)";
+    case NVFP4KV_ERR_WORKSPACE: return "workspace missing or too small";
+    case NVFP4KV_ERR_CUDA: return "CUDA call failed";
+    case NVFP4KV_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case NVFP4KV_ERR_DEVICE_INDEX: return "page id or slot out of range";
+    case NVFP4KV_ERR_UNSUPPORTED: return "device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+int nvfp4kv_debug_wait_timeout(uint32_t limit_ns, void* stream) {
+  DeviceState* d = nullptr;
+  int rc;
+  if ((rc = device_state(&d))) return rc;
+  uint64_t lim = limit_ns < 1000u ? 1000u : limit_ns;
+  if (lim > 1000000000ull) lim = 1000000000ull;
+  nvfp4_debug_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(lim, d->status);
+  return launch_rc(cudaGetLastError());
+}
+
+const char* nvfp4kv_version(void) { return "nvfp4kv 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// Kernel argument blocks and launch-shape constants shared by the kernel
+// translation units and the C-ABI host code.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "codec.cuh"
+#include "ptx.cuh"
+
+namespace nvfp4kv {
+
+constexpr int kHeadDim = 128;
+constexpr int kPageSize = 16;
+
+struct AppendArgs {
+  const void* k;
+  const void* v;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int num_kv_heads;
+  int64_t num_slots;  // num_pages * page_size
+  uint8_t* k_data;
+  uint8_t* k_scale;
+  uint8_t* v_data;
+  uint8_t* v_scale;
+  float k_scale_g;
+  float v_scale_g;
+  int* status;
+};
+
+struct QuantArgs {
+  const void* x;
+  int64_t rows;
+  int mode;
+  float global_scale;
+  uint8_t* packed;
+  uint8_t* scales;
+  float* row_scales;
+};
+
+struct DequantArgs {
+  const uint8_t* packed;
+  const uint8_t* scales;
+  int64_t rows;
+  const float* row_scales;
+  float global_scale;
+  void* out;
+};
+
+// ---- decode --------------------------------------------------------------------
+constexpr int kDecSplit = 256;   // tokens per CTA (16 pages)
+constexpr int kDecWarps = 4;
+
+struct DecodeArgs {
+  const void* q;  // bf16 [B][Hq][128]
+  const uint8_t* k_data;
+  const uint8_t* k_scale;
+  const uint8_t* v_data;
+  const uint8_t* v_scale;
+  const int32_t* page_table;
+  const int32_t* kv_lens;
+  int max_pages;
+  int num_pages;
+  int num_kv_heads;
+  int num_q_heads;
+  int max_splits;
+  float k_g, v_g, sm_scale;
+  void* o;            // bf16 [B][Hq][128]
+  float* lse;         // optional [B][Hq]
+  float* part_o;      // [B][max_splits][Hq][128]
+  float* part_lse;    // [B][max_splits][Hq]  (log2 domain)
+  int* status;
+};
+
+// ---- prefill -------------------------------------------------------------------
+constexpr int kBM = 128;        // query rows per tile (tokens x grouped heads)
+constexpr int kBN = 128;        // keys per KV tile (8 pages)
+constexpr int kPagesPerTile = kBN / kPageSize;
+
+struct PrefillArgs {
+  const void* q;  // bf16 [total_q][Hq][128]
+  const uint8_t* k_scale;
+  const uint8_t* v_data;
+  const uint8_t* v_scale;
+  const int32_t* page_table;
+  const int32_t* kv_lens;
+  const int32_t* qo_indptr;
+  int64_t total_q;
+  int batch;
+  int max_pages;
+  int num_pages;
+  int num_kv_heads;
+  int num_q_heads;
+  int group;        // num_q_heads / num_kv_heads (power of two)
+  int log2_group;
+  int causal;
+  float sm_scale, k_g, v_g;
+  void* o;          // bf16 [total_q][Hq][128]
+  float* lse;       // optional [total_q][Hq]
+  const int* work;  // work[0] = item count, items from work + 4 (int2 each)
+  int* status;
+};
+
+struct PlanArgs {
+  const int32_t* kv_lens;
+  const int32_t* qo_indptr;
+  int64_t total_q;
+  int batch;
+  int max_pages;
+  int num_kv_heads;
+  int log2_group;
+  int causal;
+  int* work;  // output schedule
+  int max_items;
+  int* status;
+};
+
+// Kernels (defined in append.cu, decode.cu, prefill.cu).
+__global__ void nvfp4_kv_append_kernel(AppendArgs a);
+__global__ void nvfp4_quantize_rows_kernel(QuantArgs a);
+__global__ void nvfp4_dequantize_rows_kernel(DequantArgs a);
+
+// Launchers that hide templates (decode.cu / prefill.cu).
+cudaError_t launch_decode(const DecodeArgs& a, int batch, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, const CUtensorMap& tmap_k, int variant,
+                           int num_sms, cudaStream_t s);
+
+}  // namespace nvfp4kv

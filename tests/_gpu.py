@@ -1,0 +1,79 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the
+binding, run the oracle on the same seeded inputs, compare."""
+import numpy as np
+import torch
+
+import oracle
+from nvfp4_paged_kv_append_gb300 import workloads as W
+
+MAX_ABS = 2e-2   # attention output tolerance (max |gpu - oracle|)
+REL_FRO = 1e-2   # ||gpu - oracle||_F / ||oracle||_F
+
+
+def nk():
+    from nvfp4_paged_kv_append_gb300 import build
+    build.build()
+    from nvfp4_paged_kv_append_gb300 import binding
+    return binding
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def gpu_cache(inp, fill=0, append_order=None):
+    """Build the cache on the GPU with the CUDA append (optionally appending
+    tokens in a shuffled order)."""
+    b = nk()
+    c = b.Cache(inp.num_pages, inp.wl.num_kv_heads, inp.k_global, inp.v_global, device=dev(), fill=fill)
+    k, v, s = inp.k, inp.v, inp.slot_mapping
+    if append_order is not None:
+        k, v, s = k[append_order], v[append_order], s[append_order]
+    b.nvfp4_kv_append(k.contiguous().to(dev()), v.contiguous().to(dev()), s.contiguous().to(dev()), c)
+    return c
+
+
+def oracle_pools(inp, token_subset=None):
+    pools = oracle.Pools(inp.num_pages, inp.wl.num_kv_heads)
+    k, v, s = inp.k.float().numpy(), inp.v.float().numpy(), inp.slot_mapping.numpy()
+    if token_subset is not None:
+        k, v, s = k[token_subset], v[token_subset], s[token_subset]
+    oracle.kv_append(pools, k, v, s, inp.k_global, inp.v_global)
+    return pools
+
+
+def compare_rows(got, ref, qo_indptr):
+    """got: [total_q, Hq, D] numpy; ref: oracle dict {(b, i): (o, lse)}.
+    Returns (max_abs, rel_fro, n_rows)."""
+    diffs, refs = [], []
+    for (b, i), (o, _) in ref.items():
+        g = got[int(qo_indptr[b]) + i]
+        diffs.append(g - o)
+        refs.append(o)
+    d = np.stack(diffs)
+    r = np.stack(refs)
+    return float(np.abs(d).max()), float(np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30)), len(diffs)
+
+
+def compare_lse(got_lse, ref, qo_indptr):
+    err = 0.0
+    for (b, i), (_, lse) in ref.items():
+        err = max(err, float(np.abs(got_lse[int(qo_indptr[b]) + i] - lse).max()))
+    return err
+
+
+def run_prefill(inp, cache, variant, causal=True, with_lse=True):
+    b = nk()
+    q = inp.q.to(dev())
+    lse = torch.full((inp.wl.total_q, inp.wl.num_q_heads), float("nan"), device=dev()) if with_lse else None
+    o = b.nvfp4_paged_prefill(q, cache, inp.page_table.to(dev()), inp.kv_lens.to(dev()), inp.qo_indptr.to(dev()),
+                              causal=causal, sm_scale=inp.sm_scale, variant=variant, lse=lse)
+    torch.cuda.synchronize()
+    status = b.nvfp4kv_get_device_status()
+    return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None), status
+
+
+def oracle_prefill(pools, inp, q_mode, causal=True, rows=None):
+    return oracle.paged_attention(pools, inp.q.float().numpy(), inp.qo_indptr, inp.kv_lens, inp.page_table,
+                                  inp.wl.num_q_heads, inp.k_global, inp.v_global, causal, inp.sm_scale,
+                                  q_mode=q_mode, rows=rows)

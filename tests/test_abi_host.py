@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/nvfp4kv.h declares, the host-only size queries match
+the pages' byte accounting, and invalid arguments are rejected before any
+CUDA call."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def nk():
+    import __graft_entry__ as g
+    from nvfp4_paged_kv_append_gb300 import build
+    build.build()
+    from nvfp4_paged_kv_append_gb300 import binding
+    return binding
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "nvfp4kv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(nvfp4[a-z0-9_]*)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(nk):
+    names = header_functions()
+    assert len(names) >= 11, names
+    for n in names:
+        assert hasattr(nk.lib, n), n
+    assert sorted(nk.EXPORTED) == names
+
+
+def test_version_and_strings(nk):
+    assert b"sm_103a" in nk.lib.nvfp4kv_version()
+    assert nk.status_string(0) == "ok"
+    assert "workspace" in nk.status_string(-3)
+
+
+def test_cache_bytes_worked_examples(nk):
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "accounting.json")))
+    w = g["worked_per_token_L64"]
+    assert w["layers"] * nk.nvfp4_cache_bytes(1, 1, w["kv_heads"], w["head_dim"]) == w["nvfp4_bytes_per_token"]
+    w = g["worked_per_token_L80"]
+    assert w["layers"] * nk.nvfp4_cache_bytes(1, 1, w["kv_heads"], w["head_dim"]) == w["nvfp4_bytes_per_token"]
+    assert nk.nvfp4_cache_bytes(10, 16, 8, 128) == 10 * 16 * 8 * 144
+    assert nk.nvfp4_cache_bytes(0, 16, 8, 128) == 0
+    assert nk.nvfp4_cache_bytes(1, 16, 8, 100) == 0
+
+
+def test_workspace_sizes(nk):
+    # prefill: schedule items (8 B each) for every (q tile, kv head) + prefix
+    b = nk.nvfp4_workspace_bytes(nk.OP_PREFILL, 1, 32, 8, 16384, 0)
+    items = (16384 * 4 // 128 + 1) * 8
+    assert b >= 16 + 8 * items and b % 16 == 0
+    # decode: split partials (129 floats per split, head, request)
+    d = nk.nvfp4_workspace_bytes(nk.OP_DECODE, 32, 32, 8, 0, 32768)
+    assert d == 32 * 128 * 32 * 129 * 4
+    assert nk.nvfp4_workspace_bytes(nk.OP_DECODE, 2, 6, 4, 0, 100) == 0  # Hq % Hkv != 0
+    assert nk.nvfp4_workspace_bytes(7, 1, 8, 8, 1, 1) == 0
+
+
+def test_invalid_arguments_rejected_on_host(nk):
+    lib = nk.lib
+    null = None
+    # no cache descriptor
+    assert lib.nvfp4_kv_append(null, null, null, 1, null, null) == -1
+    d = nk.CacheDesc(16, 16, 32, 48, 4, 16, 2, 128, 1.0, 1.0)
+    assert lib.nvfp4_kv_append(null, null, null, 1, ctypes.byref(d), null) == -1  # null k/v
+    bad = nk.CacheDesc(16, 16, 32, 48, 4, 8, 2, 128, 1.0, 1.0)  # page_size 8
+    assert lib.nvfp4_kv_append(null, null, null, 0, ctypes.byref(bad), null) == -1
+    bad = nk.CacheDesc(17, 16, 32, 48, 4, 16, 2, 128, 1.0, 1.0)  # misaligned pool
+    assert lib.nvfp4_kv_append(null, null, null, 0, ctypes.byref(bad), null) == -1
+    bad = nk.CacheDesc(16, 16, 32, 48, 4, 16, 2, 128, 0.0, 1.0)  # zero scale
+    assert lib.nvfp4_kv_append(null, null, null, 0, ctypes.byref(bad), null) == -1
+    assert lib.nvfp4_kv_append(null, null, null, 0, ctypes.byref(d), null) == 0  # empty append is a no-op
+    # prefill: Hq not a multiple of Hkv, bad variant, missing workspace
+    args = lambda hq, variant, ws: (16, 8, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, variant, 16, null, ws, 64, null)
+    assert lib.nvfp4_paged_prefill(*args(3, 0, 16)) == -1
+    assert lib.nvfp4_paged_prefill(*args(6, 0, 16)) == -1   # ratio 3 is not a power of two
+    assert lib.nvfp4_paged_prefill(*args(4, 2, 16)) == -1
+    assert lib.nvfp4_paged_prefill(*args(4, 0, null)) == -3
+    # decode: group of 32 unsupported; workspace too small
+    assert lib.nvfp4_paged_decode(16, 64, ctypes.byref(d), 16, 1, 16, 1, 0.1, 16, null, 16, 16, null) == -1
+    assert lib.nvfp4_paged_decode(16, 4, ctypes.byref(d), 16, 1, 16, 1, 0.1, 16, null, 16, 16, null) == -3
+    # quantize: bad mode / non-positive global scale
+    assert lib.nvfp4_quantize_rows(16, 1, 5, 1.0, 16, 16, null, null) == -1
+    assert lib.nvfp4_quantize_rows(16, 1, 0, -1.0, 16, 16, null, null) == -1

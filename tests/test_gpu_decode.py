@@ -1,0 +1,72 @@
+"""Paged decode on the GPU against the oracle (BF16 query, decoded K/V):
+max-abs <= 2e-2 and relative Frobenius <= 1e-2 ("NVFP4 KV cache prefill vs
+decode performance", section "Decode can win on fewer bytes read")."""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_paged_kv_append_gb300 import workloads as W
+
+from . import _gpu as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode_case(wl, fill=0, sample=None):
+    inp = W.make_inputs(wl)
+    b = G.nk()
+    cache = G.gpu_cache(inp, fill=fill)
+    # the decode query of request b is its (single) query row
+    q = inp.q.to(G.dev())
+    lse = torch.full((wl.batch, wl.num_q_heads), float("nan"), device=G.dev())
+    o = b.nvfp4_paged_decode(q, cache, inp.page_table.to(G.dev()), inp.kv_lens.to(G.dev()), sm_scale=inp.sm_scale,
+                             lse=lse)
+    torch.cuda.synchronize()
+    assert b.nvfp4kv_get_device_status() == 0
+    reqs = range(wl.batch) if sample is None else sample
+    rows = [(r, 0) for r in reqs if wl.kv_lens[r] > 0]
+    pools = G.oracle_pools(inp)
+    ref = G.oracle_prefill(pools, inp, "bf16", causal=False, rows=rows)
+    got = o.float().cpu().numpy()
+    mx, fro, n = G.compare_rows(got, ref, inp.qo_indptr)
+    lerr = G.compare_lse(lse.cpu().numpy(), ref, inp.qo_indptr)
+    return mx, fro, lerr, got, inp
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8, 16])
+def test_decode_groups(group):
+    wl = W.Workload(f"dec_g{group}", [1] * 5, [1, 17, 256, 257, 700], 2 * group, 2, seed=group)
+    mx, fro, lerr, _, _ = _decode_case(wl)
+    assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
+    assert lerr <= 1e-3, lerr
+
+
+def test_decode_outliers_and_junk_pool():
+    """Pool bytes outside the written slots are 0x7F (an E4M3 NaN): every
+    unused slot of a partly filled page must be ignored."""
+    wl = W.Workload("dec_out", [1] * 3, [33, 513, 1000], 8, 2, dist="outliers", seed=4)
+    mx, fro, lerr, got, _ = _decode_case(wl, fill=0x7F)
+    assert np.isfinite(got).all()
+    assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
+
+
+def test_decode_full_size_sampled():
+    """32 requests with kv_len ~ U[1K, 32K], 32/8 heads, at full size; the
+    oracle checks 8 requests including the longest and the shortest."""
+    wl = W.decode_batch()
+    kv = np.array(wl.kv_lens)
+    sample = sorted({int(kv.argmax()), int(kv.argmin()), 0, 5, 11, 17, 23, 31})
+    mx, fro, lerr, _, _ = _decode_case(wl, sample=sample)
+    assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
+    assert lerr <= 1e-3
+
+
+def test_decode_empty_request():
+    wl = W.Workload("dec_empty", [1, 1], [0, 40], 4, 2, seed=8)
+    inp = W.make_inputs(wl)
+    b = G.nk()
+    cache = G.gpu_cache(inp)
+    o = b.nvfp4_paged_decode(inp.q.to(G.dev()), cache, inp.page_table.to(G.dev()), inp.kv_lens.to(G.dev()),
+                             sm_scale=inp.sm_scale)
+    torch.cuda.synchronize()
+    assert float(o[0].abs().max()) == 0.0

@@ -1,0 +1,131 @@
+"""Paged prefill on the GPU against the oracle.  A4Q is compared with the
+oracle's A4Q query (same per-row quantization), the dequant-ahead variant with
+the BF16 query; max-abs <= 2e-2 and relative Frobenius <= 1e-2 ("NVFP4 KV
+cache A4Q prefill explained", sections "Quantize Q instead of expanding K",
+"Compare A4Q with dequantize-ahead repacking", "Make query accuracy a release
+gate")."""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_paged_kv_append_gb300 import workloads as W
+
+from . import _gpu as G
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [(0, "a4q"), (1, "bf16")]
+
+
+def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None):
+    got, lse, status = G.run_prefill(inp, cache, variant, causal=causal)
+    assert status == 0
+    ref = G.oracle_prefill(pools, inp, q_mode, causal=causal, rows=rows)
+    mx, fro, n = G.compare_rows(got, ref, inp.qo_indptr)
+    lerr = G.compare_lse(lse, ref, inp.qo_indptr)
+    assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro, n)
+    assert lerr <= 2e-3, lerr
+    return got, ref
+
+
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+@pytest.mark.parametrize("cfg", ["tiny", "small_ragged"])
+def test_prefill_full_parity(cfg, variant, q_mode):
+    inp = W.make_inputs(W.CONFIGS[cfg]())
+    cache = G.gpu_cache(inp)
+    _check(inp, cache, G.oracle_pools(inp), variant, q_mode)
+
+
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_noncausal_and_groups(variant, q_mode):
+    for group, hkv in [(1, 3), (8, 1), (16, 2)]:
+        wl = W.Workload(f"nc_g{group}", [70, 3], [150, 40], group * hkv, hkv, causal=False, seed=group)
+        inp = W.make_inputs(wl)
+        cache = G.gpu_cache(inp, fill=0x7F)   # junk in unused slots must not leak
+        _check(inp, cache, G.oracle_pools(inp), variant, q_mode, causal=False)
+
+
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_zero_length_and_edge_rows(variant, q_mode):
+    """A request with q_len 0, one with q_len 1 over a long cache, a zero
+    query row, kv_len not a multiple of the page or tile size."""
+    wl = W.Workload("edge", [0, 1, 129, 5], [0, 300, 129, 1000], 4, 2, seed=6)
+    inp = W.make_inputs(wl)
+    q = inp.q.clone()
+    q[3] = 0
+    inp.q = q
+    cache = G.gpu_cache(inp, fill=0x7F)
+    _check(inp, cache, G.oracle_pools(inp), variant, q_mode)
+
+
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_shortq_longkv(variant, q_mode):
+    """batch 4, q 128 at the end of kv 2048, 32/8 heads, permuted pages: all
+    rows of request 0, sampled rows of the others."""
+    inp = W.make_inputs(W.short_q_long_kv())
+    cache = G.gpu_cache(inp)
+    rows = [(0, i) for i in range(128)] + [r for r in W.sample_rows(inp.wl, 6) if r[0] != 0]
+    _check(inp, cache, G.oracle_pools(inp), variant, q_mode, rows=rows)
+
+
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_tails(variant, q_mode):
+    """8 requests x 16 new queries over 16,400 cached tokens (sampled rows)."""
+    inp = W.make_inputs(W.chunked_tails())
+    cache = G.gpu_cache(inp)
+    rows = [(b, i) for b in (0, 7) for i in range(16)] + W.sample_rows(inp.wl, 2)
+    _check(inp, cache, G.oracle_pools(inp), variant, q_mode, rows=rows)
+
+
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_full_16k_sampled(variant, q_mode):
+    """The 16K causal configuration at full size, as the benchmark runs it
+    (cache built by the CUDA append in shuffled order); sampled rows."""
+    inp = W.make_inputs(W.full_prefill_16k())
+    cache = G.gpu_cache(inp, append_order=W.shuffled_append_order(inp.wl.total_kv))
+    rows = W.sample_rows(inp.wl, 14)
+    _check(inp, cache, G.oracle_pools(inp), variant, q_mode, rows=rows)
+
+
+def test_prefill_long_ragged_sampled():
+    """32,768 + 7,001 tokens, 64/8 heads, A4Q; sampled rows of both requests."""
+    inp = W.make_inputs(W.long_prefill_ragged())
+    cache = G.gpu_cache(inp)
+    rows = W.sample_rows(inp.wl, 5)
+    _check(inp, cache, G.oracle_pools(inp), 0, "a4q", rows=rows)
+
+
+def test_a4q_is_closer_to_its_own_reference():
+    """The A4Q kernel really quantizes Q: its output is nearer the oracle's A4Q
+    result than the BF16-query result, and the gap between the two oracle
+    results (the A4Q error) is reported."""
+    inp = W.make_inputs(W.tiny_causal())
+    cache = G.gpu_cache(inp)
+    pools = G.oracle_pools(inp)
+    got, _, _ = G.run_prefill(inp, cache, 0)
+    ra = G.oracle_prefill(pools, inp, "a4q")
+    rb = G.oracle_prefill(pools, inp, "bf16")
+    to_a, _, _ = G.compare_rows(got, ra, inp.qo_indptr)
+    to_b, _, _ = G.compare_rows(got, rb, inp.qo_indptr)
+    a4q_err = max(float(np.abs(ra[k][0] - rb[k][0]).max()) for k in ra)
+    print(f"A4Q vs BF16-Q max-abs error (oracle): {a4q_err:.4g}; kernel to A4Q ref {to_a:.3g}, to BF16 ref {to_b:.3g}")
+    assert to_a < to_b
+
+
+def test_prefill_bad_page_and_shape_flagged():
+    b = G.nk()
+    inp = W.make_inputs(W.Workload("bad", [20], [40], 4, 2, seed=3))
+    cache = G.gpu_cache(inp)
+    pt = inp.page_table.clone()
+    pt[0, 1] = inp.num_pages + 100                 # out of range: skipped + flagged
+    o = b.nvfp4_paged_prefill(inp.q.to(G.dev()), cache, pt.to(G.dev()), inp.kv_lens.to(G.dev()),
+                              inp.qo_indptr.to(G.dev()), sm_scale=inp.sm_scale)
+    torch.cuda.synchronize()
+    assert b.nvfp4kv_get_device_status() == -6
+    assert torch.isfinite(o.float()).all()
+    kvl = inp.kv_lens.clone()
+    kvl[0] = 10                                     # causal with q_len 20 > kv_len 10
+    b.nvfp4_paged_prefill(inp.q.to(G.dev()), cache, inp.page_table.to(G.dev()), kvl.to(G.dev()),
+                          inp.qo_indptr.to(G.dev()), sm_scale=inp.sm_scale)
+    torch.cuda.synchronize()
+    assert b.nvfp4kv_get_device_status() == -2
