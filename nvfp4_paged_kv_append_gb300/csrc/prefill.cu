@@ -78,6 +78,8 @@ struct Bars {
   uint64_t* q_full;
   uint64_t* q_empty;
   uint64_t* drain;
+  uint64_t* qs_empty;   // softmax has read the item's row scales
+  uint64_t* sfa_ready;  // transform warps have staged the item's Q block scales
 };
 
 __device__ __forceinline__ Bars make_bars(uint64_t* base) {
@@ -94,6 +96,8 @@ __device__ __forceinline__ Bars make_bars(uint64_t* base) {
   b.q_full = base + 18;
   b.q_empty = base + 19;
   b.drain = base + 20;
+  b.qs_empty = base + 21;
+  b.sfa_ready = base + 22;
   return b;
 }
 
@@ -122,10 +126,6 @@ __device__ __forceinline__ bool get_item(const PrefillArgs& a, int round, Item& 
   const int last_key = a.causal ? it.kv_len - it.q_len + it.tok0 + it.n_tok - 1 : it.kv_len - 1;
   it.n_tiles = last_key / kBN + 1;
   return true;
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -266,7 +266,12 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
   for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
-    if (item_ctr > 0 && !mbar_wait(bars.q_empty, (item_ctr - 1) & 1u, a.status)) return;
+    // The previous item's Q tile, Q block scales and row scales must be
+    // consumed (last QK issued and finished; softmax has read its row scales)
+    // before they are overwritten.  Waiting on both also keeps the softmax
+    // less than one q_full phase behind.
+    if (item_ctr > 0 && !mbar_wait_warp(bars.q_empty, (item_ctr - 1) & 1u, a.status)) return;
+    if (item_ctr > 0 && !mbar_wait_warp(bars.qs_empty, (item_ctr - 1) & 1u, a.status)) return;
     // ---- Q tile ------------------------------------------------------------
     {
       const int r = tid;
@@ -320,7 +325,9 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
         sfa_stage[r] = make_uint2(sc[0] | (sc[1] << 8) | (sc[2] << 16) | (sc[3] << 24),
                                   sc[4] | (sc[5] << 8) | (sc[6] << 16) | (sc[7] << 24));
         qscale[r] = g_row;
-        named_bar_sync(1, 128);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.sfa_ready);
+        if (!mbar_wait_warp(bars.sfa_ready, item_ctr & 1u, a.status)) return;
         // Q block scales -> TMEM: lane i of each quadrant, column 4s+j holds
         // the four scales of k-step s for row 32j+i (replicated per quadrant).
         uint32_t va[8];
@@ -350,11 +357,11 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
     for (int j = 0; j < item.n_tiles; ++j) {
       const uint32_t it = it_ctr + j;
       const uint32_t st = it % L::kStages, b = it & 1u;
-      if (!mbar_wait(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
+      if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
       const uint8_t* stage = smem + L::kOffStage + st * kStageBytes;
       const int valid_pages = mask_slot[st];
       const int key_base = j * kBN;
-      if (it >= 2 && !mbar_wait(&bars.s_full[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+      if (it >= 2 && !mbar_wait_warp(&bars.s_full[b], ((it >> 1) - 1u) & 1u, a.status)) return;
       if constexpr (L::kA4Q) {
         // K block scales -> TMEM (same replicated layout as Q's)
         const uint8_t* ks = stage + kStageKData;
@@ -395,7 +402,7 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.sfb_full[b]);
       // ---- V -> FP16, MN-major 128B-swizzled operand ---------------------------
-      if (it >= 2 && !mbar_wait(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+      if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
       {
         uint8_t* vb = smem + L::kOffV + b * kTileBuf16;
         const uint8_t* vd = stage + kStageKData + kStageKScale;
@@ -446,18 +453,20 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
   for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
-    if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
+    if (!mbar_wait_warp(bars.q_full, item_ctr & 1u, a.status)) return;
     const int tq = item.tok0 + (r >> lg);
     const bool valid = (r >> lg) < item.n_tok;
     const int hq = item.kvh * G + (r & (G - 1));
     const int limit = !valid ? -1 : (a.causal ? item.kv_len - item.q_len + tq : item.kv_len - 1);
     const float c_r = (L::kA4Q ? qscale[r] : 1.0f) * a.k_g * a.sm_scale * kLog2e;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.qs_empty);
     float m_run = -INFINITY, l_run = 0.0f;
     for (int j = 0; j < item.n_tiles; ++j) {
       const uint32_t it = it_ctr + j;
       const uint32_t b = it & 1u;
       const uint32_t s_col = b ? kColS1 : kColS0;
-      if (!mbar_wait(&bars.s_full[b], (it >> 1) & 1u, a.status)) return;
+      if (!mbar_wait_warp(&bars.s_full[b], (it >> 1) & 1u, a.status)) return;
       tc_fence_after();
       uint32_t sr[128];
 #pragma unroll
@@ -476,26 +485,32 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
 #pragma unroll
       for (int c = 0; c < 128; c += 2) mx = fmaxf(mx, fmaxf(s[c], s[c + 1]));
       const float m_tile = masked ? mx : mx * c_r;
-      if (m_tile > m_run + kRescaleThreshold) {
-        const float alpha = fast_exp2(m_run - m_tile);  // 0 when m_run = -inf
+      // Lazy rescale: a row moves its running max only when the tile max
+      // exceeds it by more than 2^8.  O is rescaled by the whole warp (TMEM
+      // loads/stores are warp-collective), with factor 1 for rows that keep
+      // their max.
+      float alpha = 1.0f;
+      const bool need = m_tile > m_run + kRescaleThreshold;
+      if (need) {
+        alpha = fast_exp2(m_run - m_tile);  // 0 when m_run = -inf
         l_run *= alpha;
-        if (j > 0) {
-          // O must hold PV of the previous tile before it is rescaled
-          const uint32_t pit = it - 1u;
-          if (!mbar_wait(&bars.pv_done[pit & 1u], (pit >> 1) & 1u, a.status)) return;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(lane_base + kColO + 32 * c, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st16(lane_base + kColO + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
-            tmem_st16(lane_base + kColO + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
-          }
-        }
         m_run = m_tile;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O must hold PV of the previous tile before it is rescaled
+        const uint32_t pit = it - 1u;
+        if (!mbar_wait_warp(&bars.pv_done[pit & 1u], (pit >> 1) & 1u, a.status)) return;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(lane_base + kColO + 32 * c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st16(lane_base + kColO + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+          tmem_st16(lane_base + kColO + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+        }
       }
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
       const float cs = masked ? 1.0f : c_r;
@@ -517,7 +532,7 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
       if (lane == 0) mbar_arrive(&bars.p_full[b]);
     }
     // ---- epilogue ---------------------------------------------------------------
-    if (!mbar_wait(bars.o_full, item_ctr & 1u, a.status)) return;
+    if (!mbar_wait_warp(bars.o_full, item_ctr & 1u, a.status)) return;
     tc_fence_after();
     const float inv_l = (l_run > 0.0f) ? a.v_g / l_run : 0.0f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) +
@@ -577,6 +592,8 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
     mbar_init(bars.q_full, 4);
     mbar_init(bars.q_empty, 1);
     mbar_init(bars.drain, 1);
+    mbar_init(bars.qs_empty, 4);
+    mbar_init(bars.sfa_ready, 4);
     fence_barrier_init();
   }
   if (warp == kProducerWarp && lane == 0) prefetch_tmap(tmap_k);

@@ -77,6 +77,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// Whole-warp variant: every lane waits, and the outcome is made uniform so
+// that no lane goes on to a warp-collective instruction (tcgen05.ld/st,
+// shuffles) while another lane has given up.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, status, limit_ns);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // ---- async proxy fences --------------------------------------------------------
 // Generic-proxy shared-memory writes made visible to the async proxy (tensor
 // core / TMA) before a barrier hand-off.

@@ -21,6 +21,7 @@ Parity status per function:
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import ctypes
 import os
 import subprocess
@@ -36,6 +37,19 @@ GLOBAL = 0
 PER_ROW = 1
 
 _lib = None
+
+# Independent (request, head) problems and disjoint token ranges of the append
+# run on a thread pool: ctypes releases the GIL inside the C calls, and no two
+# tasks write the same output.  Nothing about the arithmetic changes.
+WORKERS = max(1, min(32, os.cpu_count() or 1))
+
+
+def _pmap(fn, items):
+    items = list(items)
+    if WORKERS == 1 or len(items) <= 1:
+        return [fn(x) for x in items]
+    with cf.ThreadPoolExecutor(max_workers=WORKERS) as ex:
+        return list(ex.map(fn, items))
 
 
 def build(force: bool = False) -> str:
@@ -179,11 +193,18 @@ def kv_append(pools: Pools, k, v, slot_mapping, k_g: float, v_g: float) -> None:
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     T, Hkv, D = k.shape
     assert Hkv == pools.Hkv and D == pools.D and slots.shape == (T,)
-    rc = _load().orc_kv_append(_ptr(k), _ptr(v), _ptr(slots), T, Hkv, D, pools.page_size,
-                               pools.num_pages, float(np.float32(k_g)), float(np.float32(v_g)),
-                               _ptr(pools.k_data), _ptr(pools.k_scale), _ptr(pools.v_data),
-                               _ptr(pools.v_scale))
-    if rc != 0:
+    lib = _load()
+    step = max(1024, (T + WORKERS - 1) // WORKERS)
+
+    def run(t0):
+        n = min(step, T - t0)
+        return lib.orc_kv_append(
+            ctypes.c_void_p(k.ctypes.data + t0 * k.strides[0]), ctypes.c_void_p(v.ctypes.data + t0 * v.strides[0]),
+            ctypes.c_void_p(slots.ctypes.data + t0 * 8), n, Hkv, D, pools.page_size, pools.num_pages,
+            float(np.float32(k_g)), float(np.float32(v_g)), _ptr(pools.k_data), _ptr(pools.k_scale),
+            _ptr(pools.v_data), _ptr(pools.v_scale))
+
+    if T > 0 and any(rc != 0 for rc in _pmap(run, range(0, T, step))):
         raise ValueError("slot out of range")
 
 
@@ -254,23 +275,30 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
         for b, i in rows:
             want.setdefault(int(b), []).append(int(i))
     result = {}
+
+    def one(task):
+        b, h, pos = task
+        q_len, kv_len = int(qo[b + 1] - qo[b]), int(kvl[b])
+        kd = gather_decode(pools, "k", pt[b], kv_len, h, k_g)
+        vd = gather_decode(pools, "v", pt[b], kv_len, h, v_g)
+        res = []
+        for gq in range(G):
+            hq = h * G + gq
+            qr = q[qo[b] + pos, hq, :]
+            qd = decode_q_a4q(qr) if q_mode == "a4q" else qr.astype(np.float64)
+            res.append((hq,) + attention_rows(qd, pos, q_len, kd, vd, causal, sm_scale))
+        return b, pos, res
+
+    tasks = []
     for b, positions in want.items():
-        q_len = int(qo[b + 1] - qo[b])
-        kv_len = int(kvl[b])
-        positions = sorted(set(positions))
-        pos = np.array(positions, np.int32)
-        outs = {i: (np.zeros((Hq, pools.D)), np.zeros(Hq)) for i in positions}
+        pos = np.array(sorted(set(positions)), np.int32)
         for h in range(Hkv):
-            kd = gather_decode(pools, "k", pt[b], kv_len, h, k_g)
-            vd = gather_decode(pools, "v", pt[b], kv_len, h, v_g)
-            for gq in range(G):
-                hq = h * G + gq
-                qr = q[qo[b] + pos, hq, :]
-                qd = decode_q_a4q(qr) if q_mode == "a4q" else qr.astype(np.float64)
-                o, lse = attention_rows(qd, pos, q_len, kd, vd, causal, sm_scale)
-                for r, i in enumerate(positions):
-                    outs[i][0][hq] = o[r]
-                    outs[i][1][hq] = lse[r]
-        for i in positions:
-            result[(b, i)] = outs[i]
+            tasks.append((b, h, pos))
+    for b, pos, res in _pmap(one, tasks):
+        for i in pos:
+            result.setdefault((b, int(i)), (np.zeros((Hq, pools.D)), np.zeros(Hq)))
+        for hq, o, lse in res:
+            for r, i in enumerate(pos):
+                result[(b, int(i))][0][hq] = o[r]
+                result[(b, int(i))][1][hq] = lse[r]
     return result

@@ -6,8 +6,15 @@ import torch
 import oracle
 from nvfp4_paged_kv_append_gb300 import workloads as W
 
-MAX_ABS = 2e-2   # attention output tolerance (max |gpu - oracle|)
+MAX_ABS = 2e-2   # attention output tolerance: max |gpu - oracle| beyond the output's bf16 rounding
 REL_FRO = 1e-2   # ||gpu - oracle||_F / ||oracle||_F
+
+
+def bf16_half_ulp(x):
+    """Half a bf16 unit in the last place of |x| (8 significant bits): the
+    rounding the stored bf16 output adds on top of the kernel's own error."""
+    a = np.maximum(np.abs(x), np.float64(2.0 ** -126))
+    return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
 
 
 def nk():
@@ -19,6 +26,24 @@ def nk():
 
 def dev():
     return torch.device("cuda:0")
+
+
+_INPUTS = {}
+_POOLS = {}
+
+
+def inputs(cfg):
+    """Seeded inputs of a named configuration, built once per session."""
+    if cfg not in _INPUTS:
+        _INPUTS[cfg] = W.make_inputs(W.CONFIGS[cfg]())
+    return _INPUTS[cfg]
+
+
+def pools_for(cfg):
+    """Oracle cache of a named configuration, built once per session."""
+    if cfg not in _POOLS:
+        _POOLS[cfg] = oracle_pools(inputs(cfg))
+    return _POOLS[cfg]
 
 
 def gpu_cache(inp, fill=0, append_order=None):
@@ -44,7 +69,9 @@ def oracle_pools(inp, token_subset=None):
 
 def compare_rows(got, ref, qo_indptr):
     """got: [total_q, Hq, D] numpy; ref: oracle dict {(b, i): (o, lse)}.
-    Returns (max_abs, rel_fro, n_rows)."""
+    Returns (max_abs, rel_fro, n_rows) where max_abs is the largest
+    |gpu - oracle| in excess of half a bf16 ulp of the oracle value (the
+    output is stored as bf16)."""
     diffs, refs = [], []
     for (b, i), (o, _) in ref.items():
         g = got[int(qo_indptr[b]) + i]
@@ -52,7 +79,8 @@ def compare_rows(got, ref, qo_indptr):
         refs.append(o)
     d = np.stack(diffs)
     r = np.stack(refs)
-    return float(np.abs(d).max()), float(np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30)), len(diffs)
+    excess = np.maximum(np.abs(d) - bf16_half_ulp(r), 0.0)
+    return float(excess.max()), float(np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30)), len(diffs)
 
 
 def compare_lse(got_lse, ref, qo_indptr):

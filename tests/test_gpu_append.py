@@ -22,18 +22,18 @@ def _assert_same(cache, pools):
 
 @pytest.mark.parametrize("cfg", ["tiny", "small_ragged", "shortq"])
 def test_append_bit_exact(cfg):
-    inp = W.make_inputs(W.CONFIGS[cfg](), with_q=False)
+    inp = G.inputs(cfg)
     order = W.shuffled_append_order(inp.wl.total_kv)
     cache = G.gpu_cache(inp, append_order=order)
-    _assert_same(cache, G.oracle_pools(inp))
+    _assert_same(cache, G.pools_for(cfg))
     assert G.nk().nvfp4kv_get_device_status() == 0
 
 
 def test_append_bit_exact_full_16k():
     """The 16K-token configuration at full size, tokens appended in shuffled order."""
-    inp = W.make_inputs(W.full_prefill_16k(), with_q=False)
+    inp = G.inputs("prefill16k")
     cache = G.gpu_cache(inp, append_order=W.shuffled_append_order(inp.wl.total_kv))
-    _assert_same(cache, G.oracle_pools(inp))
+    _assert_same(cache, G.pools_for("prefill16k"))
 
 
 def test_append_sampled_full_40k():

@@ -31,9 +31,9 @@ def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None):
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 @pytest.mark.parametrize("cfg", ["tiny", "small_ragged"])
 def test_prefill_full_parity(cfg, variant, q_mode):
-    inp = W.make_inputs(W.CONFIGS[cfg]())
+    inp = G.inputs(cfg)
     cache = G.gpu_cache(inp)
-    _check(inp, cache, G.oracle_pools(inp), variant, q_mode)
+    _check(inp, cache, G.pools_for(cfg), variant, q_mode)
 
 
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
@@ -62,29 +62,29 @@ def test_prefill_zero_length_and_edge_rows(variant, q_mode):
 def test_prefill_shortq_longkv(variant, q_mode):
     """batch 4, q 128 at the end of kv 2048, 32/8 heads, permuted pages: all
     rows of request 0, sampled rows of the others."""
-    inp = W.make_inputs(W.short_q_long_kv())
+    inp = G.inputs("shortq")
     cache = G.gpu_cache(inp)
     rows = [(0, i) for i in range(128)] + [r for r in W.sample_rows(inp.wl, 6) if r[0] != 0]
-    _check(inp, cache, G.oracle_pools(inp), variant, q_mode, rows=rows)
+    _check(inp, cache, G.pools_for("shortq"), variant, q_mode, rows=rows)
 
 
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 def test_prefill_tails(variant, q_mode):
     """8 requests x 16 new queries over 16,400 cached tokens (sampled rows)."""
-    inp = W.make_inputs(W.chunked_tails())
+    inp = G.inputs("tails")
     cache = G.gpu_cache(inp)
     rows = [(b, i) for b in (0, 7) for i in range(16)] + W.sample_rows(inp.wl, 2)
-    _check(inp, cache, G.oracle_pools(inp), variant, q_mode, rows=rows)
+    _check(inp, cache, G.pools_for("tails"), variant, q_mode, rows=rows)
 
 
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 def test_prefill_full_16k_sampled(variant, q_mode):
     """The 16K causal configuration at full size, as the benchmark runs it
     (cache built by the CUDA append in shuffled order); sampled rows."""
-    inp = W.make_inputs(W.full_prefill_16k())
+    inp = G.inputs("prefill16k")
     cache = G.gpu_cache(inp, append_order=W.shuffled_append_order(inp.wl.total_kv))
     rows = W.sample_rows(inp.wl, 14)
-    _check(inp, cache, G.oracle_pools(inp), variant, q_mode, rows=rows)
+    _check(inp, cache, G.pools_for("prefill16k"), variant, q_mode, rows=rows)
 
 
 def test_prefill_long_ragged_sampled():
@@ -99,9 +99,9 @@ def test_a4q_is_closer_to_its_own_reference():
     """The A4Q kernel really quantizes Q: its output is nearer the oracle's A4Q
     result than the BF16-query result, and the gap between the two oracle
     results (the A4Q error) is reported."""
-    inp = W.make_inputs(W.tiny_causal())
+    inp = G.inputs("tiny")
     cache = G.gpu_cache(inp)
-    pools = G.oracle_pools(inp)
+    pools = G.pools_for("tiny")
     got, _, _ = G.run_prefill(inp, cache, 0)
     ra = G.oracle_prefill(pools, inp, "a4q")
     rb = G.oracle_prefill(pools, inp, "bf16")
