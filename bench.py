@@ -66,7 +66,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, FileNotFoundError):
@@ -208,15 +208,17 @@ def run_ours(args, rank, world, dev):
     flops = wl.flops()
     f_qk, f_pv = prefill_flops_split(wl)
 
-    # ---- headline: K timed steps, barrier + synchronize on both sides
+    # ---- headline: K timed steps, barrier + synchronize on both sides.
+    # Clocks are sampled from the warm-up through the component timings.
+    clocks = ClockSampler(physical_gpu_index())
+    clocks.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         nk_bench.flush()
         step()
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    clocks = ClockSampler(physical_gpu_index())
-    clocks.start()
     t_wall0 = time.perf_counter()
     ev = []
     pf_ev = []
@@ -233,7 +235,6 @@ def run_ours(args, rank, world, dev):
         ev.append((s, m, e))
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall0
-    clk = clocks.stop()
     step_ms = [s.elapsed_time(e) for s, m, e in ev]
     app_ms = [s.elapsed_time(m) for s, m, e in ev]
     pre_ms = [m.elapsed_time(e) for s, m, e in ev]
@@ -245,12 +246,13 @@ def run_ours(args, rank, world, dev):
     value = flops * world / (ms * 1e-3) / 1e12
 
     # ---- components (each timed alone, L2 flushed before every call)
-    K = max(args.steps, 5)
+    K = max(min(args.steps, 50), 5)
     app = nk_bench.time_fn(append, K, 3)
     pre = nk_bench.time_fn(prefill, K, 3)
     dqa = nk_bench.time_fn(lambda: prefill(nk.VARIANT_DQ_AHEAD), K, 3)
     app_bytes = APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads
     dec = decode_component(nk, nk_bench, dev, K)
+    clk = clocks.stop()
 
     pre_avg = statistics.mean(pre)
     achieved = flops / (statistics.mean(pre_ms) * 1e-3) / 1e12
@@ -431,7 +433,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="prefill16k", choices=sorted(W.CONFIGS))
