@@ -134,6 +134,28 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
                         const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
                         void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/* nvfp4_paged_prefill without a workspace argument, for callers that cannot
+ * allocate device memory: an engine that plans all device memory up front and
+ * allows no cudaMalloc on its serving path (an allocation can synchronize the
+ * device), or a host that passes a kernel only its inputs and outputs.  The
+ * pages have no counterpart of this call; it is a packaging of the same
+ * kernels.  The work schedule lives in a static device array of
+ * nvfp4_paged_prefill_noalloc_max_bytes() bytes (1 MiB) that every GPU which
+ * loads the library holds until the process exits.  Arguments and results are
+ * those of nvfp4_paged_prefill.  Returns NVFP4KV_ERR_WORKSPACE when the
+ * schedule of the call (nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, ...)) is
+ * larger than the array.  The first call on a device looks up the array's
+ * device address (make it before any stream capture).  All calls share the
+ * array: calls that overlap on the GPU race.  Allocates nothing. */
+int nvfp4_paged_prefill_noalloc(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                                const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                                const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale,
+                                int32_t variant, void* o, float* lse, void* stream);
+
+/* Size in bytes of the static schedule array used by
+ * nvfp4_paged_prefill_noalloc.  Host-only. */
+size_t nvfp4_paged_prefill_noalloc_max_bytes(void);
+
 /* Paged decode: one query token per request attends to all kv_lens[b] cached
  * tokens ("NVFP4 KV cache prefill vs decode performance", section "Decode can
  * win on fewer bytes read": decode reads the long cache for one new token and
