@@ -164,6 +164,23 @@ class Bench:
         return [s.elapsed_time(e) for s, e in times]
 
 
+def time_graph(nk_bench, fn, steps, warmup=3):
+    """Per-replay device time (ms) of `fn` captured once into a CUDA graph
+    (no host launch gaps inside the events); L2 flushed before every replay,
+    outside the events.  Returns None if the capture is not possible."""
+    try:
+        fn()
+        torch.cuda.synchronize(nk_bench.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize(nk_bench.dev)
+        return nk_bench.time_fn(g.replay, steps, warmup)
+    except Exception as e:  # pragma: no cover - reported in the JSON line
+        print(f"graph timing unavailable: {e}", file=sys.stderr)
+        return None
+
+
 def setup_prefill(nk, dev, wl):
     inp = W.make_inputs(wl)
     order = W.shuffled_append_order(inp.wl.total_kv)
@@ -174,9 +191,13 @@ def setup_prefill(nk, dev, wl):
     q = inp.q.to(dev)
     pt, kvl, qo = inp.page_table.to(dev), inp.kv_lens.to(dev), inp.qo_indptr.to(dev)
     out = torch.empty_like(q)
+    # room for repack mode (V dequantized once per KV tile) and the schedule-only size
     ws = torch.empty(nk.nvfp4_workspace_bytes(nk.OP_PREFILL, wl.batch, wl.num_q_heads, wl.num_kv_heads,
-                                              wl.total_q, 0), dtype=torch.uint8, device=dev)
-    return dict(inp=inp, k=k, v=v, slots=slots, cache=cache, q=q, pt=pt, kvl=kvl, qo=qo, out=out, ws=ws)
+                                              wl.total_q, pt.shape[1] * 16), dtype=torch.uint8, device=dev)
+    ws_min = torch.empty(nk.nvfp4_workspace_bytes(nk.OP_PREFILL, wl.batch, wl.num_q_heads, wl.num_kv_heads,
+                                                  wl.total_q, 0), dtype=torch.uint8, device=dev)
+    return dict(inp=inp, k=k, v=v, slots=slots, cache=cache, q=q, pt=pt, kvl=kvl, qo=qo, out=out, ws=ws,
+                ws_min=ws_min)
 
 
 def run_ours(args, rank, world, dev):
@@ -190,9 +211,9 @@ def run_ours(args, rank, world, dev):
     def append():
         nk.nvfp4_kv_append(P["k"], P["v"], P["slots"], P["cache"])
 
-    def prefill(variant=nk.VARIANT_A4Q):
+    def prefill(variant=nk.VARIANT_A4Q, ws="ws"):
         nk.nvfp4_paged_prefill(P["q"], P["cache"], P["pt"], P["kvl"], P["qo"], causal=wl.causal,
-                               sm_scale=inp.sm_scale, variant=variant, out=P["out"], workspace=P["ws"])
+                               sm_scale=inp.sm_scale, variant=variant, out=P["out"], workspace=P[ws])
 
     def step():
         append()
@@ -248,8 +269,11 @@ def run_ours(args, rank, world, dev):
     # ---- components (each timed alone, L2 flushed before every call)
     K = max(min(args.steps, 50), 5)
     app = nk_bench.time_fn(append, K, 3)
+    app_g = time_graph(nk_bench, append, K)
     pre = nk_bench.time_fn(prefill, K, 3)
     dqa = nk_bench.time_fn(lambda: prefill(nk.VARIANT_DQ_AHEAD), K, 3)
+    pre_ik = nk_bench.time_fn(lambda: prefill(nk.VARIANT_A4Q, "ws_min"), K, 3)
+    dqa_ik = nk_bench.time_fn(lambda: prefill(nk.VARIANT_DQ_AHEAD, "ws_min"), K, 3)
     app_bytes = APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads
     dec = decode_component(nk, nk_bench, dev, K)
     clk = clocks.stop()
@@ -269,7 +293,7 @@ def run_ours(args, rank, world, dev):
         "vs_baseline": None, "dtype": "nvfp4(e2m1+e4m3) QK, f16 PV, f32 accum", "data": "synthetic",
         "config": {"workload": wl.name, "batch": wl.batch, "seq_len": wl.q_lens[0], "q_heads": wl.num_q_heads,
                    "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16, "causal": wl.causal,
-                   "step": "append(K,V 16384 tok, shuffled slots) + A4Q paged prefill",
+                   "step": "append(K,V 16384 tok, shuffled slots) + A4Q paged prefill (repack mode)",
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every timed step, outside the events",
                    "parallelism": f"replicas x{world}"},
         "step_breakdown_ms": {"append": round(statistics.mean(app_ms), 4), "prefill": round(statistics.mean(pre_ms), 4)},
@@ -282,15 +306,26 @@ def run_ours(args, rank, world, dev):
             "append": {"ms": round(statistics.mean(app), 4),
                        "GB/s": round(app_bytes / (statistics.mean(app) * 1e-3) / 1e9, 1),
                        "frac_of_hbm": round(app_bytes / (statistics.mean(app) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                       "graph_ms": round(statistics.mean(app_g), 4) if app_g else None,
+                       "graph_GB/s": round(app_bytes / (statistics.mean(app_g) * 1e-3) / 1e9, 1) if app_g else None,
+                       "graph_frac_of_hbm": round(app_bytes / (statistics.mean(app_g) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+                       if app_g else None,
                        "bytes": app_bytes},
-            "prefill_a4q": {"ms": round(pre_avg, 4), "TFLOP/s": round(flops / (pre_avg * 1e-3) / 1e12, 2)},
+            "prefill_a4q": {"ms": round(pre_avg, 4), "TFLOP/s": round(flops / (pre_avg * 1e-3) / 1e12, 2),
+                            "mode": "V repacked once per KV tile"},
+            "prefill_a4q_inkernel": {"ms": round(statistics.mean(pre_ik), 4),
+                                     "TFLOP/s": round(flops / (statistics.mean(pre_ik) * 1e-3) / 1e12, 2),
+                                     "mode": "V dequantized in the kernel"},
             "prefill_dq_ahead": {"ms": round(statistics.mean(dqa), 4),
                                  "TFLOP/s": round(flops / (statistics.mean(dqa) * 1e-3) / 1e12, 2),
-                                 "frac_of_bf16": round(flops / (statistics.mean(dqa) * 1e-3) / 1e12 / p16, 4)},
+                                 "frac_of_bf16": round(flops / (statistics.mean(dqa) * 1e-3) / 1e12 / p16, 4),
+                                 "mode": "K and V repacked once per KV tile"},
+            "prefill_dq_ahead_inkernel": {"ms": round(statistics.mean(dqa_ik), 4),
+                                          "TFLOP/s": round(flops / (statistics.mean(dqa_ik) * 1e-3) / 1e12, 2)},
             "decode": dec,
         },
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,  # append, schedule, V repack, attention
         "clocks": clk,
         "wall_s_timed_loop": round(t_wall, 3),
     }
@@ -313,11 +348,17 @@ def decode_component(nk, nk_bench, dev, K):
         nk.nvfp4_paged_decode(q, cache, pt, kvl, sm_scale=inp.sm_scale, out=out, workspace=ws)
 
     t = nk_bench.time_fn(dec, K, 3)
+    tg = time_graph(nk_bench, dec, K)
     peaks = measured_peaks()
     bytes_ = CACHE_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads
     gbs = bytes_ / (statistics.mean(t) * 1e-3) / 1e9
-    return {"workload": wl.name, "ms": round(statistics.mean(t), 4), "GB/s": round(gbs, 1),
-            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "bytes": bytes_}
+    out = {"workload": wl.name, "ms": round(statistics.mean(t), 4), "GB/s": round(gbs, 1),
+           "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "bytes": bytes_}
+    if tg:
+        g = bytes_ / (statistics.mean(tg) * 1e-3) / 1e9
+        out.update({"graph_ms": round(statistics.mean(tg), 4), "graph_GB/s": round(g, 1),
+                    "graph_frac_of_hbm": round(g / peaks["hbm_gbs"], 4)})
+    return out
 
 
 def e2e_measure(nk, nk_bench, dev, P, wl, args):

@@ -126,7 +126,16 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  * workspace:  device buffer of at least
  *             nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, batch, num_q_heads,
  *             num_kv_heads, total_q, 0) bytes, 16-byte aligned; its contents
- *             are overwritten (it holds the work schedule).
+ *             are overwritten (it holds the work schedule).  Given
+ *             nvfp4_workspace_bytes(..., total_q, max_pages_per_req * 16)
+ *             bytes, the call may also run in repack mode:
+ *             when requests average two or more q tiles (128 rows of query
+ *             tokens x grouped heads) per kv head, V (and K for the
+ *             dequant-ahead variant) is first dequantized once per
+ *             128-key tile into the workspace ("NVFP4 KV cache A4Q prefill
+ *             explained", section "Compare A4Q with dequantize-ahead
+ *             repacking"), instead of once per q tile inside the kernel.
+ *             Results are identical either way.
  * num_q_heads must be a multiple of num_kv_heads with a power-of-two ratio
  * of at most 128.  q_len == 0 requests produce nothing. */
 int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
@@ -169,8 +178,11 @@ int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t
                        int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o,
                        float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes for op (NVFP4KV_OP_PREFILL uses total_q, NVFP4KV_OP_DECODE
- * uses max_kv_len).  Host-only, no CUDA call.  Returns 0 for bad arguments. */
+/* Workspace bytes for op.  NVFP4KV_OP_PREFILL: the schedule for total_q
+ * query tokens, plus, when max_kv_len > 0, the repack tiles (64 KB per
+ * request, kv head and 128-key tile of max_kv_len).  NVFP4KV_OP_DECODE: the
+ * split-KV partials for max_kv_len.  Host-only, no CUDA call.  Returns 0 for
+ * bad arguments. */
 size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int64_t total_q,
                              int32_t max_kv_len);
 

@@ -155,8 +155,9 @@ def nvfp4_paged_prefill(q: torch.Tensor, cache: Cache, page_table: torch.Tensor,
         out = torch.empty_like(q)
     if sm_scale is None:
         sm_scale = HEAD_DIM ** -0.5
-    need = nvfp4_workspace_bytes(OP_PREFILL, batch, hq, cache.num_kv_heads, total_q, 0)
     if workspace is None:
+        need = nvfp4_workspace_bytes(OP_PREFILL, batch, hq, cache.num_kv_heads, total_q,
+                                     page_table.shape[1] * PAGE_SIZE)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     d = cache.desc()
     _check("nvfp4_paged_prefill", lib.nvfp4_paged_prefill(

@@ -103,7 +103,23 @@ int64_t prefill_max_items(int64_t total_q, int batch, int num_q_heads, int num_k
   return (static_cast<int64_t>((total_q * group + kBM - 1) / kBM) + batch) * num_kv_heads;
 }
 
+// Prefill workspace: [16 B header][items: 8 B each][unit prefix][tile prefix]
+// padded to 1 KB, then (repack mode) V tiles and K tiles of 32 KB each for
+// every (request, kv head, KV tile) the batch can hold.
+constexpr size_t kRepackTileBytes = 32768;
+size_t prefill_sched_bytes(int64_t max_items, int batch) {
+  const size_t b = 16 + 8 * static_cast<size_t>(max_items) + 8 * (static_cast<size_t>(batch) + 1);
+  return (b + 1023) & ~size_t(1023);
+}
+size_t prefill_repack_tiles(int batch, int num_kv_heads, int64_t max_kv_len) {
+  if (max_kv_len <= 0) return 0;
+  return static_cast<size_t>(batch) * num_kv_heads * static_cast<size_t>((max_kv_len + kBN - 1) / kBN);
+}
+
 int launch_rc(cudaError_t e) { return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA; }
+
+// Decode workspace starts with the item schedule: count + per-request prefix.
+size_t decode_sched_bytes(int batch) { return (16 + 4 * (static_cast<size_t>(batch) + 1) + 15) & ~size_t(15); }
 
 // A wait that can only end by its time limit (nothing arrives on `bar`).
 __global__ void nvfp4_debug_wait_kernel(uint64_t limit_ns, int* status) {
@@ -128,13 +144,13 @@ size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int
   if (op == NVFP4KV_OP_PREFILL) {
     if (total_q < 0) return 0;
     const int64_t items = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
-    const size_t bytes = 16 + 8 * static_cast<size_t>(items) + 4 * (static_cast<size_t>(batch) + 1);
-    return (bytes + 15) & ~static_cast<size_t>(15);
+    return prefill_sched_bytes(items, batch) +
+           2 * kRepackTileBytes * prefill_repack_tiles(batch, num_kv_heads, max_kv_len);
   }
   if (op == NVFP4KV_OP_DECODE) {
     if (max_kv_len < 0) return 0;
     const size_t splits = (static_cast<size_t>(max_kv_len) + kDecSplit - 1) / kDecSplit;
-    return static_cast<size_t>(batch) * splits * num_q_heads * (kHeadDim + 1) * sizeof(float);
+    return decode_sched_bytes(batch) + static_cast<size_t>(batch) * splits * num_q_heads * (kHeadDim + 1) * sizeof(float);
   }
   return 0;
 }
@@ -164,9 +180,13 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
   a.k_scale_g = cache->k_global_scale;
   a.v_scale_g = cache->v_global_scale;
   a.status = d->status;
-  const int64_t threads = rows * 4;
-  dim3 grid(static_cast<unsigned>((threads + 255) / 256), 2);
-  nvfp4_kv_append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  // one persistent wave: 8 CTAs of 256 threads per SM, grid-stride over the
+  // 8 * num_tokens * Hkv units of K and V
+  const int64_t units = rows * 8;
+  const int64_t want = (units + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(d->num_sms) * 8;
+  nvfp4_kv_append_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0,
+                           static_cast<cudaStream_t>(stream)>>>(a);
   return launch_rc(cudaGetLastError());
 }
 
@@ -186,21 +206,35 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
   if (total_q * num_q_heads >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
   if (batch == 0 || total_q == 0) return NVFP4KV_OK;
   if (!q || !o || !page_table || !kv_lens || !qo_indptr || !aligned16(q) || !aligned16(o)) return NVFP4KV_ERR_ARG;
-  const size_t need = nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, batch, num_q_heads, cache->num_kv_heads, total_q, 0);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return NVFP4KV_ERR_WORKSPACE;
   const int64_t max_items = prefill_max_items(total_q, batch, num_q_heads, cache->num_kv_heads);
   if (max_items >= (int64_t(1) << 30)) return NVFP4KV_ERR_ARG;
+  const size_t sched = prefill_sched_bytes(max_items, batch);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < sched) return NVFP4KV_ERR_WORKSPACE;
+  // Repack mode (each V tile dequantized once, into the workspace) when the
+  // workspace holds a tile for every (request, kv head, KV tile) the page
+  // table allows and requests average at least two q tiles per kv head.
+  const size_t rtiles = prefill_repack_tiles(batch, cache->num_kv_heads, static_cast<int64_t>(max_pages_per_req) * kPageSize);
+  const int64_t qtiles = (total_q * (num_q_heads / cache->num_kv_heads) + kBM - 1) / kBM;
+  const bool repack = workspace_bytes >= sched + 2 * kRepackTileBytes * rtiles && qtiles >= 2 * static_cast<int64_t>(batch);
   DeviceState* d = nullptr;
   if ((rc = device_state(&d))) return rc;
   if ((rc = get_encoder())) return rc;
 
-  CUtensorMap tmap;
-  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(cache->num_pages) * cache->num_kv_heads * kPageSize};
+  CUtensorMap tmap, tmap_s;
+  const cuuint64_t rows = static_cast<cuuint64_t>(cache->num_pages) * cache->num_kv_heads;
+  const cuuint64_t dims[2] = {64, rows * kPageSize};
   const cuuint64_t strides[1] = {64};
   const cuuint32_t box[2] = {64, kPageSize};
   const cuuint32_t estr[2] = {1, 1};
   if (g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, cache->k_data, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return NVFP4KV_ERR_CUDA;
+  const cuuint64_t dims_s[2] = {128, rows};  // one 128-byte scale page per (page, kv head)
+  const cuuint64_t strides_s[1] = {128};
+  const cuuint32_t box_s[2] = {128, 1};
+  if (g_encode(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, cache->k_scale, dims_s, strides_s, box_s, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return NVFP4KV_ERR_CUDA;
 
@@ -219,6 +253,7 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
 
   PrefillArgs a;
   a.q = q;
+  a.k_data = static_cast<const uint8_t*>(cache->k_data);
   a.k_scale = static_cast<const uint8_t*>(cache->k_scale);
   a.v_data = static_cast<const uint8_t*>(cache->v_data);
   a.v_scale = static_cast<const uint8_t*>(cache->v_scale);
@@ -240,8 +275,13 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
   a.o = o;
   a.lse = lse;
   a.work = static_cast<const int*>(workspace);
+  a.tile_prefix = static_cast<const int*>(workspace) + 4 + 2 * max_items + (batch + 1);
+  uint8_t* rbase = static_cast<uint8_t*>(workspace) + sched;
+  a.repack_v = repack ? rbase : nullptr;
+  a.repack_k = repack ? rbase + kRepackTileBytes * rtiles : nullptr;
   a.status = d->status;
-  return launch_rc(launch_prefill(a, plan, tmap, variant, d->num_sms, static_cast<cudaStream_t>(stream)));
+  return launch_rc(
+      launch_prefill(a, plan, tmap, tmap_s, variant, repack, d->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t* cache, const int32_t* page_table,
@@ -281,11 +321,13 @@ int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t
   a.sm_scale = sm_scale;
   a.o = o;
   a.lse = lse;
-  float* ws = static_cast<float*>(workspace);
+  a.batch = batch;
+  a.sched = static_cast<int*>(workspace);
+  float* ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + decode_sched_bytes(batch));
   a.part_o = ws;
   a.part_lse = ws + static_cast<size_t>(batch) * a.max_splits * num_q_heads * kHeadDim;
   a.status = d->status;
-  return launch_rc(launch_decode(a, batch, static_cast<cudaStream_t>(stream)));
+  return launch_rc(launch_decode(a, batch, d->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 int nvfp4_quantize_rows(const void* x, int64_t rows, int32_t mode, float global_scale, void* packed, void* scales,

@@ -20,40 +20,76 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return r;
 }
 
-__global__ void __launch_bounds__(256) nvfp4_kv_append_kernel(AppendArgs a) {
-  const int tensor = blockIdx.y;  // 0 = K, 1 = V
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t row = gid >> 2;  // token * Hkv + head
-  const int part = static_cast<int>(gid & 3);
-  if (row >= a.num_tokens * a.num_kv_heads) return;
-  const int64_t t = row / a.num_kv_heads;
-  const int h = static_cast<int>(row - t * a.num_kv_heads);
-  const int64_t slot = a.slot_mapping[t];
-  if (slot < 0) return;
-  if (slot >= a.num_slots) {
+// One unit = 32 values (64 B of bf16) of one (token, kv head) row of K or V:
+// two 16-value blocks -> 16 code bytes + 2 scale bytes.
+struct AppendUnit {
+  uint4 w[4];
+  int64_t slot;
+};
+
+__device__ __forceinline__ void append_load(const AppendArgs& a, int64_t u, int64_t units_per_tensor,
+                                            AppendUnit& x) {
+  const int tensor = u >= units_per_tensor;
+  const int64_t uu = u - tensor * units_per_tensor;
+  const int64_t row = uu >> 2;  // token * Hkv + head
+  const int part = static_cast<int>(uu & 3);
+  const uint16_t* src = reinterpret_cast<const uint16_t*>(tensor ? a.v : a.k) + row * kHeadDim + part * 32;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x.w[i] = ld_stream_v4(src + 8 * i);
+  x.slot = a.slot_mapping[row / a.num_kv_heads];
+}
+
+__device__ __forceinline__ void append_store(const AppendArgs& a, int64_t u, int64_t units_per_tensor,
+                                             const AppendUnit& x) {
+  if (x.slot < 0) return;
+  if (x.slot >= a.num_slots) {
     set_status(a.status, kDevBadSlot);
     return;
   }
-  const uint16_t* src = reinterpret_cast<const uint16_t*>(tensor ? a.v : a.k) + row * kHeadDim + part * 32;
-  const float g = tensor ? a.v_scale_g : a.k_scale_g;
-  float x[32];
+  const int tensor = u >= units_per_tensor;
+  const int64_t uu = u - tensor * units_per_tensor;
+  const int64_t row = uu >> 2;
+  const int part = static_cast<int>(uu & 3);
+  const int h = static_cast<int>(row % a.num_kv_heads);
+  float v[32];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint4 w = ld_stream_v4(src + 8 * i);
-    bf16x2_to_f32(w.x, x[8 * i + 0], x[8 * i + 1]);
-    bf16x2_to_f32(w.y, x[8 * i + 2], x[8 * i + 3]);
-    bf16x2_to_f32(w.z, x[8 * i + 4], x[8 * i + 5]);
-    bf16x2_to_f32(w.w, x[8 * i + 6], x[8 * i + 7]);
+    bf16x2_to_f32(x.w[i].x, v[8 * i + 0], v[8 * i + 1]);
+    bf16x2_to_f32(x.w[i].y, v[8 * i + 2], v[8 * i + 3]);
+    bf16x2_to_f32(x.w[i].z, v[8 * i + 4], v[8 * i + 5]);
+    bf16x2_to_f32(x.w[i].w, v[8 * i + 6], v[8 * i + 7]);
   }
+  const float g = tensor ? a.v_scale_g : a.k_scale_g;
   uint4 codes;
-  const uint32_t s0 = quant_block16(x, g, codes.x, codes.y);
-  const uint32_t s1 = quant_block16(x + 16, g, codes.z, codes.w);
-  const int64_t page = slot >> 4, off = slot & 15;
+  const uint32_t s0 = quant_block16(v, g, codes.x, codes.y);
+  const uint32_t s1 = quant_block16(v + 16, g, codes.z, codes.w);
+  const int64_t page = x.slot >> 4, off = x.slot & 15;
   const int64_t tok_row = (page * a.num_kv_heads + h) * kPageSize + off;
   uint8_t* data = tensor ? a.v_data : a.k_data;
   uint8_t* scale = tensor ? a.v_scale : a.k_scale;
   *reinterpret_cast<uint4*>(data + tok_row * (kHeadDim / 2) + part * 16) = codes;
   *reinterpret_cast<uint16_t*>(scale + tok_row * (kHeadDim / 16) + part * 2) = static_cast<uint16_t>(s0 | (s1 << 8));
+}
+
+// Grid-stride over all units of K then V, two units per thread per step so
+// that 128 B of loads per thread are in flight before any is consumed.
+__global__ void __launch_bounds__(256) nvfp4_kv_append_kernel(AppendArgs a) {
+  const int64_t per_tensor = a.num_tokens * a.num_kv_heads * 4;
+  const int64_t total = 2 * per_tensor;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; u + stride < total; u += 2 * stride) {
+    AppendUnit x0, x1;
+    append_load(a, u, per_tensor, x0);
+    append_load(a, u + stride, per_tensor, x1);
+    append_store(a, u, per_tensor, x0);
+    append_store(a, u + stride, per_tensor, x1);
+  }
+  if (u < total) {
+    AppendUnit x0;
+    append_load(a, u, per_tensor, x0);
+    append_store(a, u, per_tensor, x0);
+  }
 }
 
 // Standalone quantizer (same codec; GLOBAL or PER_ROW scale).  One warp per

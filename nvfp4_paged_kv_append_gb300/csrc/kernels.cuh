@@ -65,6 +65,8 @@ struct DecodeArgs {
   int num_kv_heads;
   int num_q_heads;
   int max_splits;
+  int batch;
+  int* sched;         // [0] item count, [4..] per-request item prefix (batch+1)
   float k_g, v_g, sm_scale;
   void* o;            // bf16 [B][Hq][128]
   float* lse;         // optional [B][Hq]
@@ -80,6 +82,7 @@ constexpr int kPagesPerTile = kBN / kPageSize;
 
 struct PrefillArgs {
   const void* q;  // bf16 [total_q][Hq][128]
+  const uint8_t* k_data;
   const uint8_t* k_scale;
   const uint8_t* v_data;
   const uint8_t* v_scale;
@@ -98,7 +101,10 @@ struct PrefillArgs {
   float sm_scale, k_g, v_g;
   void* o;          // bf16 [total_q][Hq][128]
   float* lse;       // optional [total_q][Hq]
-  const int* work;  // work[0] = item count, items from work + 4 (int2 each)
+  const int* work;  // [0] item count, [1] repacked tile count; items (int2) from work + 4
+  const int* tile_prefix;  // [batch+1] per-request KV-tile prefix (repack mode)
+  uint8_t* repack_v;       // repacked V tiles (32 KB each), repack mode
+  uint8_t* repack_k;       // repacked K tiles (BF16), repack mode, dequant-ahead variant
   int* status;
 };
 
@@ -122,8 +128,8 @@ __global__ void nvfp4_quantize_rows_kernel(QuantArgs a);
 __global__ void nvfp4_dequantize_rows_kernel(DequantArgs a);
 
 // Launchers that hide templates (decode.cu / prefill.cu).
-cudaError_t launch_decode(const DecodeArgs& a, int batch, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, const CUtensorMap& tmap_k, int variant,
-                           int num_sms, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, const CUtensorMap& tmap_k,
+                           const CUtensorMap& tmap_ks, int variant, bool repack, int num_sms, cudaStream_t s);
 
 }  // namespace nvfp4kv

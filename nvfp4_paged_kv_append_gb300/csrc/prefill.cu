@@ -7,19 +7,30 @@
 // the G query heads of one kv head, so each K/V tile fetched serves the whole
 // GQA group.  Per KV tile of 128 keys (8 pages):
 //
-//   producer warp   TMA: packed K pages (64B-swizzled, straight into the
-//                   FP4 MMA operand layout), K scales, packed V, V scales
+//   producer warp   TMA: packed K pages (64B-swizzled, straight into the FP4
+//                   MMA operand layout) and K scale pages; V either as packed
+//                   pages + scales (in-kernel mode) or as one 32 KB FP16 tile
+//                   prepared once per (request, kv head, tile) by the repack
+//                   pre-pass (repack mode)
 //   transform WG    A4Q: K block scales -> TMEM (UE4M3 scale operand of the
-//                   block-scaled MMA); DQ-ahead: K -> BF16 once per tile.
-//                   V -> FP16 in the MMA's MN-major layout (exact).
-//                   At each item start: Q tile -> NVFP4 (per-row dual level
-//                   scale) + Q block scales -> TMEM (A4Q), or Q -> smem (BF16).
+//                   block-scaled MMA).  In-kernel mode also: V -> FP16 in the
+//                   MMA's MN-major layout (exact), and for the dequant-ahead
+//                   variant K -> BF16.  At each item start: Q tile -> NVFP4
+//                   (per-row dual level scale) + Q block scales -> TMEM (A4Q),
+//                   or Q -> shared memory as BF16 (dequant-ahead).
 //   MMA warp        S = Q K^T: tcgen05 kind::mxf4nvf4 (scale_vec 4X, UE4M3),
-//                   or kind::f16 BF16 (DQ-ahead), fp32 S in TMEM (double
-//                   buffered).  O += P V: kind::f16 with P read from TMEM.
-//   softmax WG      one TMEM lane (= one row) per thread: causal mask, online
-//                   softmax in the log2 domain with lazy O rescaling, P as
-//                   FP16 written back over S; epilogue O * v_scale / l.
+//                   or kind::f16 BF16 (dequant-ahead); fp32 S in TMEM, double
+//                   buffered.  O += P V: kind::f16 with P read from TMEM.
+//   softmax WGs     two warpgroups, one TMEM lane (= one row) per thread, each
+//                   owning 64 of the tile's 128 keys (and 64 of O's columns):
+//                   causal mask, row max exchanged through shared memory,
+//                   online softmax in the log2 domain with lazy O rescaling,
+//                   P as FP16 written back over S; epilogue O * v_scale / l.
+//
+// Repack mode follows the pages' "convert an NVFP4 tile once before repeated
+// MMA use": every q tile of a request that visits a KV tile would otherwise
+// dequantize the same V values again.  It is used when the caller's workspace
+// has room and requests have at least two q tiles per kv head on average.
 //
 // PV runs on FP16 operands: every dequantized V value (E2M1 x E4M3) is exact
 // in FP16 (and in BF16), while FP16 keeps 3 more mantissa bits of P.
@@ -33,45 +44,57 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
 
-constexpr int kThreads = 320;  // warps 0-3 transform, 4-7 softmax, 8 producer, 9 MMA
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+// warps 0-3 transform, 4-7 softmax half 0, 8-11 softmax half 1,
+// 12 producer, 13 MMA, 14-15 idle (they complete the fourth warpgroup)
+constexpr int kThreads = 512;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 
 // TMEM columns
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA = 384, kColSFB = 392;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kStageKData = 8192, kStageKScale = 1024, kStageVData = 8192, kStageVScale = 1024;
-constexpr uint32_t kStageBytes = kStageKData + kStageKScale + kStageVData + kStageVScale;  // 18 KB
-constexpr uint32_t kTileBuf16 = 32768;  // 128 keys x 128 values x 2 B
+constexpr uint32_t kKData = 8192, kKScale = 1024, kVData = 8192, kVScale = 1024;
+constexpr uint32_t kTile16 = 32768;  // 128 keys x 128 values x 2 B
 
-template <int VARIANT>
+// Shared-memory layout per (variant, mode).  Stage contents:
+//   in-kernel:     K codes 8 KB | K scales 1 KB | V codes 8 KB | V scales 1 KB
+//   A4Q repack:    K codes 8 KB | K scales 1 KB | V tile (FP16) 32 KB
+//   DQ repack:     K tile (BF16) 32 KB | V tile (FP16) 32 KB
+template <int VARIANT, bool REPACK>
 struct Layout {
   static constexpr bool kA4Q = VARIANT == 0;
-  static constexpr int kStages = kA4Q ? 3 : 2;
+  static constexpr int kStages = REPACK ? (kA4Q ? 4 : 2) : (kA4Q ? 3 : 2);
+  static constexpr uint32_t kStageBytes =
+      REPACK ? (kA4Q ? kKData + kKScale + kTile16 : 2 * kTile16) : kKData + kKScale + kVData + kVScale;
+  static constexpr uint32_t kStageV = REPACK ? (kA4Q ? kKData + kKScale : kTile16) : kKData + kKScale;
   static constexpr uint32_t kQBytes = kA4Q ? 8192u : 32768u;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffStage = kOffQ + kQBytes;
-  static constexpr uint32_t kOffV = kOffStage + kStages * kStageBytes;
-  static constexpr uint32_t kOffK = kOffV + 2 * kTileBuf16;  // DQ-ahead only
-  static constexpr uint32_t kOffSmall = kOffK + (kA4Q ? 0u : 2 * kTileBuf16);
+  static constexpr uint32_t kOffV = kOffStage + kStages * kStageBytes;            // in-kernel V buffers
+  static constexpr uint32_t kOffK = kOffV + (REPACK ? 0u : 2 * kTile16);          // in-kernel DQ K buffers
+  static constexpr uint32_t kOffSmall = kOffK + ((!REPACK && !kA4Q) ? 2 * kTile16 : 0u);
   static constexpr uint32_t kOffQScale = kOffSmall;            // 128 floats
   static constexpr uint32_t kOffSfaStage = kOffQScale + 512;   // 128 x 8 B
   static constexpr uint32_t kOffMask = kOffSfaStage + 1024;    // per-stage page mask
-  static constexpr uint32_t kOffBar = kOffMask + 64;
+  static constexpr uint32_t kOffXmax = kOffMask + 64;          // [2 parity][2 half][128] row maxima
+  static constexpr uint32_t kOffXl = kOffXmax + 2048;          // [2 half][128] row sums
+  static constexpr uint32_t kOffBar = kOffXl + 1024;
   static constexpr uint32_t kNumBars = 32;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kOffTmemSlot + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1 KB alignment
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
+  static_assert(kStageBytes % 1024 == 0 && kStageV % 1024 == 0, "1 KB aligned operands");
 };
 
 struct Bars {
-  uint64_t* kv_full;   // [3]
-  uint64_t* kv_empty;  // [3]
-  uint64_t* sfb_full;  // [2] (A4Q: K scales in TMEM; DQ-ahead: K tile in BF16)
+  uint64_t* kv_full;   // [4]
+  uint64_t* kv_empty;  // [4]
+  uint64_t* sfb_full;  // [2] (A4Q: K scales in TMEM; in-kernel dequant-ahead: K tile in BF16)
   uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
-  uint64_t* vdq_full;  // [2]
+  uint64_t* vdq_full;  // [2] in-kernel mode: V tile in FP16
   uint64_t* pv_done;   // [2]
   uint64_t* o_full;
   uint64_t* o_empty;
@@ -80,24 +103,26 @@ struct Bars {
   uint64_t* drain;
   uint64_t* qs_empty;   // softmax has read the item's row scales
   uint64_t* sfa_ready;  // transform warps have staged the item's Q block scales
+  uint64_t* xchg;       // [4] per TMEM quadrant: the two softmax halves of a row meet
 };
 
 __device__ __forceinline__ Bars make_bars(uint64_t* base) {
   Bars b;
   b.kv_full = base + 0;
-  b.kv_empty = base + 3;
-  b.sfb_full = base + 6;
-  b.s_full = base + 8;
-  b.p_full = base + 10;
-  b.vdq_full = base + 12;
-  b.pv_done = base + 14;
-  b.o_full = base + 16;
-  b.o_empty = base + 17;
-  b.q_full = base + 18;
-  b.q_empty = base + 19;
-  b.drain = base + 20;
-  b.qs_empty = base + 21;
-  b.sfa_ready = base + 22;
+  b.kv_empty = base + 4;
+  b.sfb_full = base + 8;
+  b.s_full = base + 10;
+  b.p_full = base + 12;
+  b.vdq_full = base + 14;
+  b.pv_done = base + 16;
+  b.o_full = base + 18;
+  b.o_empty = base + 19;
+  b.q_full = base + 20;
+  b.q_empty = base + 21;
+  b.drain = base + 22;
+  b.qs_empty = base + 23;
+  b.sfa_ready = base + 24;
+  b.xchg = base + 25;  // 25..28
   return b;
 }
 
@@ -134,6 +159,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -141,16 +172,61 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 // 16-byte chunk `cc` (0..7) of row `r` in a 128B-swizzled [rows][128 B] tile.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t cc) { return r * 128u + (((cc ^ r) & 7u) << 4); }
+
+// Store the four 16-byte chunks o0..o3 of one (key, 32-value group c) unit
+// into a 128B-swizzled operand tile.  Lanes holding groups 2-3 store their
+// chunks in the order 2,3,0,1 so that every 8-lane phase of a warp-wide
+// shared-memory store hits 8 different bank groups.
+__device__ __forceinline__ void store_unit_sw128(uint8_t* tile, int key, int c, const uint32_t (&o0)[4],
+                                                 const uint32_t (&o1)[4], const uint32_t (&o2)[4],
+                                                 const uint32_t (&o3)[4]) {
+  uint8_t* dst = tile + (c >> 1) * 16384;
+  const uint32_t cc = (c & 1) * 4;
+  const bool rot = (c >> 1) != 0;
+  const uint4 a0 = make_uint4(o0[0], o0[1], o0[2], o0[3]), a1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+  const uint4 a2 = make_uint4(o2[0], o2[1], o2[2], o2[3]), a3 = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 2 : 0))) = rot ? a2 : a0;
+  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 3 : 1))) = rot ? a3 : a1;
+  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 0 : 2))) = rot ? a0 : a2;
+  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 1 : 3))) = rot ? a1 : a3;
+}
+
 // 16-byte chunk `c` (0..3) of row `r` in a 64B-swizzled [rows][64 B] tile.
 __device__ __forceinline__ uint32_t sw64_off(uint32_t r, uint32_t c) { return r * 64u + (((c ^ (r >> 1)) & 3u) << 4); }
 
+// Dequantize 32 values (16 code bytes, two 16-value blocks) of one row.
+template <bool BF16>
+__device__ __forceinline__ void dequant_unit(uint4 src, uint32_t sc01, uint32_t (&o0)[4], uint32_t (&o1)[4],
+                                             uint32_t (&o2)[4], uint32_t (&o3)[4]) {
+  if (BF16) {
+    const uint32_t s0 = scale_bf16x2_x2p112(sc01 & 0xFFu), s1 = scale_bf16x2_x2p112(sc01 >> 8);
+    dequant8_bf16(src.x, s0, o0);
+    dequant8_bf16(src.y, s0, o1);
+    dequant8_bf16(src.z, s1, o2);
+    dequant8_bf16(src.w, s1, o3);
+  } else {
+    const uint32_t s0 = scale_f16x2(sc01 & 0xFFu), s1 = scale_f16x2(sc01 >> 8);
+    dequant8_f16(src.x, s0, o0);
+    dequant8_f16(src.y, s0, o1);
+    dequant8_f16(src.z, s1, o2);
+    dequant8_f16(src.w, s1, o3);
+  }
+}
+
+// Index of the repacked tile (request b, kv head h, KV tile j).
+__device__ __forceinline__ int64_t repack_index(const PrefillArgs& a, int b, int h, int j) {
+  const int p0 = a.tile_prefix[b], n_t = a.tile_prefix[b + 1] - p0;
+  return static_cast<int64_t>(p0) * a.num_kv_heads + static_cast<int64_t>(h) * n_t + j;
+}
+
 // ---------------------------------------------------------------------------
 // producer warp
-template <int VARIANT>
-__device__ void producer_loop(const PrefillArgs& a, const CUtensorMap* tmap_k, uint8_t* smem, const Bars& bars,
-                              int lane) {
-  using L = Layout<VARIANT>;
+template <int VARIANT, bool REPACK>
+__device__ void producer_loop(const PrefillArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_ks,
+                              uint8_t* smem, const Bars& bars, int lane) {
+  using L = Layout<VARIANT, REPACK>;
   int* mask_slot = reinterpret_cast<int*>(smem + L::kOffMask);
+  const int32_t oob_row = a.num_pages * a.num_kv_heads;  // first row past the pools: a TMA box there reads zeros
   uint32_t it_ctr = 0;
   Item item;
   for (int round = 0; get_item(a, round, item); ++round) {
@@ -166,24 +242,47 @@ __device__ void producer_loop(const PrefillArgs& a, const CUtensorMap* tmap_k, u
         }
       }
       const unsigned valid = __ballot_sync(0xffffffffu, pid >= 0);
+      // K codes and K scales: all 8 pages through TMA (pages that hold no
+      // data read zeros); V: packed pages (in-kernel) or one repacked tile.
+      uint32_t bytes;
+      if constexpr (REPACK && !L::kA4Q) bytes = 2 * kTile16;
+      else if constexpr (REPACK) bytes = kPagesPerTile * (1024 + 128) + kTile16;
+      else bytes = kPagesPerTile * (1024 + 128) + __popc(valid) * (1024 + 128);
       bool ok = true;
       if (lane == 0) {
         ok = mbar_wait(&bars.kv_empty[st], ph ^ 1u, a.status);
         if (ok) {
           mask_slot[st] = static_cast<int>(valid);
-          mbar_arrive_expect_tx(&bars.kv_full[st], __popc(valid) * (kStageBytes / kPagesPerTile));
+          mbar_arrive_expect_tx(&bars.kv_full[st], bytes);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) return;
-      if (pid >= 0) {
-        uint8_t* stage = smem + L::kOffStage + st * kStageBytes;
-        const int64_t row = (static_cast<int64_t>(pid) * a.num_kv_heads + item.kvh) * kPageSize;
-        tma_load_2d(stage + lane * 1024, tmap_k, 0, static_cast<int32_t>(row), &bars.kv_full[st]);
-        bulk_load(stage + kStageKData + lane * 128, a.k_scale + row * 8, 128, &bars.kv_full[st]);
-        bulk_load(stage + kStageKData + kStageKScale + lane * 1024, a.v_data + row * 64, 1024, &bars.kv_full[st]);
-        bulk_load(stage + kStageKData + kStageKScale + kStageVData + lane * 128, a.v_scale + row * 8, 128,
-                  &bars.kv_full[st]);
+      uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
+      if constexpr (REPACK && !L::kA4Q) {
+        if (lane == 0) {
+          const int64_t t = repack_index(a, item.b, item.kvh, j);
+          bulk_load(stage, a.repack_k + t * kTile16, kTile16, &bars.kv_full[st]);
+          bulk_load(stage + L::kStageV, a.repack_v + t * kTile16, kTile16, &bars.kv_full[st]);
+        }
+      } else {
+        if (lane < kPagesPerTile) {
+          const int32_t rowp = pid >= 0 ? pid * a.num_kv_heads + item.kvh : oob_row;
+          tma_load_2d(stage + lane * 1024, tmap_k, 0, rowp * kPageSize, &bars.kv_full[st]);
+          tma_load_2d(stage + kKData + lane * 128, tmap_ks, 0, rowp, &bars.kv_full[st]);
+        }
+        if constexpr (REPACK) {
+          if (lane == 0) {
+            const int64_t t = repack_index(a, item.b, item.kvh, j);
+            bulk_load(stage + L::kStageV, a.repack_v + t * kTile16, kTile16, &bars.kv_full[st]);
+          }
+        } else {
+          if (pid >= 0) {
+            const int64_t row = (static_cast<int64_t>(pid) * a.num_kv_heads + item.kvh) * kPageSize;
+            bulk_load(stage + kKData + kKScale + lane * 1024, a.v_data + row * 64, 1024, &bars.kv_full[st]);
+            bulk_load(stage + kKData + kKScale + kVData + lane * 128, a.v_scale + row * 8, 128, &bars.kv_full[st]);
+          }
+        }
       }
     }
   }
@@ -191,9 +290,9 @@ __device__ void producer_loop(const PrefillArgs& a, const CUtensorMap* tmap_k, u
 
 // ---------------------------------------------------------------------------
 // MMA warp (lane 0 only)
-template <int VARIANT>
+template <int VARIANT, bool REPACK>
 __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase) {
-  using L = Layout<VARIANT>;
+  using L = Layout<VARIANT, REPACK>;
   const uint32_t q_s = smem_u32(smem + L::kOffQ);
   const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   const uint32_t idesc_qk = L::kA4Q ? idesc_mxf4nvf4(128, 128) : idesc_f16(128, 128, 1, 1, 0, 0);
@@ -202,10 +301,12 @@ __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, 
   auto do_pv = [&](uint32_t it, bool first) -> bool {
     const uint32_t b = it & 1u, ph = (it >> 1) & 1u;
     if (!mbar_wait(&bars.p_full[b], ph, a.status)) return false;
-    if (!mbar_wait(&bars.vdq_full[b], ph, a.status)) return false;
+    if (!REPACK && !mbar_wait(&bars.vdq_full[b], ph, a.status)) return false;
     if (first && !mbar_wait(bars.o_empty, (item_ctr & 1u) ^ 1u, a.status)) return false;
     tc_fence_after();
-    const uint32_t v_s = smem_u32(smem + L::kOffV + b * kTileBuf16);
+    const uint32_t st = it % L::kStages;
+    const uint32_t v_s = REPACK ? smem_u32(smem + L::kOffStage + st * L::kStageBytes + L::kStageV)
+                                : smem_u32(smem + L::kOffV + b * kTile16);
     const uint32_t s_col = b ? kColS1 : kColS0;
 #pragma unroll
     for (uint32_t k = 0; k < 8; ++k) {
@@ -213,6 +314,7 @@ __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, 
                  (first && k == 0) ? 0u : 1u);
     }
     tc_commit(&bars.pv_done[b]);
+    if (REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's V tile has been read
     return true;
   };
   for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
@@ -222,19 +324,20 @@ __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, 
       const uint32_t it = it_ctr + j;
       const uint32_t st = it % L::kStages, b = it & 1u;
       if (!mbar_wait(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
-      if (!mbar_wait(&bars.sfb_full[b], (it >> 1) & 1u, a.status)) return;
+      if ((L::kA4Q || !REPACK) && !mbar_wait(&bars.sfb_full[b], (it >> 1) & 1u, a.status)) return;
       if (it >= 2 && !mbar_wait(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
       tc_fence_after();
       const uint32_t s_col = b ? kColS1 : kColS0;
+      const uint32_t stage_s = smem_u32(smem + L::kOffStage + st * L::kStageBytes);
       if constexpr (L::kA4Q) {
-        const uint32_t k_s = smem_u32(smem + L::kOffStage + st * kStageBytes);
 #pragma unroll
         for (uint32_t s = 0; s < 2; ++s) {
-          mma_nvf4_ss(tbase + s_col, smem_desc(q_s + 32 * s, 16, 512, kSwz64), smem_desc(k_s + 32 * s, 16, 512, kSwz64),
-                      idesc_qk, tbase + kColSFA + 4 * s, tbase + kColSFB + 8 * b + 4 * s, s > 0 ? 1u : 0u);
+          mma_nvf4_ss(tbase + s_col, smem_desc(q_s + 32 * s, 16, 512, kSwz64),
+                      smem_desc(stage_s + 32 * s, 16, 512, kSwz64), idesc_qk, tbase + kColSFA + 4 * s,
+                      tbase + kColSFB + 8 * b + 4 * s, s > 0 ? 1u : 0u);
         }
       } else {
-        const uint32_t k_s = smem_u32(smem + L::kOffK + b * kTileBuf16);
+        const uint32_t k_s = REPACK ? stage_s : smem_u32(smem + L::kOffK + b * kTile16);
 #pragma unroll
         for (uint32_t k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
@@ -243,7 +346,7 @@ __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, 
         }
       }
       tc_commit(&bars.s_full[b]);
-      tc_commit(&bars.kv_empty[st]);
+      if (!REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's K has been read
       if (j == item.n_tiles - 1) tc_commit(bars.q_empty);
       if (j >= 1 && !do_pv(it - 1, j == 1)) return;
     }
@@ -255,9 +358,9 @@ __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, 
 
 // ---------------------------------------------------------------------------
 // transform warpgroup (warps 0-3): thread = Q row / TMEM lane
-template <int VARIANT>
+template <int VARIANT, bool REPACK>
 __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int tid) {
-  using L = Layout<VARIANT>;
+  using L = Layout<VARIANT, REPACK>;
   const int warp = tid >> 5, lane = tid & 31;
   const int G = a.group, lg = a.log2_group;
   float* qscale = reinterpret_cast<float*>(smem + L::kOffQScale);
@@ -278,50 +381,50 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
       const int tq = item.tok0 + (r >> lg);
       const bool valid = (r >> lg) < item.n_tok;
       const int hq = item.kvh * G + (r & (G - 1));
-      uint32_t w[64];
-      if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) +
-                                                          (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          uint4 v = src[i];
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) w[i] = 0u;
-      }
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) +
+                                                        (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim);
       if constexpr (L::kA4Q) {
+        // pass 1: row amax (the row stays in L1 for pass 2)
         float amax = 0.0f;
+        if (valid) {
+#pragma unroll 4
+          for (int i = 0; i < 16; ++i) {
+            const uint4 v = src[i];
+            const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float lo, hi;
-          bf16x2_to_f32(w[i], lo, hi);
-          amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
-        }
-        const float g_row = __fdiv_rn(amax, 2688.0f);
-        uint32_t codes[16];
-        uint32_t sc[8];
-#pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
-          float x[16];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) bf16x2_to_f32(w[8 * blk + i], x[2 * i], x[2 * i + 1]);
-          if (g_row != 0.0f) {
-            sc[blk] = quant_block16(x, g_row, codes[2 * blk], codes[2 * blk + 1]);
-          } else {
-            sc[blk] = 0u;
-            codes[2 * blk] = codes[2 * blk + 1] = 0u;
+            for (int k = 0; k < 4; ++k) {
+              float lo, hi;
+              bf16x2_to_f32(ww[k], lo, hi);
+              amax = fmax3(amax, fabsf(lo), fabsf(hi));
+            }
           }
         }
+        const float g_row = __fdiv_rn(amax, 2688.0f);
+        // pass 2: per 32-value chunk (two blocks) -> 16 code bytes, 2 scales
         uint8_t* qrow = smem + L::kOffQ;
+        uint32_t sc[8];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t cw[4] = {0u, 0u, 0u, 0u};
+          sc[2 * c] = sc[2 * c + 1] = 0u;
+          if (valid && g_row != 0.0f) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(qrow + sw64_off(r, c)) =
-              make_uint4(codes[4 * c], codes[4 * c + 1], codes[4 * c + 2], codes[4 * c + 3]);
+            for (int blk = 0; blk < 2; ++blk) {
+              const uint4 v0 = src[4 * c + 2 * blk], v1 = src[4 * c + 2 * blk + 1];
+              float x[16];
+              bf16x2_to_f32(v0.x, x[0], x[1]);
+              bf16x2_to_f32(v0.y, x[2], x[3]);
+              bf16x2_to_f32(v0.z, x[4], x[5]);
+              bf16x2_to_f32(v0.w, x[6], x[7]);
+              bf16x2_to_f32(v1.x, x[8], x[9]);
+              bf16x2_to_f32(v1.y, x[10], x[11]);
+              bf16x2_to_f32(v1.z, x[12], x[13]);
+              bf16x2_to_f32(v1.w, x[14], x[15]);
+              sc[2 * c + blk] = quant_block16(x, g_row, cw[2 * blk], cw[2 * blk + 1]);
+            }
+          }
+          *reinterpret_cast<uint4*>(qrow + sw64_off(r, c)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        }
         sfa_stage[r] = make_uint2(sc[0] | (sc[1] << 8) | (sc[2] << 16) | (sc[3] << 24),
                                   sc[4] | (sc[5] << 8) | (sc[6] << 16) | (sc[7] << 24));
         qscale[r] = g_row;
@@ -332,20 +435,21 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
         // the four scales of k-step s for row 32j+i (replicated per quadrant).
         uint32_t va[8];
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
+        for (int s2 = 0; s2 < 2; ++s2)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint2 v = sfa_stage[32 * j + lane];
-            va[4 * s + j] = s ? v.y : v.x;
+            va[4 * s2 + j] = s2 ? v.y : v.x;
           }
         tmem_st8(tmem_addr(tbase, 32 * warp, kColSFA), va);
         tmem_wait_st();
       } else {
         uint8_t* qt = smem + L::kOffQ;
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          *reinterpret_cast<uint4*>(qt + (c >> 3) * 16384 + sw128_off(r, c & 7)) =
-              make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+#pragma unroll 4
+        for (int c = 0; c < 16; ++c) {
+          const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(qt + (c >> 3) * 16384 + sw128_off(r, c & 7)) = v;
+        }
         qscale[r] = 1.0f;
       }
       fence_proxy_async_smem();
@@ -358,55 +462,47 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
       const uint32_t it = it_ctr + j;
       const uint32_t st = it % L::kStages, b = it & 1u;
       if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
-      const uint8_t* stage = smem + L::kOffStage + st * kStageBytes;
+      const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
       const int valid_pages = mask_slot[st];
       const int key_base = j * kBN;
-      if (it >= 2 && !mbar_wait_warp(&bars.s_full[b], ((it >> 1) - 1u) & 1u, a.status)) return;
-      if constexpr (L::kA4Q) {
-        // K block scales -> TMEM (same replicated layout as Q's)
-        const uint8_t* ks = stage + kStageKData;
-        uint32_t vb[8];
+      if (L::kA4Q || !REPACK) {
+        if (it >= 2 && !mbar_wait_warp(&bars.s_full[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+        if constexpr (L::kA4Q) {
+          // K block scales -> TMEM (same replicated layout as Q's)
+          const uint8_t* ks = stage + kKData;
+          uint32_t vb[8];
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
+          for (int s = 0; s < 2; ++s)
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) vb[4 * s + jj] = *reinterpret_cast<const uint32_t*>(ks + (32 * jj + lane) * 8 + 4 * s);
-        tmem_st8(tmem_addr(tbase, 32 * warp, kColSFB + 8 * b), vb);
-        tmem_wait_st();
-        tc_fence_before();
-      } else {
-        // K -> BF16 (exact), K-major 128B-swizzled operand
-        uint8_t* kb = smem + L::kOffK + b * kTileBuf16;
-        const uint8_t* kd = stage;
-        const uint8_t* ks = stage + kStageKData;
+            for (int jj = 0; jj < 4; ++jj)
+              vb[4 * s + jj] = *reinterpret_cast<const uint32_t*>(ks + (32 * jj + lane) * 8 + 4 * s);
+          tmem_st8(tmem_addr(tbase, 32 * warp, kColSFB + 8 * b), vb);
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          // K -> BF16 (exact), K-major 128B-swizzled operand
+          uint8_t* kb = smem + L::kOffK + b * kTile16;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int u = tid + 128 * i;
-          const int key = u >> 2, c = u & 3;
-          const uint4 src = *reinterpret_cast<const uint4*>(kd + sw64_off(key, c));
-          const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(ks + key * 8 + 2 * c);
-          const uint32_t s0 = scale_bf16x2_x2p112(sc01 & 0xFFu), s1 = scale_bf16x2_x2p112(sc01 >> 8);
-          uint32_t o0[4], o1[4], o2[4], o3[4];
-          dequant8_bf16(src.x, s0, o0);
-          dequant8_bf16(src.y, s0, o1);
-          dequant8_bf16(src.z, s1, o2);
-          dequant8_bf16(src.w, s1, o3);
-          uint8_t* dst = kb + (c >> 1) * 16384;
-          const uint32_t cc = (c & 1) * 4;
-          *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + 0)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-          *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + 1)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-          *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + 2)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-          *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + 3)) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+          for (int i = 0; i < 4; ++i) {
+            const int u = tid + 128 * i;
+            const int key = u >> 2, c = u & 3;
+            const uint4 src = *reinterpret_cast<const uint4*>(stage + sw64_off(key, c));
+            const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(stage + kKData + key * 8 + 2 * c);
+            uint32_t o0[4], o1[4], o2[4], o3[4];
+            dequant_unit<true>(src, sc01, o0, o1, o2, o3);
+            store_unit_sw128(kb, key, c, o0, o1, o2, o3);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.sfb_full[b]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.sfb_full[b]);
-      // ---- V -> FP16, MN-major 128B-swizzled operand ---------------------------
-      if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
-      {
-        uint8_t* vb = smem + L::kOffV + b * kTileBuf16;
-        const uint8_t* vd = stage + kStageKData + kStageKScale;
-        const uint8_t* vs = vd + kStageVData;
+      if constexpr (!REPACK) {
+        // ---- V -> FP16, MN-major 128B-swizzled operand -------------------------
+        if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+        uint8_t* vb = smem + L::kOffV + b * kTile16;
+        const uint8_t* vd = stage + kKData + kKScale;
+        const uint8_t* vs = vd + kVData;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int u = tid + 128 * i;
@@ -416,42 +512,47 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
           if (live) {
             const uint4 src = *reinterpret_cast<const uint4*>(vd + key * 64 + 16 * c);
             const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(vs + key * 8 + 2 * c);
-            const uint32_t s0 = scale_f16x2(sc01 & 0xFFu), s1 = scale_f16x2(sc01 >> 8);
-            dequant8_f16(src.x, s0, o0);
-            dequant8_f16(src.y, s0, o1);
-            dequant8_f16(src.z, s1, o2);
-            dequant8_f16(src.w, s1, o3);
+            dequant_unit<false>(src, sc01, o0, o1, o2, o3);
           }
-          uint8_t* dst = vb + (c >> 1) * 16384;
-          const uint32_t cc = (c & 1) * 4;
-          *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + 0)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-          *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + 1)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-          *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + 2)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-          *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + 3)) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+          store_unit_sw128(vb, key, c, o0, o1, o2, o3);
         }
         fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.vdq_full[b]);
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars.vdq_full[b]);
-        mbar_arrive(&bars.kv_empty[st]);
-      }
+      if (lane == 0) mbar_arrive(&bars.kv_empty[st]);
     }
     it_ctr += item.n_tiles;
   }
 }
 
 // ---------------------------------------------------------------------------
-// softmax warpgroup (warps 4-7): thread = TMEM lane = row
-template <int VARIANT>
-__device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int r) {
-  using L = Layout<VARIANT>;
+// softmax warpgroups (warps 4-11): thread = TMEM lane = row; warpgroup `half`
+// owns keys 64*half .. 64*half+63 of every tile and O columns of the same range
+template <int VARIANT, bool REPACK>
+__device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int r,
+                             int half) {
+  using L = Layout<VARIANT, REPACK>;
   const int quad = r >> 5, lane = r & 31;
   const int G = a.group, lg = a.log2_group;
   const float* qscale = reinterpret_cast<const float*>(smem + L::kOffQScale);
+  float* xmax = reinterpret_cast<float*>(smem + L::kOffXmax);  // [parity][half][row]
+  float* xl = reinterpret_cast<float*>(smem + L::kOffXl);      // [half][row]
   const uint32_t lane_base = tmem_addr(tbase, 32 * quad, 0);
-  uint32_t it_ctr = 0, item_ctr = 0;
+  const uint32_t ocol = kColO + 64 * half;
+  uint32_t it_ctr = 0, item_ctr = 0, xphase = 0;
   Item item;
+  // The two halves of a row meet on xchg[quad]; every meeting is one phase.
+  auto meet = [&]() -> bool {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.xchg[quad]);
+    const bool ok = mbar_wait_warp(&bars.xchg[quad], xphase & 1u, a.status);
+    ++xphase;
+    tc_fence_after();
+    return ok;
+  };
   for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
     if (!mbar_wait_warp(bars.q_full, item_ctr & 1u, a.status)) return;
     const int tq = item.tok0 + (r >> lg);
@@ -461,86 +562,105 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
     const float c_r = (L::kA4Q ? qscale[r] : 1.0f) * a.k_g * a.sm_scale * kLog2e;
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.qs_empty);
-    float m_run = -INFINITY, l_run = 0.0f;
+    float m_run = -INFINITY;
+    float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
     for (int j = 0; j < item.n_tiles; ++j) {
       const uint32_t it = it_ctr + j;
       const uint32_t b = it & 1u;
       const uint32_t s_col = b ? kColS1 : kColS0;
       if (!mbar_wait_warp(&bars.s_full[b], (it >> 1) & 1u, a.status)) return;
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      uint32_t sr[64];
+      tmem_ld32(lane_base + s_col + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(lane_base + s_col + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_ld();
       float* s = reinterpret_cast<float*>(sr);
-      const int key0 = j * kBN;
-      // Tiles crossing the row's last visible key are scaled and masked here;
-      // all others fold the scale into the exponent's FMA.
-      const bool masked = key0 + kBN - 1 > limit;
+      const int key0 = j * kBN + 64 * half;
+      // Keys past the row's last visible one are masked (scale applied here);
+      // unmasked halves fold the scale into the exponent's FMA below.
+      const bool masked = key0 + 63 > limit;
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = (key0 + c > limit) ? -INFINITY : s[c] * c_r;
+        for (int c = 0; c < 64; ++c) s[c] = (key0 + c > limit) ? -INFINITY : s[c] * c_r;
       }
-      float mx = -INFINITY;
+      float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) mx = fmaxf(mx, fmaxf(s[c], s[c + 1]));
-      const float m_tile = masked ? mx : mx * c_r;
-      // Lazy rescale: a row moves its running max only when the tile max
-      // exceeds it by more than 2^8.  O is rescaled by the whole warp (TMEM
-      // loads/stores are warp-collective), with factor 1 for rows that keep
-      // their max.
+      for (int c = 6; c < 62; c += 4) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+      }
+      const float mx = fmax3(mx0, mx1, fmaxf(s[62], s[63]));
+      const float m_half = masked ? mx : mx * c_r;
+      float* xm = xmax + (j & 1) * 256;
+      xm[half * 128 + r] = m_half;
+      if (!meet()) return;  // both halves have read their S and published their max
+      const float m_tile = fmaxf(m_half, xm[(half ^ 1) * 128 + r]);
+      // Lazy rescale: the running max moves only when the tile max exceeds it
+      // by more than 2^8.  TMEM loads/stores are warp-collective, so the whole
+      // warp rescales its 64 O columns, with factor 1 for rows that keep
+      // their max.  Both halves take identical decisions (same m_tile).
       float alpha = 1.0f;
       const bool need = m_tile > m_run + kRescaleThreshold;
       if (need) {
         alpha = fast_exp2(m_run - m_tile);  // 0 when m_run = -inf
-        l_run *= alpha;
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lacc[i] = __fmul2_rn(lacc[i], a2);
         m_run = m_tile;
       }
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O must hold PV of the previous tile before it is rescaled
-        const uint32_t pit = it - 1u;
+        const uint32_t pit = it - 1u;  // O must hold PV of the previous tile
         if (!mbar_wait_warp(&bars.pv_done[pit & 1u], (pit >> 1) & 1u, a.status)) return;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
           uint32_t ov[32];
-          tmem_ld32(lane_base + kColO + 32 * c, ov);
+          tmem_ld32(lane_base + ocol + 32 * c, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st16(lane_base + kColO + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
-          tmem_st16(lane_base + kColO + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+          tmem_st16(lane_base + ocol + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+          tmem_st16(lane_base + ocol + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
       const float cs = masked ? 1.0f : c_r;
-      float lsum = 0.0f;
-      uint32_t pk[64];
+      const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_exp2(fmaf(s[2 * c], cs, -m_use));
-        const float p1 = fast_exp2(fmaf(s[2 * c + 1], cs, -m_use));
-        lsum += p0 + p1;
-        pk[c] = pack_f16x2(p0, p1);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int e = 32 * h2 + 2 * c;
+          const float2 t = __ffma2_rn(make_float2(s[e], s[e + 1]), cs2, nm2);
+          const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+          lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
+          pk[c] = pack_f16x2(p.x, p.y);
+        }
+        // P of keys 64*half.. goes to TMEM columns 32*half.. of the S buffer
+        // (the other half finished reading those columns before the meeting).
+        tmem_st16(lane_base + s_col + 32 * half + 16 * h2, pk);
       }
-      l_run += lsum;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_st16(lane_base + s_col + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full[b]);
     }
-    // ---- epilogue ---------------------------------------------------------------
+    // ---- epilogue: combine the halves' row sums, scale this half of O ---------
+    const float l_half = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y) + (lacc[2].x + lacc[2].y) +
+                         (lacc[3].x + lacc[3].y);
+    xl[half * 128 + r] = l_half;
+    if (!meet()) return;
+    const float l_run = l_half + xl[(half ^ 1) * 128 + r];
     if (!mbar_wait_warp(bars.o_full, item_ctr & 1u, a.status)) return;
     tc_fence_after();
     const float inv_l = (l_run > 0.0f) ? a.v_g / l_run : 0.0f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) +
-                          (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
+                          (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim + 64 * half;
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
       uint32_t ov[32];
-      tmem_ld32(lane_base + kColO + 32 * c, ov);
+      tmem_ld32(lane_base + ocol + 32 * c, ov);
       tmem_wait_ld();
       if (valid) {
         uint32_t pb[16];
@@ -556,7 +676,7 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
         dst[3] = make_uint4(pb[12], pb[13], pb[14], pb[15]);
       }
     }
-    if (valid && a.lse)
+    if (half == 0 && valid && a.lse)
       a.lse[static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq] =
           (l_run > 0.0f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
     tc_fence_before();
@@ -566,9 +686,10 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
   }
 }
 
-template <int VARIANT>
-__device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtensorMap* tmap_k) {
-  using L = Layout<VARIANT>;
+template <int VARIANT, bool REPACK>
+__device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtensorMap* tmap_k,
+                                             const CUtensorMap* tmap_ks) {
+  using L = Layout<VARIANT, REPACK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -578,25 +699,29 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   if (tid == 0) {
     for (int i = 0; i < L::kStages; ++i) {
       mbar_init(&bars.kv_full[i], 1);
-      mbar_init(&bars.kv_empty[i], 5);  // QK commit + one arrive per transform warp
+      mbar_init(&bars.kv_empty[i], 5);  // one MMA commit + one arrive per transform warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.sfb_full[i], 4);
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], 4);
+      mbar_init(&bars.p_full[i], 8);
       mbar_init(&bars.vdq_full[i], 4);
       mbar_init(&bars.pv_done[i], 1);
     }
     mbar_init(bars.o_full, 1);
-    mbar_init(bars.o_empty, 4);
+    mbar_init(bars.o_empty, 8);
     mbar_init(bars.q_full, 4);
     mbar_init(bars.q_empty, 1);
     mbar_init(bars.drain, 1);
-    mbar_init(bars.qs_empty, 4);
+    mbar_init(bars.qs_empty, 8);
     mbar_init(bars.sfa_ready, 4);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.xchg[i], 2);
     fence_barrier_init();
   }
-  if (warp == kProducerWarp && lane == 0) prefetch_tmap(tmap_k);
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(tmap_k);
+    prefetch_tmap(tmap_ks);
+  }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -607,14 +732,14 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   const uint32_t tbase = *tmem_slot;
 
   if (warp < 4) {
-    transform_loop<VARIANT>(a, smem, bars, tbase, tid);
-  } else if (warp < 8) {
-    softmax_loop<VARIANT>(a, smem, bars, tbase, tid - 128);
+    transform_loop<VARIANT, REPACK>(a, smem, bars, tbase, tid);
+  } else if (warp < 12) {
+    softmax_loop<VARIANT, REPACK>(a, smem, bars, tbase, (tid - 128) & 127, (tid - 128) >> 7);
   } else if (warp == kProducerWarp) {
-    producer_loop<VARIANT>(a, tmap_k, smem, bars, lane);
-  } else {
+    producer_loop<VARIANT, REPACK>(a, tmap_k, tmap_ks, smem, bars, lane);
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      mma_loop<VARIANT>(a, smem, bars, tbase);
+      mma_loop<VARIANT, REPACK>(a, smem, bars, tbase);
       // drain: every MMA issued by this thread has finished before TMEM is freed
       tc_commit(bars.drain);
     }
@@ -630,53 +755,155 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   }
 }
 
+// Kernel names carry the variant and the V path, so a trace shows which ran.
 __global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_prefill_a4q_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k) {
-  prefill_body<0>(a, &tmap_k);
+    nvfp4_prefill_a4q_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                                   const __grid_constant__ CUtensorMap tmap_ks) {
+  prefill_body<0, false>(a, &tmap_k, &tmap_ks);
 }
-
 __global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_prefill_dqahead_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k) {
-  prefill_body<1>(a, &tmap_k);
+    nvfp4_prefill_a4q_vrepack_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                                           const __grid_constant__ CUtensorMap tmap_ks) {
+  prefill_body<0, true>(a, &tmap_k, &tmap_ks);
+}
+__global__ void __launch_bounds__(kThreads, 1)
+    nvfp4_prefill_dqahead_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                                       const __grid_constant__ CUtensorMap tmap_ks) {
+  prefill_body<1, false>(a, &tmap_k, &tmap_ks);
+}
+__global__ void __launch_bounds__(kThreads, 1)
+    nvfp4_prefill_dqahead_repack_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                                              const __grid_constant__ CUtensorMap tmap_ks) {
+  prefill_body<1, true>(a, &tmap_k, &tmap_ks);
 }
 
 // ---------------------------------------------------------------------------
-// schedule: items (request, q tile, kv head) sorted by decreasing KV-tile count
+// repack pre-pass: each (request, kv head, KV tile) once -> 32 KB FP16 V tile
+// (and a BF16 K tile for the dequant-ahead variant) in the exact operand
+// layout the attention kernel's MMAs read; keys past kv_len are zeros.
+__global__ void __launch_bounds__(128) nvfp4_prefill_repack_kernel(PrefillArgs a, int with_k) {
+  const int tid = threadIdx.x;
+  const int total = a.work[1];
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    int lo = 0, hi = a.batch - 1;  // last b with tile_prefix[b] * Hkv <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.tile_prefix[mid] * a.num_kv_heads <= t) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int n_t = a.tile_prefix[b + 1] - a.tile_prefix[b];
+    const int r = t - a.tile_prefix[b] * a.num_kv_heads;
+    const int h = r / n_t, j = r - h * n_t;
+    const int kv_len = a.kv_lens[b];
+    for (int tensor = with_k ? 0 : 1; tensor < 2; ++tensor) {
+      const uint8_t* data = tensor ? a.v_data : a.k_data;
+      const uint8_t* scl = tensor ? a.v_scale : a.k_scale;
+      uint8_t* dst = (tensor ? a.repack_v : a.repack_k) + static_cast<int64_t>(t) * kTile16;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int u = tid + 128 * i;
+        const int key = u >> 2, c = u & 3;
+        const int abs_key = j * kBN + key;
+        uint32_t o0[4] = {0, 0, 0, 0}, o1[4] = {0, 0, 0, 0}, o2[4] = {0, 0, 0, 0}, o3[4] = {0, 0, 0, 0};
+        if (abs_key < kv_len) {
+          const int pid = a.page_table[static_cast<int64_t>(b) * a.max_pages + (abs_key >> 4)];
+          if (pid >= 0 && pid < a.num_pages) {
+            const int64_t row = (static_cast<int64_t>(pid) * a.num_kv_heads + h) * kPageSize + (abs_key & 15);
+            const uint4 src = *reinterpret_cast<const uint4*>(data + row * 64 + 16 * c);
+            const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(scl + row * 8 + 2 * c);
+            if (tensor) dequant_unit<false>(src, sc01, o0, o1, o2, o3);
+            else dequant_unit<true>(src, sc01, o0, o1, o2, o3);
+          } else {
+            set_status(a.status, kDevBadPage);
+          }
+        }
+        uint8_t* d = dst + (c >> 1) * 16384;
+        const uint32_t cc = (c & 1) * 4;
+        *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 0)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+        *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 1)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 2)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+        *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 3)) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// schedule: items (request, q tile, kv head) sorted by decreasing KV-tile
+// count, and the per-request KV-tile prefix used by repack mode
 constexpr int kMaxCostBins = 4096;
+
+// Inclusive prefix sum over the 1024 threads of the block.
+__device__ __forceinline__ int block_inclusive_scan(int v, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_sums[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int r = v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  __syncthreads();
+  return r;
+}
 
 __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
   __shared__ int hist[kMaxCostBins];
-  __shared__ int s_total;
+  __shared__ int warp_sums[32];
   const int tid = threadIdx.x;
-  int* prefix = a.work + 4 + 2 * a.max_items;  // [batch + 1] unit prefix (scratch)
+  int* prefix = a.work + 4 + 2 * a.max_items;  // [batch + 1] unit prefix
+  int* tprefix = prefix + a.batch + 1;         // [batch + 1] KV-tile prefix
   const int tpq_shift = 7 - a.log2_group;      // log2(tokens per q tile)
   for (int i = tid; i < kMaxCostBins; i += blockDim.x) hist[i] = 0;
-  if (tid == 0) {
-    int total = 0;
-    for (int b = 0; b < a.batch; ++b) {
-      prefix[b] = total;
+  // 1) units per request (q tiles x kv heads), KV tiles per request, prefixes
+  int carry = 0, tcarry = 0;
+  for (int base = 0; base < a.batch; base += blockDim.x) {
+    const int b = base + tid;
+    int cnt = 0, tiles = 0;
+    if (b < a.batch) {
       const int q0 = a.qo_indptr[b], q1 = a.qo_indptr[b + 1];
       const int q_len = q1 - q0, kv_len = a.kv_lens[b];
-      bool bad = q_len < 0 || q0 < 0 || q1 > a.total_q || kv_len < 0 ||
-                 kv_len > a.max_pages * kPageSize || (a.causal && q_len > kv_len);
+      const bool bad = q_len < 0 || q0 < 0 || q1 > a.total_q || kv_len < 0 ||
+                       kv_len > a.max_pages * kPageSize || (a.causal && q_len > kv_len);
       if (bad) {
         set_status(a.status, kDevBadShape);
-        continue;
+      } else if (q_len > 0) {
+        cnt = ((q_len + (1 << tpq_shift) - 1) >> tpq_shift) * a.num_kv_heads;
+        tiles = max(1, (kv_len + kBN - 1) / kBN);
       }
-      const int n_qt = (q_len + (1 << tpq_shift) - 1) >> tpq_shift;
-      const int add = n_qt * a.num_kv_heads;
-      if (total + add > a.max_items) {
-        set_status(a.status, kDevBadShape);
-        continue;
-      }
-      total += add;
     }
+    const int incl = block_inclusive_scan(cnt, warp_sums);
+    if (b < a.batch) prefix[b] = carry + incl - cnt;
+    carry += warp_sums[31];  // block total of this chunk
+    __syncthreads();
+    const int tincl = block_inclusive_scan(tiles, warp_sums);
+    if (b < a.batch) tprefix[b] = tcarry + tincl - tiles;
+    tcarry += warp_sums[31];
+    __syncthreads();
+  }
+  int total = carry;
+  if (total > a.max_items) {  // cannot happen when qo_indptr is non-decreasing
+    set_status(a.status, kDevBadShape);
+    total = a.max_items;
+  }
+  if (tid == 0) {
     prefix[a.batch] = total;
-    s_total = total;
+    tprefix[a.batch] = tcarry;
     a.work[0] = total;
+    a.work[1] = tcarry * a.num_kv_heads;
   }
   __syncthreads();
-  const int total = s_total;
   auto cost_of = [&](int u, int& b, int& qt, int& kvh) -> int {
     int lo = 0, hi = a.batch - 1;  // last b with prefix[b] <= u
     while (lo < hi) {
@@ -693,20 +920,28 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
     const int last_key = a.causal ? kv_len - q_len + tok0 + n_tok - 1 : kv_len - 1;
     return min(last_key / kBN + 1, kMaxCostBins - 1);
   };
+  // 2) histogram of costs
   for (int u = tid; u < total; u += blockDim.x) {
     int b, qt, kvh;
     atomicAdd(&hist[cost_of(u, b, qt, kvh)], 1);
   }
   __syncthreads();
-  if (tid == 0) {  // exclusive offsets, largest cost first
-    int run = 0;
-    for (int c = kMaxCostBins - 1; c >= 0; --c) {
-      const int n = hist[c];
-      hist[c] = run;
-      run += n;
-    }
+  // 3) exclusive offsets, largest cost first: thread t owns 4 bins from the top
+  constexpr int kPer = kMaxCostBins / 1024;
+  int v[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    v[i] = hist[kMaxCostBins - 1 - (tid * kPer + i)];
+    sum += v[i];
+  }
+  int run = block_inclusive_scan(sum, warp_sums) - sum;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    hist[kMaxCostBins - 1 - (tid * kPer + i)] = run;
+    run += v[i];
   }
   __syncthreads();
+  // 4) scatter the items
   int2* items = reinterpret_cast<int2*>(a.work + 4);
   for (int u = tid; u < total; u += blockDim.x) {
     int b, qt, kvh;
@@ -716,27 +951,34 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
   }
 }
 
+template <typename K>
+cudaError_t launch_main(K kernel, uint32_t smem, const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmks,
+                        int num_sms, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<num_sms, kThreads, smem, s>>>(a, tmk, tmks);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-size_t prefill_smem_bytes(int variant) { return variant == 0 ? Layout<0>::kAlloc : Layout<1>::kAlloc; }
-
-cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, const CUtensorMap& tmap_k, int variant,
-                           int num_sms, cudaStream_t s) {
+cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, const CUtensorMap& tmap_k,
+                           const CUtensorMap& tmap_ks, int variant, bool repack, int num_sms, cudaStream_t s) {
   nvfp4_prefill_plan_kernel<<<1, 1024, 0, s>>>(plan);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (variant == 0) {
-    e = cudaFuncSetAttribute(nvfp4_prefill_a4q_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<0>::kAlloc);
+  if (repack) {
+    nvfp4_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a, variant == 1 ? 1 : 0);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    nvfp4_prefill_a4q_sm103_kernel<<<num_sms, kThreads, Layout<0>::kAlloc, s>>>(a, tmap_k);
-  } else {
-    e = cudaFuncSetAttribute(nvfp4_prefill_dqahead_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<1>::kAlloc);
-    if (e != cudaSuccess) return e;
-    nvfp4_prefill_dqahead_sm103_kernel<<<num_sms, kThreads, Layout<1>::kAlloc, s>>>(a, tmap_k);
   }
-  return cudaGetLastError();
+  if (variant == 0)
+    return repack ? launch_main(nvfp4_prefill_a4q_vrepack_sm103_kernel, Layout<0, true>::kAlloc, a, tmap_k, tmap_ks,
+                                num_sms, s)
+                  : launch_main(nvfp4_prefill_a4q_sm103_kernel, Layout<0, false>::kAlloc, a, tmap_k, tmap_ks, num_sms, s);
+  return repack ? launch_main(nvfp4_prefill_dqahead_repack_sm103_kernel, Layout<1, true>::kAlloc, a, tmap_k, tmap_ks,
+                              num_sms, s)
+                : launch_main(nvfp4_prefill_dqahead_sm103_kernel, Layout<1, false>::kAlloc, a, tmap_k, tmap_ks, num_sms, s);
 }
 
 }  // namespace nvfp4kv

@@ -61,16 +61,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Default limit of one wait: 2 s of wall time.  A healthy pipeline never waits
 // longer than one kernel's runtime.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Each try_wait may suspend the thread for up to this long; the hardware wakes
+// it as soon as the phase completes, so a waiting warp does not spin on the
+// issue slots that the working warps need.
+constexpr uint32_t kSuspendHintNs = 1000000u;
+
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 
 // Bounded wait on the phase with parity `parity`.  Returns false (and sets
 // kDevTimeout) if the phase did not complete within `limit_ns`.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  const uint32_t hint = limit_ns < kSuspendHintNs ? static_cast<uint32_t>(limit_ns) : kSuspendHintNs;
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, hint)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
       set_status(status, kDevTimeout);
       return false;
     }

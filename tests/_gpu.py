@@ -90,12 +90,23 @@ def compare_lse(got_lse, ref, qo_indptr):
     return err
 
 
-def run_prefill(inp, cache, variant, causal=True, with_lse=True):
+def prefill_workspace(inp, mode):
+    """mode "auto": room for repack mode (used when the batch qualifies);
+    "inkernel": the schedule only, so V is dequantized inside the kernel."""
+    b = nk()
+    wl = inp.wl
+    max_kv = inp.page_table.shape[1] * 16 if mode == "auto" else 0
+    n = b.nvfp4_workspace_bytes(b.OP_PREFILL, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.total_q, max_kv)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=dev())
+
+
+def run_prefill(inp, cache, variant, causal=True, with_lse=True, mode="auto"):
     b = nk()
     q = inp.q.to(dev())
     lse = torch.full((inp.wl.total_q, inp.wl.num_q_heads), float("nan"), device=dev()) if with_lse else None
     o = b.nvfp4_paged_prefill(q, cache, inp.page_table.to(dev()), inp.kv_lens.to(dev()), inp.qo_indptr.to(dev()),
-                              causal=causal, sm_scale=inp.sm_scale, variant=variant, lse=lse)
+                              causal=causal, sm_scale=inp.sm_scale, variant=variant, lse=lse,
+                              workspace=prefill_workspace(inp, mode))
     torch.cuda.synchronize()
     status = b.nvfp4kv_get_device_status()
     return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None), status

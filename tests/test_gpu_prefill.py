@@ -17,8 +17,8 @@ pytestmark = pytest.mark.gpu
 VARIANTS = [(0, "a4q"), (1, "bf16")]
 
 
-def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None):
-    got, lse, status = G.run_prefill(inp, cache, variant, causal=causal)
+def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None, mode="auto"):
+    got, lse, status = G.run_prefill(inp, cache, variant, causal=causal, mode=mode)
     assert status == 0
     ref = G.oracle_prefill(pools, inp, q_mode, causal=causal, rows=rows)
     mx, fro, n = G.compare_rows(got, ref, inp.qo_indptr)
@@ -28,12 +28,15 @@ def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None):
     return got, ref
 
 
+@pytest.mark.parametrize("mode", ["auto", "inkernel"])
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 @pytest.mark.parametrize("cfg", ["tiny", "small_ragged"])
-def test_prefill_full_parity(cfg, variant, q_mode):
+def test_prefill_full_parity(cfg, variant, q_mode, mode):
+    """Every row; "auto" runs the repack pre-pass (these batches average two
+    or more q tiles per kv head), "inkernel" dequantizes V in the kernel."""
     inp = G.inputs(cfg)
     cache = G.gpu_cache(inp)
-    _check(inp, cache, G.pools_for(cfg), variant, q_mode)
+    _check(inp, cache, G.pools_for(cfg), variant, q_mode, mode=mode)
 
 
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
@@ -58,14 +61,15 @@ def test_prefill_zero_length_and_edge_rows(variant, q_mode):
     _check(inp, cache, G.oracle_pools(inp), variant, q_mode)
 
 
+@pytest.mark.parametrize("mode", ["auto", "inkernel"])
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
-def test_prefill_shortq_longkv(variant, q_mode):
+def test_prefill_shortq_longkv(variant, q_mode, mode):
     """batch 4, q 128 at the end of kv 2048, 32/8 heads, permuted pages: all
     rows of request 0, sampled rows of the others."""
     inp = G.inputs("shortq")
     cache = G.gpu_cache(inp)
     rows = [(0, i) for i in range(128)] + [r for r in W.sample_rows(inp.wl, 6) if r[0] != 0]
-    _check(inp, cache, G.pools_for("shortq"), variant, q_mode, rows=rows)
+    _check(inp, cache, G.pools_for("shortq"), variant, q_mode, rows=rows, mode=mode)
 
 
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
@@ -77,14 +81,15 @@ def test_prefill_tails(variant, q_mode):
     _check(inp, cache, G.pools_for("tails"), variant, q_mode, rows=rows)
 
 
+@pytest.mark.parametrize("mode", ["auto", "inkernel"])
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
-def test_prefill_full_16k_sampled(variant, q_mode):
+def test_prefill_full_16k_sampled(variant, q_mode, mode):
     """The 16K causal configuration at full size, as the benchmark runs it
     (cache built by the CUDA append in shuffled order); sampled rows."""
     inp = G.inputs("prefill16k")
     cache = G.gpu_cache(inp, append_order=W.shuffled_append_order(inp.wl.total_kv))
     rows = W.sample_rows(inp.wl, 14)
-    _check(inp, cache, G.pools_for("prefill16k"), variant, q_mode, rows=rows)
+    _check(inp, cache, G.pools_for("prefill16k"), variant, q_mode, rows=rows, mode=mode)
 
 
 def test_prefill_long_ragged_sampled():
