@@ -12,13 +12,13 @@
 //                   pages + scales (in-kernel mode) or as one 32 KB FP16 tile
 //                   prepared once per (request, kv head, tile) by the repack
 //                   pre-pass (repack mode)
-//   transform WG    A4Q: K block scales -> TMEM (UE4M3 scale operand of the
-//                   block-scaled MMA).  In-kernel mode also: V -> FP16 in the
-//                   MMA's MN-major layout (exact), and for the dequant-ahead
-//                   variant K -> BF16.  At each item start: Q tile -> NVFP4
-//                   (per-row dual level scale) + Q block scales -> TMEM (A4Q),
-//                   or Q -> shared memory as BF16 (dequant-ahead).
-//   MMA warp        S = Q K^T: tcgen05 kind::mxf4nvf4 (scale_vec 4X, UE4M3),
+//   transform WG    At each item start: Q tile -> NVFP4 (per-row dual level
+//                   scale) + Q block scales -> TMEM (A4Q), or Q -> shared
+//                   memory as BF16 (dequant-ahead).  In-kernel mode, per KV
+//                   tile: V -> FP16 in the MMA's MN-major layout (exact), and
+//                   for the dequant-ahead variant K -> BF16.
+//   MMA warp        K block scales -> scale-factor atoms -> TMEM (tcgen05.cp);
+//                   S = Q K^T: tcgen05 kind::mxf4nvf4 (scale_vec 4X, UE4M3),
 //                   or kind::f16 BF16 (dequant-ahead); fp32 S in TMEM, double
 //                   buffered.  O += P V: kind::f16 with P read from TMEM.
 //   softmax WGs     two warpgroups, one TMEM lane (= one row) per thread, each
@@ -42,7 +42,9 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
+// log2 units: a row's running max moves (and O is rescaled) only when a tile
+// exceeds it by more than this, so P stays <= 2^15, inside FP16's range.
+constexpr float kRescaleThreshold = 15.0f;
 
 // warps 0-3 transform, 4-7 softmax half 0, 8-11 softmax half 1,
 // 12 producer, 13 MMA, 14-15 idle (they complete the fourth warpgroup)
@@ -76,7 +78,8 @@ struct Layout {
   static constexpr uint32_t kOffSmall = kOffK + ((!REPACK && !kA4Q) ? 2 * kTile16 : 0u);
   static constexpr uint32_t kOffQScale = kOffSmall;            // 128 floats
   static constexpr uint32_t kOffSfaStage = kOffQScale + 512;   // 128 x 8 B
-  static constexpr uint32_t kOffMask = kOffSfaStage + 1024;    // per-stage page mask
+  static constexpr uint32_t kOffSfbAtoms = kOffSfaStage + 1024; // [2 buffers][2 k-steps][512 B] K scale atoms
+  static constexpr uint32_t kOffMask = kOffSfbAtoms + 2048;    // per-stage page mask
   static constexpr uint32_t kOffXmax = kOffMask + 64;          // [2 parity][2 half][128] row maxima
   static constexpr uint32_t kOffXl = kOffXmax + 2048;          // [2 half][128] row sums
   static constexpr uint32_t kOffBar = kOffXl + 1024;
@@ -91,7 +94,7 @@ struct Layout {
 struct Bars {
   uint64_t* kv_full;   // [4]
   uint64_t* kv_empty;  // [4]
-  uint64_t* sfb_full;  // [2] (A4Q: K scales in TMEM; in-kernel dequant-ahead: K tile in BF16)
+  uint64_t* sfb_full;  // [2] in-kernel dequant-ahead: K tile in BF16
   uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
   uint64_t* vdq_full;  // [2] in-kernel mode: V tile in FP16
@@ -289,69 +292,104 @@ __device__ void producer_loop(const PrefillArgs& a, const CUtensorMap* tmap_k, c
 }
 
 // ---------------------------------------------------------------------------
-// MMA warp (lane 0 only)
+// MMA warp: all 32 lanes wait and (A4Q) rearrange the tile's K block scales
+// into the scale-factor atom the block-scaled MMA reads (row n of the 128-row
+// atom at byte (n%32)*16 + (n/32)*4, four 16-value blocks per word); lane 0
+// copies the atoms into TMEM with tcgen05.cp and issues every MMA.  The copy
+// and the MMAs are tcgen05 operations of one thread and run in issue order.
 template <int VARIANT, bool REPACK>
-__device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase) {
+__device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int lane) {
   using L = Layout<VARIANT, REPACK>;
   const uint32_t q_s = smem_u32(smem + L::kOffQ);
   const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   const uint32_t idesc_qk = L::kA4Q ? idesc_mxf4nvf4(128, 128) : idesc_f16(128, 128, 1, 1, 0, 0);
+  uint8_t* atoms = smem + L::kOffSfbAtoms;
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
   auto do_pv = [&](uint32_t it, bool first) -> bool {
     const uint32_t b = it & 1u, ph = (it >> 1) & 1u;
-    if (!mbar_wait(&bars.p_full[b], ph, a.status)) return false;
-    if (!REPACK && !mbar_wait(&bars.vdq_full[b], ph, a.status)) return false;
-    if (first && !mbar_wait(bars.o_empty, (item_ctr & 1u) ^ 1u, a.status)) return false;
+    if (!mbar_wait_warp(&bars.p_full[b], ph, a.status)) return false;
+    if (!REPACK && !mbar_wait_warp(&bars.vdq_full[b], ph, a.status)) return false;
+    if (first && !mbar_wait_warp(bars.o_empty, (item_ctr & 1u) ^ 1u, a.status)) return false;
     tc_fence_after();
-    const uint32_t st = it % L::kStages;
-    const uint32_t v_s = REPACK ? smem_u32(smem + L::kOffStage + st * L::kStageBytes + L::kStageV)
-                                : smem_u32(smem + L::kOffV + b * kTile16);
-    const uint32_t s_col = b ? kColS1 : kColS0;
+    if (lane == 0) {
+      const uint32_t st = it % L::kStages;
+      const uint32_t v_s = REPACK ? smem_u32(smem + L::kOffStage + st * L::kStageBytes + L::kStageV)
+                                  : smem_u32(smem + L::kOffV + b * kTile16);
+      const uint32_t s_col = b ? kColS1 : kColS0;
 #pragma unroll
-    for (uint32_t k = 0; k < 8; ++k) {
-      mma_f16_ts(tbase + kColO, tbase + s_col + 8 * k, smem_desc(v_s + k * 2048, 16384, 1024, kSwz128), idesc_pv,
-                 (first && k == 0) ? 0u : 1u);
+      for (uint32_t k = 0; k < 8; ++k) {
+        mma_f16_ts(tbase + kColO, tbase + s_col + 8 * k, smem_desc(v_s + k * 2048, 16384, 1024, kSwz128), idesc_pv,
+                   (first && k == 0) ? 0u : 1u);
+      }
+      tc_commit(&bars.pv_done[b]);
+      if (REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's V tile has been read
     }
-    tc_commit(&bars.pv_done[b]);
-    if (REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's V tile has been read
+    __syncwarp();
     return true;
   };
   for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
-    if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
+    if (!mbar_wait_warp(bars.q_full, item_ctr & 1u, a.status)) return;
     tc_fence_after();
     for (int j = 0; j < item.n_tiles; ++j) {
       const uint32_t it = it_ctr + j;
       const uint32_t st = it % L::kStages, b = it & 1u;
-      if (!mbar_wait(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
-      if ((L::kA4Q || !REPACK) && !mbar_wait(&bars.sfb_full[b], (it >> 1) & 1u, a.status)) return;
-      if (it >= 2 && !mbar_wait(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
-      tc_fence_after();
-      const uint32_t s_col = b ? kColS1 : kColS0;
-      const uint32_t stage_s = smem_u32(smem + L::kOffStage + st * L::kStageBytes);
+      if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
+      const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
       if constexpr (L::kA4Q) {
+        // Atom buffer b was last read by the scale copy of tile it-2; that
+        // copy precedes QK(it-2), whose S the softmax had consumed before
+        // p_full(it-2), already waited on.
+        const uint8_t* ks = stage + kKData;  // [128 tokens][8 scale bytes]
+        uint8_t* at = atoms + b * 1024;
+        uint32_t w0[4], w1[4];
 #pragma unroll
-        for (uint32_t s = 0; s < 2; ++s) {
-          mma_nvf4_ss(tbase + s_col, smem_desc(q_s + 32 * s, 16, 512, kSwz64),
-                      smem_desc(stage_s + 32 * s, 16, 512, kSwz64), idesc_qk, tbase + kColSFA + 4 * s,
-                      tbase + kColSFB + 8 * b + 4 * s, s > 0 ? 1u : 0u);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint2 v = *reinterpret_cast<const uint2*>(ks + (lane + 32 * q4) * 8);
+          w0[q4] = v.x;
+          w1[q4] = v.y;
         }
-      } else {
-        const uint32_t k_s = REPACK ? stage_s : smem_u32(smem + L::kOffK + b * kTile16);
-#pragma unroll
-        for (uint32_t k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ss(tbase + s_col, smem_desc(q_s + off, 16, 1024, kSwz128), smem_desc(k_s + off, 16, 1024, kSwz128),
-                     idesc_qk, k > 0 ? 1u : 0u);
-        }
+        *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        *reinterpret_cast<uint4*>(at + 512 + lane * 16) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+      } else if constexpr (!REPACK) {
+        if (!mbar_wait_warp(&bars.sfb_full[b], (it >> 1) & 1u, a.status)) return;
       }
-      tc_commit(&bars.s_full[b]);
-      if (!REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's K has been read
-      if (j == item.n_tiles - 1) tc_commit(bars.q_empty);
+      if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t s_col = b ? kColS1 : kColS0;
+        const uint32_t stage_s = smem_u32(stage);
+        if constexpr (L::kA4Q) {
+          const uint32_t at_s = smem_u32(atoms + b * 1024);
+          tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b, smem_desc(at_s, 0, 128, kSwzNone));
+          tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b + 4, smem_desc(at_s + 512, 0, 128, kSwzNone));
+#pragma unroll
+          for (uint32_t s = 0; s < 2; ++s) {
+            mma_nvf4_ss(tbase + s_col, smem_desc(q_s + 32 * s, 16, 512, kSwz64),
+                        smem_desc(stage_s + 32 * s, 16, 512, kSwz64), idesc_qk, tbase + kColSFA + 4 * s,
+                        tbase + kColSFB + 8 * b + 4 * s, s > 0 ? 1u : 0u);
+          }
+        } else {
+          const uint32_t k_s = REPACK ? stage_s : smem_u32(smem + L::kOffK + b * kTile16);
+#pragma unroll
+          for (uint32_t k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+            mma_f16_ss(tbase + s_col, smem_desc(q_s + off, 16, 1024, kSwz128),
+                       smem_desc(k_s + off, 16, 1024, kSwz128), idesc_qk, k > 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(&bars.s_full[b]);
+        if (!REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's K has been read
+        if (j == item.n_tiles - 1) tc_commit(bars.q_empty);
+      }
+      __syncwarp();
       if (j >= 1 && !do_pv(it - 1, j == 1)) return;
     }
     if (!do_pv(it_ctr + item.n_tiles - 1, item.n_tiles == 1)) return;
-    tc_commit(bars.o_full);
+    if (lane == 0) tc_commit(bars.o_full);
+    __syncwarp();
     it_ctr += item.n_tiles;
   }
 }
@@ -457,30 +495,19 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.q_full);
     }
-    // ---- KV tiles ------------------------------------------------------------
-    for (int j = 0; j < item.n_tiles; ++j) {
-      const uint32_t it = it_ctr + j;
-      const uint32_t st = it % L::kStages, b = it & 1u;
-      if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
-      const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
-      const int valid_pages = mask_slot[st];
-      const int key_base = j * kBN;
-      if (L::kA4Q || !REPACK) {
-        if (it >= 2 && !mbar_wait_warp(&bars.s_full[b], ((it >> 1) - 1u) & 1u, a.status)) return;
-        if constexpr (L::kA4Q) {
-          // K block scales -> TMEM (same replicated layout as Q's)
-          const uint8_t* ks = stage + kKData;
-          uint32_t vb[8];
-#pragma unroll
-          for (int s = 0; s < 2; ++s)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-              vb[4 * s + jj] = *reinterpret_cast<const uint32_t*>(ks + (32 * jj + lane) * 8 + 4 * s);
-          tmem_st8(tmem_addr(tbase, 32 * warp, kColSFB + 8 * b), vb);
-          tmem_wait_st();
-          tc_fence_before();
-        } else {
-          // K -> BF16 (exact), K-major 128B-swizzled operand
+    // ---- KV tiles (in-kernel mode: dequantize V, and K for dequant-ahead) ----
+    if constexpr (!REPACK) {
+      for (int j = 0; j < item.n_tiles; ++j) {
+        const uint32_t it = it_ctr + j;
+        const uint32_t st = it % L::kStages, b = it & 1u;
+        if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
+        const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
+        const int valid_pages = mask_slot[st];
+        const int key_base = j * kBN;
+        if constexpr (!L::kA4Q) {
+          // K -> BF16 (exact), K-major 128B-swizzled operand; buffer b was
+          // read by QK(it-2)
+          if (it >= 2 && !mbar_wait_warp(&bars.s_full[b], ((it >> 1) - 1u) & 1u, a.status)) return;
           uint8_t* kb = smem + L::kOffK + b * kTile16;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -493,12 +520,10 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
             store_unit_sw128(kb, key, c, o0, o1, o2, o3);
           }
           fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.sfb_full[b]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.sfb_full[b]);
-      }
-      if constexpr (!REPACK) {
-        // ---- V -> FP16, MN-major 128B-swizzled operand -------------------------
+        // ---- V -> FP16, MN-major 128B-swizzled operand; buffer b was read by PV(it-2)
         if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
         uint8_t* vb = smem + L::kOffV + b * kTile16;
         const uint8_t* vd = stage + kKData + kKScale;
@@ -518,10 +543,11 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.vdq_full[b]);
+        if (lane == 0) {
+          mbar_arrive(&bars.vdq_full[b]);
+          mbar_arrive(&bars.kv_empty[st]);
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.kv_empty[st]);
     }
     it_ctr += item.n_tiles;
   }
@@ -699,7 +725,9 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   if (tid == 0) {
     for (int i = 0; i < L::kStages; ++i) {
       mbar_init(&bars.kv_full[i], 1);
-      mbar_init(&bars.kv_empty[i], 5);  // one MMA commit + one arrive per transform warp
+      // one MMA commit, plus one arrive per transform warp when the transform
+      // warpgroup reads the stage (in-kernel mode)
+      mbar_init(&bars.kv_empty[i], REPACK ? 1 : 5);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.sfb_full[i], 4);
@@ -738,11 +766,9 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   } else if (warp == kProducerWarp) {
     producer_loop<VARIANT, REPACK>(a, tmap_k, tmap_ks, smem, bars, lane);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      mma_loop<VARIANT, REPACK>(a, smem, bars, tbase);
-      // drain: every MMA issued by this thread has finished before TMEM is freed
-      tc_commit(bars.drain);
-    }
+    mma_loop<VARIANT, REPACK>(a, smem, bars, tbase, lane);
+    // drain: every MMA issued by lane 0 has finished before TMEM is freed
+    if (lane == 0) tc_commit(bars.drain);
     __syncwarp();
   }
   tc_fence_before();
