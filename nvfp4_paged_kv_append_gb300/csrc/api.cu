@@ -1,8 +1,7 @@
 // C ABI of libnvfp4kv.so: argument validation on the host, the device status
-// word, TMA descriptors for the K pools, and kernel launches.  No entry point
+// word, and kernel launches.  No entry point
 // allocates device memory; nothing throws across the boundary.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -33,7 +32,6 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Per-device set-up on first use (device current): capability check, SM
 // count, status word address.
@@ -64,18 +62,6 @@ int device_state(DeviceState** out) {
   return d.rc;
 }
 
-int get_encoder() {
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_encode) return NVFP4KV_OK;
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || fn == nullptr)
-    return NVFP4KV_ERR_CUDA;
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  return NVFP4KV_OK;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool finite_pos(float x) { return std::isfinite(x) && x > 0.0f; }
 
@@ -104,9 +90,9 @@ int64_t prefill_max_items(int64_t total_q, int batch, int num_q_heads, int num_k
 }
 
 // Prefill workspace: [16 B header][items: 8 B each][unit prefix][tile prefix]
-// padded to 1 KB, then (repack mode) V tiles and K tiles of 32 KB each for
-// every (request, kv head, KV tile) the batch can hold.
-constexpr size_t kRepackTileBytes = 32768;
+// padded to 1 KB, then (repack mode) one record of up to 64 KB for every
+// (request, kv head, KV tile) the batch can hold.
+constexpr size_t kRepackRecordBytes = 65536;
 size_t prefill_sched_bytes(int64_t max_items, int batch) {
   const size_t b = 16 + 8 * static_cast<size_t>(max_items) + 8 * (static_cast<size_t>(batch) + 1);
   return (b + 1023) & ~size_t(1023);
@@ -145,7 +131,7 @@ size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int
     if (total_q < 0) return 0;
     const int64_t items = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
     return prefill_sched_bytes(items, batch) +
-           2 * kRepackTileBytes * prefill_repack_tiles(batch, num_kv_heads, max_kv_len);
+           kRepackRecordBytes * prefill_repack_tiles(batch, num_kv_heads, max_kv_len);
   }
   if (op == NVFP4KV_OP_DECODE) {
     if (max_kv_len < 0) return 0;
@@ -215,28 +201,9 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
   // table allows and requests average at least two q tiles per kv head.
   const size_t rtiles = prefill_repack_tiles(batch, cache->num_kv_heads, static_cast<int64_t>(max_pages_per_req) * kPageSize);
   const int64_t qtiles = (total_q * (num_q_heads / cache->num_kv_heads) + kBM - 1) / kBM;
-  const bool repack = workspace_bytes >= sched + 2 * kRepackTileBytes * rtiles && qtiles >= 2 * static_cast<int64_t>(batch);
+  const bool repack = workspace_bytes >= sched + kRepackRecordBytes * rtiles && qtiles >= 2 * static_cast<int64_t>(batch);
   DeviceState* d = nullptr;
   if ((rc = device_state(&d))) return rc;
-  if ((rc = get_encoder())) return rc;
-
-  CUtensorMap tmap, tmap_s;
-  const cuuint64_t rows = static_cast<cuuint64_t>(cache->num_pages) * cache->num_kv_heads;
-  const cuuint64_t dims[2] = {64, rows * kPageSize};
-  const cuuint64_t strides[1] = {64};
-  const cuuint32_t box[2] = {64, kPageSize};
-  const cuuint32_t estr[2] = {1, 1};
-  if (g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, cache->k_data, dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return NVFP4KV_ERR_CUDA;
-  const cuuint64_t dims_s[2] = {128, rows};  // one 128-byte scale page per (page, kv head)
-  const cuuint64_t strides_s[1] = {128};
-  const cuuint32_t box_s[2] = {128, 1};
-  if (g_encode(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, cache->k_scale, dims_s, strides_s, box_s, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return NVFP4KV_ERR_CUDA;
 
   PlanArgs plan;
   plan.kv_lens = kv_lens;
@@ -276,12 +243,9 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
   a.lse = lse;
   a.work = static_cast<const int*>(workspace);
   a.tile_prefix = static_cast<const int*>(workspace) + 4 + 2 * max_items + (batch + 1);
-  uint8_t* rbase = static_cast<uint8_t*>(workspace) + sched;
-  a.repack_v = repack ? rbase : nullptr;
-  a.repack_k = repack ? rbase + kRepackTileBytes * rtiles : nullptr;
+  a.repack = repack ? static_cast<uint8_t*>(workspace) + sched : nullptr;
   a.status = d->status;
-  return launch_rc(
-      launch_prefill(a, plan, tmap, tmap_s, variant, repack, d->num_sms, static_cast<cudaStream_t>(stream)));
+  return launch_rc(launch_prefill(a, plan, variant, repack, d->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t* cache, const int32_t* page_table,

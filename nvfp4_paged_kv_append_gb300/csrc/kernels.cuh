@@ -1,7 +1,6 @@
 // Kernel argument blocks and launch-shape constants shared by the kernel
 // translation units and the C-ABI host code.
 #pragma once
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -103,8 +102,7 @@ struct PrefillArgs {
   float* lse;       // optional [total_q][Hq]
   const int* work;  // [0] item count, [1] repacked tile count; items (int2) from work + 4
   const int* tile_prefix;  // [batch+1] per-request KV-tile prefix (repack mode)
-  uint8_t* repack_v;       // repacked V tiles (32 KB each), repack mode
-  uint8_t* repack_k;       // repacked K tiles (BF16), repack mode, dequant-ahead variant
+  uint8_t* repack;         // repack mode: one record per (request, kv head, KV tile)
   int* status;
 };
 
@@ -129,7 +127,7 @@ __global__ void nvfp4_dequantize_rows_kernel(DequantArgs a);
 
 // Launchers that hide templates (decode.cu / prefill.cu).
 cudaError_t launch_decode(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, const CUtensorMap& tmap_k,
-                           const CUtensorMap& tmap_ks, int variant, bool repack, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
+                           cudaStream_t s);
 
 }  // namespace nvfp4kv

@@ -7,11 +7,12 @@
 // the G query heads of one kv head, so each K/V tile fetched serves the whole
 // GQA group.  Per KV tile of 128 keys (8 pages):
 //
-//   producer warp   TMA: packed K pages (64B-swizzled, straight into the FP4
-//                   MMA operand layout) and K scale pages; V either as packed
-//                   pages + scales (in-kernel mode) or as one 32 KB FP16 tile
-//                   prepared once per (request, kv head, tile) by the repack
-//                   pre-pass (repack mode)
+//   loader warps    In-kernel mode: cp.async gathers of the tile's 8 pages
+//                   (K codes into the 64B-swizzled FP4 MMA operand layout, K
+//                   block scales into the MMA's scale-factor atoms, V codes and
+//                   scales as stored).  Repack mode: one bulk copy of the
+//                   tile's record, prepared once per (request, kv head, tile)
+//                   by the repack pre-pass in the exact shared-memory layout.
 //   transform WG    At each item start: Q tile -> NVFP4 (per-row dual level
 //                   scale) + Q block scales -> TMEM (A4Q), or Q -> shared
 //                   memory as BF16 (dequant-ahead).  In-kernel mode, per KV
@@ -47,9 +48,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 15.0f;
 
 // warps 0-3 transform, 4-7 softmax half 0, 8-11 softmax half 1,
-// 12 producer, 13 MMA, 14-15 idle (they complete the fourth warpgroup)
+// 12 and 14 loaders, 13 MMA, 15 idle (it completes the fourth warpgroup)
 constexpr int kThreads = 512;
-constexpr int kProducerWarp = 12;
+constexpr int kLoaderWarp0 = 12, kLoaderWarp1 = 14;
+constexpr int kLoaderThreads = 64;
 constexpr int kMmaWarp = 13;
 
 // TMEM columns
@@ -63,10 +65,15 @@ constexpr uint32_t kTile16 = 32768;  // 128 keys x 128 values x 2 B
 //   in-kernel:     K codes 8 KB | K scales 1 KB | V codes 8 KB | V scales 1 KB
 //   A4Q repack:    K codes 8 KB | K scales 1 KB | V tile (FP16) 32 KB
 //   DQ repack:     K tile (BF16) 32 KB | V tile (FP16) 32 KB
+// K codes are 64B-swizzled [key][64 B] rows.  A4Q K scales are two 512-byte
+// scale-factor atoms (k-steps 0 and 1: key n's four block scales at byte
+// (n % 32) * 16 + (n / 32) * 4), ready for tcgen05.cp; dequant-ahead keeps
+// them as stored ([key][8 B]).  A repack-mode stage is one record of the
+// repack pre-pass, byte for byte.
 template <int VARIANT, bool REPACK>
 struct Layout {
   static constexpr bool kA4Q = VARIANT == 0;
-  static constexpr int kStages = REPACK ? (kA4Q ? 4 : 2) : (kA4Q ? 3 : 2);
+  static constexpr int kStages = REPACK ? (kA4Q ? 5 : 2) : (kA4Q ? 6 : 3);
   static constexpr uint32_t kStageBytes =
       REPACK ? (kA4Q ? kKData + kKScale + kTile16 : 2 * kTile16) : kKData + kKScale + kVData + kVScale;
   static constexpr uint32_t kStageV = REPACK ? (kA4Q ? kKData + kKScale : kTile16) : kKData + kKScale;
@@ -78,12 +85,10 @@ struct Layout {
   static constexpr uint32_t kOffSmall = kOffK + ((!REPACK && !kA4Q) ? 2 * kTile16 : 0u);
   static constexpr uint32_t kOffQScale = kOffSmall;            // 128 floats
   static constexpr uint32_t kOffSfaStage = kOffQScale + 512;   // 128 x 8 B
-  static constexpr uint32_t kOffSfbAtoms = kOffSfaStage + 1024; // [2 buffers][2 k-steps][512 B] K scale atoms
-  static constexpr uint32_t kOffMask = kOffSfbAtoms + 2048;    // per-stage page mask
-  static constexpr uint32_t kOffXmax = kOffMask + 64;          // [2 parity][2 half][128] row maxima
+  static constexpr uint32_t kOffXmax = kOffSfaStage + 1024;    // [2 parity][2 half][128] row maxima
   static constexpr uint32_t kOffXl = kOffXmax + 2048;          // [2 half][128] row sums
   static constexpr uint32_t kOffBar = kOffXl + 1024;
-  static constexpr uint32_t kNumBars = 32;
+  static constexpr uint32_t kNumBars = 34;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kOffTmemSlot + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1 KB alignment
@@ -92,8 +97,8 @@ struct Layout {
 };
 
 struct Bars {
-  uint64_t* kv_full;   // [4]
-  uint64_t* kv_empty;  // [4]
+  uint64_t* kv_full;   // [6]
+  uint64_t* kv_empty;  // [6]
   uint64_t* sfb_full;  // [2] in-kernel dequant-ahead: K tile in BF16
   uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
@@ -112,20 +117,20 @@ struct Bars {
 __device__ __forceinline__ Bars make_bars(uint64_t* base) {
   Bars b;
   b.kv_full = base + 0;
-  b.kv_empty = base + 4;
-  b.sfb_full = base + 8;
-  b.s_full = base + 10;
-  b.p_full = base + 12;
-  b.vdq_full = base + 14;
-  b.pv_done = base + 16;
-  b.o_full = base + 18;
-  b.o_empty = base + 19;
-  b.q_full = base + 20;
-  b.q_empty = base + 21;
-  b.drain = base + 22;
-  b.qs_empty = base + 23;
-  b.sfa_ready = base + 24;
-  b.xchg = base + 25;  // 25..28
+  b.kv_empty = base + 6;
+  b.sfb_full = base + 12;
+  b.s_full = base + 14;
+  b.p_full = base + 16;
+  b.vdq_full = base + 18;
+  b.pv_done = base + 20;
+  b.o_full = base + 22;
+  b.o_empty = base + 23;
+  b.q_full = base + 24;
+  b.q_empty = base + 25;
+  b.drain = base + 26;
+  b.qs_empty = base + 27;
+  b.sfa_ready = base + 28;
+  b.xchg = base + 29;  // 29..32
   return b;
 }
 
@@ -223,87 +228,81 @@ __device__ __forceinline__ int64_t repack_index(const PrefillArgs& a, int b, int
 }
 
 // ---------------------------------------------------------------------------
-// producer warp
+// loader warps (12 and 14): t = 0..63.  In-kernel mode, thread t gathers a
+// slice of page p = t / 8 of the tile with cp.async; a page past kv_len (or
+// with an invalid id) reads as zeros.  Repack mode: thread 0 issues the one
+// bulk copy of the tile's record.
 template <int VARIANT, bool REPACK>
-__device__ void producer_loop(const PrefillArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_ks,
-                              uint8_t* smem, const Bars& bars, int lane) {
+__device__ void loader_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, int t) {
   using L = Layout<VARIANT, REPACK>;
-  int* mask_slot = reinterpret_cast<int*>(smem + L::kOffMask);
-  const int32_t oob_row = a.num_pages * a.num_kv_heads;  // first row past the pools: a TMA box there reads zeros
+  const int p = t >> 3, sub = t & 7;
   uint32_t it_ctr = 0;
   Item item;
   for (int round = 0; get_item(a, round, item); ++round) {
     for (int j = 0; j < item.n_tiles; ++j, ++it_ctr) {
       const uint32_t st = it_ctr % L::kStages, ph = (it_ctr / L::kStages) & 1u;
-      int pid = -1;
-      const int page_idx = j * kPagesPerTile + lane;
-      if (lane < kPagesPerTile && page_idx * kPageSize < item.kv_len) {
-        pid = a.page_table[static_cast<int64_t>(item.b) * a.max_pages + page_idx];
-        if (pid < 0 || pid >= a.num_pages) {
-          set_status(a.status, kDevBadPage);
-          pid = -1;
-        }
-      }
-      const unsigned valid = __ballot_sync(0xffffffffu, pid >= 0);
-      // K codes and K scales: all 8 pages through TMA (pages that hold no
-      // data read zeros); V: packed pages (in-kernel) or one repacked tile.
-      uint32_t bytes;
-      if constexpr (REPACK && !L::kA4Q) bytes = 2 * kTile16;
-      else if constexpr (REPACK) bytes = kPagesPerTile * (1024 + 128) + kTile16;
-      else bytes = kPagesPerTile * (1024 + 128) + __popc(valid) * (1024 + 128);
-      bool ok = true;
-      if (lane == 0) {
-        ok = mbar_wait(&bars.kv_empty[st], ph ^ 1u, a.status);
-        if (ok) {
-          mask_slot[st] = static_cast<int>(valid);
-          mbar_arrive_expect_tx(&bars.kv_full[st], bytes);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) return;
       uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
-      if constexpr (REPACK && !L::kA4Q) {
-        if (lane == 0) {
-          const int64_t t = repack_index(a, item.b, item.kvh, j);
-          bulk_load(stage, a.repack_k + t * kTile16, kTile16, &bars.kv_full[st]);
-          bulk_load(stage + L::kStageV, a.repack_v + t * kTile16, kTile16, &bars.kv_full[st]);
+      if constexpr (REPACK) {
+        if (t == 0) {
+          if (!mbar_wait(&bars.kv_empty[st], ph ^ 1u, a.status)) return;
+          mbar_arrive_expect_tx(&bars.kv_full[st], L::kStageBytes);
+          bulk_load(stage, a.repack + repack_index(a, item.b, item.kvh, j) * L::kStageBytes, L::kStageBytes,
+                    &bars.kv_full[st]);
         }
       } else {
-        if (lane < kPagesPerTile) {
-          const int32_t rowp = pid >= 0 ? pid * a.num_kv_heads + item.kvh : oob_row;
-          tma_load_2d(stage + lane * 1024, tmap_k, 0, rowp * kPageSize, &bars.kv_full[st]);
-          tma_load_2d(stage + kKData + lane * 128, tmap_ks, 0, rowp, &bars.kv_full[st]);
+        int pid = -1;
+        const int page_idx = j * kPagesPerTile + p;
+        if (page_idx * kPageSize < item.kv_len) {
+          pid = a.page_table[static_cast<int64_t>(item.b) * a.max_pages + page_idx];
+          if (pid < 0 || pid >= a.num_pages) {
+            if (sub == 0) set_status(a.status, kDevBadPage);
+            pid = -1;
+          }
         }
-        if constexpr (REPACK) {
-          if (lane == 0) {
-            const int64_t t = repack_index(a, item.b, item.kvh, j);
-            bulk_load(stage + L::kStageV, a.repack_v + t * kTile16, kTile16, &bars.kv_full[st]);
+        const uint32_t n16 = pid >= 0 ? 16u : 0u, n4 = pid >= 0 ? 4u : 0u;
+        const int64_t row0 = (static_cast<int64_t>(pid >= 0 ? pid : 0) * a.num_kv_heads + item.kvh) * kPageSize;
+        if (!mbar_wait_warp(&bars.kv_empty[st], ph ^ 1u, a.status)) return;
+        const uint32_t st_s = smem_u32(stage);
+        const uint8_t* kd = a.k_data + row0 * 64;
+        const uint8_t* vd = a.v_data + row0 * 64;
+        // codes: the page's 64 chunks of 16 B, chunk q = token q/4, quarter q%4
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = sub + 8 * i, n = p * kPageSize + (q >> 2), c = q & 3;
+          cp_async16(st_s + sw64_off(n, c), kd + q * 16, n16);
+          cp_async16(st_s + kKData + kKScale + n * 64 + c * 16, vd + q * 16, n16);
+        }
+        // V scales: 16 B = two tokens' 8 scale bytes
+        cp_async16(st_s + kKData + kKScale + kVData + (p * kPageSize + 2 * sub) * 8,
+                   a.v_scale + row0 * 8 + sub * 16, n16);
+        if constexpr (L::kA4Q) {
+          // K scales into the scale-factor atoms: 4 bytes = one token's scales
+          // for one 64-value k-step
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int q = sub + 8 * i, r = q >> 1, ks = q & 1, n = p * kPageSize + r;
+            cp_async4(st_s + kKData + ks * 512 + (n & 31) * 16 + (n >> 5) * 4, a.k_scale + (row0 + r) * 8 + 4 * ks,
+                      n4);
           }
         } else {
-          if (pid >= 0) {
-            const int64_t row = (static_cast<int64_t>(pid) * a.num_kv_heads + item.kvh) * kPageSize;
-            bulk_load(stage + kKData + kKScale + lane * 1024, a.v_data + row * 64, 1024, &bars.kv_full[st]);
-            bulk_load(stage + kKData + kKScale + kVData + lane * 128, a.v_scale + row * 8, 128, &bars.kv_full[st]);
-          }
+          cp_async16(st_s + kKData + (p * kPageSize + 2 * sub) * 8, a.k_scale + row0 * 8 + sub * 16, n16);
         }
+        cp_async_mbar_arrive(&bars.kv_full[st]);
       }
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// MMA warp: all 32 lanes wait and (A4Q) rearrange the tile's K block scales
-// into the scale-factor atom the block-scaled MMA reads (row n of the 128-row
-// atom at byte (n%32)*16 + (n/32)*4, four 16-value blocks per word); lane 0
-// copies the atoms into TMEM with tcgen05.cp and issues every MMA.  The copy
-// and the MMAs are tcgen05 operations of one thread and run in issue order.
+// MMA warp: all 32 lanes wait; lane 0 copies the tile's K scale atoms into
+// TMEM with tcgen05.cp (A4Q) and issues every MMA.  The copy and the MMAs are
+// tcgen05 operations of one thread and run in issue order.
 template <int VARIANT, bool REPACK>
 __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int lane) {
   using L = Layout<VARIANT, REPACK>;
   const uint32_t q_s = smem_u32(smem + L::kOffQ);
   const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   const uint32_t idesc_qk = L::kA4Q ? idesc_mxf4nvf4(128, 128) : idesc_f16(128, 128, 1, 1, 0, 0);
-  uint8_t* atoms = smem + L::kOffSfbAtoms;
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
   auto do_pv = [&](uint32_t it, bool first) -> bool {
@@ -336,24 +335,7 @@ __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, 
       const uint32_t st = it % L::kStages, b = it & 1u;
       if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
       const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
-      if constexpr (L::kA4Q) {
-        // Atom buffer b was last read by the scale copy of tile it-2; that
-        // copy precedes QK(it-2), whose S the softmax had consumed before
-        // p_full(it-2), already waited on.
-        const uint8_t* ks = stage + kKData;  // [128 tokens][8 scale bytes]
-        uint8_t* at = atoms + b * 1024;
-        uint32_t w0[4], w1[4];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint2 v = *reinterpret_cast<const uint2*>(ks + (lane + 32 * q4) * 8);
-          w0[q4] = v.x;
-          w1[q4] = v.y;
-        }
-        *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-        *reinterpret_cast<uint4*>(at + 512 + lane * 16) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-      } else if constexpr (!REPACK) {
+      if constexpr (!L::kA4Q && !REPACK) {
         if (!mbar_wait_warp(&bars.sfb_full[b], (it >> 1) & 1u, a.status)) return;
       }
       if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
@@ -362,7 +344,11 @@ __device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, 
         const uint32_t s_col = b ? kColS1 : kColS0;
         const uint32_t stage_s = smem_u32(stage);
         if constexpr (L::kA4Q) {
-          const uint32_t at_s = smem_u32(atoms + b * 1024);
+          // In-kernel mode the K codes and scale atoms arrived through
+          // cp.async (generic proxy); the tensor core reads them next.
+          if constexpr (!REPACK) fence_proxy_async_smem();
+          // SFB buffer b was last read by QK(it-2), finished before PV(it-2).
+          const uint32_t at_s = stage_s + kKData;
           tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b, smem_desc(at_s, 0, 128, kSwzNone));
           tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b + 4, smem_desc(at_s + 512, 0, 128, kSwzNone));
 #pragma unroll
@@ -403,7 +389,6 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
   const int G = a.group, lg = a.log2_group;
   float* qscale = reinterpret_cast<float*>(smem + L::kOffQScale);
   uint2* sfa_stage = reinterpret_cast<uint2*>(smem + L::kOffSfaStage);
-  const int* mask_slot = reinterpret_cast<const int*>(smem + L::kOffMask);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
   for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
@@ -502,7 +487,6 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
         const uint32_t st = it % L::kStages, b = it & 1u;
         if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
         const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
-        const int valid_pages = mask_slot[st];
         const int key_base = j * kBN;
         if constexpr (!L::kA4Q) {
           // K -> BF16 (exact), K-major 128B-swizzled operand; buffer b was
@@ -532,7 +516,7 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
         for (int i = 0; i < 4; ++i) {
           const int u = tid + 128 * i;
           const int key = u >> 2, c = u & 3;
-          const bool live = (key_base + key < item.kv_len) && ((valid_pages >> (key >> 4)) & 1);
+          const bool live = key_base + key < item.kv_len;  // invalid pages were loaded as zeros
           uint32_t o0[4] = {0, 0, 0, 0}, o1[4] = {0, 0, 0, 0}, o2[4] = {0, 0, 0, 0}, o3[4] = {0, 0, 0, 0};
           if (live) {
             const uint4 src = *reinterpret_cast<const uint4*>(vd + key * 64 + 16 * c);
@@ -713,8 +697,7 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
 }
 
 template <int VARIANT, bool REPACK>
-__device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtensorMap* tmap_k,
-                                             const CUtensorMap* tmap_ks) {
+__device__ __forceinline__ void prefill_body(const PrefillArgs& a) {
   using L = Layout<VARIANT, REPACK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -724,7 +707,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   const Bars bars = make_bars(bar_base);
   if (tid == 0) {
     for (int i = 0; i < L::kStages; ++i) {
-      mbar_init(&bars.kv_full[i], 1);
+      mbar_init(&bars.kv_full[i], REPACK ? 1 : kLoaderThreads);  // bulk copy + tx, or one cp.async arrival per loader thread
       // one MMA commit, plus one arrive per transform warp when the transform
       // warpgroup reads the stage (in-kernel mode)
       mbar_init(&bars.kv_empty[i], REPACK ? 1 : 5);
@@ -746,10 +729,6 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
     for (int i = 0; i < 4; ++i) mbar_init(&bars.xchg[i], 2);
     fence_barrier_init();
   }
-  if (warp == kProducerWarp && lane == 0) {
-    prefetch_tmap(tmap_k);
-    prefetch_tmap(tmap_ks);
-  }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -763,8 +742,8 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
     transform_loop<VARIANT, REPACK>(a, smem, bars, tbase, tid);
   } else if (warp < 12) {
     softmax_loop<VARIANT, REPACK>(a, smem, bars, tbase, (tid - 128) & 127, (tid - 128) >> 7);
-  } else if (warp == kProducerWarp) {
-    producer_loop<VARIANT, REPACK>(a, tmap_k, tmap_ks, smem, bars, lane);
+  } else if (warp == kLoaderWarp0 || warp == kLoaderWarp1) {
+    loader_loop<VARIANT, REPACK>(a, smem, bars, (warp == kLoaderWarp0 ? 0 : 32) + lane);
   } else if (warp == kMmaWarp) {
     mma_loop<VARIANT, REPACK>(a, smem, bars, tbase, lane);
     // drain: every MMA issued by lane 0 has finished before TMEM is freed
@@ -783,31 +762,31 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
 
 // Kernel names carry the variant and the V path, so a trace shows which ran.
 __global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_prefill_a4q_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
-                                   const __grid_constant__ CUtensorMap tmap_ks) {
-  prefill_body<0, false>(a, &tmap_k, &tmap_ks);
+    nvfp4_prefill_a4q_sm103_kernel(const PrefillArgs a) {
+  prefill_body<0, false>(a);
 }
 __global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_prefill_a4q_vrepack_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
-                                           const __grid_constant__ CUtensorMap tmap_ks) {
-  prefill_body<0, true>(a, &tmap_k, &tmap_ks);
+    nvfp4_prefill_a4q_vrepack_sm103_kernel(const PrefillArgs a) {
+  prefill_body<0, true>(a);
 }
 __global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_prefill_dqahead_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
-                                       const __grid_constant__ CUtensorMap tmap_ks) {
-  prefill_body<1, false>(a, &tmap_k, &tmap_ks);
+    nvfp4_prefill_dqahead_sm103_kernel(const PrefillArgs a) {
+  prefill_body<1, false>(a);
 }
 __global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_prefill_dqahead_repack_sm103_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
-                                              const __grid_constant__ CUtensorMap tmap_ks) {
-  prefill_body<1, true>(a, &tmap_k, &tmap_ks);
+    nvfp4_prefill_dqahead_repack_sm103_kernel(const PrefillArgs a) {
+  prefill_body<1, true>(a);
 }
 
 // ---------------------------------------------------------------------------
-// repack pre-pass: each (request, kv head, KV tile) once -> 32 KB FP16 V tile
-// (and a BF16 K tile for the dequant-ahead variant) in the exact operand
-// layout the attention kernel's MMAs read; keys past kv_len are zeros.
-__global__ void __launch_bounds__(128) nvfp4_prefill_repack_kernel(PrefillArgs a, int with_k) {
+// repack pre-pass: each (request, kv head, KV tile) once -> one record laid
+// out exactly like a repack-mode stage, so the attention kernel moves it with
+// a single bulk copy.  A4Q: K codes (64B-swizzled) | K scale atoms | V (FP16,
+// MN-major 128B-swizzled); dequant-ahead: K (BF16, K-major 128B-swizzled) | V.
+// Keys past kv_len are zeros.
+template <int VARIANT>
+__global__ void __launch_bounds__(128) nvfp4_prefill_repack_kernel(PrefillArgs a) {
+  using L = Layout<VARIANT, true>;
   const int tid = threadIdx.x;
   const int total = a.work[1];
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -821,27 +800,49 @@ __global__ void __launch_bounds__(128) nvfp4_prefill_repack_kernel(PrefillArgs a
     const int r = t - a.tile_prefix[b] * a.num_kv_heads;
     const int h = r / n_t, j = r - h * n_t;
     const int kv_len = a.kv_lens[b];
-    for (int tensor = with_k ? 0 : 1; tensor < 2; ++tensor) {
+    uint8_t* rec = a.repack + static_cast<int64_t>(t) * L::kStageBytes;
+    // cache row of key `key` of this tile, or -1 (past kv_len / invalid page)
+    auto row_of = [&](int key) -> int64_t {
+      const int abs_key = j * kBN + key;
+      if (abs_key >= kv_len) return -1;
+      const int pid = a.page_table[static_cast<int64_t>(b) * a.max_pages + (abs_key >> 4)];
+      if (pid < 0 || pid >= a.num_pages) {
+        set_status(a.status, kDevBadPage);
+        return -1;
+      }
+      return (static_cast<int64_t>(pid) * a.num_kv_heads + h) * kPageSize + (abs_key & 15);
+    };
+    if constexpr (VARIANT == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int u = tid + 128 * i, key = u >> 2, c = u & 3;
+        const int64_t row = row_of(key);
+        const uint4 v = row >= 0 ? *reinterpret_cast<const uint4*>(a.k_data + row * 64 + 16 * c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(rec + sw64_off(key, c)) = v;
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int u = tid + 128 * i, key = u >> 1, ks = u & 1;
+        const int64_t row = row_of(key);
+        const uint32_t w = row >= 0 ? *reinterpret_cast<const uint32_t*>(a.k_scale + row * 8 + 4 * ks) : 0u;
+        *reinterpret_cast<uint32_t*>(rec + kKData + ks * 512 + (key & 31) * 16 + (key >> 5) * 4) = w;
+      }
+    }
+    for (int tensor = VARIANT == 0 ? 1 : 0; tensor < 2; ++tensor) {
       const uint8_t* data = tensor ? a.v_data : a.k_data;
       const uint8_t* scl = tensor ? a.v_scale : a.k_scale;
-      uint8_t* dst = (tensor ? a.repack_v : a.repack_k) + static_cast<int64_t>(t) * kTile16;
+      uint8_t* dst = rec + (tensor ? L::kStageV : 0u);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int u = tid + 128 * i;
         const int key = u >> 2, c = u & 3;
-        const int abs_key = j * kBN + key;
+        const int64_t row = row_of(key);
         uint32_t o0[4] = {0, 0, 0, 0}, o1[4] = {0, 0, 0, 0}, o2[4] = {0, 0, 0, 0}, o3[4] = {0, 0, 0, 0};
-        if (abs_key < kv_len) {
-          const int pid = a.page_table[static_cast<int64_t>(b) * a.max_pages + (abs_key >> 4)];
-          if (pid >= 0 && pid < a.num_pages) {
-            const int64_t row = (static_cast<int64_t>(pid) * a.num_kv_heads + h) * kPageSize + (abs_key & 15);
-            const uint4 src = *reinterpret_cast<const uint4*>(data + row * 64 + 16 * c);
-            const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(scl + row * 8 + 2 * c);
-            if (tensor) dequant_unit<false>(src, sc01, o0, o1, o2, o3);
-            else dequant_unit<true>(src, sc01, o0, o1, o2, o3);
-          } else {
-            set_status(a.status, kDevBadPage);
-          }
+        if (row >= 0) {
+          const uint4 src = *reinterpret_cast<const uint4*>(data + row * 64 + 16 * c);
+          const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(scl + row * 8 + 2 * c);
+          if (tensor) dequant_unit<false>(src, sc01, o0, o1, o2, o3);
+          else dequant_unit<true>(src, sc01, o0, o1, o2, o3);
         }
         uint8_t* d = dst + (c >> 1) * 16384;
         const uint32_t cc = (c & 1) * 4;
@@ -978,33 +979,31 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
 }
 
 template <typename K>
-cudaError_t launch_main(K kernel, uint32_t smem, const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmks,
-                        int num_sms, cudaStream_t s) {
+cudaError_t launch_main(K kernel, uint32_t smem, const PrefillArgs& a, int num_sms, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<num_sms, kThreads, smem, s>>>(a, tmk, tmks);
+  kernel<<<num_sms, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, const CUtensorMap& tmap_k,
-                           const CUtensorMap& tmap_ks, int variant, bool repack, int num_sms, cudaStream_t s) {
+cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
+                           cudaStream_t s) {
   nvfp4_prefill_plan_kernel<<<1, 1024, 0, s>>>(plan);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (repack) {
-    nvfp4_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a, variant == 1 ? 1 : 0);
+    if (variant == 0) nvfp4_prefill_repack_kernel<0><<<num_sms * 8, 128, 0, s>>>(a);
+    else nvfp4_prefill_repack_kernel<1><<<num_sms * 8, 128, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (variant == 0)
-    return repack ? launch_main(nvfp4_prefill_a4q_vrepack_sm103_kernel, Layout<0, true>::kAlloc, a, tmap_k, tmap_ks,
-                                num_sms, s)
-                  : launch_main(nvfp4_prefill_a4q_sm103_kernel, Layout<0, false>::kAlloc, a, tmap_k, tmap_ks, num_sms, s);
-  return repack ? launch_main(nvfp4_prefill_dqahead_repack_sm103_kernel, Layout<1, true>::kAlloc, a, tmap_k, tmap_ks,
-                              num_sms, s)
-                : launch_main(nvfp4_prefill_dqahead_sm103_kernel, Layout<1, false>::kAlloc, a, tmap_k, tmap_ks, num_sms, s);
+    return repack ? launch_main(nvfp4_prefill_a4q_vrepack_sm103_kernel, Layout<0, true>::kAlloc, a, num_sms, s)
+                  : launch_main(nvfp4_prefill_a4q_sm103_kernel, Layout<0, false>::kAlloc, a, num_sms, s);
+  return repack ? launch_main(nvfp4_prefill_dqahead_repack_sm103_kernel, Layout<1, true>::kAlloc, a, num_sms, s)
+                : launch_main(nvfp4_prefill_dqahead_sm103_kernel, Layout<1, false>::kAlloc, a, num_sms, s);
 }
 
 }  // namespace nvfp4kv

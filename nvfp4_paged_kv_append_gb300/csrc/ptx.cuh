@@ -103,6 +103,23 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, i
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// ---- cp.async (LSU path) -----------------------------------------------------------
+// Copies of 16 or 4 bytes global -> shared that read only `src_bytes` bytes
+// of the source (0 or the full size) and fill the rest of the destination
+// with zeros.  Small scattered pieces (paged K/V) go this way: the bulk-copy
+// engine spends a fixed cost per copy that makes 128 B - 1 KB pieces slow.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// One arrival on `bar` once every cp.async this thread has issued so far has
+// landed.  The arrival is part of the barrier's expected count (noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ---- async proxy fences --------------------------------------------------------
 // Generic-proxy shared-memory writes made visible to the async proxy (tensor
 // core / TMA) before a barrier hand-off.
@@ -110,25 +127,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ---- TMA / bulk copies -----------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
+// ---- bulk copies (one contiguous run, global -> shared, completing on an mbarrier) ----
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
 // ---- tcgen05: tensor memory ------------------------------------------------------
