@@ -47,15 +47,19 @@ constexpr float kLn2 = 0.6931471805599453f;
 // exceeds it by more than this, so P stays <= 2^15, inside FP16's range.
 constexpr float kRescaleThreshold = 15.0f;
 
-// warps 0-3 transform, 4-7 softmax half 0, 8-11 softmax half 1,
-// 12 and 14 loaders, 13 MMA, 15 idle (it completes the fourth warpgroup)
+// warps 0 QK issue (and TMEM allocation), 1-2 loaders, 3 PV issue, 4-7
+// transform, 8-11 softmax half 0, 12-15 softmax half 1.  A warp reaches only
+// the TMEM lane quadrant (warp id % 4), which the transform and softmax
+// warpgroups keep: row r of a tile lives in quadrant r / 32.
 constexpr int kThreads = 512;
-constexpr int kLoaderWarp0 = 12, kLoaderWarp1 = 14;
+constexpr int kMmaWarp = 0, kPvWarp = 3;
+constexpr int kLoaderWarp0 = 1, kLoaderWarp1 = 2;
 constexpr int kLoaderThreads = 64;
-constexpr int kMmaWarp = 13;
+constexpr int kTransformTid0 = 128, kSoftmaxTid0 = 256;
 
-// TMEM columns
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA = 384, kColSFB = 392;
+// TMEM columns: S double buffer (fp32), O (fp32), P (FP16 pairs, one tile),
+// Q block scales, K block scales (double buffer)
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384, kColSFA = 448, kColSFB = 456;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kKData = 8192, kKScale = 1024, kVData = 8192, kVScale = 1024;
@@ -88,7 +92,7 @@ struct Layout {
   static constexpr uint32_t kOffXmax = kOffSfaStage + 1024;    // [2 parity][2 half][128] row maxima
   static constexpr uint32_t kOffXl = kOffXmax + 2048;          // [2 half][128] row sums
   static constexpr uint32_t kOffBar = kOffXl + 1024;
-  static constexpr uint32_t kNumBars = 34;
+  static constexpr uint32_t kNumBars = 36;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kOffTmemSlot + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1 KB alignment
@@ -101,6 +105,7 @@ struct Bars {
   uint64_t* kv_empty;  // [6]
   uint64_t* sfb_full;  // [2] in-kernel dequant-ahead: K tile in BF16
   uint64_t* s_full;    // [2]
+  uint64_t* s_free;    // [2] softmax has loaded S: the buffer may take the next QK
   uint64_t* p_full;    // [2]
   uint64_t* vdq_full;  // [2] in-kernel mode: V tile in FP16
   uint64_t* pv_done;   // [2]
@@ -131,6 +136,7 @@ __device__ __forceinline__ Bars make_bars(uint64_t* base) {
   b.qs_empty = base + 27;
   b.sfa_ready = base + 28;
   b.xchg = base + 29;  // 29..32
+  b.s_free = base + 33;  // 33..34
   return b;
 }
 
@@ -294,94 +300,98 @@ __device__ void loader_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bar
 }
 
 // ---------------------------------------------------------------------------
-// MMA warp: all 32 lanes wait; lane 0 copies the tile's K scale atoms into
-// TMEM with tcgen05.cp (A4Q) and issues every MMA.  The copy and the MMAs are
-// tcgen05 operations of one thread and run in issue order.
+// MMA issue: one thread issues every QK (warp 0, lane 0) and another every PV
+// (warp 3, lane 0).  A thread that issues tcgen05.mma is held until the
+// tensor core has nearly finished it, so with a single issuer every barrier
+// wait, commit and fence would sit between MMAs; with two, one thread's
+// bookkeeping overlaps the other's MMAs.  Each thread's commits track its own
+// MMAs.  The two streams meet only through the softmax: P(it) exists only
+// after S(it) was read, so PV(it) finishing implies QK(it) finished.
 template <int VARIANT, bool REPACK>
-__device__ void mma_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int lane) {
+__device__ void qk_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase) {
   using L = Layout<VARIANT, REPACK>;
   const uint32_t q_s = smem_u32(smem + L::kOffQ);
-  const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   const uint32_t idesc_qk = L::kA4Q ? idesc_mxf4nvf4(128, 128) : idesc_f16(128, 128, 1, 1, 0, 0);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
-  auto do_pv = [&](uint32_t it, bool first) -> bool {
-    const uint32_t b = it & 1u, ph = (it >> 1) & 1u;
-    if (!mbar_wait_warp(&bars.p_full[b], ph, a.status)) return false;
-    if (!REPACK && !mbar_wait_warp(&bars.vdq_full[b], ph, a.status)) return false;
-    if (first && !mbar_wait_warp(bars.o_empty, (item_ctr & 1u) ^ 1u, a.status)) return false;
-    tc_fence_after();
-    if (lane == 0) {
-      const uint32_t st = it % L::kStages;
+  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
+    if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
+    for (int j = 0; j < item.n_tiles; ++j) {
+      const uint32_t it = it_ctr + j;
+      const uint32_t st = it % L::kStages, b = it & 1u;
+      if (!mbar_wait(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
+      if constexpr (!L::kA4Q && !REPACK) {
+        if (!mbar_wait(&bars.sfb_full[b], (it >> 1) & 1u, a.status)) return;
+      }
+      // S buffer b held S(it-2) until the softmax loaded it
+      if (it >= 2 && !mbar_wait(&bars.s_free[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+      tc_fence_after();
+      const uint32_t s_col = b ? kColS1 : kColS0;
+      const uint32_t stage_s = smem_u32(smem + L::kOffStage + st * L::kStageBytes);
+      if constexpr (L::kA4Q) {
+        // In-kernel mode the K codes and scale atoms arrived through
+        // cp.async (generic proxy); the tensor core reads them next.
+        if constexpr (!REPACK) fence_proxy_async_smem();
+        // SFB buffer b was last read by QK(it-2), finished before s_free(it-2).
+        const uint32_t at_s = stage_s + kKData;
+        tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b, smem_desc(at_s, 0, 128, kSwzNone));
+        tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b + 4, smem_desc(at_s + 512, 0, 128, kSwzNone));
+#pragma unroll
+        for (uint32_t s = 0; s < 2; ++s) {
+          mma_nvf4_ss(tbase + s_col, smem_desc(q_s + 32 * s, 16, 512, kSwz64),
+                      smem_desc(stage_s + 32 * s, 16, 512, kSwz64), idesc_qk, tbase + kColSFA + 4 * s,
+                      tbase + kColSFB + 8 * b + 4 * s, s > 0 ? 1u : 0u);
+        }
+      } else {
+        const uint32_t k_s = REPACK ? stage_s : smem_u32(smem + L::kOffK + b * kTile16);
+#pragma unroll
+        for (uint32_t k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_f16_ss(tbase + s_col, smem_desc(q_s + off, 16, 1024, kSwz128), smem_desc(k_s + off, 16, 1024, kSwz128),
+                     idesc_qk, k > 0 ? 1u : 0u);
+        }
+      }
+      tc_commit(&bars.s_full[b]);
+      if (!REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's K has been read
+      if (j == item.n_tiles - 1) tc_commit(bars.q_empty);
+    }
+    it_ctr += item.n_tiles;
+  }
+}
+
+template <int VARIANT, bool REPACK>
+__device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase) {
+  using L = Layout<VARIANT, REPACK>;
+  const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
+  uint32_t it_ctr = 0, item_ctr = 0;
+  Item item;
+  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
+    for (int j = 0; j < item.n_tiles; ++j) {
+      const uint32_t it = it_ctr + j;
+      const uint32_t st = it % L::kStages, b = it & 1u, ph = (it >> 1) & 1u;
+      if (!mbar_wait(&bars.p_full[b], ph, a.status)) return;
+      if (!REPACK && !mbar_wait(&bars.vdq_full[b], ph, a.status)) return;
+      // the first PV of an item overwrites O: the previous item's epilogue
+      // must have read it
+      if (j == 0 && !mbar_wait(bars.o_empty, (item_ctr & 1u) ^ 1u, a.status)) return;
+      tc_fence_after();
       const uint32_t v_s = REPACK ? smem_u32(smem + L::kOffStage + st * L::kStageBytes + L::kStageV)
                                   : smem_u32(smem + L::kOffV + b * kTile16);
-      const uint32_t s_col = b ? kColS1 : kColS0;
 #pragma unroll
       for (uint32_t k = 0; k < 8; ++k) {
-        mma_f16_ts(tbase + kColO, tbase + s_col + 8 * k, smem_desc(v_s + k * 2048, 16384, 1024, kSwz128), idesc_pv,
-                   (first && k == 0) ? 0u : 1u);
+        mma_f16_ts(tbase + kColO, tbase + kColP + 8 * k, smem_desc(v_s + k * 2048, 16384, 1024, kSwz128), idesc_pv,
+                   (j == 0 && k == 0) ? 0u : 1u);
       }
       tc_commit(&bars.pv_done[b]);
       if (REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's V tile has been read
     }
-    __syncwarp();
-    return true;
-  };
-  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
-    if (!mbar_wait_warp(bars.q_full, item_ctr & 1u, a.status)) return;
-    tc_fence_after();
-    for (int j = 0; j < item.n_tiles; ++j) {
-      const uint32_t it = it_ctr + j;
-      const uint32_t st = it % L::kStages, b = it & 1u;
-      if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
-      const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
-      if constexpr (!L::kA4Q && !REPACK) {
-        if (!mbar_wait_warp(&bars.sfb_full[b], (it >> 1) & 1u, a.status)) return;
-      }
-      if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t s_col = b ? kColS1 : kColS0;
-        const uint32_t stage_s = smem_u32(stage);
-        if constexpr (L::kA4Q) {
-          // In-kernel mode the K codes and scale atoms arrived through
-          // cp.async (generic proxy); the tensor core reads them next.
-          if constexpr (!REPACK) fence_proxy_async_smem();
-          // SFB buffer b was last read by QK(it-2), finished before PV(it-2).
-          const uint32_t at_s = stage_s + kKData;
-          tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b, smem_desc(at_s, 0, 128, kSwzNone));
-          tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b + 4, smem_desc(at_s + 512, 0, 128, kSwzNone));
-#pragma unroll
-          for (uint32_t s = 0; s < 2; ++s) {
-            mma_nvf4_ss(tbase + s_col, smem_desc(q_s + 32 * s, 16, 512, kSwz64),
-                        smem_desc(stage_s + 32 * s, 16, 512, kSwz64), idesc_qk, tbase + kColSFA + 4 * s,
-                        tbase + kColSFB + 8 * b + 4 * s, s > 0 ? 1u : 0u);
-          }
-        } else {
-          const uint32_t k_s = REPACK ? stage_s : smem_u32(smem + L::kOffK + b * kTile16);
-#pragma unroll
-          for (uint32_t k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_f16_ss(tbase + s_col, smem_desc(q_s + off, 16, 1024, kSwz128),
-                       smem_desc(k_s + off, 16, 1024, kSwz128), idesc_qk, k > 0 ? 1u : 0u);
-          }
-        }
-        tc_commit(&bars.s_full[b]);
-        if (!REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's K has been read
-        if (j == item.n_tiles - 1) tc_commit(bars.q_empty);
-      }
-      __syncwarp();
-      if (j >= 1 && !do_pv(it - 1, j == 1)) return;
-    }
-    if (!do_pv(it_ctr + item.n_tiles - 1, item.n_tiles == 1)) return;
-    if (lane == 0) tc_commit(bars.o_full);
-    __syncwarp();
+    tc_commit(bars.o_full);
     it_ctr += item.n_tiles;
   }
 }
 
 // ---------------------------------------------------------------------------
-// transform warpgroup (warps 0-3): thread = Q row / TMEM lane
+// transform warpgroup (warps 4-7): thread = Q row / TMEM lane
 template <int VARIANT, bool REPACK>
 __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int tid) {
   using L = Layout<VARIANT, REPACK>;
@@ -538,7 +548,7 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
 }
 
 // ---------------------------------------------------------------------------
-// softmax warpgroups (warps 4-11): thread = TMEM lane = row; warpgroup `half`
+// softmax warpgroups (warps 8-15): thread = TMEM lane = row; warpgroup `half`
 // owns keys 64*half .. 64*half+63 of every tile and O columns of the same range
 template <int VARIANT, bool REPACK>
 __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int r,
@@ -584,6 +594,10 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
       tmem_ld32(lane_base + s_col + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_ld32(lane_base + s_col + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_ld();
+      // S is in registers: the buffer may take QK(it+2)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_free[b]);
       float* s = reinterpret_cast<float*>(sr);
       const int key0 = j * kBN + 64 * half;
       // Keys past the row's last visible one are masked (scale applied here);
@@ -606,8 +620,8 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
       if (!meet()) return;  // both halves have read their S and published their max
       const float m_tile = fmaxf(m_half, xm[(half ^ 1) * 128 + r]);
       // Lazy rescale: the running max moves only when the tile max exceeds it
-      // by more than 2^8.  TMEM loads/stores are warp-collective, so the whole
-      // warp rescales its 64 O columns, with factor 1 for rows that keep
+      // by more than 2^15.  TMEM loads/stores are warp-collective, so the
+      // whole warp rescales its 64 O columns, with factor 1 for rows that keep
       // their max.  Both halves take identical decisions (same m_tile).
       float alpha = 1.0f;
       const bool need = m_tile > m_run + kRescaleThreshold;
@@ -618,10 +632,25 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
         for (int i = 0; i < 4; ++i) lacc[i] = __fmul2_rn(lacc[i], a2);
         m_run = m_tile;
       }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        const uint32_t pit = it - 1u;  // O must hold PV of the previous tile
+      const bool rescale_o = j > 0 && __any_sync(0xffffffffu, need);
+      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+      const float cs = masked ? 1.0f : c_r;
+      const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-m_use, -m_use);
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float2 t = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), cs2, nm2);
+        const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+        lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
+        pk[c] = pack_f16x2(p.x, p.y);
+      }
+      // P and O belong to the tensor core until PV(it-1) has finished.
+      if (it > 0) {
+        const uint32_t pit = it - 1u;
         if (!mbar_wait_warp(&bars.pv_done[pit & 1u], (pit >> 1) & 1u, a.status)) return;
         tc_fence_after();
+      }
+      if (rescale_o) {
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           uint32_t ov[32];
@@ -633,24 +662,9 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
           tmem_st16(lane_base + ocol + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
         }
       }
-      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-      const float cs = masked ? 1.0f : c_r;
-      const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-m_use, -m_use);
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int e = 32 * h2 + 2 * c;
-          const float2 t = __ffma2_rn(make_float2(s[e], s[e + 1]), cs2, nm2);
-          const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-          lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
-          pk[c] = pack_f16x2(p.x, p.y);
-        }
-        // P of keys 64*half.. goes to TMEM columns 32*half.. of the S buffer
-        // (the other half finished reading those columns before the meeting).
-        tmem_st16(lane_base + s_col + 32 * half + 16 * h2, pk);
-      }
+      // P of keys 64*half.. goes to P columns 32*half..
+      tmem_st16(lane_base + kColP + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      tmem_st16(lane_base + kColP + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -715,6 +729,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.sfb_full[i], 4);
       mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_free[i], 8);
       mbar_init(&bars.p_full[i], 8);
       mbar_init(&bars.vdq_full[i], 4);
       mbar_init(&bars.pv_done[i], 1);
@@ -723,7 +738,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a) {
     mbar_init(bars.o_empty, 8);
     mbar_init(bars.q_full, 4);
     mbar_init(bars.q_empty, 1);
-    mbar_init(bars.drain, 1);
+    mbar_init(bars.drain, 2);  // one commit per MMA-issuing thread
     mbar_init(bars.qs_empty, 8);
     mbar_init(bars.sfa_ready, 4);
     for (int i = 0; i < 4; ++i) mbar_init(&bars.xchg[i], 2);
@@ -738,17 +753,17 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a) {
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp < 4) {
-    transform_loop<VARIANT, REPACK>(a, smem, bars, tbase, tid);
-  } else if (warp < 12) {
-    softmax_loop<VARIANT, REPACK>(a, smem, bars, tbase, (tid - 128) & 127, (tid - 128) >> 7);
+  if (tid >= kSoftmaxTid0) {
+    softmax_loop<VARIANT, REPACK>(a, smem, bars, tbase, (tid - kSoftmaxTid0) & 127, (tid - kSoftmaxTid0) >> 7);
+  } else if (tid >= kTransformTid0) {
+    transform_loop<VARIANT, REPACK>(a, smem, bars, tbase, tid - kTransformTid0);
   } else if (warp == kLoaderWarp0 || warp == kLoaderWarp1) {
     loader_loop<VARIANT, REPACK>(a, smem, bars, (warp == kLoaderWarp0 ? 0 : 32) + lane);
-  } else if (warp == kMmaWarp) {
-    mma_loop<VARIANT, REPACK>(a, smem, bars, tbase, lane);
-    // drain: every MMA issued by lane 0 has finished before TMEM is freed
-    if (lane == 0) tc_commit(bars.drain);
-    __syncwarp();
+  } else if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
+    if (warp == kMmaWarp) qk_loop<VARIANT, REPACK>(a, smem, bars, tbase);
+    else pv_loop<VARIANT, REPACK>(a, smem, bars, tbase);
+    // drain: every MMA this thread issued has finished before TMEM is freed
+    tc_commit(bars.drain);
   }
   tc_fence_before();
   __syncthreads();
