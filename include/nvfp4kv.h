@@ -143,6 +143,26 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
                         const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
                         void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The two halves of nvfp4_paged_prefill, for callers that time or overlap
+ * them separately.  nvfp4_paged_prefill_plan writes the work schedule into
+ * the workspace and, in repack mode, the repacked K/V tile records of this
+ * cache; nvfp4_paged_prefill_run launches only the attention kernel, which
+ * reads them.  run must follow plan on the same stream with the same
+ * arguments (the pair computes the same mode from them) and the same
+ * workspace, with the cache unchanged in between; otherwise its result is
+ * undefined.  nvfp4_paged_prefill(...) is plan(...) then run(...).  Arguments
+ * and errors as for nvfp4_paged_prefill (plan takes no q, o, lse or
+ * sm_scale).  Neither allocates. */
+int nvfp4_paged_prefill_plan(int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                             const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                             const int32_t* qo_indptr, int32_t batch, int32_t causal, int32_t variant,
+                             void* workspace, size_t workspace_bytes, void* stream);
+int nvfp4_paged_prefill_run(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                            const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                            const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale,
+                            int32_t variant, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* nvfp4_paged_prefill without a workspace argument, for callers that cannot
  * allocate device memory: an engine that plans all device memory up front and
  * allows no cudaMalloc on its serving path (an allocation can synchronize the

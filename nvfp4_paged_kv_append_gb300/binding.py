@@ -31,7 +31,8 @@ PAGE_SIZE = 16
 EXPORTED = ["nvfp4_kv_append", "nvfp4_paged_prefill", "nvfp4_paged_decode", "nvfp4_workspace_bytes",
             "nvfp4_cache_bytes", "nvfp4_quantize_rows", "nvfp4_dequantize_rows", "nvfp4kv_get_device_status",
             "nvfp4kv_status_string", "nvfp4kv_version", "nvfp4kv_debug_wait_timeout",
-            "nvfp4_paged_prefill_noalloc", "nvfp4_paged_prefill_noalloc_max_bytes"]
+            "nvfp4_paged_prefill_noalloc", "nvfp4_paged_prefill_noalloc_max_bytes",
+            "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run"]
 
 
 class CacheDesc(ctypes.Structure):
@@ -57,6 +58,8 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4_kv_append.argtypes = [P, P, P, i64, D, P]
     lib.nvfp4_paged_prefill.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, P, P, P, sz, P]
     lib.nvfp4_paged_decode.argtypes = [P, i32, D, P, i32, P, i32, f32, P, P, P, sz, P]
+    lib.nvfp4_paged_prefill_plan.argtypes = [i64, i32, D, P, i32, P, P, i32, i32, i32, P, sz, P]
+    lib.nvfp4_paged_prefill_run.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, P, P, P, sz, P]
     lib.nvfp4_paged_prefill_noalloc.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, P, P, P]
     lib.nvfp4_paged_prefill_noalloc_max_bytes.argtypes = []
     lib.nvfp4_paged_prefill_noalloc_max_bytes.restype = sz
@@ -73,6 +76,7 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4kv_debug_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.nvfp4kv_debug_wait_timeout.restype = ctypes.c_int
     for name in ("nvfp4_kv_append", "nvfp4_paged_prefill", "nvfp4_paged_prefill_noalloc", "nvfp4_paged_decode",
+                 "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run",
                  "nvfp4_quantize_rows",
                  "nvfp4_dequantize_rows", "nvfp4kv_get_device_status"):
         getattr(lib, name).restype = ctypes.c_int
@@ -164,6 +168,36 @@ def nvfp4_paged_prefill(q: torch.Tensor, cache: Cache, page_table: torch.Tensor,
         _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
         _ptr(qo_indptr), batch, int(bool(causal)), float(sm_scale), int(variant), _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def nvfp4_paged_prefill_plan(cache: Cache, total_q: int, num_q_heads: int, page_table: torch.Tensor,
+                             kv_lens: torch.Tensor, qo_indptr: torch.Tensor, workspace: torch.Tensor,
+                             causal: bool = True, variant: int = VARIANT_A4Q, stream=None) -> None:
+    """Schedule (and, in repack mode, the repacked tile records) into the workspace."""
+    d = cache.desc()
+    _check("nvfp4_paged_prefill_plan", lib.nvfp4_paged_prefill_plan(
+        total_q, num_q_heads, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+        _ptr(qo_indptr), kv_lens.shape[0], int(bool(causal)), int(variant), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def nvfp4_paged_prefill_run(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, kv_lens: torch.Tensor,
+                            qo_indptr: torch.Tensor, workspace: torch.Tensor, causal: bool = True,
+                            sm_scale: Optional[float] = None, variant: int = VARIANT_A4Q,
+                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """The attention kernel alone, reading the schedule a matching plan call wrote."""
+    total_q, hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if sm_scale is None:
+        sm_scale = HEAD_DIM ** -0.5
+    d = cache.desc()
+    _check("nvfp4_paged_prefill_run", lib.nvfp4_paged_prefill_run(
+        _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+        _ptr(qo_indptr), kv_lens.shape[0], int(bool(causal)), float(sm_scale), int(variant), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
 

@@ -176,10 +176,18 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
   return launch_rc(cudaGetLastError());
 }
 
-int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
-                        const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
-                        const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
-                        void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+enum PrefillStage { kStagePlan = 1, kStageRun = 2 };
+
+// Validates the arguments, fills the kernel argument blocks and launches the
+// requested stages.  q/o/lse/sm_scale are only used by the run stage.
+int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                   const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                   const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant, void* o,
+                   float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_cache(cache);
   if (rc) return rc;
   if (batch < 0 || total_q < 0 || max_pages_per_req <= 0) return NVFP4KV_ERR_ARG;
@@ -188,10 +196,11 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
   if (lg < 0 || lg > 7) return NVFP4KV_ERR_ARG;
   if (causal != 0 && causal != 1) return NVFP4KV_ERR_ARG;
   if (variant != NVFP4KV_VARIANT_A4Q && variant != NVFP4KV_VARIANT_DQ_AHEAD) return NVFP4KV_ERR_ARG;
-  if (!std::isfinite(sm_scale)) return NVFP4KV_ERR_ARG;
+  if ((stages & kStageRun) && !std::isfinite(sm_scale)) return NVFP4KV_ERR_ARG;
   if (total_q * num_q_heads >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
   if (batch == 0 || total_q == 0) return NVFP4KV_OK;
-  if (!q || !o || !page_table || !kv_lens || !qo_indptr || !aligned16(q) || !aligned16(o)) return NVFP4KV_ERR_ARG;
+  if (!page_table || !kv_lens || !qo_indptr) return NVFP4KV_ERR_ARG;
+  if ((stages & kStageRun) && (!q || !o || !aligned16(q) || !aligned16(o))) return NVFP4KV_ERR_ARG;
   const int64_t max_items = prefill_max_items(total_q, batch, num_q_heads, cache->num_kv_heads);
   if (max_items >= (int64_t(1) << 30)) return NVFP4KV_ERR_ARG;
   const size_t sched = prefill_sched_bytes(max_items, batch);
@@ -245,8 +254,45 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
   a.tile_prefix = static_cast<const int*>(workspace) + 4 + 2 * max_items + (batch + 1);
   a.repack = repack ? static_cast<uint8_t*>(workspace) + sched : nullptr;
   a.status = d->status;
-  return launch_rc(launch_prefill(a, plan, variant, repack, d->num_sms, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (stages & kStagePlan) {
+    if ((rc = launch_rc(launch_prefill_plan(a, plan, variant, repack, d->num_sms, st)))) return rc;
+  }
+  if (stages & kStageRun) return launch_rc(launch_prefill_attend(a, variant, repack, d->num_sms, st));
+  return NVFP4KV_OK;
 }
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                        const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                        const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
+                        void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_stages(kStagePlan | kStageRun, q, total_q, num_q_heads, cache, page_table, max_pages_per_req,
+                        kv_lens, qo_indptr, batch, causal, sm_scale, variant, o, lse, workspace, workspace_bytes,
+                        stream);
+}
+
+int nvfp4_paged_prefill_plan(int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                             const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                             const int32_t* qo_indptr, int32_t batch, int32_t causal, int32_t variant,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_stages(kStagePlan, nullptr, total_q, num_q_heads, cache, page_table, max_pages_per_req, kv_lens,
+                        qo_indptr, batch, causal, 0.0f, variant, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+int nvfp4_paged_prefill_run(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+                            const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                            const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale,
+                            int32_t variant, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  return prefill_stages(kStageRun, q, total_q, num_q_heads, cache, page_table, max_pages_per_req, kv_lens,
+                        qo_indptr, batch, causal, sm_scale, variant, o, lse, workspace, workspace_bytes, stream);
+}
+
+
 
 int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t* cache, const int32_t* page_table,
                        int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o,

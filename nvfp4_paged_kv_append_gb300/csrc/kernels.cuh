@@ -127,7 +127,9 @@ __global__ void nvfp4_dequantize_rows_kernel(DequantArgs a);
 
 // Launchers that hide templates (decode.cu / prefill.cu).
 cudaError_t launch_decode(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
-                           cudaStream_t s);
+// Schedule (+ repack pre-pass) and the attention kernel, launched separately.
+cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
+                                cudaStream_t s);
+cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s);
 
 }  // namespace nvfp4kv

@@ -1003,17 +1003,17 @@ cudaError_t launch_main(K kernel, uint32_t smem, const PrefillArgs& a, int num_s
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
-                           cudaStream_t s) {
+cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
+                                cudaStream_t s) {
   nvfp4_prefill_plan_kernel<<<1, 1024, 0, s>>>(plan);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (repack) {
-    if (variant == 0) nvfp4_prefill_repack_kernel<0><<<num_sms * 8, 128, 0, s>>>(a);
-    else nvfp4_prefill_repack_kernel<1><<<num_sms * 8, 128, 0, s>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  if (e != cudaSuccess || !repack) return e;
+  if (variant == 0) nvfp4_prefill_repack_kernel<0><<<num_sms * 8, 128, 0, s>>>(a);
+  else nvfp4_prefill_repack_kernel<1><<<num_sms * 8, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s) {
   if (variant == 0)
     return repack ? launch_main(nvfp4_prefill_a4q_vrepack_sm103_kernel, Layout<0, true>::kAlloc, a, num_sms, s)
                   : launch_main(nvfp4_prefill_a4q_sm103_kernel, Layout<0, false>::kAlloc, a, num_sms, s);

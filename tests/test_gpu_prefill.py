@@ -134,3 +134,25 @@ def test_prefill_bad_page_and_shape_flagged():
                           inp.qo_indptr.to(G.dev()), sm_scale=inp.sm_scale)
     torch.cuda.synchronize()
     assert b.nvfp4kv_get_device_status() == -2
+
+
+@pytest.mark.parametrize("mode", ["auto", "inkernel"])
+@pytest.mark.parametrize("variant", [0, 1])
+def test_plan_then_run_equals_single_call(variant, mode):
+    """nvfp4_paged_prefill_plan + nvfp4_paged_prefill_run produce the same bytes
+    as nvfp4_paged_prefill, in repack and in-kernel mode, and a plan can be
+    reused by several runs over the same cache."""
+    b = G.nk()
+    inp = G.inputs("shortq")
+    cache = G.gpu_cache(inp)
+    d = G.dev()
+    q, pt, kvl, qo = inp.q.to(d), inp.page_table.to(d), inp.kv_lens.to(d), inp.qo_indptr.to(d)
+    ws = G.prefill_workspace(inp, mode)
+    ref = b.nvfp4_paged_prefill(q, cache, pt, kvl, qo, sm_scale=inp.sm_scale, variant=variant, workspace=ws)
+    ws2 = G.prefill_workspace(inp, mode)
+    b.nvfp4_paged_prefill_plan(cache, inp.wl.total_q, inp.wl.num_q_heads, pt, kvl, qo, ws2, variant=variant)
+    for _ in range(2):
+        got = b.nvfp4_paged_prefill_run(q, cache, pt, kvl, qo, ws2, sm_scale=inp.sm_scale, variant=variant)
+        torch.cuda.synchronize()
+        assert b.nvfp4kv_get_device_status() == 0
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
