@@ -305,7 +305,7 @@ def run_ours(args, rank, world, dev):
         "step_breakdown_ms": {"append": round(statistics.mean(app_ms), 4), "prefill": round(statistics.mean(pre_ms), 4),
                               "prefill_plan_and_repack": round(statistics.mean(plan_ms), 4),
                               "prefill_attention": round(statistics.mean(attn_ms), 4)},
-        "roofline": {"bound": "tensor", "kernel": "nvfp4_prefill_a4q_vrepack_sm103_kernel", "achieved": round(achieved, 2),
+        "roofline": {"bound": "tensor", "kernel": "nvfp4_prefill_a4q_2cta_sm103_kernel", "achieved": round(achieved, 2),
                      "peak": round(peak_eff, 2), "unit": "TFLOP/s", "frac": round(achieved / peak_eff, 4),
                      "traffic": prefill_traffic_bytes(),
                      "peak_basis": f"t = F_QK/(bf16 x {FP4_OVER_BF16:g}) + F_PV/bf16 with bf16 = {p16} TFLOP/s "
@@ -479,20 +479,20 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------------- ncu traffic
-# DRAM read + write of one attention launch (nvfp4_prefill_a4q_vrepack_sm103_kernel,
+# DRAM read + write of one attention launch (nvfp4_prefill_a4q_2cta_sm103_kernel,
 # 16K causal, 32/8 heads) from the ncu capture summarised in
 # profiles/prefill_a4q_16k_ncu.md, keyed by the digest of the kernel source it
-# was taken on: once prefill.cu changes the figure no longer describes the
+# was taken on: once that source changes the figure no longer describes the
 # kernel and is reported as null.
-PREFILL_TRAFFIC = {"prefill_cu_sha256_16": "0fc229a80d16c331", "bytes": 177435648 + 94498304}
+PREFILL_TRAFFIC = {"source": "prefill_a4q.cu", "sha256_16": "", "bytes": None}
 
 
 def prefill_traffic_bytes():
     import hashlib
-    src = os.path.join(ROOT, "nvfp4_paged_kv_append_gb300", "csrc", "prefill.cu")
+    src = os.path.join(ROOT, "nvfp4_paged_kv_append_gb300", "csrc", PREFILL_TRAFFIC["source"])
     with open(src, "rb") as f:
         dig = hashlib.sha256(f.read()).hexdigest()[:16]
-    return PREFILL_TRAFFIC["bytes"] if dig == PREFILL_TRAFFIC["prefill_cu_sha256_16"] else None
+    return PREFILL_TRAFFIC["bytes"] if dig == PREFILL_TRAFFIC["sha256_16"] else None
 
 
 # ---------------------------------------------------------------------------- ranks

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libnvfp4kv.so")
-UNITS = ["append", "decode", "prefill", "api", "noalloc"]
+UNITS = ["append", "decode", "prefill", "prefill_a4q", "api", "noalloc"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", ARCH, "-Xcompiler", "-fPIC", "-ftz=false",
               "-prec-div=true", "-prec-sqrt=true", "-I" + INCLUDE, "-I" + CSRC]

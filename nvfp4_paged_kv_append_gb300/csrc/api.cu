@@ -90,16 +90,26 @@ int64_t prefill_max_items(int64_t total_q, int batch, int num_q_heads, int num_k
 }
 
 // Prefill workspace: [16 B header][items: 8 B each][unit prefix][tile prefix]
-// padded to 1 KB, then (repack mode) one record of up to 64 KB for every
-// (request, kv head, KV tile) the batch can hold.
-constexpr size_t kRepackRecordBytes = 65536;
+// padded to 1 KB, then (repack mode) one record for every (request, kv head,
+// KV tile) the batch can hold: 64 KB per 128-key tile for the dequant-ahead
+// kernel, 36 KB per 112-key tile for the A4Q kernel.
+constexpr size_t kRepackRecordBytesDq = 65536;
+size_t prefill_repack_bytes(int variant, int batch, int num_kv_heads, int64_t max_kv_len);
 size_t prefill_sched_bytes(int64_t max_items, int batch) {
   const size_t b = 16 + 8 * static_cast<size_t>(max_items) + 8 * (static_cast<size_t>(batch) + 1);
   return (b + 1023) & ~size_t(1023);
 }
-size_t prefill_repack_tiles(int batch, int num_kv_heads, int64_t max_kv_len) {
+size_t prefill_repack_tiles(int batch, int num_kv_heads, int64_t max_kv_len, int bn) {
   if (max_kv_len <= 0) return 0;
-  return static_cast<size_t>(batch) * num_kv_heads * static_cast<size_t>((max_kv_len + kBN - 1) / kBN);
+  return static_cast<size_t>(batch) * num_kv_heads * static_cast<size_t>((max_kv_len + bn - 1) / bn);
+}
+// Keys per KV tile of the attention kernel that runs (variant, mode).
+int prefill_tile_keys(int variant, bool repack) { return (variant == 0 && repack) ? prefill_a4q_2cta_tile_keys() : kBN; }
+size_t prefill_repack_bytes(int variant, int batch, int num_kv_heads, int64_t max_kv_len) {
+  if (variant == 0)
+    return prefill_a4q_2cta_record_bytes() *
+           prefill_repack_tiles(batch, num_kv_heads, max_kv_len, prefill_a4q_2cta_tile_keys());
+  return kRepackRecordBytesDq * prefill_repack_tiles(batch, num_kv_heads, max_kv_len, kBN);
 }
 
 int launch_rc(cudaError_t e) { return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA; }
@@ -130,8 +140,9 @@ size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int
   if (op == NVFP4KV_OP_PREFILL) {
     if (total_q < 0) return 0;
     const int64_t items = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
-    return prefill_sched_bytes(items, batch) +
-           kRepackRecordBytes * prefill_repack_tiles(batch, num_kv_heads, max_kv_len);
+    const size_t a4q = prefill_repack_bytes(0, batch, num_kv_heads, max_kv_len);
+    const size_t dq = prefill_repack_bytes(1, batch, num_kv_heads, max_kv_len);
+    return prefill_sched_bytes(items, batch) + (a4q > dq ? a4q : dq);
   }
   if (op == NVFP4KV_OP_DECODE) {
     if (max_kv_len < 0) return 0;
@@ -208,9 +219,10 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   // Repack mode (each V tile dequantized once, into the workspace) when the
   // workspace holds a tile for every (request, kv head, KV tile) the page
   // table allows and requests average at least two q tiles per kv head.
-  const size_t rtiles = prefill_repack_tiles(batch, cache->num_kv_heads, static_cast<int64_t>(max_pages_per_req) * kPageSize);
+  const size_t rbytes =
+      prefill_repack_bytes(variant, batch, cache->num_kv_heads, static_cast<int64_t>(max_pages_per_req) * kPageSize);
   const int64_t qtiles = (total_q * (num_q_heads / cache->num_kv_heads) + kBM - 1) / kBM;
-  const bool repack = workspace_bytes >= sched + kRepackRecordBytes * rtiles && qtiles >= 2 * static_cast<int64_t>(batch);
+  const bool repack = workspace_bytes >= sched + rbytes && qtiles >= 2 * static_cast<int64_t>(batch);
   DeviceState* d = nullptr;
   if ((rc = device_state(&d))) return rc;
 
@@ -223,6 +235,7 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   plan.num_kv_heads = cache->num_kv_heads;
   plan.log2_group = lg;
   plan.causal = causal;
+  plan.bn = prefill_tile_keys(variant, repack);
   plan.work = static_cast<int*>(workspace);
   plan.max_items = static_cast<int>(max_items);
   plan.status = d->status;

@@ -5,10 +5,12 @@
 //
 // Split-KV: a work item is (request, kv head, 256-token split).  A small
 // schedule kernel turns kv_lens into per-request item prefixes; then one
-// persistent wave of CTAs (3 per SM) walks the items.  For each item warp 0
-// issues up to 64 bulk copies (K/V codes 1 KB + scales 128 B per page) onto
-// one mbarrier, into one of two shared-memory stages, so the next item's
-// bytes are in flight while the current one is computed.  Four warps take
+// persistent wave of CTAs (3 per SM) walks the items.  For each item all
+// threads gather its pages (K/V codes 1 KB + scales 128 B per page) with
+// cp.async into one of two shared-memory stages, completing on one mbarrier,
+// so the next item's bytes are in flight while the current one is computed.
+// (Per-page bulk copies cost the copy engine a fixed time each, which capped
+// the item rate; cp.async spreads the same bytes over the load units.)  Four warps take
 // 16-token chunks of the item.  The G query heads of the kv group are the
 // M rows of an m16n8k16 f16 MMA: the packed codes are dequantized (exactly,
 // e2m1 x e4m3 fits f16) straight into B-fragment registers, so no dequantized
@@ -97,32 +99,35 @@ __device__ __forceinline__ bool decode_item(const DecodeArgs& a, int idx, DecIte
   return true;
 }
 
-// Warp 0: resolve the item's pages and start their copies into `stage`.
+// All 128 threads gather the item's pages into `stage` with cp.async: thread
+// t serves page t / 8 (K and V codes, 16 B at a time, plus one 16-byte piece
+// of each scale page); a page past the item or with an invalid id is skipped
+// or zero-filled.  Each thread then arrives on `bar` once its copies land.
 __device__ __forceinline__ void issue_item(const DecodeArgs& a, const DecItem& it, uint8_t* stage, uint64_t* bar,
-                                           int* page_ok, int lane) {
-  int pid = -1;
-  if (lane < it.n_pages) {
-    pid = a.page_table[static_cast<int64_t>(it.b) * a.max_pages + it.split * 16 + lane];
+                                           int* page_ok, int tid) {
+  const int p = tid >> 3, sub = tid & 7;
+  if (p < it.n_pages) {
+    int pid = a.page_table[static_cast<int64_t>(it.b) * a.max_pages + it.split * 16 + p];
     if (pid < 0 || pid >= a.num_pages) {
-      set_status(a.status, kDevBadPage);
+      if (sub == 0) set_status(a.status, kDevBadPage);
       pid = -1;
     }
+    if (sub == 0) page_ok[p] = pid >= 0;
+    const uint32_t n16 = pid >= 0 ? 16u : 0u;
+    const int64_t row = (static_cast<int64_t>(pid >= 0 ? pid : 0) * a.num_kv_heads + it.h) * kPageSize;
+    const uint32_t sK = smem_u32(stage), sKs = sK + kSplitBytesK, sV = sKs + kSplitBytesS, sVs = sV + kSplitBytesK;
+    const uint8_t* gk = a.k_data + row * 64;
+    const uint8_t* gv = a.v_data + row * 64;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = sub + 8 * i;
+      cp_async16(sK + p * 1024 + c * 16, gk + c * 16, n16);
+      cp_async16(sV + p * 1024 + c * 16, gv + c * 16, n16);
+    }
+    cp_async16(sKs + p * 128 + sub * 16, a.k_scale + row * 8 + sub * 16, n16);
+    cp_async16(sVs + p * 128 + sub * 16, a.v_scale + row * 8 + sub * 16, n16);
   }
-  if (lane < 16) page_ok[lane] = pid >= 0;
-  const unsigned valid = __ballot_sync(0xffffffffu, pid >= 0);
-  if (lane == 0) mbar_arrive_expect_tx(bar, __popc(valid) * 2u * (1024u + 128u));
-  __syncwarp();
-  if (pid >= 0) {
-    const int64_t row = (static_cast<int64_t>(pid) * a.num_kv_heads + it.h) * kPageSize;
-    uint8_t* sK = stage;
-    uint8_t* sKs = stage + kSplitBytesK;
-    uint8_t* sV = sKs + kSplitBytesS;
-    uint8_t* sVs = sV + kSplitBytesK;
-    bulk_load(sK + lane * 1024, a.k_data + row * 64, 1024, bar);
-    bulk_load(sKs + lane * 128, a.k_scale + row * 8, 128, bar);
-    bulk_load(sV + lane * 1024, a.v_data + row * 64, 1024, bar);
-    bulk_load(sVs + lane * 128, a.v_scale + row * 8, 128, bar);
-  }
+  cp_async_mbar_arrive(bar);
 }
 
 // Persistent: CTA c takes items c, c + grid, ...; two shared-memory stages so
@@ -138,16 +143,14 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    mbar_init(&bars[0], 128);  // one cp.async arrival per thread
+    mbar_init(&bars[1], 128);
     fence_barrier_init();
   }
   __syncthreads();
   DecItem nxt;
-  if (warp == 0) {
-    for (int k = 0; k < 2; ++k)
-      if (decode_item(a, blockIdx.x + k * gridDim.x, nxt)) issue_item(a, nxt, dsmem + k * kStageBytes, &bars[k], page_ok_sh[k], lane);
-  }
+  for (int k = 0; k < 2; ++k)
+    if (decode_item(a, blockIdx.x + k * gridDim.x, nxt)) issue_item(a, nxt, dsmem + k * kStageBytes, &bars[k], page_ok_sh[k], tid);
   DecItem it;
   for (int k = 0; decode_item(a, blockIdx.x + k * gridDim.x, it); ++k) {
     const int stg = k & 1;
@@ -348,12 +351,9 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
         if (d == 0) a.part_lse[pi] = lse2;
       }
     }
-    // This stage was written through the generic proxy (zeroed scales, merge
-    // scratch) and is refilled next by bulk copies (async proxy).
-    fence_proxy_async_smem();
     __syncthreads();  // every thread is done with this stage
-    if (warp == 0 && decode_item(a, blockIdx.x + (k + 2) * gridDim.x, nxt))
-      issue_item(a, nxt, dsmem + stg * kStageBytes, &bars[stg], page_ok_sh[stg], lane);
+    if (decode_item(a, blockIdx.x + (k + 2) * gridDim.x, nxt))
+      issue_item(a, nxt, dsmem + stg * kStageBytes, &bars[stg], page_ok_sh[stg], tid);
   }
 }
 

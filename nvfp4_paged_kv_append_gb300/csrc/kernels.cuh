@@ -115,6 +115,7 @@ struct PlanArgs {
   int num_kv_heads;
   int log2_group;
   int causal;
+  int bn;     // keys per KV tile of the attention kernel the schedule is for
   int* work;  // output schedule
   int max_items;
   int* status;
@@ -131,5 +132,10 @@ cudaError_t launch_decode(const DecodeArgs& a, int batch, int num_sms, cudaStrea
 cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s);
+// A4Q in repack mode: two CTAs per SM, 112-key tiles (prefill_a4q.cu).
+size_t prefill_a4q_2cta_record_bytes();
+int prefill_a4q_2cta_tile_keys();
+cudaError_t launch_prefill_a4q_2cta_repack(const PrefillArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill_a4q_2cta(const PrefillArgs& a, int num_sms, cudaStream_t s);
 
 }  // namespace nvfp4kv

@@ -35,17 +35,14 @@
 //
 // PV runs on FP16 operands: every dequantized V value (E2M1 x E4M3) is exact
 // in FP16 (and in BF16), while FP16 keeps 3 more mantissa bits of P.
-#include "kernels.cuh"
+#include "prefill_common.cuh"
 
 namespace nvfp4kv {
 
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-// log2 units: a row's running max moves (and O is rescaled) only when a tile
-// exceeds it by more than this, so P stays <= 2^15, inside FP16's range.
-constexpr float kRescaleThreshold = 15.0f;
+using namespace prefill_detail;
+
 
 // warps 0 QK issue (and TMEM allocation), 1-2 loaders, 3 PV issue, 4-7
 // transform, 8-11 softmax half 0, 12-15 softmax half 1.  A warp reaches only
@@ -140,99 +137,6 @@ __device__ __forceinline__ Bars make_bars(uint64_t* base) {
   return b;
 }
 
-struct Item {
-  int b, qt, kvh;
-  int q_start, q_len, kv_len;
-  int tok0, n_tok, n_tiles;
-};
-
-// Items are sorted by decreasing cost; CTAs take them in snake order.
-__device__ __forceinline__ bool get_item(const PrefillArgs& a, int round, Item& it) {
-  const int n_items = a.work[0];
-  const int grid = gridDim.x;
-  const int idx = round * grid + ((round & 1) ? (grid - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
-  if (idx >= n_items) return false;
-  const int2 w = reinterpret_cast<const int2*>(a.work + 4)[idx];
-  it.b = w.x;
-  it.qt = w.y >> 8;
-  it.kvh = w.y & 255;
-  it.q_start = a.qo_indptr[it.b];
-  it.q_len = a.qo_indptr[it.b + 1] - it.q_start;
-  it.kv_len = a.kv_lens[it.b];
-  const int tpq = kBM >> a.log2_group;
-  it.tok0 = it.qt * tpq;
-  it.n_tok = min(tpq, it.q_len - it.tok0);
-  const int last_key = a.causal ? it.kv_len - it.q_len + it.tok0 + it.n_tok - 1 : it.kv_len - 1;
-  it.n_tiles = last_key / kBN + 1;
-  return true;
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// 16-byte chunk `cc` (0..7) of row `r` in a 128B-swizzled [rows][128 B] tile.
-__device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t cc) { return r * 128u + (((cc ^ r) & 7u) << 4); }
-
-// Store the four 16-byte chunks o0..o3 of one (key, 32-value group c) unit
-// into a 128B-swizzled operand tile.  Lanes holding groups 2-3 store their
-// chunks in the order 2,3,0,1 so that every 8-lane phase of a warp-wide
-// shared-memory store hits 8 different bank groups.
-__device__ __forceinline__ void store_unit_sw128(uint8_t* tile, int key, int c, const uint32_t (&o0)[4],
-                                                 const uint32_t (&o1)[4], const uint32_t (&o2)[4],
-                                                 const uint32_t (&o3)[4]) {
-  uint8_t* dst = tile + (c >> 1) * 16384;
-  const uint32_t cc = (c & 1) * 4;
-  const bool rot = (c >> 1) != 0;
-  const uint4 a0 = make_uint4(o0[0], o0[1], o0[2], o0[3]), a1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-  const uint4 a2 = make_uint4(o2[0], o2[1], o2[2], o2[3]), a3 = make_uint4(o3[0], o3[1], o3[2], o3[3]);
-  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 2 : 0))) = rot ? a2 : a0;
-  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 3 : 1))) = rot ? a3 : a1;
-  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 0 : 2))) = rot ? a0 : a2;
-  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 1 : 3))) = rot ? a1 : a3;
-}
-
-// 16-byte chunk `c` (0..3) of row `r` in a 64B-swizzled [rows][64 B] tile.
-__device__ __forceinline__ uint32_t sw64_off(uint32_t r, uint32_t c) { return r * 64u + (((c ^ (r >> 1)) & 3u) << 4); }
-
-// Dequantize 32 values (16 code bytes, two 16-value blocks) of one row.
-template <bool BF16>
-__device__ __forceinline__ void dequant_unit(uint4 src, uint32_t sc01, uint32_t (&o0)[4], uint32_t (&o1)[4],
-                                             uint32_t (&o2)[4], uint32_t (&o3)[4]) {
-  if (BF16) {
-    const uint32_t s0 = scale_bf16x2_x2p112(sc01 & 0xFFu), s1 = scale_bf16x2_x2p112(sc01 >> 8);
-    dequant8_bf16(src.x, s0, o0);
-    dequant8_bf16(src.y, s0, o1);
-    dequant8_bf16(src.z, s1, o2);
-    dequant8_bf16(src.w, s1, o3);
-  } else {
-    const uint32_t s0 = scale_f16x2(sc01 & 0xFFu), s1 = scale_f16x2(sc01 >> 8);
-    dequant8_f16(src.x, s0, o0);
-    dequant8_f16(src.y, s0, o1);
-    dequant8_f16(src.z, s1, o2);
-    dequant8_f16(src.w, s1, o3);
-  }
-}
-
-// Index of the repacked tile (request b, kv head h, KV tile j).
-__device__ __forceinline__ int64_t repack_index(const PrefillArgs& a, int b, int h, int j) {
-  const int p0 = a.tile_prefix[b], n_t = a.tile_prefix[b + 1] - p0;
-  return static_cast<int64_t>(p0) * a.num_kv_heads + static_cast<int64_t>(h) * n_t + j;
-}
-
 // ---------------------------------------------------------------------------
 // loader warps (12 and 14): t = 0..63.  In-kernel mode, thread t gathers a
 // slice of page p = t / 8 of the tile with cp.async; a page past kv_len (or
@@ -244,7 +148,7 @@ __device__ void loader_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bar
   const int p = t >> 3, sub = t & 7;
   uint32_t it_ctr = 0;
   Item item;
-  for (int round = 0; get_item(a, round, item); ++round) {
+  for (int round = 0; get_item<kBN>(a, round, item); ++round) {
     for (int j = 0; j < item.n_tiles; ++j, ++it_ctr) {
       const uint32_t st = it_ctr % L::kStages, ph = (it_ctr / L::kStages) & 1u;
       uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
@@ -314,7 +218,7 @@ __device__ void qk_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
   const uint32_t idesc_qk = L::kA4Q ? idesc_mxf4nvf4(128, 128) : idesc_f16(128, 128, 1, 1, 0, 0);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
-  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item<kBN>(a, round, item); ++round, ++item_ctr) {
     if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
     for (int j = 0; j < item.n_tiles; ++j) {
       const uint32_t it = it_ctr + j;
@@ -365,7 +269,7 @@ __device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
   const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
-  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item<kBN>(a, round, item); ++round, ++item_ctr) {
     for (int j = 0; j < item.n_tiles; ++j) {
       const uint32_t it = it_ctr + j;
       const uint32_t st = it % L::kStages, b = it & 1u, ph = (it >> 1) & 1u;
@@ -401,7 +305,7 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
   uint2* sfa_stage = reinterpret_cast<uint2*>(smem + L::kOffSfaStage);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
-  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item<kBN>(a, round, item); ++round, ++item_ctr) {
     // The previous item's Q tile, Q block scales and row scales must be
     // consumed (last QK issued and finished; softmax has read its row scales)
     // before they are overwritten.  Waiting on both also keeps the softmax
@@ -417,49 +321,8 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) +
                                                         (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim);
       if constexpr (L::kA4Q) {
-        // pass 1: row amax (the row stays in L1 for pass 2)
-        float amax = 0.0f;
-        if (valid) {
-#pragma unroll 4
-          for (int i = 0; i < 16; ++i) {
-            const uint4 v = src[i];
-            const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float lo, hi;
-              bf16x2_to_f32(ww[k], lo, hi);
-              amax = fmax3(amax, fabsf(lo), fabsf(hi));
-            }
-          }
-        }
-        const float g_row = __fdiv_rn(amax, 2688.0f);
-        // pass 2: per 32-value chunk (two blocks) -> 16 code bytes, 2 scales
-        uint8_t* qrow = smem + L::kOffQ;
-        uint32_t sc[8];
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t cw[4] = {0u, 0u, 0u, 0u};
-          sc[2 * c] = sc[2 * c + 1] = 0u;
-          if (valid && g_row != 0.0f) {
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-              const uint4 v0 = src[4 * c + 2 * blk], v1 = src[4 * c + 2 * blk + 1];
-              float x[16];
-              bf16x2_to_f32(v0.x, x[0], x[1]);
-              bf16x2_to_f32(v0.y, x[2], x[3]);
-              bf16x2_to_f32(v0.z, x[4], x[5]);
-              bf16x2_to_f32(v0.w, x[6], x[7]);
-              bf16x2_to_f32(v1.x, x[8], x[9]);
-              bf16x2_to_f32(v1.y, x[10], x[11]);
-              bf16x2_to_f32(v1.z, x[12], x[13]);
-              bf16x2_to_f32(v1.w, x[14], x[15]);
-              sc[2 * c + blk] = quant_block16(x, g_row, cw[2 * blk], cw[2 * blk + 1]);
-            }
-          }
-          *reinterpret_cast<uint4*>(qrow + sw64_off(r, c)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        }
-        sfa_stage[r] = make_uint2(sc[0] | (sc[1] << 8) | (sc[2] << 16) | (sc[3] << 24),
-                                  sc[4] | (sc[5] << 8) | (sc[6] << 16) | (sc[7] << 24));
+        float g_row;
+        sfa_stage[r] = quantize_q_row(src, valid, smem + L::kOffQ, r, g_row);
         qscale[r] = g_row;
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.sfa_ready);
@@ -573,7 +436,7 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
     tc_fence_after();
     return ok;
   };
-  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item<kBN>(a, round, item); ++round, ++item_ctr) {
     if (!mbar_wait_warp(bars.q_full, item_ctr & 1u, a.status)) return;
     const int tq = item.tok0 + (r >> lg);
     const bool valid = (r >> lg) < item.n_tok;
@@ -776,13 +639,10 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a) {
 }
 
 // Kernel names carry the variant and the V path, so a trace shows which ran.
+// (A4Q in repack mode runs the two-CTA kernel of prefill_a4q.cu.)
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_prefill_a4q_sm103_kernel(const PrefillArgs a) {
   prefill_body<0, false>(a);
-}
-__global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_prefill_a4q_vrepack_sm103_kernel(const PrefillArgs a) {
-  prefill_body<0, true>(a);
 }
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_prefill_dqahead_sm103_kernel(const PrefillArgs a) {
@@ -922,7 +782,7 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
         set_status(a.status, kDevBadShape);
       } else if (q_len > 0) {
         cnt = ((q_len + (1 << tpq_shift) - 1) >> tpq_shift) * a.num_kv_heads;
-        tiles = max(1, (kv_len + kBN - 1) / kBN);
+        tiles = max(1, (kv_len + a.bn - 1) / a.bn);
       }
     }
     const int incl = block_inclusive_scan(cnt, warp_sums);
@@ -960,7 +820,7 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
     const int tok0 = qt << tpq_shift;
     const int n_tok = min(1 << tpq_shift, q_len - tok0);
     const int last_key = a.causal ? kv_len - q_len + tok0 + n_tok - 1 : kv_len - 1;
-    return min(last_key / kBN + 1, kMaxCostBins - 1);
+    return min(last_key / a.bn + 1, kMaxCostBins - 1);
   };
   // 2) histogram of costs
   for (int u = tid; u < total; u += blockDim.x) {
@@ -1008,14 +868,14 @@ cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int 
   nvfp4_prefill_plan_kernel<<<1, 1024, 0, s>>>(plan);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !repack) return e;
-  if (variant == 0) nvfp4_prefill_repack_kernel<0><<<num_sms * 8, 128, 0, s>>>(a);
-  else nvfp4_prefill_repack_kernel<1><<<num_sms * 8, 128, 0, s>>>(a);
+  if (variant == 0) return launch_prefill_a4q_2cta_repack(a, num_sms, s);
+  nvfp4_prefill_repack_kernel<1><<<num_sms * 8, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s) {
   if (variant == 0)
-    return repack ? launch_main(nvfp4_prefill_a4q_vrepack_sm103_kernel, Layout<0, true>::kAlloc, a, num_sms, s)
+    return repack ? launch_prefill_a4q_2cta(a, num_sms, s)
                   : launch_main(nvfp4_prefill_a4q_sm103_kernel, Layout<0, false>::kAlloc, a, num_sms, s);
   return repack ? launch_main(nvfp4_prefill_dqahead_repack_sm103_kernel, Layout<1, true>::kAlloc, a, num_sms, s)
                 : launch_main(nvfp4_prefill_dqahead_sm103_kernel, Layout<1, false>::kAlloc, a, num_sms, s);

@@ -1,0 +1,436 @@
+// A4Q paged prefill, repack mode, two CTAs per SM ("NVFP4 KV cache A4Q
+// prefill explained", sections "Quantize Q instead of expanding K" and
+// "Compare A4Q with dequantize-ahead repacking").
+//
+// Same method as prefill.cu (per-row NVFP4 Q, block-scaled FP4 QK on the
+// cache's own codes and scales, online softmax, FP16 PV on V converted once
+// per tile), arranged so that two independent CTAs share each SM.  Each CTA
+// owns one 128-row q tile at a time and 256 TMEM columns:
+//
+//   S (columns 0-111, fp32; P as FP16 pairs written back over 0-55),
+//   Q block scales (112-119), K block scales (120-127), O (128-255, fp32)
+//
+// which is why a KV tile is 112 keys (7 pages).  Inside a CTA the work of one
+// tile is a strict chain -- QK, softmax, PV, then the next QK may overwrite
+// S -- but the other CTA's chain runs in the gaps: while one softmax works,
+// the tensor core serves the other CTA.  A softmax thread owns one whole row
+// (112 keys), so no row statistics are exchanged between warps.
+//
+//   warp 0 lane 0   TMEM allocation; every MMA: tcgen05.cp of the tile's K
+//                   scale atoms, QK (kind::mxf4nvf4, N = 112), PV (kind::f16,
+//                   P from TMEM, K = 112)
+//   warp 1 lane 0   one bulk copy per tile of the repacked record
+//   warps 4-7       thread = row: Q quantization at each item start, the
+//                   softmax of every tile, the epilogue
+#include "prefill_common.cuh"
+
+namespace nvfp4kv {
+
+namespace {
+
+using namespace prefill_detail;
+
+constexpr int kBN2 = 112;
+constexpr int kThreads2 = 256;
+constexpr int kStages2 = 2;
+constexpr uint32_t kCols2 = 256;
+constexpr uint32_t kColS2 = 0, kColSFA2 = 112, kColSFB2 = 120, kColO2 = 128;
+constexpr uint32_t kKCodes2 = kBN2 * 64;                         // 7 KB, 64B-swizzled rows
+constexpr uint32_t kKAtoms2 = 1024;                              // two 512-byte scale atoms
+constexpr uint32_t kVChunk2 = kBN2 * 128;                        // 64 head dims x 112 keys, FP16
+constexpr uint32_t kRecord2 = kKCodes2 + kKAtoms2 + 2 * kVChunk2;  // 36 KB
+static_assert(kRecord2 % 1024 == 0 && (kKCodes2 + kKAtoms2) % 1024 == 0, "1 KB aligned operands");
+
+// per-thread register budgets: issue/loader warpgroup and softmax warpgroup
+constexpr uint32_t kRegsIssue2 = 56, kRegsSoftmax2 = 200;
+static_assert(128 * (kRegsIssue2 + kRegsSoftmax2) <= kThreads2 * 128, "register budgets exceed the launch");
+
+// shared memory
+constexpr uint32_t kOffQ2 = 0;                                   // 8 KB FP4 Q tile
+constexpr uint32_t kOffStage2 = 8192;
+constexpr uint32_t kOffSfa2 = kOffStage2 + kStages2 * kRecord2;  // [128] uint2 Q scale words
+constexpr uint32_t kOffBar2 = kOffSfa2 + 1024;
+constexpr uint32_t kNumBars2 = 16;
+constexpr uint32_t kOffSlot2 = kOffBar2 + kNumBars2 * 8;
+constexpr uint32_t kAlloc2 = kOffSlot2 + 16 + 1024;              // + slack for 1 KB alignment
+static_assert(2 * kAlloc2 <= 228 * 1024, "two CTAs per SM");
+
+struct Bars2 {
+  uint64_t* kv_full;   // [2]
+  uint64_t* kv_empty;  // [2]
+  uint64_t* s_full;    // S of the current tile is in TMEM
+  uint64_t* p_full;    // P written over S (4 softmax warps)
+  uint64_t* pv_done;   // PV of the current tile finished: S/P, O and the stage are free
+  uint64_t* q_full;    // Q tile and its scales ready (4 softmax warps)
+  uint64_t* q_empty;   // last QK of the item finished
+  uint64_t* o_empty;   // the epilogue has read O (4 softmax warps)
+  uint64_t* sfa_ready; // the item's Q scale words are staged (4 softmax warps)
+  uint64_t* drain;
+};
+
+__device__ __forceinline__ Bars2 make_bars2(uint64_t* base) {
+  Bars2 b;
+  b.kv_full = base + 0;
+  b.kv_empty = base + 2;
+  b.s_full = base + 4;
+  b.p_full = base + 5;
+  b.pv_done = base + 6;
+  b.q_full = base + 7;
+  b.q_empty = base + 8;
+  b.o_empty = base + 9;
+  b.sfa_ready = base + 10;
+  b.drain = base + 11;
+  return b;
+}
+
+// ---------------------------------------------------------------------------
+// MMA thread.  Per tile: QK (after the previous PV released S), then PV once
+// the softmax has written P.
+__device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, const Bars2& bars, uint32_t tbase) {
+  const uint32_t q_s = smem_u32(smem + kOffQ2);
+  const uint32_t idesc_qk = idesc_mxf4nvf4(128, kBN2);
+  const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
+  uint32_t it = 0, item_ctr = 0;
+  Item item;
+  for (int round = 0; get_item<kBN2>(a, round, item); ++round, ++item_ctr) {
+    if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
+    for (int j = 0; j < item.n_tiles; ++j, ++it) {
+      const uint32_t st = it % kStages2;
+      const uint32_t stage_s = smem_u32(smem + kOffStage2 + st * kRecord2);
+      if (!mbar_wait(&bars.kv_full[st], (it / kStages2) & 1u, a.status)) return;
+      if (it > 0 && !mbar_wait(bars.pv_done, (it - 1) & 1u, a.status)) return;
+      tc_fence_after();
+      const uint32_t at_s = stage_s + kKCodes2;
+      tc_cp_32x128b_warpx4(tbase + kColSFB2, smem_desc(at_s, 0, 128, kSwzNone));
+      tc_cp_32x128b_warpx4(tbase + kColSFB2 + 4, smem_desc(at_s + 512, 0, 128, kSwzNone));
+#pragma unroll
+      for (uint32_t s = 0; s < 2; ++s) {
+        mma_nvf4_ss(tbase + kColS2, smem_desc(q_s + 32 * s, 16, 512, kSwz64),
+                    smem_desc(stage_s + 32 * s, 16, 512, kSwz64), idesc_qk, tbase + kColSFA2 + 4 * s,
+                    tbase + kColSFB2 + 4 * s, s > 0 ? 1u : 0u);
+      }
+      tc_commit(bars.s_full);
+      if (j == item.n_tiles - 1) tc_commit(bars.q_empty);
+      if (!mbar_wait(bars.p_full, it & 1u, a.status)) return;
+      // the item's first PV overwrites O: the previous epilogue must have read it
+      if (j == 0 && !mbar_wait(bars.o_empty, (item_ctr & 1u) ^ 1u, a.status)) return;
+      tc_fence_after();
+      const uint32_t v_s = stage_s + kKCodes2 + kKAtoms2;
+#pragma unroll
+      for (uint32_t k = 0; k < kBN2 / 16; ++k) {
+        mma_f16_ts(tbase + kColO2, tbase + kColS2 + 8 * k, smem_desc(v_s + k * 2048, kVChunk2, 1024, kSwz128),
+                   idesc_pv, (j == 0 && k == 0) ? 0u : 1u);
+      }
+      tc_commit(bars.pv_done);
+      tc_commit(&bars.kv_empty[st]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Loader thread: one bulk copy per tile.
+__device__ __forceinline__ void load_thread(const PrefillArgs& a, uint8_t* smem, const Bars2& bars) {
+  uint32_t it = 0;
+  Item item;
+  for (int round = 0; get_item<kBN2>(a, round, item); ++round) {
+    for (int j = 0; j < item.n_tiles; ++j, ++it) {
+      const uint32_t st = it % kStages2;
+      if (!mbar_wait(&bars.kv_empty[st], ((it / kStages2) & 1u) ^ 1u, a.status)) return;
+      mbar_arrive_expect_tx(&bars.kv_full[st], kRecord2);
+      bulk_load(smem + kOffStage2 + st * kRecord2, a.repack + repack_index(a, item.b, item.kvh, j) * kRecord2,
+                kRecord2, &bars.kv_full[st]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Softmax warpgroup: thread r = TMEM lane r = row r of the q tile.
+__device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem, const Bars2& bars, uint32_t tbase,
+                                             int r) {
+  const int quad = r >> 5, lane = r & 31;
+  const int G = a.group, lg = a.log2_group;
+  uint2* sfa_stage = reinterpret_cast<uint2*>(smem + kOffSfa2);
+  const uint32_t lane_base = tmem_addr(tbase, 32 * quad, 0);
+  uint32_t it = 0, item_ctr = 0;
+  Item item;
+  for (int round = 0; get_item<kBN2>(a, round, item); ++round, ++item_ctr) {
+    const int tq = item.tok0 + (r >> lg);
+    const bool valid = (r >> lg) < item.n_tok;
+    const int hq = item.kvh * G + (r & (G - 1));
+    const int limit = !valid ? -1 : (a.causal ? item.kv_len - item.q_len + tq : item.kv_len - 1);
+    // ---- Q tile: the previous item's last QK must have finished reading it
+    if (item_ctr > 0 && !mbar_wait_warp(bars.q_empty, (item_ctr - 1) & 1u, a.status)) return;
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) +
+                                                      (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) *
+                                                          kHeadDim);
+    float g_row;
+    sfa_stage[r] = quantize_q_row(src, valid, smem + kOffQ2, r, g_row);
+    const float c_r = g_row * a.k_g * a.sm_scale * kLog2e;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.sfa_ready);
+    if (!mbar_wait_warp(bars.sfa_ready, item_ctr & 1u, a.status)) return;
+    // Q block scales -> TMEM: lane i of each quadrant, column 4s+j holds the
+    // four scales of k-step s for row 32j+i (replicated per quadrant)
+    {
+      uint32_t va[8];
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint2 v = sfa_stage[32 * j + lane];
+          va[4 * s2 + j] = s2 ? v.y : v.x;
+        }
+      tmem_st8(lane_base + kColSFA2, va);
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.q_full);
+
+    float m_run = -INFINITY;
+    float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+    for (int j = 0; j < item.n_tiles; ++j, ++it) {
+      if (!mbar_wait_warp(bars.s_full, it & 1u, a.status)) return;
+      tc_fence_after();
+      uint32_t sr[kBN2];
+      tmem_ld32(lane_base + kColS2, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(lane_base + kColS2 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(lane_base + kColS2 + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+      tmem_ld16(lane_base + kColS2 + 96, *reinterpret_cast<uint32_t(*)[16]>(&sr[96]));
+      tmem_wait_ld();
+      float* s = reinterpret_cast<float*>(sr);
+      const int key0 = j * kBN2;
+      if (key0 + kBN2 - 1 > limit) {
+#pragma unroll
+        for (int c = 0; c < kBN2; ++c) s[c] = (key0 + c > limit) ? -INFINITY : s[c];
+      }
+      // row maximum over the raw scores (c_r > 0 commutes with the maximum)
+      float mxq[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float* sq = s + 28 * q4;
+        float m = fmax3(sq[0], sq[1], sq[2]);
+#pragma unroll
+        for (int c = 3; c < 27; c += 2) m = fmax3(m, sq[c], sq[c + 1]);
+        mxq[q4] = fmaxf(m, sq[27]);
+      }
+      const float m_tile = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]) * c_r;
+      // Lazy rescale: the running max moves only when the tile exceeds it by
+      // more than 2^15 (P stays inside FP16).  O is stable here: this QK was
+      // issued after the previous PV finished.
+      const bool need = m_tile > m_run + kRescaleThreshold;
+      float alpha = 1.0f;
+      if (need) {
+        alpha = fast_exp2(m_run - m_tile);  // 0 when m_run = -inf
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lacc[i] = __fmul2_rn(lacc[i], a2);
+        m_run = m_tile;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(lane_base + kColO2 + 32 * c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st16(lane_base + kColO2 + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+          tmem_st16(lane_base + kColO2 + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+        }
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+      const float2 cs2 = make_float2(c_r, c_r), nm2 = make_float2(-m_use, -m_use);
+      uint32_t pk[kBN2 / 2];
+#pragma unroll
+      for (int c = 0; c < kBN2 / 2; ++c) {
+        const float2 t = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), cs2, nm2);
+        const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+        lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
+        pk[c] = pack_f16x2(p.x, p.y);
+      }
+      // P over the first 56 columns of S (already read into registers)
+      tmem_st16(lane_base + kColS2, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      tmem_st16(lane_base + kColS2 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      tmem_st16(lane_base + kColS2 + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
+      tmem_st8(lane_base + kColS2 + 48, *reinterpret_cast<uint32_t(*)[8]>(&pk[48]));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.p_full);
+    }
+    // ---- epilogue: O * v_scale / l -------------------------------------------
+    const float l_run = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y) + (lacc[2].x + lacc[2].y) +
+                        (lacc[3].x + lacc[3].y);
+    if (!mbar_wait_warp(bars.pv_done, (it - 1) & 1u, a.status)) return;
+    tc_fence_after();
+    const float inv_l = (l_run > 0.0f) ? a.v_g / l_run : 0.0f;
+    __nv_bfloat16* orow =
+        reinterpret_cast<__nv_bfloat16*>(a.o) + (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ov[32];
+      tmem_ld32(lane_base + kColO2 + 32 * c, ov);
+      tmem_wait_ld();
+      if (valid) {
+        uint32_t pb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+          pb[i] = *reinterpret_cast<uint32_t*>(&v);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+        dst[0] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+        dst[1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+        dst[2] = make_uint4(pb[8], pb[9], pb[10], pb[11]);
+        dst[3] = make_uint4(pb[12], pb[13], pb[14], pb[15]);
+      }
+    }
+    if (valid && a.lse)
+      a.lse[static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq] =
+          (l_run > 0.0f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.o_empty);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads2, 2) nvfp4_prefill_a4q_2cta_sm103_kernel(const PrefillArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Bars2 bars = make_bars2(reinterpret_cast<uint64_t*>(smem + kOffBar2));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot2);
+  if (tid == 0) {
+    for (int i = 0; i < kStages2; ++i) {
+      mbar_init(&bars.kv_full[i], 1);
+      mbar_init(&bars.kv_empty[i], 1);
+    }
+    mbar_init(bars.s_full, 1);
+    mbar_init(bars.p_full, 4);
+    mbar_init(bars.pv_done, 1);
+    mbar_init(bars.q_full, 4);
+    mbar_init(bars.q_empty, 1);
+    mbar_init(bars.o_empty, 4);
+    mbar_init(bars.sfa_ready, 4);
+    mbar_init(bars.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kCols2);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  // Register budgets (launched with 128 per thread): warps 0-3 give up to 56,
+  // the softmax warpgroup takes 200; 128 x (56 + 200) = 32,768 = 256 x 128.
+  if (warp >= 4) {
+    regs_inc<kRegsSoftmax2>();
+    softmax_rows(a, smem, bars, tbase, tid - 128);
+  } else {
+    regs_dec<kRegsIssue2>();
+    if (warp == 0 && lane == 0) {
+      mma_thread(a, smem, bars, tbase);
+      tc_commit(bars.drain);  // every MMA of this thread has finished before TMEM is freed
+    } else if (warp == 1 && lane == 0) {
+      load_thread(a, smem, bars);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) mbar_wait(bars.drain, 0, a.status);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, kCols2);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Repack pre-pass for this kernel: each (request, kv head, 112-key tile) once
+// -> one 36 KB record laid out exactly like a stage: K codes (64B-swizzled
+// rows), K scale atoms (rows past 112 zero), V as FP16 in the MN-major
+// 128B-swizzled operand layout (two chunks of 64 head dims x 112 keys).  Keys
+// past kv_len are zeros.
+__global__ void __launch_bounds__(128) nvfp4_prefill_repack112_kernel(PrefillArgs a) {
+  const int tid = threadIdx.x;
+  const int total = a.work[1];
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    int lo = 0, hi = a.batch - 1;  // last b with tile_prefix[b] * Hkv <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.tile_prefix[mid] * a.num_kv_heads <= t) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int n_t = a.tile_prefix[b + 1] - a.tile_prefix[b];
+    const int rr = t - a.tile_prefix[b] * a.num_kv_heads;
+    const int h = rr / n_t, j = rr - h * n_t;
+    const int kv_len = a.kv_lens[b];
+    uint8_t* rec = a.repack + static_cast<int64_t>(t) * kRecord2;
+    auto row_of = [&](int key) -> int64_t {
+      const int abs_key = j * kBN2 + key;
+      if (key >= kBN2 || abs_key >= kv_len) return -1;
+      const int pid = a.page_table[static_cast<int64_t>(b) * a.max_pages + (abs_key >> 4)];
+      if (pid < 0 || pid >= a.num_pages) {
+        set_status(a.status, kDevBadPage);
+        return -1;
+      }
+      return (static_cast<int64_t>(pid) * a.num_kv_heads + h) * kPageSize + (abs_key & 15);
+    };
+    // K codes: 112 rows x 4 chunks of 16 B
+    for (int u = tid; u < kBN2 * 4; u += 128) {
+      const int key = u >> 2, c = u & 3;
+      const int64_t row = row_of(key);
+      const uint4 v = row >= 0 ? *reinterpret_cast<const uint4*>(a.k_data + row * 64 + 16 * c) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(rec + sw64_off(key, c)) = v;
+    }
+    // K scale atoms: 128 rows (rows past 112 zero) x 2 k-steps
+    for (int u = tid; u < 256; u += 128) {
+      const int key = u >> 1, ks = u & 1;
+      const int64_t row = row_of(key);
+      const uint32_t w = row >= 0 ? *reinterpret_cast<const uint32_t*>(a.k_scale + row * 8 + 4 * ks) : 0u;
+      *reinterpret_cast<uint32_t*>(rec + kKCodes2 + ks * 512 + (key & 31) * 16 + (key >> 5) * 4) = w;
+    }
+    // V: 112 keys x 4 groups of 32 values -> FP16, MN-major 128B-swizzled
+    uint8_t* vt = rec + kKCodes2 + kKAtoms2;
+    for (int u = tid; u < kBN2 * 4; u += 128) {
+      const int key = u >> 2, c = u & 3;
+      const int64_t row = row_of(key);
+      uint32_t o0[4] = {0, 0, 0, 0}, o1[4] = {0, 0, 0, 0}, o2[4] = {0, 0, 0, 0}, o3[4] = {0, 0, 0, 0};
+      if (row >= 0) {
+        const uint4 src = *reinterpret_cast<const uint4*>(a.v_data + row * 64 + 16 * c);
+        const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(a.v_scale + row * 8 + 2 * c);
+        dequant_unit<false>(src, sc01, o0, o1, o2, o3);
+      }
+      uint8_t* d = vt + (c >> 1) * kVChunk2;
+      const uint32_t cc = (c & 1) * 4;
+      *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 0)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+      *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 1)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 2)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+      *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 3)) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+    }
+  }
+}
+
+}  // namespace
+
+size_t prefill_a4q_2cta_record_bytes() { return kRecord2; }
+int prefill_a4q_2cta_tile_keys() { return kBN2; }
+
+cudaError_t launch_prefill_a4q_2cta_repack(const PrefillArgs& a, int num_sms, cudaStream_t s) {
+  nvfp4_prefill_repack112_kernel<<<num_sms * 8, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_a4q_2cta(const PrefillArgs& a, int num_sms, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(nvfp4_prefill_a4q_2cta_sm103_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc2);
+  if (e != cudaSuccess) return e;
+  nvfp4_prefill_a4q_2cta_sm103_kernel<<<2 * num_sms, kThreads2, kAlloc2, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4kv

@@ -120,6 +120,20 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// ---- per-warpgroup register budgets -------------------------------------------
+// Every warp of a warpgroup executes the same call, and the code that relies
+// on a budget follows the call in the same branch.  The budgets of all
+// warpgroups must add up to no more than the registers the block was launched
+// with, or an increase waits forever.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- async proxy fences --------------------------------------------------------
 // Generic-proxy shared-memory writes made visible to the async proxy (tensor
 // core / TMA) before a barrier hand-off.
