@@ -10,16 +10,24 @@
 // cp.async into one of two shared-memory stages, completing on one mbarrier,
 // so the next item's bytes are in flight while the current one is computed.
 // (Per-page bulk copies cost the copy engine a fixed time each, which capped
-// the item rate; cp.async spreads the same bytes over the load units.)  Four warps take
-// 16-token chunks of the item.  The G query heads of the kv group are the
-// M rows of an m16n8k16 f16 MMA: the packed codes are dequantized (exactly,
-// e2m1 x e4m3 fits f16) straight into B-fragment registers, so no dequantized
-// copy of K or V is ever written.  The head dimension is permuted inside the
-// MMA's K index so that each lane's fragment is 16 contiguous code bytes; the
-// query carries the same permutation.  Queries are bf16; each head is
-// multiplied by a power of two (exact) to sit inside f16's range and the
-// factor is removed from the scores in fp32.  Partial (o, lse) per split are
-// merged by a second kernel.
+// the item rate; cp.async spreads the same bytes over the load units.)
+//
+// Four warps take 16-token chunks of the item; the packed codes are
+// dequantized (exactly: e2m1 x e4m3 fits f16) straight into MMA fragment
+// registers, so no dequantized copy of K or V is ever written.
+//   S = q K^T   m16n8k16 with the G query heads as the M rows and 8 tokens as
+//               N.  The head dimension is permuted inside the MMA's K index so
+//               that each lane's K fragment is 16 contiguous code bytes; the
+//               query carries the same permutation.
+//   O^T += V^T P^T   m16n8k16 with head dimensions as the M rows (eight
+//               m-tiles), the chunk's 16 tokens as K and the heads as N.  The
+//               scores' accumulator layout is already P^T's operand layout, and
+//               lane (g, t) reads one 8-byte code run (head dims 16g..16g+15,
+//               one scale block) per token.
+// Queries are bf16; each head is multiplied by a power of two (exact) to sit
+// inside f16's range and the factor is removed from the scores in fp32.  The
+// running max moves lazily.  Partial (o, lse) per split are merged by a
+// second kernel.
 #include "kernels.cuh"
 
 namespace nvfp4kv {
@@ -55,17 +63,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// dequantize one code byte (two values) times an f16x2 scale
-__device__ __forceinline__ uint32_t dq2(uint32_t byte, uint32_t sc) {
-  uint32_t h = cvt_e2m1x2_to_f16x2(byte);
-  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&h), *reinterpret_cast<__half2*>(&sc));
-  return *reinterpret_cast<uint32_t*>(&r);
+// Dequantize four code bytes (eight values) times an f16x2 scale: out[i] holds
+// the values of byte i (low nibble in the low half).  The bytes are taken as
+// sub-registers of the word, so no shifts are needed.
+__device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t sc, uint32_t (&out)[4]) {
+  uint32_t h0, h1, h2, h3;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+  const __half2 s2 = *reinterpret_cast<const __half2*>(&sc);
+  __half2 r0 = __hmul2(*reinterpret_cast<__half2*>(&h0), s2), r1 = __hmul2(*reinterpret_cast<__half2*>(&h1), s2);
+  __half2 r2 = __hmul2(*reinterpret_cast<__half2*>(&h2), s2), r3 = __hmul2(*reinterpret_cast<__half2*>(&h3), s2);
+  out[0] = *reinterpret_cast<uint32_t*>(&r0);
+  out[1] = *reinterpret_cast<uint32_t*>(&r1);
+  out[2] = *reinterpret_cast<uint32_t*>(&r2);
+  out[3] = *reinterpret_cast<uint32_t*>(&r3);
 }
 
-// Token (relative to a 16-token chunk) carried by MMA column n of QK n-tile
-// nt, which is also row 8*nt + n of the PV K index.  Lanes reading "k index
-// 2t" then touch four consecutive token rows (no shared-memory bank clash).
-__device__ __forceinline__ int chunk_token(int nt, int n) { return 8 * nt + (n >> 1) + 4 * (n & 1); }
+// log2 units: a head's running max moves only when a chunk exceeds it by more
+// than this (P <= 2^15 stays inside FP16)
+constexpr float kDecRescaleThreshold = 15.0f;
 
 constexpr int kSplitBytesK = kDecSplit * 64;
 constexpr int kSplitBytesS = kDecSplit * 8;
@@ -135,6 +154,7 @@ __device__ __forceinline__ void issue_item(const DecodeArgs& a, const DecItem& i
 template <int G>
 __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(DecodeArgs a) {
   constexpr bool kTwoRows = G > 8;  // MMA rows g+8 carry heads 8..15
+  constexpr int kHeadBlocks = kTwoRows ? 2 : 1;
   extern __shared__ __align__(128) uint8_t dsmem_raw[];
   uint8_t* dsmem = dsmem_raw + ((128u - (smem_u32(dsmem_raw) & 127u)) & 127u);
   __shared__ uint64_t bars[2];
@@ -211,92 +231,100 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
     }
     __syncthreads();
 
+    // Row state per query head (rows g and g+8 of the QK tile); every lane of
+    // a quad holds the same running max, and a partial sum over its tokens.
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-    float acc[16][4];
+    // O^T accumulators: m-tile mt holds head dims 16g + 2mt (row g) and
+    // 16g + 2mt + 1 (row g+8) for heads 2t, 2t+1 (+8 for the second block)
+    float acc[kHeadBlocks][8][4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    for (int nb = 0; nb < kHeadBlocks; ++nb)
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) acc[nb][mt][0] = acc[nb][mt][1] = acc[nb][mt][2] = acc[nb][mt][3] = 0.0f;
 
     const int n_chunks = ok ? n_pages : 0;
     for (int c = warp; c < n_chunks; c += kDecWarps) {
       const int cbase = c * 16;
       const bool page_valid = page_ok[c] != 0;
-      // ---- S = q K^T for the chunk's two 8-token n-tiles
+      // ---- S = q K^T; n-tile nt column n is token 8nt + n of the chunk
       float s[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
-        const int tok = cbase + chunk_token(nt, g);
+        const int tok = cbase + 8 * nt + g;
         const uint4 kc = *reinterpret_cast<const uint4*>(sK + tok * 64 + 16 * t);
         const uint32_t ks = *reinterpret_cast<const uint16_t*>(sKs + tok * 8 + 2 * t);
         const uint32_t sc0 = scale_f16x2(ks & 0xFFu), sc1 = scale_f16x2(ks >> 8);
         const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
 #pragma unroll
-        for (int st = 0; st < 8; ++st) {
-          const uint32_t w = kw[st >> 1] >> (16 * (st & 1));
-          const uint32_t sc = st < 4 ? sc0 : sc1;
-          const uint32_t b0 = dq2(w & 0xFFu, sc), b1 = dq2((w >> 8) & 0xFFu, sc);
-          mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[st][0], qa[st][1], qa[st][2], qa[st][3], b0, b1);
+        for (int wi = 0; wi < 4; ++wi) {
+          uint32_t h[4];
+          dq4_f16(kw[wi], wi < 2 ? sc0 : sc1, h);
+          mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[2 * wi][0], qa[2 * wi][1], qa[2 * wi][2],
+                        qa[2 * wi][3], h[0], h[1]);
+          mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[2 * wi + 1][0], qa[2 * wi + 1][1],
+                        qa[2 * wi + 1][2], qa[2 * wi + 1][3], h[2], h[3]);
         }
       }
-      // ---- online softmax (log2 domain); rows g and g+8
-      float p[2][4];
+      // ---- online softmax (log2 domain), lazy rescale; lane (g, t) holds
+      // tokens 2t, 2t+1, 8+2t, 9+2t of heads g (and g+8)
+      uint32_t pb[kHeadBlocks][2];
 #pragma unroll
-      for (int r = 0; r < (kTwoRows ? 2 : 1); ++r) {
+      for (int r = 0; r < kHeadBlocks; ++r) {
         float x[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int nt = i >> 1, col = 2 * t + (i & 1);
-          const int tok = cbase + chunk_token(nt, col);
-          x[i] = (page_valid && tok < n_tok) ? s[nt][2 * r + (i & 1)] * crow[r] : -INFINITY;
+          const int tok = cbase + 8 * (i >> 1) + 2 * t + (i & 1);
+          x[i] = (page_valid && tok < n_tok) ? s[i >> 1][2 * r + (i & 1)] * crow[r] : -INFINITY;
         }
         float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
         cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
         cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
-        const float m_new = fmaxf(m_run[r], cm);
-        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-        const float alpha = fast_exp2(m_run[r] - m_use);
-        m_run[r] = m_new;
-        float ps = 0.0f;
+        // the running max moves only when the chunk exceeds it by more than
+        // 2^15, so P stays inside FP16
+        const bool need = cm > m_run[r] + kDecRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? fast_exp2(m_run[r] - cm) : 1.0f;  // 0 when m_run = -inf
+          if (need) m_run[r] = cm;
+          l_run[r] *= alpha;
+          // O^T columns are heads 2t, 2t+1: their factors live in quads 2t, 2t+1
+          const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t), a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float e = fast_exp2(x[i] - m_use);
-          p[i >> 1][2 * r + (i & 1)] = e;
-          ps += e;
+          for (int mt = 0; mt < 8; ++mt) {
+            acc[r][mt][0] *= a0;
+            acc[r][mt][1] *= a1;
+            acc[r][mt][2] *= a0;
+            acc[r][mt][3] *= a1;
+          }
         }
-        l_run[r] = l_run[r] * alpha + ps;
+        const float m_use = (m_run[r] == -INFINITY) ? 0.0f : m_run[r];
+        float p[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          acc[j][2 * r] *= alpha;
-          acc[j][2 * r + 1] *= alpha;
-        }
+        for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_use);
+        l_run[r] += (p[0] + p[1]) + (p[2] + p[3]);
+        pb[r][0] = pack_f16x2(p[0], p[1]);
+        pb[r][1] = pack_f16x2(p[2], p[3]);
       }
-      if (!kTwoRows) {
-        p[0][2] = p[0][3] = p[1][2] = p[1][3] = 0.0f;
-      }
-      const uint32_t pa0 = pack_f16x2(p[0][0], p[0][1]), pa1 = pack_f16x2(p[0][2], p[0][3]);
-      const uint32_t pa2 = pack_f16x2(p[1][0], p[1][1]), pa3 = pack_f16x2(p[1][2], p[1][3]);
-      // ---- O += P V; lane's V rows: tokens t, t+4 (k 2t, 2t+1) and 8+t, 12+t
-      uint32_t vx[4][4], vy[4][4];
+      // ---- O^T += V^T P^T: A = V^T (rows: head dims, k: tokens), B = P^T
+      // Lane (g, t) needs tokens 2t, 2t+1, 8+2t, 9+2t at code bytes 8g..8g+7
+      // (head dims 16g..16g+15: one scale block).
+      uint32_t v[4][8];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const int tok = cbase + (q4 & 1) * 4 + (q4 >> 1) * 8 + t;
+        const int tok = cbase + 8 * (q4 >> 1) + 2 * t + (q4 & 1);
         const uint2 vc = *reinterpret_cast<const uint2*>(sV + tok * 64 + 8 * g);
         const uint32_t sc = scale_f16x2(sVs[tok * 8 + g]);
-        dequant8_f16(vc.x, sc, vx[q4]);
-        dequant8_f16(vc.y, sc, vy[q4]);
+        dq4_f16(vc.x, sc, *reinterpret_cast<uint32_t(*)[4]>(&v[q4][0]));
+        dq4_f16(vc.y, sc, *reinterpret_cast<uint32_t(*)[4]>(&v[q4][4]));
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        // value index j of the lane's 16-wide d block: word j/2 (of vx|vy), half j%2
-        const int w = (j >> 1) & 3;
-        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
-        const uint32_t* A0 = (j < 8) ? vx[0] : vy[0];
-        const uint32_t* A1 = (j < 8) ? vx[1] : vy[1];
-        const uint32_t* A2 = (j < 8) ? vx[2] : vy[2];
-        const uint32_t* A3 = (j < 8) ? vx[3] : vy[3];
-        const uint32_t b0 = prmt(A0[w], A1[w], sel);
-        const uint32_t b1 = prmt(A2[w], A3[w], sel);
-        mma_f16_16816(acc[j][0], acc[j][1], acc[j][2], acc[j][3], pa0, pa1, pa2, pa3, b0, b1);
+      for (int mt = 0; mt < 8; ++mt) {
+        const uint32_t a0 = prmt(v[0][mt], v[1][mt], 0x5410u), a1 = prmt(v[0][mt], v[1][mt], 0x7632u);
+        const uint32_t a2 = prmt(v[2][mt], v[3][mt], 0x5410u), a3 = prmt(v[2][mt], v[3][mt], 0x7632u);
+#pragma unroll
+        for (int nb = 0; nb < kHeadBlocks; ++nb)
+          mma_f16_16816(acc[nb][mt][0], acc[nb][mt][1], acc[nb][mt][2], acc[nb][mt][3], a0, a1, a2, a3, pb[nb][0],
+                        pb[nb][1]);
       }
     }
 
@@ -309,17 +337,18 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
     __syncthreads();
     float* red_o = reinterpret_cast<float*>(sK);  // [warp][16 heads][128]: 32 KB of the 36 KB stage
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int head = g + 8 * r;
-      if (r == 1 && !kTwoRows) break;
+    for (int r = 0; r < kHeadBlocks; ++r) {
       if (t == 0) {
-        red_m[warp][head] = m_run[r];
-        red_l[warp][head] = l_run[r];
+        red_m[warp][g + 8 * r] = m_run[r];
+        red_l[warp][g + 8 * r] = l_run[r];
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        red_o[(warp * 16 + head) * kHeadDim + 16 * (2 * t) + j] = acc[j][2 * r];
-        red_o[(warp * 16 + head) * kHeadDim + 16 * (2 * t + 1) + j] = acc[j][2 * r + 1];
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d = 16 * g + 2 * mt;
+        float* o0 = red_o + (warp * 16 + 8 * r + 2 * t) * kHeadDim;
+        float* o1 = o0 + kHeadDim;
+        *reinterpret_cast<float2*>(o0 + d) = make_float2(acc[r][mt][0], acc[r][mt][2]);
+        *reinterpret_cast<float2*>(o1 + d) = make_float2(acc[r][mt][1], acc[r][mt][3]);
       }
     }
     __syncthreads();
