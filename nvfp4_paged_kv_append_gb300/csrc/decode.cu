@@ -86,14 +86,14 @@ __device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t sc, uint32_t (&out)
 // than this (P <= 2^15 stays inside FP16)
 constexpr float kDecRescaleThreshold = 15.0f;
 
-constexpr int kSplitBytesK = kDecSplit * 64;
-constexpr int kSplitBytesS = kDecSplit * 8;
+constexpr int kSplitBytesK = kDecUnit * 64;
+constexpr int kSplitBytesS = kDecUnit * 8;
 constexpr int kStageBytes = 2 * (kSplitBytesK + kSplitBytesS);  // 36 KB: K, K scales, V, V scales
 constexpr int kDecCtasPerSm = 3;
 constexpr int kDecSmem = 2 * kStageBytes + 1024;                 // two stages + alignment slack
 
 struct DecItem {
-  int b, h, split, n_tok, n_pages;
+  int b, h, split, n_tok, n_units;
 };
 
 // Items are (request, kv head, split) in request-major order; the prefix of
@@ -114,25 +114,42 @@ __device__ __forceinline__ bool decode_item(const DecodeArgs& a, int idx, DecIte
   it.h = r / n_s;
   it.split = r - it.h * n_s;
   it.n_tok = min(kDecSplit, kv_len - it.split * kDecSplit);
-  it.n_pages = (it.n_tok + kPageSize - 1) / kPageSize;
+  it.n_units = (it.n_tok + kDecUnit - 1) / kDecUnit;
   return true;
 }
 
-// All 128 threads gather the item's pages into `stage` with cp.async: thread
+// Tokens of unit u of an item (at most 256 = 16 pages).
+__device__ __forceinline__ int unit_tokens(const DecItem& it, int u) { return min(kDecUnit, it.n_tok - u * kDecUnit); }
+
+// Raw page id of the page this thread gathers for unit u of an item (page
+// tid / 8 of the unit), or -1 past the unit.  Loaded one unit ahead so that
+// the global-load latency is off the path of the gather; checked there.
+__device__ __forceinline__ int unit_page(const DecodeArgs& a, const DecItem& it, int u, int tid) {
+  const int p = tid >> 3;
+  if (p * kPageSize >= unit_tokens(it, u)) return -1;
+  return a.page_table[static_cast<int64_t>(it.b) * a.max_pages + (it.split * kDecSplit + u * kDecUnit) / kPageSize + p];
+}
+
+// All 128 threads gather unit u of an item into `stage` with cp.async: thread
 // t serves page t / 8 (K and V codes, 16 B at a time, plus one 16-byte piece
-// of each scale page); a page past the item or with an invalid id is skipped
-// or zero-filled.  Each thread then arrives on `bar` once its copies land.
-__device__ __forceinline__ void issue_item(const DecodeArgs& a, const DecItem& it, uint8_t* stage, uint64_t* bar,
-                                           int* page_ok, int tid) {
+// of each scale page).  A page with an invalid id (flagged) reads as zeros,
+// and so do the V scales of tokens past the item's end -- their values are
+// then exactly 0 whatever codes the page holds.  Each thread arrives on `bar`
+// once its copies land.
+__device__ __forceinline__ void issue_unit(const DecodeArgs& a, const DecItem& it, int u, int pid, uint8_t* stage,
+                                           uint64_t* bar, int* page_ok, int tid) {
   const int p = tid >> 3, sub = tid & 7;
-  if (p < it.n_pages) {
-    int pid = a.page_table[static_cast<int64_t>(it.b) * a.max_pages + it.split * 16 + p];
-    if (pid < 0 || pid >= a.num_pages) {
+  const int n_tok = unit_tokens(it, u);
+  if (p * kPageSize < n_tok) {
+    if (pid >= a.num_pages || pid < 0) {
       if (sub == 0) set_status(a.status, kDevBadPage);
       pid = -1;
     }
     if (sub == 0) page_ok[p] = pid >= 0;
     const uint32_t n16 = pid >= 0 ? 16u : 0u;
+    // V scales of tokens 2 sub, 2 sub + 1 of this page: 8 bytes per live token
+    const int live = min(max(n_tok - p * kPageSize - 2 * sub, 0), 2);
+    const uint32_t nvs = pid >= 0 ? 8u * live : 0u;
     const int64_t row = (static_cast<int64_t>(pid >= 0 ? pid : 0) * a.num_kv_heads + it.h) * kPageSize;
     const uint32_t sK = smem_u32(stage), sKs = sK + kSplitBytesK, sV = sKs + kSplitBytesS, sVs = sV + kSplitBytesK;
     const uint8_t* gk = a.k_data + row * 64;
@@ -144,13 +161,50 @@ __device__ __forceinline__ void issue_item(const DecodeArgs& a, const DecItem& i
       cp_async16(sV + p * 1024 + c * 16, gv + c * 16, n16);
     }
     cp_async16(sKs + p * 128 + sub * 16, a.k_scale + row * 8 + sub * 16, n16);
-    cp_async16(sVs + p * 128 + sub * 16, a.v_scale + row * 8 + sub * 16, n16);
+    cp_async16(sVs + p * 128 + sub * 16, a.v_scale + row * 8 + sub * 16, nvs);
   }
   cp_async_mbar_arrive(bar);
 }
 
-// Persistent: CTA c takes items c, c + grid, ...; two shared-memory stages so
-// that the copies of item k+1 run while item k is computed.
+// Raw bf16 query rows of an item for lane (g, t): d = 32t .. 32t+31 of heads
+// g and g+8 (zeros past the group).  Loaded one item ahead.
+template <int G>
+__device__ __forceinline__ void load_q_raw(const DecodeArgs& a, const DecItem& it, int g, int t, uint4 (&qr)[2][4]) {
+  const uint16_t* qb =
+      reinterpret_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(it.b) * a.num_q_heads + it.h * G) * kHeadDim;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int head = g + 8 * r;
+    const bool live = (r == 0 || G > 8) && head < G;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      qr[r][i] = live ? reinterpret_cast<const uint4*>(qb + head * kHeadDim + 32 * t)[i] : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Iterator over the CTA's stream of units (item blockIdx.x + k * grid, unit u).
+struct UnitCursor {
+  int k, u;
+  bool has;
+  DecItem it;
+};
+__device__ __forceinline__ void cursor_start(const DecodeArgs& a, UnitCursor& c) {
+  c.k = 0;
+  c.u = 0;
+  c.has = decode_item(a, blockIdx.x, c.it);
+}
+__device__ __forceinline__ void cursor_next(const DecodeArgs& a, UnitCursor& c) {
+  if (++c.u >= c.it.n_units) {
+    c.u = 0;
+    ++c.k;
+    c.has = decode_item(a, blockIdx.x + c.k * gridDim.x, c.it);
+  }
+}
+
+// Persistent: CTA c takes items c, c + grid, ...  Each item (up to 1024
+// tokens) streams through two shared-memory stages of 256 tokens, so the
+// copies of the next unit run while the current one is computed; the four
+// warps' partial results are merged once per item.
 template <int G>
 __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(DecodeArgs a) {
   constexpr bool kTwoRows = G > 8;  // MMA rows g+8 carry heads 8..15
@@ -160,6 +214,7 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   __shared__ uint64_t bars[2];
   __shared__ int page_ok_sh[2][16];
   __shared__ float red_m[kDecWarps][16], red_l[kDecWarps][16];
+  __shared__ float mw[kDecWarps][16];   // merge weights exp2(m_w - m) / L per head
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   if (tid == 0) {
@@ -168,42 +223,33 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
     fence_barrier_init();
   }
   __syncthreads();
-  DecItem nxt;
-  for (int k = 0; k < 2; ++k)
-    if (decode_item(a, blockIdx.x + k * gridDim.x, nxt)) issue_item(a, nxt, dsmem + k * kStageBytes, &bars[k], page_ok_sh[k], tid);
+  // issue cursor: two units ahead of the compute
+  UnitCursor ic;
+  cursor_start(a, ic);
+  for (int s = 0; s < 2 && ic.has; ++s) {
+    issue_unit(a, ic.it, ic.u, unit_page(a, ic.it, ic.u, tid), dsmem + s * kStageBytes, &bars[s], page_ok_sh[s], tid);
+    cursor_next(a, ic);
+  }
   DecItem it;
+  uint4 qr[2][4];
+  if (decode_item(a, blockIdx.x, it)) load_q_raw<G>(a, it, g, t, qr);
+  uint32_t uc = 0;  // units consumed: stage uc & 1, phase (uc >> 1) & 1
   for (int k = 0; decode_item(a, blockIdx.x + k * gridDim.x, it); ++k) {
-    const int stg = k & 1;
-    uint8_t* sK = dsmem + stg * kStageBytes;
-    uint8_t* sKs = sK + kSplitBytesK;
-    uint8_t* sV = sKs + kSplitBytesS;
-    uint8_t* sVs = sV + kSplitBytesK;
-    const int* page_ok = page_ok_sh[stg];
-    const int b = it.b, h = it.h, n_tok = it.n_tok, n_pages = it.n_pages;
-
-    // ---- query fragments (overlap the copies) ------------------------------
+    const int b = it.b, h = it.h;
+    // ---- query fragments from the rows loaded one item ahead ------------------
     // Lane (g, t) owns d = 32t .. 32t+31 of heads g and g+8.
-    const uint16_t* qb =
-        reinterpret_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * a.num_q_heads + h * G) * kHeadDim;
     uint32_t qa[8][4];
     float crow[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const int head = g + 8 * r;
       float x[32];
-      if ((r == 0 || kTwoRows) && head < G) {
-        const uint4* src = reinterpret_cast<const uint4*>(qb + head * kHeadDim + 32 * t);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w = src[i];
-          bf16x2_to_f32(w.x, x[8 * i + 0], x[8 * i + 1]);
-          bf16x2_to_f32(w.y, x[8 * i + 2], x[8 * i + 3]);
-          bf16x2_to_f32(w.z, x[8 * i + 4], x[8 * i + 5]);
-          bf16x2_to_f32(w.w, x[8 * i + 6], x[8 * i + 7]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = 0.0f;
+      for (int i = 0; i < 4; ++i) {
+        const uint4 w = qr[r][i];
+        bf16x2_to_f32(w.x, x[8 * i + 0], x[8 * i + 1]);
+        bf16x2_to_f32(w.y, x[8 * i + 2], x[8 * i + 3]);
+        bf16x2_to_f32(w.z, x[8 * i + 4], x[8 * i + 5]);
+        bf16x2_to_f32(w.w, x[8 * i + 6], x[8 * i + 7]);
       }
       float amax = 0.0f;
 #pragma unroll
@@ -220,16 +266,10 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
         qa[s][r + 2] = pack_f16x2(x[4 * s + 2] * up, x[4 * s + 3] * up);
       }
     }
-
-    const bool ok = mbar_wait(&bars[stg], (k >> 1) & 1, a.status);
-    // zero the V scales of tokens that hold no data (past kv_len, or a page
-    // that was not loaded) so that their values are exactly 0
-    if (ok) {
-      for (int i = tid; i < n_pages * kPageSize; i += 128) {
-        if (i >= n_tok || !page_ok[i >> 4]) *reinterpret_cast<uint2*>(sVs + i * 8) = make_uint2(0u, 0u);
-      }
+    {
+      DecItem nx1;
+      if (decode_item(a, blockIdx.x + (k + 1) * gridDim.x, nx1)) load_q_raw<G>(a, nx1, g, t, qr);
     }
-    __syncthreads();
 
     // Row state per query head (rows g and g+8 of the QK tile); every lane of
     // a quad holds the same running max, and a partial sum over its tokens.
@@ -242,147 +282,175 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) acc[nb][mt][0] = acc[nb][mt][1] = acc[nb][mt][2] = acc[nb][mt][3] = 0.0f;
 
-    const int n_chunks = ok ? n_pages : 0;
-    for (int c = warp; c < n_chunks; c += kDecWarps) {
-      const int cbase = c * 16;
-      const bool page_valid = page_ok[c] != 0;
-      // ---- S = q K^T; n-tile nt column n is token 8nt + n of the chunk
-      float s[2][4];
+    for (int u = 0; u < it.n_units; ++u, ++uc) {
+      const int stg = uc & 1;
+      uint8_t* sK = dsmem + stg * kStageBytes;
+      uint8_t* sKs = sK + kSplitBytesK;
+      uint8_t* sV = sKs + kSplitBytesS;
+      uint8_t* sVs = sV + kSplitBytesK;
+      const int* page_ok = page_ok_sh[stg];
+      const int n_tok = unit_tokens(it, u);
+      // the page this thread gathers for the unit issued after this one
+      const int pid_next = ic.has ? unit_page(a, ic.it, ic.u, tid) : -1;
+      const bool ok = mbar_wait(&bars[stg], (uc >> 1) & 1, a.status);
+      const int n_chunks = ok ? (n_tok + 15) / 16 : 0;
+      for (int c = warp; c < n_chunks; c += kDecWarps) {
+        const int cbase = c * 16;
+        const bool page_valid = page_ok[c] != 0;
+        // ---- S = q K^T; n-tile nt column n is token 8nt + n of the chunk
+        float s[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
-        const int tok = cbase + 8 * nt + g;
-        const uint4 kc = *reinterpret_cast<const uint4*>(sK + tok * 64 + 16 * t);
-        const uint32_t ks = *reinterpret_cast<const uint16_t*>(sKs + tok * 8 + 2 * t);
-        const uint32_t sc0 = scale_f16x2(ks & 0xFFu), sc1 = scale_f16x2(ks >> 8);
-        const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
+        for (int nt = 0; nt < 2; ++nt) {
+          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
+          const int tok = cbase + 8 * nt + g;
+          const uint4 kc = *reinterpret_cast<const uint4*>(sK + tok * 64 + 16 * t);
+          const uint32_t ks = *reinterpret_cast<const uint16_t*>(sKs + tok * 8 + 2 * t);
+          const uint32_t sc0 = scale_f16x2(ks & 0xFFu), sc1 = scale_f16x2(ks >> 8);
+          const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          uint32_t h[4];
-          dq4_f16(kw[wi], wi < 2 ? sc0 : sc1, h);
-          mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[2 * wi][0], qa[2 * wi][1], qa[2 * wi][2],
-                        qa[2 * wi][3], h[0], h[1]);
-          mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[2 * wi + 1][0], qa[2 * wi + 1][1],
-                        qa[2 * wi + 1][2], qa[2 * wi + 1][3], h[2], h[3]);
-        }
-      }
-      // ---- online softmax (log2 domain), lazy rescale; lane (g, t) holds
-      // tokens 2t, 2t+1, 8+2t, 9+2t of heads g (and g+8)
-      uint32_t pb[kHeadBlocks][2];
-#pragma unroll
-      for (int r = 0; r < kHeadBlocks; ++r) {
-        float x[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tok = cbase + 8 * (i >> 1) + 2 * t + (i & 1);
-          x[i] = (page_valid && tok < n_tok) ? s[i >> 1][2 * r + (i & 1)] * crow[r] : -INFINITY;
-        }
-        float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
-        // the running max moves only when the chunk exceeds it by more than
-        // 2^15, so P stays inside FP16
-        const bool need = cm > m_run[r] + kDecRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? fast_exp2(m_run[r] - cm) : 1.0f;  // 0 when m_run = -inf
-          if (need) m_run[r] = cm;
-          l_run[r] *= alpha;
-          // O^T columns are heads 2t, 2t+1: their factors live in quads 2t, 2t+1
-          const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t), a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            acc[r][mt][0] *= a0;
-            acc[r][mt][1] *= a1;
-            acc[r][mt][2] *= a0;
-            acc[r][mt][3] *= a1;
+          for (int wi = 0; wi < 4; ++wi) {
+            uint32_t hh[4];
+            dq4_f16(kw[wi], wi < 2 ? sc0 : sc1, hh);
+            mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[2 * wi][0], qa[2 * wi][1], qa[2 * wi][2],
+                          qa[2 * wi][3], hh[0], hh[1]);
+            mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[2 * wi + 1][0], qa[2 * wi + 1][1],
+                          qa[2 * wi + 1][2], qa[2 * wi + 1][3], hh[2], hh[3]);
           }
         }
-        const float m_use = (m_run[r] == -INFINITY) ? 0.0f : m_run[r];
-        float p[4];
+        // ---- online softmax (log2 domain), lazy rescale; lane (g, t) holds
+        // tokens 2t, 2t+1, 8+2t, 9+2t of heads g (and g+8)
+        uint32_t pb[kHeadBlocks][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_use);
-        l_run[r] += (p[0] + p[1]) + (p[2] + p[3]);
-        pb[r][0] = pack_f16x2(p[0], p[1]);
-        pb[r][1] = pack_f16x2(p[2], p[3]);
+        for (int r = 0; r < kHeadBlocks; ++r) {
+          float x[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tok = cbase + 8 * (i >> 1) + 2 * t + (i & 1);
+            x[i] = (page_valid && tok < n_tok) ? s[i >> 1][2 * r + (i & 1)] * crow[r] : -INFINITY;
+          }
+          float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+          // the running max moves only when the chunk exceeds it by more than
+          // 2^15, so P stays inside FP16
+          const bool need = cm > m_run[r] + kDecRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? fast_exp2(m_run[r] - cm) : 1.0f;  // 0 when m_run = -inf
+            if (need) m_run[r] = cm;
+            l_run[r] *= alpha;
+            // O^T columns are heads 2t, 2t+1: their factors live in quads 2t, 2t+1
+            const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t), a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              acc[r][mt][0] *= a0;
+              acc[r][mt][1] *= a1;
+              acc[r][mt][2] *= a0;
+              acc[r][mt][3] *= a1;
+            }
+          }
+          const float m_use = (m_run[r] == -INFINITY) ? 0.0f : m_run[r];
+          float p[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_use);
+          l_run[r] += (p[0] + p[1]) + (p[2] + p[3]);
+          pb[r][0] = pack_f16x2(p[0], p[1]);
+          pb[r][1] = pack_f16x2(p[2], p[3]);
+        }
+        // ---- O^T += V^T P^T: A = V^T (rows: head dims, k: tokens), B = P^T
+        // Lane (g, t) needs tokens 2t, 2t+1, 8+2t, 9+2t at code bytes 8g..8g+7
+        // (head dims 16g..16g+15: one scale block).
+        uint32_t v[4][8];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int tok = cbase + 8 * (q4 >> 1) + 2 * t + (q4 & 1);
+          const uint2 vc = *reinterpret_cast<const uint2*>(sV + tok * 64 + 8 * g);
+          const uint32_t sc = scale_f16x2(sVs[tok * 8 + g]);
+          dq4_f16(vc.x, sc, *reinterpret_cast<uint32_t(*)[4]>(&v[q4][0]));
+          dq4_f16(vc.y, sc, *reinterpret_cast<uint32_t(*)[4]>(&v[q4][4]));
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const uint32_t a0 = prmt(v[0][mt], v[1][mt], 0x5410u), a1 = prmt(v[0][mt], v[1][mt], 0x7632u);
+          const uint32_t a2 = prmt(v[2][mt], v[3][mt], 0x5410u), a3 = prmt(v[2][mt], v[3][mt], 0x7632u);
+#pragma unroll
+          for (int nb = 0; nb < kHeadBlocks; ++nb)
+            mma_f16_16816(acc[nb][mt][0], acc[nb][mt][1], acc[nb][mt][2], acc[nb][mt][3], a0, a1, a2, a3, pb[nb][0],
+                          pb[nb][1]);
+        }
       }
-      // ---- O^T += V^T P^T: A = V^T (rows: head dims, k: tokens), B = P^T
-      // Lane (g, t) needs tokens 2t, 2t+1, 8+2t, 9+2t at code bytes 8g..8g+7
-      // (head dims 16g..16g+15: one scale block).
-      uint32_t v[4][8];
+      const bool last = u == it.n_units - 1;
+      if (last) {
+        // ---- merge the four warps through this stage's shared memory ---------
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int tok = cbase + 8 * (q4 >> 1) + 2 * t + (q4 & 1);
-        const uint2 vc = *reinterpret_cast<const uint2*>(sV + tok * 64 + 8 * g);
-        const uint32_t sc = scale_f16x2(sVs[tok * 8 + g]);
-        dq4_f16(vc.x, sc, *reinterpret_cast<uint32_t(*)[4]>(&v[q4][0]));
-        dq4_f16(vc.y, sc, *reinterpret_cast<uint32_t(*)[4]>(&v[q4][4]));
+        for (int r = 0; r < 2; ++r) {
+          l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+          l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+        }
+        __syncthreads();  // every warp is done reading the stage
+        float* red_o = reinterpret_cast<float*>(sK);  // [warp][16 heads][128]: 32 KB of the 36 KB stage
+#pragma unroll
+        for (int r = 0; r < kHeadBlocks; ++r) {
+          if (t == 0) {
+            red_m[warp][g + 8 * r] = m_run[r];
+            red_l[warp][g + 8 * r] = l_run[r];
+          }
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const int d = 16 * g + 2 * mt;
+            float* o0 = red_o + (warp * 16 + 8 * r + 2 * t) * kHeadDim;
+            float* o1 = o0 + kHeadDim;
+            *reinterpret_cast<float2*>(o0 + d) = make_float2(acc[r][mt][0], acc[r][mt][2]);
+            *reinterpret_cast<float2*>(o1 + d) = make_float2(acc[r][mt][1], acc[r][mt][3]);
+          }
+        }
+        __syncthreads();
+        const bool single = a.kv_lens[b] <= kDecSplit;
+        // per head: the combined max and sum, and each warp's weight
+        // exp2(m_w - m) / L, computed once
+        if (tid < G) {
+          const int head = tid;
+          float m = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, red_m[w][head]);
+          const float mu = (m == -INFINITY) ? 0.0f : m;
+          float f[kDecWarps], L = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kDecWarps; ++w) {
+            f[w] = fast_exp2(red_m[w][head] - mu);
+            L += red_l[w][head] * f[w];
+          }
+          const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+#pragma unroll
+          for (int w = 0; w < kDecWarps; ++w) mw[w][head] = f[w] * inv;
+          const float lse2 = (L > 0.0f) ? mu + __log2f(L) : -INFINITY;
+          const int hq = h * G + head;
+          if (single) {
+            if (a.lse) a.lse[static_cast<int64_t>(b) * a.num_q_heads + hq] = lse2 * kLn2;
+          } else {
+            a.part_lse[(static_cast<int64_t>(b) * a.max_splits + it.split) * a.num_q_heads + hq] = lse2;
+          }
+        }
+        __syncthreads();
+        for (int i = tid; i < G * kHeadDim; i += 128) {
+          const int head = i >> 7, d = i & 127;
+          float on = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kDecWarps; ++w) on += red_o[(w * 16 + head) * kHeadDim + d] * mw[w][head];
+          const int hq = h * G + head;
+          if (single) {
+            reinterpret_cast<__nv_bfloat16*>(a.o)[(static_cast<int64_t>(b) * a.num_q_heads + hq) * kHeadDim + d] =
+                __float2bfloat16_rn(on * a.v_g);
+          } else {
+            a.part_o[((static_cast<int64_t>(b) * a.max_splits + it.split) * a.num_q_heads + hq) * kHeadDim + d] = on;
+          }
+        }
       }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const uint32_t a0 = prmt(v[0][mt], v[1][mt], 0x5410u), a1 = prmt(v[0][mt], v[1][mt], 0x7632u);
-        const uint32_t a2 = prmt(v[2][mt], v[3][mt], 0x5410u), a3 = prmt(v[2][mt], v[3][mt], 0x7632u);
-#pragma unroll
-        for (int nb = 0; nb < kHeadBlocks; ++nb)
-          mma_f16_16816(acc[nb][mt][0], acc[nb][mt][1], acc[nb][mt][2], acc[nb][mt][3], a0, a1, a2, a3, pb[nb][0],
-                        pb[nb][1]);
+      __syncthreads();  // every thread is done with this stage
+      if (ic.has) {
+        issue_unit(a, ic.it, ic.u, pid_next, dsmem + stg * kStageBytes, &bars[stg], page_ok_sh[stg], tid);
+        cursor_next(a, ic);
       }
     }
-
-    // ---- merge the four warps (the stage's shared memory is free now) -------
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-      l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-    }
-    __syncthreads();
-    float* red_o = reinterpret_cast<float*>(sK);  // [warp][16 heads][128]: 32 KB of the 36 KB stage
-#pragma unroll
-    for (int r = 0; r < kHeadBlocks; ++r) {
-      if (t == 0) {
-        red_m[warp][g + 8 * r] = m_run[r];
-        red_l[warp][g + 8 * r] = l_run[r];
-      }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int d = 16 * g + 2 * mt;
-        float* o0 = red_o + (warp * 16 + 8 * r + 2 * t) * kHeadDim;
-        float* o1 = o0 + kHeadDim;
-        *reinterpret_cast<float2*>(o0 + d) = make_float2(acc[r][mt][0], acc[r][mt][2]);
-        *reinterpret_cast<float2*>(o1 + d) = make_float2(acc[r][mt][1], acc[r][mt][3]);
-      }
-    }
-    __syncthreads();
-    const int kv_len = a.kv_lens[b];
-    const bool single = kv_len <= kDecSplit;
-    for (int i = tid; i < G * kHeadDim; i += 128) {
-      const int head = i >> 7, d = i & 127;
-      float m = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, red_m[w][head]);
-      const float mu = (m == -INFINITY) ? 0.0f : m;
-      float L = 0.0f, o = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float f = fast_exp2(red_m[w][head] - mu);
-        L += red_l[w][head] * f;
-        o += red_o[(w * 16 + head) * kHeadDim + d] * f;
-      }
-      const float on = (L > 0.0f) ? o / L : 0.0f;
-      const float lse2 = (L > 0.0f) ? mu + __log2f(L) : -INFINITY;
-      const int hq = h * G + head;
-      if (single) {
-        reinterpret_cast<__nv_bfloat16*>(a.o)[(static_cast<int64_t>(b) * a.num_q_heads + hq) * kHeadDim + d] =
-            __float2bfloat16_rn(on * a.v_g);
-        if (a.lse && d == 0) a.lse[static_cast<int64_t>(b) * a.num_q_heads + hq] = lse2 * kLn2;
-      } else {
-        const int64_t pi = (static_cast<int64_t>(b) * a.max_splits + it.split) * a.num_q_heads + hq;
-        a.part_o[pi * kHeadDim + d] = on;
-        if (d == 0) a.part_lse[pi] = lse2;
-      }
-    }
-    __syncthreads();  // every thread is done with this stage
-    if (decode_item(a, blockIdx.x + (k + 2) * gridDim.x, nxt))
-      issue_item(a, nxt, dsmem + stg * kStageBytes, &bars[stg], page_ok_sh[stg], tid);
   }
 }
 

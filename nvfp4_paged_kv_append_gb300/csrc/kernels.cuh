@@ -48,7 +48,8 @@ struct DequantArgs {
 };
 
 // ---- decode --------------------------------------------------------------------
-constexpr int kDecSplit = 256;   // tokens per CTA (16 pages)
+constexpr int kDecSplit = 1024;  // tokens per work item (one partial result)
+constexpr int kDecUnit = 256;    // tokens per shared-memory stage (16 pages)
 constexpr int kDecWarps = 4;
 
 struct DecodeArgs {
