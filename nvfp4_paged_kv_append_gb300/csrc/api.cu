@@ -114,8 +114,11 @@ size_t prefill_repack_bytes(int variant, int batch, int num_kv_heads, int64_t ma
 
 int launch_rc(cudaError_t e) { return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA; }
 
-// Decode workspace starts with the item schedule: count + per-request prefix.
-size_t decode_sched_bytes(int batch) { return (16 + 4 * (static_cast<size_t>(batch) + 1) + 15) & ~size_t(15); }
+// Decode workspace starts with the item schedule: a 16-byte header, then one
+// 16-byte record per (request, kv head, split).
+size_t decode_sched_bytes(int batch, int num_kv_heads, size_t splits) {
+  return 16 + 16 * static_cast<size_t>(batch) * num_kv_heads * splits;
+}
 
 // A wait that can only end by its time limit (nothing arrives on `bar`).
 __global__ void nvfp4_debug_wait_kernel(uint64_t limit_ns, int* status) {
@@ -147,7 +150,8 @@ size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int
   if (op == NVFP4KV_OP_DECODE) {
     if (max_kv_len < 0) return 0;
     const size_t splits = (static_cast<size_t>(max_kv_len) + kDecSplit - 1) / kDecSplit;
-    return decode_sched_bytes(batch) + static_cast<size_t>(batch) * splits * num_q_heads * (kHeadDim + 1) * sizeof(float);
+    return decode_sched_bytes(batch, num_kv_heads, splits) +
+           static_cast<size_t>(batch) * splits * num_q_heads * (kHeadDim + 1) * sizeof(float);
   }
   return 0;
 }
@@ -346,7 +350,8 @@ int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t
   a.lse = lse;
   a.batch = batch;
   a.sched = static_cast<int*>(workspace);
-  float* ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + decode_sched_bytes(batch));
+  float* ws = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       decode_sched_bytes(batch, cache->num_kv_heads, a.max_splits));
   a.part_o = ws;
   a.part_lse = ws + static_cast<size_t>(batch) * a.max_splits * num_q_heads * kHeadDim;
   a.status = d->status;

@@ -96,24 +96,20 @@ struct DecItem {
   int b, h, split, n_tok, n_units;
 };
 
-// Items are (request, kv head, split) in request-major order; the prefix of
-// items per request (written by the schedule kernel) maps an index back.
-__device__ __forceinline__ bool decode_item(const DecodeArgs& a, int idx, DecItem& it) {
+// The schedule lists item records (request, kv head, split, tokens): full
+// 1024-token items first, then the shorter last splits.  CTA c takes the
+// record of round k at k * grid + c, in reverse order on odd rounds, so that
+// every CTA gets a similar amount of work.
+__device__ __forceinline__ bool decode_item(const DecodeArgs& a, int round, DecItem& it) {
   const int total = a.sched[0];
+  const int grid = gridDim.x, c = blockIdx.x;
+  const int idx = round * grid + ((round & 1) ? grid - 1 - c : c);
   if (idx >= total) return false;
-  const int* prefix = a.sched + 4;
-  int lo = 0, hi = a.batch - 1;  // last b with prefix[b] <= idx
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= idx) lo = mid; else hi = mid - 1;
-  }
-  const int kv_len = a.kv_lens[lo];
-  const int n_s = (kv_len + kDecSplit - 1) / kDecSplit;
-  const int r = idx - prefix[lo];
-  it.b = lo;
-  it.h = r / n_s;
-  it.split = r - it.h * n_s;
-  it.n_tok = min(kDecSplit, kv_len - it.split * kDecSplit);
+  const int4 r = reinterpret_cast<const int4*>(a.sched + 4)[idx];
+  it.b = r.x;
+  it.h = r.y;
+  it.split = r.z;
+  it.n_tok = r.w;
   it.n_units = (it.n_tok + kDecUnit - 1) / kDecUnit;
   return true;
 }
@@ -191,13 +187,13 @@ struct UnitCursor {
 __device__ __forceinline__ void cursor_start(const DecodeArgs& a, UnitCursor& c) {
   c.k = 0;
   c.u = 0;
-  c.has = decode_item(a, blockIdx.x, c.it);
+  c.has = decode_item(a, 0, c.it);
 }
 __device__ __forceinline__ void cursor_next(const DecodeArgs& a, UnitCursor& c) {
   if (++c.u >= c.it.n_units) {
     c.u = 0;
     ++c.k;
-    c.has = decode_item(a, blockIdx.x + c.k * gridDim.x, c.it);
+    c.has = decode_item(a, c.k, c.it);
   }
 }
 
@@ -232,9 +228,9 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   }
   DecItem it;
   uint4 qr[2][4];
-  if (decode_item(a, blockIdx.x, it)) load_q_raw<G>(a, it, g, t, qr);
+  if (decode_item(a, 0, it)) load_q_raw<G>(a, it, g, t, qr);
   uint32_t uc = 0;  // units consumed: stage uc & 1, phase (uc >> 1) & 1
-  for (int k = 0; decode_item(a, blockIdx.x + k * gridDim.x, it); ++k) {
+  for (int k = 0; decode_item(a, k, it); ++k) {
     const int b = it.b, h = it.h;
     // ---- query fragments from the rows loaded one item ahead ------------------
     // Lane (g, t) owns d = 32t .. 32t+31 of heads g and g+8.
@@ -268,7 +264,7 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
     }
     {
       DecItem nx1;
-      if (decode_item(a, blockIdx.x + (k + 1) * gridDim.x, nx1)) load_q_raw<G>(a, nx1, g, t, qr);
+      if (decode_item(a, k + 1, nx1)) load_q_raw<G>(a, nx1, g, t, qr);
     }
 
     // Row state per query head (rows g and g+8 of the QK tile); every lane of
@@ -454,47 +450,77 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   }
 }
 
-// Schedule: items per request (splits x kv heads) and their prefix.
+// Block-wide exclusive prefix sum over the 1024 threads (returns the exclusive
+// value; *total receives the sum).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) warp_sums[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0);
+  *total = warp_sums[31];
+  __syncthreads();
+  return incl - v;
+}
+
+// Schedule: one record per (request, kv head, 1024-token split), full splits
+// first, then each request's shorter last split.
 __global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
   __shared__ int warp_sums[32];
-  int* prefix = a.sched + 4;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  int carry = 0;
+  int4* items = reinterpret_cast<int4*>(a.sched + 4);
+  const int tid = threadIdx.x;
+  // pass 1: total full items (to place the short ones after them)
+  int n_full_total = 0;
   for (int base = 0; base < a.batch; base += blockDim.x) {
     const int b = base + tid;
-    int cnt = 0;
+    int full = 0;
     if (b < a.batch) {
       const int kv_len = a.kv_lens[b];
       if (kv_len > a.max_pages * kPageSize) set_status(a.status, kDevBadShape);
-      else if (kv_len > 0) cnt = ((kv_len + kDecSplit - 1) / kDecSplit) * a.num_kv_heads;
+      else if (kv_len > 0) full = (kv_len / kDecSplit) * a.num_kv_heads;
     }
-    int v = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += n;
-    }
-    if (lane == 31) warp_sums[wid] = v;
-    __syncthreads();
-    if (wid == 0) {
-      int w = warp_sums[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += n;
+    int tot;
+    block_exclusive_scan(full, warp_sums, &tot);
+    n_full_total += tot;
+  }
+  // pass 2: write the records
+  int full_carry = 0, part_carry = 0;
+  for (int base = 0; base < a.batch; base += blockDim.x) {
+    const int b = base + tid;
+    int full = 0, part = 0, kv_len = 0;
+    if (b < a.batch) {
+      kv_len = a.kv_lens[b];
+      if (kv_len > 0 && kv_len <= a.max_pages * kPageSize) {
+        full = kv_len / kDecSplit;
+        part = (kv_len % kDecSplit) ? 1 : 0;
       }
-      warp_sums[lane] = w;
     }
-    __syncthreads();
-    const int incl = v + (wid > 0 ? warp_sums[wid - 1] : 0);
-    if (b < a.batch) prefix[b] = carry + incl - cnt;
-    carry += warp_sums[31];
-    __syncthreads();
+    int ftot, ptot;
+    const int fpos = full_carry + block_exclusive_scan(full * a.num_kv_heads, warp_sums, &ftot);
+    const int ppos = n_full_total + part_carry + block_exclusive_scan(part * a.num_kv_heads, warp_sums, &ptot);
+    for (int sp = 0; sp < full; ++sp)
+      for (int h = 0; h < a.num_kv_heads; ++h) items[fpos + sp * a.num_kv_heads + h] = make_int4(b, h, sp, kDecSplit);
+    if (part)
+      for (int h = 0; h < a.num_kv_heads; ++h) items[ppos + h] = make_int4(b, h, full, kv_len - full * kDecSplit);
+    full_carry += ftot;
+    part_carry += ptot;
   }
-  if (tid == 0) {
-    prefix[a.batch] = carry;
-    a.sched[0] = carry;
-  }
+  if (tid == 0) a.sched[0] = full_carry + part_carry;
 }
 
 // Merge the split partials of requests with more than one split; write zeros

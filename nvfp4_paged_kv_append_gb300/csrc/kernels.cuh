@@ -66,7 +66,7 @@ struct DecodeArgs {
   int num_q_heads;
   int max_splits;
   int batch;
-  int* sched;         // [0] item count, [4..] per-request item prefix (batch+1)
+  int* sched;         // [0] item count; item records (int4 b, h, split, n_tok) from sched + 4
   float k_g, v_g, sm_scale;
   void* o;            // bf16 [B][Hq][128]
   float* lse;         // optional [B][Hq]

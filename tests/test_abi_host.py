@@ -59,7 +59,8 @@ def test_workspace_sizes(nk):
     assert b >= 16 + 8 * items and b % 16 == 0
     # decode: split partials (129 floats per split, head, request)
     d = nk.nvfp4_workspace_bytes(nk.OP_DECODE, 32, 32, 8, 0, 32768)
-    assert d == 16 * ((16 + 4 * 33 + 15) // 16) + 32 * 32 * 32 * 129 * 4  # 1024-token splits
+    # schedule: 16 B header + one 16 B record per (request, kv head, 1024-token split)
+    assert d == 16 + 16 * 32 * 8 * 32 + 32 * 32 * 32 * 129 * 4
     assert nk.nvfp4_workspace_bytes(nk.OP_DECODE, 2, 6, 4, 0, 100) == 0  # Hq % Hkv != 0
     assert nk.nvfp4_workspace_bytes(7, 1, 8, 8, 1, 1) == 0
 
