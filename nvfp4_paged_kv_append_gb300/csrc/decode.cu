@@ -97,21 +97,38 @@ struct DecItem {
 };
 
 // The schedule lists item records (request, kv head, split, tokens): full
-// 1024-token items first, then the shorter last splits.  CTA c takes the
-// record of round k at k * grid + c, in reverse order on odd rounds, so that
-// every CTA gets a similar amount of work.
-__device__ __forceinline__ bool decode_item(const DecodeArgs& a, int round, DecItem& it) {
-  const int total = a.sched[0];
-  const int grid = gridDim.x, c = blockIdx.x;
-  const int idx = round * grid + ((round & 1) ? grid - 1 - c : c);
-  if (idx >= total) return false;
-  const int4 r = reinterpret_cast<const int4*>(a.sched + 4)[idx];
+// 1024-token items first, then the shorter last splits.  CTAs claim records
+// in that order from a counter (sched[1]), so the short items fill the tail.
+__device__ __forceinline__ DecItem item_of(int4 r) {
+  DecItem it;
   it.b = r.x;
   it.h = r.y;
   it.split = r.z;
   it.n_tok = r.w;
-  it.n_units = (it.n_tok + kDecUnit - 1) / kDecUnit;
-  return true;
+  it.n_units = (r.w + kDecUnit - 1) / kDecUnit;
+  return it;
+}
+
+// Claimed records of this CTA in claim order, four deep: the copy cursor runs
+// at most two units ahead of the compute, so at most three items are live.
+struct ClaimRing {
+  int4 rec[4];
+  int n_valid;  // records claimed so far that hold an item
+  int done;     // the schedule is exhausted
+};
+
+// Claim the next record (all threads call it; thread 0 takes the counter).
+__device__ __forceinline__ void claim_item(const DecodeArgs& a, ClaimRing* ring) {
+  if (threadIdx.x == 0) {
+    const int idx = atomicAdd(a.sched + 1, 1);
+    if (idx < a.sched[0]) {
+      ring->rec[ring->n_valid & 3] = reinterpret_cast<const int4*>(a.sched + 4)[idx];
+      ++ring->n_valid;
+    } else {
+      ring->done = 1;
+    }
+  }
+  __syncthreads();
 }
 
 // Tokens of unit u of an item (at most 256 = 16 pages).
@@ -178,26 +195,32 @@ __device__ __forceinline__ void load_q_raw(const DecodeArgs& a, const DecItem& i
   }
 }
 
-// Iterator over the CTA's stream of units (item blockIdx.x + k * grid, unit u).
+// The copy cursor: (claimed item ci, unit u) of the next unit to gather.
 struct UnitCursor {
-  int k, u;
+  int ci, u;
   bool has;
   DecItem it;
 };
-__device__ __forceinline__ void cursor_start(const DecodeArgs& a, UnitCursor& c) {
-  c.k = 0;
-  c.u = 0;
-  c.has = decode_item(a, 0, c.it);
+__device__ __forceinline__ void cursor_load(ClaimRing* ring, UnitCursor& c) {
+  c.has = c.ci < ring->n_valid;
+  if (c.has) c.it = item_of(ring->rec[c.ci & 3]);
 }
-__device__ __forceinline__ void cursor_next(const DecodeArgs& a, UnitCursor& c) {
+__device__ __forceinline__ void cursor_start(const DecodeArgs& a, ClaimRing* ring, UnitCursor& c) {
+  c.ci = 0;
+  c.u = 0;
+  claim_item(a, ring);
+  cursor_load(ring, c);
+}
+__device__ __forceinline__ void cursor_next(const DecodeArgs& a, ClaimRing* ring, UnitCursor& c) {
   if (++c.u >= c.it.n_units) {
     c.u = 0;
-    ++c.k;
-    c.has = decode_item(a, c.k, c.it);
+    ++c.ci;
+    if (!ring->done) claim_item(a, ring);  // uniform: ring->done is read after a barrier
+    cursor_load(ring, c);
   }
 }
 
-// Persistent: CTA c takes items c, c + grid, ...  Each item (up to 1024
+// Persistent: CTAs claim items from the schedule.  Each item (up to 1024
 // tokens) streams through two shared-memory stages of 256 tokens, so the
 // copies of the next unit run while the current one is computed; the four
 // warps' partial results are merged once per item.
@@ -211,27 +234,33 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   __shared__ int page_ok_sh[2][16];
   __shared__ float red_m[kDecWarps][16], red_l[kDecWarps][16];
   __shared__ float mw[kDecWarps][16];   // merge weights exp2(m_w - m) / L per head
+  __shared__ ClaimRing ring;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   if (tid == 0) {
     mbar_init(&bars[0], 128);  // one cp.async arrival per thread
     mbar_init(&bars[1], 128);
     fence_barrier_init();
+    ring.n_valid = 0;
+    ring.done = 0;
   }
   __syncthreads();
   // issue cursor: two units ahead of the compute
   UnitCursor ic;
-  cursor_start(a, ic);
+  cursor_start(a, &ring, ic);
   for (int s = 0; s < 2 && ic.has; ++s) {
     issue_unit(a, ic.it, ic.u, unit_page(a, ic.it, ic.u, tid), dsmem + s * kStageBytes, &bars[s], page_ok_sh[s], tid);
-    cursor_next(a, ic);
+    cursor_next(a, &ring, ic);
   }
   DecItem it;
   uint4 qr[2][4];
-  if (decode_item(a, 0, it)) load_q_raw<G>(a, it, g, t, qr);
+  bool q_ready = false;  // qr holds the query rows of the next item to compute
   uint32_t uc = 0;  // units consumed: stage uc & 1, phase (uc >> 1) & 1
-  for (int k = 0; decode_item(a, k, it); ++k) {
+  for (int k = 0; k < ring.n_valid; ++k) {
+    it = item_of(ring.rec[k & 3]);
     const int b = it.b, h = it.h;
+    if (!q_ready) load_q_raw<G>(a, it, g, t, qr);
+    q_ready = false;
     // ---- query fragments from the rows loaded one item ahead ------------------
     // Lane (g, t) owns d = 32t .. 32t+31 of heads g and g+8.
     uint32_t qa[8][4];
@@ -262,10 +291,6 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
         qa[s][r + 2] = pack_f16x2(x[4 * s + 2] * up, x[4 * s + 3] * up);
       }
     }
-    {
-      DecItem nx1;
-      if (decode_item(a, k + 1, nx1)) load_q_raw<G>(a, nx1, g, t, qr);
-    }
 
     // Row state per query head (rows g and g+8 of the QK tile); every lane of
     // a quad holds the same running max, and a partial sum over its tokens.
@@ -286,8 +311,13 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
       uint8_t* sVs = sV + kSplitBytesK;
       const int* page_ok = page_ok_sh[stg];
       const int n_tok = unit_tokens(it, u);
-      // the page this thread gathers for the unit issued after this one
+      // the page this thread gathers for the unit issued after this one, and
+      // the next item's query rows once that item is claimed
       const int pid_next = ic.has ? unit_page(a, ic.it, ic.u, tid) : -1;
+      if (!q_ready && k + 1 < ring.n_valid) {
+        load_q_raw<G>(a, item_of(ring.rec[(k + 1) & 3]), g, t, qr);
+        q_ready = true;
+      }
       const bool ok = mbar_wait(&bars[stg], (uc >> 1) & 1, a.status);
       const int n_chunks = ok ? (n_tok + 15) / 16 : 0;
       for (int c = warp; c < n_chunks; c += kDecWarps) {
@@ -444,7 +474,7 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
       __syncthreads();  // every thread is done with this stage
       if (ic.has) {
         issue_unit(a, ic.it, ic.u, pid_next, dsmem + stg * kStageBytes, &bars[stg], page_ok_sh[stg], tid);
-        cursor_next(a, ic);
+        cursor_next(a, &ring, ic);
       }
     }
   }
@@ -520,7 +550,10 @@ __global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
     full_carry += ftot;
     part_carry += ptot;
   }
-  if (tid == 0) a.sched[0] = full_carry + part_carry;
+  if (tid == 0) {
+    a.sched[0] = full_carry + part_carry;
+    a.sched[1] = 0;  // claim counter of the attention kernel
+  }
 }
 
 // Merge the split partials of requests with more than one split; write zeros
