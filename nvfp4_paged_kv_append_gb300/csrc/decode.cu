@@ -528,25 +528,40 @@ __global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
     block_exclusive_scan(full, warp_sums, &tot);
     n_full_total += tot;
   }
-  // pass 2: write the records
+  // pass 2: write the records; the whole block shares each chunk of requests
+  __shared__ int req_first[1024], req_fpos[1024], req_ppos[1024];
   int full_carry = 0, part_carry = 0;
   for (int base = 0; base < a.batch; base += blockDim.x) {
     const int b = base + tid;
-    int full = 0, part = 0, kv_len = 0;
+    int full = 0, part = 0;
     if (b < a.batch) {
-      kv_len = a.kv_lens[b];
+      const int kv_len = a.kv_lens[b];
       if (kv_len > 0 && kv_len <= a.max_pages * kPageSize) {
         full = kv_len / kDecSplit;
         part = (kv_len % kDecSplit) ? 1 : 0;
       }
     }
-    int ftot, ptot;
-    const int fpos = full_carry + block_exclusive_scan(full * a.num_kv_heads, warp_sums, &ftot);
-    const int ppos = n_full_total + part_carry + block_exclusive_scan(part * a.num_kv_heads, warp_sums, &ptot);
-    for (int sp = 0; sp < full; ++sp)
-      for (int h = 0; h < a.num_kv_heads; ++h) items[fpos + sp * a.num_kv_heads + h] = make_int4(b, h, sp, kDecSplit);
-    if (part)
-      for (int h = 0; h < a.num_kv_heads; ++h) items[ppos + h] = make_int4(b, h, full, kv_len - full * kDecSplit);
+    int ftot, ptot, rtot;
+    req_fpos[tid] = full_carry + block_exclusive_scan(full * a.num_kv_heads, warp_sums, &ftot);
+    req_ppos[tid] = n_full_total + part_carry + block_exclusive_scan(part * a.num_kv_heads, warp_sums, &ptot);
+    req_first[tid] = block_exclusive_scan((full + part) * a.num_kv_heads, warp_sums, &rtot);
+    __syncthreads();
+    const int n_req = min(static_cast<int>(blockDim.x), a.batch - base);
+    for (int i = tid; i < rtot; i += blockDim.x) {
+      int lo = 0, hi = n_req - 1;  // last request of the chunk with req_first <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (req_first[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      const int rb = base + lo;
+      const int kv_len = a.kv_lens[rb];
+      const int rfull = kv_len / kDecSplit;
+      const int j = i - req_first[lo];
+      const int sp = j / a.num_kv_heads, h = j - sp * a.num_kv_heads;
+      if (sp < rfull) items[req_fpos[lo] + sp * a.num_kv_heads + h] = make_int4(rb, h, sp, kDecSplit);
+      else items[req_ppos[lo] + h] = make_int4(rb, h, rfull, kv_len - rfull * kDecSplit);
+    }
+    __syncthreads();
     full_carry += ftot;
     part_carry += ptot;
   }
@@ -557,9 +572,13 @@ __global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
 }
 
 // Merge the split partials of requests with more than one split; write zeros
-// for empty requests.
+// for empty requests.  One CTA per (q head, request), one thread per head
+// dimension: the splits' weights exp2(lse_s - m) are computed once into
+// shared memory, then each thread sums its column with independent loads.
 __global__ void __launch_bounds__(128) nvfp4_decode_combine_kernel(DecodeArgs a) {
-  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  extern __shared__ float wsh[];  // [max_splits] split weights
+  __shared__ float red[4];
+  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, warp = d >> 5;
   const int kv_len = a.kv_lens[b];
   const int64_t orow = (static_cast<int64_t>(b) * a.num_q_heads + hq) * kHeadDim;
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
@@ -572,15 +591,41 @@ __global__ void __launch_bounds__(128) nvfp4_decode_combine_kernel(DecodeArgs a)
   if (n_s <= 1) return;
   const int64_t base = static_cast<int64_t>(b) * a.max_splits * a.num_q_heads + hq;
   float m = -INFINITY;
-  for (int s = 0; s < n_s; ++s) m = fmaxf(m, a.part_lse[base + static_cast<int64_t>(s) * a.num_q_heads]);
-  const float mu = (m == -INFINITY) ? 0.0f : m;
-  float L = 0.0f, acc = 0.0f;
-  for (int s = 0; s < n_s; ++s) {
-    const int64_t pi = base + static_cast<int64_t>(s) * a.num_q_heads;
-    const float w = fast_exp2(a.part_lse[pi] - mu);
-    L += w;
-    acc += w * a.part_o[pi * kHeadDim + d];
+  for (int sp = d; sp < n_s; sp += blockDim.x) {
+    const float v = a.part_lse[base + static_cast<int64_t>(sp) * a.num_q_heads];
+    wsh[sp] = v;
+    m = fmaxf(m, v);
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  const float mu = (m == -INFINITY) ? 0.0f : m;
+  __syncthreads();
+  float L = 0.0f;
+  for (int sp = d; sp < n_s; sp += blockDim.x) {
+    const float w = fast_exp2(wsh[sp] - mu);
+    wsh[sp] = w;
+    L += w;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  if (lane == 0) red[warp] = L;
+  __syncthreads();
+  L = (red[0] + red[1]) + (red[2] + red[3]);
+  float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
+  const float* po = a.part_o + base * kHeadDim + d;
+  const int64_t stride = static_cast<int64_t>(a.num_q_heads) * kHeadDim;
+  int sp = 0;
+  for (; sp + 3 < n_s; sp += 4) {
+    acc0 += wsh[sp] * po[sp * stride];
+    acc1 += wsh[sp + 1] * po[(sp + 1) * stride];
+    acc2 += wsh[sp + 2] * po[(sp + 2) * stride];
+    acc3 += wsh[sp + 3] * po[(sp + 3) * stride];
+  }
+  for (; sp < n_s; ++sp) acc0 += wsh[sp] * po[sp * stride];
+  const float acc = (acc0 + acc1) + (acc2 + acc3);
   const float on = (L > 0.0f) ? acc / L : 0.0f;
   o[orow + d] = __float2bfloat16_rn(on * a.v_g);
   if (a.lse && d == 0) a.lse[static_cast<int64_t>(b) * a.num_q_heads + hq] = (L > 0.0f) ? (mu + __log2f(L)) * kLn2 : -INFINITY;
@@ -596,7 +641,13 @@ cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStr
   nvfp4_paged_decode_kernel<G><<<num_sms * kDecCtasPerSm, 128, kDecSmem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  nvfp4_decode_combine_kernel<<<dim3(a.num_q_heads, batch), 128, 0, s>>>(a);
+  const size_t wbytes = static_cast<size_t>(a.max_splits) * sizeof(float);  // split weights
+  if (wbytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(nvfp4_decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(wbytes));
+    if (e != cudaSuccess) return e;
+  }
+  nvfp4_decode_combine_kernel<<<dim3(a.num_q_heads, batch), 128, wbytes, s>>>(a);
   return cudaGetLastError();
 }
 
