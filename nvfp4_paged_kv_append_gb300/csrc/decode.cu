@@ -86,11 +86,20 @@ __device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t sc, uint32_t (&out)
 // than this (P <= 2^15 stays inside FP16)
 constexpr float kDecRescaleThreshold = 15.0f;
 
-constexpr int kSplitBytesK = kDecUnit * 64;
-constexpr int kSplitBytesS = kDecUnit * 8;
+constexpr int kUnit = kDecUnit;
+constexpr int kPagesPerUnit = kUnit / kPageSize;
+constexpr int kThrPerPage = 128 / kPagesPerUnit;  // gather threads per page
+constexpr int kSplitBytesK = kUnit * 64;
+constexpr int kSplitBytesS = kUnit * 8;
 constexpr int kStageBytes = 2 * (kSplitBytesK + kSplitBytesS);  // 36 KB: K, K scales, V, V scales
 constexpr int kDecCtasPerSm = 3;
 constexpr int kDecSmem = 2 * kStageBytes + 1024;                 // two stages + alignment slack
+// The four warps' partial O are merged through the stage just consumed:
+// [warp][head][kRedRow] fp32, rows padded by two words so that the
+// accumulator stores of a warp spread over the banks.
+constexpr int kRedRow = kHeadDim + 2;
+static_assert(kDecWarps * 16 * kRedRow * 4 <= kStageBytes, "merge buffer fits one stage");
+static_assert(kThrPerPage == 8 || kThrPerPage == 16, "gather split");
 
 struct DecItem {
   int b, h, split, n_tok, n_units;
@@ -105,7 +114,7 @@ __device__ __forceinline__ DecItem item_of(int4 r) {
   it.h = r.y;
   it.split = r.z;
   it.n_tok = r.w;
-  it.n_units = (r.w + kDecUnit - 1) / kDecUnit;
+  it.n_units = (r.w + kUnit - 1) / kUnit;
   return it;
 }
 
@@ -132,26 +141,26 @@ __device__ __forceinline__ void claim_item(const DecodeArgs& a, ClaimRing* ring)
 }
 
 // Tokens of unit u of an item (at most 256 = 16 pages).
-__device__ __forceinline__ int unit_tokens(const DecItem& it, int u) { return min(kDecUnit, it.n_tok - u * kDecUnit); }
+__device__ __forceinline__ int unit_tokens(const DecItem& it, int u) { return min(kUnit, it.n_tok - u * kUnit); }
 
 // Raw page id of the page this thread gathers for unit u of an item (page
 // tid / 8 of the unit), or -1 past the unit.  Loaded one unit ahead so that
 // the global-load latency is off the path of the gather; checked there.
 __device__ __forceinline__ int unit_page(const DecodeArgs& a, const DecItem& it, int u, int tid) {
-  const int p = tid >> 3;
+  const int p = tid / kThrPerPage;
   if (p * kPageSize >= unit_tokens(it, u)) return -1;
-  return a.page_table[static_cast<int64_t>(it.b) * a.max_pages + (it.split * kDecSplit + u * kDecUnit) / kPageSize + p];
+  return a.page_table[static_cast<int64_t>(it.b) * a.max_pages + (it.split * kDecSplit + u * kUnit) / kPageSize + p];
 }
 
 // All 128 threads gather unit u of an item into `stage` with cp.async: thread
 // t serves page t / 8 (K and V codes, 16 B at a time, plus one 16-byte piece
-// of each scale page).  A page with an invalid id (flagged) reads as zeros,
+// of each scale page; V code rows are permuted, see the PV step).  A page with an invalid id (flagged) reads as zeros,
 // and so do the V scales of tokens past the item's end -- their values are
 // then exactly 0 whatever codes the page holds.  Each thread arrives on `bar`
 // once its copies land.
 __device__ __forceinline__ void issue_unit(const DecodeArgs& a, const DecItem& it, int u, int pid, uint8_t* stage,
                                            uint64_t* bar, int* page_ok, int tid) {
-  const int p = tid >> 3, sub = tid & 7;
+  const int p = tid / kThrPerPage, sub = tid % kThrPerPage;
   const int n_tok = unit_tokens(it, u);
   if (p * kPageSize < n_tok) {
     if (pid >= a.num_pages || pid < 0) {
@@ -160,21 +169,23 @@ __device__ __forceinline__ void issue_unit(const DecodeArgs& a, const DecItem& i
     }
     if (sub == 0) page_ok[p] = pid >= 0;
     const uint32_t n16 = pid >= 0 ? 16u : 0u;
-    // V scales of tokens 2 sub, 2 sub + 1 of this page: 8 bytes per live token
-    const int live = min(max(n_tok - p * kPageSize - 2 * sub, 0), 2);
+    // V scales of tokens 2 ps, 2 ps + 1 of this page: 8 bytes per live token
+    const int ps = sub & 7;
+    const int live = min(max(n_tok - p * kPageSize - 2 * ps, 0), 2);
     const uint32_t nvs = pid >= 0 ? 8u * live : 0u;
     const int64_t row = (static_cast<int64_t>(pid >= 0 ? pid : 0) * a.num_kv_heads + it.h) * kPageSize;
     const uint32_t sK = smem_u32(stage), sKs = sK + kSplitBytesK, sV = sKs + kSplitBytesS, sVs = sV + kSplitBytesK;
     const uint8_t* gk = a.k_data + row * 64;
     const uint8_t* gv = a.v_data + row * 64;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int c = sub + 8 * i;
+    for (int i = 0; i < 64 / kThrPerPage; ++i) {
+      const int c = sub + kThrPerPage * i;
+      const int vrow = c >> 2, vprow = vrow ^ ((vrow >> 1) & 1);  // V row permutation (bank spread)
       cp_async16(sK + p * 1024 + c * 16, gk + c * 16, n16);
-      cp_async16(sV + p * 1024 + c * 16, gv + c * 16, n16);
+      cp_async16(sV + p * 1024 + (vprow * 4 + (c & 3)) * 16, gv + c * 16, n16);
     }
-    cp_async16(sKs + p * 128 + sub * 16, a.k_scale + row * 8 + sub * 16, n16);
-    cp_async16(sVs + p * 128 + sub * 16, a.v_scale + row * 8 + sub * 16, nvs);
+    if (kThrPerPage == 8 || sub < 8) cp_async16(sKs + p * 128 + ps * 16, a.k_scale + row * 8 + ps * 16, n16);
+    if (kThrPerPage == 8 || sub >= 8) cp_async16(sVs + p * 128 + ps * 16, a.v_scale + row * 8 + ps * 16, nvs);
   }
   cp_async_mbar_arrive(bar);
 }
@@ -231,7 +242,7 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   extern __shared__ __align__(128) uint8_t dsmem_raw[];
   uint8_t* dsmem = dsmem_raw + ((128u - (smem_u32(dsmem_raw) & 127u)) & 127u);
   __shared__ uint64_t bars[2];
-  __shared__ int page_ok_sh[2][16];
+  __shared__ int page_ok_sh[2][kPagesPerUnit];
   __shared__ float red_m[kDecWarps][16], red_l[kDecWarps][16];
   __shared__ float mw[kDecWarps][16];   // merge weights exp2(m_w - m) / L per head
   __shared__ ClaimRing ring;
@@ -245,6 +256,8 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
     ring.done = 0;
   }
   __syncthreads();
+  grid_dep_launch();  // the combine grid may be scheduled as CTAs finish
+  grid_dep_wait();    // the schedule written by the plan kernel
   // issue cursor: two units ahead of the compute
   UnitCursor ic;
   cursor_start(a, &ring, ic);
@@ -331,7 +344,8 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
           const int tok = cbase + 8 * nt + g;
           const uint4 kc = *reinterpret_cast<const uint4*>(sK + tok * 64 + 16 * t);
           const uint32_t ks = *reinterpret_cast<const uint16_t*>(sKs + tok * 8 + 2 * t);
-          const uint32_t sc0 = scale_f16x2(ks & 0xFFu), sc1 = scale_f16x2(ks >> 8);
+          const uint32_t hs = cvt_e4m3x2_to_f16x2(ks);
+          const uint32_t sc0 = prmt(hs, hs, 0x1010u), sc1 = prmt(hs, hs, 0x3232u);
           const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {
@@ -354,13 +368,14 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
             const int tok = cbase + 8 * (i >> 1) + 2 * t + (i & 1);
             x[i] = (page_valid && tok < n_tok) ? s[i >> 1][2 * r + (i & 1)] * crow[r] : -INFINITY;
           }
+          // The running max moves only when the chunk exceeds it by more than
+          // 2^15, so P stays inside FP16.  A quad's max can pass that bound
+          // only if one of its lanes does, so the quad reduction runs only then.
           float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
-          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
-          // the running max moves only when the chunk exceeds it by more than
-          // 2^15, so P stays inside FP16
-          const bool need = cm > m_run[r] + kDecRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
+          if (__any_sync(0xffffffffu, cm > m_run[r] + kDecRescaleThreshold)) {
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+            const bool need = cm > m_run[r] + kDecRescaleThreshold;
             const float alpha = need ? fast_exp2(m_run[r] - cm) : 1.0f;  // 0 when m_run = -inf
             if (need) m_run[r] = cm;
             l_run[r] *= alpha;
@@ -384,20 +399,40 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
         }
         // ---- O^T += V^T P^T: A = V^T (rows: head dims, k: tokens), B = P^T
         // Lane (g, t) needs tokens 2t, 2t+1, 8+2t, 9+2t at code bytes 8g..8g+7
-        // (head dims 16g..16g+15: one scale block).
-        uint32_t v[4][8];
+        // (head dims 16g..16g+15: one scale block).  The nibbles of a token
+        // pair (a, b) are interleaved byte by byte before conversion, so each
+        // converted f16 pair is (token a, token b) at one head dimension: an
+        // A-fragment register as it stands.  The pair's two scales form one
+        // f16x2 multiplier.  V rows sit in shared memory with row r stored at
+        // r ^ ((r >> 1) & 1), so the four rows 2t + c of a load hit both
+        // halves of the banks.
+        uint32_t va[2][16];  // [pair][2j + e]: head dim 16g + 2j + e, j = 0..7
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int tok = cbase + 8 * (q4 >> 1) + 2 * t + (q4 & 1);
-          const uint2 vc = *reinterpret_cast<const uint2*>(sV + tok * 64 + 8 * g);
-          const uint32_t sc = scale_f16x2(sVs[tok * 8 + g]);
-          dq4_f16(vc.x, sc, *reinterpret_cast<uint32_t(*)[4]>(&v[q4][0]));
-          dq4_f16(vc.y, sc, *reinterpret_cast<uint32_t(*)[4]>(&v[q4][4]));
+        for (int tp = 0; tp < 2; ++tp) {
+          const int tok_a = cbase + 8 * tp + 2 * t;
+          const uint2 ca = *reinterpret_cast<const uint2*>(sV + (tok_a ^ (t & 1)) * 64 + 8 * g);
+          const uint2 cb = *reinterpret_cast<const uint2*>(sV + ((tok_a + 1) ^ (t & 1)) * 64 + 8 * g);
+          const uint32_t sab =
+              static_cast<uint32_t>(sVs[tok_a * 8 + g]) | (static_cast<uint32_t>(sVs[(tok_a + 1) * 8 + g]) << 8);
+          const uint32_t sc = cvt_e4m3x2_to_f16x2(sab);
+          const uint32_t wa[2] = {ca.x, ca.y}, wb[2] = {cb.x, cb.y};
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t ev = (wa[h2] & 0x0F0F0F0Fu) | ((wb[h2] << 4) & 0xF0F0F0F0u);
+            const uint32_t od = ((wa[h2] >> 4) & 0x0F0F0F0Fu) | (wb[h2] & 0xF0F0F0F0u);
+            uint32_t e4[4], o4[4];
+            dq4_f16(ev, sc, e4);
+            dq4_f16(od, sc, o4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              va[tp][2 * (4 * h2 + i)] = e4[i];
+              va[tp][2 * (4 * h2 + i) + 1] = o4[i];
+            }
+          }
         }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t a0 = prmt(v[0][mt], v[1][mt], 0x5410u), a1 = prmt(v[0][mt], v[1][mt], 0x7632u);
-          const uint32_t a2 = prmt(v[2][mt], v[3][mt], 0x5410u), a3 = prmt(v[2][mt], v[3][mt], 0x7632u);
+          const uint32_t a0 = va[0][2 * mt], a1 = va[0][2 * mt + 1], a2 = va[1][2 * mt], a3 = va[1][2 * mt + 1];
 #pragma unroll
           for (int nb = 0; nb < kHeadBlocks; ++nb)
             mma_f16_16816(acc[nb][mt][0], acc[nb][mt][1], acc[nb][mt][2], acc[nb][mt][3], a0, a1, a2, a3, pb[nb][0],
@@ -413,20 +448,22 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
           l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
         }
         __syncthreads();  // every warp is done reading the stage
-        float* red_o = reinterpret_cast<float*>(sK);  // [warp][16 heads][128]: 32 KB of the 36 KB stage
+        float* red_o = reinterpret_cast<float*>(sK);  // [warp][G][kRedRow]
 #pragma unroll
         for (int r = 0; r < kHeadBlocks; ++r) {
           if (t == 0) {
             red_m[warp][g + 8 * r] = m_run[r];
             red_l[warp][g + 8 * r] = l_run[r];
           }
+          if (8 * r + 2 * t < G) {
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            const int d = 16 * g + 2 * mt;
-            float* o0 = red_o + (warp * 16 + 8 * r + 2 * t) * kHeadDim;
-            float* o1 = o0 + kHeadDim;
-            *reinterpret_cast<float2*>(o0 + d) = make_float2(acc[r][mt][0], acc[r][mt][2]);
-            *reinterpret_cast<float2*>(o1 + d) = make_float2(acc[r][mt][1], acc[r][mt][3]);
+            for (int mt = 0; mt < 8; ++mt) {
+              const int d = 16 * g + 2 * mt;
+              float* o0 = red_o + (warp * G + 8 * r + 2 * t) * kRedRow;
+              *reinterpret_cast<float2*>(o0 + d) = make_float2(acc[r][mt][0], acc[r][mt][2]);
+              if (8 * r + 2 * t + 1 < G)
+                *reinterpret_cast<float2*>(o0 + kRedRow + d) = make_float2(acc[r][mt][1], acc[r][mt][3]);
+            }
           }
         }
         __syncthreads();
@@ -461,7 +498,7 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
           const int head = i >> 7, d = i & 127;
           float on = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kDecWarps; ++w) on += red_o[(w * 16 + head) * kHeadDim + d] * mw[w][head];
+          for (int w = 0; w < kDecWarps; ++w) on += red_o[(w * G + head) * kRedRow + d] * mw[w][head];
           const int hq = h * G + head;
           if (single) {
             reinterpret_cast<__nv_bfloat16*>(a.o)[(static_cast<int64_t>(b) * a.num_q_heads + hq) * kHeadDim + d] =
@@ -480,90 +517,108 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   }
 }
 
-// Block-wide exclusive prefix sum over the 1024 threads (returns the exclusive
-// value; *total receives the sum).
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+// Block-wide exclusive prefix sums of two counts over the 1024 threads
+// (returns the exclusive values; *total receives the sums).
+__device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2* warp_sums, int2* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int x = v;
+  int2 x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += n;
+    const int nx = __shfl_up_sync(0xffffffffu, x.x, o), ny = __shfl_up_sync(0xffffffffu, x.y, o);
+    if (lane >= o) {
+      x.x += nx;
+      x.y += ny;
+    }
   }
   if (lane == 31) warp_sums[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    int w = warp_sums[lane];
+    int2 w = warp_sums[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += n;
+      const int nx = __shfl_up_sync(0xffffffffu, w.x, o), ny = __shfl_up_sync(0xffffffffu, w.y, o);
+      if (lane >= o) {
+        w.x += nx;
+        w.y += ny;
+      }
     }
     warp_sums[lane] = w;
   }
   __syncthreads();
-  const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0);
+  const int2 before = wid > 0 ? warp_sums[wid - 1] : make_int2(0, 0);
   *total = warp_sums[31];
   __syncthreads();
-  return incl - v;
+  return make_int2(x.x + before.x - v.x, x.y + before.y - v.y);
 }
 
-// Schedule: one record per (request, kv head, 1024-token split), full splits
-// first, then each request's shorter last split.
+// Schedule: one record per (request, kv head, 1024-token split).  All full
+// splits come first; then each request's shorter last split, longest first,
+// so that the items claimed last are the shortest.  Requests are taken 1024 at
+// a time (one pass for the usual batch sizes); the longest-first order holds
+// within each such chunk.
 __global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
-  __shared__ int warp_sums[32];
+  grid_dep_launch();  // the attention grid may start its prologue now
+  __shared__ int2 warp_sums[32];
+  __shared__ int req_len[1024], req_first[1024], req_fpos[1024], req_ppos[1024];
   int4* items = reinterpret_cast<int4*>(a.sched + 4);
-  const int tid = threadIdx.x;
-  // pass 1: total full items (to place the short ones after them)
+  const int tid = threadIdx.x, H = a.num_kv_heads, cap = a.max_pages * kPageSize;
+  // total of the full items of all requests (the partial ones follow them)
   int n_full_total = 0;
-  for (int base = 0; base < a.batch; base += blockDim.x) {
-    const int b = base + tid;
-    int full = 0;
-    if (b < a.batch) {
-      const int kv_len = a.kv_lens[b];
-      if (kv_len > a.max_pages * kPageSize) set_status(a.status, kDevBadShape);
-      else if (kv_len > 0) full = (kv_len / kDecSplit) * a.num_kv_heads;
+  if (a.batch > static_cast<int>(blockDim.x)) {
+    for (int base = 0; base < a.batch; base += blockDim.x) {
+      const int b = base + tid;
+      const int kv_len = b < a.batch ? a.kv_lens[b] : 0;
+      int2 tot;
+      block_exclusive_scan2(make_int2(kv_len > 0 && kv_len <= cap ? kv_len / kDecSplit : 0, 0), warp_sums, &tot);
+      n_full_total += tot.x * H;
     }
-    int tot;
-    block_exclusive_scan(full, warp_sums, &tot);
-    n_full_total += tot;
   }
-  // pass 2: write the records; the whole block shares each chunk of requests
-  __shared__ int req_first[1024], req_fpos[1024], req_ppos[1024];
   int full_carry = 0, part_carry = 0;
   for (int base = 0; base < a.batch; base += blockDim.x) {
     const int b = base + tid;
-    int full = 0, part = 0;
+    const int n_req = min(static_cast<int>(blockDim.x), a.batch - base);
+    int kv_len = 0;
     if (b < a.batch) {
-      const int kv_len = a.kv_lens[b];
-      if (kv_len > 0 && kv_len <= a.max_pages * kPageSize) {
-        full = kv_len / kDecSplit;
-        part = (kv_len % kDecSplit) ? 1 : 0;
+      kv_len = a.kv_lens[b];
+      if (kv_len > cap) set_status(a.status, kDevBadShape);
+      if (kv_len < 0 || kv_len > cap) kv_len = 0;
+    }
+    const int full = kv_len / kDecSplit, plen = kv_len % kDecSplit;
+    req_len[tid] = plen;
+    int2 tot;
+    const int2 ex = block_exclusive_scan2(make_int2(full, plen > 0 ? 1 : 0), warp_sums, &tot);
+    if (a.batch <= static_cast<int>(blockDim.x)) n_full_total = tot.x * H;
+    // rank of this request's last split among the chunk's: longer first,
+    // then request order
+    int rank = 0;
+    if (plen > 0) {
+      for (int j = 0; j < n_req; ++j) {
+        const int lj = req_len[j];
+        rank += (lj > plen || (lj == plen && j < tid)) ? 1 : 0;
       }
     }
-    int ftot, ptot, rtot;
-    req_fpos[tid] = full_carry + block_exclusive_scan(full * a.num_kv_heads, warp_sums, &ftot);
-    req_ppos[tid] = n_full_total + part_carry + block_exclusive_scan(part * a.num_kv_heads, warp_sums, &ptot);
-    req_first[tid] = block_exclusive_scan((full + part) * a.num_kv_heads, warp_sums, &rtot);
+    __syncthreads();  // every thread has read req_len
+    req_len[tid] = kv_len;
+    req_fpos[tid] = full_carry + ex.x * H;
+    req_ppos[tid] = n_full_total + part_carry + rank * H;
+    req_first[tid] = (ex.x + ex.y) * H;
     __syncthreads();
-    const int n_req = min(static_cast<int>(blockDim.x), a.batch - base);
+    const int rtot = (tot.x + tot.y) * H;
     for (int i = tid; i < rtot; i += blockDim.x) {
       int lo = 0, hi = n_req - 1;  // last request of the chunk with req_first <= i
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (req_first[mid] <= i) lo = mid; else hi = mid - 1;
       }
-      const int rb = base + lo;
-      const int kv_len = a.kv_lens[rb];
-      const int rfull = kv_len / kDecSplit;
+      const int len = req_len[lo], rfull = len / kDecSplit;
       const int j = i - req_first[lo];
-      const int sp = j / a.num_kv_heads, h = j - sp * a.num_kv_heads;
-      if (sp < rfull) items[req_fpos[lo] + sp * a.num_kv_heads + h] = make_int4(rb, h, sp, kDecSplit);
-      else items[req_ppos[lo] + h] = make_int4(rb, h, rfull, kv_len - rfull * kDecSplit);
+      const int sp = j / H, h = j - sp * H;
+      if (sp < rfull) items[req_fpos[lo] + sp * H + h] = make_int4(base + lo, h, sp, kDecSplit);
+      else items[req_ppos[lo] + h] = make_int4(base + lo, h, rfull, len - rfull * kDecSplit);
     }
     __syncthreads();
-    full_carry += ftot;
-    part_carry += ptot;
+    full_carry += tot.x * H;
+    part_carry += tot.y * H;
   }
   if (tid == 0) {
     a.sched[0] = full_carry + part_carry;
@@ -578,11 +633,12 @@ __global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
 __global__ void __launch_bounds__(128) nvfp4_decode_combine_kernel(DecodeArgs a) {
   extern __shared__ float wsh[];  // [max_splits] split weights
   __shared__ float red[4];
+  grid_dep_wait();  // the attention kernel's partials
   const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, warp = d >> 5;
   const int kv_len = a.kv_lens[b];
   const int64_t orow = (static_cast<int64_t>(b) * a.num_q_heads + hq) * kHeadDim;
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
-  if (kv_len <= 0) {
+  if (kv_len <= 0 || kv_len > a.max_pages * kPageSize) {  // empty, or flagged by the plan
     o[orow + d] = __float2bfloat16_rn(0.0f);
     if (a.lse && d == 0) a.lse[static_cast<int64_t>(b) * a.num_q_heads + hq] = -INFINITY;
     return;
@@ -628,7 +684,25 @@ __global__ void __launch_bounds__(128) nvfp4_decode_combine_kernel(DecodeArgs a)
   const float acc = (acc0 + acc1) + (acc2 + acc3);
   const float on = (L > 0.0f) ? acc / L : 0.0f;
   o[orow + d] = __float2bfloat16_rn(on * a.v_g);
-  if (a.lse && d == 0) a.lse[static_cast<int64_t>(b) * a.num_q_heads + hq] = (L > 0.0f) ? (mu + __log2f(L)) * kLn2 : -INFINITY;
+  if (a.lse && d == 0)
+    a.lse[static_cast<int64_t>(b) * a.num_q_heads + hq] = (L > 0.0f) ? (mu + __log2f(L)) * kLn2 : -INFINITY;
+}
+
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous one in the stream finishes, and waits for it in grid_dep_wait.
+cudaError_t launch_dependent(void (*kernel)(DecodeArgs), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             const DecodeArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 template <int G>
@@ -638,8 +712,7 @@ cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStr
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(nvfp4_paged_decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;
-  nvfp4_paged_decode_kernel<G><<<num_sms * kDecCtasPerSm, 128, kDecSmem, s>>>(a);
-  e = cudaGetLastError();
+  e = launch_dependent(nvfp4_paged_decode_kernel<G>, dim3(num_sms * kDecCtasPerSm), dim3(128), kDecSmem, s, a);
   if (e != cudaSuccess) return e;
   const size_t wbytes = static_cast<size_t>(a.max_splits) * sizeof(float);  // split weights
   if (wbytes > 48 * 1024) {
@@ -647,8 +720,7 @@ cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStr
                              static_cast<int>(wbytes));
     if (e != cudaSuccess) return e;
   }
-  nvfp4_decode_combine_kernel<<<dim3(a.num_q_heads, batch), 128, wbytes, s>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(nvfp4_decode_combine_kernel, dim3(a.num_q_heads, batch), dim3(128), wbytes, s, a);
 }
 
 }  // namespace

@@ -299,6 +299,14 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2_to_f16x2(uint32_t byte) {
   asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(out) : "r"(byte));
   return out;
 }
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start before the previous kernel in the stream ends;
+// grid_dep_wait() blocks until that kernel has completed and its memory
+// writes are visible (it returns at once for an ordinary launch).
+// grid_dep_launch() lets the next such kernel start launching early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Two E4M3 bytes (low byte -> low half) -> f16x2 (exact).
 __device__ __forceinline__ uint32_t cvt_e4m3x2_to_f16x2(uint32_t two_bytes) {
   uint32_t out;

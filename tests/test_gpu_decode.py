@@ -70,3 +70,38 @@ def test_decode_empty_request():
                              sm_scale=inp.sm_scale)
     torch.cuda.synchronize()
     assert float(o[0].abs().max()) == 0.0
+
+
+def test_decode_more_than_1024_requests():
+    """1,100 requests (the schedule takes them 1,024 at a time), mostly short
+    with some over two splits; sampled requests against the oracle."""
+    rng = np.random.default_rng(21)
+    kv = rng.integers(1, 200, size=1100)
+    long_ = rng.choice(1100, size=60, replace=False)
+    kv[long_] = rng.integers(1025, 2600, size=60)
+    wl = W.Workload("dec_1100", [1] * 1100, [int(x) for x in kv], 8, 2, seed=21)
+    sample = sorted({0, 1023, 1024, 1099, int(kv.argmax())} | {int(x) for x in long_[:6]})
+    mx, fro, lerr, _, _ = _decode_case(wl, sample=sample)
+    assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
+    assert lerr <= 1e-3, lerr
+
+
+def test_decode_kv_len_beyond_table_flagged():
+    """A kv_len longer than the page table allows is flagged (shape error);
+    that request's output is zero and the others are unaffected."""
+    wl = W.Workload("dec_bad", [1] * 3, [300, 1500, 40], 8, 2, seed=9)
+    inp = W.make_inputs(wl)
+    b = G.nk()
+    cache = G.gpu_cache(inp)
+    kvl = inp.kv_lens.clone()
+    kvl[1] = inp.page_table.shape[1] * 16 + 1
+    o = b.nvfp4_paged_decode(inp.q.to(G.dev()), cache, inp.page_table.to(G.dev()), kvl.to(G.dev()),
+                             sm_scale=inp.sm_scale)
+    torch.cuda.synchronize()
+    assert b.nvfp4kv_get_device_status() == -2
+    got = o.float().cpu().numpy()
+    assert float(np.abs(got[1]).max()) == 0.0
+    pools = G.oracle_pools(inp)
+    ref = G.oracle_prefill(pools, inp, "bf16", causal=False, rows=[(0, 0), (2, 0)])
+    mx, fro, _ = G.compare_rows(got, ref, inp.qo_indptr)
+    assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
