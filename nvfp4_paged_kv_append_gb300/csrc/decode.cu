@@ -3,27 +3,31 @@
 // "Decode can win on fewer bytes read": decode re-reads the whole history and
 // is bandwidth-bound, so fewer bytes per token is the win).
 //
-// Split-KV: a work item is (request, kv head, 256-token split).  A small
-// schedule kernel turns kv_lens into per-request item prefixes; then one
-// persistent wave of CTAs (3 per SM) walks the items.  For each item all
-// threads gather its pages (K/V codes 1 KB + scales 128 B per page) with
-// cp.async into one of two shared-memory stages, completing on one mbarrier,
-// so the next item's bytes are in flight while the current one is computed.
-// (Per-page bulk copies cost the copy engine a fixed time each, which capped
-// the item rate; cp.async spreads the same bytes over the load units.)
+// Split-KV: a work item is (request, kv head, split of up to 1024 tokens).  A
+// schedule kernel writes one record per item, full splits first and then the
+// shorter last splits, longest first; one persistent wave of CTAs (3 per SM)
+// claims records from a counter.  An item streams through two shared-memory
+// stages of 256 tokens (K/V codes 1 KB + scales 128 B per page, gathered with
+// cp.async by all threads and completing on one mbarrier), so the next unit's
+// bytes are in flight while the current one is computed.  (Per-page bulk
+// copies cost the copy engine a fixed time each, which capped the rate;
+// cp.async spreads the same bytes over the load units.)  The schedule, the
+// attention kernel and the combine kernel are chained by programmatic
+// dependent launch.
 //
-// Four warps take 16-token chunks of the item; the packed codes are
-// dequantized (exactly: e2m1 x e4m3 fits f16) straight into MMA fragment
-// registers, so no dequantized copy of K or V is ever written.
-//   S = q K^T   m16n8k16 with the G query heads as the M rows and 8 tokens as
-//               N.  The head dimension is permuted inside the MMA's K index so
-//               that each lane's K fragment is 16 contiguous code bytes; the
-//               query carries the same permutation.
+// Four warps take 16-token chunks of a unit; the packed codes are dequantized
+// (exactly: e2m1 x e4m3 fits f16) straight into MMA fragment registers, so no
+// dequantized copy of K or V is ever written.
+//   S^T = K q^T   m16n8k16 with the chunk's 16 tokens as the M rows and the
+//               query heads as N.  The head dimension is permuted inside the
+//               MMA's K index so that each lane converts 16 contiguous code
+//               bytes of each of its two tokens; the query carries the same
+//               permutation.
 //   O^T += V^T P^T   m16n8k16 with head dimensions as the M rows (eight
-//               m-tiles), the chunk's 16 tokens as K and the heads as N.  The
-//               scores' accumulator layout is already P^T's operand layout, and
-//               lane (g, t) reads one 8-byte code run (head dims 16g..16g+15,
-//               one scale block) per token.
+//               m-tiles), the chunk's tokens as K and the heads as N.  P^T's
+//               operand comes from the scores by one 8x8 transpose
+//               (movmatrix) per token half, and lane (g, t) reads one 8-byte
+//               code run (head dims 16g..16g+15, one scale block) per token.
 // Queries are bf16; each head is multiplied by a power of two (exact) to sit
 // inside f16's range and the factor is removed from the scores in fp32.  The
 // running max moves lazily.  Partial (o, lse) per split are merged by a
@@ -54,6 +58,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// 8x8 transpose of b16 elements held in the MMA fragment layout: lane (g, t)
+// gives row g, columns 2t, 2t+1 and receives row g, columns 2t, 2t+1 of the
+// transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
   return r;
 }
 
@@ -275,15 +288,17 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
     if (!q_ready) load_q_raw<G>(a, it, g, t, qr);
     q_ready = false;
     // ---- query fragments from the rows loaded one item ahead ------------------
-    // Lane (g, t) owns d = 32t .. 32t+31 of heads g and g+8.
-    uint32_t qa[8][4];
-    float crow[2];
+    // B operand of S^T = K q^T: lane (g, t) owns head dims 32t .. 32t+31 of
+    // head g (+8 for the second block); MMA j's k positions 2t, 2t+1 are dims
+    // 32t + 4j + {0, 1} and positions 2t+8, 2t+9 are dims 32t + 4j + {2, 3}.
+    uint32_t qb[kHeadBlocks][8][2];
+    float crow[kHeadBlocks][2];  // score scale of heads 2t, 2t+1 (+8 nb)
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
+    for (int nb = 0; nb < kHeadBlocks; ++nb) {
       float x[32];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint4 w = qr[r][i];
+        const uint4 w = qr[nb][i];
         bf16x2_to_f32(w.x, x[8 * i + 0], x[8 * i + 1]);
         bf16x2_to_f32(w.y, x[8 * i + 2], x[8 * i + 3]);
         bf16x2_to_f32(w.z, x[8 * i + 4], x[8 * i + 5]);
@@ -297,17 +312,24 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
       // power of two bringing the head's amax into [2^14, 2^15): exact in f16
       const int e = (amax > 0.0f) ? (14 - ilogbf(amax)) : 0;
       const float up = ldexpf(1.0f, e);
-      crow[r] = a.sm_scale * a.k_g * kLog2e * ldexpf(1.0f, -e);
+      const float c_own = a.sm_scale * a.k_g * kLog2e * ldexpf(1.0f, -e);  // head g (+8 nb)
+      crow[nb][0] = __shfl_sync(0xffffffffu, c_own, 8 * t);
+      crow[nb][1] = __shfl_sync(0xffffffffu, c_own, 8 * t + 4);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        qa[s][r] = pack_f16x2(x[4 * s] * up, x[4 * s + 1] * up);
-        qa[s][r + 2] = pack_f16x2(x[4 * s + 2] * up, x[4 * s + 3] * up);
+      for (int j = 0; j < 8; ++j) {
+        qb[nb][j][0] = pack_f16x2(x[4 * j] * up, x[4 * j + 1] * up);
+        qb[nb][j][1] = pack_f16x2(x[4 * j + 2] * up, x[4 * j + 3] * up);
       }
     }
 
-    // Row state per query head (rows g and g+8 of the QK tile); every lane of
-    // a quad holds the same running max, and a partial sum over its tokens.
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+    // Row state of heads 2t, 2t+1 (+8 nb): all lanes of a column group t hold
+    // the same running max, and a partial sum over their own tokens.
+    float m_run[kHeadBlocks][2], l_run[kHeadBlocks][2];
+#pragma unroll
+    for (int nb = 0; nb < kHeadBlocks; ++nb) {
+      m_run[nb][0] = m_run[nb][1] = -INFINITY;
+      l_run[nb][0] = l_run[nb][1] = 0.0f;
+    }
     // O^T accumulators: m-tile mt holds head dims 16g + 2mt (row g) and
     // 16g + 2mt + 1 (row g+8) for heads 2t, 2t+1 (+8 for the second block)
     float acc[kHeadBlocks][8][4];
@@ -336,66 +358,86 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
       for (int c = warp; c < n_chunks; c += kDecWarps) {
         const int cbase = c * 16;
         const bool page_valid = page_ok[c] != 0;
-        // ---- S = q K^T; n-tile nt column n is token 8nt + n of the chunk
-        float s[2][4];
+        // ---- S^T = K q^T: m rows are the chunk's tokens (lane rows g, g+8),
+        // n columns the heads.  Each lane converts 16 code bytes of each of
+        // its two tokens, whose byte pairs are the A registers of MMAs 2wi and
+        // 2wi + 1.
+        float s[kHeadBlocks][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
-          const int tok = cbase + 8 * nt + g;
-          const uint4 kc = *reinterpret_cast<const uint4*>(sK + tok * 64 + 16 * t);
-          const uint32_t ks = *reinterpret_cast<const uint16_t*>(sKs + tok * 8 + 2 * t);
-          const uint32_t hs = cvt_e4m3x2_to_f16x2(ks);
-          const uint32_t sc0 = prmt(hs, hs, 0x1010u), sc1 = prmt(hs, hs, 0x3232u);
-          const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
+        for (int nb = 0; nb < kHeadBlocks; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.0f;
+        {
+          const int tok0 = cbase + g, tok1 = tok0 + 8;
+          const uint4 k0 = *reinterpret_cast<const uint4*>(sK + tok0 * 64 + 16 * t);
+          const uint4 k1 = *reinterpret_cast<const uint4*>(sK + tok1 * 64 + 16 * t);
+          const uint32_t hs0 = cvt_e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sKs + tok0 * 8 + 2 * t));
+          const uint32_t hs1 = cvt_e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sKs + tok1 * 8 + 2 * t));
+          const uint32_t sc0[2] = {prmt(hs0, hs0, 0x1010u), prmt(hs0, hs0, 0x3232u)};
+          const uint32_t sc1[2] = {prmt(hs1, hs1, 0x1010u), prmt(hs1, hs1, 0x3232u)};
+          const uint32_t kw0[4] = {k0.x, k0.y, k0.z, k0.w}, kw1[4] = {k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {
-            uint32_t hh[4];
-            dq4_f16(kw[wi], wi < 2 ? sc0 : sc1, hh);
-            mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[2 * wi][0], qa[2 * wi][1], qa[2 * wi][2],
-                          qa[2 * wi][3], hh[0], hh[1]);
-            mma_f16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa[2 * wi + 1][0], qa[2 * wi + 1][1],
-                          qa[2 * wi + 1][2], qa[2 * wi + 1][3], hh[2], hh[3]);
-          }
-        }
-        // ---- online softmax (log2 domain), lazy rescale; lane (g, t) holds
-        // tokens 2t, 2t+1, 8+2t, 9+2t of heads g (and g+8)
-        uint32_t pb[kHeadBlocks][2];
+            uint32_t h0[4], h1[4];
+            dq4_f16(kw0[wi], sc0[wi >> 1], h0);
+            dq4_f16(kw1[wi], sc1[wi >> 1], h1);
 #pragma unroll
-        for (int r = 0; r < kHeadBlocks; ++r) {
-          float x[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int tok = cbase + 8 * (i >> 1) + 2 * t + (i & 1);
-            x[i] = (page_valid && tok < n_tok) ? s[i >> 1][2 * r + (i & 1)] * crow[r] : -INFINITY;
-          }
-          // The running max moves only when the chunk exceeds it by more than
-          // 2^15, so P stays inside FP16.  A quad's max can pass that bound
-          // only if one of its lanes does, so the quad reduction runs only then.
-          float cm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-          if (__any_sync(0xffffffffu, cm > m_run[r] + kDecRescaleThreshold)) {
-            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
-            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
-            const bool need = cm > m_run[r] + kDecRescaleThreshold;
-            const float alpha = need ? fast_exp2(m_run[r] - cm) : 1.0f;  // 0 when m_run = -inf
-            if (need) m_run[r] = cm;
-            l_run[r] *= alpha;
-            // O^T columns are heads 2t, 2t+1: their factors live in quads 2t, 2t+1
-            const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t), a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              acc[r][mt][0] *= a0;
-              acc[r][mt][1] *= a1;
-              acc[r][mt][2] *= a0;
-              acc[r][mt][3] *= a1;
+            for (int nb = 0; nb < kHeadBlocks; ++nb) {
+              mma_f16_16816(s[nb][0], s[nb][1], s[nb][2], s[nb][3], h0[0], h1[0], h0[1], h1[1], qb[nb][2 * wi][0],
+                            qb[nb][2 * wi][1]);
+              mma_f16_16816(s[nb][0], s[nb][1], s[nb][2], s[nb][3], h0[2], h1[2], h0[3], h1[3],
+                            qb[nb][2 * wi + 1][0], qb[nb][2 * wi + 1][1]);
             }
           }
-          const float m_use = (m_run[r] == -INFINITY) ? 0.0f : m_run[r];
-          float p[4];
+        }
+        // ---- online softmax (log2 domain), lazy rescale.  Lane (g, t) holds
+        // tokens g and g+8 of heads 2t, 2t+1 (+8 nb).
+        const int lim = page_valid ? n_tok - cbase : 0;
+        const bool live0 = g < lim, live1 = g + 8 < lim;
+        uint32_t pb[kHeadBlocks][2];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_use);
-          l_run[r] += (p[0] + p[1]) + (p[2] + p[3]);
-          pb[r][0] = pack_f16x2(p[0], p[1]);
-          pb[r][1] = pack_f16x2(p[2], p[3]);
+        for (int nb = 0; nb < kHeadBlocks; ++nb) {
+          float x[4];
+          x[0] = live0 ? s[nb][0] * crow[nb][0] : -INFINITY;
+          x[1] = live0 ? s[nb][1] * crow[nb][1] : -INFINITY;
+          x[2] = live1 ? s[nb][2] * crow[nb][0] : -INFINITY;
+          x[3] = live1 ? s[nb][3] * crow[nb][1] : -INFINITY;
+          // The running max moves only when the chunk exceeds it by more than
+          // 2^15, so P stays inside FP16.  A head's chunk max can pass that
+          // bound only if one of its lanes does, so the reduction over the
+          // eight lanes of a column group runs only then.
+          float cm0 = fmaxf(x[0], x[2]), cm1 = fmaxf(x[1], x[3]);
+          if (__any_sync(0xffffffffu, cm0 > m_run[nb][0] + kDecRescaleThreshold ||
+                                          cm1 > m_run[nb][1] + kDecRescaleThreshold)) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, o));
+              cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, o));
+            }
+            const bool need0 = cm0 > m_run[nb][0] + kDecRescaleThreshold;
+            const bool need1 = cm1 > m_run[nb][1] + kDecRescaleThreshold;
+            const float al0 = need0 ? fast_exp2(m_run[nb][0] - cm0) : 1.0f;  // 0 when m_run = -inf
+            const float al1 = need1 ? fast_exp2(m_run[nb][1] - cm1) : 1.0f;
+            if (need0) m_run[nb][0] = cm0;
+            if (need1) m_run[nb][1] = cm1;
+            l_run[nb][0] *= al0;
+            l_run[nb][1] *= al1;
+            // O^T columns 2t, 2t+1 are this lane's heads
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              acc[nb][mt][0] *= al0;
+              acc[nb][mt][1] *= al1;
+              acc[nb][mt][2] *= al0;
+              acc[nb][mt][3] *= al1;
+            }
+          }
+          const float mu0 = (m_run[nb][0] == -INFINITY) ? 0.0f : m_run[nb][0];
+          const float mu1 = (m_run[nb][1] == -INFINITY) ? 0.0f : m_run[nb][1];
+          const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
+          const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
+          l_run[nb][0] += p0 + p2;
+          l_run[nb][1] += p1 + p3;
+          // P^T as the B operand of PV: an 8x8 transpose of each token half
+          pb[nb][0] = movmatrix_trans(pack_f16x2(p0, p1));
+          pb[nb][1] = movmatrix_trans(pack_f16x2(p2, p3));
         }
         // ---- O^T += V^T P^T: A = V^T (rows: head dims, k: tokens), B = P^T
         // Lane (g, t) needs tokens 2t, 2t+1, 8+2t, 9+2t at code bytes 8g..8g+7
@@ -443,17 +485,21 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
       if (last) {
         // ---- merge the four warps through this stage's shared memory ---------
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-          l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-        }
+        for (int nb = 0; nb < kHeadBlocks; ++nb)
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            l_run[nb][0] += __shfl_xor_sync(0xffffffffu, l_run[nb][0], o);
+            l_run[nb][1] += __shfl_xor_sync(0xffffffffu, l_run[nb][1], o);
+          }
         __syncthreads();  // every warp is done reading the stage
         float* red_o = reinterpret_cast<float*>(sK);  // [warp][G][kRedRow]
 #pragma unroll
         for (int r = 0; r < kHeadBlocks; ++r) {
-          if (t == 0) {
-            red_m[warp][g + 8 * r] = m_run[r];
-            red_l[warp][g + 8 * r] = l_run[r];
+          if (g == 0) {
+            red_m[warp][8 * r + 2 * t] = m_run[r][0];
+            red_l[warp][8 * r + 2 * t] = l_run[r][0];
+            red_m[warp][8 * r + 2 * t + 1] = m_run[r][1];
+            red_l[warp][8 * r + 2 * t + 1] = l_run[r][1];
           }
           if (8 * r + 2 * t < G) {
 #pragma unroll
