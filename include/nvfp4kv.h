@@ -192,8 +192,13 @@ size_t nvfp4_paged_prefill_noalloc_max_bytes(void);
  * q, o:       bf16 [batch][num_q_heads][128].
  * lse:        optional fp32 [batch][num_q_heads].
  * workspace:  nvfp4_workspace_bytes(NVFP4KV_OP_DECODE, batch, num_q_heads,
- *             num_kv_heads, 0, max_pages_per_req*16) bytes (split-KV
- *             partials).  kv_lens[b] == 0 gives a zero output row. */
+ *             num_kv_heads, 0, max_pages_per_req*16) bytes: the split
+ *             schedule and the split-KV partials.  Rewritten by every call,
+ *             so calls that share a workspace must be ordered on one
+ *             stream.
+ * kv_lens[b] == 0 gives a zero output row (lse -inf); a kv_lens[b] above
+ * max_pages_per_req*16 does too and sets NVFP4KV_ERR_SHAPE in the device
+ * status. */
 int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t* cache, const int32_t* page_table,
                        int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o,
                        float* lse, void* workspace, size_t workspace_bytes, void* stream);

@@ -563,10 +563,10 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   }
 }
 
-// Block-wide exclusive prefix sums of two counts over the 1024 threads
-// (returns the exclusive values; *total receives the sums).
+// Block-wide exclusive prefix sums of two counts (returns the exclusive
+// values; *total receives the sums).  blockDim.x is a multiple of 32.
 __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2* warp_sums, int2* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int2 x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -579,7 +579,7 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2* warp_sums, i
   if (lane == 31) warp_sums[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    int2 w = warp_sums[lane];
+    int2 w = lane < nw ? warp_sums[lane] : make_int2(0, 0);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int nx = __shfl_up_sync(0xffffffffu, w.x, o), ny = __shfl_up_sync(0xffffffffu, w.y, o);
@@ -592,20 +592,22 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2* warp_sums, i
   }
   __syncthreads();
   const int2 before = wid > 0 ? warp_sums[wid - 1] : make_int2(0, 0);
-  *total = warp_sums[31];
+  *total = warp_sums[nw - 1];
   __syncthreads();
   return make_int2(x.x + before.x - v.x, x.y + before.y - v.y);
 }
 
 // Schedule: one record per (request, kv head, 1024-token split).  All full
 // splits come first; then each request's shorter last split, longest first,
-// so that the items claimed last are the shortest.  Requests are taken 1024 at
-// a time (one pass for the usual batch sizes); the longest-first order holds
-// within each such chunk.
-__global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
+// so that the items claimed last are the shortest.  Requests are taken
+// kPlanThreads at a time (one pass for the usual batch sizes); the
+// longest-first order holds within each such chunk.  Every CTA of the grid
+// computes the same prefix sums and writes its share of the records.
+constexpr int kPlanThreads = 256, kPlanCtas = 16;
+__global__ void __launch_bounds__(kPlanThreads) nvfp4_decode_plan_kernel(DecodeArgs a) {
   grid_dep_launch();  // the attention grid may start its prologue now
   __shared__ int2 warp_sums[32];
-  __shared__ int req_len[1024], req_first[1024], req_fpos[1024], req_ppos[1024];
+  __shared__ int req_len[kPlanThreads], req_first[kPlanThreads], req_fpos[kPlanThreads], req_ppos[kPlanThreads];
   int4* items = reinterpret_cast<int4*>(a.sched + 4);
   const int tid = threadIdx.x, H = a.num_kv_heads, cap = a.max_pages * kPageSize;
   // total of the full items of all requests (the partial ones follow them)
@@ -650,7 +652,7 @@ __global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
     req_first[tid] = (ex.x + ex.y) * H;
     __syncthreads();
     const int rtot = (tot.x + tot.y) * H;
-    for (int i = tid; i < rtot; i += blockDim.x) {
+    for (int i = tid + blockIdx.x * blockDim.x; i < rtot; i += blockDim.x * gridDim.x) {
       int lo = 0, hi = n_req - 1;  // last request of the chunk with req_first <= i
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -666,7 +668,7 @@ __global__ void __launch_bounds__(1024) nvfp4_decode_plan_kernel(DecodeArgs a) {
     full_carry += tot.x * H;
     part_carry += tot.y * H;
   }
-  if (tid == 0) {
+  if (tid == 0 && blockIdx.x == 0) {
     a.sched[0] = full_carry + part_carry;
     a.sched[1] = 0;  // claim counter of the attention kernel
   }
@@ -753,7 +755,7 @@ cudaError_t launch_dependent(void (*kernel)(DecodeArgs), dim3 grid, dim3 block, 
 
 template <int G>
 cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s) {
-  nvfp4_decode_plan_kernel<<<1, 1024, 0, s>>>(a);
+  nvfp4_decode_plan_kernel<<<kPlanCtas, kPlanThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(nvfp4_paged_decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
