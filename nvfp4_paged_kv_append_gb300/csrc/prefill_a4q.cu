@@ -11,10 +11,14 @@
 //   Q block scales (112-119), K block scales (120-127), O (128-255, fp32)
 //
 // which is why a KV tile is 112 keys (7 pages).  Inside a CTA the work of one
-// tile is a strict chain -- QK, softmax, PV, then the next QK may overwrite
-// S -- but the other CTA's chain runs in the gaps: while one softmax works,
-// the tensor core serves the other CTA.  A softmax thread owns one whole row
-// (112 keys), so no row statistics are exchanged between warps.
+// tile is a chain -- QK, softmax, PV, then the next QK may overwrite S -- but
+// the other CTA's chain runs in the gaps: while one softmax works, the tensor
+// core serves the other CTA.  The chain is shortened twice: PV starts on the
+// first 64 keys while the softmax still works on the rest, and the next QK is
+// issued right behind the PV (the tensor operations of one thread run in issue
+// order, so it overwrites S only after the PV has read its P).  A softmax
+// thread owns one whole row (112 keys), so no row statistics are exchanged
+// between warps.
 //
 //   warp 0 lane 0   TMEM allocation; every MMA: tcgen05.cp of the tile's K
 //                   scale atoms, QK (kind::mxf4nvf4, N = 112), PV (kind::f16,
@@ -31,6 +35,11 @@ namespace {
 using namespace prefill_detail;
 
 constexpr int kBN2 = 112;
+// PV of a tile runs in two parts: steps 0-3 (keys 0-63) as soon as the
+// softmax has written their P, steps 4-6 (keys 64-111) after the rest.  Part
+// i covers PV steps [kPvBound(i), kPvBound(i + 1)), 16 keys per step.
+constexpr int kPvParts = 2;
+__host__ __device__ constexpr int kPvBound(int i) { return i == 0 ? 0 : i == 1 ? 4 : kBN2 / 16; }
 constexpr int kThreads2 = 256;
 constexpr int kStages2 = 2;
 constexpr uint32_t kCols2 = 256;
@@ -66,6 +75,7 @@ struct Bars2 {
   uint64_t* o_empty;   // the epilogue has read O (4 softmax warps)
   uint64_t* sfa_ready; // the item's Q scale words are staged (4 softmax warps)
   uint64_t* drain;
+  uint64_t* p_part;    // P of keys 0-63 written (4 softmax warps)
 };
 
 __device__ __forceinline__ Bars2 make_bars2(uint64_t* base) {
@@ -80,12 +90,13 @@ __device__ __forceinline__ Bars2 make_bars2(uint64_t* base) {
   b.o_empty = base + 9;
   b.sfa_ready = base + 10;
   b.drain = base + 11;
+  b.p_part = base + 12;
   return b;
 }
 
 // ---------------------------------------------------------------------------
-// MMA thread.  Per tile: QK (after the previous PV released S), then PV once
-// the softmax has written P.
+// MMA thread.  Per tile: QK (queued behind the previous PV, which releases
+// S), then PV in two parts as the softmax writes P.
 __device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, const Bars2& bars, uint32_t tbase) {
   const uint32_t q_s = smem_u32(smem + kOffQ2);
   const uint32_t idesc_qk = idesc_mxf4nvf4(128, kBN2);
@@ -98,7 +109,6 @@ __device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, 
       const uint32_t st = it % kStages2;
       const uint32_t stage_s = smem_u32(smem + kOffStage2 + st * kRecord2);
       if (!mbar_wait(&bars.kv_full[st], (it / kStages2) & 1u, a.status)) return;
-      if (it > 0 && !mbar_wait(bars.pv_done, (it - 1) & 1u, a.status)) return;
       tc_fence_after();
       const uint32_t at_s = stage_s + kKCodes2;
       tc_cp_32x128b_warpx4(tbase + kColSFB2, smem_desc(at_s, 0, 128, kSwzNone));
@@ -111,15 +121,19 @@ __device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, 
       }
       tc_commit(bars.s_full);
       if (j == item.n_tiles - 1) tc_commit(bars.q_empty);
-      if (!mbar_wait(bars.p_full, it & 1u, a.status)) return;
       // the item's first PV overwrites O: the previous epilogue must have read it
       if (j == 0 && !mbar_wait(bars.o_empty, (item_ctr & 1u) ^ 1u, a.status)) return;
-      tc_fence_after();
       const uint32_t v_s = stage_s + kKCodes2 + kKAtoms2;
 #pragma unroll
-      for (uint32_t k = 0; k < kBN2 / 16; ++k) {
-        mma_f16_ts(tbase + kColO2, tbase + kColS2 + 8 * k, smem_desc(v_s + k * 2048, kVChunk2, 1024, kSwz128),
-                   idesc_pv, (j == 0 && k == 0) ? 0u : 1u);
+      for (int part = 0; part < kPvParts; ++part) {
+        uint64_t* ready = part + 1 < kPvParts ? &bars.p_part[part] : bars.p_full;
+        if (!mbar_wait(ready, it & 1u, a.status)) return;
+        tc_fence_after();
+#pragma unroll
+        for (int k = kPvBound(part); k < kPvBound(part + 1); ++k) {
+          mma_f16_ts(tbase + kColO2, tbase + kColS2 + 8 * k, smem_desc(v_s + k * 2048, kVChunk2, 1024, kSwz128),
+                     idesc_pv, (j == 0 && k == 0) ? 0u : 1u);
+        }
       }
       tc_commit(bars.pv_done);
       tc_commit(&bars.kv_empty[st]);
@@ -217,8 +231,9 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
       }
       const float m_tile = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]) * c_r;
       // Lazy rescale: the running max moves only when the tile exceeds it by
-      // more than 2^15 (P stays inside FP16).  O is stable here: this QK was
-      // issued after the previous PV finished.
+      // more than 2^15 (P stays inside FP16).  O is stable here: s_full
+      // completes only after every earlier tensor operation of the MMA
+      // thread, the previous PV included.
       const bool need = m_tile > m_run + kRescaleThreshold;
       float alpha = 1.0f;
       if (need) {
@@ -242,23 +257,28 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
       }
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
       const float2 cs2 = make_float2(c_r, c_r), nm2 = make_float2(-m_use, -m_use);
+      // P over the first 56 columns of S (already read into registers), one
+      // PV part at a time: part i is columns 8 kPvBound(i) .. 8 kPvBound(i+1) - 1
       uint32_t pk[kBN2 / 2];
 #pragma unroll
-      for (int c = 0; c < kBN2 / 2; ++c) {
-        const float2 t = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), cs2, nm2);
-        const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-        lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
-        pk[c] = pack_f16x2(p.x, p.y);
+      for (int part = 0; part < kPvParts; ++part) {
+#pragma unroll
+        for (int c = 8 * kPvBound(part); c < 8 * kPvBound(part + 1); ++c) {
+          const float2 t = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), cs2, nm2);
+          const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+          lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
+          pk[c] = pack_f16x2(p.x, p.y);
+        }
+        const int c0 = 8 * kPvBound(part), c1 = 8 * kPvBound(part + 1);
+#pragma unroll
+        for (int g16 = 0; g16 < (c1 - c0) / 16; ++g16)
+          tmem_st16(lane_base + kColS2 + c0 + 16 * g16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c0 + 16 * g16]));
+        if ((c1 - c0) % 16) tmem_st8(lane_base + kColS2 + c1 - 8, *reinterpret_cast<uint32_t(*)[8]>(&pk[c1 - 8]));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(part + 1 < kPvParts ? &bars.p_part[part] : bars.p_full);
       }
-      // P over the first 56 columns of S (already read into registers)
-      tmem_st16(lane_base + kColS2, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-      tmem_st16(lane_base + kColS2 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-      tmem_st16(lane_base + kColS2 + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
-      tmem_st8(lane_base + kColS2 + 48, *reinterpret_cast<uint32_t(*)[8]>(&pk[48]));
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.p_full);
     }
     // ---- epilogue: O * v_scale / l -------------------------------------------
     const float l_run = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y) + (lacc[2].x + lacc[2].y) +
@@ -315,6 +335,7 @@ __global__ void __launch_bounds__(kThreads2, 2) nvfp4_prefill_a4q_2cta_sm103_ker
     mbar_init(bars.o_empty, 4);
     mbar_init(bars.sfa_ready, 4);
     mbar_init(bars.drain, 1);
+    mbar_init(bars.p_part, 4);
     fence_barrier_init();
   }
   if (warp == 0) {
