@@ -484,7 +484,7 @@ def run_reference(args, rank, world):
 # profiles/prefill_a4q_16k_ncu.md, keyed by the digest of the kernel source it
 # was taken on: once that source changes the figure no longer describes the
 # kernel and is reported as null.
-PREFILL_TRAFFIC = {"source": "prefill_a4q.cu", "sha256_16": "a33ca9d7c5eb14e4", "bytes": 182485760 + 95159552}
+PREFILL_TRAFFIC = {"source": "prefill_a4q.cu", "sha256_16": "1e9eb777704b4aa0", "bytes": 182606848 + 93962752}
 
 
 def prefill_traffic_bytes():
