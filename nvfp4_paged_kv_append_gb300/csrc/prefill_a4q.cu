@@ -7,25 +7,25 @@
 // per tile), arranged so that two independent CTAs share each SM.  Each CTA
 // owns one 128-row q tile at a time and 256 TMEM columns:
 //
-//   S (columns 0-111, fp32; P as FP16 pairs written back over 0-55),
-//   Q block scales (112-119), K block scales (120-127), O (128-255, fp32)
+//   S half 0 (columns 0-63, keys 0-63 of the KV tile; its P as FP16 pairs
+//   over 0-31), S half 1 (64-111, keys 64-111; P over 64-87), Q block scales
+//   (112-119), K block scales (120-127), O (128-255, fp32)
 //
-// which is why a KV tile is 112 keys (7 pages).  Inside a CTA the work of one
-// tile is a chain -- QK, softmax, PV, then the next QK may overwrite S -- but
-// the other CTA's chain runs in the gaps: while one softmax works, the tensor
-// core serves the other CTA.  The chain is shortened twice: PV starts on the
-// first 64 keys while the softmax still works on the rest, and the next QK is
-// issued right behind the PV (the tensor operations of one thread run in issue
-// order, so it overwrites S only after the PV has read its P).  A softmax
-// thread owns one whole row (112 keys), so no row statistics are exchanged
-// between warps.
+// which is why a KV tile is 112 keys (7 pages).  The two halves of S work as
+// a double buffer: the QK of one half runs while the softmax works on the
+// other, and each half's PV starts as soon as its P is written.  The tensor
+// operations of one thread run in issue order, so a QK queued right behind
+// the PV of the same half overwrites S only after the PV has read P from it.
+// The other CTA on the SM fills the tensor core's remaining gaps.  A softmax
+// thread owns one whole row, so no row statistics are exchanged between
+// warps.
 //
-//   warp 0 lane 0   TMEM allocation; every MMA: tcgen05.cp of the tile's K
-//                   scale atoms, QK (kind::mxf4nvf4, N = 112), PV (kind::f16,
-//                   P from TMEM, K = 112)
+//   warp 0 lane 0   TMEM allocation; every tensor operation: per half, the
+//                   tcgen05.cp of its K scale atoms, QK (kind::mxf4nvf4,
+//                   N = 64 or 48), PV (kind::f16, P from TMEM)
 //   warp 1 lane 0   one bulk copy per tile of the repacked record
 //   warps 4-7       thread = row: Q quantization at each item start, the
-//                   softmax of every tile, the epilogue
+//                   softmax of every half tile, the epilogue
 #include "prefill_common.cuh"
 
 namespace nvfp4kv {
@@ -35,17 +35,17 @@ namespace {
 using namespace prefill_detail;
 
 constexpr int kBN2 = 112;
-// PV of a tile runs in two parts: steps 0-3 (keys 0-63) as soon as the
-// softmax has written their P, steps 4-6 (keys 64-111) after the rest.  Part
-// i covers PV steps [kPvBound(i), kPvBound(i + 1)), 16 keys per step.
-constexpr int kPvParts = 2;
-__host__ __device__ constexpr int kPvBound(int i) { return i == 0 ? 0 : i == 1 ? 4 : kBN2 / 16; }
+// A tile is two halves, keys 0-63 (h = 0) and 64-111 (h = 1), each with its
+// own S columns, QK and PV, so that the QK of one half runs while the softmax
+// works on the other.
+__host__ __device__ constexpr int half_keys(int h) { return h == 0 ? 64 : kBN2 - 64; }
+__host__ __device__ constexpr uint32_t half_col(int h) { return h == 0 ? 0u : 64u; }
 constexpr int kThreads2 = 256;
 constexpr int kStages2 = 2;
 constexpr uint32_t kCols2 = 256;
 constexpr uint32_t kColS2 = 0, kColSFA2 = 112, kColSFB2 = 120, kColO2 = 128;
 constexpr uint32_t kKCodes2 = kBN2 * 64;                         // 7 KB, 64B-swizzled rows
-constexpr uint32_t kKAtoms2 = 1024;                              // two 512-byte scale atoms
+constexpr uint32_t kKAtoms2 = 2048;  // per half: two k-steps x 512 B, the half's keys from row 0
 constexpr uint32_t kVChunk2 = kBN2 * 128;                        // 64 head dims x 112 keys, FP16
 constexpr uint32_t kRecord2 = kKCodes2 + kKAtoms2 + 2 * kVChunk2;  // 36 KB
 static_assert(kRecord2 % 1024 == 0 && (kKCodes2 + kKAtoms2) % 1024 == 0, "1 KB aligned operands");
@@ -67,15 +67,14 @@ static_assert(2 * kAlloc2 <= 228 * 1024, "two CTAs per SM");
 struct Bars2 {
   uint64_t* kv_full;   // [2]
   uint64_t* kv_empty;  // [2]
-  uint64_t* s_full;    // S of the current tile is in TMEM
-  uint64_t* p_full;    // P written over S (4 softmax warps)
-  uint64_t* pv_done;   // PV of the current tile finished: S/P, O and the stage are free
+  uint64_t* s_full;    // [half] S of the half is in TMEM
+  uint64_t* p_full;    // [half] P of the half written over its S (4 softmax warps)
+  uint64_t* pv_done;   // [half] PV of the half finished
   uint64_t* q_full;    // Q tile and its scales ready (4 softmax warps)
   uint64_t* q_empty;   // last QK of the item finished
   uint64_t* o_empty;   // the epilogue has read O (4 softmax warps)
   uint64_t* sfa_ready; // the item's Q scale words are staged (4 softmax warps)
   uint64_t* drain;
-  uint64_t* p_part;    // P of keys 0-63 written (4 softmax warps)
 };
 
 __device__ __forceinline__ Bars2 make_bars2(uint64_t* base) {
@@ -83,60 +82,94 @@ __device__ __forceinline__ Bars2 make_bars2(uint64_t* base) {
   b.kv_full = base + 0;
   b.kv_empty = base + 2;
   b.s_full = base + 4;
-  b.p_full = base + 5;
-  b.pv_done = base + 6;
-  b.q_full = base + 7;
-  b.q_empty = base + 8;
-  b.o_empty = base + 9;
-  b.sfa_ready = base + 10;
-  b.drain = base + 11;
-  b.p_part = base + 12;
+  b.p_full = base + 6;
+  b.pv_done = base + 8;
+  b.q_full = base + 10;
+  b.q_empty = base + 11;
+  b.o_empty = base + 12;
+  b.sfa_ready = base + 13;
+  b.drain = base + 14;
   return b;
 }
 
 // ---------------------------------------------------------------------------
-// MMA thread.  Per tile: QK (queued behind the previous PV, which releases
-// S), then PV in two parts as the softmax writes P.
+// MMA thread.  Issue order, one 112-key tile j at a time:
+//     PV_0(j)  QK_0(j+1)  PV_1(j)  QK_1(j+1)
+// (half h: scale copy, then QK into the half's S; PV once the softmax has
+// written the half's P).  The tensor operations of one thread run in issue
+// order, so QK_h(j+1) overwrites S only after PV_h(j) has read P from it, and
+// the scale copy for one half only after the other half's QK has read the
+// previous scales.
+template <int h>
+__device__ __forceinline__ void qk_half(uint32_t q_s, uint32_t stage_s, uint32_t tbase) {
+  const uint32_t at_s = stage_s + kKCodes2 + 1024u * h;
+  tc_cp_32x128b_warpx4(tbase + kColSFB2, smem_desc(at_s, 0, 128, kSwzNone));
+  tc_cp_32x128b_warpx4(tbase + kColSFB2 + 4, smem_desc(at_s + 512, 0, 128, kSwzNone));
+  const uint32_t idesc = idesc_mxf4nvf4(128, half_keys(h));
+  const uint32_t k_s = stage_s + 64u * 64u * h;  // K code rows of the half (64 B each)
+#pragma unroll
+  for (uint32_t s = 0; s < 2; ++s)
+    mma_nvf4_ss(tbase + kColS2 + half_col(h), smem_desc(q_s + 32 * s, 16, 512, kSwz64),
+                smem_desc(k_s + 32 * s, 16, 512, kSwz64), idesc, tbase + kColSFA2 + 4 * s, tbase + kColSFB2 + 4 * s,
+                s > 0 ? 1u : 0u);
+}
+
+template <int h>
+__device__ __forceinline__ void pv_half(uint32_t stage_s, uint32_t tbase, bool first, uint32_t idesc_pv) {
+  const uint32_t v_s = stage_s + kKCodes2 + kKAtoms2;
+#pragma unroll
+  for (int k = 0; k < half_keys(h) / 16; ++k) {
+    const int kk = (h == 0 ? 0 : 4) + k;  // 16-key step within the tile
+    mma_f16_ts(tbase + kColO2, tbase + kColS2 + half_col(h) + 8 * k,
+               smem_desc(v_s + kk * 2048, kVChunk2, 1024, kSwz128), idesc_pv, (first && kk == 0) ? 0u : 1u);
+  }
+}
+
 __device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, const Bars2& bars, uint32_t tbase) {
   const uint32_t q_s = smem_u32(smem + kOffQ2);
-  const uint32_t idesc_qk = idesc_mxf4nvf4(128, kBN2);
   const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   uint32_t it = 0, item_ctr = 0;
   Item item;
   for (int round = 0; get_item<kBN2>(a, round, item); ++round, ++item_ctr) {
     if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
+    // prologue: both halves of tile 0
+    uint32_t stage_s = smem_u32(smem + kOffStage2 + (it % kStages2) * kRecord2);
+    if (!mbar_wait(&bars.kv_full[it % kStages2], (it / kStages2) & 1u, a.status)) return;
+    tc_fence_after();
+    qk_half<0>(q_s, stage_s, tbase);
+    tc_commit(&bars.s_full[0]);
+    qk_half<1>(q_s, stage_s, tbase);
+    tc_commit(&bars.s_full[1]);
+    if (item.n_tiles == 1) tc_commit(bars.q_empty);
     for (int j = 0; j < item.n_tiles; ++j, ++it) {
       const uint32_t st = it % kStages2;
-      const uint32_t stage_s = smem_u32(smem + kOffStage2 + st * kRecord2);
-      if (!mbar_wait(&bars.kv_full[st], (it / kStages2) & 1u, a.status)) return;
-      tc_fence_after();
-      const uint32_t at_s = stage_s + kKCodes2;
-      tc_cp_32x128b_warpx4(tbase + kColSFB2, smem_desc(at_s, 0, 128, kSwzNone));
-      tc_cp_32x128b_warpx4(tbase + kColSFB2 + 4, smem_desc(at_s + 512, 0, 128, kSwzNone));
-#pragma unroll
-      for (uint32_t s = 0; s < 2; ++s) {
-        mma_nvf4_ss(tbase + kColS2, smem_desc(q_s + 32 * s, 16, 512, kSwz64),
-                    smem_desc(stage_s + 32 * s, 16, 512, kSwz64), idesc_qk, tbase + kColSFA2 + 4 * s,
-                    tbase + kColSFB2 + 4 * s, s > 0 ? 1u : 0u);
-      }
-      tc_commit(bars.s_full);
-      if (j == item.n_tiles - 1) tc_commit(bars.q_empty);
+      const bool more = j + 1 < item.n_tiles;
+      const uint32_t next_s = smem_u32(smem + kOffStage2 + ((it + 1) % kStages2) * kRecord2);
       // the item's first PV overwrites O: the previous epilogue must have read it
       if (j == 0 && !mbar_wait(bars.o_empty, (item_ctr & 1u) ^ 1u, a.status)) return;
-      const uint32_t v_s = stage_s + kKCodes2 + kKAtoms2;
-#pragma unroll
-      for (int part = 0; part < kPvParts; ++part) {
-        uint64_t* ready = part + 1 < kPvParts ? &bars.p_part[part] : bars.p_full;
-        if (!mbar_wait(ready, it & 1u, a.status)) return;
+      // half 0: PV of tile j, then QK of tile j + 1
+      if (!mbar_wait(&bars.p_full[0], it & 1u, a.status)) return;
+      tc_fence_after();
+      pv_half<0>(stage_s, tbase, j == 0, idesc_pv);
+      tc_commit(&bars.pv_done[0]);
+      if (more) {
+        if (!mbar_wait(&bars.kv_full[(it + 1) % kStages2], ((it + 1) / kStages2) & 1u, a.status)) return;
         tc_fence_after();
-#pragma unroll
-        for (int k = kPvBound(part); k < kPvBound(part + 1); ++k) {
-          mma_f16_ts(tbase + kColO2, tbase + kColS2 + 8 * k, smem_desc(v_s + k * 2048, kVChunk2, 1024, kSwz128),
-                     idesc_pv, (j == 0 && k == 0) ? 0u : 1u);
-        }
+        qk_half<0>(q_s, next_s, tbase);
+        tc_commit(&bars.s_full[0]);
       }
-      tc_commit(bars.pv_done);
+      // half 1
+      if (!mbar_wait(&bars.p_full[1], it & 1u, a.status)) return;
+      tc_fence_after();
+      pv_half<1>(stage_s, tbase, j == 0, idesc_pv);
+      tc_commit(&bars.pv_done[1]);
       tc_commit(&bars.kv_empty[st]);
+      if (more) {
+        qk_half<1>(q_s, next_s, tbase);
+        tc_commit(&bars.s_full[1]);
+        if (j + 2 == item.n_tiles) tc_commit(bars.q_empty);
+      }
+      stage_s = next_s;
     }
   }
 }
@@ -155,6 +188,87 @@ __device__ __forceinline__ void load_thread(const PrefillArgs& a, uint8_t* smem,
                 kRecord2, &bars.kv_full[st]);
     }
   }
+}
+
+// Softmax of half h of tile j for row lane_base's thread: S -> P (over S),
+// running max and sum.  Returns false when a wait timed out.
+template <int h>
+__device__ __forceinline__ bool softmax_half(const PrefillArgs& a, const Bars2& bars, uint32_t lane_base, int lane,
+                                             int j, uint32_t it, int limit, float c_r, float& m_run,
+                                             float2 (&lacc)[4]) {
+  constexpr int kMaxKeys = 64;
+  constexpr int nk = half_keys(h);
+  if (!mbar_wait_warp(&bars.s_full[h], it & 1u, a.status)) return false;
+  tc_fence_after();
+  uint32_t sr[kMaxKeys];
+  const uint32_t s_addr = lane_base + kColS2 + half_col(h);
+  tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+  if (h == 0) tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+  else tmem_ld16(s_addr + 32, *reinterpret_cast<uint32_t(*)[16]>(&sr[32]));
+  tmem_wait_ld();
+  float* s = reinterpret_cast<float*>(sr);
+  const int key0 = j * kBN2 + 64 * h;
+  if (key0 + nk - 1 > limit) {
+#pragma unroll
+    for (int c = 0; c < nk; ++c) s[c] = (key0 + c > limit) ? -INFINITY : s[c];
+  }
+  // half maximum over the raw scores (c_r > 0 commutes with the maximum)
+  float mxq[4];
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const float* sq = s + (nk / 4) * q4;
+    float m = fmax3(sq[0], sq[1], sq[2]);
+#pragma unroll
+    for (int c = 3; c + 1 < nk / 4; c += 2) m = fmax3(m, sq[c], sq[c + 1]);
+    if ((nk / 4) % 2 == 0) m = fmaxf(m, sq[nk / 4 - 1]);
+    mxq[q4] = m;
+  }
+  const float m_tile = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]) * c_r;
+  // Lazy rescale: the running max moves only when the half exceeds it by
+  // more than 2^15 (P stays inside FP16).  O then holds the other
+  // half's latest PV, which may still be running: wait for it first.
+  const bool need = m_tile > m_run + kRescaleThreshold;
+  float alpha = 1.0f;
+  if (need) {
+    alpha = fast_exp2(m_run - m_tile);  // 0 when m_run = -inf
+    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) lacc[i] = __fmul2_rn(lacc[i], a2);
+    m_run = m_tile;
+  }
+  if ((h == 1 || j > 0) && __any_sync(0xffffffffu, need)) {
+    if (!mbar_wait_warp(&bars.pv_done[1 - h], (h == 0 ? it - 1 : it) & 1u, a.status)) return false;
+    tc_fence_after();
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ov[32];
+      tmem_ld32(lane_base + kColO2 + 32 * c, ov);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+      tmem_st16(lane_base + kColO2 + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+      tmem_st16(lane_base + kColO2 + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+    }
+  }
+  const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+  const float2 cs2 = make_float2(c_r, c_r), nm2 = make_float2(-m_use, -m_use);
+  uint32_t pk[kMaxKeys / 2];
+#pragma unroll
+  for (int c = 0; c < nk / 2; ++c) {
+    const float2 t = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), cs2, nm2);
+    const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+    lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
+    pk[c] = pack_f16x2(p.x, p.y);
+  }
+  // P over the half's first nk/2 S columns (already read into registers)
+  tmem_st16(s_addr, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+  if (h == 0) tmem_st16(s_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+  else tmem_st8(s_addr + 16, *reinterpret_cast<uint32_t(*)[8]>(&pk[16]));
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars.p_full[h]);
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -205,89 +319,17 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
     float m_run = -INFINITY;
     float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
     for (int j = 0; j < item.n_tiles; ++j, ++it) {
-      if (!mbar_wait_warp(bars.s_full, it & 1u, a.status)) return;
-      tc_fence_after();
-      uint32_t sr[kBN2];
-      tmem_ld32(lane_base + kColS2, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(lane_base + kColS2 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(lane_base + kColS2 + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      tmem_ld16(lane_base + kColS2 + 96, *reinterpret_cast<uint32_t(*)[16]>(&sr[96]));
-      tmem_wait_ld();
-      float* s = reinterpret_cast<float*>(sr);
-      const int key0 = j * kBN2;
-      if (key0 + kBN2 - 1 > limit) {
-#pragma unroll
-        for (int c = 0; c < kBN2; ++c) s[c] = (key0 + c > limit) ? -INFINITY : s[c];
-      }
-      // row maximum over the raw scores (c_r > 0 commutes with the maximum)
-      float mxq[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const float* sq = s + 28 * q4;
-        float m = fmax3(sq[0], sq[1], sq[2]);
-#pragma unroll
-        for (int c = 3; c < 27; c += 2) m = fmax3(m, sq[c], sq[c + 1]);
-        mxq[q4] = fmaxf(m, sq[27]);
-      }
-      const float m_tile = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]) * c_r;
-      // Lazy rescale: the running max moves only when the tile exceeds it by
-      // more than 2^15 (P stays inside FP16).  O is stable here: s_full
-      // completes only after every earlier tensor operation of the MMA
-      // thread, the previous PV included.
-      const bool need = m_tile > m_run + kRescaleThreshold;
-      float alpha = 1.0f;
-      if (need) {
-        alpha = fast_exp2(m_run - m_tile);  // 0 when m_run = -inf
-        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) lacc[i] = __fmul2_rn(lacc[i], a2);
-        m_run = m_tile;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(lane_base + kColO2 + 32 * c, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st16(lane_base + kColO2 + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
-          tmem_st16(lane_base + kColO2 + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
-        }
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-      const float2 cs2 = make_float2(c_r, c_r), nm2 = make_float2(-m_use, -m_use);
-      // P over the first 56 columns of S (already read into registers), one
-      // PV part at a time: part i is columns 8 kPvBound(i) .. 8 kPvBound(i+1) - 1
-      uint32_t pk[kBN2 / 2];
-#pragma unroll
-      for (int part = 0; part < kPvParts; ++part) {
-#pragma unroll
-        for (int c = 8 * kPvBound(part); c < 8 * kPvBound(part + 1); ++c) {
-          const float2 t = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), cs2, nm2);
-          const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-          lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
-          pk[c] = pack_f16x2(p.x, p.y);
-        }
-        const int c0 = 8 * kPvBound(part), c1 = 8 * kPvBound(part + 1);
-#pragma unroll
-        for (int g16 = 0; g16 < (c1 - c0) / 16; ++g16)
-          tmem_st16(lane_base + kColS2 + c0 + 16 * g16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c0 + 16 * g16]));
-        if ((c1 - c0) % 16) tmem_st8(lane_base + kColS2 + c1 - 8, *reinterpret_cast<uint32_t(*)[8]>(&pk[c1 - 8]));
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(part + 1 < kPvParts ? &bars.p_part[part] : bars.p_full);
-      }
+      if (!softmax_half<0>(a, bars, lane_base, lane, j, it, limit, c_r, m_run, lacc)) return;
+      if (!softmax_half<1>(a, bars, lane_base, lane, j, it, limit, c_r, m_run, lacc)) return;
     }
     // ---- epilogue: O * v_scale / l -------------------------------------------
     const float l_run = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y) + (lacc[2].x + lacc[2].y) +
                         (lacc[3].x + lacc[3].y);
-    if (!mbar_wait_warp(bars.pv_done, (it - 1) & 1u, a.status)) return;
+    if (!mbar_wait_warp(&bars.pv_done[1], (it - 1) & 1u, a.status)) return;
     tc_fence_after();
     const float inv_l = (l_run > 0.0f) ? a.v_g / l_run : 0.0f;
-    __nv_bfloat16* orow =
-        reinterpret_cast<__nv_bfloat16*>(a.o) + (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) +
+                          (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t ov[32];
@@ -297,7 +339,8 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
         uint32_t pb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+          __nv_bfloat162 v =
+              __floats2bfloat162_rn(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
           pb[i] = *reinterpret_cast<uint32_t*>(&v);
         }
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
@@ -327,15 +370,16 @@ __global__ void __launch_bounds__(kThreads2, 2) nvfp4_prefill_a4q_2cta_sm103_ker
       mbar_init(&bars.kv_full[i], 1);
       mbar_init(&bars.kv_empty[i], 1);
     }
-    mbar_init(bars.s_full, 1);
-    mbar_init(bars.p_full, 4);
-    mbar_init(bars.pv_done, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&bars.s_full[h], 1);
+      mbar_init(&bars.p_full[h], 4);
+      mbar_init(&bars.pv_done[h], 1);
+    }
     mbar_init(bars.q_full, 4);
     mbar_init(bars.q_empty, 1);
     mbar_init(bars.o_empty, 4);
     mbar_init(bars.sfa_ready, 4);
     mbar_init(bars.drain, 1);
-    mbar_init(bars.p_part, 4);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -408,12 +452,14 @@ __global__ void __launch_bounds__(128) nvfp4_prefill_repack112_kernel(PrefillArg
       const uint4 v = row >= 0 ? *reinterpret_cast<const uint4*>(a.k_data + row * 64 + 16 * c) : make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(rec + sw64_off(key, c)) = v;
     }
-    // K scale atoms: 128 rows (rows past 112 zero) x 2 k-steps
-    for (int u = tid; u < 256; u += 128) {
-      const int key = u >> 1, ks = u & 1;
-      const int64_t row = row_of(key);
+    // K scale atoms of each half: 128 rows (the half's keys, then zeros) x 2
+    // k-steps; half h starts at key 64 h
+    for (int u = tid; u < 512; u += 128) {
+      const int h = u >> 8, r = (u >> 1) & 127, ks = u & 1;
+      const int key = 64 * h + r;
+      const int64_t row = (r < half_keys(h)) ? row_of(key) : -1;
       const uint32_t w = row >= 0 ? *reinterpret_cast<const uint32_t*>(a.k_scale + row * 8 + 4 * ks) : 0u;
-      *reinterpret_cast<uint32_t*>(rec + kKCodes2 + ks * 512 + (key & 31) * 16 + (key >> 5) * 4) = w;
+      *reinterpret_cast<uint32_t*>(rec + kKCodes2 + 1024 * h + ks * 512 + (r & 31) * 16 + (r >> 5) * 4) = w;
     }
     // V: 112 keys x 4 groups of 32 values -> FP16, MN-major 128B-swizzled
     uint8_t* vt = rec + kKCodes2 + kKAtoms2;
