@@ -131,10 +131,11 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  *             bytes, the call may also run in repack mode:
  *             when requests average two or more q tiles (128 rows of query
  *             tokens x grouped heads) per kv head, V (and K for the
- *             dequant-ahead variant) is first dequantized once per
- *             128-key tile into the workspace ("NVFP4 KV cache A4Q prefill
- *             explained", section "Compare A4Q with dequantize-ahead
- *             repacking"), instead of once per q tile inside the kernel.
+ *             dequant-ahead variant) is first dequantized once per KV
+ *             tile (112 keys for A4Q, 128 for dequant-ahead) into the
+ *             workspace ("NVFP4 KV cache A4Q prefill explained", section
+ *             "Compare A4Q with dequantize-ahead repacking"), instead of
+ *             once per q tile inside the kernel.
  *             Results are identical either way.
  * num_q_heads must be a multiple of num_kv_heads with a power-of-two ratio
  * of at most 128.  q_len == 0 requests produce nothing. */
@@ -204,8 +205,9 @@ int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t
                        float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes for op.  NVFP4KV_OP_PREFILL: the schedule for total_q
- * query tokens, plus, when max_kv_len > 0, the repack tiles (64 KB per
- * request, kv head and 128-key tile of max_kv_len).  NVFP4KV_OP_DECODE: the
+ * query tokens, plus, when max_kv_len > 0, room for the repack records of
+ * either variant (per request and kv head: 37 KB per 112-key A4Q tile or
+ * 64 KB per 128-key dequant-ahead tile of max_kv_len, the larger total).  NVFP4KV_OP_DECODE: the
  * split-KV partials for max_kv_len.  Host-only, no CUDA call.  Returns 0 for
  * bad arguments. */
 size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int64_t total_q,

@@ -92,7 +92,7 @@ int64_t prefill_max_items(int64_t total_q, int batch, int num_q_heads, int num_k
 // Prefill workspace: [16 B header][items: 8 B each][unit prefix][tile prefix]
 // padded to 1 KB, then (repack mode) one record for every (request, kv head,
 // KV tile) the batch can hold: 64 KB per 128-key tile for the dequant-ahead
-// kernel, 36 KB per 112-key tile for the A4Q kernel.
+// kernel, 37 KB per 112-key tile for the A4Q kernel.
 constexpr size_t kRepackRecordBytesDq = 65536;
 size_t prefill_repack_bytes(int variant, int batch, int num_kv_heads, int64_t max_kv_len);
 size_t prefill_sched_bytes(int64_t max_items, int batch) {

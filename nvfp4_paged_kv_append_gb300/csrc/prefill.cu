@@ -654,14 +654,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// repack pre-pass: each (request, kv head, KV tile) once -> one record laid
-// out exactly like a repack-mode stage, so the attention kernel moves it with
-// a single bulk copy.  A4Q: K codes (64B-swizzled) | K scale atoms | V (FP16,
-// MN-major 128B-swizzled); dequant-ahead: K (BF16, K-major 128B-swizzled) | V.
-// Keys past kv_len are zeros.
-template <int VARIANT>
+// Dequant-ahead repack pre-pass: each (request, kv head, KV tile) once -> one
+// record laid out exactly like a repack-mode stage, so the attention kernel
+// moves it with a single bulk copy: K (BF16, K-major 128B-swizzled) | V (FP16,
+// MN-major 128B-swizzled).  Keys past kv_len are zeros.  (A4Q records are
+// written by the repack kernel of prefill_a4q.cu.)
 __global__ void __launch_bounds__(128) nvfp4_prefill_repack_kernel(PrefillArgs a) {
-  using L = Layout<VARIANT, true>;
+  using L = Layout<1, true>;
   const int tid = threadIdx.x;
   const int total = a.work[1];
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -687,23 +686,7 @@ __global__ void __launch_bounds__(128) nvfp4_prefill_repack_kernel(PrefillArgs a
       }
       return (static_cast<int64_t>(pid) * a.num_kv_heads + h) * kPageSize + (abs_key & 15);
     };
-    if constexpr (VARIANT == 0) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int u = tid + 128 * i, key = u >> 2, c = u & 3;
-        const int64_t row = row_of(key);
-        const uint4 v = row >= 0 ? *reinterpret_cast<const uint4*>(a.k_data + row * 64 + 16 * c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(rec + sw64_off(key, c)) = v;
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int u = tid + 128 * i, key = u >> 1, ks = u & 1;
-        const int64_t row = row_of(key);
-        const uint32_t w = row >= 0 ? *reinterpret_cast<const uint32_t*>(a.k_scale + row * 8 + 4 * ks) : 0u;
-        *reinterpret_cast<uint32_t*>(rec + kKData + ks * 512 + (key & 31) * 16 + (key >> 5) * 4) = w;
-      }
-    }
-    for (int tensor = VARIANT == 0 ? 1 : 0; tensor < 2; ++tensor) {
+    for (int tensor = 0; tensor < 2; ++tensor) {
       const uint8_t* data = tensor ? a.v_data : a.k_data;
       const uint8_t* scl = tensor ? a.v_scale : a.k_scale;
       uint8_t* dst = rec + (tensor ? L::kStageV : 0u);
@@ -869,7 +852,7 @@ cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !repack) return e;
   if (variant == 0) return launch_prefill_a4q_2cta_repack(a, num_sms, s);
-  nvfp4_prefill_repack_kernel<1><<<num_sms * 8, 128, 0, s>>>(a);
+  nvfp4_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -47,7 +47,7 @@ constexpr uint32_t kColS2 = 0, kColSFA2 = 112, kColSFB2 = 120, kColO2 = 128;
 constexpr uint32_t kKCodes2 = kBN2 * 64;                         // 7 KB, 64B-swizzled rows
 constexpr uint32_t kKAtoms2 = 2048;  // per half: two k-steps x 512 B, the half's keys from row 0
 constexpr uint32_t kVChunk2 = kBN2 * 128;                        // 64 head dims x 112 keys, FP16
-constexpr uint32_t kRecord2 = kKCodes2 + kKAtoms2 + 2 * kVChunk2;  // 36 KB
+constexpr uint32_t kRecord2 = kKCodes2 + kKAtoms2 + 2 * kVChunk2;  // 37 KB
 static_assert(kRecord2 % 1024 == 0 && (kKCodes2 + kKAtoms2) % 1024 == 0, "1 KB aligned operands");
 
 // per-thread register budgets: issue/loader warpgroup and softmax warpgroup
@@ -416,10 +416,10 @@ __global__ void __launch_bounds__(kThreads2, 2) nvfp4_prefill_a4q_2cta_sm103_ker
 
 // ---------------------------------------------------------------------------
 // Repack pre-pass for this kernel: each (request, kv head, 112-key tile) once
-// -> one 36 KB record laid out exactly like a stage: K codes (64B-swizzled
-// rows), K scale atoms (rows past 112 zero), V as FP16 in the MN-major
-// 128B-swizzled operand layout (two chunks of 64 head dims x 112 keys).  Keys
-// past kv_len are zeros.
+// -> one 37 KB record laid out exactly like a stage: K codes (64B-swizzled
+// rows), the K scale atoms of each half (its keys from row 0, the remaining
+// rows zero), V as FP16 in the MN-major 128B-swizzled operand layout (two
+// chunks of 64 head dims x 112 keys).  Keys past kv_len are zeros.
 __global__ void __launch_bounds__(128) nvfp4_prefill_repack112_kernel(PrefillArgs a) {
   const int tid = threadIdx.x;
   const int total = a.work[1];
