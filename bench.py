@@ -371,7 +371,11 @@ def decode_component(nk, nk_bench, dev, K):
 
 def e2e_measure(nk, nk_bench, dev, P, wl, args):
     """Host (pinned) inputs copied in, append + prefill through the public
-    API, output copied back: all inside the timed region."""
+    API, output copied back: every step's copies are inside the timed
+    region.  Steps are pipelined the way a server runs them: the inputs of
+    step i+1 are copied in (one stream) while step i computes (another) and
+    the output of step i-1 is copied out (a third), with double-buffered
+    device inputs and outputs."""
     inp = P["inp"]
     order = W.shuffled_append_order(inp.wl.total_kv)
     hk = inp.k[order].contiguous().pin_memory()
@@ -380,23 +384,59 @@ def e2e_measure(nk, nk_bench, dev, P, wl, args):
     hq = inp.q.contiguous().pin_memory()
     hpt, hkv, hqo = inp.page_table.pin_memory(), inp.kv_lens.pin_memory(), inp.qo_indptr.pin_memory()
     ho = torch.empty(hq.shape, dtype=torch.bfloat16).pin_memory()
-    dk, dv, ds, dq = torch.empty_like(P["k"]), torch.empty_like(P["v"]), torch.empty_like(P["slots"]), torch.empty_like(P["q"])
-    dpt, dkv, dqo = torch.empty_like(P["pt"]), torch.empty_like(P["kvl"]), torch.empty_like(P["qo"])
-    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hs, hq, hpt, hkv, hqo))
+    host_in = (hk, hv, hs, hq, hpt, hkv, hqo)
+    dev_in = [tuple(torch.empty_like(t, device=dev) for t in host_in) for _ in range(2)]
+    dev_out = [torch.empty_like(P["out"]) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = ho.numel() * ho.element_size()
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
-        for d, h in ((dk, hk), (dv, hv), (ds, hs), (dq, hq), (dpt, hpt), (dkv, hkv), (dqo, hqo)):
-            d.copy_(h, non_blocking=True)
-        nk.nvfp4_kv_append(dk, dv, ds, P["cache"])
-        nk.nvfp4_paged_prefill(dq, P["cache"], dpt, dkv, dqo, causal=wl.causal, sm_scale=inp.sm_scale,
-                               out=P["out"], workspace=P["ws"])
-        ho.copy_(P["out"], non_blocking=True)
+    def step(i):
+        buf = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(comp_done[buf])  # step i-2 no longer reads these inputs
+            for d, h in zip(dev_in[buf], host_in):
+                d.copy_(h, non_blocking=True)
+            in_ready[buf].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(in_ready[buf])
+            if i >= 2:
+                s_comp.wait_event(out_done[buf])  # step i-2's output has been copied out
+            dk, dv, ds, dq, dpt, dkv, dqo = dev_in[buf]
+            nk.nvfp4_kv_append(dk, dv, ds, P["cache"])
+            nk.nvfp4_paged_prefill(dq, P["cache"], dpt, dkv, dqo, causal=wl.causal, sm_scale=inp.sm_scale,
+                                   out=dev_out[buf], workspace=P["ws"])
+            comp_done[buf].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[buf])
+            ho.copy_(dev_out[buf], non_blocking=True)
+            out_done[buf].record(s_out)
 
-    t = nk_bench.time_fn(one, max(args.steps, 3), 2)
-    ms = statistics.mean(t)
+    def run(n):
+        for i in range(n):
+            step(i)
+        for st in (s_in, s_comp, s_out):
+            torch.cuda.current_stream(dev).wait_stream(st)
+
+    run(3)  # warm-up
+    torch.cuda.synchronize(dev)
+    n = max(args.steps, 3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for st in (s_in, s_comp, s_out):
+        st.wait_stream(torch.cuda.current_stream(dev))
+    run(n)
+    t1.record()
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / n
     return {"value": round(wl.flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": "copy-in of step i+1, compute of step i and copy-out of step i-1 on three streams",
+            "l2": "not flushed: every step moves 201 MB in and 134 MB out, more than the 129 MB L2"}
 
 
 # ---------------------------------------------------------------------------- oracle arm
