@@ -1,0 +1,91 @@
+"""The pins catch plausible mistakes.  Each test plants one mistake in the
+oracle -- on the CPU, through a proxy that replaces a single oracle function
+with a wrong variant -- and checks that the pin written for that part of the
+oracle fails on it.  (The formats and rules are those of "NVFP4 KV cache vs
+NVFP4 weights", section "NVFP4 KV cache vs NVFP4 weights", and "NVFP4 KV
+cache A4Q prefill explained", section "Quantize Q instead of expanding K".)"""
+import math
+
+import numpy as np
+import pytest
+
+from . import test_oracle_attention as A
+from . import test_oracle_codec as C
+from . import test_oracle_formats as F
+
+E2M1_MAGS = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+class Mutant:
+    """The oracle with some functions replaced."""
+
+    def __init__(self, base, **replaced):
+        self._base = base
+        self.__dict__.update(replaced)
+
+    def __getattr__(self, name):
+        return getattr(self._base, name)
+
+
+def _fails(pin, *args):
+    with pytest.raises(AssertionError):
+        pin(*args)
+
+
+def test_e2m1_ties_away_from_zero_is_caught(orc):
+    def ties_away(x):
+        sign = 8 if math.copysign(1.0, x) < 0 else 0
+        a = min(abs(x), 6.0)
+        code = min(range(8), key=lambda c: (abs(E2M1_MAGS[c] - a), -E2M1_MAGS[c]))
+        return code | sign
+
+    _fails(F.test_e2m1_tie_rules, Mutant(orc, e2m1_encode=ties_away))
+
+
+def test_e4m3_truncation_is_caught(orc):
+    vals = np.array([orc.e4m3_value(b) for b in range(127)])
+
+    def truncate(x):
+        x = np.minimum(np.asarray(x, np.float64), 448.0)
+        return np.array([int(np.nonzero(vals <= xi)[0].max()) for xi in x], np.uint8)
+
+    _fails(F.test_e4m3_encode_rne_vs_torch_cast, Mutant(orc, e4m3_encode_array=truncate))
+
+
+def test_e2m1_exponent_bias_is_caught(orc):
+    def bias0(code):
+        s, e, m = (code >> 3) & 1, (code >> 1) & 3, code & 1
+        mag = float(m) if e == 0 else 2.0 ** e * (1 + 0.5 * m)
+        return -mag if s else mag
+
+    _fails(F.test_e2m1_decode_all_codes, Mutant(orc, e2m1_value=bias0))
+
+
+def test_swapped_nibble_order_is_caught(orc):
+    def swapped(x, g):
+        packed, scale = orc.quantize_block16(x, g)
+        packed = np.asarray(packed, np.uint8)
+        return ((packed >> 4) | (packed << 4)).astype(np.uint8), scale
+
+    _fails(C.test_hand_worked_blocks, Mutant(orc, quantize_block16=swapped))
+
+
+def test_dropped_factor_six_in_the_scale_is_caught(orc):
+    def no_six(x, g):
+        return orc.quantize_block16(x, g / 6.0)
+
+    _fails(C.test_round_trip_codes_and_scales, Mutant(orc, quantize_block16=no_six), 1.0)
+
+
+def test_top_left_causal_alignment_is_caught(orc):
+    def top_left(q, pos, q_len, k, v, causal, sm_scale):
+        return orc.attention_rows(q, pos, len(k), k, v, causal, sm_scale)
+
+    _fails(A.test_attention_vs_library, Mutant(orc, attention_rows=top_left), 5, 19, True)
+
+
+def test_dropped_softmax_scale_is_caught(orc):
+    def unscaled(q, pos, q_len, k, v, causal, sm_scale):
+        return orc.attention_rows(q, pos, q_len, k, v, causal, 1.0)
+
+    _fails(A.test_attention_vs_library, Mutant(orc, attention_rows=unscaled), 9, 33, False)
