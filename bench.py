@@ -297,11 +297,7 @@ def run_ours(args, rank, world, dev):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "nvfp4(e2m1+e4m3) QK, f16 PV, f32 accum", "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.batch, "seq_len": wl.q_lens[0], "q_heads": wl.num_q_heads,
-                   "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16, "causal": wl.causal,
-                   "step": "append(K,V 16384 tok, shuffled slots) + A4Q paged prefill (repack mode)",
-                   "flops_per_step": flops, "l2": "flushed (256 MB write) before every timed step, outside the events",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(wl, world),
         "step_breakdown_ms": {"append": round(statistics.mean(app_ms), 4), "prefill": round(statistics.mean(pre_ms), 4),
                               "prefill_plan_and_repack": round(statistics.mean(plan_ms), 4),
                               "prefill_attention": round(statistics.mean(attn_ms), 4)},
@@ -439,6 +435,15 @@ def e2e_measure(nk, nk_bench, dev, P, wl, args):
             "l2": "not flushed: every step moves 201 MB in and 134 MB out, more than the 129 MB L2"}
 
 
+def bench_config(wl, world):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": wl.name, "batch": wl.batch, "seq_len": wl.q_lens[0], "q_heads": wl.num_q_heads,
+            "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16, "causal": wl.causal,
+            "step": "append(K,V 16384 tok, shuffled slots) + A4Q paged prefill (repack mode)",
+            "flops_per_step": wl.flops(), "l2": "flushed (256 MB write) before every timed step, outside the events",
+            "parallelism": f"replicas x{world}"}
+
+
 # ---------------------------------------------------------------------------- oracle arm
 _ORACLE = {}
 
@@ -512,7 +517,7 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(times) * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": W.full_prefill_16k().name, "sample": "bounded CPU sample per step"},
+            "config": dict(bench_config(W.full_prefill_16k(), world), sample="bounded CPU sample per step"),
             "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
