@@ -208,11 +208,15 @@ __device__ __forceinline__ bool softmax_half(const PrefillArgs& a, const Bars2& 
   tmem_wait_ld();
   float* s = reinterpret_cast<float*>(sr);
   const int key0 = j * kBN2 + 64 * h;
-  if (key0 + nk - 1 > limit) {
+  // On a half with masked keys the kept scores are scaled here, so that a
+  // zero row scale (an all-zero query row, or a row past the request) never
+  // multiplies -inf
+  const bool masked = key0 + nk - 1 > limit;
+  if (masked) {
 #pragma unroll
-    for (int c = 0; c < nk; ++c) s[c] = (key0 + c > limit) ? -INFINITY : s[c];
+    for (int c = 0; c < nk; ++c) s[c] = (key0 + c > limit) ? -INFINITY : s[c] * c_r;
   }
-  // half maximum over the raw scores (c_r > 0 commutes with the maximum)
+  // half maximum (c_r >= 0 commutes with the maximum)
   float mxq[4];
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
@@ -223,7 +227,8 @@ __device__ __forceinline__ bool softmax_half(const PrefillArgs& a, const Bars2& 
     if ((nk / 4) % 2 == 0) m = fmaxf(m, sq[nk / 4 - 1]);
     mxq[q4] = m;
   }
-  const float m_tile = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]) * c_r;
+  const float mx = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]);
+  const float m_tile = masked ? mx : mx * c_r;
   // Lazy rescale: the running max moves only when the half exceeds it by
   // more than 2^15 (P stays inside FP16).  O then holds the other
   // half's latest PV, which may still be running: wait for it first.
@@ -251,7 +256,8 @@ __device__ __forceinline__ bool softmax_half(const PrefillArgs& a, const Bars2& 
     }
   }
   const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-  const float2 cs2 = make_float2(c_r, c_r), nm2 = make_float2(-m_use, -m_use);
+  const float cs = masked ? 1.0f : c_r;
+  const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-m_use, -m_use);
   uint32_t pk[kMaxKeys / 2];
 #pragma unroll
   for (int c = 0; c < nk / 2; ++c) {

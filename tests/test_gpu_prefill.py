@@ -156,3 +156,21 @@ def test_plan_then_run_equals_single_call(variant, mode):
         torch.cuda.synchronize()
         assert b.nvfp4kv_get_device_status() == 0
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_zero_query_rows_repack_mode(variant, q_mode):
+    """All-zero query rows (a per-row Q scale of 0) in repack mode, on the
+    causal diagonal tiles where keys are masked: the output is the mean of
+    the visible V rows, never NaN."""
+    import copy
+    base = G.inputs("shortq")  # averages four q tiles per kv head: repack mode
+    inp = copy.copy(base)
+    q = base.q.clone()
+    zero_tokens = [0, 5, 127, 128 + 64, 3 * 128 + 127]
+    q[zero_tokens] = 0
+    inp.q = q
+    cache = G.gpu_cache(inp)
+    rows = [(0, i) for i in range(128)] + [(1, 64), (3, 127), (2, 0), (2, 127)]
+    got, _ = _check(inp, cache, G.pools_for("shortq"), variant, q_mode, rows=rows, mode="auto")
+    assert np.isfinite(got).all()
