@@ -91,3 +91,26 @@ def test_invalid_arguments_rejected_on_host(nk):
     # quantize: bad mode / non-positive global scale
     assert lib.nvfp4_quantize_rows(16, 1, 5, 1.0, 16, 16, null, null) == -1
     assert lib.nvfp4_quantize_rows(16, 1, 0, -1.0, 16, 16, null, null) == -1
+
+
+def test_plan_run_and_noalloc_reject_bad_arguments_on_host(nk):
+    """The split prefill entry points and the allocation-free one validate
+    their arguments before touching the device, like nvfp4_paged_prefill."""
+    lib = nk.lib
+    null = None
+    d = nk.CacheDesc(16, 16, 32, 48, 4, 16, 2, 128, 1.0, 1.0)
+    plan = lambda hq, causal, variant, ws: lib.nvfp4_paged_prefill_plan(
+        16, hq, ctypes.byref(d), 16, 1, 16, 16, 1, causal, variant, ws, 4096, null)
+    assert plan(3, 1, 0, 16) == -1   # Hq not a multiple of Hkv
+    assert plan(4, 2, 0, 16) == -1   # causal must be 0 or 1
+    assert plan(4, 1, 7, 16) == -1   # unknown variant
+    assert plan(4, 1, 0, null) == -3  # no workspace
+    run = lambda q, scale: lib.nvfp4_paged_prefill_run(
+        q, 16, 4, ctypes.byref(d), 16, 1, 16, 16, 1, 1, scale, 0, 16, null, 16, 4096, null)
+    assert run(16, float("nan")) == -1  # sm_scale must be finite
+    assert run(8, 0.1) == -1            # q not 16-byte aligned
+    assert run(null, 0.1) == -1         # no q
+    noalloc = lambda hq: lib.nvfp4_paged_prefill_noalloc(
+        16, 16, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, 0, 16, null, null)
+    assert noalloc(0) == -1
+    assert noalloc(3) == -1
