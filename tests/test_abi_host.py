@@ -114,3 +114,30 @@ def test_plan_run_and_noalloc_reject_bad_arguments_on_host(nk):
         16, 16, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, 0, 16, null, null)
     assert noalloc(0) == -1
     assert noalloc(3) == -1
+
+
+def test_header_and_library_from_plain_c(nk, tmp_path):
+    """The boundary is a C ABI: a C99 program that includes the header and
+    links the library calls the host-only entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(nk.lib._name)
+    src = tmp_path / "use_abi.c"
+    src.write_text(
+        "#include <stdio.h>\n#include <string.h>\n#include \"nvfp4kv.h\"\n"
+        "int main(void) {\n"
+        "  /* 144 B per token and kv head (K and V): one 16-token page of 8 heads */\n"
+        "  if (nvfp4_cache_bytes(1, 16, 8, 128) != 16 * 8 * 144) return 1;\n"
+        "  if (nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, 2, 6, 4, 0, 100) != 0) return 2;\n"
+        "  if (strlen(nvfp4kv_version()) == 0) return 3;\n"
+        "  if (nvfp4kv_status_string(NVFP4KV_ERR_SHAPE) == NULL) return 4;\n"
+        "  printf(\"ok\\n\");\n  return 0;\n}\n")
+    exe = tmp_path / "use_abi"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", str(src), "-I", os.path.join(root, "include"), "-L", libdir,
+                    "-lnvfp4kv", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
