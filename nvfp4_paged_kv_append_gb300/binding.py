@@ -96,11 +96,53 @@ def _check(where: str, rc: int) -> None:
 
 
 def _ptr(t: Optional[torch.Tensor]):
+    """Device pointer of a contiguous CUDA tensor.  Every pointer of the ABI
+    except the cache descriptor is a device pointer, so a host tensor is
+    refused here rather than handed to a kernel."""
     if t is None:
         return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to nvfp4kv must live on a CUDA device")
     if not t.is_contiguous():
         raise ValueError("tensors passed to nvfp4kv must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_dtype(t: Optional[torch.Tensor], dtype, name: str) -> None:
+    if t is not None:
+        _require(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check_rows(q: torch.Tensor, name: str = "q") -> None:
+    _check_dtype(q, torch.bfloat16, name)
+    _require(q.dim() == 3 and q.shape[2] == HEAD_DIM, f"{name} must be [tokens][heads][{HEAD_DIM}]")
+
+
+def _check_tables(page_table: torch.Tensor, kv_lens: torch.Tensor, qo_indptr: Optional[torch.Tensor]) -> int:
+    """Dtypes and shapes of the request metadata; returns the batch size."""
+    _check_dtype(page_table, torch.int32, "page_table")
+    _check_dtype(kv_lens, torch.int32, "kv_lens")
+    _require(kv_lens.dim() == 1, "kv_lens must be [batch]")
+    batch = kv_lens.shape[0]
+    _require(page_table.dim() == 2 and page_table.shape[0] == batch, "page_table must be [batch][max_pages]")
+    if qo_indptr is not None:
+        _check_dtype(qo_indptr, torch.int32, "qo_indptr")
+        _require(qo_indptr.dim() == 1 and qo_indptr.shape[0] == batch + 1, "qo_indptr must be [batch + 1]")
+    return batch
+
+
+def _check_out(out: Optional[torch.Tensor], lse: Optional[torch.Tensor], rows: int, heads: int) -> None:
+    if out is not None:
+        _check_rows(out, "out")
+        _require(tuple(out.shape) == (rows, heads, HEAD_DIM), "out must have the shape of q")
+    if lse is not None:
+        _check_dtype(lse, torch.float32, "lse")
+        _require(tuple(lse.shape) == (rows, heads), "lse must be [tokens][heads]")
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -140,7 +182,11 @@ def nvfp4_workspace_bytes(op: int, batch: int, num_q_heads: int, num_kv_heads: i
 
 
 def nvfp4_kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, cache: Cache, stream=None) -> None:
-    assert k.dtype == torch.bfloat16 and v.dtype == torch.bfloat16 and slot_mapping.dtype == torch.int64
+    _check_rows(k, "k")
+    _check_rows(v, "v")
+    _require(k.shape == v.shape and k.shape[1] == cache.num_kv_heads, "k and v must be [tokens][kv heads][128]")
+    _check_dtype(slot_mapping, torch.int64, "slot_mapping")
+    _require(slot_mapping.dim() == 1 and slot_mapping.shape[0] == k.shape[0], "slot_mapping must be [tokens]")
     d = cache.desc()
     _check("nvfp4_kv_append", lib.nvfp4_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
                                                   ctypes.byref(d), _stream(stream)))
@@ -151,10 +197,10 @@ def nvfp4_paged_prefill(q: torch.Tensor, cache: Cache, page_table: torch.Tensor,
                         variant: int = VARIANT_A4Q, out: Optional[torch.Tensor] = None,
                         lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                         stream=None) -> torch.Tensor:
-    assert q.dtype == torch.bfloat16 and page_table.dtype == torch.int32
-    assert kv_lens.dtype == torch.int32 and qo_indptr.dtype == torch.int32
+    _check_rows(q)
+    batch = _check_tables(page_table, kv_lens, qo_indptr)
     total_q, hq, _ = q.shape
-    batch = kv_lens.shape[0]
+    _check_out(out, lse, total_q, hq)
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
@@ -175,6 +221,8 @@ def nvfp4_paged_prefill_plan(cache: Cache, total_q: int, num_q_heads: int, page_
                              kv_lens: torch.Tensor, qo_indptr: torch.Tensor, workspace: torch.Tensor,
                              causal: bool = True, variant: int = VARIANT_A4Q, stream=None) -> None:
     """Schedule (and, in repack mode, the repacked tile records) into the workspace."""
+    _check_tables(page_table, kv_lens, qo_indptr)
+    _check_dtype(workspace, torch.uint8, "workspace")
     d = cache.desc()
     _check("nvfp4_paged_prefill_plan", lib.nvfp4_paged_prefill_plan(
         total_q, num_q_heads, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
@@ -188,7 +236,11 @@ def nvfp4_paged_prefill_run(q: torch.Tensor, cache: Cache, page_table: torch.Ten
                             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                             stream=None) -> torch.Tensor:
     """The attention kernel alone, reading the schedule a matching plan call wrote."""
+    _check_rows(q)
+    _check_tables(page_table, kv_lens, qo_indptr)
+    _check_dtype(workspace, torch.uint8, "workspace")
     total_q, hq, _ = q.shape
+    _check_out(out, lse, total_q, hq)
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
@@ -212,9 +264,10 @@ def nvfp4_paged_prefill_noalloc(q: torch.Tensor, cache: Cache, page_table: torch
     """Same as nvfp4_paged_prefill but with the work schedule in the
     library's static device array: for callers that cannot allocate device
     memory at call time.  Calls that overlap on the GPU race on that array."""
-    assert q.dtype == torch.bfloat16 and page_table.dtype == torch.int32
-    assert kv_lens.dtype == torch.int32 and qo_indptr.dtype == torch.int32
+    _check_rows(q)
+    _check_tables(page_table, kv_lens, qo_indptr)
     total_q, hq, _ = q.shape
+    _check_out(out, lse, total_q, hq)
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
@@ -231,8 +284,11 @@ def nvfp4_paged_decode(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, 
                        sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                        lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                        stream=None) -> torch.Tensor:
-    assert q.dtype == torch.bfloat16 and page_table.dtype == torch.int32 and kv_lens.dtype == torch.int32
-    batch, hq, _ = q.shape
+    _check_rows(q)
+    batch = _check_tables(page_table, kv_lens, None)
+    _require(q.shape[0] == batch, "q must be [batch][heads][128] (one query token per request)")
+    _, hq, _ = q.shape
+    _check_out(out, lse, batch, hq)
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
@@ -249,7 +305,8 @@ def nvfp4_paged_decode(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, 
 
 
 def nvfp4_quantize_rows(x: torch.Tensor, mode: int = QUANT_GLOBAL, global_scale: float = 1.0, stream=None):
-    assert x.dtype == torch.bfloat16 and x.shape[-1] == HEAD_DIM
+    _check_dtype(x, torch.bfloat16, "x")
+    _require(x.shape[-1] == HEAD_DIM, f"x must be [...][{HEAD_DIM}]")
     rows = x.numel() // HEAD_DIM
     packed = torch.empty(rows, HEAD_DIM // 2, dtype=torch.uint8, device=x.device)
     scales = torch.empty(rows, HEAD_DIM // 16, dtype=torch.uint8, device=x.device)
@@ -261,7 +318,13 @@ def nvfp4_quantize_rows(x: torch.Tensor, mode: int = QUANT_GLOBAL, global_scale:
 
 def nvfp4_dequantize_rows(packed: torch.Tensor, scales: torch.Tensor, row_scales: Optional[torch.Tensor] = None,
                           global_scale: float = 1.0, stream=None) -> torch.Tensor:
+    _check_dtype(packed, torch.uint8, "packed")
+    _check_dtype(scales, torch.uint8, "scales")
+    _check_dtype(row_scales, torch.float32, "row_scales")
     rows = packed.shape[0]
+    _require(tuple(packed.shape) == (rows, HEAD_DIM // 2) and tuple(scales.shape) == (rows, HEAD_DIM // 16),
+             "packed must be [rows][64] and scales [rows][8]")
+    _require(row_scales is None or tuple(row_scales.shape) == (rows,), "row_scales must be [rows]")
     out = torch.empty(rows, HEAD_DIM, dtype=torch.bfloat16, device=packed.device)
     _check("nvfp4_dequantize_rows", lib.nvfp4_dequantize_rows(_ptr(packed), _ptr(scales), rows, _ptr(row_scales),
                                                               float(global_scale), _ptr(out), _stream(stream)))
