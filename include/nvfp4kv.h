@@ -116,9 +116,16 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  * causal:     1 = query i of a request sees keys j <= kv_len - q_len + i
  *             (bottom-right alignment); 0 = every query sees all kv_len keys.
  * sm_scale:   softmax scale applied to q.k (e.g. 1/sqrt(128)).
- * variant:    NVFP4KV_VARIANT_A4Q or NVFP4KV_VARIANT_DQ_AHEAD.  The A4Q query
- *             scheme is per (token, head) row: g_row = amax_row/2688, then the
- *             same 16-value block codec as the cache.
+ * variant:    NVFP4KV_VARIANT_A4Q or NVFP4KV_VARIANT_DQ_AHEAD.
+ * q_global_scale: the A4Q query scale scheme ("NVFP4 KV cache A4Q prefill
+ *             explained", section "Make query accuracy a release gate": the
+ *             scheme is a recorded choice).  0 = per (token, head) row, dual
+ *             level: g_row = amax_row/2688.  > 0 = this one fp32 scale for
+ *             every query row: a per-tensor dual-level scheme when the caller
+ *             passes amax(Q)/2688, a single-level scheme when it passes 1.
+ *             Either way the row is then coded with the cache's 16-value
+ *             block codec.  Must be finite and >= 0; ignored by
+ *             NVFP4KV_VARIANT_DQ_AHEAD (its query stays BF16).
  * o:          bf16 [total_q][num_q_heads][128] output (rows of q not covered
  *             by qo_indptr are left untouched).
  * lse:        optional fp32 [total_q][num_q_heads] natural-log sum-exp of the
@@ -136,13 +143,15 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  *             workspace ("NVFP4 KV cache A4Q prefill explained", section
  *             "Compare A4Q with dequantize-ahead repacking"), instead of
  *             once per q tile inside the kernel.
- *             Results are identical either way.
+ *             Both modes compute the same attention; they differ only in
+ *             KV tile size and so in the order of the fp32 accumulation.
  * num_q_heads must be a multiple of num_kv_heads with a power-of-two ratio
  * of at most 128.  q_len == 0 requests produce nothing. */
 int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
                         const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
                         const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
-                        void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+                        float q_global_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                        void* stream);
 
 /* The two halves of nvfp4_paged_prefill, for callers that time or overlap
  * them separately.  nvfp4_paged_prefill_plan writes the work schedule into
@@ -152,8 +161,8 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
  * arguments (the pair computes the same mode from them) and the same
  * workspace, with the cache unchanged in between; otherwise its result is
  * undefined.  nvfp4_paged_prefill(...) is plan(...) then run(...).  Arguments
- * and errors as for nvfp4_paged_prefill (plan takes no q, o, lse or
- * sm_scale).  Neither allocates. */
+ * and errors as for nvfp4_paged_prefill (plan takes no q, o, lse,
+ * sm_scale or q_global_scale).  Neither allocates. */
 int nvfp4_paged_prefill_plan(int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
                              const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
                              const int32_t* qo_indptr, int32_t batch, int32_t causal, int32_t variant,
@@ -161,8 +170,8 @@ int nvfp4_paged_prefill_plan(int64_t total_q, int32_t num_q_heads, const nvfp4kv
 int nvfp4_paged_prefill_run(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
                             const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
                             const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale,
-                            int32_t variant, void* o, float* lse, void* workspace, size_t workspace_bytes,
-                            void* stream);
+                            int32_t variant, float q_global_scale, void* o, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 /* nvfp4_paged_prefill without a workspace argument, for callers that cannot
  * allocate device memory: an engine that plans all device memory up front and
@@ -171,16 +180,21 @@ int nvfp4_paged_prefill_run(const void* q, int64_t total_q, int32_t num_q_heads,
  * pages have no counterpart of this call; it is a packaging of the same
  * kernels.  The work schedule lives in a static device array of
  * nvfp4_paged_prefill_noalloc_max_bytes() bytes (1 MiB) that every GPU which
- * loads the library holds until the process exits.  Arguments and results are
- * those of nvfp4_paged_prefill.  Returns NVFP4KV_ERR_WORKSPACE when the
- * schedule of the call (nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, ...)) is
- * larger than the array.  The first call on a device looks up the array's
- * device address (make it before any stream capture).  All calls share the
- * array: calls that overlap on the GPU race.  Allocates nothing. */
+ * loads the library holds until the process exits; only the schedule is
+ * stored there, so the call always runs in-kernel mode (V dequantized inside
+ * the attention kernel) and its output equals, bit for bit, that of
+ * nvfp4_paged_prefill given a schedule-only workspace.  Arguments and results
+ * are those of nvfp4_paged_prefill.  Returns NVFP4KV_ERR_WORKSPACE when the
+ * schedule of the call (nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, ..., 0)) is
+ * larger than the array, and NVFP4KV_ERR_UNSUPPORTED on a device that is not
+ * sm_103.  The first call on a device looks up the array's device address
+ * (make it before any stream capture); the address is kept for the life of
+ * the process, which assumes one CUDA context per device.  All calls share
+ * the array: calls that overlap on the GPU race.  Allocates nothing. */
 int nvfp4_paged_prefill_noalloc(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
                                 const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
                                 const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale,
-                                int32_t variant, void* o, float* lse, void* stream);
+                                int32_t variant, float q_global_scale, void* o, float* lse, void* stream);
 
 /* Size in bytes of the static schedule array used by
  * nvfp4_paged_prefill_noalloc.  Host-only. */

@@ -56,11 +56,11 @@ def _load() -> ctypes.CDLL:
     P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     D = ctypes.POINTER(CacheDesc)
     lib.nvfp4_kv_append.argtypes = [P, P, P, i64, D, P]
-    lib.nvfp4_paged_prefill.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, P, P, P, sz, P]
+    lib.nvfp4_paged_prefill.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, f32, P, P, P, sz, P]
     lib.nvfp4_paged_decode.argtypes = [P, i32, D, P, i32, P, i32, f32, P, P, P, sz, P]
     lib.nvfp4_paged_prefill_plan.argtypes = [i64, i32, D, P, i32, P, P, i32, i32, i32, P, sz, P]
-    lib.nvfp4_paged_prefill_run.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, P, P, P, sz, P]
-    lib.nvfp4_paged_prefill_noalloc.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, P, P, P]
+    lib.nvfp4_paged_prefill_run.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, f32, P, P, P, sz, P]
+    lib.nvfp4_paged_prefill_noalloc.argtypes = [P, i64, i32, D, P, i32, P, P, i32, i32, f32, i32, f32, P, P, P]
     lib.nvfp4_paged_prefill_noalloc_max_bytes.argtypes = []
     lib.nvfp4_paged_prefill_noalloc_max_bytes.restype = sz
     lib.nvfp4_workspace_bytes.argtypes = [i32, i32, i32, i32, i64, i32]
@@ -145,8 +145,31 @@ def _check_out(out: Optional[torch.Tensor], lse: Optional[torch.Tensor], rows: i
         _require(tuple(lse.shape) == (rows, heads), "lse must be [tokens][heads]")
 
 
-def _stream(stream) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _device(*tensors) -> torch.device:
+    """The one CUDA device every given tensor lives on.  The library launches
+    on the current device with pointers that must belong to it, so a host
+    tensor or tensors spread over several devices are refused here."""
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors passed to nvfp4kv must live on a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"tensors passed to nvfp4kv must share one device ({dev} and {t.device})")
+    if dev is None:
+        raise ValueError("tensors passed to nvfp4kv must live on a CUDA device")
+    return dev
+
+
+def _stream(stream, dev: torch.device) -> ctypes.c_void_p:
+    """The caller's stream (or the current stream of `dev`); it must belong to
+    the device the tensors live on."""
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if s.device != dev:
+        raise ValueError(f"stream is on {s.device} but the tensors are on {dev}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -166,7 +189,17 @@ class Cache:
         self.num_pages, self.num_kv_heads = num_pages, num_kv_heads
         self.k_global_scale, self.v_global_scale = float(k_global_scale), float(v_global_scale)
 
+    def pools(self):
+        return (self.k_data, self.k_scale, self.v_data, self.v_scale)
+
     def desc(self) -> CacheDesc:
+        """Host descriptor of the four pools.  The pools are device memory that
+        the kernels read and write, so a host-memory cache is refused."""
+        for t in self.pools():
+            if not t.is_cuda:
+                raise ValueError("cache pools must live on a CUDA device")
+            if not t.is_contiguous() or t.dtype != torch.uint8:
+                raise ValueError("cache pools must be contiguous uint8 tensors")
         return CacheDesc(self.k_data.data_ptr(), self.k_scale.data_ptr(), self.v_data.data_ptr(),
                          self.v_scale.data_ptr(), self.num_pages, PAGE_SIZE, self.num_kv_heads, HEAD_DIM,
                          self.k_global_scale, self.v_global_scale)
@@ -187,20 +220,27 @@ def nvfp4_kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor
     _require(k.shape == v.shape and k.shape[1] == cache.num_kv_heads, "k and v must be [tokens][kv heads][128]")
     _check_dtype(slot_mapping, torch.int64, "slot_mapping")
     _require(slot_mapping.dim() == 1 and slot_mapping.shape[0] == k.shape[0], "slot_mapping must be [tokens]")
-    d = cache.desc()
-    _check("nvfp4_kv_append", lib.nvfp4_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
-                                                  ctypes.byref(d), _stream(stream)))
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), k, v, slot_mapping)
+    with torch.cuda.device(dev):
+        _check("nvfp4_kv_append", lib.nvfp4_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
+                                                      ctypes.byref(d), _stream(stream, dev)))
 
 
 def nvfp4_paged_prefill(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, kv_lens: torch.Tensor,
                         qo_indptr: torch.Tensor, causal: bool = True, sm_scale: Optional[float] = None,
                         variant: int = VARIANT_A4Q, out: Optional[torch.Tensor] = None,
                         lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                        stream=None) -> torch.Tensor:
+                        stream=None, q_global_scale: float = 0.0) -> torch.Tensor:
+    """A4Q (or dequant-ahead) paged prefill.  q_global_scale selects the A4Q
+    query scale scheme: 0 = per (token, head) row, amax/2688; > 0 = that one
+    scale for every row (per-tensor, or 1 for single level)."""
     _check_rows(q)
     batch = _check_tables(page_table, kv_lens, qo_indptr)
     total_q, hq, _ = q.shape
     _check_out(out, lse, total_q, hq)
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), q, page_table, kv_lens, qo_indptr, out, lse, workspace)
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
@@ -208,12 +248,13 @@ def nvfp4_paged_prefill(q: torch.Tensor, cache: Cache, page_table: torch.Tensor,
     if workspace is None:
         need = nvfp4_workspace_bytes(OP_PREFILL, batch, hq, cache.num_kv_heads, total_q,
                                      page_table.shape[1] * PAGE_SIZE)
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    d = cache.desc()
-    _check("nvfp4_paged_prefill", lib.nvfp4_paged_prefill(
-        _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
-        _ptr(qo_indptr), batch, int(bool(causal)), float(sm_scale), int(variant), _ptr(out), _ptr(lse),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check("nvfp4_paged_prefill", lib.nvfp4_paged_prefill(
+            _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+            _ptr(qo_indptr), batch, int(bool(causal)), float(sm_scale), int(variant), float(q_global_scale),
+            _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream, dev)))
     return out
 
 
@@ -223,33 +264,38 @@ def nvfp4_paged_prefill_plan(cache: Cache, total_q: int, num_q_heads: int, page_
     """Schedule (and, in repack mode, the repacked tile records) into the workspace."""
     _check_tables(page_table, kv_lens, qo_indptr)
     _check_dtype(workspace, torch.uint8, "workspace")
-    d = cache.desc()
-    _check("nvfp4_paged_prefill_plan", lib.nvfp4_paged_prefill_plan(
-        total_q, num_q_heads, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
-        _ptr(qo_indptr), kv_lens.shape[0], int(bool(causal)), int(variant), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), page_table, kv_lens, qo_indptr, workspace)
+    with torch.cuda.device(dev):
+        _check("nvfp4_paged_prefill_plan", lib.nvfp4_paged_prefill_plan(
+            total_q, num_q_heads, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+            _ptr(qo_indptr), kv_lens.shape[0], int(bool(causal)), int(variant), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream, dev)))
 
 
 def nvfp4_paged_prefill_run(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, kv_lens: torch.Tensor,
                             qo_indptr: torch.Tensor, workspace: torch.Tensor, causal: bool = True,
                             sm_scale: Optional[float] = None, variant: int = VARIANT_A4Q,
                             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                            stream=None) -> torch.Tensor:
+                            stream=None, q_global_scale: float = 0.0) -> torch.Tensor:
     """The attention kernel alone, reading the schedule a matching plan call wrote."""
     _check_rows(q)
     _check_tables(page_table, kv_lens, qo_indptr)
     _check_dtype(workspace, torch.uint8, "workspace")
     total_q, hq, _ = q.shape
     _check_out(out, lse, total_q, hq)
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), q, page_table, kv_lens, qo_indptr, workspace, out, lse)
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
         sm_scale = HEAD_DIM ** -0.5
-    d = cache.desc()
-    _check("nvfp4_paged_prefill_run", lib.nvfp4_paged_prefill_run(
-        _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
-        _ptr(qo_indptr), kv_lens.shape[0], int(bool(causal)), float(sm_scale), int(variant), _ptr(out),
-        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    with torch.cuda.device(dev):
+        _check("nvfp4_paged_prefill_run", lib.nvfp4_paged_prefill_run(
+            _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+            _ptr(qo_indptr), kv_lens.shape[0], int(bool(causal)), float(sm_scale), int(variant),
+            float(q_global_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream, dev)))
     return out
 
 
@@ -260,23 +306,27 @@ def nvfp4_paged_prefill_noalloc_max_bytes() -> int:
 def nvfp4_paged_prefill_noalloc(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, kv_lens: torch.Tensor,
                                 qo_indptr: torch.Tensor, causal: bool = True, sm_scale: Optional[float] = None,
                                 variant: int = VARIANT_A4Q, out: Optional[torch.Tensor] = None,
-                                lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                                lse: Optional[torch.Tensor] = None, stream=None,
+                                q_global_scale: float = 0.0) -> torch.Tensor:
     """Same as nvfp4_paged_prefill but with the work schedule in the
     library's static device array: for callers that cannot allocate device
-    memory at call time.  Calls that overlap on the GPU race on that array."""
+    memory at call time.  Always runs in-kernel mode.  Calls that overlap on
+    the GPU race on that array."""
     _check_rows(q)
     _check_tables(page_table, kv_lens, qo_indptr)
     total_q, hq, _ = q.shape
     _check_out(out, lse, total_q, hq)
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), q, page_table, kv_lens, qo_indptr, out, lse)
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
         sm_scale = HEAD_DIM ** -0.5
-    d = cache.desc()
-    _check("nvfp4_paged_prefill_noalloc", lib.nvfp4_paged_prefill_noalloc(
-        _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
-        _ptr(qo_indptr), kv_lens.shape[0], int(bool(causal)), float(sm_scale), int(variant), _ptr(out), _ptr(lse),
-        _stream(stream)))
+    with torch.cuda.device(dev):
+        _check("nvfp4_paged_prefill_noalloc", lib.nvfp4_paged_prefill_noalloc(
+            _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+            _ptr(qo_indptr), kv_lens.shape[0], int(bool(causal)), float(sm_scale), int(variant),
+            float(q_global_scale), _ptr(out), _ptr(lse), _stream(stream, dev)))
     return out
 
 
@@ -289,30 +339,35 @@ def nvfp4_paged_decode(q: torch.Tensor, cache: Cache, page_table: torch.Tensor, 
     _require(q.shape[0] == batch, "q must be [batch][heads][128] (one query token per request)")
     _, hq, _ = q.shape
     _check_out(out, lse, batch, hq)
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), q, page_table, kv_lens, out, lse, workspace)
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
         sm_scale = HEAD_DIM ** -0.5
     need = nvfp4_workspace_bytes(OP_DECODE, batch, hq, cache.num_kv_heads, 0, page_table.shape[1] * PAGE_SIZE)
     if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    d = cache.desc()
-    _check("nvfp4_paged_decode", lib.nvfp4_paged_decode(
-        _ptr(q), hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens), batch,
-        float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check("nvfp4_paged_decode", lib.nvfp4_paged_decode(
+            _ptr(q), hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens), batch,
+            float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream, dev)))
     return out
 
 
 def nvfp4_quantize_rows(x: torch.Tensor, mode: int = QUANT_GLOBAL, global_scale: float = 1.0, stream=None):
     _check_dtype(x, torch.bfloat16, "x")
     _require(x.shape[-1] == HEAD_DIM, f"x must be [...][{HEAD_DIM}]")
+    dev = _device(x)
     rows = x.numel() // HEAD_DIM
-    packed = torch.empty(rows, HEAD_DIM // 2, dtype=torch.uint8, device=x.device)
-    scales = torch.empty(rows, HEAD_DIM // 16, dtype=torch.uint8, device=x.device)
-    row_scales = torch.empty(rows, dtype=torch.float32, device=x.device) if mode == QUANT_PER_ROW else None
-    _check("nvfp4_quantize_rows", lib.nvfp4_quantize_rows(_ptr(x), rows, mode, float(global_scale), _ptr(packed),
-                                                          _ptr(scales), _ptr(row_scales), _stream(stream)))
+    packed = torch.empty(rows, HEAD_DIM // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(rows, HEAD_DIM // 16, dtype=torch.uint8, device=dev)
+    row_scales = torch.empty(rows, dtype=torch.float32, device=dev) if mode == QUANT_PER_ROW else None
+    with torch.cuda.device(dev):
+        _check("nvfp4_quantize_rows", lib.nvfp4_quantize_rows(_ptr(x), rows, mode, float(global_scale),
+                                                              _ptr(packed), _ptr(scales), _ptr(row_scales),
+                                                              _stream(stream, dev)))
     return packed, scales, row_scales
 
 
@@ -325,15 +380,26 @@ def nvfp4_dequantize_rows(packed: torch.Tensor, scales: torch.Tensor, row_scales
     _require(tuple(packed.shape) == (rows, HEAD_DIM // 2) and tuple(scales.shape) == (rows, HEAD_DIM // 16),
              "packed must be [rows][64] and scales [rows][8]")
     _require(row_scales is None or tuple(row_scales.shape) == (rows,), "row_scales must be [rows]")
-    out = torch.empty(rows, HEAD_DIM, dtype=torch.bfloat16, device=packed.device)
-    _check("nvfp4_dequantize_rows", lib.nvfp4_dequantize_rows(_ptr(packed), _ptr(scales), rows, _ptr(row_scales),
-                                                              float(global_scale), _ptr(out), _stream(stream)))
+    dev = _device(packed, scales, row_scales)
+    out = torch.empty(rows, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    with torch.cuda.device(dev):
+        _check("nvfp4_dequantize_rows", lib.nvfp4_dequantize_rows(_ptr(packed), _ptr(scales), rows,
+                                                                  _ptr(row_scales), float(global_scale), _ptr(out),
+                                                                  _stream(stream, dev)))
     return out
 
 
+def _current_device() -> torch.device:
+    return torch.device("cuda", torch.cuda.current_device())
+
+
 def nvfp4kv_debug_wait_timeout(limit_ns: int, stream=None) -> None:
-    _check("nvfp4kv_debug_wait_timeout", lib.nvfp4kv_debug_wait_timeout(int(limit_ns), _stream(stream)))
+    dev = stream.device if stream is not None else _current_device()
+    with torch.cuda.device(dev):
+        _check("nvfp4kv_debug_wait_timeout", lib.nvfp4kv_debug_wait_timeout(int(limit_ns), _stream(stream, dev)))
 
 
 def nvfp4kv_get_device_status(stream=None) -> int:
-    return int(lib.nvfp4kv_get_device_status(_stream(stream)))
+    dev = stream.device if stream is not None else _current_device()
+    with torch.cuda.device(dev):
+        return int(lib.nvfp4kv_get_device_status(_stream(stream, dev)))

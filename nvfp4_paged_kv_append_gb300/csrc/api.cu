@@ -62,6 +62,18 @@ int device_state(DeviceState** out) {
   return d.rc;
 }
 
+}  // namespace
+
+// Capability check of the current device for code outside this file (the
+// allocation-free entry point checks the device before it touches its
+// static array): NVFP4KV_OK, NVFP4KV_ERR_UNSUPPORTED or NVFP4KV_ERR_CUDA.
+int nvfp4kv::current_device_status() {
+  DeviceState* d = nullptr;
+  return device_state(&d);
+}
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool finite_pos(float x) { return std::isfinite(x) && x > 0.0f; }
 
@@ -201,8 +213,8 @@ enum PrefillStage { kStagePlan = 1, kStageRun = 2 };
 // requested stages.  q/o/lse/sm_scale are only used by the run stage.
 int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
                    const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
-                   const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant, void* o,
-                   float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+                   const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
+                   float q_global_scale, void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_cache(cache);
   if (rc) return rc;
   if (batch < 0 || total_q < 0 || max_pages_per_req <= 0) return NVFP4KV_ERR_ARG;
@@ -212,6 +224,7 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   if (causal != 0 && causal != 1) return NVFP4KV_ERR_ARG;
   if (variant != NVFP4KV_VARIANT_A4Q && variant != NVFP4KV_VARIANT_DQ_AHEAD) return NVFP4KV_ERR_ARG;
   if ((stages & kStageRun) && !std::isfinite(sm_scale)) return NVFP4KV_ERR_ARG;
+  if (!std::isfinite(q_global_scale) || q_global_scale < 0.0f) return NVFP4KV_ERR_ARG;
   if (total_q * num_q_heads >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
   if (batch == 0 || total_q == 0) return NVFP4KV_OK;
   if (!page_table || !kv_lens || !qo_indptr) return NVFP4KV_ERR_ARG;
@@ -265,6 +278,7 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   a.sm_scale = sm_scale;
   a.k_g = cache->k_global_scale;
   a.v_g = cache->v_global_scale;
+  a.q_g = variant == NVFP4KV_VARIANT_A4Q ? q_global_scale : 0.0f;
   a.o = o;
   a.lse = lse;
   a.work = static_cast<const int*>(workspace);
@@ -286,10 +300,11 @@ extern "C" {
 int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
                         const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
                         const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
-                        void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+                        float q_global_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                        void* stream) {
   return prefill_stages(kStagePlan | kStageRun, q, total_q, num_q_heads, cache, page_table, max_pages_per_req,
-                        kv_lens, qo_indptr, batch, causal, sm_scale, variant, o, lse, workspace, workspace_bytes,
-                        stream);
+                        kv_lens, qo_indptr, batch, causal, sm_scale, variant, q_global_scale, o, lse, workspace,
+                        workspace_bytes, stream);
 }
 
 int nvfp4_paged_prefill_plan(int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
@@ -297,16 +312,18 @@ int nvfp4_paged_prefill_plan(int64_t total_q, int32_t num_q_heads, const nvfp4kv
                              const int32_t* qo_indptr, int32_t batch, int32_t causal, int32_t variant,
                              void* workspace, size_t workspace_bytes, void* stream) {
   return prefill_stages(kStagePlan, nullptr, total_q, num_q_heads, cache, page_table, max_pages_per_req, kv_lens,
-                        qo_indptr, batch, causal, 0.0f, variant, nullptr, nullptr, workspace, workspace_bytes, stream);
+                        qo_indptr, batch, causal, 0.0f, variant, 0.0f, nullptr, nullptr, workspace, workspace_bytes,
+                        stream);
 }
 
 int nvfp4_paged_prefill_run(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
                             const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
                             const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale,
-                            int32_t variant, void* o, float* lse, void* workspace, size_t workspace_bytes,
-                            void* stream) {
+                            int32_t variant, float q_global_scale, void* o, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream) {
   return prefill_stages(kStageRun, q, total_q, num_q_heads, cache, page_table, max_pages_per_req, kv_lens,
-                        qo_indptr, batch, causal, sm_scale, variant, o, lse, workspace, workspace_bytes, stream);
+                        qo_indptr, batch, causal, sm_scale, variant, q_global_scale, o, lse, workspace,
+                        workspace_bytes, stream);
 }
 
 

@@ -99,6 +99,7 @@ struct PrefillArgs {
   int log2_group;
   int causal;
   float sm_scale, k_g, v_g;
+  float q_g;        // A4Q query scale: 0 = per row (amax/2688), > 0 = this scale for every row
   void* o;          // bf16 [total_q][Hq][128]
   float* lse;       // optional [total_q][Hq]
   const int* work;  // [0] item count, [1] repacked tile count; items (int2) from work + 4
@@ -121,6 +122,10 @@ struct PlanArgs {
   int max_items;
   int* status;
 };
+
+// Per-device set-up and capability check of the current device (api.cu):
+// NVFP4KV_OK, NVFP4KV_ERR_UNSUPPORTED (not sm_103) or NVFP4KV_ERR_CUDA.
+int current_device_status();
 
 // Kernels (defined in append.cu, decode.cu, prefill.cu).
 __global__ void nvfp4_kv_append_kernel(AppendArgs a);

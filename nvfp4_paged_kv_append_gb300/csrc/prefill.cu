@@ -322,7 +322,7 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
                                                         (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim);
       if constexpr (L::kA4Q) {
         float g_row;
-        sfa_stage[r] = quantize_q_row(src, valid, smem + L::kOffQ, r, g_row);
+        sfa_stage[r] = quantize_q_row(src, valid, smem + L::kOffQ, r, a.q_g, g_row);
         qscale[r] = g_row;
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.sfa_ready);

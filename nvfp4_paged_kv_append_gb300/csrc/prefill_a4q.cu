@@ -298,7 +298,7 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
                                                       (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) *
                                                           kHeadDim);
     float g_row;
-    sfa_stage[r] = quantize_q_row(src, valid, smem + kOffQ2, r, g_row);
+    sfa_stage[r] = quantize_q_row(src, valid, smem + kOffQ2, r, a.q_g, g_row);
     const float c_r = g_row * a.k_g * a.sm_scale * kLog2e;
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.sfa_ready);

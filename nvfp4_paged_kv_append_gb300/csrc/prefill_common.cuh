@@ -108,14 +108,17 @@ __device__ __forceinline__ int64_t repack_index(const PrefillArgs& a, int b, int
 }
 
 // Quantize one 128-value bf16 row of Q A4Q-style ("NVFP4 KV cache A4Q prefill
-// explained", section "Quantize Q instead of expanding K"; per-row dual-level
-// scale): g_row = amax/2688, then the cache's 16-value block codec.  Writes
-// the 64 code bytes into row r of a 64B-swizzled FP4 tile and returns the
-// eight E4M3 block scales as two words (k-steps 0 and 1); zeros for an
-// invalid row.
-__device__ __forceinline__ uint2 quantize_q_row(const uint4* src, bool valid, uint8_t* qtile, int r, float& g_row) {
+// explained", section "Quantize Q instead of expanding K"; the section "Make
+// query accuracy a release gate" leaves the scale scheme open).  With q_g = 0
+// the scale is per row, dual level: g_row = amax/2688; with q_g > 0 every row
+// uses q_g (one per-tensor scale, or 1 for a single-level scheme).  Then the
+// cache's 16-value block codec.  Writes the 64 code bytes into row r of a
+// 64B-swizzled FP4 tile and returns the eight E4M3 block scales as two words
+// (k-steps 0 and 1); zeros for an invalid row.
+__device__ __forceinline__ uint2 quantize_q_row(const uint4* src, bool valid, uint8_t* qtile, int r, float q_g,
+                                                float& g_row) {
   float amax = 0.0f;
-  if (valid) {
+  if (valid && q_g == 0.0f) {
 #pragma unroll 4
     for (int i = 0; i < 16; ++i) {
       const uint4 v = src[i];
@@ -128,7 +131,7 @@ __device__ __forceinline__ uint2 quantize_q_row(const uint4* src, bool valid, ui
       }
     }
   }
-  g_row = __fdiv_rn(amax, 2688.0f);
+  g_row = q_g != 0.0f ? q_g : __fdiv_rn(amax, 2688.0f);
   uint32_t sc[8];
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {

@@ -205,3 +205,24 @@ def sample_rows(wl: Workload, per_request: int, seed: int = 0):
             pos.update(torch.randint(0, ql, (per_request,), generator=gen).tolist())
         rows.extend((b, int(i)) for i in sorted(pos))
     return rows
+
+
+def tile_rows(wl: Workload, rows_per_tile: int = 128, seed: int = 0):
+    """(request, position) pairs with one seeded query position inside every
+    block of rows_per_tile // group consecutive query tokens of every request
+    (a block of 128 rows = tokens x grouped heads), plus the first and last
+    query of every request.  Used to reach every (request, q block) of a large
+    batch with an affordable number of rows."""
+    gen = torch.Generator().manual_seed(seed + 13)
+    tpq = max(1, rows_per_tile // wl.group)
+    rows = []
+    for b, ql in enumerate(wl.q_lens):
+        if ql == 0:
+            continue
+        pos = {0, ql - 1}
+        n_blocks = (ql + tpq - 1) // tpq
+        off = torch.randint(0, tpq, (n_blocks,), generator=gen).tolist()
+        for t in range(n_blocks):
+            pos.add(min(ql - 1, t * tpq + off[t]))
+        rows.extend((b, int(i)) for i in sorted(pos))
+    return rows

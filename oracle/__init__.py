@@ -276,29 +276,35 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
             want.setdefault(int(b), []).append(int(i))
     result = {}
 
-    def one(task):
-        b, h, pos = task
-        q_len, kv_len = int(qo[b + 1] - qo[b]), int(kvl[b])
-        kd = gather_decode(pools, "k", pt[b], kv_len, h, k_g)
-        vd = gather_decode(pools, "v", pt[b], kv_len, h, v_g)
-        res = []
-        for gq in range(G):
-            hq = h * G + gq
-            qr = q[qo[b] + pos, hq, :]
-            qd = decode_q_a4q(qr) if q_mode == "a4q" else qr.astype(np.float64)
-            res.append((hq,) + attention_rows(qd, pos, q_len, kd, vd, causal, sm_scale))
-        return b, pos, res
-
-    tasks = []
+    # One request at a time: decode its K and V once per kv head, then run
+    # the rows in chunks so that every worker thread has work even when a
+    # request has few kv heads and many sampled rows.
     for b, positions in want.items():
-        pos = np.array(sorted(set(positions)), np.int32)
-        for h in range(Hkv):
-            tasks.append((b, h, pos))
-    for b, pos, res in _pmap(one, tasks):
-        for i in pos:
-            result.setdefault((b, int(i)), (np.zeros((Hq, pools.D)), np.zeros(Hq)))
-        for hq, o, lse in res:
-            for r, i in enumerate(pos):
-                result[(b, int(i))][0][hq] = o[r]
-                result[(b, int(i))][1][hq] = lse[r]
+        q_len, kv_len = int(qo[b + 1] - qo[b]), int(kvl[b])
+        pos_all = np.array(sorted(set(positions)), np.int32)
+        dec = dict(zip(range(Hkv), _pmap(
+            lambda h: (gather_decode(pools, "k", pt[b], kv_len, h, k_g),
+                       gather_decode(pools, "v", pt[b], kv_len, h, v_g)), range(Hkv))))
+        n_chunks = max(1, min(len(pos_all), -(-2 * WORKERS // Hkv)))
+        chunks = [c for c in np.array_split(pos_all, n_chunks) if len(c)]
+
+        def one(task):
+            h, pos = task
+            kd, vd = dec[h]
+            res = []
+            for gq in range(G):
+                hq = h * G + gq
+                qr = q[qo[b] + pos, hq, :]
+                qd = decode_q_a4q(qr) if q_mode == "a4q" else qr.astype(np.float64)
+                res.append((hq,) + attention_rows(qd, pos, q_len, kd, vd, causal, sm_scale))
+            return pos, res
+
+        for i in pos_all:
+            result[(b, int(i))] = (np.zeros((Hq, pools.D)), np.zeros(Hq))
+        for pos, res in _pmap(one, [(h, c) for h in range(Hkv) for c in chunks]):
+            for hq, o, lse in res:
+                for r, i in enumerate(pos):
+                    result[(b, int(i))][0][hq] = o[r]
+                    result[(b, int(i))][1][hq] = lse[r]
+        del dec
     return result

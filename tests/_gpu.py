@@ -116,3 +116,23 @@ def oracle_prefill(pools, inp, q_mode, causal=True, rows=None):
     return oracle.paged_attention(pools, inp.q.float().numpy(), inp.qo_indptr, inp.kv_lens, inp.page_table,
                                   inp.wl.num_q_heads, inp.k_global, inp.v_global, causal, inp.sm_scale,
                                   q_mode=q_mode, rows=rows)
+
+
+_ORACLE_OUT = {}
+
+
+def oracle_prefill_cached(cfg, q_mode, rows, causal=True):
+    """oracle_prefill on a named configuration's session inputs, computed once
+    per (configuration, query mode, row set) and shared by the tests that run
+    the same rows in several kernel modes."""
+    key = (cfg, q_mode, causal, None if rows is None else tuple(rows))
+    if key not in _ORACLE_OUT:
+        _ORACLE_OUT[key] = oracle_prefill(pools_for(cfg), inputs(cfg), q_mode, causal=causal, rows=rows)
+    return _ORACLE_OUT[key]
+
+
+def repack_mode_expected(wl):
+    """The library's rule for repack mode given a workspace with room for the
+    records: requests average at least two 128-row q tiles per kv head."""
+    qtiles = (wl.total_q * wl.group + 127) // 128
+    return qtiles >= 2 * wl.batch

@@ -80,11 +80,14 @@ def test_invalid_arguments_rejected_on_host(nk):
     assert lib.nvfp4_kv_append(null, null, null, 0, ctypes.byref(bad), null) == -1
     assert lib.nvfp4_kv_append(null, null, null, 0, ctypes.byref(d), null) == 0  # empty append is a no-op
     # prefill: Hq not a multiple of Hkv, bad variant, missing workspace
-    args = lambda hq, variant, ws: (16, 8, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, variant, 16, null, ws, 64, null)
+    args = lambda hq, variant, ws, qg=0.0: (16, 8, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, variant, qg, 16,
+                                            null, ws, 64, null)
     assert lib.nvfp4_paged_prefill(*args(3, 0, 16)) == -1
     assert lib.nvfp4_paged_prefill(*args(6, 0, 16)) == -1   # ratio 3 is not a power of two
     assert lib.nvfp4_paged_prefill(*args(4, 2, 16)) == -1
     assert lib.nvfp4_paged_prefill(*args(4, 0, null)) == -3
+    assert lib.nvfp4_paged_prefill(*args(4, 0, 16, -1.0)) == -1          # query scale must be >= 0
+    assert lib.nvfp4_paged_prefill(*args(4, 0, 16, float("nan"))) == -1  # and finite
     # decode: group of 32 unsupported; workspace too small
     assert lib.nvfp4_paged_decode(16, 64, ctypes.byref(d), 16, 1, 16, 1, 0.1, 16, null, 16, 16, null) == -1
     assert lib.nvfp4_paged_decode(16, 4, ctypes.byref(d), 16, 1, 16, 1, 0.1, 16, null, 16, 16, null) == -3
@@ -106,12 +109,12 @@ def test_plan_run_and_noalloc_reject_bad_arguments_on_host(nk):
     assert plan(4, 1, 7, 16) == -1   # unknown variant
     assert plan(4, 1, 0, null) == -3  # no workspace
     run = lambda q, scale: lib.nvfp4_paged_prefill_run(
-        q, 16, 4, ctypes.byref(d), 16, 1, 16, 16, 1, 1, scale, 0, 16, null, 16, 4096, null)
+        q, 16, 4, ctypes.byref(d), 16, 1, 16, 16, 1, 1, scale, 0, 0.0, 16, null, 16, 4096, null)
     assert run(16, float("nan")) == -1  # sm_scale must be finite
     assert run(8, 0.1) == -1            # q not 16-byte aligned
     assert run(null, 0.1) == -1         # no q
     noalloc = lambda hq: lib.nvfp4_paged_prefill_noalloc(
-        16, 16, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, 0, 16, null, null)
+        16, 16, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, 0, 0.0, 16, null, null)
     assert noalloc(0) == -1
     assert noalloc(3) == -1
 

@@ -80,3 +80,26 @@ def test_bad_dtypes_and_shapes_are_refused(b, inp):
         b.nvfp4_paged_prefill_run(inp.q, c, inp.page_table, inp.kv_lens, inp.qo_indptr, torch.empty(16))
     with pytest.raises(ValueError, match="packed must be"):
         b.nvfp4_dequantize_rows(torch.zeros(6, 32, dtype=torch.uint8), torch.zeros(6, 8, dtype=torch.uint8))
+
+
+def test_host_cache_is_refused_first(b, inp):
+    """The cache pools are checked before the other tensors: a cache in host
+    memory is named in the error even when the other arguments are fine."""
+    c = _cache(b, inp)
+    with pytest.raises(ValueError, match="cache pools must live on a CUDA device"):
+        b.nvfp4_paged_prefill(inp.q, c, inp.page_table, inp.kv_lens, inp.qo_indptr)
+    with pytest.raises(ValueError, match="cache pools must live on a CUDA device"):
+        b.nvfp4_kv_append(inp.k, inp.v, inp.slot_mapping, c)
+    qd = inp.q[inp.qo_indptr[1:] - 1].contiguous()
+    with pytest.raises(ValueError, match="cache pools must live on a CUDA device"):
+        b.nvfp4_paged_decode(qd, c, inp.page_table, inp.kv_lens)
+
+
+def test_device_helper_refuses_host_and_mixed_tensors(b):
+    with pytest.raises(ValueError, match="must live on a CUDA device"):
+        b._device(torch.zeros(2), None)
+    with pytest.raises(ValueError, match="must live on a CUDA device"):
+        b._device(None)
+    # any non-CUDA device is refused, not only the host
+    with pytest.raises(ValueError, match="must live on a CUDA device"):
+        b._device(torch.zeros(2, device="meta"))

@@ -17,10 +17,11 @@ pytestmark = pytest.mark.gpu
 VARIANTS = [(0, "a4q"), (1, "bf16")]
 
 
-def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None, mode="auto"):
+def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None, mode="auto", ref=None):
     got, lse, status = G.run_prefill(inp, cache, variant, causal=causal, mode=mode)
     assert status == 0
-    ref = G.oracle_prefill(pools, inp, q_mode, causal=causal, rows=rows)
+    if ref is None:
+        ref = G.oracle_prefill(pools, inp, q_mode, causal=causal, rows=rows)
     mx, fro, n = G.compare_rows(got, ref, inp.qo_indptr)
     lerr = G.compare_lse(lse, ref, inp.qo_indptr)
     assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro, n)
@@ -65,11 +66,12 @@ def test_prefill_zero_length_and_edge_rows(variant, q_mode):
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 def test_prefill_shortq_longkv(variant, q_mode, mode):
     """batch 4, q 128 at the end of kv 2048, 32/8 heads, permuted pages: all
-    rows of request 0, sampled rows of the others."""
+    rows of request 0 and one row of every 128-row q tile of the others."""
     inp = G.inputs("shortq")
     cache = G.gpu_cache(inp)
-    rows = [(0, i) for i in range(128)] + [r for r in W.sample_rows(inp.wl, 6) if r[0] != 0]
-    _check(inp, cache, G.pools_for("shortq"), variant, q_mode, rows=rows, mode=mode)
+    rows = sorted(set([(0, i) for i in range(128)] + W.tile_rows(inp.wl)))
+    ref = G.oracle_prefill_cached("shortq", q_mode, rows)
+    _check(inp, cache, None, variant, q_mode, mode=mode, ref=ref)
 
 
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
@@ -85,19 +87,56 @@ def test_prefill_tails(variant, q_mode):
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 def test_prefill_full_16k_sampled(variant, q_mode, mode):
     """The 16K causal configuration at full size, as the benchmark runs it
-    (cache built by the CUDA append in shuffled order); sampled rows."""
+    (cache built by the CUDA append in shuffled order).  One seeded query
+    position inside every 128-row q tile (32 tokens x 4 grouped heads), so
+    every (q tile, kv head) work item of the schedule is checked: 512
+    positions x 32 heads."""
     inp = G.inputs("prefill16k")
     cache = G.gpu_cache(inp, append_order=W.shuffled_append_order(inp.wl.total_kv))
-    rows = W.sample_rows(inp.wl, 14)
-    _check(inp, cache, G.pools_for("prefill16k"), variant, q_mode, rows=rows, mode=mode)
+    rows = W.tile_rows(inp.wl)
+    assert len({(b, i // 32) for b, i in rows}) == 16384 // 32
+    ref = G.oracle_prefill_cached("prefill16k", q_mode, rows)
+    _check(inp, cache, None, variant, q_mode, mode=mode, ref=ref)
 
 
-def test_prefill_long_ragged_sampled():
-    """32,768 + 7,001 tokens, 64/8 heads, A4Q; sampled rows of both requests."""
-    inp = W.make_inputs(W.long_prefill_ragged())
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_long_ragged_every_tile(variant, q_mode):
+    """32,768 + 7,001 tokens in one batch, 64/8 heads (16 tokens per 128-row
+    q tile): one seeded query position in every q tile of both requests,
+    both variants (repack mode)."""
+    inp = G.inputs("prefill32k")
     cache = G.gpu_cache(inp)
-    rows = W.sample_rows(inp.wl, 5)
-    _check(inp, cache, G.oracle_pools(inp), 0, "a4q", rows=rows)
+    rows = W.tile_rows(inp.wl)
+    tiles = {(b, i // 16) for b, i in rows}
+    assert len(tiles) == 32768 // 16 + (7001 + 15) // 16
+    ref = G.oracle_prefill_cached("prefill32k", q_mode, rows)
+    _check(inp, cache, None, variant, q_mode, ref=ref)
+
+
+@pytest.mark.parametrize("mode", ["auto", "inkernel"])
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_group1_repack(variant, q_mode, mode):
+    """One query head per kv head (G = 1): 128 tokens per q tile.  Two
+    requests average more than two q tiles per kv head, so "auto" runs the
+    repack-mode kernels (the two-CTA kernel for A4Q); every row is checked."""
+    wl = W.Workload("g1_repack", [300, 260], [420, 260], 3, 3, seed=17)
+    assert G.repack_mode_expected(wl)
+    inp = W.make_inputs(wl)
+    cache = G.gpu_cache(inp, fill=0x7F)
+    _check(inp, cache, G.oracle_pools(inp), variant, q_mode, mode=mode)
+
+
+@pytest.mark.parametrize("mode", ["auto", "inkernel"])
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_prefill_wide_groups(group, variant, q_mode, mode):
+    """GQA ratios up to the largest the library accepts (128: one query token
+    per 128-row q tile), causal, ragged; every row against the oracle."""
+    hkv = 2 if group == 32 else 1
+    wl = W.Workload(f"wide_g{group}", [21, 5, 1], [40, 133, 1], group * hkv, hkv, seed=group)
+    inp = W.make_inputs(wl)
+    cache = G.gpu_cache(inp, fill=0x7F)
+    _check(inp, cache, G.oracle_pools(inp), variant, q_mode, mode=mode)
 
 
 def test_a4q_is_closer_to_its_own_reference():

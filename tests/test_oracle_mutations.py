@@ -89,3 +89,20 @@ def test_dropped_softmax_scale_is_caught(orc):
         return orc.attention_rows(q, pos, q_len, k, v, causal, 1.0)
 
     _fails(A.test_attention_vs_library, Mutant(orc, attention_rows=unscaled), 9, 33, False)
+
+
+def test_division_instead_of_reciprocal_is_caught(orc):
+    """Codes taken from fl32(x / fl32(g * s)) instead of x times the rounded
+    reciprocal: the hand-worked block with a non-power-of-two scale differs."""
+    def divided(x, g):
+        x = np.asarray(x, np.float32)
+        g = np.float32(g)
+        amax = np.float32(np.abs(x).max())
+        s_real = np.float32(amax / np.float32(np.float32(6.0) * g)) if amax > 0 else np.float32(0.0)
+        scale = orc.e4m3_encode(s_real)
+        d = np.float32(g * np.float32(orc.e4m3_value(scale)))
+        codes = [0] * 16 if d == 0 else [orc.e2m1_encode(np.float32(xi / d)) for xi in x]
+        packed = np.array([codes[2 * i] | (codes[2 * i + 1] << 4) for i in range(8)], np.uint8)
+        return packed, scale
+
+    _fails(C.test_hand_worked_blocks, Mutant(orc, quantize_block16=divided))
