@@ -5,9 +5,14 @@ A step is one pass of the path over the 16K-token causal prefill workload:
 append the 16,384 tokens' K and V (8 kv heads, shuffled slot order) into the
 NVFP4 cache, then run the A4Q paged prefill (32 q heads) over it.  The
 headline value is prefill TFLOP/s per step (4*D FLOPs per visible causal
-(query, key) pair per q head).  The same run also reports append GB/s, A4Q
-prefill alone, the dequant-ahead variant, and paged decode GB/s on the batch-32
-decode workload (kv_len ~ U[1K, 32K]).
+(query, key) pair per q head).  The same run also reports, each timed alone
+with L2 flushed: append GB/s, the A4Q prefill in both modes and the
+dequant-ahead variant at 16K, the other workloads of the benchmark matrix
+(4 x 128 queries over 2K keys; 8 x 16-query tails over 16,400 keys, in GB/s
+of cache read; 32,768 + 7,001 tokens, append and prefill), paged decode GB/s
+on the batch-32 decode workload (kv_len ~ U[1K, 32K]), the measured A4Q error
+against a BF16 query and against exact attention, and the CPU oracle's rate
+on the host cores with its parity against the kernel's output.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torch.distributed.run; every rank runs an independent
@@ -131,6 +136,32 @@ def prefill_flops_split(wl: W.Workload):
     return f / 2, f / 2
 
 
+def prefill_roof_s(wl: W.Workload, peaks, a4q: bool = True) -> float:
+    """Tensor-roofline time of one prefill: QK at the FP4 rate and PV at the
+    16-bit rate (A4Q), or both at the 16-bit rate (dequant-ahead)."""
+    f_qk, f_pv = prefill_flops_split(wl)
+    p16 = peaks["bf16_tflops"] * 1e12
+    return (f_qk / (p16 * FP4_OVER_BF16) + f_pv / p16) if a4q else (f_qk + f_pv) / p16
+
+
+def host_cores() -> int:
+    """Host cores this process may run on (its affinity mask)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+_INPUTS = {}
+
+
+def inputs_of(cfg: str) -> W.Inputs:
+    """Seeded inputs of a named workload, generated once per run."""
+    if cfg not in _INPUTS:
+        _INPUTS[cfg] = W.make_inputs(W.CONFIGS[cfg]())
+    return _INPUTS[cfg]
+
+
 # ---------------------------------------------------------------------------- our arm
 class Bench:
     def __init__(self, dev):
@@ -181,8 +212,8 @@ def time_graph(nk_bench, fn, steps, warmup=3):
         return None
 
 
-def setup_prefill(nk, dev, wl):
-    inp = W.make_inputs(wl)
+def setup_prefill(nk, dev, inp):
+    wl = inp.wl
     order = W.shuffled_append_order(inp.wl.total_kv)
     k = inp.k[order].contiguous().to(dev)
     v = inp.v[order].contiguous().to(dev)
@@ -204,9 +235,9 @@ def run_ours(args, rank, world, dev):
     nk_bench = Bench(dev)
     nk = nk_bench.nk
     peaks = measured_peaks()
-    wl = W.CONFIGS[args.config]()
-    P = setup_prefill(nk, dev, wl)
-    inp = P["inp"]
+    inp = inputs_of(args.config)
+    wl = inp.wl
+    P = setup_prefill(nk, dev, inp)
 
     def append():
         nk.nvfp4_kv_append(P["k"], P["v"], P["slots"], P["cache"])
@@ -271,6 +302,9 @@ def run_ours(args, rank, world, dev):
     ms = max_over_ranks(statistics.mean(step_ms), world, dev)
     value = whole_job_tflops(flops, world, ms)
 
+    # the A4Q output of the last timed step, for the oracle's parity check
+    a4q_out = P["out"].float().cpu() if rank == 0 and not args.no_cpu_baseline else None
+
     # ---- components (each timed alone, L2 flushed before every call)
     K = max(min(args.steps, 50), 5)
     app = nk_bench.time_fn(append, K, 3)
@@ -280,15 +314,24 @@ def run_ours(args, rank, world, dev):
     pre_ik = nk_bench.time_fn(lambda: prefill(nk.VARIANT_A4Q, "ws_min"), K, 3)
     dqa_ik = nk_bench.time_fn(lambda: prefill(nk.VARIANT_DQ_AHEAD, "ws_min"), K, 3)
     app_bytes = APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads
-    dec = decode_component(nk, nk_bench, dev, K)
+    comps = {
+        "append": gbs_entry(app, app_bytes, peaks, app_g),
+        "prefill_a4q": tflops_entry(pre, wl, peaks, True, "V repacked once per KV tile"),
+        "prefill_a4q_inkernel": tflops_entry(pre_ik, wl, peaks, True, "V dequantized in the kernel"),
+        "prefill_dq_ahead": tflops_entry(dqa, wl, peaks, False, "K and V repacked once per KV tile"),
+        "prefill_dq_ahead_inkernel": tflops_entry(dqa_ik, wl, peaks, False, "K and V dequantized in the kernel"),
+    }
+    if not args.no_matrix:
+        comps["shortq"] = shortq_component(nk, nk_bench, dev, K, peaks)
+        comps["tails"] = tails_component(nk, nk_bench, dev, K, peaks)
+        comps["prefill32k"] = long_component(nk, nk_bench, dev, K, peaks)
+    comps["decode"] = decode_component(nk, nk_bench, dev, K)
     clk = clocks.stop()
 
-    pre_avg = statistics.mean(pre)
     # the dominant kernel: the attention launch, timed inside the timed steps
     achieved = flops / (statistics.mean(attn_ms) * 1e-3) / 1e12
     p16 = peaks["bf16_tflops"]
-    t_roof = f_qk / (p16 * FP4_OVER_BF16 * 1e12) + f_pv / (p16 * 1e12)
-    peak_eff = flops / t_roof / 1e12
+    peak_eff = flops / prefill_roof_s(wl, peaks) / 1e12
 
     # ---- end to end through the public API with host buffers
     e2e = e2e_measure(nk, nk_bench, dev, P, wl, args) if not args.no_e2e else None
@@ -306,36 +349,114 @@ def run_ours(args, rank, world, dev):
                      "traffic": prefill_traffic_bytes(),
                      "peak_basis": f"t = F_QK/(bf16 x {FP4_OVER_BF16:g}) + F_PV/bf16 with bf16 = {p16} TFLOP/s "
                                    f"({peaks['source']} burst)"},
-        "components": {
-            "append": {"ms": round(statistics.mean(app), 4),
-                       "GB/s": round(app_bytes / (statistics.mean(app) * 1e-3) / 1e9, 1),
-                       "frac_of_hbm": round(app_bytes / (statistics.mean(app) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                       "graph_ms": round(statistics.mean(app_g), 4) if app_g else None,
-                       "graph_GB/s": round(app_bytes / (statistics.mean(app_g) * 1e-3) / 1e9, 1) if app_g else None,
-                       "graph_frac_of_hbm": round(app_bytes / (statistics.mean(app_g) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
-                       if app_g else None,
-                       "bytes": app_bytes},
-            "prefill_a4q": {"ms": round(pre_avg, 4), "TFLOP/s": round(flops / (pre_avg * 1e-3) / 1e12, 2),
-                            "mode": "V repacked once per KV tile"},
-            "prefill_a4q_inkernel": {"ms": round(statistics.mean(pre_ik), 4),
-                                     "TFLOP/s": round(flops / (statistics.mean(pre_ik) * 1e-3) / 1e12, 2),
-                                     "mode": "V dequantized in the kernel"},
-            "prefill_dq_ahead": {"ms": round(statistics.mean(dqa), 4),
-                                 "TFLOP/s": round(flops / (statistics.mean(dqa) * 1e-3) / 1e12, 2),
-                                 "frac_of_bf16": round(flops / (statistics.mean(dqa) * 1e-3) / 1e12 / p16, 4),
-                                 "mode": "K and V repacked once per KV tile"},
-            "prefill_dq_ahead_inkernel": {"ms": round(statistics.mean(dqa_ik), 4),
-                                          "TFLOP/s": round(flops / (statistics.mean(dqa_ik) * 1e-3) / 1e12, 2)},
-            "decode": dec,
-        },
+        "components": comps,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,  # append, schedule, repack pre-pass, attention
         "clocks": clk,
         "wall_s_timed_loop": round(t_wall, 3),
     }
+    if not args.no_accuracy:
+        result["a4q_error"] = a4q_error_report(nk, dev)
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds, a4q_out)
     return result
+
+
+def gbs_entry(times, nbytes, peaks, graph_times=None):
+    """Component entry of an HBM-bound call: mean time, algorithmic GB/s and
+    the fraction of the measured copy bandwidth (and the same replayed from a
+    CUDA graph, when given)."""
+    t = statistics.mean(times)
+    gbs = nbytes / (t * 1e-3) / 1e9
+    e = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "bytes": nbytes}
+    if graph_times:
+        tg = statistics.mean(graph_times)
+        g = nbytes / (tg * 1e-3) / 1e9
+        e.update({"graph_ms": round(tg, 4), "graph_GB/s": round(g, 1), "graph_frac_of_hbm": round(g / peaks["hbm_gbs"], 4)})
+    return e
+
+
+def tflops_entry(times, wl, peaks, a4q, mode):
+    """Component entry of a prefill: mean time, TFLOP/s and the fraction of
+    its tensor roofline (mixed FP4/16-bit for A4Q, 16-bit for dequant-ahead)."""
+    t = statistics.mean(times)
+    return {"workload": wl.name, "ms": round(t, 4), "TFLOP/s": round(wl.flops() / (t * 1e-3) / 1e12, 2),
+            "frac_of_roofline": round(prefill_roof_s(wl, peaks, a4q) / (t * 1e-3), 4),
+            "roofline": "FP4 QK + 16-bit PV" if a4q else "16-bit QK + PV", "mode": mode}
+
+
+class PrefillCase:
+    """A workload's cache (built by the library's append) and its prefill
+    buffers, for the component timings."""
+
+    def __init__(self, nk, dev, inp, shuffled_append=False):
+        self.nk, self.inp = nk, inp
+        wl = inp.wl
+        order = W.shuffled_append_order(wl.total_kv) if shuffled_append else torch.arange(wl.total_kv)
+        self.k = inp.k[order].contiguous().to(dev)
+        self.v = inp.v[order].contiguous().to(dev)
+        self.slots = inp.slot_mapping[order].contiguous().to(dev)
+        self.cache = nk.Cache(inp.num_pages, wl.num_kv_heads, inp.k_global, inp.v_global, device=dev)
+        self.append()
+        self.q = inp.q.to(dev)
+        self.pt, self.kvl, self.qo = inp.page_table.to(dev), inp.kv_lens.to(dev), inp.qo_indptr.to(dev)
+        self.out = torch.empty_like(self.q)
+        self.ws = torch.empty(nk.nvfp4_workspace_bytes(nk.OP_PREFILL, wl.batch, wl.num_q_heads, wl.num_kv_heads,
+                                                       wl.total_q, self.pt.shape[1] * 16),
+                              dtype=torch.uint8, device=dev)
+
+    def append(self):
+        self.nk.nvfp4_kv_append(self.k, self.v, self.slots, self.cache)
+
+    def prefill(self, variant):
+        wl = self.inp.wl
+        self.nk.nvfp4_paged_prefill(self.q, self.cache, self.pt, self.kvl, self.qo, causal=wl.causal,
+                                    sm_scale=self.inp.sm_scale, variant=variant, out=self.out, workspace=self.ws)
+
+
+def shortq_component(nk, nk_bench, dev, K, peaks):
+    """Batch 4 x q 128 at the end of kv 2,048, 32/8 heads, permuted pages (the
+    repack comparison shape): both variants, repack mode (four q tiles per kv
+    head)."""
+    c = PrefillCase(nk, dev, inputs_of("shortq"))
+    wl = c.inp.wl
+    a = nk_bench.time_fn(lambda: c.prefill(nk.VARIANT_A4Q), K, 3)
+    d = nk_bench.time_fn(lambda: c.prefill(nk.VARIANT_DQ_AHEAD), K, 3)
+    return {"a4q": tflops_entry(a, wl, peaks, True, "repack"),
+            "dq_ahead": tflops_entry(d, wl, peaks, False, "repack")}
+
+
+def tails_component(nk, nk_bench, dev, K, peaks):
+    """Chunked-prefill tails: 8 requests x 16 new queries over 16,400 cached
+    tokens, 32/8 heads.  One q tile per (request, kv head), so the in-kernel
+    mode runs; bound by reading the cache: GB/s of cache bytes read."""
+    c = PrefillCase(nk, dev, inputs_of("tails"))
+    wl = c.inp.wl
+    kv_bytes = CACHE_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads
+    res = {}
+    for name, variant in (("a4q", nk.VARIANT_A4Q), ("dq_ahead", nk.VARIANT_DQ_AHEAD)):
+        t = nk_bench.time_fn(lambda: c.prefill(variant), K, 3)
+        e = gbs_entry(t, kv_bytes, peaks)
+        e["TFLOP/s"] = round(wl.flops() / (statistics.mean(t) * 1e-3) / 1e12, 2)
+        e["mode"] = "in-kernel (one q tile per request and kv head)"
+        res[name] = e
+    res["workload"] = wl.name
+    return res
+
+
+def long_component(nk, nk_bench, dev, K, peaks):
+    """32,768 + 7,001 tokens in one batch, 64/8 heads: the append of all
+    39,769 tokens (GB/s) and the A4Q prefill (TFLOP/s, repack mode)."""
+    c = PrefillCase(nk, dev, inputs_of("prefill32k"), shuffled_append=True)
+    wl = c.inp.wl
+    app = nk_bench.time_fn(c.append, K, 3)
+    pre = nk_bench.time_fn(lambda: c.prefill(nk.VARIANT_A4Q), max(3, K // 4), 2)
+    res = {"workload": wl.name,
+           "append": gbs_entry(app, APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads, peaks),
+           "prefill_a4q": tflops_entry(pre, wl, peaks, True, "repack")}
+    del c
+    torch.cuda.empty_cache()
+    return res
 
 
 def decode_component(nk, nk_bench, dev, K):
@@ -353,16 +474,9 @@ def decode_component(nk, nk_bench, dev, K):
 
     t = nk_bench.time_fn(dec, K, 3)
     tg = time_graph(nk_bench, dec, K)
-    peaks = measured_peaks()
-    bytes_ = CACHE_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads
-    gbs = bytes_ / (statistics.mean(t) * 1e-3) / 1e9
-    out = {"workload": wl.name, "ms": round(statistics.mean(t), 4), "GB/s": round(gbs, 1),
-           "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "bytes": bytes_}
-    if tg:
-        g = bytes_ / (statistics.mean(tg) * 1e-3) / 1e9
-        out.update({"graph_ms": round(statistics.mean(tg), 4), "graph_GB/s": round(g, 1),
-                    "graph_frac_of_hbm": round(g / peaks["hbm_gbs"], 4)})
-    return out
+    e = gbs_entry(t, CACHE_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads, measured_peaks(), tg)
+    e["workload"] = wl.name
+    return e
 
 
 def e2e_measure(nk, nk_bench, dev, P, wl, args):
@@ -444,6 +558,134 @@ def bench_config(wl, world):
             "parallelism": f"replicas x{world}"}
 
 
+# ---------------------------------------------------------------------------- A4Q accuracy
+# Measured accuracy of the A4Q query ("NVFP4 KV cache A4Q prefill explained",
+# section "Make query accuracy a release gate": lengths, head shapes, causal
+# masks and scale outliers are checked, the query scale scheme -- single or
+# dual level -- is a recorded choice, and long contexts amplify score error).
+# Every output compared comes from the library's kernels:
+#   o_a4q    A4Q prefill (query quantized to NVFP4 inside the kernel),
+#   o_bf16q  dequant-ahead prefill (BF16 query) on the same NVFP4 cache,
+# and o_exact is softmax attention in float64 (plain torch on the host) over
+# the UNQUANTIZED bf16 Q, K and V.  So o_a4q - o_bf16q is what the query
+# quantization adds, o_bf16q - o_exact is the NVFP4 cache alone, and
+# o_a4q - o_exact the whole A4Q path.
+Q_SCHEMES = {
+    "per_row": "dual level per (token, head) row: g_row = amax_row/2688 (q_global_scale 0, the default)",
+    "per_tensor": "dual level per tensor: one g = amax(Q)/2688 for every row",
+    "single_level": "single level: g = 1, the E4M3 block scales alone",
+}
+
+
+def q_scale_for(scheme: str, q: torch.Tensor) -> float:
+    """The q_global_scale argument that selects `scheme` for query tensor q."""
+    if scheme == "per_row":
+        return 0.0
+    if scheme == "single_level":
+        return 1.0
+    amax = np.float32(q.float().abs().max().item())
+    return float(np.float32(amax / np.float32(2688.0)))
+
+
+def exact_rows(inp: W.Inputs, rows):
+    """float64 softmax attention over the unquantized bf16 values for the
+    given (request, position) rows: {(b, i): [Hq, D] numpy}."""
+    wl = inp.wl
+    G = wl.group
+    out = {}
+    by_req = {}
+    for b, i in rows:
+        by_req.setdefault(b, set()).add(i)
+    for b, positions in by_req.items():
+        pos = torch.tensor(sorted(positions), dtype=torch.int64)
+        q_len, kv_len = wl.q_lens[b], wl.kv_lens[b]
+        k0 = int(inp.kv_indptr[b])
+        qrows = inp.q[int(inp.qo_indptr[b]) + pos].to(torch.float64)          # [n, Hq, D]
+        k = inp.k[k0:k0 + kv_len].to(torch.float64)                             # [kv, Hkv, D]
+        v = inp.v[k0:k0 + kv_len].to(torch.float64)
+        last = (kv_len - q_len + pos) if wl.causal else torch.full_like(pos, kv_len - 1)
+        mask = torch.arange(kv_len)[None, :] > last[:, None]                   # [n, kv]
+        o = torch.empty(len(pos), wl.num_q_heads, wl.head_dim, dtype=torch.float64)
+        for h in range(wl.num_kv_heads):
+            s = torch.einsum("ngd,kd->ngk", qrows[:, h * G:(h + 1) * G, :], k[:, h, :]) * inp.sm_scale
+            p = torch.softmax(s.masked_fill(mask[:, None, :], -math.inf), dim=-1)
+            o[:, h * G:(h + 1) * G, :] = torch.einsum("ngk,kd->ngd", p, v[:, h, :])
+        for r, i in enumerate(pos.tolist()):
+            out[(b, i)] = o[r].numpy()
+    return out
+
+
+def err_stats(got: dict, ref: dict):
+    """max-abs and relative Frobenius of got - ref over the rows of ref."""
+    d = np.stack([got[k] - ref[k] for k in ref])
+    r = np.stack([ref[k] for k in ref])
+    return {"max_abs": round(float(np.abs(d).max()), 6),
+            "rel_fro": round(float(np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30)), 6)}
+
+
+def kernel_rows(out: torch.Tensor, inp: W.Inputs, rows):
+    o = out.float().cpu().numpy().astype(np.float64)
+    return {(b, i): o[int(inp.qo_indptr[b]) + i] for b, i in rows}
+
+
+def accuracy_run(nk, dev, inp, rows, schemes=("per_row",)):
+    """Kernel outputs on `rows` of one workload: the BF16-query dequant-ahead
+    prefill and the A4Q prefill under each query scale scheme."""
+    c = PrefillCase(nk, dev, inp)
+    res = {}
+    c.prefill(nk.VARIANT_DQ_AHEAD)
+    res["bf16q"] = kernel_rows(c.out, inp, rows)
+    for sch in schemes:
+        wl = inp.wl
+        nk.nvfp4_paged_prefill(c.q, c.cache, c.pt, c.kvl, c.qo, causal=wl.causal, sm_scale=inp.sm_scale,
+                               variant=nk.VARIANT_A4Q, out=c.out, workspace=c.ws,
+                               q_global_scale=q_scale_for(sch, inp.q))
+        res[sch] = kernel_rows(c.out, inp, rows)
+    torch.cuda.synchronize(dev)
+    st = nk.nvfp4kv_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the accuracy run")
+    del c
+    torch.cuda.empty_cache()
+    return res
+
+
+def a4q_error_report(nk, dev):
+    """The a4q_error object of the benchmark line: the A4Q error on sampled
+    rows of the outlier config (every row), the 16K and the 32K + 7K configs,
+    then the query scale schemes x context length."""
+    per = {}
+    for cfg, rows_of in (("tiny", lambda wl: [(b, i) for b in range(wl.batch) for i in range(wl.q_lens[b])]),
+                         ("prefill16k", lambda wl: W.sample_rows(wl, 6)),
+                         ("prefill32k", lambda wl: W.sample_rows(wl, 3))):
+        inp = inputs_of(cfg)
+        rows = rows_of(inp.wl)
+        k = accuracy_run(nk, dev, inp, rows)
+        ex = exact_rows(inp, rows)
+        per[cfg] = {"workload": inp.wl.name, "values": inp.wl.dist, "rows": len(rows),
+                    "a4q_vs_bf16q": err_stats(k["per_row"], k["bf16q"]),
+                    "a4q_vs_exact": err_stats(k["per_row"], ex), "bf16q_vs_exact": err_stats(k["bf16q"], ex)}
+    sweep = {}
+    for L in (1024, 4096, 16384, 32768):
+        wl = W.Workload(f"tail_q64_kv{L}_h32x8_outliers", [64], [L], 32, 8, dist="outliers", seed=L)
+        inp = W.make_inputs(wl)
+        rows = W.sample_rows(wl, 6)
+        k = accuracy_run(nk, dev, inp, rows, tuple(Q_SCHEMES))
+        ex = exact_rows(inp, rows)
+        e = {"rows": len(rows), "bf16q_vs_exact": err_stats(k["bf16q"], ex)}
+        for sch in Q_SCHEMES:
+            e[sch] = {"vs_exact": err_stats(k[sch], ex), "vs_bf16q": err_stats(k[sch], k["bf16q"])}
+        sweep[str(L)] = e
+    return {"q_scheme": Q_SCHEMES["per_row"] + "; then one E4M3 scale per 16 values (nearest even) and E2M1 "
+                                               "codes (nearest even), the cache's block codec",
+            "outputs": "o_a4q: A4Q kernel; o_bf16q: dequant-ahead kernel (BF16 query) on the same NVFP4 cache; "
+                       "o_exact: float64 attention on the unquantized bf16 Q, K, V",
+            "configs": per,
+            "q_scheme_x_kv_len": {"workload": "64-query tail at the end of kv_len keys, 32/8 heads, N(0,1) with "
+                                              "2% of the channels x8; seeded rows",
+                                  "schemes": Q_SCHEMES, "by_kv_len": sweep}}
+
+
 # ---------------------------------------------------------------------------- oracle arm
 _ORACLE = {}
 
@@ -464,80 +706,124 @@ def oracle_setup():
     kd = oracle.gather_decode(pools, "k", inp.page_table[0].numpy(), wl.kv_lens[0], 0, inp.k_global)
     vd = oracle.gather_decode(pools, "v", inp.page_table[0].numpy(), wl.kv_lens[0], 0, inp.v_global)
     _ORACLE.update(dict(wl=wl, inp=inp, kd=kd, vd=vd, q=inp.q.float().numpy(), append_s=t_app,
-                        append_gbs=APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads / t_app / 1e9,
-                        rng=np.random.default_rng(0)))
+                        append_gbs=APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads / t_app / 1e9))
     return _ORACLE
 
 
-def oracle_rows(seconds: float):
+def oracle_rows(seconds: float, workers: int, collect: bool = False):
     """The oracle as it stands: A4Q attention for seeded query rows of the
-    four q heads of kv head 0 until `seconds` have passed.  Returns
-    (TFLOP/s, rows, seconds)."""
+    four q heads of kv head 0 of the 16K workload, on `workers` host threads
+    (each runs independent rows; the C oracle releases the interpreter lock),
+    until `seconds` have passed.  Returns (TFLOP/s, rows, seconds, results)
+    with results a list of (positions, q head, o) when `collect`."""
+    import concurrent.futures as cf
+
     import oracle
     o = oracle_setup()
     wl, inp = o["wl"], o["inp"]
-    flops, rows = 0.0, 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds:
-        pos = np.sort(o["rng"].integers(0, wl.q_lens[0], 8)).astype(np.int32)
-        for gq in range(wl.group):
-            qd = oracle.decode_q_a4q(o["q"][pos, gq, :])
-            oracle.attention_rows(qd, pos, wl.q_lens[0], o["kd"], o["vd"], True, inp.sm_scale)
-            flops += float(np.sum(4.0 * 128 * (pos.astype(np.float64) + 1)))
-            rows += len(pos)
+
+    def worker(idx):
+        rng = np.random.default_rng(1000 + idx)
+        flops, rows, res = 0.0, 0, []
+        while time.perf_counter() - t0 < seconds:
+            pos = np.sort(rng.integers(0, wl.q_lens[0], 8)).astype(np.int32)
+            for gq in range(wl.group):
+                qd = oracle.decode_q_a4q(o["q"][pos, gq, :])
+                out, _ = oracle.attention_rows(qd, pos, wl.q_lens[0], o["kd"], o["vd"], True, inp.sm_scale)
+                flops += float(np.sum(4.0 * 128 * (pos.astype(np.float64) + 1)))
+                rows += len(pos)
+                if collect:
+                    res.append((pos, gq, out))
+        return flops, rows, res
+
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        parts = list(ex.map(worker, range(workers)))
     dt = time.perf_counter() - t0
-    return flops / dt / 1e12, rows, dt
+    flops = sum(p[0] for p in parts)
+    rows = sum(p[1] for p in parts)
+    return flops / dt / 1e12, rows, dt, [r for p in parts for r in p[2]]
 
 
-def cpu_baseline(seconds):
-    v, rows, dt = oracle_rows(seconds)
+def half_bf16_ulp(x):
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
+
+
+def cpu_baseline(seconds, gpu_out=None):
+    """The oracle timed on the host's cores; when the kernel's output of the
+    same workload is given, the oracle rows are also compared with it (raw
+    max-abs, max-abs beyond the half bf16 ulp of the stored output, relative
+    Frobenius)."""
+    cores = host_cores()
+    v, rows, dt, res = oracle_rows(seconds, cores, collect=gpu_out is not None)
     o = oracle_setup()
-    return {"value": round(v, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} causal A4Q query rows of the 16K workload (q heads 0-3) in {dt:.1f} s; "
-                      f"oracle append of all 16,384 tokens x 8 heads took {o['append_s']:.1f} s "
-                      f"({o['append_gbs']:.3f} GB/s)"}
+    out = {"value": round(v, 9), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+           "sample": f"{rows} causal A4Q query rows of the 16K workload (q heads 0-3) in {dt:.1f} s on "
+                     f"{cores} threads; oracle append of all 16,384 tokens x 8 heads took {o['append_s']:.1f} s "
+                     f"({o['append_gbs']:.3f} GB/s)"}
+    if gpu_out is not None and res:
+        g = gpu_out.numpy().astype(np.float64)
+        d, r = [], []
+        for pos, gq, ref in res:
+            d.append(g[pos, gq, :] - ref)
+            r.append(ref)
+        d, r = np.concatenate(d), np.concatenate(r)
+        out["parity_vs_kernel"] = {
+            "rows": int(d.shape[0]), "kernel": "nvfp4_prefill_a4q_2cta_sm103_kernel (last timed step)",
+            "max_abs_raw": round(float(np.abs(d).max()), 6),
+            "max_abs_beyond_half_bf16_ulp": round(float(np.maximum(np.abs(d) - half_bf16_ulp(r), 0).max()), 6),
+            "rel_fro": round(float(np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30)), 7),
+            "tolerance": {"max_abs": 2e-2, "rel_fro": 1e-2}}
+    return out
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
+    cores = host_cores()
     per_step = min(args.cpu_seconds, 150.0 / (args.steps + args.warmup))
     oracle_setup()
     vals, times = [], []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        v, rows, dt = oracle_rows(per_step)
+        v, rows, dt, _ = oracle_rows(per_step, cores)
         if i >= args.warmup:
             vals.append(v)
             times.append(time.perf_counter() - t0)
     value = statistics.mean(vals)
     o = oracle_setup()
-    desc = (f"each step: causal A4Q query rows of the 16K workload for {per_step:.1f} s on one core; "
+    desc = (f"each step: causal A4Q query rows of the 16K workload for {per_step:.1f} s on {cores} threads; "
             f"oracle append of the full cache took {o['append_s']:.1f} s")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(times) * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": dict(bench_config(W.full_prefill_16k(), world), sample="bounded CPU sample per step"),
-            "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 # ---------------------------------------------------------------------------- ncu traffic
 # DRAM read + write of one attention launch (nvfp4_prefill_a4q_2cta_sm103_kernel,
-# 16K causal, 32/8 heads) from the ncu capture summarised in
-# profiles/prefill_a4q_16k_ncu.md, keyed by the digest of the kernel source it
-# was taken on: once that source changes the figure no longer describes the
-# kernel and is reported as null.
-PREFILL_TRAFFIC = {"source": "prefill_a4q.cu", "sha256_16": "9d235b9533aab863", "bytes": 184646400 + 95481344}
+# 16K causal, 32/8 heads) from one ncu capture, keyed by a digest of the
+# kernel's sources as captured: once they change the figure no longer
+# describes the kernel and is reported as null.
+PREFILL_TRAFFIC = {"sources": ["prefill_a4q.cu", "prefill_common.cuh", "kernels.cuh", "codec.cuh", "ptx.cuh"],
+                   "sha256_16": None, "bytes": None}
+
+
+def prefill_sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in PREFILL_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, "nvfp4_paged_kv_append_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def prefill_traffic_bytes():
-    import hashlib
-    src = os.path.join(ROOT, "nvfp4_paged_kv_append_gb300", "csrc", PREFILL_TRAFFIC["source"])
-    with open(src, "rb") as f:
-        dig = hashlib.sha256(f.read()).hexdigest()[:16]
-    return PREFILL_TRAFFIC["bytes"] if dig == PREFILL_TRAFFIC["sha256_16"] else None
+    return PREFILL_TRAFFIC["bytes"] if prefill_sources_digest() == PREFILL_TRAFFIC["sha256_16"] else None
 
 
 # ---------------------------------------------------------------------------- ranks
@@ -568,6 +854,8 @@ def main():
     ap.add_argument("--config", default="prefill16k", choices=sorted(W.CONFIGS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-accuracy", action="store_true", help="skip the A4Q accuracy report")
+    ap.add_argument("--no-matrix", action="store_true", help="skip the other workloads' component timings")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

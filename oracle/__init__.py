@@ -15,9 +15,14 @@ Parity status per function:
   e2m1/e4m3 codec, block quantizer, append, gather/decode, attention,
   cache_bytes -- pinned by tests/test_oracle_*.py (format definitions, a
   library cast, brute force, closed forms, the pages' worked byte counts).
-  quantize_rows(mode=PER_ROW), the A4Q Q scheme -- the pages leave the scheme
-  open, so it is pinned only to its stated reading (round trip and error
-  bound), not to any external value: parity unpinned against the pages.
+  dense_attention (attention on the unquantized values, the reference of the
+  accuracy report) -- pinned against scipy softmax on a ragged batch.
+  decode_q_a4q with a single caller-given scale (per-tensor or single-level
+  query scheme) -- the GLOBAL mode of the cache's block codec, pinned by the
+  codec pins and an exact round trip.
+  quantize_rows(mode=PER_ROW), the per-row A4Q Q scheme -- the pages leave
+  the scheme open, so it is pinned only to its stated reading (round trip and
+  error bound), not to any external value: parity unpinned against the pages.
 """
 from __future__ import annotations
 
@@ -242,21 +247,28 @@ def cache_bytes(num_pages: int, page_size: int, Hkv: int, D: int) -> int:
     return int(_load().orc_cache_bytes(num_pages, page_size, Hkv, D))
 
 
-def decode_q_a4q(q_rows) -> np.ndarray:
-    """A4Q query as the kernel sees it: per-row dual-level quantization then
-    decode (R6, R5).  q_rows: [n, D] float32 -> [n, D] float64."""
+def decode_q_a4q(q_rows, q_scale: float = 0.0) -> np.ndarray:
+    """A4Q query as the kernel sees it, quantized then decoded (R6, R5).
+    q_scale 0: per-row dual-level scale (R6); q_scale > 0: that one scale for
+    every row (the GLOBAL mode of the same block codec -- a per-tensor scale,
+    or 1 for a single-level scheme).  q_rows: [n, D] float32 -> [n, D]
+    float64."""
+    if q_scale > 0:
+        packed, scales, _ = quantize_rows(q_rows, GLOBAL, q_scale)
+        return dequantize_rows(packed, scales, g=q_scale)
     packed, scales, row_g = quantize_rows(q_rows, PER_ROW)
     return dequantize_rows(packed, scales, row_g=row_g)
 
 
 def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_g: float,
                     v_g: float, causal: bool, sm_scale: float, q_mode: str = "bf16",
-                    rows=None):
+                    rows=None, q_scale: float = 0.0):
     """Attention of a ragged batch over the paged cache.
 
     q: [total_q, Hq, D] float32 (bf16 values); q_mode "bf16" uses q as is,
-    "a4q" uses the per-row quantized-then-decoded query.  rows: optional list of
-    (request, position) pairs to evaluate (all rows of every request if None).
+    "a4q" uses the quantized-then-decoded query (per-row scale, or the single
+    scale q_scale when it is > 0).  rows: optional list of (request, position)
+    pairs to evaluate (all rows of every request if None).
     Returns dict {(request, position): (o [Hq, D], lse [Hq])}.
     """
     q = _f32(q)
@@ -295,7 +307,7 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
             for gq in range(G):
                 hq = h * G + gq
                 qr = q[qo[b] + pos, hq, :]
-                qd = decode_q_a4q(qr) if q_mode == "a4q" else qr.astype(np.float64)
+                qd = decode_q_a4q(qr, q_scale) if q_mode == "a4q" else qr.astype(np.float64)
                 res.append((hq,) + attention_rows(qd, pos, q_len, kd, vd, causal, sm_scale))
             return pos, res
 
@@ -307,4 +319,46 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
                     result[(b, int(i))][0][hq] = o[r]
                     result[(b, int(i))][1][hq] = lse[r]
         del dec
+    return result
+
+
+def dense_attention(q, qo_indptr, k, v, kv_indptr, Hq: int, causal: bool, sm_scale: float, rows):
+    """Attention of the given (request, position) rows on the UNQUANTIZED
+    values: q [total_q, Hq, D], k and v [total_kv, Hkv, D] float32 (bf16
+    values), request b's keys are rows kv_indptr[b] .. kv_indptr[b+1]-1.  No
+    cache codec is involved: this is the fp64 reference the quantization error
+    is measured against.  Returns {(request, position): (o [Hq, D], lse [Hq])}."""
+    q = _f32(q)
+    k = _f32(k)
+    v = _f32(v)
+    qo = np.asarray(qo_indptr, dtype=np.int64)
+    kvi = np.asarray(kv_indptr, dtype=np.int64)
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    want = {}
+    for b, i in rows:
+        want.setdefault(int(b), set()).add(int(i))
+    result = {}
+    for b, positions in want.items():
+        pos_all = np.array(sorted(positions), np.int32)
+        q_len = int(qo[b + 1] - qo[b])
+        k0, k1 = int(kvi[b]), int(kvi[b + 1])
+
+        def one(h):
+            kd = np.ascontiguousarray(k[k0:k1, h, :], dtype=np.float64)
+            vd = np.ascontiguousarray(v[k0:k1, h, :], dtype=np.float64)
+            res = []
+            for gq in range(G):
+                hq = h * G + gq
+                qr = q[qo[b] + pos_all, hq, :].astype(np.float64)
+                res.append((hq,) + attention_rows(qr, pos_all, q_len, kd, vd, causal, sm_scale))
+            return res
+
+        for i in pos_all:
+            result[(b, int(i))] = (np.zeros((Hq, k.shape[2])), np.zeros(Hq))
+        for res in _pmap(one, range(Hkv)):
+            for hq, o, lse in res:
+                for r, i in enumerate(pos_all):
+                    result[(b, int(i))][0][hq] = o[r]
+                    result[(b, int(i))][1][hq] = lse[r]
     return result

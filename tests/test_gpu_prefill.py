@@ -213,3 +213,33 @@ def test_prefill_zero_query_rows_repack_mode(variant, q_mode):
     rows = [(0, i) for i in range(128)] + [(1, 64), (3, 127), (2, 0), (2, 127)]
     got, _ = _check(inp, cache, G.pools_for("shortq"), variant, q_mode, rows=rows, mode="auto")
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("mode", ["auto", "inkernel"])
+@pytest.mark.parametrize("scheme", ["per_tensor", "single_level"])
+@pytest.mark.parametrize("cfg", ["tiny", "shortq"])
+def test_prefill_query_scale_schemes(cfg, scheme, mode):
+    """The A4Q query with one scale for every row (q_global_scale > 0): a
+    per-tensor dual-level scale fl32(amax(Q)/2688), or 1 (single level), in
+    both kernel modes, against the oracle's query coded with the same scale
+    ("NVFP4 KV cache A4Q prefill explained", section "Make query accuracy a
+    release gate": the scheme is a recorded choice)."""
+    b = G.nk()
+    inp = G.inputs(cfg)
+    qf = inp.q.float().numpy()
+    g = float(np.float32(np.float32(np.abs(qf).max()) / np.float32(2688.0))) if scheme == "per_tensor" else 1.0
+    cache = G.gpu_cache(inp)
+    d = G.dev()
+    lse = torch.empty(inp.wl.total_q, inp.wl.num_q_heads, device=d)
+    o = b.nvfp4_paged_prefill(inp.q.to(d), cache, inp.page_table.to(d), inp.kv_lens.to(d), inp.qo_indptr.to(d),
+                              sm_scale=inp.sm_scale, variant=0, lse=lse, workspace=G.prefill_workspace(inp, mode),
+                              q_global_scale=g)
+    torch.cuda.synchronize()
+    assert b.nvfp4kv_get_device_status() == 0
+    rows = None if cfg == "tiny" else W.tile_rows(inp.wl)
+    ref = G.oracle.paged_attention(G.pools_for(cfg), qf, inp.qo_indptr, inp.kv_lens, inp.page_table,
+                                   inp.wl.num_q_heads, inp.k_global, inp.v_global, True, inp.sm_scale,
+                                   q_mode="a4q", rows=rows, q_scale=g)
+    mx, fro, n = G.compare_rows(o.float().cpu().numpy(), ref, inp.qo_indptr)
+    assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro, n)
+    assert G.compare_lse(lse.cpu().numpy(), ref, inp.qo_indptr) <= 2e-3

@@ -129,3 +129,26 @@ def test_a4q_error_grows_with_outliers(orc):
         errs[dist] = diff / scale
         assert diff > 0
     assert errs["outliers"] > errs["normal"]
+
+
+def test_dense_attention_ragged_batch_vs_library(orc):
+    """The unquantized reference used for the accuracy report: a ragged batch
+    with grouped heads, every row against scipy softmax on the raw values."""
+    rng = np.random.default_rng(31)
+    q_lens, kv_lens, Hq, Hkv, D = [3, 5], [9, 5], 4, 2, 16
+    q = rng.standard_normal((sum(q_lens), Hq, D)).astype(np.float32)
+    k = rng.standard_normal((sum(kv_lens), Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((sum(kv_lens), Hkv, D)).astype(np.float32)
+    qo = np.array([0, 3, 8])
+    kvi = np.array([0, 9, 14])
+    rows = [(b, i) for b in range(2) for i in range(q_lens[b])]
+    got = orc.dense_attention(q, qo, k, v, kvi, Hq, True, 0.25, rows)
+    for b, i in rows:
+        for hq in range(Hq):
+            h = hq // (Hq // Hkv)
+            kb = k[kvi[b]:kvi[b + 1], h].astype(np.float64)
+            vb = v[kvi[b]:kvi[b + 1], h].astype(np.float64)
+            o_ref, lse_ref = lib_attention(q[qo[b] + i, hq][None].astype(np.float64), kb, vb, [i], q_lens[b],
+                                           True, 0.25)
+            np.testing.assert_allclose(got[(b, i)][0][hq], o_ref[0], rtol=1e-12, atol=1e-12)
+            assert abs(got[(b, i)][1][hq] - lse_ref[0]) < 1e-12

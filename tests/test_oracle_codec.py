@@ -145,3 +145,26 @@ def test_append_layout_and_skip(orc):
     assert not flat[~written].any()
     with pytest.raises(ValueError):
         orc.kv_append(pools, k[:1], v[:1], np.array([6 * 16], np.int64), kg, vg)
+
+
+@pytest.mark.parametrize("q_scale", [1.0, 0.375])
+def test_single_scale_query_round_trip(orc, q_scale):
+    """The A4Q query with one caller-given scale for every row (per-tensor or
+    single-level scheme): values that are exactly code x E4M3 scale x q_scale,
+    with one |code| = 6 per 16-value block, come back unchanged."""
+    rng = np.random.default_rng(int(q_scale * 64))
+    rows = []
+    for _ in range(12):
+        row = []
+        for blk in range(8):
+            s = orc.e4m3_value(int(rng.integers(0x20, 0x60)))
+            codes = rng.integers(0, 16, 16)
+            codes[rng.integers(0, 16)] = 7
+            row += [orc.e2m1_value(int(c)) * s * q_scale for c in codes]
+        rows.append(row)
+    x = np.array(rows, np.float64)
+    assert np.all(x.astype(np.float32).astype(np.float64) == x)
+    got = orc.decode_q_a4q(x.astype(np.float32), q_scale)
+    np.testing.assert_array_equal(got, x)
+    # the per-row scheme on the same rows differs (its scale is amax/2688)
+    assert not np.array_equal(orc.decode_q_a4q(x.astype(np.float32)), x)
