@@ -15,6 +15,9 @@ Parity status per function:
   e2m1/e4m3 codec, block quantizer, append, gather/decode, attention,
   cache_bytes -- pinned by tests/test_oracle_*.py (format definitions, a
   library cast, brute force, closed forms, the pages' worked byte counts).
+  FP8 comparison cache (fp8_* and FP8Pools) -- the element codec pinned
+  against torch's float8_e4m3fn cast, the byte count against the pages'
+  131,072 B per token, attention through the same pinned definition.
   dense_attention (attention on the unquantized values, the reference of the
   accuracy report) -- pinned against scipy softmax on a ragged batch.
   decode_q_a4q with a single caller-given scale (per-tensor or single-level
@@ -96,6 +99,15 @@ def _load():
         lib.orc_attention_rows.argtypes = [P, P, i32, i32, P, P, i32, i32, i32, f64, P, P]
         lib.orc_cache_bytes.restype = i64
         lib.orc_cache_bytes.argtypes = [i64, i32, i32, i32]
+        lib.orc_fp8_encode.restype = ctypes.c_uint
+        lib.orc_fp8_encode.argtypes = [f32]
+        lib.orc_fp8_quantize_rows.argtypes = [P, i64, f32, P]
+        lib.orc_fp8_kv_append.restype = i32
+        lib.orc_fp8_kv_append.argtypes = [P, P, P, i64, i32, i32, i32, i64, f32, f32, P, P]
+        lib.orc_fp8_gather_decode.restype = i32
+        lib.orc_fp8_gather_decode.argtypes = [P, P, i32, i32, i32, i32, i32, i64, f32, P]
+        lib.orc_fp8_cache_bytes.restype = i64
+        lib.orc_fp8_cache_bytes.argtypes = [i64, i32, i32, i32]
         _lib = lib
     return _lib
 
@@ -213,6 +225,68 @@ def kv_append(pools: Pools, k, v, slot_mapping, k_g: float, v_g: float) -> None:
         raise ValueError("slot out of range")
 
 
+# --- FP8 (E4M3) comparison cache (readings F1..F3 of nvfp4_oracle.h) -------
+
+def fp8_encode_array(x) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.orc_fp8_encode(float(v)) for v in _f32(x).ravel()], dtype=np.uint8)
+
+
+def fp8_quantize(x, g: float) -> np.ndarray:
+    """Any-shape float32 array -> uint8 codes with per-tensor scale g (F1, F2)."""
+    x = _f32(x)
+    out = np.zeros(x.shape, np.uint8)
+    _load().orc_fp8_quantize_rows(_ptr(x), x.size, float(np.float32(g)), _ptr(out))
+    return out
+
+
+class FP8Pools:
+    """The two byte pools of one layer's FP8 cache (F3):
+    data [pages][Hkv][page_size][D], one E4M3 code per value."""
+
+    def __init__(self, num_pages: int, Hkv: int, D: int = 128, page_size: int = 16, fill: int = 0):
+        self.num_pages, self.Hkv, self.D, self.page_size = num_pages, Hkv, D, page_size
+        shp = (num_pages, Hkv, page_size, D)
+        self.k_data = np.full(shp, fill, np.uint8)
+        self.v_data = np.full(shp, fill, np.uint8)
+
+
+def fp8_kv_append(pools: FP8Pools, k, v, slot_mapping, k_g: float, v_g: float) -> None:
+    """k, v: [T, Hkv, D] float32 (bf16 values); slot_mapping: [T] int64."""
+    k = _f32(k)
+    v = _f32(v)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T, Hkv, D = k.shape
+    assert Hkv == pools.Hkv and D == pools.D and slots.shape == (T,)
+    lib = _load()
+    step = max(1024, (T + WORKERS - 1) // WORKERS)
+
+    def run(t0):
+        n = min(step, T - t0)
+        return lib.orc_fp8_kv_append(
+            ctypes.c_void_p(k.ctypes.data + t0 * k.strides[0]), ctypes.c_void_p(v.ctypes.data + t0 * v.strides[0]),
+            ctypes.c_void_p(slots.ctypes.data + t0 * 8), n, Hkv, D, pools.page_size, pools.num_pages,
+            float(np.float32(k_g)), float(np.float32(v_g)), _ptr(pools.k_data), _ptr(pools.v_data))
+
+    if T > 0 and any(rc != 0 for rc in _pmap(run, range(0, T, step))):
+        raise ValueError("slot out of range")
+
+
+def fp8_gather_decode(pools: FP8Pools, which: str, page_row, kv_len: int, head: int, g: float) -> np.ndarray:
+    data = pools.k_data if which == "k" else pools.v_data
+    row = np.ascontiguousarray(page_row, dtype=np.int32)
+    out = np.zeros((kv_len, pools.D), np.float64)
+    rc = _load().orc_fp8_gather_decode(_ptr(data), _ptr(row), kv_len, head, pools.Hkv, pools.D, pools.page_size,
+                                       pools.num_pages, float(np.float32(g)), _ptr(out))
+    if rc != 0:
+        raise ValueError("page id out of range")
+    return out
+
+
+def fp8_cache_bytes(num_pages: int, page_size: int, Hkv: int, D: int) -> int:
+    return int(_load().orc_fp8_cache_bytes(num_pages, page_size, Hkv, D))
+
+
 def gather_decode(pools: Pools, which: str, page_row, kv_len: int, head: int, g: float) -> np.ndarray:
     data = pools.k_data if which == "k" else pools.v_data
     scale = pools.k_scale if which == "k" else pools.v_scale
@@ -263,7 +337,8 @@ def decode_q_a4q(q_rows, q_scale: float = 0.0) -> np.ndarray:
 def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_g: float,
                     v_g: float, causal: bool, sm_scale: float, q_mode: str = "bf16",
                     rows=None, q_scale: float = 0.0):
-    """Attention of a ragged batch over the paged cache.
+    """Attention of a ragged batch over the paged cache (an NVFP4 `Pools` or
+    an FP8 `FP8Pools`, decoded by R5 or F3).
 
     q: [total_q, Hq, D] float32 (bf16 values); q_mode "bf16" uses q as is,
     "a4q" uses the quantized-then-decoded query (per-row scale, or the single
@@ -294,9 +369,10 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
     for b, positions in want.items():
         q_len, kv_len = int(qo[b + 1] - qo[b]), int(kvl[b])
         pos_all = np.array(sorted(set(positions)), np.int32)
+        gather = fp8_gather_decode if isinstance(pools, FP8Pools) else gather_decode
         dec = dict(zip(range(Hkv), _pmap(
-            lambda h: (gather_decode(pools, "k", pt[b], kv_len, h, k_g),
-                       gather_decode(pools, "v", pt[b], kv_len, h, v_g)), range(Hkv))))
+            lambda h: (gather(pools, "k", pt[b], kv_len, h, k_g),
+                       gather(pools, "v", pt[b], kv_len, h, v_g)), range(Hkv))))
         n_chunks = max(1, min(len(pos_all), -(-2 * WORKERS // Hkv)))
         chunks = [c for c in np.array_split(pos_all, n_chunks) if len(c)]
 

@@ -237,3 +237,63 @@ void orc_attention_rows(const double* q, const int32_t* pos, int n_rows,
 int64_t orc_cache_bytes(int64_t num_pages, int page_size, int Hkv, int D) {
   return 2 * num_pages * (int64_t)page_size * Hkv * (int64_t)(D / 2 + D / 16);
 }
+
+/* ---- FP8 (E4M3) cache, the comparison format of the pages -----------------
+ * "NVFP4 KV cache prefill vs decode performance", sections "NVFP4 stores 4.5
+ * bits per value before padding" (an 8-bit FP8 value per element) and "A
+ * worked per-token cache estimate" (FP8 bytes per token = 2 * L * H * D, one
+ * byte per value before any separate scale metadata).  Readings F1..F3 are
+ * stated in nvfp4_oracle.h. */
+
+/* F2: sign of x, then the nearest E4M3 magnitude (R1's encoder, which
+ * saturates at 448 and breaks ties to the even code). */
+unsigned orc_fp8_encode(float x) {
+  unsigned mag = orc_e4m3_encode(fabsf(x));
+  return (signbit(x) ? 0x80u : 0u) | mag;
+}
+
+/* F1, F2: one per-tensor scale g; each value times the correctly rounded
+ * reciprocal of g, then coded. */
+void orc_fp8_quantize_rows(const float* x, int64_t n, float g, uint8_t* out) {
+  float inv = 1.0f / g; /* fl32(1 / g) */
+  for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)orc_fp8_encode(x[i] * inv);
+}
+
+/* Cache write of the FP8 format: token t of K and V into slot
+ * slot_mapping[t] (R8 layout with D bytes per token row). */
+int orc_fp8_kv_append(const float* k, const float* v, const int64_t* slot_mapping,
+                      int64_t T, int Hkv, int D, int page_size, int64_t num_pages,
+                      float k_g, float v_g, uint8_t* k_data, uint8_t* v_data) {
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_pages * page_size) return -1;
+    int64_t page = slot / page_size, off = slot % page_size;
+    for (int h = 0; h < Hkv; ++h) {
+      orc_fp8_quantize_rows(k + (t * Hkv + h) * (int64_t)D, D, k_g,
+                            k_data + pool_offset(page, off, h, Hkv, page_size, D));
+      orc_fp8_quantize_rows(v + (t * Hkv + h) * (int64_t)D, D, v_g,
+                            v_data + pool_offset(page, off, h, Hkv, page_size, D));
+    }
+  }
+  return 0;
+}
+
+/* F3: x = e4m3(byte) * g, exact in fp64. */
+int orc_fp8_gather_decode(const uint8_t* data, const int32_t* page_row, int kv_len,
+                          int head, int Hkv, int D, int page_size, int64_t num_pages,
+                          float g, double* out) {
+  for (int j = 0; j < kv_len; ++j) {
+    int64_t page = page_row[j / page_size];
+    int64_t off = j % page_size;
+    if (page < 0 || page >= num_pages) return -1;
+    const uint8_t* row = data + pool_offset(page, off, head, Hkv, page_size, D);
+    for (int d = 0; d < D; ++d) out[(int64_t)j * D + d] = orc_e4m3_value(row[d]) * (double)g;
+  }
+  return 0;
+}
+
+/* "A worked per-token cache estimate": 2 * pages * page_size * Hkv * D. */
+int64_t orc_fp8_cache_bytes(int64_t num_pages, int page_size, int Hkv, int D) {
+  return 2 * num_pages * (int64_t)page_size * Hkv * (int64_t)D;
+}

@@ -46,6 +46,17 @@
  *   R8 cache layout  data [page][kv_head][page_size][D/2] bytes,
  *                    scales [page][kv_head][page_size][D/16] bytes,
  *                    slot = page * page_size + offset, negative slot = skip.
+ *
+ * The FP8 comparison cache ("NVFP4 KV cache prefill vs decode performance",
+ * sections "NVFP4 stores 4.5 bits per value before padding" and "A worked
+ * per-token cache estimate": one 8-bit FP8 value per element, scale metadata
+ * kept apart):
+ *   F1 scale         one fp32 scale per tensor (K and V), value = e4m3 * g.
+ *   F2 encode        code = sign | E4M3 magnitude nearest-even, saturating at
+ *                    448, of fl32(x * fl32(1 / g)) (R1's encoder on |q|); a
+ *                    negative value that rounds to zero keeps its sign (0x80).
+ *   F3 layout        data [page][kv_head][page_size][D] bytes, slots as R8;
+ *                    decode x = e4m3(byte) * g, exact in fp64.
  */
 #ifndef NVFP4_ORACLE_H
 #define NVFP4_ORACLE_H
@@ -105,6 +116,17 @@ void orc_attention_rows(const double* q, const int32_t* pos, int n_rows,
                         int q_len, const double* k, const double* v,
                         int kv_len, int D, int causal, double sm_scale,
                         double* out, double* lse);
+
+/* FP8 cache (F1..F3). */
+unsigned orc_fp8_encode(float x);
+void orc_fp8_quantize_rows(const float* x, int64_t n, float g, uint8_t* out);
+int orc_fp8_kv_append(const float* k, const float* v, const int64_t* slot_mapping,
+                      int64_t T, int Hkv, int D, int page_size, int64_t num_pages,
+                      float k_g, float v_g, uint8_t* k_data, uint8_t* v_data);
+int orc_fp8_gather_decode(const uint8_t* data, const int32_t* page_row, int kv_len,
+                          int head, int Hkv, int D, int page_size, int64_t num_pages,
+                          float g, double* out);
+int64_t orc_fp8_cache_bytes(int64_t num_pages, int page_size, int Hkv, int D);
 
 /* Cache bytes for one layer's K and V pools ([PD] "A worked per-token cache
  * estimate"): 2 * pages * page_size * Hkv * (D/2 + D/16). */

@@ -106,3 +106,21 @@ def test_division_instead_of_reciprocal_is_caught(orc):
         return packed, scale
 
     _fails(C.test_hand_worked_blocks, Mutant(orc, quantize_block16=divided))
+
+
+def test_fp8_truncation_and_dropped_sign_are_caught(orc):
+    """An FP8 element encoder that truncates toward zero, or one that drops
+    the sign, fails the pin against torch's float8_e4m3fn cast."""
+    from . import test_oracle_fp8 as P8
+    vals = np.array([orc.e4m3_value(b) for b in range(0x7F)])
+
+    def truncate(x):
+        x = np.asarray(x, np.float32).ravel()
+        mag = np.array([int(np.nonzero(vals <= min(abs(float(xi)), 448.0))[0].max()) for xi in x], np.uint8)
+        return mag | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
+
+    def unsigned(x):
+        return orc.fp8_encode_array(np.abs(np.asarray(x, np.float32)))
+
+    _fails(P8.test_fp8_encode_matches_torch_cast, Mutant(orc, fp8_encode_array=truncate))
+    _fails(P8.test_fp8_encode_matches_torch_cast, Mutant(orc, fp8_encode_array=unsigned))
