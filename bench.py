@@ -315,7 +315,7 @@ def run_ours(args, rank, world, dev):
     dqa_ik = nk_bench.time_fn(lambda: prefill(nk.VARIANT_DQ_AHEAD, "ws_min"), K, 3)
     app_bytes = APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads
     comps = {
-        "append": gbs_entry(app, app_bytes, peaks, app_g),
+        "append": dict(gbs_entry(app, app_bytes, peaks, app_g), copy_same_bytes=copy_reference(nk_bench, app_bytes, K)),
         "prefill_a4q": tflops_entry(pre, wl, peaks, True, "V repacked once per KV tile"),
         "prefill_a4q_inkernel": tflops_entry(pre_ik, wl, peaks, True, "V dequantized in the kernel"),
         "prefill_dq_ahead": tflops_entry(dqa, wl, peaks, False, "K and V repacked once per KV tile"),
@@ -326,6 +326,8 @@ def run_ours(args, rank, world, dev):
         comps["tails"] = tails_component(nk, nk_bench, dev, K, peaks)
         comps["prefill32k"] = long_component(nk, nk_bench, dev, K, peaks)
     comps["decode"] = decode_component(nk, nk_bench, dev, K)
+    if not args.no_matrix:
+        comps["fp8"] = fp8_component(nk, nk_bench, dev, K, peaks, comps)
     clk = clocks.stop()
 
     # the dominant kernel: the attention launch, timed inside the timed steps
@@ -360,6 +362,18 @@ def run_ours(args, rank, world, dev):
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds, a4q_out)
     return result
+
+
+def copy_reference(nk_bench, nbytes, K):
+    """A plain device copy that moves the same number of bytes (nbytes/2 read
+    + nbytes/2 written), timed like the components: what a transfer of this
+    size reaches on this GPU, launch, ramp and drain included."""
+    src = torch.empty(nbytes // 2, dtype=torch.uint8, device=nk_bench.dev).fill_(1)
+    dst = torch.empty_like(src)
+    t = statistics.mean(nk_bench.time_fn(lambda: dst.copy_(src), K, 3))
+    gbs = nbytes / (t * 1e-3) / 1e9
+    return {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / measured_peaks()["hbm_gbs"], 4),
+            "what": "torch copy of nbytes/2 (same bytes moved), L2 flushed before every call"}
 
 
 def gbs_entry(times, nbytes, peaks, graph_times=None):
@@ -454,6 +468,7 @@ def long_component(nk, nk_bench, dev, K, peaks):
     res = {"workload": wl.name,
            "append": gbs_entry(app, APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads, peaks),
            "prefill_a4q": tflops_entry(pre, wl, peaks, True, "repack")}
+    res["append"]["copy_same_bytes"] = copy_reference(nk_bench, res["append"]["bytes"], K)
     del c
     torch.cuda.empty_cache()
     return res
@@ -477,6 +492,57 @@ def decode_component(nk, nk_bench, dev, K):
     e = gbs_entry(t, CACHE_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads, measured_peaks(), tg)
     e["workload"] = wl.name
     return e
+
+
+FP8_APPEND_BYTES_PER_TOKEN_HEAD = 2 * (256 + 128)  # K and V: bf16 read + one code byte per value written
+FP8_CACHE_BYTES_PER_TOKEN_HEAD = 2 * 128           # K and V codes read by decode
+
+
+def fp8_component(nk, nk_bench, dev, K, peaks, comps):
+    """The FP8 (E4M3) comparison cache on the same shapes: append and prefill
+    of the 16K workload, decode of the batch-32 workload, and the NVFP4 / FP8
+    time ratios ("NVFP4 KV cache A4Q prefill explained", section "Build the
+    benchmark matrix": FP8 and the NVFP4 paths on the same revision)."""
+    inp = inputs_of("prefill16k")
+    wl = inp.wl
+    ks, vs = W.fp8_scale(inp.k), W.fp8_scale(inp.v)
+    order = W.shuffled_append_order(wl.total_kv)
+    k, v, slots = (inp.k[order].contiguous().to(dev), inp.v[order].contiguous().to(dev),
+                   inp.slot_mapping[order].contiguous().to(dev))
+    cache = nk.Fp8Cache(inp.num_pages, wl.num_kv_heads, ks, vs, device=dev)
+    q, pt, kvl, qo = inp.q.to(dev), inp.page_table.to(dev), inp.kv_lens.to(dev), inp.qo_indptr.to(dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(nk.fp8_workspace_bytes(nk.OP_PREFILL, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.total_q,
+                                            pt.shape[1] * 16), dtype=torch.uint8, device=dev)
+    app = nk_bench.time_fn(lambda: nk.fp8_kv_append(k, v, slots, cache), K, 3)
+    pre = nk_bench.time_fn(lambda: nk.fp8_paged_prefill(q, cache, pt, kvl, qo, causal=True, sm_scale=inp.sm_scale,
+                                                        out=out, workspace=ws), K, 3)
+    res = {"format": "E4M3, one fp32 scale per tensor (amax/448), 128 B per (token, kv head) per tensor",
+           "append": gbs_entry(app, FP8_APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads, peaks),
+           "prefill": tflops_entry(pre, wl, peaks, False, "BF16 query; K/V converted once per 128-key tile, "
+                                                          "BF16 QK + FP16 PV")}
+    del k, v, slots, cache, q, out, ws
+    torch.cuda.empty_cache()
+    dwl = W.decode_batch()
+    dinp = W.make_inputs(dwl)
+    dcache = nk.Fp8Cache(dinp.num_pages, dwl.num_kv_heads, W.fp8_scale(dinp.k), W.fp8_scale(dinp.v), device=dev)
+    nk.fp8_kv_append(dinp.k.to(dev), dinp.v.to(dev), dinp.slot_mapping.to(dev), dcache)
+    dq, dpt, dkvl = dinp.q.to(dev), dinp.page_table.to(dev), dinp.kv_lens.to(dev)
+    dout = torch.empty_like(dq)
+    dws = torch.empty(nk.fp8_workspace_bytes(nk.OP_DECODE, dwl.batch, dwl.num_q_heads, dwl.num_kv_heads, 0,
+                                             dpt.shape[1] * 16), dtype=torch.uint8, device=dev)
+    dec = nk_bench.time_fn(lambda: nk.fp8_paged_decode(dq, dcache, dpt, dkvl, sm_scale=dinp.sm_scale, out=dout,
+                                                       workspace=dws), K, 3)
+    res["decode"] = gbs_entry(dec, FP8_CACHE_BYTES_PER_TOKEN_HEAD * dwl.total_kv * dwl.num_kv_heads, peaks)
+    res["decode"]["workload"] = dwl.name
+    res["nvfp4_over_fp8_time"] = {
+        "append_16k": round(comps["append"]["ms"] / res["append"]["ms"], 3),
+        "prefill_16k_a4q": round(comps["prefill_a4q"]["ms"] / res["prefill"]["ms"], 3),
+        "prefill_16k_dq_ahead": round(comps["prefill_dq_ahead"]["ms"] / res["prefill"]["ms"], 3),
+        "decode_b32": round(comps["decode"]["ms"] / res["decode"]["ms"], 3),
+        "pages_context": "SM120 with FlashInfer: prefill 16K stock 21.0 / A4Q 18.0 vs FP8 11.1 ms; "
+                         "decode 9.63 vs 12.35 us; append 8.39 vs 3.01 us (other hardware)"}
+    return res
 
 
 def e2e_measure(nk, nk_bench, dev, P, wl, args):

@@ -32,7 +32,8 @@
  *     nvfp4kv_get_device_status(); the offending entries are skipped.
  *   - Nothing crosses the ABI as an exception; nothing calls exit().
  *   - Bounds: num_pages * page_size * num_kv_heads < 2^31 token-heads,
- *     total_q * num_q_heads < 2^31.
+ *     total_q * num_q_heads < 2^31, and an append's num_tokens *
+ *     num_kv_heads < 2^31.
  */
 #ifndef NVFP4KV_H
 #define NVFP4KV_H
@@ -249,6 +250,65 @@ int nvfp4_quantize_rows(const void* x, int64_t rows, int32_t mode, float global_
  * rounded to bf16 (exact when the product has at most 8 significant bits). */
 int nvfp4_dequantize_rows(const void* packed, const void* scales, int64_t rows, const float* row_scales,
                           float global_scale, void* out, void* stream);
+
+/* ---- FP8 (E4M3) comparison cache --------------------------------------------
+ * The format the pages weigh NVFP4 against ("NVFP4 KV cache prefill vs decode
+ * performance", sections "NVFP4 stores 4.5 bits per value before padding" and
+ * "A worked per-token cache estimate": one 8-bit FP8 value per element, 2 * L
+ * * H * D bytes per token, scale metadata kept apart; "NVFP4 KV cache A4Q
+ * prefill explained", section "Build the benchmark matrix": run FP8 and the
+ * NVFP4 paths on the same revision).  One fp32 scale per tensor; a value
+ * decodes as e4m3(code) * scale.  Per layer the caller owns two device pools
+ * (16-byte aligned):
+ *
+ *   k_data, v_data   uint8 [num_pages][num_kv_heads][page_size][head_dim]
+ *
+ * 256 bytes per (token, kv head) for K and V.  Slots, page tables, request
+ * metadata, workspaces, errors and streams follow the NVFP4 calls. */
+typedef struct fp8kv_cache {
+  void* k_data;
+  void* v_data;
+  int32_t num_pages;
+  int32_t page_size;    /* must be 16 */
+  int32_t num_kv_heads;
+  int32_t head_dim;     /* must be 128 */
+  float k_scale;        /* decode multiplier of K (> 0, finite) */
+  float v_scale;        /* decode multiplier of V (> 0, finite) */
+} fp8kv_cache_t;
+
+/* FP8 cache write: code = E4M3(x * (1/scale)) with 1/scale the correctly
+ * rounded fp32 reciprocal, nearest even, saturating at +-448; a negative value
+ * that rounds to zero keeps its sign bit.  Arguments as for nvfp4_kv_append. */
+int fp8_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                  const fp8kv_cache_t* cache, void* stream);
+
+/* Paged prefill over the FP8 cache with a BF16 query: K and V are converted
+ * once per (request, kv head, 128-key tile) into the workspace (E4M3 is exact
+ * in BF16 and FP16), then QK runs on BF16 and PV on FP16 tensor-core MMA --
+ * the FP8 baseline of the comparison.  Arguments as for nvfp4_paged_prefill
+ * without variant and q_global_scale; the workspace must hold
+ * fp8_workspace_bytes(NVFP4KV_OP_PREFILL, batch, num_q_heads, num_kv_heads,
+ * total_q, max_pages_per_req * 16) bytes (NVFP4KV_ERR_WORKSPACE otherwise). */
+int fp8_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const fp8kv_cache_t* cache,
+                      const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                      const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, void* o, float* lse,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Paged decode over the FP8 cache (BF16 query, one token per request).
+ * Arguments, workspace and results as for nvfp4_paged_decode. */
+int fp8_paged_decode(const void* q, int32_t num_q_heads, const fp8kv_cache_t* cache, const int32_t* page_table,
+                     int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o,
+                     float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of the FP8 calls (NVFP4KV_OP_PREFILL: the schedule plus the
+ * converted tiles for max_kv_len, which must be > 0; NVFP4KV_OP_DECODE: as for
+ * NVFP4).  Host-only; 0 for bad arguments. */
+size_t fp8_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int64_t total_q,
+                           int32_t max_kv_len);
+
+/* Bytes of one layer's two FP8 pools: 2 * num_pages * page_size *
+ * num_kv_heads * head_dim ("A worked per-token cache estimate").  Host-only. */
+size_t fp8_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
 
 /* Synchronizes `stream`, then returns and clears the device status word of
  * the current device: 0, or the NVFP4KV_ERR_* code of the first recorded

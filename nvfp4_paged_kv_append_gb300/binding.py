@@ -32,7 +32,8 @@ EXPORTED = ["nvfp4_kv_append", "nvfp4_paged_prefill", "nvfp4_paged_decode", "nvf
             "nvfp4_cache_bytes", "nvfp4_quantize_rows", "nvfp4_dequantize_rows", "nvfp4kv_get_device_status",
             "nvfp4kv_status_string", "nvfp4kv_version", "nvfp4kv_debug_wait_timeout",
             "nvfp4_paged_prefill_noalloc", "nvfp4_paged_prefill_noalloc_max_bytes",
-            "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run"]
+            "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run",
+            "fp8_kv_append", "fp8_paged_prefill", "fp8_paged_decode", "fp8_workspace_bytes", "fp8_cache_bytes"]
 
 
 class CacheDesc(ctypes.Structure):
@@ -40,6 +41,12 @@ class CacheDesc(ctypes.Structure):
                 ("v_scale", ctypes.c_void_p), ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("k_global_scale", ctypes.c_float), ("v_global_scale", ctypes.c_float)]
+
+
+class Fp8CacheDesc(ctypes.Structure):
+    _fields_ = [("k_data", ctypes.c_void_p), ("v_data", ctypes.c_void_p), ("num_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class NvFp4Error(RuntimeError):
@@ -73,12 +80,21 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4kv_status_string.argtypes = [ctypes.c_int]
     lib.nvfp4kv_status_string.restype = ctypes.c_char_p
     lib.nvfp4kv_version.restype = ctypes.c_char_p
+    F = ctypes.POINTER(Fp8CacheDesc)
+    lib.fp8_kv_append.argtypes = [P, P, P, i64, F, P]
+    lib.fp8_paged_prefill.argtypes = [P, i64, i32, F, P, i32, P, P, i32, i32, f32, P, P, P, sz, P]
+    lib.fp8_paged_decode.argtypes = [P, i32, F, P, i32, P, i32, f32, P, P, P, sz, P]
+    lib.fp8_workspace_bytes.argtypes = [i32, i32, i32, i32, i64, i32]
+    lib.fp8_workspace_bytes.restype = sz
+    lib.fp8_cache_bytes.argtypes = [i32, i32, i32, i32]
+    lib.fp8_cache_bytes.restype = sz
     lib.nvfp4kv_debug_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.nvfp4kv_debug_wait_timeout.restype = ctypes.c_int
     for name in ("nvfp4_kv_append", "nvfp4_paged_prefill", "nvfp4_paged_prefill_noalloc", "nvfp4_paged_decode",
                  "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run",
                  "nvfp4_quantize_rows",
-                 "nvfp4_dequantize_rows", "nvfp4kv_get_device_status"):
+                 "nvfp4_dequantize_rows", "nvfp4kv_get_device_status", "fp8_kv_append", "fp8_paged_prefill",
+                 "fp8_paged_decode"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -203,6 +219,108 @@ class Cache:
         return CacheDesc(self.k_data.data_ptr(), self.k_scale.data_ptr(), self.v_data.data_ptr(),
                          self.v_scale.data_ptr(), self.num_pages, PAGE_SIZE, self.num_kv_heads, HEAD_DIM,
                          self.k_global_scale, self.v_global_scale)
+
+
+class Fp8Cache:
+    """One layer's FP8 (E4M3) comparison cache: two caller-owned device pools
+    [pages][kv heads][16][128] of codes, plus the two per-tensor scales."""
+
+    def __init__(self, num_pages: int, num_kv_heads: int, k_scale: float, v_scale: float, device=None,
+                 fill: Optional[int] = 0):
+        dev = device or torch.device("cuda")
+        shp = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM)
+        self.k_data = torch.full(shp, int(fill or 0), dtype=torch.uint8, device=dev)
+        self.v_data = torch.full(shp, int(fill or 0), dtype=torch.uint8, device=dev)
+        self.num_pages, self.num_kv_heads = num_pages, num_kv_heads
+        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
+
+    def pools(self):
+        return (self.k_data, self.v_data)
+
+    def desc(self) -> Fp8CacheDesc:
+        """Host descriptor of the two pools (which must be device memory)."""
+        for t in self.pools():
+            if not t.is_cuda:
+                raise ValueError("cache pools must live on a CUDA device")
+            if not t.is_contiguous() or t.dtype != torch.uint8:
+                raise ValueError("cache pools must be contiguous uint8 tensors")
+        return Fp8CacheDesc(self.k_data.data_ptr(), self.v_data.data_ptr(), self.num_pages, PAGE_SIZE,
+                            self.num_kv_heads, HEAD_DIM, self.k_scale, self.v_scale)
+
+
+def fp8_cache_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib.fp8_cache_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
+def fp8_workspace_bytes(op: int, batch: int, num_q_heads: int, num_kv_heads: int, total_q: int = 0,
+                        max_kv_len: int = 0) -> int:
+    return int(lib.fp8_workspace_bytes(op, batch, num_q_heads, num_kv_heads, total_q, max_kv_len))
+
+
+def fp8_kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, cache: Fp8Cache, stream=None) -> None:
+    _check_rows(k, "k")
+    _check_rows(v, "v")
+    _require(k.shape == v.shape and k.shape[1] == cache.num_kv_heads, "k and v must be [tokens][kv heads][128]")
+    _check_dtype(slot_mapping, torch.int64, "slot_mapping")
+    _require(slot_mapping.dim() == 1 and slot_mapping.shape[0] == k.shape[0], "slot_mapping must be [tokens]")
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), k, v, slot_mapping)
+    with torch.cuda.device(dev):
+        _check("fp8_kv_append", lib.fp8_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0], ctypes.byref(d),
+                                                  _stream(stream, dev)))
+
+
+def fp8_paged_prefill(q: torch.Tensor, cache: Fp8Cache, page_table: torch.Tensor, kv_lens: torch.Tensor,
+                      qo_indptr: torch.Tensor, causal: bool = True, sm_scale: Optional[float] = None,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Paged prefill over the FP8 cache (BF16 query; K/V converted once per
+    KV tile, BF16 QK and FP16 PV on the tensor cores)."""
+    _check_rows(q)
+    batch = _check_tables(page_table, kv_lens, qo_indptr)
+    total_q, hq, _ = q.shape
+    _check_out(out, lse, total_q, hq)
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), q, page_table, kv_lens, qo_indptr, out, lse, workspace)
+    if out is None:
+        out = torch.empty_like(q)
+    if sm_scale is None:
+        sm_scale = HEAD_DIM ** -0.5
+    if workspace is None:
+        need = fp8_workspace_bytes(OP_PREFILL, batch, hq, cache.num_kv_heads, total_q, page_table.shape[1] * PAGE_SIZE)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check("fp8_paged_prefill", lib.fp8_paged_prefill(
+            _ptr(q), total_q, hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+            _ptr(qo_indptr), batch, int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream, dev)))
+    return out
+
+
+def fp8_paged_decode(q: torch.Tensor, cache: Fp8Cache, page_table: torch.Tensor, kv_lens: torch.Tensor,
+                     sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    _check_rows(q)
+    batch = _check_tables(page_table, kv_lens, None)
+    _require(q.shape[0] == batch, "q must be [batch][heads][128] (one query token per request)")
+    _, hq, _ = q.shape
+    _check_out(out, lse, batch, hq)
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), q, page_table, kv_lens, out, lse, workspace)
+    if out is None:
+        out = torch.empty_like(q)
+    if sm_scale is None:
+        sm_scale = HEAD_DIM ** -0.5
+    need = fp8_workspace_bytes(OP_DECODE, batch, hq, cache.num_kv_heads, 0, page_table.shape[1] * PAGE_SIZE)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check("fp8_paged_decode", lib.fp8_paged_decode(
+            _ptr(q), hq, ctypes.byref(d), _ptr(page_table), page_table.shape[1], _ptr(kv_lens), batch,
+            float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream, dev)))
+    return out
 
 
 def nvfp4_cache_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:

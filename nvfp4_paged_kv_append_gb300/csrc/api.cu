@@ -11,10 +11,6 @@
 #include "kernels.cuh"
 #include "nvfp4kv.h"
 
-namespace nvfp4kv {
-size_t prefill_smem_bytes(int variant);
-}
-
 using namespace nvfp4kv;
 
 namespace {
@@ -27,6 +23,7 @@ struct DeviceState {
   bool init = false;
   int rc = NVFP4KV_OK;
   int num_sms = 0;
+  int append_ctas = 1;    // resident append CTAs per SM
   int* status = nullptr;  // device address of g_status_word on this device
 };
 
@@ -54,6 +51,7 @@ int device_state(DeviceState** out) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return NVFP4KV_ERR_CUDA;
       d.status = static_cast<int*>(p);
+      d.append_ctas = append_ctas_per_sm();
       d.rc = NVFP4KV_OK;
     }
     d.init = true;
@@ -87,6 +85,36 @@ int check_cache(const nvfp4kv_cache_t* c) {
   if (static_cast<int64_t>(c->num_pages) * c->num_kv_heads * kPageSize >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
   if (!finite_pos(c->k_global_scale) || !finite_pos(c->v_global_scale)) return NVFP4KV_ERR_ARG;
   return NVFP4KV_OK;
+}
+
+int check_fp8_cache(const fp8kv_cache_t* c) {
+  if (!c) return NVFP4KV_ERR_ARG;
+  if (!c->k_data || !c->v_data || !aligned16(c->k_data) || !aligned16(c->v_data)) return NVFP4KV_ERR_ARG;
+  if (c->page_size != kPageSize || c->head_dim != kHeadDim) return NVFP4KV_ERR_ARG;
+  if (c->num_pages <= 0 || c->num_kv_heads <= 0 || c->num_kv_heads > 255) return NVFP4KV_ERR_ARG;
+  if (static_cast<int64_t>(c->num_pages) * c->num_kv_heads * kPageSize >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  if (!finite_pos(c->k_scale) || !finite_pos(c->v_scale)) return NVFP4KV_ERR_ARG;
+  return NVFP4KV_OK;
+}
+
+// One layer's cache as the kernels see it: NVFP4 (codes + block scales +
+// per-tensor scales) or FP8 (codes + per-tensor scales, no scale pools).
+struct CacheView {
+  const uint8_t *k_data, *k_scale, *v_data, *v_scale;
+  int num_pages, num_kv_heads;
+  float k_g, v_g;
+  bool fp8;
+};
+
+CacheView view_of(const nvfp4kv_cache_t* c) {
+  return CacheView{static_cast<const uint8_t*>(c->k_data), static_cast<const uint8_t*>(c->k_scale),
+                   static_cast<const uint8_t*>(c->v_data), static_cast<const uint8_t*>(c->v_scale),
+                   c->num_pages, c->num_kv_heads, c->k_global_scale, c->v_global_scale, false};
+}
+
+CacheView view_of(const fp8kv_cache_t* c) {
+  return CacheView{static_cast<const uint8_t*>(c->k_data), nullptr, static_cast<const uint8_t*>(c->v_data), nullptr,
+                   c->num_pages, c->num_kv_heads, c->k_scale, c->v_scale, true};
 }
 
 int log2_exact(int x) {
@@ -140,6 +168,44 @@ __global__ void nvfp4_debug_wait_kernel(uint64_t limit_ns, int* status) {
   mbar_wait(&bar, 0, status, limit_ns);
 }
 
+// Cache write of either format: validation of the tensors, one persistent
+// wave of the format's append kernel.
+int append_impl(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, const CacheView& c,
+                void* stream) {
+  int rc;
+  if (num_tokens < 0) return NVFP4KV_ERR_ARG;
+  if (num_tokens == 0) return NVFP4KV_OK;
+  if (!k || !v || !slot_mapping || !aligned16(k) || !aligned16(v)) return NVFP4KV_ERR_ARG;
+  const int64_t rows = num_tokens * c.num_kv_heads;
+  if (num_tokens >= (int64_t(1) << 31) || rows >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  AppendArgs a;
+  a.k = k;
+  a.v = v;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = c.num_kv_heads;
+  a.num_slots = static_cast<int64_t>(c.num_pages) * kPageSize;
+  a.k_data = const_cast<uint8_t*>(c.k_data);
+  a.k_scale = const_cast<uint8_t*>(c.k_scale);
+  a.v_data = const_cast<uint8_t*>(c.v_data);
+  a.v_scale = const_cast<uint8_t*>(c.v_scale);
+  a.k_scale_g = c.k_g;
+  a.v_scale_g = c.v_g;
+  a.row_magic = ((uint64_t(1) << 40) + c.num_kv_heads - 1) / c.num_kv_heads;
+  a.status = d->status;
+  // one persistent wave (as many CTAs of 256 threads as fit on every SM);
+  // each warp step covers four rows, 2 * rows rows of K and V in all
+  const int64_t warps = (2 * rows + 3) / 4;
+  const int64_t want = (warps + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(d->num_sms) * d->append_ctas;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  if (c.fp8) fp8_kv_append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  else nvfp4_kv_append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_rc(cudaGetLastError());
+}
+
 }  // namespace
 
 extern "C" {
@@ -170,37 +236,16 @@ size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int
 
 int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
                     const nvfp4kv_cache_t* cache, void* stream) {
-  int rc = check_cache(cache);
+  const int rc = check_cache(cache);
   if (rc) return rc;
-  if (num_tokens < 0) return NVFP4KV_ERR_ARG;
-  if (num_tokens == 0) return NVFP4KV_OK;
-  if (!k || !v || !slot_mapping || !aligned16(k) || !aligned16(v)) return NVFP4KV_ERR_ARG;
-  const int64_t rows = num_tokens * cache->num_kv_heads;
-  if (rows * 4 / 256 + 1 >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
-  DeviceState* d = nullptr;
-  if ((rc = device_state(&d))) return rc;
-  AppendArgs a;
-  a.k = k;
-  a.v = v;
-  a.slot_mapping = slot_mapping;
-  a.num_tokens = num_tokens;
-  a.num_kv_heads = cache->num_kv_heads;
-  a.num_slots = static_cast<int64_t>(cache->num_pages) * cache->page_size;
-  a.k_data = static_cast<uint8_t*>(cache->k_data);
-  a.k_scale = static_cast<uint8_t*>(cache->k_scale);
-  a.v_data = static_cast<uint8_t*>(cache->v_data);
-  a.v_scale = static_cast<uint8_t*>(cache->v_scale);
-  a.k_scale_g = cache->k_global_scale;
-  a.v_scale_g = cache->v_global_scale;
-  a.status = d->status;
-  // one persistent wave: 8 CTAs of 256 threads per SM, grid-stride over the
-  // 8 * num_tokens * Hkv units of K and V
-  const int64_t units = rows * 8;
-  const int64_t want = (units + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(d->num_sms) * 8;
-  nvfp4_kv_append_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0,
-                           static_cast<cudaStream_t>(stream)>>>(a);
-  return launch_rc(cudaGetLastError());
+  return append_impl(k, v, slot_mapping, num_tokens, view_of(cache), stream);
+}
+
+int fp8_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                  const fp8kv_cache_t* cache, void* stream) {
+  const int rc = check_fp8_cache(cache);
+  if (rc) return rc;
+  return append_impl(k, v, slot_mapping, num_tokens, view_of(cache), stream);
 }
 
 }  // extern "C"
@@ -210,16 +255,17 @@ namespace {
 enum PrefillStage { kStagePlan = 1, kStageRun = 2 };
 
 // Validates the arguments, fills the kernel argument blocks and launches the
-// requested stages.  q/o/lse/sm_scale are only used by the run stage.
-int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
+// requested stages.  q/o/lse/sm_scale are only used by the run stage.  An FP8
+// cache always runs in repack mode (records converted once per KV tile, then
+// the dequant-ahead attention), so its workspace must hold the records.
+int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_heads, const CacheView& c,
                    const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
                    const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
                    float q_global_scale, void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_cache(cache);
-  if (rc) return rc;
+  int rc;
   if (batch < 0 || total_q < 0 || max_pages_per_req <= 0) return NVFP4KV_ERR_ARG;
-  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return NVFP4KV_ERR_ARG;
-  const int lg = log2_exact(num_q_heads / cache->num_kv_heads);
+  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0) return NVFP4KV_ERR_ARG;
+  const int lg = log2_exact(num_q_heads / c.num_kv_heads);
   if (lg < 0 || lg > 7) return NVFP4KV_ERR_ARG;
   if (causal != 0 && causal != 1) return NVFP4KV_ERR_ARG;
   if (variant != NVFP4KV_VARIANT_A4Q && variant != NVFP4KV_VARIANT_DQ_AHEAD) return NVFP4KV_ERR_ARG;
@@ -229,7 +275,7 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   if (batch == 0 || total_q == 0) return NVFP4KV_OK;
   if (!page_table || !kv_lens || !qo_indptr) return NVFP4KV_ERR_ARG;
   if ((stages & kStageRun) && (!q || !o || !aligned16(q) || !aligned16(o))) return NVFP4KV_ERR_ARG;
-  const int64_t max_items = prefill_max_items(total_q, batch, num_q_heads, cache->num_kv_heads);
+  const int64_t max_items = prefill_max_items(total_q, batch, num_q_heads, c.num_kv_heads);
   if (max_items >= (int64_t(1) << 30)) return NVFP4KV_ERR_ARG;
   const size_t sched = prefill_sched_bytes(max_items, batch);
   if (!workspace || !aligned16(workspace) || workspace_bytes < sched) return NVFP4KV_ERR_WORKSPACE;
@@ -237,9 +283,13 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   // workspace holds a tile for every (request, kv head, KV tile) the page
   // table allows and requests average at least two q tiles per kv head.
   const size_t rbytes =
-      prefill_repack_bytes(variant, batch, cache->num_kv_heads, static_cast<int64_t>(max_pages_per_req) * kPageSize);
-  const int64_t qtiles = (total_q * (num_q_heads / cache->num_kv_heads) + kBM - 1) / kBM;
-  const bool repack = workspace_bytes >= sched + rbytes && qtiles >= 2 * static_cast<int64_t>(batch);
+      prefill_repack_bytes(variant, batch, c.num_kv_heads, static_cast<int64_t>(max_pages_per_req) * kPageSize);
+  const int64_t qtiles = (total_q * (num_q_heads / c.num_kv_heads) + kBM - 1) / kBM;
+  bool repack = workspace_bytes >= sched + rbytes && qtiles >= 2 * static_cast<int64_t>(batch);
+  if (c.fp8) {
+    if (workspace_bytes < sched + rbytes) return NVFP4KV_ERR_WORKSPACE;
+    repack = true;
+  }
   DeviceState* d = nullptr;
   if ((rc = device_state(&d))) return rc;
 
@@ -249,7 +299,7 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   plan.total_q = total_q;
   plan.batch = batch;
   plan.max_pages = max_pages_per_req;
-  plan.num_kv_heads = cache->num_kv_heads;
+  plan.num_kv_heads = c.num_kv_heads;
   plan.log2_group = lg;
   plan.causal = causal;
   plan.bn = prefill_tile_keys(variant, repack);
@@ -259,25 +309,25 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
 
   PrefillArgs a;
   a.q = q;
-  a.k_data = static_cast<const uint8_t*>(cache->k_data);
-  a.k_scale = static_cast<const uint8_t*>(cache->k_scale);
-  a.v_data = static_cast<const uint8_t*>(cache->v_data);
-  a.v_scale = static_cast<const uint8_t*>(cache->v_scale);
+  a.k_data = c.k_data;
+  a.k_scale = c.k_scale;
+  a.v_data = c.v_data;
+  a.v_scale = c.v_scale;
   a.page_table = page_table;
   a.kv_lens = kv_lens;
   a.qo_indptr = qo_indptr;
   a.total_q = total_q;
   a.batch = batch;
   a.max_pages = max_pages_per_req;
-  a.num_pages = cache->num_pages;
-  a.num_kv_heads = cache->num_kv_heads;
+  a.num_pages = c.num_pages;
+  a.num_kv_heads = c.num_kv_heads;
   a.num_q_heads = num_q_heads;
   a.group = 1 << lg;
   a.log2_group = lg;
   a.causal = causal;
   a.sm_scale = sm_scale;
-  a.k_g = cache->k_global_scale;
-  a.v_g = cache->v_global_scale;
+  a.k_g = c.k_g;
+  a.v_g = c.v_g;
   a.q_g = variant == NVFP4KV_VARIANT_A4Q ? q_global_scale : 0.0f;
   a.o = o;
   a.lse = lse;
@@ -286,11 +336,60 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   a.repack = repack ? static_cast<uint8_t*>(workspace) + sched : nullptr;
   a.status = d->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.fp8) return launch_rc(launch_prefill_fp8(a, plan, d->num_sms, st));  // plan + repack + attention
   if (stages & kStagePlan) {
     if ((rc = launch_rc(launch_prefill_plan(a, plan, variant, repack, d->num_sms, st)))) return rc;
   }
   if (stages & kStageRun) return launch_rc(launch_prefill_attend(a, variant, repack, d->num_sms, st));
   return NVFP4KV_OK;
+}
+
+// Paged decode of either format.
+int decode_impl(const void* q, int32_t num_q_heads, const CacheView& c, const int32_t* page_table,
+                int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o, float* lse,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  int rc;
+  if (batch < 0 || max_pages_per_req <= 0) return NVFP4KV_ERR_ARG;
+  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0) return NVFP4KV_ERR_ARG;
+  const int lg = log2_exact(num_q_heads / c.num_kv_heads);
+  if (lg < 0 || lg > 4) return NVFP4KV_ERR_ARG;
+  if (!std::isfinite(sm_scale)) return NVFP4KV_ERR_ARG;
+  if (batch == 0) return NVFP4KV_OK;
+  if (!q || !o || !page_table || !kv_lens || !aligned16(q) || !aligned16(o)) return NVFP4KV_ERR_ARG;
+  const int64_t max_kv = static_cast<int64_t>(max_pages_per_req) * kPageSize;
+  if (max_kv >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
+  const size_t need = nvfp4_workspace_bytes(NVFP4KV_OP_DECODE, batch, num_q_heads, c.num_kv_heads, 0,
+                                            static_cast<int32_t>(max_kv));
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return NVFP4KV_ERR_WORKSPACE;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  DecodeArgs a;
+  a.q = q;
+  a.k_data = c.k_data;
+  a.k_scale = c.k_scale;
+  a.v_data = c.v_data;
+  a.v_scale = c.v_scale;
+  a.page_table = page_table;
+  a.kv_lens = kv_lens;
+  a.max_pages = max_pages_per_req;
+  a.num_pages = c.num_pages;
+  a.num_kv_heads = c.num_kv_heads;
+  a.num_q_heads = num_q_heads;
+  a.max_splits = static_cast<int>((max_kv + kDecSplit - 1) / kDecSplit);
+  a.k_g = c.k_g;
+  a.v_g = c.v_g;
+  a.sm_scale = sm_scale;
+  a.o = o;
+  a.lse = lse;
+  a.batch = batch;
+  a.sched = static_cast<int*>(workspace);
+  float* ws = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       decode_sched_bytes(batch, c.num_kv_heads, a.max_splits));
+  a.part_o = ws;
+  a.part_lse = ws + static_cast<size_t>(batch) * a.max_splits * num_q_heads * kHeadDim;
+  a.status = d->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return launch_rc(c.fp8 ? launch_decode_fp8(a, batch, d->num_sms, st) : launch_decode(a, batch, d->num_sms, st));
 }
 
 }  // namespace
@@ -302,18 +401,22 @@ int nvfp4_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, con
                         const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, int32_t variant,
                         float q_global_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
                         void* stream) {
-  return prefill_stages(kStagePlan | kStageRun, q, total_q, num_q_heads, cache, page_table, max_pages_per_req,
-                        kv_lens, qo_indptr, batch, causal, sm_scale, variant, q_global_scale, o, lse, workspace,
-                        workspace_bytes, stream);
+  const int rc = check_cache(cache);
+  if (rc) return rc;
+  return prefill_stages(kStagePlan | kStageRun, q, total_q, num_q_heads, view_of(cache), page_table,
+                        max_pages_per_req, kv_lens, qo_indptr, batch, causal, sm_scale, variant, q_global_scale, o,
+                        lse, workspace, workspace_bytes, stream);
 }
 
 int nvfp4_paged_prefill_plan(int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
                              const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
                              const int32_t* qo_indptr, int32_t batch, int32_t causal, int32_t variant,
                              void* workspace, size_t workspace_bytes, void* stream) {
-  return prefill_stages(kStagePlan, nullptr, total_q, num_q_heads, cache, page_table, max_pages_per_req, kv_lens,
-                        qo_indptr, batch, causal, 0.0f, variant, 0.0f, nullptr, nullptr, workspace, workspace_bytes,
-                        stream);
+  const int rc = check_cache(cache);
+  if (rc) return rc;
+  return prefill_stages(kStagePlan, nullptr, total_q, num_q_heads, view_of(cache), page_table, max_pages_per_req,
+                        kv_lens, qo_indptr, batch, causal, 0.0f, variant, 0.0f, nullptr, nullptr, workspace,
+                        workspace_bytes, stream);
 }
 
 int nvfp4_paged_prefill_run(const void* q, int64_t total_q, int32_t num_q_heads, const nvfp4kv_cache_t* cache,
@@ -321,58 +424,56 @@ int nvfp4_paged_prefill_run(const void* q, int64_t total_q, int32_t num_q_heads,
                             const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale,
                             int32_t variant, float q_global_scale, void* o, float* lse, void* workspace,
                             size_t workspace_bytes, void* stream) {
-  return prefill_stages(kStageRun, q, total_q, num_q_heads, cache, page_table, max_pages_per_req, kv_lens,
+  const int rc = check_cache(cache);
+  if (rc) return rc;
+  return prefill_stages(kStageRun, q, total_q, num_q_heads, view_of(cache), page_table, max_pages_per_req, kv_lens,
                         qo_indptr, batch, causal, sm_scale, variant, q_global_scale, o, lse, workspace,
                         workspace_bytes, stream);
 }
 
-
-
 int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t* cache, const int32_t* page_table,
                        int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o,
                        float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_cache(cache);
+  const int rc = check_cache(cache);
   if (rc) return rc;
-  if (batch < 0 || max_pages_per_req <= 0) return NVFP4KV_ERR_ARG;
-  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return NVFP4KV_ERR_ARG;
-  const int lg = log2_exact(num_q_heads / cache->num_kv_heads);
-  if (lg < 0 || lg > 4) return NVFP4KV_ERR_ARG;
-  if (!std::isfinite(sm_scale)) return NVFP4KV_ERR_ARG;
-  if (batch == 0) return NVFP4KV_OK;
-  if (!q || !o || !page_table || !kv_lens || !aligned16(q) || !aligned16(o)) return NVFP4KV_ERR_ARG;
-  const int64_t max_kv = static_cast<int64_t>(max_pages_per_req) * kPageSize;
-  if (max_kv >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
-  const size_t need = nvfp4_workspace_bytes(NVFP4KV_OP_DECODE, batch, num_q_heads, cache->num_kv_heads, 0,
-                                            static_cast<int32_t>(max_kv));
-  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return NVFP4KV_ERR_WORKSPACE;
-  DeviceState* d = nullptr;
-  if ((rc = device_state(&d))) return rc;
-  DecodeArgs a;
-  a.q = q;
-  a.k_data = static_cast<const uint8_t*>(cache->k_data);
-  a.k_scale = static_cast<const uint8_t*>(cache->k_scale);
-  a.v_data = static_cast<const uint8_t*>(cache->v_data);
-  a.v_scale = static_cast<const uint8_t*>(cache->v_scale);
-  a.page_table = page_table;
-  a.kv_lens = kv_lens;
-  a.max_pages = max_pages_per_req;
-  a.num_pages = cache->num_pages;
-  a.num_kv_heads = cache->num_kv_heads;
-  a.num_q_heads = num_q_heads;
-  a.max_splits = static_cast<int>((max_kv + kDecSplit - 1) / kDecSplit);
-  a.k_g = cache->k_global_scale;
-  a.v_g = cache->v_global_scale;
-  a.sm_scale = sm_scale;
-  a.o = o;
-  a.lse = lse;
-  a.batch = batch;
-  a.sched = static_cast<int*>(workspace);
-  float* ws = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       decode_sched_bytes(batch, cache->num_kv_heads, a.max_splits));
-  a.part_o = ws;
-  a.part_lse = ws + static_cast<size_t>(batch) * a.max_splits * num_q_heads * kHeadDim;
-  a.status = d->status;
-  return launch_rc(launch_decode(a, batch, d->num_sms, static_cast<cudaStream_t>(stream)));
+  return decode_impl(q, num_q_heads, view_of(cache), page_table, max_pages_per_req, kv_lens, batch, sm_scale, o, lse,
+                     workspace, workspace_bytes, stream);
+}
+
+size_t fp8_cache_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_pages <= 0 || page_size <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  return 2ull * static_cast<size_t>(num_pages) * page_size * num_kv_heads * head_dim;
+}
+
+size_t fp8_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int64_t total_q,
+                           int32_t max_kv_len) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+  if (op == NVFP4KV_OP_PREFILL) {
+    if (total_q < 0 || max_kv_len <= 0) return 0;
+    const int64_t items = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
+    return prefill_sched_bytes(items, batch) + prefill_repack_bytes(1, batch, num_kv_heads, max_kv_len);
+  }
+  return nvfp4_workspace_bytes(op, batch, num_q_heads, num_kv_heads, total_q, max_kv_len);
+}
+
+int fp8_paged_prefill(const void* q, int64_t total_q, int32_t num_q_heads, const fp8kv_cache_t* cache,
+                      const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+                      const int32_t* qo_indptr, int32_t batch, int32_t causal, float sm_scale, void* o, float* lse,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  const int rc = check_fp8_cache(cache);
+  if (rc) return rc;
+  return prefill_stages(kStagePlan | kStageRun, q, total_q, num_q_heads, view_of(cache), page_table,
+                        max_pages_per_req, kv_lens, qo_indptr, batch, causal, sm_scale, NVFP4KV_VARIANT_DQ_AHEAD,
+                        0.0f, o, lse, workspace, workspace_bytes, stream);
+}
+
+int fp8_paged_decode(const void* q, int32_t num_q_heads, const fp8kv_cache_t* cache, const int32_t* page_table,
+                     int32_t max_pages_per_req, const int32_t* kv_lens, int32_t batch, float sm_scale, void* o,
+                     float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  const int rc = check_fp8_cache(cache);
+  if (rc) return rc;
+  return decode_impl(q, num_q_heads, view_of(cache), page_table, max_pages_per_req, kv_lens, batch, sm_scale, o, lse,
+                     workspace, workspace_bytes, stream);
 }
 
 int nvfp4_quantize_rows(const void* x, int64_t rows, int32_t mode, float global_scale, void* packed, void* scales,

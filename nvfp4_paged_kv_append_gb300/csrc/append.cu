@@ -4,10 +4,13 @@
 // vectors, chooses block scales, packs FP4 data and maps it into paged slots).
 //
 // HBM-bound: per (token, kv head) and tensor, 256 B are read and 72 B written.
-// Four threads share one 128-value row: each reads 64 contiguous bytes (four
-// 16-byte streaming loads), encodes two 16-value blocks and writes one 16-byte
-// vector of codes plus a 2-byte scale pair; the four threads of a row write
-// the row's 64 code bytes and 8 scale bytes contiguously.
+// A lane owns one 16-value block (32 B of bf16, two 16-byte streaming loads)
+// and writes its 8 code bytes and its scale byte; eight lanes cover a row, so
+// a warp reads four consecutive rows (1 KB) per step and writes each row's 64
+// code bytes and 8 scale bytes contiguously.  Rows of K come first, then rows
+// of V.  One persistent wave of CTAs (as many as fit on every SM) strides
+// over the rows, and each lane loads its next block before it encodes the
+// current one, so the encode of one step overlaps the loads of the next.
 #include "kernels.cuh"
 
 namespace nvfp4kv {
@@ -20,76 +23,128 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return r;
 }
 
-// One unit = 32 values (64 B of bf16) of one (token, kv head) row of K or V:
-// two 16-value blocks -> 16 code bytes + 2 scale bytes.
-struct AppendUnit {
-  uint4 w[4];
-  int64_t slot;
+namespace {
+
+// One lane's 16-value block, loaded one step ahead of its encoding.
+struct AppendBlock {
+  uint4 lo, hi;  // the 16 bf16 values
+  int64_t slot;  // destination slot of the row's token
+  int row;       // token * Hkv + head within the tensor
+  int tensor;    // 0 = K, 1 = V, -1 = no block (past the end)
 };
 
-__device__ __forceinline__ void append_load(const AppendArgs& a, int64_t u, int64_t units_per_tensor,
-                                            AppendUnit& x) {
-  const int tensor = u >= units_per_tensor;
-  const int64_t uu = u - tensor * units_per_tensor;
-  const int64_t row = uu >> 2;  // token * Hkv + head
-  const int part = static_cast<int>(uu & 3);
-  const uint16_t* src = reinterpret_cast<const uint16_t*>(tensor ? a.v : a.k) + row * kHeadDim + part * 32;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) x.w[i] = ld_stream_v4(src + 8 * i);
-  x.slot = a.slot_mapping[row / a.num_kv_heads];
+// token of a row: floor(row / Hkv) by a multiply-shift (exact for
+// row < 2^31 and Hkv <= 255, which the host checks)
+__device__ __forceinline__ int row_token(int row, uint64_t magic) {
+  return static_cast<int>((static_cast<uint64_t>(row) * magic) >> 40);
 }
 
-__device__ __forceinline__ void append_store(const AppendArgs& a, int64_t u, int64_t units_per_tensor,
-                                             const AppendUnit& x) {
-  if (x.slot < 0) return;
-  if (x.slot >= a.num_slots) {
+__device__ __forceinline__ void append_fetch(const AppendArgs& a, int64_t step, int lane, AppendBlock& blk) {
+  const int64_t rows = a.num_tokens * a.num_kv_heads;
+  const int64_t gr = step * 4 + (lane >> 3);
+  blk.tensor = -1;
+  if (gr >= 2 * rows) return;
+  blk.tensor = gr >= rows;
+  blk.row = static_cast<int>(gr - blk.tensor * rows);
+  const uint16_t* src =
+      reinterpret_cast<const uint16_t*>(blk.tensor ? a.v : a.k) + static_cast<int64_t>(blk.row) * kHeadDim + (lane & 7) * 16;
+  blk.lo = ld_stream_v4(src);
+  blk.hi = ld_stream_v4(src + 8);
+  blk.slot = a.slot_mapping[row_token(blk.row, a.row_magic)];
+}
+
+__device__ __forceinline__ void append_encode(const AppendArgs& a, const AppendBlock& blk, int lane) {
+  if (blk.tensor < 0 || blk.slot < 0) return;  // past the end, or a padding token
+  if (blk.slot >= a.num_slots) {
     set_status(a.status, kDevBadSlot);
     return;
   }
-  const int tensor = u >= units_per_tensor;
-  const int64_t uu = u - tensor * units_per_tensor;
-  const int64_t row = uu >> 2;
-  const int part = static_cast<int>(uu & 3);
-  const int h = static_cast<int>(row % a.num_kv_heads);
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    bf16x2_to_f32(x.w[i].x, v[8 * i + 0], v[8 * i + 1]);
-    bf16x2_to_f32(x.w[i].y, v[8 * i + 2], v[8 * i + 3]);
-    bf16x2_to_f32(x.w[i].z, v[8 * i + 4], v[8 * i + 5]);
-    bf16x2_to_f32(x.w[i].w, v[8 * i + 6], v[8 * i + 7]);
-  }
-  const float g = tensor ? a.v_scale_g : a.k_scale_g;
-  uint4 codes;
-  const uint32_t s0 = quant_block16(v, g, codes.x, codes.y);
-  const uint32_t s1 = quant_block16(v + 16, g, codes.z, codes.w);
-  const int64_t page = x.slot >> 4, off = x.slot & 15;
-  const int64_t tok_row = (page * a.num_kv_heads + h) * kPageSize + off;
-  uint8_t* data = tensor ? a.v_data : a.k_data;
-  uint8_t* scale = tensor ? a.v_scale : a.k_scale;
-  *reinterpret_cast<uint4*>(data + tok_row * (kHeadDim / 2) + part * 16) = codes;
-  *reinterpret_cast<uint16_t*>(scale + tok_row * (kHeadDim / 16) + part * 2) = static_cast<uint16_t>(s0 | (s1 << 8));
+  float x[16];
+  bf16x2_to_f32(blk.lo.x, x[0], x[1]);
+  bf16x2_to_f32(blk.lo.y, x[2], x[3]);
+  bf16x2_to_f32(blk.lo.z, x[4], x[5]);
+  bf16x2_to_f32(blk.lo.w, x[6], x[7]);
+  bf16x2_to_f32(blk.hi.x, x[8], x[9]);
+  bf16x2_to_f32(blk.hi.y, x[10], x[11]);
+  bf16x2_to_f32(blk.hi.z, x[12], x[13]);
+  bf16x2_to_f32(blk.hi.w, x[14], x[15]);
+  uint32_t c0, c1;
+  const uint32_t sc = quant_block16(x, blk.tensor ? a.v_scale_g : a.k_scale_g, c0, c1);
+  const int h = blk.row - row_token(blk.row, a.row_magic) * a.num_kv_heads;
+  const int64_t tok_row = ((blk.slot >> 4) * a.num_kv_heads + h) * kPageSize + (blk.slot & 15);
+  const int b = lane & 7;
+  *reinterpret_cast<uint2*>((blk.tensor ? a.v_data : a.k_data) + tok_row * (kHeadDim / 2) + b * 8) = make_uint2(c0, c1);
+  (blk.tensor ? a.v_scale : a.k_scale)[tok_row * (kHeadDim / 16) + b] = static_cast<uint8_t>(sc);
 }
 
-// Grid-stride over all units of K then V, two units per thread per step so
-// that 128 B of loads per thread are in flight before any is consumed.
+}  // namespace
+
+// A warp's step covers four rows (of K, then of V); warps stride over the
+// steps with one block per lane in flight ahead of the one being encoded.
 __global__ void __launch_bounds__(256) nvfp4_kv_append_kernel(AppendArgs a) {
-  const int64_t per_tensor = a.num_tokens * a.num_kv_heads * 4;
-  const int64_t total = 2 * per_tensor;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; u + stride < total; u += 2 * stride) {
-    AppendUnit x0, x1;
-    append_load(a, u, per_tensor, x0);
-    append_load(a, u + stride, per_tensor, x1);
-    append_store(a, u, per_tensor, x0);
-    append_store(a, u + stride, per_tensor, x1);
+  const int64_t steps = (2 * a.num_tokens * a.num_kv_heads + 3) / 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  AppendBlock cur, next;
+  cur.tensor = -1;
+  if (w0 < steps) append_fetch(a, w0, lane, cur);
+  for (int64_t st = w0; st < steps; st += nw) {
+    next.tensor = -1;
+    if (st + nw < steps) append_fetch(a, st + nw, lane, next);
+    append_encode(a, cur, lane);
+    cur = next;
   }
-  if (u < total) {
-    AppendUnit x0;
-    append_load(a, u, per_tensor, x0);
-    append_store(a, u, per_tensor, x0);
+}
+
+// FP8 cache write (the comparison format: one E4M3 code per value and one
+// fp32 scale per tensor, "NVFP4 KV cache prefill vs decode performance",
+// section "A worked per-token cache estimate").  code = E4M3(x * (1/g)),
+// nearest even and saturating at 448 (hardware cvt), with 1/g the correctly
+// rounded reciprocal.  Same lane layout as the NVFP4 append: a lane encodes
+// 16 values of a row and writes 16 code bytes.
+__global__ void __launch_bounds__(256) fp8_kv_append_kernel(AppendArgs a) {
+  const int64_t steps = (2 * a.num_tokens * a.num_kv_heads + 3) / 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const float inv_k = __frcp_rn(a.k_scale_g), inv_v = __frcp_rn(a.v_scale_g);
+  AppendBlock cur, next;
+  cur.tensor = -1;
+  if (w0 < steps) append_fetch(a, w0, lane, cur);
+  for (int64_t st = w0; st < steps; st += nw) {
+    next.tensor = -1;
+    if (st + nw < steps) append_fetch(a, st + nw, lane, next);
+    if (cur.tensor >= 0 && cur.slot >= 0) {
+      if (cur.slot >= a.num_slots) {
+        set_status(a.status, kDevBadSlot);
+      } else {
+        const float inv = cur.tensor ? inv_v : inv_k;
+        const uint32_t w[8] = {cur.lo.x, cur.lo.y, cur.lo.z, cur.lo.w, cur.hi.x, cur.hi.y, cur.hi.z, cur.hi.w};
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float x0, x1, x2, x3;
+          bf16x2_to_f32(w[2 * i], x0, x1);
+          bf16x2_to_f32(w[2 * i + 1], x2, x3);
+          pk[i] = cvt_e4m3x2(__fmul_rn(x0, inv), __fmul_rn(x1, inv)) |
+                  (cvt_e4m3x2(__fmul_rn(x2, inv), __fmul_rn(x3, inv)) << 16);
+        }
+        const int h = cur.row - row_token(cur.row, a.row_magic) * a.num_kv_heads;
+        const int64_t tok_row = ((cur.slot >> 4) * a.num_kv_heads + h) * kPageSize + (cur.slot & 15);
+        *reinterpret_cast<uint4*>((cur.tensor ? a.v_data : a.k_data) + tok_row * kHeadDim + (lane & 7) * 16) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    cur = next;
   }
+}
+
+int append_ctas_per_sm() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nvfp4_kv_append_kernel, 256, 0) != cudaSuccess || n < 1)
+    return 1;
+  return n;
 }
 
 // Standalone quantizer (same codec; GLOBAL or PER_ROW scale).  One warp per

@@ -99,20 +99,29 @@ __device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t sc, uint32_t (&out)
 // than this (P <= 2^15 stays inside FP16)
 constexpr float kDecRescaleThreshold = 15.0f;
 
-constexpr int kUnit = kDecUnit;
-constexpr int kPagesPerUnit = kUnit / kPageSize;
-constexpr int kThrPerPage = 128 / kPagesPerUnit;  // gather threads per page
-constexpr int kSplitBytesK = kUnit * 64;
-constexpr int kSplitBytesS = kUnit * 8;
-constexpr int kStageBytes = 2 * (kSplitBytesK + kSplitBytesS);  // 36 KB: K, K scales, V, V scales
+// Per-format layout of a shared-memory stage.  NVFP4: 64 code bytes and 8
+// scale bytes per token row, 256-token units (K, K scales, V, V scales: 36 KB).
+// FP8: 128 code bytes per token row, 128-token units (K, V: 32 KB), each row's
+// 16-byte chunks XOR-swizzled by the row's low three bits so that the fragment
+// loads of a warp spread over the banks.
+template <bool FP8>
+struct DecFmt {
+  static constexpr int kUnit = FP8 ? 128 : 256;
+  static constexpr int kRow = FP8 ? 128 : 64;        // code bytes per token row
+  static constexpr int kBytesK = kUnit * kRow;
+  static constexpr int kBytesS = FP8 ? 0 : kUnit * 8;
+  static constexpr int kStage = 2 * (kBytesK + kBytesS);
+  static constexpr int kPagesPerUnit = kUnit / kPageSize;
+  static constexpr int kThrPerPage = 128 / kPagesPerUnit;  // gather threads per page
+  static constexpr int kSmem = 2 * kStage + 1024;          // two stages + alignment slack
+  // The four warps' partial O are merged through the stage just consumed:
+  // [warp][head][kRedRow] fp32, rows padded by two words (where they fit) so
+  // that the accumulator stores of a warp spread over the banks.
+  static constexpr int kRedRow = (kDecWarps * 16 * (kHeadDim + 2) * 4 <= kStage) ? kHeadDim + 2 : kHeadDim;
+  static_assert(kDecWarps * 16 * kRedRow * 4 <= kStage, "merge buffer fits one stage");
+  static_assert(kThrPerPage == 8 || kThrPerPage == 16, "gather split");
+};
 constexpr int kDecCtasPerSm = 3;
-constexpr int kDecSmem = 2 * kStageBytes + 1024;                 // two stages + alignment slack
-// The four warps' partial O are merged through the stage just consumed:
-// [warp][head][kRedRow] fp32, rows padded by two words so that the
-// accumulator stores of a warp spread over the banks.
-constexpr int kRedRow = kHeadDim + 2;
-static_assert(kDecWarps * 16 * kRedRow * 4 <= kStageBytes, "merge buffer fits one stage");
-static_assert(kThrPerPage == 8 || kThrPerPage == 16, "gather split");
 
 struct DecItem {
   int b, h, split, n_tok, n_units;
@@ -121,13 +130,14 @@ struct DecItem {
 // The schedule lists item records (request, kv head, split, tokens): full
 // 1024-token items first, then the shorter last splits.  CTAs claim records
 // in that order from a counter (sched[1]), so the short items fill the tail.
+template <bool FP8>
 __device__ __forceinline__ DecItem item_of(int4 r) {
   DecItem it;
   it.b = r.x;
   it.h = r.y;
   it.split = r.z;
   it.n_tok = r.w;
-  it.n_units = (r.w + kUnit - 1) / kUnit;
+  it.n_units = (r.w + DecFmt<FP8>::kUnit - 1) / DecFmt<FP8>::kUnit;
   return it;
 }
 
@@ -153,16 +163,21 @@ __device__ __forceinline__ void claim_item(const DecodeArgs& a, ClaimRing* ring)
   __syncthreads();
 }
 
-// Tokens of unit u of an item (at most 256 = 16 pages).
-__device__ __forceinline__ int unit_tokens(const DecItem& it, int u) { return min(kUnit, it.n_tok - u * kUnit); }
+// Tokens of unit u of an item (at most one unit).
+template <bool FP8>
+__device__ __forceinline__ int unit_tokens(const DecItem& it, int u) {
+  return min(DecFmt<FP8>::kUnit, it.n_tok - u * DecFmt<FP8>::kUnit);
+}
 
 // Raw page id of the page this thread gathers for unit u of an item (page
 // tid / 8 of the unit), or -1 past the unit.  Loaded one unit ahead so that
 // the global-load latency is off the path of the gather; checked there.
+template <bool FP8>
 __device__ __forceinline__ int unit_page(const DecodeArgs& a, const DecItem& it, int u, int tid) {
-  const int p = tid / kThrPerPage;
-  if (p * kPageSize >= unit_tokens(it, u)) return -1;
-  return a.page_table[static_cast<int64_t>(it.b) * a.max_pages + (it.split * kDecSplit + u * kUnit) / kPageSize + p];
+  const int p = tid / DecFmt<FP8>::kThrPerPage;
+  if (p * kPageSize >= unit_tokens<FP8>(it, u)) return -1;
+  return a.page_table[static_cast<int64_t>(it.b) * a.max_pages +
+                      (it.split * kDecSplit + u * DecFmt<FP8>::kUnit) / kPageSize + p];
 }
 
 // All 128 threads gather unit u of an item into `stage` with cp.async: thread
@@ -171,10 +186,42 @@ __device__ __forceinline__ int unit_page(const DecodeArgs& a, const DecItem& it,
 // and so do the V scales of tokens past the item's end -- their values are
 // then exactly 0 whatever codes the page holds.  Each thread arrives on `bar`
 // once its copies land.
+template <bool FP8>
 __device__ __forceinline__ void issue_unit(const DecodeArgs& a, const DecItem& it, int u, int pid, uint8_t* stage,
                                            uint64_t* bar, int* page_ok, int tid) {
+  using F = DecFmt<FP8>;
+  constexpr int kThrPerPage = F::kThrPerPage;
   const int p = tid / kThrPerPage, sub = tid % kThrPerPage;
-  const int n_tok = unit_tokens(it, u);
+  const int n_tok = unit_tokens<FP8>(it, u);
+  if constexpr (FP8) {
+    // FP8: thread t copies 8 of the 128 16-byte chunks of page t / 16 of K
+    // and of V.  Rows of tokens past the item's end, and pages with an
+    // invalid id (flagged), read as zeros: E4M3 has NaN codes, and a NaN V
+    // value would reach the output through a zero softmax weight.
+    if (p * kPageSize < n_tok) {
+      if (pid >= a.num_pages || pid < 0) {
+        if (sub == 0) set_status(a.status, kDevBadPage);
+        pid = -1;
+      }
+      if (sub == 0) page_ok[p] = pid >= 0;
+      const int live = pid >= 0 ? min(n_tok - p * kPageSize, kPageSize) : 0;
+      const int64_t row = (static_cast<int64_t>(pid >= 0 ? pid : 0) * a.num_kv_heads + it.h) * kPageSize;
+      const uint32_t sK = smem_u32(stage), sV = sK + F::kBytesK;
+      const uint8_t* gk = a.k_data + row * 128;
+      const uint8_t* gv = a.v_data + row * 128;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = sub + 16 * i;       // chunk of the page: token c / 8, piece c % 8
+        const int tok = c >> 3, r = p * kPageSize + tok;
+        const uint32_t n = tok < live ? 16u : 0u;
+        const uint32_t dst = r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        cp_async16(sK + dst, gk + c * 16, n);
+        cp_async16(sV + dst, gv + c * 16, n);
+      }
+    }
+    cp_async_mbar_arrive(bar);
+    return;
+  }
   if (p * kPageSize < n_tok) {
     if (pid >= a.num_pages || pid < 0) {
       if (sub == 0) set_status(a.status, kDevBadPage);
@@ -187,7 +234,7 @@ __device__ __forceinline__ void issue_unit(const DecodeArgs& a, const DecItem& i
     const int live = min(max(n_tok - p * kPageSize - 2 * ps, 0), 2);
     const uint32_t nvs = pid >= 0 ? 8u * live : 0u;
     const int64_t row = (static_cast<int64_t>(pid >= 0 ? pid : 0) * a.num_kv_heads + it.h) * kPageSize;
-    const uint32_t sK = smem_u32(stage), sKs = sK + kSplitBytesK, sV = sKs + kSplitBytesS, sVs = sV + kSplitBytesK;
+    const uint32_t sK = smem_u32(stage), sKs = sK + F::kBytesK, sV = sKs + F::kBytesS, sVs = sV + F::kBytesK;
     const uint8_t* gk = a.k_data + row * 64;
     const uint8_t* gv = a.v_data + row * 64;
 #pragma unroll
@@ -225,37 +272,41 @@ struct UnitCursor {
   bool has;
   DecItem it;
 };
+template <bool FP8>
 __device__ __forceinline__ void cursor_load(ClaimRing* ring, UnitCursor& c) {
   c.has = c.ci < ring->n_valid;
-  if (c.has) c.it = item_of(ring->rec[c.ci & 3]);
+  if (c.has) c.it = item_of<FP8>(ring->rec[c.ci & 3]);
 }
+template <bool FP8>
 __device__ __forceinline__ void cursor_start(const DecodeArgs& a, ClaimRing* ring, UnitCursor& c) {
   c.ci = 0;
   c.u = 0;
   claim_item(a, ring);
-  cursor_load(ring, c);
+  cursor_load<FP8>(ring, c);
 }
+template <bool FP8>
 __device__ __forceinline__ void cursor_next(const DecodeArgs& a, ClaimRing* ring, UnitCursor& c) {
   if (++c.u >= c.it.n_units) {
     c.u = 0;
     ++c.ci;
     if (!ring->done) claim_item(a, ring);  // uniform: ring->done is read after a barrier
-    cursor_load(ring, c);
+    cursor_load<FP8>(ring, c);
   }
 }
 
 // Persistent: CTAs claim items from the schedule.  Each item (up to 1024
-// tokens) streams through two shared-memory stages of 256 tokens, so the
-// copies of the next unit run while the current one is computed; the four
-// warps' partial results are merged once per item.
-template <int G>
-__global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(DecodeArgs a) {
+// tokens) streams through two shared-memory stages of one unit (256 tokens
+// of NVFP4, 128 of FP8), so the copies of the next unit run while the current
+// one is computed; the four warps' partial results are merged once per item.
+template <int G, bool FP8>
+__device__ __forceinline__ void decode_body(const DecodeArgs& a) {
+  using F = DecFmt<FP8>;
   constexpr bool kTwoRows = G > 8;  // MMA rows g+8 carry heads 8..15
   constexpr int kHeadBlocks = kTwoRows ? 2 : 1;
   extern __shared__ __align__(128) uint8_t dsmem_raw[];
   uint8_t* dsmem = dsmem_raw + ((128u - (smem_u32(dsmem_raw) & 127u)) & 127u);
   __shared__ uint64_t bars[2];
-  __shared__ int page_ok_sh[2][kPagesPerUnit];
+  __shared__ int page_ok_sh[2][F::kPagesPerUnit];
   __shared__ float red_m[kDecWarps][16], red_l[kDecWarps][16];
   __shared__ float mw[kDecWarps][16];   // merge weights exp2(m_w - m) / L per head
   __shared__ ClaimRing ring;
@@ -273,17 +324,18 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
   grid_dep_wait();    // the schedule written by the plan kernel
   // issue cursor: two units ahead of the compute
   UnitCursor ic;
-  cursor_start(a, &ring, ic);
+  cursor_start<FP8>(a, &ring, ic);
   for (int s = 0; s < 2 && ic.has; ++s) {
-    issue_unit(a, ic.it, ic.u, unit_page(a, ic.it, ic.u, tid), dsmem + s * kStageBytes, &bars[s], page_ok_sh[s], tid);
-    cursor_next(a, &ring, ic);
+    issue_unit<FP8>(a, ic.it, ic.u, unit_page<FP8>(a, ic.it, ic.u, tid), dsmem + s * F::kStage, &bars[s],
+                    page_ok_sh[s], tid);
+    cursor_next<FP8>(a, &ring, ic);
   }
   DecItem it;
   uint4 qr[2][4];
   bool q_ready = false;  // qr holds the query rows of the next item to compute
   uint32_t uc = 0;  // units consumed: stage uc & 1, phase (uc >> 1) & 1
   for (int k = 0; k < ring.n_valid; ++k) {
-    it = item_of(ring.rec[k & 3]);
+    it = item_of<FP8>(ring.rec[k & 3]);
     const int b = it.b, h = it.h;
     if (!q_ready) load_q_raw<G>(a, it, g, t, qr);
     q_ready = false;
@@ -340,17 +392,17 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
 
     for (int u = 0; u < it.n_units; ++u, ++uc) {
       const int stg = uc & 1;
-      uint8_t* sK = dsmem + stg * kStageBytes;
-      uint8_t* sKs = sK + kSplitBytesK;
-      uint8_t* sV = sKs + kSplitBytesS;
-      uint8_t* sVs = sV + kSplitBytesK;
+      uint8_t* sK = dsmem + stg * F::kStage;
+      uint8_t* sKs = sK + F::kBytesK;  // NVFP4 only
+      uint8_t* sV = sKs + F::kBytesS;
+      uint8_t* sVs = sV + F::kBytesK;  // NVFP4 only
       const int* page_ok = page_ok_sh[stg];
-      const int n_tok = unit_tokens(it, u);
+      const int n_tok = unit_tokens<FP8>(it, u);
       // the page this thread gathers for the unit issued after this one, and
       // the next item's query rows once that item is claimed
-      const int pid_next = ic.has ? unit_page(a, ic.it, ic.u, tid) : -1;
+      const int pid_next = ic.has ? unit_page<FP8>(a, ic.it, ic.u, tid) : -1;
       if (!q_ready && k + 1 < ring.n_valid) {
-        load_q_raw<G>(a, item_of(ring.rec[(k + 1) & 3]), g, t, qr);
+        load_q_raw<G>(a, item_of<FP8>(ring.rec[(k + 1) & 3]), g, t, qr);
         q_ready = true;
       }
       const bool ok = mbar_wait(&bars[stg], (uc >> 1) & 1, a.status);
@@ -365,7 +417,28 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
         float s[kHeadBlocks][4];
 #pragma unroll
         for (int nb = 0; nb < kHeadBlocks; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.0f;
-        {
+        if constexpr (FP8) {
+          // lane (g, t): 32 code bytes (head dims 32t .. 32t+31) of tokens g
+          // and g + 8; word j holds dims 32t + 4j + 0..3, whose halves are the
+          // A registers (k positions 2t, 2t+1 and 2t+8, 2t+9) of MMA j.  The
+          // per-tensor scale is part of the score scale.
+          const int tok0 = cbase + g, tok1 = tok0 + 8;
+          const int x0 = tok0 & 7, x1 = tok1 & 7;  // chunk swizzle of the rows
+          const uint4 k0a = *reinterpret_cast<const uint4*>(sK + tok0 * 128 + (((2 * t) ^ x0) << 4));
+          const uint4 k0b = *reinterpret_cast<const uint4*>(sK + tok0 * 128 + (((2 * t + 1) ^ x0) << 4));
+          const uint4 k1a = *reinterpret_cast<const uint4*>(sK + tok1 * 128 + (((2 * t) ^ x1) << 4));
+          const uint4 k1b = *reinterpret_cast<const uint4*>(sK + tok1 * 128 + (((2 * t + 1) ^ x1) << 4));
+          const uint32_t kw0[8] = {k0a.x, k0a.y, k0a.z, k0a.w, k0b.x, k0b.y, k0b.z, k0b.w};
+          const uint32_t kw1[8] = {k1a.x, k1a.y, k1a.z, k1a.w, k1b.x, k1b.y, k1b.z, k1b.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t a0 = cvt_e4m3x2_to_f16x2(kw0[j] & 0xFFFFu), a2 = cvt_e4m3x2_to_f16x2(kw0[j] >> 16);
+            const uint32_t a1 = cvt_e4m3x2_to_f16x2(kw1[j] & 0xFFFFu), a3 = cvt_e4m3x2_to_f16x2(kw1[j] >> 16);
+#pragma unroll
+            for (int nb = 0; nb < kHeadBlocks; ++nb)
+              mma_f16_16816(s[nb][0], s[nb][1], s[nb][2], s[nb][3], a0, a1, a2, a3, qb[nb][j][0], qb[nb][j][1]);
+          }
+        } else {
           const int tok0 = cbase + g, tok1 = tok0 + 8;
           const uint4 k0 = *reinterpret_cast<const uint4*>(sK + tok0 * 64 + 16 * t);
           const uint4 k1 = *reinterpret_cast<const uint4*>(sK + tok1 * 64 + 16 * t);
@@ -449,6 +522,26 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
         // r ^ ((r >> 1) & 1), so the four rows 2t + c of a load hit both
         // halves of the banks.
         uint32_t va[2][16];  // [pair][2j + e]: head dim 16g + 2j + e, j = 0..7
+        if constexpr (FP8) {
+          // FP8: 16 code bytes (head dims 16g .. 16g+15) of each token of the
+          // pair; byte i of token a and byte i of token b form one E4M3 pair,
+          // converted to the f16 pair (a, b) at head dim 16g + i.
+#pragma unroll
+          for (int tp = 0; tp < 2; ++tp) {
+            const int tok_a = cbase + 8 * tp + 2 * t, tok_b = tok_a + 1;
+            const uint4 ca = *reinterpret_cast<const uint4*>(sV + tok_a * 128 + ((g ^ (tok_a & 7)) << 4));
+            const uint4 cb = *reinterpret_cast<const uint4*>(sV + tok_b * 128 + ((g ^ (tok_b & 7)) << 4));
+            const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t lo = prmt(wa[w], wb[w], 0x5140u), hi = prmt(wa[w], wb[w], 0x7362u);
+              va[tp][4 * w + 0] = cvt_e4m3x2_to_f16x2(lo & 0xFFFFu);
+              va[tp][4 * w + 1] = cvt_e4m3x2_to_f16x2(lo >> 16);
+              va[tp][4 * w + 2] = cvt_e4m3x2_to_f16x2(hi & 0xFFFFu);
+              va[tp][4 * w + 3] = cvt_e4m3x2_to_f16x2(hi >> 16);
+            }
+          }
+        } else {
 #pragma unroll
         for (int tp = 0; tp < 2; ++tp) {
           const int tok_a = cbase + 8 * tp + 2 * t;
@@ -472,6 +565,7 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
             }
           }
         }
+        }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const uint32_t a0 = va[0][2 * mt], a1 = va[0][2 * mt + 1], a2 = va[1][2 * mt], a3 = va[1][2 * mt + 1];
@@ -492,7 +586,7 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
             l_run[nb][1] += __shfl_xor_sync(0xffffffffu, l_run[nb][1], o);
           }
         __syncthreads();  // every warp is done reading the stage
-        float* red_o = reinterpret_cast<float*>(sK);  // [warp][G][kRedRow]
+        float* red_o = reinterpret_cast<float*>(sK);  // [warp][G][F::kRedRow]
 #pragma unroll
         for (int r = 0; r < kHeadBlocks; ++r) {
           if (g == 0) {
@@ -505,10 +599,10 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
               const int d = 16 * g + 2 * mt;
-              float* o0 = red_o + (warp * G + 8 * r + 2 * t) * kRedRow;
+              float* o0 = red_o + (warp * G + 8 * r + 2 * t) * F::kRedRow;
               *reinterpret_cast<float2*>(o0 + d) = make_float2(acc[r][mt][0], acc[r][mt][2]);
               if (8 * r + 2 * t + 1 < G)
-                *reinterpret_cast<float2*>(o0 + kRedRow + d) = make_float2(acc[r][mt][1], acc[r][mt][3]);
+                *reinterpret_cast<float2*>(o0 + F::kRedRow + d) = make_float2(acc[r][mt][1], acc[r][mt][3]);
             }
           }
         }
@@ -544,7 +638,7 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
           const int head = i >> 7, d = i & 127;
           float on = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kDecWarps; ++w) on += red_o[(w * G + head) * kRedRow + d] * mw[w][head];
+          for (int w = 0; w < kDecWarps; ++w) on += red_o[(w * G + head) * F::kRedRow + d] * mw[w][head];
           const int hq = h * G + head;
           if (single) {
             reinterpret_cast<__nv_bfloat16*>(a.o)[(static_cast<int64_t>(b) * a.num_q_heads + hq) * kHeadDim + d] =
@@ -556,11 +650,20 @@ __global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(
       }
       __syncthreads();  // every thread is done with this stage
       if (ic.has) {
-        issue_unit(a, ic.it, ic.u, pid_next, dsmem + stg * kStageBytes, &bars[stg], page_ok_sh[stg], tid);
-        cursor_next(a, &ring, ic);
+        issue_unit<FP8>(a, ic.it, ic.u, pid_next, dsmem + stg * F::kStage, &bars[stg], page_ok_sh[stg], tid);
+        cursor_next<FP8>(a, &ring, ic);
       }
     }
   }
+}
+
+template <int G>
+__global__ void __launch_bounds__(128, kDecCtasPerSm) nvfp4_paged_decode_kernel(DecodeArgs a) {
+  decode_body<G, false>(a);
+}
+template <int G>
+__global__ void __launch_bounds__(128, kDecCtasPerSm) fp8_paged_decode_kernel(DecodeArgs a) {
+  decode_body<G, true>(a);
 }
 
 // Block-wide exclusive prefix sums of two counts (returns the exclusive
@@ -753,14 +856,15 @@ cudaError_t launch_dependent(void (*kernel)(DecodeArgs), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-template <int G>
+template <int G, bool FP8>
 cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s) {
   nvfp4_decode_plan_kernel<<<kPlanCtas, kPlanThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(nvfp4_paged_decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+  void (*kern)(DecodeArgs) = FP8 ? fp8_paged_decode_kernel<G> : nvfp4_paged_decode_kernel<G>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DecFmt<FP8>::kSmem);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(nvfp4_paged_decode_kernel<G>, dim3(num_sms * kDecCtasPerSm), dim3(128), kDecSmem, s, a);
+  e = launch_dependent(kern, dim3(num_sms * kDecCtasPerSm), dim3(128), DecFmt<FP8>::kSmem, s, a);
   if (e != cudaSuccess) return e;
   const size_t wbytes = static_cast<size_t>(a.max_splits) * sizeof(float);  // split weights
   if (wbytes > 48 * 1024) {
@@ -771,17 +875,26 @@ cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStr
   return launch_dependent(nvfp4_decode_combine_kernel, dim3(a.num_q_heads, batch), dim3(128), wbytes, s, a);
 }
 
+template <bool FP8>
+cudaError_t launch_decode_fmt(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s) {
+  switch (a.num_q_heads / a.num_kv_heads) {
+    case 1: return launch_decode_g<1, FP8>(a, batch, num_sms, s);
+    case 2: return launch_decode_g<2, FP8>(a, batch, num_sms, s);
+    case 4: return launch_decode_g<4, FP8>(a, batch, num_sms, s);
+    case 8: return launch_decode_g<8, FP8>(a, batch, num_sms, s);
+    case 16: return launch_decode_g<16, FP8>(a, batch, num_sms, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s) {
-  switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_decode_g<1>(a, batch, num_sms, s);
-    case 2: return launch_decode_g<2>(a, batch, num_sms, s);
-    case 4: return launch_decode_g<4>(a, batch, num_sms, s);
-    case 8: return launch_decode_g<8>(a, batch, num_sms, s);
-    case 16: return launch_decode_g<16>(a, batch, num_sms, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_decode_fmt<false>(a, batch, num_sms, s);
+}
+
+cudaError_t launch_decode_fp8(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s) {
+  return launch_decode_fmt<true>(a, batch, num_sms, s);
 }
 
 }  // namespace nvfp4kv

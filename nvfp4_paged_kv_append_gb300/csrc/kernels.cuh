@@ -25,6 +25,7 @@ struct AppendArgs {
   uint8_t* v_scale;
   float k_scale_g;
   float v_scale_g;
+  uint64_t row_magic;  // ceil(2^40 / num_kv_heads): row / Hkv as a multiply-shift
   int* status;
 };
 
@@ -129,15 +130,24 @@ int current_device_status();
 
 // Kernels (defined in append.cu, decode.cu, prefill.cu).
 __global__ void nvfp4_kv_append_kernel(AppendArgs a);
+int append_ctas_per_sm();  // resident CTAs of 256 threads per SM of the append kernel
+// FP8 cache write (same arguments; the scale pointers are unused, k_scale_g /
+// v_scale_g are the per-tensor FP8 scales)
+__global__ void fp8_kv_append_kernel(AppendArgs a);
 __global__ void nvfp4_quantize_rows_kernel(QuantArgs a);
 __global__ void nvfp4_dequantize_rows_kernel(DequantArgs a);
 
 // Launchers that hide templates (decode.cu / prefill.cu).
 cudaError_t launch_decode(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s);
+// The same over an FP8 cache (k_data / v_data hold E4M3 codes, 128 B per token row).
+cudaError_t launch_decode_fp8(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s);
 // Schedule (+ repack pre-pass) and the attention kernel, launched separately.
 cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s);
+// FP8 cache: schedule, repack of the FP8 pages into dequant-ahead records
+// (K BF16 | V FP16 per 128-key tile), then the dequant-ahead attention.
+cudaError_t launch_prefill_fp8(const PrefillArgs& a, const PlanArgs& plan, int num_sms, cudaStream_t s);
 // A4Q in repack mode: two CTAs per SM, 112-key tiles (prefill_a4q.cu).
 size_t prefill_a4q_2cta_record_bytes();
 int prefill_a4q_2cta_tile_keys();

@@ -714,6 +714,94 @@ __global__ void __launch_bounds__(128) nvfp4_prefill_repack_kernel(PrefillArgs a
 }
 
 // ---------------------------------------------------------------------------
+// FP8 (E4M3) cache, the pages' comparison format: the attention of the
+// dequant-ahead repack mode (BF16 QK with a BF16 query, FP16 PV) over records
+// converted once per (request, kv head, 128-key tile) from FP8 pages of 128
+// code bytes per token row.  Every E4M3 value is exact in FP16 and in BF16;
+// the per-tensor scales are applied as k_g (in the score scale) and v_g (in
+// the epilogue), as for NVFP4.
+__device__ __forceinline__ void fp8_group_to_16bit(uint4 w0, uint4 w1, bool bf16, uint32_t (&o0)[4],
+                                                   uint32_t (&o1)[4], uint32_t (&o2)[4], uint32_t (&o3)[4]) {
+  const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  uint32_t h[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h[2 * i] = cvt_e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+    h[2 * i + 1] = cvt_e4m3x2_to_f16x2(w[i] >> 16);
+  }
+  if (bf16) {
+    // f16 -> bf16 by moving the exponent field (value * 2^-112, exact for
+    // every E4M3 value), then * 2^112 in bf16 (exact)
+    const uint32_t two112 = 0x77807780u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint32_t a = ((h[i] & 0x7FFF7FFFu) >> 3) | (h[i] & 0x80008000u);
+      __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&two112));
+      h[i] = *reinterpret_cast<uint32_t*>(&r);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o0[i] = h[i];
+    o1[i] = h[4 + i];
+    o2[i] = h[8 + i];
+    o3[i] = h[12 + i];
+  }
+}
+
+__global__ void __launch_bounds__(128) fp8_prefill_repack_kernel(PrefillArgs a) {
+  using L = Layout<1, true>;
+  const int tid = threadIdx.x;
+  const int total = a.work[1];
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    int lo = 0, hi = a.batch - 1;  // last b with tile_prefix[b] * Hkv <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.tile_prefix[mid] * a.num_kv_heads <= t) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int n_t = a.tile_prefix[b + 1] - a.tile_prefix[b];
+    const int r = t - a.tile_prefix[b] * a.num_kv_heads;
+    const int h = r / n_t, j = r - h * n_t;
+    const int kv_len = a.kv_lens[b];
+    uint8_t* rec = a.repack + static_cast<int64_t>(t) * L::kStageBytes;
+    for (int tensor = 0; tensor < 2; ++tensor) {
+      const uint8_t* data = tensor ? a.v_data : a.k_data;
+      uint8_t* dst = rec + (tensor ? L::kStageV : 0u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int u = tid + 128 * i;
+        const int key = u >> 2, c = u & 3;
+        const int abs_key = j * kBN + key;
+        int64_t row = -1;
+        if (abs_key < kv_len) {
+          const int pid = a.page_table[static_cast<int64_t>(b) * a.max_pages + (abs_key >> 4)];
+          if (pid < 0 || pid >= a.num_pages) set_status(a.status, kDevBadPage);
+          else row = (static_cast<int64_t>(pid) * a.num_kv_heads + h) * kPageSize + (abs_key & 15);
+        }
+        uint32_t o0[4] = {0, 0, 0, 0}, o1[4] = {0, 0, 0, 0}, o2[4] = {0, 0, 0, 0}, o3[4] = {0, 0, 0, 0};
+        if (row >= 0) {
+          const uint4* src = reinterpret_cast<const uint4*>(data + row * kHeadDim + 32 * c);
+          fp8_group_to_16bit(src[0], src[1], tensor == 0, o0, o1, o2, o3);
+        }
+        uint8_t* d = dst + (c >> 1) * 16384;
+        const uint32_t cc = (c & 1) * 4;
+        *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 0)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+        *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 1)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 2)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+        *reinterpret_cast<uint4*>(d + sw128_off(key, cc + 3)) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+      }
+    }
+  }
+}
+
+// The dequant-ahead repack attention over records converted from FP8 pages
+// (named for the format so that a trace shows which cache ran).
+__global__ void __launch_bounds__(kThreads, 1) fp8_prefill_repack_sm103_kernel(const PrefillArgs a) {
+  prefill_body<1, true>(a);
+}
+
+// ---------------------------------------------------------------------------
 // schedule: items (request, q tile, kv head) sorted by decreasing KV-tile
 // count, and the per-request KV-tile prefix used by repack mode
 constexpr int kMaxCostBins = 4096;
@@ -854,6 +942,15 @@ cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int 
   if (variant == 0) return launch_prefill_a4q_2cta_repack(a, num_sms, s);
   nvfp4_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_fp8(const PrefillArgs& a, const PlanArgs& plan, int num_sms, cudaStream_t s) {
+  nvfp4_prefill_plan_kernel<<<1, 1024, 0, s>>>(plan);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fp8_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_main(fp8_prefill_repack_sm103_kernel, Layout<1, true>::kAlloc, a, num_sms, s);
 }
 
 cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s) {

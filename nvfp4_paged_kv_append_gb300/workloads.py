@@ -141,6 +141,14 @@ def global_scale(x: torch.Tensor) -> float:
     return float(g) if g > 0 else 1.0
 
 
+def fp8_scale(x: torch.Tensor) -> float:
+    """Per-tensor scale of the FP8 comparison cache: amax / 448 in float32,
+    so that the largest value lands on the largest finite E4M3 value."""
+    amax = x.float().abs().max()
+    g = (amax / torch.tensor(448.0, dtype=torch.float32)).item()
+    return float(g) if g > 0 else 1.0
+
+
 @dataclasses.dataclass
 class Inputs:
     wl: Workload

@@ -24,7 +24,7 @@ def nk():
 def header_functions():
     text = open(os.path.join(ROOT, "include", "nvfp4kv.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(nvfp4[a-z0-9_]*)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*((?:nvfp4|fp8)[a-z0-9_]*)\s*\(", text, flags=re.M)))
 
 
 def test_exports_every_declared_symbol(nk):
@@ -144,3 +144,28 @@ def test_header_and_library_from_plain_c(nk, tmp_path):
                     "-lnvfp4kv", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
+
+
+def test_fp8_host_entry_points(nk):
+    """FP8 comparison cache: the pages' per-token byte figure and host-side
+    argument checks (no GPU needed)."""
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "accounting.json")))["worked_per_token_L64"]
+    assert g["layers"] * nk.fp8_cache_bytes(1, 1, g["kv_heads"], g["head_dim"]) == g["fp8_bytes_per_token"]
+    lib = nk.lib
+    null = None
+    d = nk.Fp8CacheDesc(16, 32, 4, 16, 2, 128, 1.0, 1.0)
+    assert lib.fp8_kv_append(null, null, null, 0, ctypes.byref(d), null) == 0     # empty append is a no-op
+    assert lib.fp8_kv_append(null, null, null, 1, ctypes.byref(d), null) == -1    # null k/v
+    bad = nk.Fp8CacheDesc(16, 32, 4, 16, 2, 128, 0.0, 1.0)                       # zero scale
+    assert lib.fp8_kv_append(null, null, null, 0, ctypes.byref(bad), null) == -1
+    bad = nk.Fp8CacheDesc(16, 40, 4, 16, 2, 128, 1.0, 1.0)                       # misaligned pool
+    assert lib.fp8_kv_append(null, null, null, 0, ctypes.byref(bad), null) == -1
+    # prefill needs room for the converted tiles
+    ws_sched = nk.nvfp4_workspace_bytes(nk.OP_PREFILL, 1, 4, 2, 8, 0)
+    assert nk.fp8_workspace_bytes(nk.OP_PREFILL, 1, 4, 2, 8, 16) == ws_sched + 2 * 65536
+    assert nk.fp8_workspace_bytes(nk.OP_PREFILL, 1, 4, 2, 8, 0) == 0
+    args = lambda hq, ws_bytes: (16, 8, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, 16, null, 16, ws_bytes, null)
+    assert lib.fp8_paged_prefill(*args(3, 1 << 20)) == -1          # Hq not a multiple of Hkv
+    assert lib.fp8_paged_prefill(*args(4, ws_sched)) == -3         # schedule only: no room for the tiles
+    assert lib.fp8_paged_decode(16, 64, ctypes.byref(d), 16, 1, 16, 1, 0.1, 16, null, 16, 16, null) == -1
+    assert lib.fp8_paged_decode(16, 4, ctypes.byref(d), 16, 1, 16, 1, 0.1, 16, null, 16, 16, null) == -3
