@@ -129,15 +129,38 @@ int64_t prefill_max_items(int64_t total_q, int batch, int num_q_heads, int num_k
   return (static_cast<int64_t>((total_q * group + kBM - 1) / kBM) + batch) * num_kv_heads;
 }
 
-// Prefill workspace: [16 B header][items: 8 B each][unit prefix][tile prefix]
-// padded to 1 KB, then (repack mode) one record for every (request, kv head,
-// KV tile) the batch can hold: 64 KB per 128-key tile for the dequant-ahead
-// kernel, 37 KB per 112-key tile for the A4Q kernel.
+// Prefill workspace: [16 B header][items: 16 B each][unit prefix][tile
+// prefix][unit table: 16 B per unit, split KV only] padded to 1 KB, then
+// (repack mode) one record for every (request, kv head, KV tile) the batch can
+// hold: 64 KB per 128-key tile for the dequant-ahead kernel, 37 KB per 112-key
+// tile for the A4Q kernel; then (split KV) one partial slot per (unit, part).
 constexpr size_t kRepackRecordBytesDq = 65536;
 size_t prefill_repack_bytes(int variant, int batch, int num_kv_heads, int64_t max_kv_len);
-size_t prefill_sched_bytes(int64_t max_items, int batch) {
-  const size_t b = 16 + 8 * static_cast<size_t>(max_items) + 8 * (static_cast<size_t>(batch) + 1);
+int64_t units_table_offset(int64_t max_items, int batch) {  // in ints, 16-byte aligned
+  return (4 + 4 * max_items + 2 * (static_cast<int64_t>(batch) + 1) + 3) & ~int64_t(3);
+}
+size_t prefill_sched_bytes(int64_t max_units, int split, int batch) {
+  const int64_t max_items = max_units * split;
+  size_t b = 4 * static_cast<size_t>(units_table_offset(max_items, batch));
+  if (split > 1) b += 16 * static_cast<size_t>(max_units);
   return (b + 1023) & ~size_t(1023);
+}
+size_t prefill_part_bytes(int64_t max_units, int split) {
+  return split > 1 ? static_cast<size_t>(max_units) * split * kPartFloats * sizeof(float) : 0;
+}
+// Split KV: when the (request, q tile, kv head) units are fewer than the CTAs
+// of the attention kernel, each unit's KV range may be cut into parts (the
+// plan picks how many for the actual units); this is the most parts the
+// workspace is laid out for.  Workspace sizing assumes the kernels with one
+// CTA per SM on 152 SMs and 128-key tiles; with more SMs at run time the
+// split shrinks to what the workspace holds.
+constexpr int kSplitSizingCtas = 152;
+int split_cap(int64_t max_units, int64_t max_tiles, int ctas) {
+  if (max_units <= 0 || max_units >= ctas) return 1;
+  int64_t s = (4 * ctas + max_units - 1) / max_units;  // room for about four items per CTA
+  if (s > kMaxSplit) s = kMaxSplit;
+  if (s > max_tiles / kMinSplitTiles) s = max_tiles / kMinSplitTiles;
+  return s > 1 ? static_cast<int>(s) : 1;
 }
 size_t prefill_repack_tiles(int batch, int num_kv_heads, int64_t max_kv_len, int bn) {
   if (max_kv_len <= 0) return 0;
@@ -220,10 +243,11 @@ size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
   if (op == NVFP4KV_OP_PREFILL) {
     if (total_q < 0) return 0;
-    const int64_t items = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
+    const int64_t units = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
     const size_t a4q = prefill_repack_bytes(0, batch, num_kv_heads, max_kv_len);
     const size_t dq = prefill_repack_bytes(1, batch, num_kv_heads, max_kv_len);
-    return prefill_sched_bytes(items, batch) + (a4q > dq ? a4q : dq);
+    const int split = split_cap(units, max_kv_len > 0 ? (max_kv_len + kBN - 1) / kBN : 0, kSplitSizingCtas);
+    return prefill_sched_bytes(units, split, batch) + (a4q > dq ? a4q : dq) + prefill_part_bytes(units, split);
   }
   if (op == NVFP4KV_OP_DECODE) {
     if (max_kv_len < 0) return 0;
@@ -275,23 +299,38 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   if (batch == 0 || total_q == 0) return NVFP4KV_OK;
   if (!page_table || !kv_lens || !qo_indptr) return NVFP4KV_ERR_ARG;
   if ((stages & kStageRun) && (!q || !o || !aligned16(q) || !aligned16(o))) return NVFP4KV_ERR_ARG;
-  const int64_t max_items = prefill_max_items(total_q, batch, num_q_heads, c.num_kv_heads);
-  if (max_items >= (int64_t(1) << 30)) return NVFP4KV_ERR_ARG;
-  const size_t sched = prefill_sched_bytes(max_items, batch);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < sched) return NVFP4KV_ERR_WORKSPACE;
+  const int64_t max_units = prefill_max_items(total_q, batch, num_q_heads, c.num_kv_heads);
+  if (max_units >= (int64_t(1) << 30) / kMaxSplit) return NVFP4KV_ERR_ARG;
+  const int64_t max_kv = static_cast<int64_t>(max_pages_per_req) * kPageSize;
+  if (max_kv / prefill_a4q_2cta_tile_keys() >= 65535) return NVFP4KV_ERR_ARG;  // tile indices fit 16 bits
+  const size_t sched1 = prefill_sched_bytes(max_units, 1, batch);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < sched1) return NVFP4KV_ERR_WORKSPACE;
   // Repack mode (each V tile dequantized once, into the workspace) when the
   // workspace holds a tile for every (request, kv head, KV tile) the page
   // table allows and requests average at least two q tiles per kv head.
-  const size_t rbytes =
-      prefill_repack_bytes(variant, batch, c.num_kv_heads, static_cast<int64_t>(max_pages_per_req) * kPageSize);
+  const size_t rbytes = prefill_repack_bytes(variant, batch, c.num_kv_heads, max_kv);
   const int64_t qtiles = (total_q * (num_q_heads / c.num_kv_heads) + kBM - 1) / kBM;
-  bool repack = workspace_bytes >= sched + rbytes && qtiles >= 2 * static_cast<int64_t>(batch);
+  bool repack = workspace_bytes >= sched1 + rbytes && qtiles >= 2 * static_cast<int64_t>(batch);
   if (c.fp8) {
-    if (workspace_bytes < sched + rbytes) return NVFP4KV_ERR_WORKSPACE;
+    if (workspace_bytes < sched1 + rbytes) return NVFP4KV_ERR_WORKSPACE;
     repack = true;
   }
   DeviceState* d = nullptr;
   if ((rc = device_state(&d))) return rc;
+  // Split KV when the units are fewer than the attention kernel's CTAs and
+  // the workspace has room for the partial results -- for the kernels with
+  // one CTA per SM.  (On the two-CTA A4Q kernel of repack mode, measured on
+  // 4 x 128 queries over 2K keys, the split items' prologues and the merge
+  // cost more than the parallelism gained: 61 against 54 us.)
+  const int bn = prefill_tile_keys(variant, repack);
+  const bool two_cta = repack && variant == NVFP4KV_VARIANT_A4Q && !c.fp8;
+  const int ctas = d->num_sms;
+  int split = two_cta ? 1 : split_cap(max_units, (max_kv + bn - 1) / bn, ctas);
+  while (split > 1 && workspace_bytes < prefill_sched_bytes(max_units, split, batch) + (repack ? rbytes : 0) +
+                                            prefill_part_bytes(max_units, split))
+    --split;
+  const int64_t max_items = max_units * split;
+  const size_t sched = prefill_sched_bytes(max_units, split, batch);
 
   PlanArgs plan;
   plan.kv_lens = kv_lens;
@@ -302,9 +341,14 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   plan.num_kv_heads = c.num_kv_heads;
   plan.log2_group = lg;
   plan.causal = causal;
-  plan.bn = prefill_tile_keys(variant, repack);
+  plan.bn = bn;
+  plan.split = split;
+  plan.ctas = ctas;
   plan.work = static_cast<int*>(workspace);
+  plan.max_units = static_cast<int>(max_units);
   plan.max_items = static_cast<int>(max_items);
+  plan.units = split > 1 ? reinterpret_cast<int4*>(static_cast<int*>(workspace) + units_table_offset(max_items, batch))
+                         : nullptr;
   plan.status = d->status;
 
   PrefillArgs a;
@@ -332,15 +376,23 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   a.o = o;
   a.lse = lse;
   a.work = static_cast<const int*>(workspace);
-  a.tile_prefix = static_cast<const int*>(workspace) + 4 + 2 * max_items + (batch + 1);
+  a.tile_prefix = static_cast<const int*>(workspace) + 4 + 4 * max_items + (batch + 1);
+  a.units = plan.units;
   a.repack = repack ? static_cast<uint8_t*>(workspace) + sched : nullptr;
+  a.part = split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sched + (repack ? rbytes : 0))
+                     : nullptr;
+  a.split = split;
+  a.max_units = static_cast<int>(max_units);
   a.status = d->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (c.fp8) return launch_rc(launch_prefill_fp8(a, plan, d->num_sms, st));  // plan + repack + attention
+  if (c.fp8) return launch_rc(launch_prefill_fp8(a, plan, d->num_sms, st));  // plan + repack + attention (+ merge)
   if (stages & kStagePlan) {
     if ((rc = launch_rc(launch_prefill_plan(a, plan, variant, repack, d->num_sms, st)))) return rc;
   }
-  if (stages & kStageRun) return launch_rc(launch_prefill_attend(a, variant, repack, d->num_sms, st));
+  if (stages & kStageRun) {
+    if ((rc = launch_rc(launch_prefill_attend(a, variant, repack, d->num_sms, st)))) return rc;
+    if (split > 1) return launch_rc(launch_prefill_merge(a, st));
+  }
   return NVFP4KV_OK;
 }
 
@@ -450,8 +502,10 @@ size_t fp8_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int32
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
   if (op == NVFP4KV_OP_PREFILL) {
     if (total_q < 0 || max_kv_len <= 0) return 0;
-    const int64_t items = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
-    return prefill_sched_bytes(items, batch) + prefill_repack_bytes(1, batch, num_kv_heads, max_kv_len);
+    const int64_t units = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
+    const int split = split_cap(units, (max_kv_len + kBN - 1) / kBN, kSplitSizingCtas);
+    return prefill_sched_bytes(units, split, batch) + prefill_repack_bytes(1, batch, num_kv_heads, max_kv_len) +
+           prefill_part_bytes(units, split);
   }
   return nvfp4_workspace_bytes(op, batch, num_q_heads, num_kv_heads, total_q, max_kv_len);
 }

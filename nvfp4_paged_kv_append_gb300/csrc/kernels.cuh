@@ -103,11 +103,25 @@ struct PrefillArgs {
   float q_g;        // A4Q query scale: 0 = per row (amax/2688), > 0 = this scale for every row
   void* o;          // bf16 [total_q][Hq][128]
   float* lse;       // optional [total_q][Hq]
-  const int* work;  // [0] item count, [1] repacked tile count; items (int2) from work + 4
+  const int* work;  // [0] item count, [1] repacked tile count, [2] unit count; items (int4) from work + 4
   const int* tile_prefix;  // [batch+1] per-request KV-tile prefix (repack mode)
+  const int4* units;       // split > 1: per unit (request, q tile << 8 | kv head, parts, 0)
   uint8_t* repack;         // repack mode: one record per (request, kv head, KV tile)
+  float* part;             // split > 1: kPartFloats per partial slot (unit * split + part)
+  int split;               // most KV parts per unit (1: no split)
+  int max_units;           // bound on the number of units (grid of the merge)
   int* status;
 };
+
+// Split KV: at most kMaxSplit parts per unit, each of at least kMinSplitTiles
+// KV tiles.
+constexpr int kMaxSplit = 16;
+constexpr int kMinSplitTiles = 4;
+
+// A split item writes its unnormalized O (fp32, relative to its running max),
+// running max (log2 units) and running sum into one partial slot:
+// O [128 rows][128] | m [128] | l [128].
+constexpr int kPartFloats = kBM * kHeadDim + 2 * kBM;
 
 struct PlanArgs {
   const int32_t* kv_lens;
@@ -119,8 +133,12 @@ struct PlanArgs {
   int log2_group;
   int causal;
   int bn;     // keys per KV tile of the attention kernel the schedule is for
+  int split;  // most KV parts per (request, q tile, kv head) unit (1: no split)
+  int ctas;   // CTAs of the attention kernel (the plan picks the parts for them)
   int* work;  // output schedule
-  int max_items;
+  int max_units;  // bound on the units (request, q tile, kv head)
+  int max_items;  // max_units * split: room for items in the schedule
+  int4* units;  // split > 1: unit table for the merge
   int* status;
 };
 
@@ -145,6 +163,8 @@ cudaError_t launch_decode_fp8(const DecodeArgs& a, int batch, int num_sms, cudaS
 cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int variant, bool repack, int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s);
+// Split KV: merge the partial results of units split into several items.
+cudaError_t launch_prefill_merge(const PrefillArgs& a, cudaStream_t s);
 // FP8 cache: schedule, repack of the FP8 pages into dequant-ahead records
 // (K BF16 | V FP16 per 128-key tile), then the dequant-ahead attention.
 cudaError_t launch_prefill_fp8(const PrefillArgs& a, const PlanArgs& plan, int num_sms, cudaStream_t s);

@@ -148,7 +148,7 @@ __device__ void loader_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bar
   const int p = t >> 3, sub = t & 7;
   uint32_t it_ctr = 0;
   Item item;
-  for (int round = 0; get_item<kBN>(a, round, item); ++round) {
+  for (int round = 0; get_item(a, round, item); ++round) {
     for (int j = 0; j < item.n_tiles; ++j, ++it_ctr) {
       const uint32_t st = it_ctr % L::kStages, ph = (it_ctr / L::kStages) & 1u;
       uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
@@ -156,12 +156,12 @@ __device__ void loader_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bar
         if (t == 0) {
           if (!mbar_wait(&bars.kv_empty[st], ph ^ 1u, a.status)) return;
           mbar_arrive_expect_tx(&bars.kv_full[st], L::kStageBytes);
-          bulk_load(stage, a.repack + repack_index(a, item.b, item.kvh, j) * L::kStageBytes, L::kStageBytes,
+          bulk_load(stage, a.repack + repack_index(a, item.b, item.kvh, item.t0 + j) * L::kStageBytes, L::kStageBytes,
                     &bars.kv_full[st]);
         }
       } else {
         int pid = -1;
-        const int page_idx = j * kPagesPerTile + p;
+        const int page_idx = (item.t0 + j) * kPagesPerTile + p;
         if (page_idx * kPageSize < item.kv_len) {
           pid = a.page_table[static_cast<int64_t>(item.b) * a.max_pages + page_idx];
           if (pid < 0 || pid >= a.num_pages) {
@@ -218,7 +218,7 @@ __device__ void qk_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
   const uint32_t idesc_qk = L::kA4Q ? idesc_mxf4nvf4(128, 128) : idesc_f16(128, 128, 1, 1, 0, 0);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
-  for (int round = 0; get_item<kBN>(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
     if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
     for (int j = 0; j < item.n_tiles; ++j) {
       const uint32_t it = it_ctr + j;
@@ -269,7 +269,7 @@ __device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
   const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
-  for (int round = 0; get_item<kBN>(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
     for (int j = 0; j < item.n_tiles; ++j) {
       const uint32_t it = it_ctr + j;
       const uint32_t st = it % L::kStages, b = it & 1u, ph = (it >> 1) & 1u;
@@ -305,7 +305,7 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
   uint2* sfa_stage = reinterpret_cast<uint2*>(smem + L::kOffSfaStage);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
-  for (int round = 0; get_item<kBN>(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
     // The previous item's Q tile, Q block scales and row scales must be
     // consumed (last QK issued and finished; softmax has read its row scales)
     // before they are overwritten.  Waiting on both also keeps the softmax
@@ -360,7 +360,7 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
         const uint32_t st = it % L::kStages, b = it & 1u;
         if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
         const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
-        const int key_base = j * kBN;
+        const int key_base = (item.t0 + j) * kBN;
         if constexpr (!L::kA4Q) {
           // K -> BF16 (exact), K-major 128B-swizzled operand; buffer b was
           // read by QK(it-2)
@@ -436,7 +436,7 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
     tc_fence_after();
     return ok;
   };
-  for (int round = 0; get_item<kBN>(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
     if (!mbar_wait_warp(bars.q_full, item_ctr & 1u, a.status)) return;
     const int tq = item.tok0 + (r >> lg);
     const bool valid = (r >> lg) < item.n_tok;
@@ -462,7 +462,7 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.s_free[b]);
       float* s = reinterpret_cast<float*>(sr);
-      const int key0 = j * kBN + 64 * half;
+      const int key0 = (item.t0 + j) * kBN + 64 * half;
       // Keys past the row's last visible one are masked (scale applied here);
       // unmasked halves fold the scale into the exponent's FMA below.
       const bool masked = key0 + 63 > limit;
@@ -544,12 +544,23 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
     const float inv_l = (l_run > 0.0f) ? a.v_g / l_run : 0.0f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) +
                           (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim + 64 * half;
+    float* prow = item.part >= 0 ? part_slot(a, item) : nullptr;  // split item: partial O, m, l
+    if (prow && half == 0) {
+      prow[kBM * kHeadDim + r] = m_run;
+      prow[kBM * kHeadDim + kBM + r] = l_run;
+    }
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
       uint32_t ov[32];
       tmem_ld32(lane_base + ocol + 32 * c, ov);
       tmem_wait_ld();
-      if (valid) {
+      if (prow) {
+        float4* dst = reinterpret_cast<float4*>(prow + r * kHeadDim + 64 * half + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                               __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+      } else if (valid) {
         uint32_t pb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -563,7 +574,7 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
         dst[3] = make_uint4(pb[12], pb[13], pb[14], pb[15]);
       }
     }
-    if (half == 0 && valid && a.lse)
+    if (!prow && half == 0 && valid && a.lse)
       a.lse[static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq] =
           (l_run > 0.0f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
     tc_fence_before();
@@ -835,7 +846,7 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
   __shared__ int hist[kMaxCostBins];
   __shared__ int warp_sums[32];
   const int tid = threadIdx.x;
-  int* prefix = a.work + 4 + 2 * a.max_items;  // [batch + 1] unit prefix
+  int* prefix = a.work + 4 + 4 * a.max_items;  // [batch + 1] unit prefix (after the int4 items)
   int* tprefix = prefix + a.batch + 1;         // [batch + 1] KV-tile prefix
   const int tpq_shift = 7 - a.log2_group;      // log2(tokens per q tile)
   for (int i = tid; i < kMaxCostBins; i += blockDim.x) hist[i] = 0;
@@ -866,18 +877,21 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
     __syncthreads();
   }
   int total = carry;
-  if (total > a.max_items) {  // cannot happen when qo_indptr is non-decreasing
+  if (total > a.max_units) {  // cannot happen when qo_indptr is non-decreasing
     set_status(a.status, kDevBadShape);
-    total = a.max_items;
+    total = a.max_units;
   }
   if (tid == 0) {
     prefix[a.batch] = total;
     tprefix[a.batch] = tcarry;
-    a.work[0] = total;
     a.work[1] = tcarry * a.num_kv_heads;
+    a.work[2] = total;
   }
+  __shared__ int n_items;
+  if (tid == 0) n_items = 0;
   __syncthreads();
-  auto cost_of = [&](int u, int& b, int& qt, int& kvh) -> int {
+  // unit u -> (request, q tile, kv head) and its KV tile count
+  auto unit_of = [&](int u, int& b, int& qt, int& kvh) -> int {
     int lo = 0, hi = a.batch - 1;  // last b with prefix[b] <= u
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -891,14 +905,43 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
     const int tok0 = qt << tpq_shift;
     const int n_tok = min(1 << tpq_shift, q_len - tok0);
     const int last_key = a.causal ? kv_len - q_len + tok0 + n_tok - 1 : kv_len - 1;
-    return min(last_key / a.bn + 1, kMaxCostBins - 1);
+    return last_key / a.bn + 1;
   };
-  // 2) histogram of costs
-  for (int u = tid; u < total; u += blockDim.x) {
-    int b, qt, kvh;
-    atomicAdd(&hist[cost_of(u, b, qt, kvh)], 1);
+  // Split KV: a unit of n tiles becomes min(split, n) items over contiguous
+  // tile ranges (the part p of `parts` covers tiles n*p/parts .. n*(p+1)/parts - 1)
+  // The number of parts S (at most a.split) minimizes the estimated makespan
+  // ceil(units * S / ctas) / S of equal units on the kernel's CTAs; a unit is
+  // cut into at most S parts of at least kMinSplitTiles tiles.
+  __shared__ int s_split;
+  if (tid == 0) {
+    int best = 1;
+    float best_t = static_cast<float>((total + a.ctas - 1) / max(a.ctas, 1));
+    for (int sp = 2; sp <= a.split; ++sp) {
+      const float t_sp = static_cast<float>((total * sp + a.ctas - 1) / a.ctas) / sp;
+      if (t_sp < best_t * 0.999f) {
+        best = sp;
+        best_t = t_sp;
+      }
+    }
+    s_split = best;
   }
   __syncthreads();
+  const int split = s_split;
+  auto parts_of = [&](int n) { return split > 1 ? min(split, max(1, n / kMinSplitTiles)) : 1; };
+  // 2) histogram of item costs (tiles per item) and the item count
+  for (int u = tid; u < total; u += blockDim.x) {
+    int b, qt, kvh;
+    const int n = unit_of(u, b, qt, kvh);
+    const int parts = parts_of(n);
+    for (int p = 0; p < parts; ++p) {
+      const int cost = (n * (p + 1)) / parts - (n * p) / parts;
+      atomicAdd(&hist[min(cost, kMaxCostBins - 1)], 1);
+    }
+    atomicAdd(&n_items, parts);
+    if (a.split > 1) a.units[u] = make_int4(b, (qt << 8) | kvh, parts, n);
+  }
+  __syncthreads();
+  if (tid == 0) a.work[0] = min(n_items, a.max_items);
   // 3) exclusive offsets, largest cost first: thread t owns 4 bins from the top
   constexpr int kPer = kMaxCostBins / 1024;
   int v[kPer], sum = 0;
@@ -914,14 +957,69 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
     run += v[i];
   }
   __syncthreads();
-  // 4) scatter the items
-  int2* items = reinterpret_cast<int2*>(a.work + 4);
+  // 4) scatter the items: (request, q tile << 8 | kv head, first tile |
+  // tiles << 16, partial slot or -1)
+  int4* items = reinterpret_cast<int4*>(a.work + 4);
   for (int u = tid; u < total; u += blockDim.x) {
     int b, qt, kvh;
-    const int c = cost_of(u, b, qt, kvh);
-    const int pos = atomicAdd(&hist[c], 1);
-    items[pos] = make_int2(b, (qt << 8) | kvh);
+    const int n = unit_of(u, b, qt, kvh);
+    const int parts = parts_of(n);
+    for (int p = 0; p < parts; ++p) {
+      const int t0 = (n * p) / parts, cnt = (n * (p + 1)) / parts - t0;
+      const int pos = atomicAdd(&hist[min(cnt, kMaxCostBins - 1)], 1);
+      if (pos < a.max_items)
+        items[pos] = make_int4(b, (qt << 8) | kvh, t0 | (cnt << 16), parts > 1 ? u * a.split + p : -1);
+    }
   }
+}
+
+// Split KV: merge the partial results of every unit that was split into
+// several items.  One warp per row (16 rows per CTA), four head dimensions per
+// lane: M = max_p m_p, w_p = 2^(m_p - M), O = sum_p w_p O_p / sum_p w_p l_p,
+// times the V tensor scale (log-sum-exp combination in the log2 domain).
+constexpr int kMergeRowsPerCta = 16;
+__global__ void __launch_bounds__(32 * kMergeRowsPerCta) nvfp4_prefill_merge_kernel(PrefillArgs a) {
+  const int u = blockIdx.x;
+  if (u >= a.work[2]) return;
+  const int4 info = a.units[u];
+  const int parts = info.z;
+  if (parts <= 1) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.y * kMergeRowsPerCta + warp;
+  const int b = info.x, qt = info.y >> 8, kvh = info.y & 255;
+  const int G = a.group, lg = a.log2_group;
+  const int q_start = a.qo_indptr[b], q_len = a.qo_indptr[b + 1] - q_start;
+  const int tok0 = qt * (kBM >> lg);
+  const int n_rows = min(kBM >> lg, q_len - tok0) << lg;
+  if (r >= n_rows) return;
+  const float* base = a.part + static_cast<int64_t>(u) * a.split * kPartFloats;
+  // lane p < parts holds part p's running max and sum
+  const float mp = lane < parts ? base[lane * kPartFloats + kBM * kHeadDim + r] : -INFINITY;
+  const float lp = lane < parts ? base[lane * kPartFloats + kBM * kHeadDim + kBM + r] : 0.0f;
+  float m = mp;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float mu = (m == -INFINITY) ? 0.0f : m;
+  const float wp = lane < parts ? fast_exp2(mp - mu) : 0.0f;  // 0 for a part with no visible key
+  float L = wp * lp;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = 0; p < parts; ++p) {
+    const float w = __shfl_sync(0xffffffffu, wp, p);
+    const float4 o4 = reinterpret_cast<const float4*>(base + p * kPartFloats + r * kHeadDim)[lane];
+    acc.x += w * o4.x;
+    acc.y += w * o4.y;
+    acc.z += w * o4.z;
+    acc.w += w * o4.w;
+  }
+  const float sc = L > 0.0f ? a.v_g / L : 0.0f;
+  const int tq = tok0 + (r >> lg), hq = kvh * G + (r & (G - 1));
+  const int64_t orow = static_cast<int64_t>(q_start + tq) * a.num_q_heads + hq;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * sc, acc.y * sc), hi = __floats2bfloat162_rn(acc.z * sc, acc.w * sc);
+  reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.o) + orow * kHeadDim)[lane] =
+      make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  if (lane == 0 && a.lse) a.lse[orow] = (L > 0.0f) ? (mu + __log2f(L)) * kLn2 : -INFINITY;
 }
 
 template <typename K>
@@ -950,7 +1048,14 @@ cudaError_t launch_prefill_fp8(const PrefillArgs& a, const PlanArgs& plan, int n
   if (e != cudaSuccess) return e;
   fp8_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return launch_main(fp8_prefill_repack_sm103_kernel, Layout<1, true>::kAlloc, a, num_sms, s);
+  if ((e = launch_main(fp8_prefill_repack_sm103_kernel, Layout<1, true>::kAlloc, a, num_sms, s)) != cudaSuccess)
+    return e;
+  return a.split > 1 ? launch_prefill_merge(a, s) : cudaSuccess;
+}
+
+cudaError_t launch_prefill_merge(const PrefillArgs& a, cudaStream_t s) {
+  nvfp4_prefill_merge_kernel<<<dim3(a.max_units, kBM / kMergeRowsPerCta), 32 * kMergeRowsPerCta, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s) {

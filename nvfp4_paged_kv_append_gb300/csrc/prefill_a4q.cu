@@ -130,7 +130,7 @@ __device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, 
   const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   uint32_t it = 0, item_ctr = 0;
   Item item;
-  for (int round = 0; get_item<kBN2>(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
     if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
     // prologue: both halves of tile 0
     uint32_t stage_s = smem_u32(smem + kOffStage2 + (it % kStages2) * kRecord2);
@@ -179,12 +179,12 @@ __device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, 
 __device__ __forceinline__ void load_thread(const PrefillArgs& a, uint8_t* smem, const Bars2& bars) {
   uint32_t it = 0;
   Item item;
-  for (int round = 0; get_item<kBN2>(a, round, item); ++round) {
+  for (int round = 0; get_item(a, round, item); ++round) {
     for (int j = 0; j < item.n_tiles; ++j, ++it) {
       const uint32_t st = it % kStages2;
       if (!mbar_wait(&bars.kv_empty[st], ((it / kStages2) & 1u) ^ 1u, a.status)) return;
       mbar_arrive_expect_tx(&bars.kv_full[st], kRecord2);
-      bulk_load(smem + kOffStage2 + st * kRecord2, a.repack + repack_index(a, item.b, item.kvh, j) * kRecord2,
+      bulk_load(smem + kOffStage2 + st * kRecord2, a.repack + repack_index(a, item.b, item.kvh, item.t0 + j) * kRecord2,
                 kRecord2, &bars.kv_full[st]);
     }
   }
@@ -194,7 +194,7 @@ __device__ __forceinline__ void load_thread(const PrefillArgs& a, uint8_t* smem,
 // running max and sum.  Returns false when a wait timed out.
 template <int h>
 __device__ __forceinline__ bool softmax_half(const PrefillArgs& a, const Bars2& bars, uint32_t lane_base, int lane,
-                                             int j, uint32_t it, int limit, float c_r, float& m_run,
+                                             int j, int jt, uint32_t it, int limit, float c_r, float& m_run,
                                              float2 (&lacc)[4]) {
   constexpr int kMaxKeys = 64;
   constexpr int nk = half_keys(h);
@@ -207,7 +207,7 @@ __device__ __forceinline__ bool softmax_half(const PrefillArgs& a, const Bars2& 
   else tmem_ld16(s_addr + 32, *reinterpret_cast<uint32_t(*)[16]>(&sr[32]));
   tmem_wait_ld();
   float* s = reinterpret_cast<float*>(sr);
-  const int key0 = j * kBN2 + 64 * h;
+  const int key0 = jt * kBN2 + 64 * h;  // jt: the tile's index in the request
   // On a half with masked keys the kept scores are scaled here, so that a
   // zero row scale (an all-zero query row, or a row past the request) never
   // multiplies -inf
@@ -287,7 +287,7 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
   const uint32_t lane_base = tmem_addr(tbase, 32 * quad, 0);
   uint32_t it = 0, item_ctr = 0;
   Item item;
-  for (int round = 0; get_item<kBN2>(a, round, item); ++round, ++item_ctr) {
+  for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
     const int tq = item.tok0 + (r >> lg);
     const bool valid = (r >> lg) < item.n_tok;
     const int hq = item.kvh * G + (r & (G - 1));
@@ -325,8 +325,8 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
     float m_run = -INFINITY;
     float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
     for (int j = 0; j < item.n_tiles; ++j, ++it) {
-      if (!softmax_half<0>(a, bars, lane_base, lane, j, it, limit, c_r, m_run, lacc)) return;
-      if (!softmax_half<1>(a, bars, lane_base, lane, j, it, limit, c_r, m_run, lacc)) return;
+      if (!softmax_half<0>(a, bars, lane_base, lane, j, item.t0 + j, it, limit, c_r, m_run, lacc)) return;
+      if (!softmax_half<1>(a, bars, lane_base, lane, j, item.t0 + j, it, limit, c_r, m_run, lacc)) return;
     }
     // ---- epilogue: O * v_scale / l -------------------------------------------
     const float l_run = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y) + (lacc[2].x + lacc[2].y) +
@@ -336,12 +336,23 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
     const float inv_l = (l_run > 0.0f) ? a.v_g / l_run : 0.0f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) +
                           (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim;
+    float* prow = item.part >= 0 ? part_slot(a, item) : nullptr;  // split item: partial O, m, l
+    if (prow) {
+      prow[kBM * kHeadDim + r] = m_run;
+      prow[kBM * kHeadDim + kBM + r] = l_run;
+    }
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t ov[32];
       tmem_ld32(lane_base + kColO2 + 32 * c, ov);
       tmem_wait_ld();
-      if (valid) {
+      if (prow) {
+        float4* dst = reinterpret_cast<float4*>(prow + r * kHeadDim + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                               __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+      } else if (valid) {
         uint32_t pb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -356,7 +367,7 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
         dst[3] = make_uint4(pb[12], pb[13], pb[14], pb[15]);
       }
     }
-    if (valid && a.lse)
+    if (!prow && valid && a.lse)
       a.lse[static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq] =
           (l_run > 0.0f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
     tc_fence_before();

@@ -12,33 +12,42 @@ constexpr float kLn2 = 0.6931471805599453f;
 // exceeds it by more than this, so P stays <= 2^15, inside FP16's range.
 constexpr float kRescaleThreshold = 15.0f;
 
+// A work item: one (request, q tile, kv head) unit over KV tiles t0 ..
+// t0 + n_tiles - 1 (all of the unit's tiles unless the unit is split), and the
+// partial slot it writes (-1: the item covers the unit and writes the output).
 struct Item {
   int b, qt, kvh;
   int q_start, q_len, kv_len;
-  int tok0, n_tok, n_tiles;
+  int tok0, n_tok;
+  int t0, n_tiles, part;
 };
 
-// Items are sorted by decreasing cost; CTAs take them in snake order.  BN is
-// the kernel's keys per KV tile.
-template <int BN>
+// Items are sorted by decreasing cost; CTAs take them in snake order.
 __device__ __forceinline__ bool get_item(const PrefillArgs& a, int round, Item& it) {
   const int n_items = a.work[0];
   const int grid = gridDim.x;
   const int idx = round * grid + ((round & 1) ? (grid - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
   if (idx >= n_items) return false;
-  const int2 w = reinterpret_cast<const int2*>(a.work + 4)[idx];
+  const int4 w = reinterpret_cast<const int4*>(a.work + 4)[idx];
   it.b = w.x;
   it.qt = w.y >> 8;
   it.kvh = w.y & 255;
+  it.t0 = w.z & 0xFFFF;
+  it.n_tiles = w.z >> 16;
+  it.part = w.w;
   it.q_start = a.qo_indptr[it.b];
   it.q_len = a.qo_indptr[it.b + 1] - it.q_start;
   it.kv_len = a.kv_lens[it.b];
   const int tpq = kBM >> a.log2_group;
   it.tok0 = it.qt * tpq;
   it.n_tok = min(tpq, it.q_len - it.tok0);
-  const int last_key = a.causal ? it.kv_len - it.q_len + it.tok0 + it.n_tok - 1 : it.kv_len - 1;
-  it.n_tiles = last_key / BN + 1;
   return true;
+}
+
+// Epilogue of a split item: row r's unnormalized O (32 columns starting at
+// col), and its running max (log2 units) and sum.
+__device__ __forceinline__ float* part_slot(const PrefillArgs& a, const Item& it) {
+  return a.part + static_cast<int64_t>(it.part) * kPartFloats;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -178,3 +178,12 @@ def test_fp8_decode_full_size_all_requests():
     mx, fro, lerr, _ = _decode(W.decode_batch())
     assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
     assert lerr <= 1e-3
+
+
+def test_fp8_prefill_split_kv():
+    """FP8 prefill with few units over long KV (the KV range is split and
+    merged): every row against the oracle."""
+    wl = W.Workload("fp8_split", [5, 40], [3000, 2500], 8, 2, seed=23)
+    inp = W.make_inputs(wl)
+    got, lse = _prefill(inp, gpu_fp8_cache(inp, fill=0x7F))
+    _check(got, lse, oracle_fp8_attention(oracle_fp8_pools(inp), inp), inp)

@@ -243,3 +243,29 @@ def test_prefill_query_scale_schemes(cfg, scheme, mode):
     mx, fro, n = G.compare_rows(o.float().cpu().numpy(), ref, inp.qo_indptr)
     assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro, n)
     assert G.compare_lse(lse.cpu().numpy(), ref, inp.qo_indptr) <= 2e-3
+
+
+SPLIT_CASES = [
+    # (name, q_lens, kv_lens, Hq, Hkv, causal): fewer (request, q tile, kv
+    # head) units than the kernel's CTAs, long KV: the KV range is split
+    ("split_g4_causal", [5, 40], [3000, 2500], 8, 2, True),
+    ("split_g1_noncausal", [3, 17], [1800, 2200], 2, 2, False),
+    ("split_g16_causal", [2, 9], [2600, 1500], 32, 2, True),
+    ("split_g4_repack", [300, 260], [2600, 2300], 8, 2, True),   # repack mode (>= 2 q tiles per kv head)
+]
+
+
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+def test_prefill_split_kv(case, variant, q_mode):
+    """Few work units over long KV ranges: with room in the workspace each
+    unit's KV range is cut into parts merged by log-sum-exp; every row
+    against the oracle, and the same rows without the split (schedule-only
+    workspace) agree with it too."""
+    name, ql, kl, hq, hkv, causal = case
+    inp = W.make_inputs(W.Workload(name, ql, kl, hq, hkv, causal=causal, seed=len(name)))
+    cache = G.gpu_cache(inp, fill=0x7F)
+    pools = G.oracle_pools(inp)
+    ref = G.oracle_prefill(pools, inp, q_mode, causal=causal)
+    _check(inp, cache, pools, variant, q_mode, causal=causal, mode="auto", ref=ref)
+    _check(inp, cache, pools, variant, q_mode, causal=causal, mode="inkernel", ref=ref)
