@@ -141,11 +141,10 @@ __device__ __forceinline__ uint2 quantize_q_row(const uint4* src, bool valid, ui
     }
   }
   g_row = q_g != 0.0f ? q_g : __fdiv_rn(amax, 2688.0f);
-  uint32_t sc[8];
+  uint32_t sw0 = 0u, sw1 = 0u;  // the eight scale bytes, k-step 0 and 1 (kept in registers)
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t cw[4] = {0u, 0u, 0u, 0u};
-    sc[2 * c] = sc[2 * c + 1] = 0u;
     if (valid && g_row != 0.0f) {
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
@@ -159,13 +158,15 @@ __device__ __forceinline__ uint2 quantize_q_row(const uint4* src, bool valid, ui
         bf16x2_to_f32(v1.y, x[10], x[11]);
         bf16x2_to_f32(v1.z, x[12], x[13]);
         bf16x2_to_f32(v1.w, x[14], x[15]);
-        sc[2 * c + blk] = quant_block16(x, g_row, cw[2 * blk], cw[2 * blk + 1]);
+        const uint32_t sc = quant_block16(x, g_row, cw[2 * blk], cw[2 * blk + 1]);
+        const uint32_t sh = 8u * ((2 * c + blk) & 3);
+        if (c < 2) sw0 |= sc << sh;
+        else sw1 |= sc << sh;
       }
     }
     *reinterpret_cast<uint4*>(qtile + sw64_off(r, c)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
   }
-  return make_uint2(sc[0] | (sc[1] << 8) | (sc[2] << 16) | (sc[3] << 24),
-                    sc[4] | (sc[5] << 8) | (sc[6] << 16) | (sc[7] << 24));
+  return make_uint2(sw0, sw1);
 }
 
 }  // namespace prefill_detail
