@@ -23,6 +23,13 @@ Parity status per function:
   decode_q_a4q with a single caller-given scale (per-tensor or single-level
   query scheme) -- the GLOBAL mode of the cache's block codec, pinned by the
   codec pins and an exact round trip.
+  FP4 PV experiment (v_token_major_page, gather_v_token_major,
+  fp4pv_attention_rows, paged_attention(pv="fp4")) -- the pages define no
+  FP4 PV, so its readings X1..X5 are this oracle's own; pinned by the
+  re-layout's axis against numpy reductions, closed forms (uniform and
+  one-hot attention), its distance to the exact attention, and the
+  reference-independence that X3 promises (tile size and threshold change
+  nothing but rounding).
   quantize_rows(mode=PER_ROW), the per-row A4Q Q scheme -- the pages leave
   the scheme open, so it is pinned only to its stated reading (round trip and
   error bound), not to any external value: parity unpinned against the pages.
@@ -108,6 +115,8 @@ def _load():
         lib.orc_fp8_gather_decode.argtypes = [P, P, i32, i32, i32, i32, i32, i64, f32, P]
         lib.orc_fp8_cache_bytes.restype = i64
         lib.orc_fp8_cache_bytes.argtypes = [i64, i32, i32, i32]
+        lib.orc_v_token_major_page.argtypes = [P, i32, P, P]
+        lib.orc_fp4pv_attention_rows.argtypes = [P, P, i32, i32, P, P, i32, i32, i32, f64, i32, i32, f32, P, P]
         _lib = lib
     return _lib
 
@@ -321,6 +330,73 @@ def cache_bytes(num_pages: int, page_size: int, Hkv: int, D: int) -> int:
     return int(_load().orc_cache_bytes(num_pages, page_size, Hkv, D))
 
 
+# --- FP4 PV experiment (readings X1..X5 in nvfp4_oracle.h) ---------------------
+
+FP4PV_TILE = 128
+FP4PV_TAU = 4
+
+
+def fp4pv_p_scale(tau: int = FP4PV_TAU) -> float:
+    """X4: g_p = fl32(2^tau / 2688)."""
+    return float(np.float32(2.0 ** tau) / np.float32(2688.0))
+
+
+def v_token_major_page(x16):
+    """X1 for one page: x16 [16, D] values (decoded without g) -> codes
+    [D, 8] uint8 (slot 2i in the low nibble of byte i) and scales [D] uint8."""
+    x = _f32(x16)
+    assert x.shape[0] == 16
+    D = x.shape[1]
+    codes = np.zeros((D, 8), np.uint8)
+    scales = np.zeros(D, np.uint8)
+    _load().orc_v_token_major_page(_ptr(x), D, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def decode_token_major(codes, scales, g: float) -> np.ndarray:
+    """Decode one page's token-major blocks: [D, 8] codes and [D] scales ->
+    [16, D] float64 values e2m1 * e4m3 * g (X1, R5)."""
+    codes = np.asarray(codes, np.uint8)
+    e2m1 = np.array([e2m1_value(c) for c in range(16)])
+    e4m3 = np.array([e4m3_value(b) for b in range(256)])
+    nib = np.stack([codes & 15, codes >> 4], axis=2).reshape(codes.shape[0], 16)  # [D, slot]
+    return (e2m1[nib] * e4m3[np.asarray(scales, np.uint8)][:, None] * float(np.float32(g))).T
+
+
+def gather_v_token_major(pools: Pools, page_row, kv_len: int, head: int, v_g: float) -> np.ndarray:
+    """X1 over a request: the first kv_len tokens of V for one kv head,
+    re-coded page by page along tokens (slots past kv_len taken as 0) and
+    decoded.  Returns [kv_len, D] float64."""
+    raw = gather_decode(pools, "v", page_row, kv_len, head, 1.0)  # e2m1 * e4m3, exact
+    n_pages = -(-kv_len // 16)
+    buf = np.zeros((n_pages * 16, pools.D), np.float32)
+    buf[:kv_len] = raw
+    out = np.zeros((n_pages * 16, pools.D), np.float64)
+    for p in range(n_pages):
+        codes, scales = v_token_major_page(buf[16 * p:16 * p + 16])
+        out[16 * p:16 * p + 16] = decode_token_major(codes, scales, v_g)
+    return out[:kv_len]
+
+
+def fp4pv_attention_rows(q, pos, q_len: int, k, vhat, causal: bool, sm_scale: float,
+                         tile: int = FP4PV_TILE, tau: int = FP4PV_TAU):
+    """X2..X5 for rows of one (request, q-head): q [n, D] decoded queries,
+    k [kv_len, D] decoded keys, vhat [kv_len, D] token-major V decoded by X1.
+    Returns (o [n, D] f64, lse [n] f64)."""
+    assert tile > 0 and tile % 16 == 0
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    vhat = np.ascontiguousarray(vhat, dtype=np.float64)
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    n, D = q.shape
+    out = np.zeros((n, D), np.float64)
+    lse = np.zeros(n, np.float64)
+    _load().orc_fp4pv_attention_rows(_ptr(q), _ptr(pos), n, q_len, _ptr(k), _ptr(vhat), k.shape[0], D,
+                                     int(bool(causal)), float(sm_scale), int(tile), int(tau),
+                                     fp4pv_p_scale(tau), _ptr(out), _ptr(lse))
+    return out, lse
+
+
 def decode_q_a4q(q_rows, q_scale: float = 0.0) -> np.ndarray:
     """A4Q query as the kernel sees it, quantized then decoded (R6, R5).
     q_scale 0: per-row dual-level scale (R6); q_scale > 0: that one scale for
@@ -336,16 +412,19 @@ def decode_q_a4q(q_rows, q_scale: float = 0.0) -> np.ndarray:
 
 def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_g: float,
                     v_g: float, causal: bool, sm_scale: float, q_mode: str = "bf16",
-                    rows=None, q_scale: float = 0.0):
+                    rows=None, q_scale: float = 0.0, pv: str = "wide"):
     """Attention of a ragged batch over the paged cache (an NVFP4 `Pools` or
     an FP8 `FP8Pools`, decoded by R5 or F3).
 
     q: [total_q, Hq, D] float32 (bf16 values); q_mode "bf16" uses q as is,
     "a4q" uses the quantized-then-decoded query (per-row scale, or the single
     scale q_scale when it is > 0).  rows: optional list of (request, position)
-    pairs to evaluate (all rows of every request if None).
+    pairs to evaluate (all rows of every request if None).  pv "wide" is the
+    definition (P and V exact); "fp4" is the FP4 PV experiment (X1..X5, NVFP4
+    pools only).
     Returns dict {(request, position): (o [Hq, D], lse [Hq])}.
     """
+    assert pv in ("wide", "fp4") and (pv == "wide" or isinstance(pools, Pools))
     q = _f32(q)
     qo = np.asarray(qo_indptr, dtype=np.int64)
     kvl = np.asarray(kv_lens, dtype=np.int64)
@@ -370,9 +449,11 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
         q_len, kv_len = int(qo[b + 1] - qo[b]), int(kvl[b])
         pos_all = np.array(sorted(set(positions)), np.int32)
         gather = fp8_gather_decode if isinstance(pools, FP8Pools) else gather_decode
+        gather_v = (lambda h: gather_v_token_major(pools, pt[b], kv_len, h, v_g)) if pv == "fp4" else \
+            (lambda h: gather(pools, "v", pt[b], kv_len, h, v_g))
+        attend = fp4pv_attention_rows if pv == "fp4" else attention_rows
         dec = dict(zip(range(Hkv), _pmap(
-            lambda h: (gather(pools, "k", pt[b], kv_len, h, k_g),
-                       gather(pools, "v", pt[b], kv_len, h, v_g)), range(Hkv))))
+            lambda h: (gather(pools, "k", pt[b], kv_len, h, k_g), gather_v(h)), range(Hkv))))
         n_chunks = max(1, min(len(pos_all), -(-2 * WORKERS // Hkv)))
         chunks = [c for c in np.array_split(pos_all, n_chunks) if len(c)]
 
@@ -384,7 +465,7 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
                 hq = h * G + gq
                 qr = q[qo[b] + pos, hq, :]
                 qd = decode_q_a4q(qr, q_scale) if q_mode == "a4q" else qr.astype(np.float64)
-                res.append((hq,) + attention_rows(qd, pos, q_len, kd, vd, causal, sm_scale))
+                res.append((hq,) + attend(qd, pos, q_len, kd, vd, causal, sm_scale))
             return pos, res
 
         for i in pos_all:

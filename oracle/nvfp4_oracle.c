@@ -297,3 +297,80 @@ int orc_fp8_gather_decode(const uint8_t* data, const int32_t* page_row, int kv_l
 int64_t orc_fp8_cache_bytes(int64_t num_pages, int page_size, int Hkv, int D) {
   return 2 * num_pages * (int64_t)page_size * Hkv * (int64_t)D;
 }
+
+/* X1 ([A4Q] "Why NVFP4 KV cache A4Q prefill exists": the cache's V scales
+ * follow the head dimension while PV reduces over tokens).  One block per
+ * head dimension d: the page's 16 slots at d, coded by R1..R4 with g = 1. */
+void orc_v_token_major_page(const float* x, int D, uint8_t* codes,
+                            uint8_t* scales) {
+  float block[16];
+  for (int d = 0; d < D; ++d) {
+    for (int t = 0; t < 16; ++t) block[t] = x[(int64_t)t * D + d];
+    orc_quantize_block16(block, 1.0f, codes + 8 * (int64_t)d, scales + d);
+  }
+}
+
+/* X2..X5 ([A4Q] "Compare A4Q with dequantize-ahead repacking": A4Q keeps a
+ * wide PV; this is the FP4 alternative, P coded by the cache's block codec
+ * against a whole-number running reference). */
+void orc_fp4pv_attention_rows(const double* q, const int32_t* pos, int n_rows,
+                              int q_len, const double* k, const double* vhat,
+                              int kv_len, int D, int causal, double sm_scale,
+                              int tile, int tau, float g_p, double* out,
+                              double* lse) {
+  const double log2e = 1.0 / log(2.0);
+  int n = kv_len > 0 ? kv_len : 1;
+  double* s = (double*)malloc(sizeof(double) * (size_t)n);
+  double* m_of = (double*)malloc(sizeof(double) * (size_t)(n / tile + 1));
+  for (int r = 0; r < n_rows; ++r) {
+    const double* qr = q + (int64_t)r * D;
+    double* o = out + (int64_t)r * D;
+    int last = causal ? kv_len - q_len + pos[r] : kv_len - 1; /* R7 */
+    if (last > kv_len - 1) last = kv_len - 1;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (last < 0) {
+      if (lse) lse[r] = -INFINITY;
+      continue;
+    }
+    /* X2 */
+    for (int j = 0; j <= last; ++j) {
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qr[d] * k[(int64_t)j * D + d];
+      s[j] = sm_scale * log2e * dot;
+    }
+    /* X3: the reference each tile is coded against */
+    int n_tiles = last / tile + 1;
+    double m = -INFINITY;
+    for (int t = 0; t < n_tiles; ++t) {
+      double mt = -INFINITY;
+      for (int j = t * tile; j < (t + 1) * tile && j <= last; ++j)
+        if (s[j] > mt) mt = s[j];
+      if (mt > m + (double)tau) m = ceil(mt);
+      m_of[t] = m;
+    }
+    double m_end = m;
+    double l = 0.0;
+    for (int j = 0; j <= last; ++j) l += exp2(s[j] - m_end);
+    /* X4, X5 */
+    for (int b0 = 0; b0 <= last; b0 += 16) {
+      int t = b0 / tile;
+      float p[16];
+      uint8_t packed[8], sc;
+      for (int i = 0; i < 16; ++i) {
+        int j = b0 + i;
+        p[i] = (j <= last) ? (float)exp2(s[j] - m_of[t]) : 0.0f;
+      }
+      orc_quantize_block16(p, g_p, packed, &sc);
+      double w = exp2(m_of[t] - m_end) * orc_e4m3_value(sc) * (double)g_p;
+      for (int i = 0; i < 16 && b0 + i <= last; ++i) {
+        unsigned code = (packed[i / 2] >> (4 * (i % 2))) & 15u; /* R4 */
+        double ph = w * orc_e2m1_value(code);
+        for (int d = 0; d < D; ++d) o[d] += ph * vhat[(int64_t)(b0 + i) * D + d];
+      }
+    }
+    for (int d = 0; d < D; ++d) o[d] /= l;
+    if (lse) lse[r] = (m_end + log2(l)) * log(2.0);
+  }
+  free(m_of);
+  free(s);
+}

@@ -57,6 +57,35 @@
  *                    negative value that rounds to zero keeps its sign (0x80).
  *   F3 layout        data [page][kv_head][page_size][D] bytes, slots as R8;
  *                    decode x = e4m3(byte) * g, exact in fp64.
+ *
+ * The FP4 PV experiment ("NVFP4 KV cache A4Q prefill explained", sections
+ * "Why NVFP4 KV cache A4Q prefill exists" and "Compare A4Q with
+ * dequantize-ahead repacking": the cache's V block scales run along the head
+ * dimension, not along the token axis that PV reduces over, so the pages keep
+ * PV wide).  The pages define no FP4 PV; these readings define the one built
+ * here:
+ *   X1 token-major V one block per (page, kv head, head dim d): the page's 16
+ *                    slots of V at d, decoded by R5 without g (e2m1 * e4m3,
+ *                    exact) with slots at or past the request's kv_len taken
+ *                    as 0, coded by R1..R4 with g = 1 (slot 2i in the low
+ *                    nibble).  Decoded value: e2m1 * e4m3 * v_g.
+ *   X2 scores        s_j = sm_scale * log2(e) * <q, k_j> (log2 units), q the
+ *                    A4Q query (R6 or a given scale), k_j by R5.
+ *   X3 reference     keys in tiles of T (keys T*t .. T*t+T-1 of the
+ *                    request); a reference m starts at -inf; a tile whose
+ *                    largest visible score mt exceeds m + tau sets
+ *                    m = ceil(mt); tile t is coded against the m in force
+ *                    after its own update (m_t).  m is a whole number, so two
+ *                    references differ by a power of two.
+ *   X4 P codes       p_j = fl32(2^(s_j - m_t)) for visible keys, 0 for the
+ *                    others; every 16 keys from a multiple of 16 are one
+ *                    block coded by R1..R4 with g = g_p; p <= 2^tau, so
+ *                    g_p = fl32(2^tau / 2688) keeps the block scale unsaturated.
+ *   X5 output        o = sum_j 2^(m_t(j) - m_end) * phat_j * vhat_j / l with
+ *                    l = sum_j 2^(s_j - m_end) (unquantized p),
+ *                    lse = (m_end + log2 l) * ln 2; a row that sees no key
+ *                    has o = 0 and lse = -inf.
+ *                    The kernel takes T = 128 and tau = 4.
  */
 #ifndef NVFP4_ORACLE_H
 #define NVFP4_ORACLE_H
@@ -127,6 +156,23 @@ int orc_fp8_gather_decode(const uint8_t* data, const int32_t* page_row, int kv_l
                           int head, int Hkv, int D, int page_size, int64_t num_pages,
                           float g, double* out);
 int64_t orc_fp8_cache_bytes(int64_t num_pages, int page_size, int Hkv, int D);
+
+/* X1: the token-major blocks of one page of V.  x: [16][D] values of the
+ * page's 16 slots (already decoded without g; zero rows for slots past
+ * kv_len).  Writes codes [D][8] (slot 2i in the low nibble of byte i) and
+ * scales [D]. */
+void orc_v_token_major_page(const float* x, int D, uint8_t* codes,
+                            uint8_t* scales);
+
+/* X2..X5: attention with FP4 P and the token-major V, for selected query
+ * rows of one (request, q-head).  q: [n_rows][D] decoded A4Q queries, k:
+ * [kv_len][D] decoded keys, vhat: [kv_len][D] token-major V decoded by X1
+ * (v_g included).  tile = T, tau as in X3, g_p as in X4. */
+void orc_fp4pv_attention_rows(const double* q, const int32_t* pos, int n_rows,
+                              int q_len, const double* k, const double* vhat,
+                              int kv_len, int D, int causal, double sm_scale,
+                              int tile, int tau, float g_p, double* out,
+                              double* lse);
 
 /* Cache bytes for one layer's K and V pools ([PD] "A worked per-token cache
  * estimate"): 2 * pages * page_size * Hkv * (D/2 + D/16). */

@@ -124,3 +124,67 @@ def test_fp8_truncation_and_dropped_sign_are_caught(orc):
 
     _fails(P8.test_fp8_encode_matches_torch_cast, Mutant(orc, fp8_encode_array=truncate))
     _fails(P8.test_fp8_encode_matches_torch_cast, Mutant(orc, fp8_encode_array=unsigned))
+
+
+def _fp4pv_rows(orc, ceil_ref=True, weight=True):
+    """X2..X5 written out in numpy on the oracle's block codec, with one step
+    that can be planted wrong: a fractional reference (no ceil), or the
+    2^(m_t - m_end) weight of earlier tiles dropped."""
+    def rows(q, pos, q_len, k, vhat, causal, sm_scale, tile=128, tau=4):
+        g_p = orc.fp4pv_p_scale(tau)
+        e2m1 = np.array([orc.e2m1_value(c) for c in range(16)])
+        out, lse = np.zeros((len(pos), k.shape[1])), np.zeros(len(pos))
+        for r, i in enumerate(pos):
+            last = k.shape[0] - q_len + int(i) if causal else k.shape[0] - 1
+            s = sm_scale * (k[: last + 1] @ q[r]) / math.log(2.0)
+            m, refs = -math.inf, []
+            for t in range(last // tile + 1):
+                mt = s[t * tile:(t + 1) * tile].max()
+                if mt > m + tau:
+                    m = math.ceil(mt) if ceil_ref else mt
+                refs.append(m)
+            l = np.exp2(s - m).sum()
+            o = np.zeros(k.shape[1])
+            for b0 in range(0, last + 1, 16):
+                n = min(16, last + 1 - b0)
+                p = np.zeros(16, np.float32)
+                p[:n] = np.exp2(s[b0:b0 + n] - refs[b0 // tile])
+                packed, sc = orc.quantize_block16(p, g_p)
+                codes = np.stack([packed & 15, packed >> 4], axis=1).ravel()[:n]
+                w = (2.0 ** (refs[b0 // tile] - m) if weight else 1.0) * orc.e4m3_value(sc) * g_p
+                o += (w * e2m1[codes]) @ vhat[b0:b0 + n]
+            out[r], lse[r] = o / l, (m + math.log2(l)) * math.log(2.0)
+        return out, lse
+    return rows
+
+
+def test_fp4pv_planted_mistakes_are_caught(orc):
+    """FP4 PV (readings X1..X5): an unquantized P, a fractional reference, a
+    dropped weight of earlier tiles, and a V re-layout that keeps the cache's
+    own axis each fail their pin."""
+    from . import test_oracle_fp4pv as P4
+    # the numpy restatement passes the pins it is planted into
+    P4.test_fp4pv_independent_of_tiling_and_threshold(Mutant(orc, fp4pv_attention_rows=_fp4pv_rows(orc)))
+
+    def unquantized(q, pos, q_len, k, vhat, causal, sm_scale, tile=128, tau=4):
+        return orc.attention_rows(q, pos, q_len, k, vhat, causal, sm_scale)
+
+    _fails(P4.test_fp4pv_close_to_exact_but_quantized, Mutant(orc, fp4pv_attention_rows=unquantized))
+    _fails(P4.test_fp4pv_independent_of_tiling_and_threshold,
+           Mutant(orc, fp4pv_attention_rows=_fp4pv_rows(orc, ceil_ref=False)))
+    _fails(P4.test_fp4pv_independent_of_tiling_and_threshold,
+           Mutant(orc, fp4pv_attention_rows=_fp4pv_rows(orc, weight=False)))
+
+    def cache_axis(x16):
+        """Blocks along the head dimension of each slot (the cache's axis),
+        codes then read out per dimension: the scale of dimension d is that of
+        slot 0's block holding d."""
+        x = np.asarray(x16, np.float32)
+        packed, scales, _ = orc.quantize_rows(x, orc.GLOBAL, 1.0)     # [16, D/2], [16, D/16]
+        D = x.shape[1]
+        nib = np.stack([packed & 15, packed >> 4], axis=2).reshape(16, D)  # [slot, d]
+        codes = (nib[0::2].T | (nib[1::2].T << 4)).astype(np.uint8)       # [D, 8]
+        return codes, scales[0][np.arange(D) // 16].astype(np.uint8)
+
+    _fails(P4.test_token_major_scales_follow_tokens, Mutant(orc, v_token_major_page=cache_axis))
+    _fails(P4.test_token_major_round_trip_on_grid, Mutant(orc, v_token_major_page=cache_axis))
