@@ -116,7 +116,8 @@ def _load():
         lib.orc_fp8_cache_bytes.restype = i64
         lib.orc_fp8_cache_bytes.argtypes = [i64, i32, i32, i32]
         lib.orc_v_token_major_page.argtypes = [P, i32, P, P]
-        lib.orc_fp4pv_attention_rows.argtypes = [P, P, i32, i32, P, P, i32, i32, i32, f64, i32, i32, f32, P, P]
+        lib.orc_fp4pv_attention_rows.argtypes = [P, P, i32, i32, P, P, i32, i32, i32, f64, i32, i32, f32, f64,
+                                                 P, P, P]
         _lib = lib
     return _lib
 
@@ -379,10 +380,12 @@ def gather_v_token_major(pools: Pools, page_row, kv_len: int, head: int, v_g: fl
 
 
 def fp4pv_attention_rows(q, pos, q_len: int, k, vhat, causal: bool, sm_scale: float,
-                         tile: int = FP4PV_TILE, tau: int = FP4PV_TAU):
+                         tile: int = FP4PV_TILE, tau: int = FP4PV_TAU, eps=None):
     """X2..X5 for rows of one (request, q-head): q [n, D] decoded queries,
     k [kv_len, D] decoded keys, vhat [kv_len, D] token-major V decoded by X1.
-    Returns (o [n, D] f64, lse [n] f64)."""
+    Returns (o [n, D] f64, lse [n] f64), and with eps given also the slack
+    [n, D]: how far o can move when P decisions within relative eps of a
+    rounding boundary go the other way."""
     assert tile > 0 and tile % 16 == 0
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
@@ -391,10 +394,12 @@ def fp4pv_attention_rows(q, pos, q_len: int, k, vhat, causal: bool, sm_scale: fl
     n, D = q.shape
     out = np.zeros((n, D), np.float64)
     lse = np.zeros(n, np.float64)
+    slack = np.zeros((n, D), np.float64) if eps is not None else None
     _load().orc_fp4pv_attention_rows(_ptr(q), _ptr(pos), n, q_len, _ptr(k), _ptr(vhat), k.shape[0], D,
                                      int(bool(causal)), float(sm_scale), int(tile), int(tau),
-                                     fp4pv_p_scale(tau), _ptr(out), _ptr(lse))
-    return out, lse
+                                     fp4pv_p_scale(tau), float(eps or 0.0), _ptr(out), _ptr(lse),
+                                     _ptr(slack) if slack is not None else None)
+    return (out, lse) if eps is None else (out, lse, slack)
 
 
 def decode_q_a4q(q_rows, q_scale: float = 0.0) -> np.ndarray:
@@ -412,7 +417,7 @@ def decode_q_a4q(q_rows, q_scale: float = 0.0) -> np.ndarray:
 
 def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_g: float,
                     v_g: float, causal: bool, sm_scale: float, q_mode: str = "bf16",
-                    rows=None, q_scale: float = 0.0, pv: str = "wide"):
+                    rows=None, q_scale: float = 0.0, pv: str = "wide", slack_eps=None):
     """Attention of a ragged batch over the paged cache (an NVFP4 `Pools` or
     an FP8 `FP8Pools`, decoded by R5 or F3).
 
@@ -421,9 +426,11 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
     scale q_scale when it is > 0).  rows: optional list of (request, position)
     pairs to evaluate (all rows of every request if None).  pv "wide" is the
     definition (P and V exact); "fp4" is the FP4 PV experiment (X1..X5, NVFP4
-    pools only).
+    pools only), and with slack_eps given each value also carries the slack
+    [Hq, D] of fp4pv_attention_rows.
     Returns dict {(request, position): (o [Hq, D], lse [Hq])}.
     """
+    assert slack_eps is None or pv == "fp4"
     assert pv in ("wide", "fp4") and (pv == "wide" or isinstance(pools, Pools))
     q = _f32(q)
     qo = np.asarray(qo_indptr, dtype=np.int64)
@@ -451,7 +458,7 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
         gather = fp8_gather_decode if isinstance(pools, FP8Pools) else gather_decode
         gather_v = (lambda h: gather_v_token_major(pools, pt[b], kv_len, h, v_g)) if pv == "fp4" else \
             (lambda h: gather(pools, "v", pt[b], kv_len, h, v_g))
-        attend = fp4pv_attention_rows if pv == "fp4" else attention_rows
+        attend = (lambda *a: fp4pv_attention_rows(*a, eps=slack_eps)) if pv == "fp4" else attention_rows
         dec = dict(zip(range(Hkv), _pmap(
             lambda h: (gather(pools, "k", pt[b], kv_len, h, k_g), gather_v(h)), range(Hkv))))
         n_chunks = max(1, min(len(pos_all), -(-2 * WORKERS // Hkv)))
@@ -469,12 +476,13 @@ def paged_attention(pools: Pools, q, qo_indptr, kv_lens, page_table, Hq: int, k_
             return pos, res
 
         for i in pos_all:
-            result[(b, int(i))] = (np.zeros((Hq, pools.D)), np.zeros(Hq))
+            result[(b, int(i))] = (np.zeros((Hq, pools.D)), np.zeros(Hq)) + \
+                ((np.zeros((Hq, pools.D)),) if slack_eps is not None else ())
         for pos, res in _pmap(one, [(h, c) for h in range(Hkv) for c in chunks]):
-            for hq, o, lse in res:
+            for hq, *vals in res:
                 for r, i in enumerate(pos):
-                    result[(b, int(i))][0][hq] = o[r]
-                    result[(b, int(i))][1][hq] = lse[r]
+                    for slot, val in enumerate(vals):
+                        result[(b, int(i))][slot][hq] = val[r]
         del dec
     return result
 

@@ -310,14 +310,64 @@ void orc_v_token_major_page(const float* x, int D, uint8_t* codes,
   }
 }
 
+/* The E2M1 rounding boundaries (midpoints of neighbouring magnitudes). */
+static const double kE2M1Mid[7] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0};
+
+/* Largest change of one coded value of a block if the decision that coded it
+ * had gone the other way: per element, a code decision within relative eps
+ * of an E2M1 boundary may take the neighbouring magnitude; the block scale,
+ * if amax/(6g) lies within relative eps of an E4M3 midpoint, may take the
+ * neighbouring byte, which re-codes the whole block (R1..R3). */
+static void block_flip_bound(const float* x, float g, const uint8_t* packed,
+                             unsigned sc, double eps, double* delta) {
+  double sdec = orc_e4m3_value(sc);
+  for (int i = 0; i < 16; ++i) delta[i] = 0.0;
+  if (sdec != 0.0) {
+    float inv = 1.0f / (g * (float)sdec);
+    for (int i = 0; i < 16; ++i) {
+      double q = fabs((double)(x[i] * inv));
+      unsigned code = (packed[i / 2] >> (4 * (i % 2))) & 7u;
+      for (int b = 0; b < 7; ++b) {
+        if (fabs(q - kE2M1Mid[b]) <= eps * kE2M1Mid[b]) {
+          unsigned alt = (code == (unsigned)b) ? (unsigned)b + 1u : (unsigned)b;
+          double d = fabs(kE2M1Mag[alt] - kE2M1Mag[code]) * sdec * (double)g;
+          if (d > delta[i]) delta[i] = d;
+        }
+      }
+    }
+  }
+  float amax = 0.0f;
+  for (int i = 0; i < 16; ++i)
+    if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+  double s_real = (double)(amax / (6.0f * g));
+  for (int nb = -1; nb <= 1; nb += 2) {
+    int alt = (int)sc + nb;
+    if (alt < 0 || alt > 0x7E || amax == 0.0f) continue;
+    double mid = 0.5 * (orc_e4m3_value(sc) + orc_e4m3_value((unsigned)alt));
+    if (fabs(s_real - mid) > eps * mid) continue;
+    double adec = orc_e4m3_value((unsigned)alt);
+    float ainv = 1.0f / (g * (float)adec);
+    for (int i = 0; i < 16; ++i) {
+      unsigned code = (packed[i / 2] >> (4 * (i % 2))) & 15u;
+      unsigned acode = orc_e2m1_encode(x[i] * ainv);
+      double d = fabs(orc_e2m1_value(acode) * adec - orc_e2m1_value(code) * sdec) * (double)g;
+      if (d > delta[i]) delta[i] = d;
+    }
+  }
+}
+
 /* X2..X5 ([A4Q] "Compare A4Q with dequantize-ahead repacking": A4Q keeps a
  * wide PV; this is the FP4 alternative, P coded by the cache's block codec
- * against a whole-number running reference). */
+ * against a whole-number running reference).  With slack != NULL, also the
+ * per-row, per-dimension bound on how far o moves when P decisions lying
+ * within relative eps of a rounding boundary go the other way
+ * (block_flip_bound), so that a result computed from scores that differ in
+ * the last bits can be checked against what is unique. */
 void orc_fp4pv_attention_rows(const double* q, const int32_t* pos, int n_rows,
                               int q_len, const double* k, const double* vhat,
                               int kv_len, int D, int causal, double sm_scale,
-                              int tile, int tau, float g_p, double* out,
-                              double* lse) {
+                              int tile, int tau, float g_p, double eps,
+                              double* out, double* lse, double* slack) {
   const double log2e = 1.0 / log(2.0);
   int n = kv_len > 0 ? kv_len : 1;
   double* s = (double*)malloc(sizeof(double) * (size_t)n);
@@ -325,9 +375,13 @@ void orc_fp4pv_attention_rows(const double* q, const int32_t* pos, int n_rows,
   for (int r = 0; r < n_rows; ++r) {
     const double* qr = q + (int64_t)r * D;
     double* o = out + (int64_t)r * D;
+    double* sl = slack ? slack + (int64_t)r * D : NULL;
     int last = causal ? kv_len - q_len + pos[r] : kv_len - 1; /* R7 */
     if (last > kv_len - 1) last = kv_len - 1;
-    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int d = 0; d < D; ++d) {
+      o[d] = 0.0;
+      if (sl) sl[d] = 0.0;
+    }
     if (last < 0) {
       if (lse) lse[r] = -INFINITY;
       continue;
@@ -361,14 +415,23 @@ void orc_fp4pv_attention_rows(const double* q, const int32_t* pos, int n_rows,
         p[i] = (j <= last) ? (float)exp2(s[j] - m_of[t]) : 0.0f;
       }
       orc_quantize_block16(p, g_p, packed, &sc);
-      double w = exp2(m_of[t] - m_end) * orc_e4m3_value(sc) * (double)g_p;
+      double wt = exp2(m_of[t] - m_end);
+      double w = wt * orc_e4m3_value(sc) * (double)g_p;
+      double delta[16];
+      if (sl) block_flip_bound(p, g_p, packed, sc, eps, delta);
       for (int i = 0; i < 16 && b0 + i <= last; ++i) {
         unsigned code = (packed[i / 2] >> (4 * (i % 2))) & 15u; /* R4 */
         double ph = w * orc_e2m1_value(code);
-        for (int d = 0; d < D; ++d) o[d] += ph * vhat[(int64_t)(b0 + i) * D + d];
+        const double* vr = vhat + (int64_t)(b0 + i) * D;
+        for (int d = 0; d < D; ++d) o[d] += ph * vr[d];
+        if (sl && delta[i] > 0.0)
+          for (int d = 0; d < D; ++d) sl[d] += wt * delta[i] * fabs(vr[d]);
       }
     }
-    for (int d = 0; d < D; ++d) o[d] /= l;
+    for (int d = 0; d < D; ++d) {
+      o[d] /= l;
+      if (sl) sl[d] /= l;
+    }
     if (lse) lse[r] = (m_end + log2(l)) * log(2.0);
   }
   free(m_of);

@@ -167,12 +167,16 @@ void orc_v_token_major_page(const float* x, int D, uint8_t* codes,
 /* X2..X5: attention with FP4 P and the token-major V, for selected query
  * rows of one (request, q-head).  q: [n_rows][D] decoded A4Q queries, k:
  * [kv_len][D] decoded keys, vhat: [kv_len][D] token-major V decoded by X1
- * (v_g included).  tile = T, tau as in X3, g_p as in X4. */
+ * (v_g included).  tile = T, tau as in X3, g_p as in X4.  slack (optional,
+ * [n_rows][D]): how far each output element can move when the P decisions
+ * (E2M1 codes, E4M3 block scales) that lie within relative eps of a rounding
+ * boundary go the other way -- the part of the result that scores differing
+ * in their last bits may legitimately change. */
 void orc_fp4pv_attention_rows(const double* q, const int32_t* pos, int n_rows,
                               int q_len, const double* k, const double* vhat,
                               int kv_len, int D, int causal, double sm_scale,
-                              int tile, int tau, float g_p, double* out,
-                              double* lse);
+                              int tile, int tau, float g_p, double eps,
+                              double* out, double* lse, double* slack);
 
 /* Cache bytes for one layer's K and V pools ([PD] "A worked per-token cache
  * estimate"): 2 * pages * page_size * Hkv * (D/2 + D/16). */

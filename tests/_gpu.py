@@ -83,10 +83,27 @@ def compare_rows(got, ref, qo_indptr):
     return float(excess.max()), float(np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30)), len(diffs)
 
 
+def compare_rows_slack(got, ref, qo_indptr):
+    """As compare_rows, for oracle values (o, lse, slack) of the FP4 PV
+    experiment: the excess is measured beyond half a bf16 ulp plus the slack
+    (how far the output may move when P decisions that lie within the
+    oracle's eps of a rounding boundary go the other way).  Also returns the
+    largest raw |gpu - oracle| and the largest slack."""
+    diffs, refs, slacks = [], [], []
+    for (b, i), (o, _, sl) in ref.items():
+        diffs.append(got[int(qo_indptr[b]) + i] - o)
+        refs.append(o)
+        slacks.append(sl)
+    d, r, sl = np.stack(diffs), np.stack(refs), np.stack(slacks)
+    excess = np.maximum(np.abs(d) - bf16_half_ulp(r) - sl, 0.0)
+    return (float(excess.max()), float(np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30)), len(diffs),
+            float(np.abs(d).max()), float(sl.max()))
+
+
 def compare_lse(got_lse, ref, qo_indptr):
     err = 0.0
-    for (b, i), (_, lse) in ref.items():
-        err = max(err, float(np.abs(got_lse[int(qo_indptr[b]) + i] - lse).max()))
+    for (b, i), vals in ref.items():
+        err = max(err, float(np.abs(got_lse[int(qo_indptr[b]) + i] - vals[1]).max()))
     return err
 
 

@@ -181,3 +181,55 @@ def test_fp4pv_independent_of_tiling_and_threshold(orc):
         o, lse = orc.fp4pv_attention_rows(q, pos, kv, k, v, True, math.log(2.0), tile=tile, tau=tau)
         np.testing.assert_allclose(o, base, rtol=1e-12, atol=1e-13)
         np.testing.assert_allclose(lse, lb, rtol=1e-12)
+
+
+def _one_block_row(orc, s, eps, D=4, seed=6):
+    """One non-causal row over len(s) keys whose log2 scores are exactly s."""
+    rng = np.random.default_rng(seed)
+    kv = len(s)
+    k = np.zeros((kv, D))
+    k[:, 0] = s
+    q = np.zeros((1, D))
+    q[0, 0] = 1.0
+    v = rng.standard_normal((kv, D))
+    return orc.fp4pv_attention_rows(q, np.array([0]), 1, k, v, False, math.log(2.0), eps=eps)
+
+
+@pytest.mark.parametrize("kind", ["code", "scale"])
+def test_fp4pv_slack_covers_a_real_flip(orc, kind):
+    """A P value placed just below and just above an E2M1 boundary (2.5, in
+    units of its block scale), or a block maximum just below and above an
+    E4M3 midpoint (27 between 26 and 28), codes differently on the two sides;
+    the slack reported on either side covers the change, and is zero with
+    eps = 0 when nothing lies exactly on a boundary."""
+    rng = np.random.default_rng(12)
+    base = rng.uniform(-3.9, -1.1, 16)
+    outs = []
+    for sign in (-1.0, 1.0):
+        s = base.copy()
+        if kind == "code":
+            s[0] = 0.0                                              # p = 1: the block scale is 28
+            s[5] = math.log2(2.5 / 6.0) + sign * 1e-6               # p * inv = 2.5 (1 +- 7e-7)
+        else:
+            s[0] = math.log2(27.0 / 28.0) + sign * 1e-6             # amax * 28 = 27 (1 +- 7e-7)
+        o, _, sl = _one_block_row(orc, s, eps=1e-5)
+        _, _, sl0 = _one_block_row(orc, s, eps=0.0)
+        assert not sl0.any()
+        outs.append((o[0], sl[0]))
+    (o_lo, sl_lo), (o_hi, sl_hi) = outs
+    moved = np.abs(o_hi - o_lo)
+    assert moved.max() > 1e-3                                       # the decision really flipped
+    # (moving the score by 1e-6 also moves that p and l, hence o,
+    # continuously by about 1e-6 relative: hence the small allowance on |o|)
+    cont = 1e-5 * (np.abs(o_lo) + np.abs(o_hi))
+    assert np.all(moved <= sl_lo + cont) and np.all(moved <= sl_hi + cont)
+
+
+def test_fp4pv_slack_zero_away_from_boundaries(orc):
+    """Uniform scores code p = 1 as 6 x E4M3(28), far from every boundary."""
+    rng = np.random.default_rng(3)
+    n, D = 40, 32
+    v = rng.standard_normal((n, D))
+    k = rng.standard_normal((n, D))
+    _, _, sl = orc.fp4pv_attention_rows(np.zeros((n, D)), np.arange(n), n, k, v, True, 0.125, eps=1e-3)
+    assert not sl.any()
