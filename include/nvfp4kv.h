@@ -62,6 +62,20 @@ extern "C" {
  * repacking"). */
 #define NVFP4KV_VARIANT_A4Q 0      /* Q quantized to NVFP4 in-kernel, QK on block-scaled FP4 MMA */
 #define NVFP4KV_VARIANT_DQ_AHEAD 1 /* K tile dequantized once to BF16, QK on BF16 MMA with BF16 Q */
+/* An experiment beyond the pages' design, which keeps PV wide because the V
+ * block scales run along the head dimension while PV reduces over tokens
+ * ("NVFP4 KV cache A4Q prefill explained", sections "Why NVFP4 KV cache A4Q
+ * prefill exists" and "Compare A4Q with dequantize-ahead repacking"): A4Q QK,
+ * and PV on block-scaled FP4 MMA too.  V is re-coded once per call along
+ * tokens (nvfp4_v_token_major's blocks, with slots past kv_len as zeros) into
+ * the workspace; P is coded per 16 keys by the cache's block codec with
+ * global scale fl32(16/2688), against a running reference that moves in
+ * whole log2 steps when a 128-key tile's largest score exceeds it by more
+ * than 4 (the kernel folds each block's reciprocal scale into the exponent,
+ * which moves a code decision only when p lies within about 1e-6 relative of
+ * a rounding boundary); the row sum uses the uncoded P.  Needs the repack
+ * workspace. */
+#define NVFP4KV_VARIANT_A4Q_FP4PV 2
 
 /* Quantize-rows modes. */
 #define NVFP4KV_QUANT_GLOBAL 0  /* one caller-given global scale for every row */
@@ -117,7 +131,10 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  * causal:     1 = query i of a request sees keys j <= kv_len - q_len + i
  *             (bottom-right alignment); 0 = every query sees all kv_len keys.
  * sm_scale:   softmax scale applied to q.k (e.g. 1/sqrt(128)).
- * variant:    NVFP4KV_VARIANT_A4Q or NVFP4KV_VARIANT_DQ_AHEAD.
+ * variant:    NVFP4KV_VARIANT_A4Q, NVFP4KV_VARIANT_DQ_AHEAD or
+ *             NVFP4KV_VARIANT_A4Q_FP4PV (NVFP4 cache only; returns
+ *             NVFP4KV_ERR_WORKSPACE unless the workspace holds the repack
+ *             records, 18 KB per 128-key tile).
  * q_global_scale: the A4Q query scale scheme ("NVFP4 KV cache A4Q prefill
  *             explained", section "Make query accuracy a release gate": the
  *             scheme is a recorded choice).  0 = per (token, head) row, dual
@@ -126,7 +143,8 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  *             passes amax(Q)/2688, a single-level scheme when it passes 1.
  *             Either way the row is then coded with the cache's 16-value
  *             block codec.  Must be finite and >= 0; ignored by
- *             NVFP4KV_VARIANT_DQ_AHEAD (its query stays BF16).
+ *             NVFP4KV_VARIANT_DQ_AHEAD (its query stays BF16); used by
+ *             NVFP4KV_VARIANT_A4Q_FP4PV as by NVFP4KV_VARIANT_A4Q.
  * o:          bf16 [total_q][num_q_heads][128] output (rows of q not covered
  *             by qo_indptr are left untouched).
  * lse:        optional fp32 [total_q][num_q_heads] natural-log sum-exp of the
@@ -188,7 +206,9 @@ int nvfp4_paged_prefill_run(const void* q, int64_t total_q, int32_t num_q_heads,
  * are those of nvfp4_paged_prefill.  Returns NVFP4KV_ERR_WORKSPACE when the
  * schedule of the call (nvfp4_workspace_bytes(NVFP4KV_OP_PREFILL, ..., 0)) is
  * larger than the array, and NVFP4KV_ERR_UNSUPPORTED on a device that is not
- * sm_103.  The first call on a device looks up the array's device address
+ * sm_103; NVFP4KV_VARIANT_A4Q_FP4PV, which reads only repacked records, is
+ * refused with NVFP4KV_ERR_WORKSPACE.  The first call on a device looks up the
+ * array's device address
  * (make it before any stream capture); the address is kept for the life of
  * the process, which assumes one CUDA context per device.  All calls share
  * the array: calls that overlap on the GPU race.  Allocates nothing. */
@@ -221,9 +241,10 @@ int nvfp4_paged_decode(const void* q, int32_t num_q_heads, const nvfp4kv_cache_t
 
 /* Workspace bytes for op.  NVFP4KV_OP_PREFILL: the schedule for total_q
  * query tokens, plus, when max_kv_len > 0, room for the repack records of
- * either variant (per request and kv head: 37 KB per 112-key A4Q tile or
- * 64 KB per 128-key dequant-ahead tile of max_kv_len, the larger total).  NVFP4KV_OP_DECODE: the
- * split-KV partials for max_kv_len.  Host-only, no CUDA call.  Returns 0 for
+ * any variant (per request and kv head: 37 KB per 112-key A4Q tile, 64 KB
+ * per 128-key dequant-ahead tile or 18 KB per 128-key FP4 PV tile of
+ * max_kv_len, the largest total).  NVFP4KV_OP_DECODE: the split-KV partials
+ * for max_kv_len.  Host-only, no CUDA call.  Returns 0 for
  * bad arguments. */
 size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int64_t total_q,
                              int32_t max_kv_len);
@@ -250,6 +271,24 @@ int nvfp4_quantize_rows(const void* x, int64_t rows, int32_t mode, float global_
  * rounded to bf16 (exact when the product has at most 8 significant bits). */
 int nvfp4_dequantize_rows(const void* packed, const void* scales, int64_t rows, const float* row_scales,
                           float global_scale, void* out, void* stream);
+
+/* The token-major re-layout of V that NVFP4KV_VARIANT_A4Q_FP4PV reads (an
+ * experiment: "NVFP4 KV cache A4Q prefill explained", section "Why NVFP4 KV
+ * cache A4Q prefill exists", notes that the cache's V block scales do not
+ * follow PV's reduction axis).  A page holds 16 tokens, so each (page, kv
+ * head, head dimension d) is one block along tokens: the 16 slots' values at
+ * d, decoded without the tensor scale (e2m1 * e4m3, exact), re-coded by the
+ * cache's block codec (as nvfp4_kv_append) with global scale 1.  A value
+ * decodes as e2m1(code) * e4m3(scale) * v_global_scale.
+ * page_ids:  device int32 [num_ids]; an id outside [0, num_pages) gives zeros
+ *            and is flagged (NVFP4KV_ERR_DEVICE_INDEX).
+ * codes:     device uint8 [num_ids][num_kv_heads][128][8], 8-byte aligned;
+ *            slot 2i in the low nibble of byte i.
+ * scales:    device uint8 [num_ids][num_kv_heads][128].
+ * Every slot of a listed page is used as written (the prefill variant
+ * treats slots past a request's kv_len as zeros). */
+int nvfp4_v_token_major(const nvfp4kv_cache_t* cache, const int32_t* page_ids, int32_t num_ids, void* codes,
+                        void* scales, void* stream);
 
 /* ---- FP8 (E4M3) comparison cache --------------------------------------------
  * The format the pages weigh NVFP4 against ("NVFP4 KV cache prefill vs decode

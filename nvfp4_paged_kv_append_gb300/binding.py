@@ -17,10 +17,18 @@ import torch
 from . import build as _build
 
 NVFP4KV_OK = 0
+NVFP4KV_ERR_ARG = -1
+NVFP4KV_ERR_SHAPE = -2
+NVFP4KV_ERR_WORKSPACE = -3
+NVFP4KV_ERR_CUDA = -4
+NVFP4KV_ERR_TIMEOUT = -5
+NVFP4KV_ERR_DEVICE_INDEX = -6
+NVFP4KV_ERR_UNSUPPORTED = -7
 ERR_NAMES = {-1: "ERR_ARG", -2: "ERR_SHAPE", -3: "ERR_WORKSPACE", -4: "ERR_CUDA", -5: "ERR_TIMEOUT",
              -6: "ERR_DEVICE_INDEX", -7: "ERR_UNSUPPORTED"}
 VARIANT_A4Q = 0
 VARIANT_DQ_AHEAD = 1
+VARIANT_A4Q_FP4PV = 2
 QUANT_GLOBAL = 0
 QUANT_PER_ROW = 1
 OP_PREFILL = 0
@@ -32,7 +40,7 @@ EXPORTED = ["nvfp4_kv_append", "nvfp4_paged_prefill", "nvfp4_paged_decode", "nvf
             "nvfp4_cache_bytes", "nvfp4_quantize_rows", "nvfp4_dequantize_rows", "nvfp4kv_get_device_status",
             "nvfp4kv_status_string", "nvfp4kv_version", "nvfp4kv_debug_wait_timeout",
             "nvfp4_paged_prefill_noalloc", "nvfp4_paged_prefill_noalloc_max_bytes",
-            "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run",
+            "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run", "nvfp4_v_token_major",
             "fp8_kv_append", "fp8_paged_prefill", "fp8_paged_decode", "fp8_workspace_bytes", "fp8_cache_bytes"]
 
 
@@ -76,6 +84,7 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4_cache_bytes.restype = sz
     lib.nvfp4_quantize_rows.argtypes = [P, i64, i32, f32, P, P, P, P]
     lib.nvfp4_dequantize_rows.argtypes = [P, P, i64, P, f32, P, P]
+    lib.nvfp4_v_token_major.argtypes = [D, P, i32, P, P, P]
     lib.nvfp4kv_get_device_status.argtypes = [P]
     lib.nvfp4kv_status_string.argtypes = [ctypes.c_int]
     lib.nvfp4kv_status_string.restype = ctypes.c_char_p
@@ -91,7 +100,7 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4kv_debug_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.nvfp4kv_debug_wait_timeout.restype = ctypes.c_int
     for name in ("nvfp4_kv_append", "nvfp4_paged_prefill", "nvfp4_paged_prefill_noalloc", "nvfp4_paged_decode",
-                 "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run",
+                 "nvfp4_paged_prefill_plan", "nvfp4_paged_prefill_run", "nvfp4_v_token_major",
                  "nvfp4_quantize_rows",
                  "nvfp4_dequantize_rows", "nvfp4kv_get_device_status", "fp8_kv_append", "fp8_paged_prefill",
                  "fp8_paged_decode"):
@@ -505,6 +514,23 @@ def nvfp4_dequantize_rows(packed: torch.Tensor, scales: torch.Tensor, row_scales
                                                                   _ptr(row_scales), float(global_scale), _ptr(out),
                                                                   _stream(stream, dev)))
     return out
+
+
+def nvfp4_v_token_major(cache: Cache, page_ids: torch.Tensor, stream=None):
+    """The token-major V blocks of the listed pages (the re-layout the FP4 PV
+    prefill variant reads): codes uint8 [n][kv heads][128][8] and scales uint8
+    [n][kv heads][128]."""
+    _check_dtype(page_ids, torch.int32, "page_ids")
+    _require(page_ids.dim() == 1 and page_ids.is_contiguous(), "page_ids must be a contiguous [n] tensor")
+    d = cache.desc()  # a host-memory cache is refused before the other tensors
+    dev = _device(*cache.pools(), page_ids)
+    n, h = page_ids.shape[0], cache.num_kv_heads
+    codes = torch.empty(n, h, HEAD_DIM, 8, dtype=torch.uint8, device=dev)
+    scales = torch.empty(n, h, HEAD_DIM, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check("nvfp4_v_token_major", lib.nvfp4_v_token_major(ctypes.byref(d), _ptr(page_ids), n, _ptr(codes),
+                                                              _ptr(scales), _stream(stream, dev)))
+    return codes, scales
 
 
 def _current_device() -> torch.device:

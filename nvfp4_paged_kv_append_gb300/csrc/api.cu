@@ -169,9 +169,11 @@ size_t prefill_repack_tiles(int batch, int num_kv_heads, int64_t max_kv_len, int
 // Keys per KV tile of the attention kernel that runs (variant, mode).
 int prefill_tile_keys(int variant, bool repack) { return (variant == 0 && repack) ? prefill_a4q_2cta_tile_keys() : kBN; }
 size_t prefill_repack_bytes(int variant, int batch, int num_kv_heads, int64_t max_kv_len) {
-  if (variant == 0)
+  if (variant == NVFP4KV_VARIANT_A4Q)
     return prefill_a4q_2cta_record_bytes() *
            prefill_repack_tiles(batch, num_kv_heads, max_kv_len, prefill_a4q_2cta_tile_keys());
+  if (variant == NVFP4KV_VARIANT_A4Q_FP4PV)
+    return prefill_fp4pv_record_bytes() * prefill_repack_tiles(batch, num_kv_heads, max_kv_len, kBN);
   return kRepackRecordBytesDq * prefill_repack_tiles(batch, num_kv_heads, max_kv_len, kBN);
 }
 
@@ -244,10 +246,13 @@ size_t nvfp4_workspace_bytes(int32_t op, int32_t batch, int32_t num_q_heads, int
   if (op == NVFP4KV_OP_PREFILL) {
     if (total_q < 0) return 0;
     const int64_t units = prefill_max_items(total_q, batch, num_q_heads, num_kv_heads);
-    const size_t a4q = prefill_repack_bytes(0, batch, num_kv_heads, max_kv_len);
-    const size_t dq = prefill_repack_bytes(1, batch, num_kv_heads, max_kv_len);
+    size_t rec = 0;  // the largest records of any variant
+    for (int v : {NVFP4KV_VARIANT_A4Q, NVFP4KV_VARIANT_DQ_AHEAD, NVFP4KV_VARIANT_A4Q_FP4PV}) {
+      const size_t r = prefill_repack_bytes(v, batch, num_kv_heads, max_kv_len);
+      rec = r > rec ? r : rec;
+    }
     const int split = split_cap(units, max_kv_len > 0 ? (max_kv_len + kBN - 1) / kBN : 0, kSplitSizingCtas);
-    return prefill_sched_bytes(units, split, batch) + (a4q > dq ? a4q : dq) + prefill_part_bytes(units, split);
+    return prefill_sched_bytes(units, split, batch) + rec + prefill_part_bytes(units, split);
   }
   if (op == NVFP4KV_OP_DECODE) {
     if (max_kv_len < 0) return 0;
@@ -292,7 +297,10 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   const int lg = log2_exact(num_q_heads / c.num_kv_heads);
   if (lg < 0 || lg > 7) return NVFP4KV_ERR_ARG;
   if (causal != 0 && causal != 1) return NVFP4KV_ERR_ARG;
-  if (variant != NVFP4KV_VARIANT_A4Q && variant != NVFP4KV_VARIANT_DQ_AHEAD) return NVFP4KV_ERR_ARG;
+  if (variant != NVFP4KV_VARIANT_A4Q && variant != NVFP4KV_VARIANT_DQ_AHEAD && variant != NVFP4KV_VARIANT_A4Q_FP4PV)
+    return NVFP4KV_ERR_ARG;
+  const bool fp4pv = variant == NVFP4KV_VARIANT_A4Q_FP4PV;
+  if (fp4pv && c.fp8) return NVFP4KV_ERR_ARG;
   if ((stages & kStageRun) && !std::isfinite(sm_scale)) return NVFP4KV_ERR_ARG;
   if (!std::isfinite(q_global_scale) || q_global_scale < 0.0f) return NVFP4KV_ERR_ARG;
   if (total_q * num_q_heads >= (int64_t(1) << 31)) return NVFP4KV_ERR_ARG;
@@ -311,7 +319,7 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   const size_t rbytes = prefill_repack_bytes(variant, batch, c.num_kv_heads, max_kv);
   const int64_t qtiles = (total_q * (num_q_heads / c.num_kv_heads) + kBM - 1) / kBM;
   bool repack = workspace_bytes >= sched1 + rbytes && qtiles >= 2 * static_cast<int64_t>(batch);
-  if (c.fp8) {
+  if (c.fp8 || fp4pv) {  // these read only repacked records
     if (workspace_bytes < sched1 + rbytes) return NVFP4KV_ERR_WORKSPACE;
     repack = true;
   }
@@ -325,7 +333,9 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   const int bn = prefill_tile_keys(variant, repack);
   const bool two_cta = repack && variant == NVFP4KV_VARIANT_A4Q && !c.fp8;
   const int ctas = d->num_sms;
-  int split = two_cta ? 1 : split_cap(max_units, (max_kv + bn - 1) / bn, ctas);
+  // (The FP4 PV variant codes P against a reference that each KV range
+  // would restart, so it always runs each unit whole.)
+  int split = (two_cta || fp4pv) ? 1 : split_cap(max_units, (max_kv + bn - 1) / bn, ctas);
   while (split > 1 && workspace_bytes < prefill_sched_bytes(max_units, split, batch) + (repack ? rbytes : 0) +
                                             prefill_part_bytes(max_units, split))
     --split;
@@ -372,7 +382,7 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   a.sm_scale = sm_scale;
   a.k_g = c.k_g;
   a.v_g = c.v_g;
-  a.q_g = variant == NVFP4KV_VARIANT_A4Q ? q_global_scale : 0.0f;
+  a.q_g = variant != NVFP4KV_VARIANT_DQ_AHEAD ? q_global_scale : 0.0f;
   a.o = o;
   a.lse = lse;
   a.work = static_cast<const int*>(workspace);
@@ -561,6 +571,22 @@ int nvfp4_dequantize_rows(const void* packed, const void* scales, int64_t rows, 
   nvfp4_dequantize_rows_kernel<<<static_cast<unsigned>((rows * 16 + 255) / 256), 256, 0,
                                  static_cast<cudaStream_t>(stream)>>>(a);
   return launch_rc(cudaGetLastError());
+}
+
+int nvfp4_v_token_major(const nvfp4kv_cache_t* cache, const int32_t* page_ids, int32_t num_ids, void* codes,
+                        void* scales, void* stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (num_ids < 0) return NVFP4KV_ERR_ARG;
+  if (num_ids == 0) return NVFP4KV_OK;
+  if (!page_ids || !codes || !scales || (reinterpret_cast<uintptr_t>(codes) & 7u)) return NVFP4KV_ERR_ARG;
+  if (static_cast<int64_t>(num_ids) * cache->num_kv_heads * kHeadDim >= (int64_t(1) << 40)) return NVFP4KV_ERR_ARG;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  TokenMajorArgs a{static_cast<const uint8_t*>(cache->v_data), static_cast<const uint8_t*>(cache->v_scale), page_ids,
+                   num_ids, cache->num_pages, cache->num_kv_heads, static_cast<uint8_t*>(codes),
+                   static_cast<uint8_t*>(scales), d->status};
+  return launch_rc(launch_v_token_major(a, d->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 int nvfp4kv_get_device_status(void* stream) {

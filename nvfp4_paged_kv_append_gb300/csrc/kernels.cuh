@@ -169,6 +169,20 @@ cudaError_t launch_prefill_merge(const PrefillArgs& a, cudaStream_t s);
 // (K BF16 | V FP16 per 128-key tile), then the dequant-ahead attention.
 cudaError_t launch_prefill_fp8(const PrefillArgs& a, const PlanArgs& plan, int num_sms, cudaStream_t s);
 // A4Q in repack mode: two CTAs per SM, 112-key tiles (prefill_a4q.cu).
+// FP4 PV: repack record size (per 128-key tile) and the page re-layout
+struct TokenMajorArgs {
+  const uint8_t* v_data;
+  const uint8_t* v_scale;
+  const int32_t* page_ids;
+  int n_ids;
+  int num_pages;
+  int num_kv_heads;
+  uint8_t* codes;   // [n_ids][Hkv][128][8]
+  uint8_t* scales;  // [n_ids][Hkv][128]
+  int* status;
+};
+size_t prefill_fp4pv_record_bytes();
+cudaError_t launch_v_token_major(const TokenMajorArgs& a, int num_sms, cudaStream_t s);
 size_t prefill_a4q_2cta_record_bytes();
 int prefill_a4q_2cta_tile_keys();
 cudaError_t launch_prefill_a4q_2cta_repack(const PrefillArgs& a, int num_sms, cudaStream_t s);

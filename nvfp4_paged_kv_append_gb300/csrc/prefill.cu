@@ -35,6 +35,18 @@
 //
 // PV runs on FP16 operands: every dequantized V value (E2M1 x E4M3) is exact
 // in FP16 (and in BF16), while FP16 keeps 3 more mantissa bits of P.
+//
+// The FP4 PV variant (an experiment: the pages keep PV wide because the
+// cache's V block scales run along the head dimension while PV reduces over
+// tokens, "NVFP4 KV cache A4Q prefill explained", sections "Why NVFP4 KV cache
+// A4Q prefill exists" and "Compare A4Q with dequantize-ahead repacking") runs
+// PV on kind::mxf4nvf4 too.  Its repack records carry V re-coded along
+// tokens (one E4M3 scale per 16 tokens of one head dimension, the cache's
+// block codec with global scale 1) as an MMA B operand beside K; the softmax
+// codes P per 16 keys with the same codec and global scale 2^4/2688, against
+// a running reference that only takes whole values (so a moved reference
+// scales P and O by exact powers of two), and writes P's codes and scale
+// atoms to shared memory for the PV MMA.
 #include "prefill_common.cuh"
 
 namespace nvfp4kv {
@@ -43,6 +55,16 @@ namespace {
 
 using namespace prefill_detail;
 
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^d for a whole number d <= 0 (or -inf), exactly; 0 below the normal range.
+__device__ __forceinline__ float exp2_whole(float d) {
+  return d < -126.0f ? 0.0f : __int_as_float((static_cast<int>(d) + 127) << 23);
+}
 
 // warps 0 QK issue (and TMEM allocation), 1-2 loaders, 3 PV issue, 4-7
 // transform, 8-11 softmax half 0, 12-15 softmax half 1.  A warp reaches only
@@ -56,16 +78,27 @@ constexpr int kTransformTid0 = 128, kSoftmaxTid0 = 256;
 
 // TMEM columns: S double buffer (fp32), O (fp32), P (FP16 pairs, one tile),
 // Q block scales, K block scales (double buffer)
+// (FP4 PV: P and V block scales, double buffered, over P's columns)
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384, kColSFA = 448, kColSFB = 456;
+constexpr uint32_t kColSFP = 384, kColSFV = 400;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kKData = 8192, kKScale = 1024, kVData = 8192, kVScale = 1024;
 constexpr uint32_t kTile16 = 32768;  // 128 keys x 128 values x 2 B
+constexpr uint32_t kPBuf = 8192 + 1024;  // FP4 PV: P codes (64B-swizzled rows) + two scale atoms
+
+// FP4 PV: P <= 2^kTauFp4 against the whole-number reference, coded with
+// global scale fl32(2^kTauFp4 / 2688) so that its block scales never saturate.
+constexpr float kTauFp4 = 4.0f;
+constexpr float kPScale = 16.0f / 2688.0f;
+constexpr float kPInvSixG = 28.0f;  // 1 / (6 g_P): a block scale is amax * 28
 
 // Shared-memory layout per (variant, mode).  Stage contents:
 //   in-kernel:     K codes 8 KB | K scales 1 KB | V codes 8 KB | V scales 1 KB
 //   A4Q repack:    K codes 8 KB | K scales 1 KB | V tile (FP16) 32 KB
 //   DQ repack:     K tile (BF16) 32 KB | V tile (FP16) 32 KB
+//   FP4 PV repack: K codes 8 KB | K scales 1 KB | token-major V codes 8 KB
+//                  (64B-swizzled [head dim][64 B]) | their scale atoms 1 KB
 // K codes are 64B-swizzled [key][64 B] rows.  A4Q K scales are two 512-byte
 // scale-factor atoms (k-steps 0 and 1: key n's four block scales at byte
 // (n % 32) * 16 + (n / 32) * 4), ready for tcgen05.cp; dequant-ahead keeps
@@ -73,17 +106,21 @@ constexpr uint32_t kTile16 = 32768;  // 128 keys x 128 values x 2 B
 // repack pre-pass, byte for byte.
 template <int VARIANT, bool REPACK>
 struct Layout {
-  static constexpr bool kA4Q = VARIANT == 0;
-  static constexpr int kStages = REPACK ? (kA4Q ? 5 : 2) : (kA4Q ? 6 : 3);
+  static constexpr bool kA4Q = VARIANT != 1;    // FP4 query, block-scaled FP4 QK
+  static constexpr bool kFp4Pv = VARIANT == 2;  // FP4 P x token-major FP4 V
+  static_assert(!kFp4Pv || REPACK, "the FP4 PV variant reads repacked records");
+  static constexpr int kStages = REPACK ? (kFp4Pv ? 6 : kA4Q ? 5 : 2) : (kA4Q ? 6 : 3);
   static constexpr uint32_t kStageBytes =
-      REPACK ? (kA4Q ? kKData + kKScale + kTile16 : 2 * kTile16) : kKData + kKScale + kVData + kVScale;
+      REPACK ? (kFp4Pv ? kKData + kKScale + kVData + kVScale : kA4Q ? kKData + kKScale + kTile16 : 2 * kTile16)
+             : kKData + kKScale + kVData + kVScale;
   static constexpr uint32_t kStageV = REPACK ? (kA4Q ? kKData + kKScale : kTile16) : kKData + kKScale;
   static constexpr uint32_t kQBytes = kA4Q ? 8192u : 32768u;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffStage = kOffQ + kQBytes;
   static constexpr uint32_t kOffV = kOffStage + kStages * kStageBytes;            // in-kernel V buffers
   static constexpr uint32_t kOffK = kOffV + (REPACK ? 0u : 2 * kTile16);          // in-kernel DQ K buffers
-  static constexpr uint32_t kOffSmall = kOffK + ((!REPACK && !kA4Q) ? 2 * kTile16 : 0u);
+  static constexpr uint32_t kOffP = kOffK + ((!REPACK && !kA4Q) ? 2 * kTile16 : 0u);  // FP4 PV: P [2]
+  static constexpr uint32_t kOffSmall = kOffP + (kFp4Pv ? 2 * kPBuf : 0u);
   static constexpr uint32_t kOffQScale = kOffSmall;            // 128 floats
   static constexpr uint32_t kOffSfaStage = kOffQScale + 512;   // 128 x 8 B
   static constexpr uint32_t kOffXmax = kOffSfaStage + 1024;    // [2 parity][2 half][128] row maxima
@@ -266,7 +303,7 @@ __device__ void qk_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
 template <int VARIANT, bool REPACK>
 __device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase) {
   using L = Layout<VARIANT, REPACK>;
-  const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
+  const uint32_t idesc_pv = L::kFp4Pv ? idesc_mxf4nvf4(128, 128) : idesc_f16(128, 128, 0, 0, 0, 1);
   uint32_t it_ctr = 0, item_ctr = 0;
   Item item;
   for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
@@ -281,10 +318,27 @@ __device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
       tc_fence_after();
       const uint32_t v_s = REPACK ? smem_u32(smem + L::kOffStage + st * L::kStageBytes + L::kStageV)
                                   : smem_u32(smem + L::kOffV + b * kTile16);
+      if constexpr (L::kFp4Pv) {
+        // P (codes and scale atoms, written by the softmax warps) and the
+        // record's token-major V.  Scale buffer b was last read by PV(it-2),
+        // which had finished before the softmax wrote P(it).
+        const uint32_t p_s = smem_u32(smem + L::kOffP + b * kPBuf);
+        tc_cp_32x128b_warpx4(tbase + kColSFP + 8 * b, smem_desc(p_s + 8192, 0, 128, kSwzNone));
+        tc_cp_32x128b_warpx4(tbase + kColSFP + 8 * b + 4, smem_desc(p_s + 8192 + 512, 0, 128, kSwzNone));
+        tc_cp_32x128b_warpx4(tbase + kColSFV + 8 * b, smem_desc(v_s + kVData, 0, 128, kSwzNone));
+        tc_cp_32x128b_warpx4(tbase + kColSFV + 8 * b + 4, smem_desc(v_s + kVData + 512, 0, 128, kSwzNone));
 #pragma unroll
-      for (uint32_t k = 0; k < 8; ++k) {
-        mma_f16_ts(tbase + kColO, tbase + kColP + 8 * k, smem_desc(v_s + k * 2048, 16384, 1024, kSwz128), idesc_pv,
-                   (j == 0 && k == 0) ? 0u : 1u);
+        for (uint32_t s = 0; s < 2; ++s) {
+          mma_nvf4_ss(tbase + kColO, smem_desc(p_s + 32 * s, 16, 512, kSwz64), smem_desc(v_s + 32 * s, 16, 512, kSwz64),
+                      idesc_pv, tbase + kColSFP + 8 * b + 4 * s, tbase + kColSFV + 8 * b + 4 * s,
+                      (j == 0 && s == 0) ? 0u : 1u);
+        }
+      } else {
+#pragma unroll
+        for (uint32_t k = 0; k < 8; ++k) {
+          mma_f16_ts(tbase + kColO, tbase + kColP + 8 * k, smem_desc(v_s + k * 2048, 16384, 1024, kSwz128), idesc_pv,
+                     (j == 0 && k == 0) ? 0u : 1u);
+        }
       }
       tc_commit(&bars.pv_done[b]);
       if (REPACK) tc_commit(&bars.kv_empty[st]);  // the stage's V tile has been read
@@ -486,29 +540,85 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
       // by more than 2^15.  TMEM loads/stores are warp-collective, so the
       // whole warp rescales its 64 O columns, with factor 1 for rows that keep
       // their max.  Both halves take identical decisions (same m_tile).
+      // (FP4 PV: the threshold is 2^4 and the reference a whole number, so
+      // alpha is an exact power of two and P <= 16 fits P's global scale.)
       float alpha = 1.0f;
-      const bool need = m_tile > m_run + kRescaleThreshold;
+      const bool need = m_tile > m_run + (L::kFp4Pv ? kTauFp4 : kRescaleThreshold);
       if (need) {
-        alpha = fast_exp2(m_run - m_tile);  // 0 when m_run = -inf
+        if constexpr (L::kFp4Pv) {
+          const float m_new = ceilf(m_tile);
+          alpha = exp2_whole(m_run - m_new);
+          m_run = m_new;
+        } else {
+          alpha = fast_exp2(m_run - m_tile);  // 0 when m_run = -inf
+          m_run = m_tile;
+        }
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int i = 0; i < 4; ++i) lacc[i] = __fmul2_rn(lacc[i], a2);
-        m_run = m_tile;
       }
       const bool rescale_o = j > 0 && __any_sync(0xffffffffu, need);
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
       const float cs = masked ? 1.0f : c_r;
       const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-m_use, -m_use);
       uint32_t pk[32];
+      uint32_t pw[8], psc = 0u;  // FP4 PV: this half's P codes (4 blocks x 8 B) and block scales
+      if constexpr (L::kFp4Pv) {
+        // P coded per 16 keys by the block codec with global scale g_P: the
+        // block scale from the block's largest p, which is 2^(its largest t)
+        // since ex2 is monotone; each code from p * inv = 2^(t - log2(g_P *
+        // scale)), the reciprocal folded into the exponent's addend.  These
+        // roundings differ from the codec's own steps by about 1e-6 relative
+        // only.  The row sum takes p = (code input) * g_P * scale, uncoded.
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float2 t = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), cs2, nm2);
-        const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-        lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
-        pk[c] = pack_f16x2(p.x, p.y);
+        for (int blk = 0; blk < 4; ++blk) {
+          const float* sb = s + 16 * blk;
+          float mb = fmax3(sb[0], sb[1], sb[2]);
+#pragma unroll
+          for (int i = 3; i < 15; i += 2) mb = fmax3(mb, sb[i], sb[i + 1]);
+          mb = fmaxf(mb, sb[15]);
+          const float amax = fast_exp2(fmaf(mb, cs, -m_use));
+          const uint32_t sc = cvt_e4m3x2(amax * kPInvSixG, 0.0f) & 0xFFu;
+          const float sdec = e4m3_to_f32(sc);
+          const float f = sdec > 0.0f ? kPScale * sdec : 1.0f;
+          const float add = -m_use - fast_log2(f);
+          const float2 add2 = make_float2(add, add);
+          float2 qsum = make_float2(0.0f, 0.0f);
+          uint32_t wlo = 0u, whi = 0u;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float2 t = __ffma2_rn(make_float2(sb[2 * c], sb[2 * c + 1]), cs2, add2);
+            const float2 qq = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+            qsum = __fadd2_rn(qsum, qq);
+            const uint32_t byte = cvt_e2m1x2(qq.x, qq.y);
+            if (c < 4) wlo |= byte << (8 * c);
+            else whi |= byte << (8 * (c - 4));
+          }
+          const bool live = sdec > 0.0f;  // a zero scale codes the block as zeros
+          pw[2 * blk] = live ? wlo : 0u;
+          pw[2 * blk + 1] = live ? whi : 0u;
+          psc |= sc << (8 * blk);
+          lacc[blk] = __ffma2_rn(qsum, make_float2(f, f), lacc[blk]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 t = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), cs2, nm2);
+          const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+          lacc[c & 3] = __fadd2_rn(lacc[c & 3], p);
+          pk[c] = pack_f16x2(p.x, p.y);
+        }
       }
-      // P and O belong to the tensor core until PV(it-1) has finished.
-      if (it > 0) {
+      if constexpr (L::kFp4Pv) {
+        // P buffer b was read by PV(it-2); O may be rescaled only once PV(it-1)
+        // has finished (the later wait covers the earlier PV).
+        if (rescale_o || it >= 2) {
+          const uint32_t pit = it - (rescale_o ? 1u : 2u);
+          if (!mbar_wait_warp(&bars.pv_done[pit & 1u], (pit >> 1) & 1u, a.status)) return;
+          tc_fence_after();
+        }
+      } else if (it > 0) {
+        // P and O belong to the tensor core until PV(it-1) has finished.
         const uint32_t pit = it - 1u;
         if (!mbar_wait_warp(&bars.pv_done[pit & 1u], (pit >> 1) & 1u, a.status)) return;
         tc_fence_after();
@@ -525,10 +635,20 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
           tmem_st16(lane_base + ocol + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
         }
       }
-      // P of keys 64*half.. goes to P columns 32*half..
-      tmem_st16(lane_base + kColP + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-      tmem_st16(lane_base + kColP + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-      tmem_wait_st();
+      if constexpr (L::kFp4Pv) {
+        // keys 64*half.. are chunks 2*half, 2*half+1 of row r and k-step
+        // `half` of the scale atoms; the tensor core reads them next
+        uint8_t* pb = smem + L::kOffP + b * kPBuf;
+        *reinterpret_cast<uint4*>(pb + sw64_off(r, 2 * half)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        *reinterpret_cast<uint4*>(pb + sw64_off(r, 2 * half + 1)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+        *reinterpret_cast<uint32_t*>(pb + 8192 + 512 * half + (r & 31) * 16 + (r >> 5) * 4) = psc;
+        fence_proxy_async_smem();
+      } else {
+        // P of keys 64*half.. goes to P columns 32*half..
+        tmem_st16(lane_base + kColP + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(lane_base + kColP + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        tmem_wait_st();
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full[b]);
@@ -541,7 +661,10 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
     const float l_run = l_half + xl[(half ^ 1) * 128 + r];
     if (!mbar_wait_warp(bars.o_full, item_ctr & 1u, a.status)) return;
     tc_fence_after();
-    const float inv_l = (l_run > 0.0f) ? a.v_g / l_run : 0.0f;
+    // FP4 PV: O accumulated P's codes times its block scales; its global
+    // scale is applied here
+    const float o_mul = L::kFp4Pv ? kPScale : 1.0f;
+    const float inv_l = (l_run > 0.0f) ? a.v_g * o_mul / l_run : 0.0f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) +
                           (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) * kHeadDim + 64 * half;
     float* prow = item.part >= 0 ? part_slot(a, item) : nullptr;  // split item: partial O, m, l
@@ -558,8 +681,8 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
         float4* dst = reinterpret_cast<float4*>(prow + r * kHeadDim + 64 * half + 32 * c);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
-                               __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+          dst[i] = make_float4(__uint_as_float(ov[4 * i]) * o_mul, __uint_as_float(ov[4 * i + 1]) * o_mul,
+                               __uint_as_float(ov[4 * i + 2]) * o_mul, __uint_as_float(ov[4 * i + 3]) * o_mul);
       } else if (valid) {
         uint32_t pb[16];
 #pragma unroll
@@ -662,6 +785,132 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_prefill_dqahead_repack_sm103_kernel(const PrefillArgs a) {
   prefill_body<1, true>(a);
+}
+__global__ void __launch_bounds__(kThreads, 1)
+    nvfp4_prefill_a4q_fp4pv_sm103_kernel(const PrefillArgs a) {
+  prefill_body<2, true>(a);
+}
+
+// ---------------------------------------------------------------------------
+// Token-major V (FP4 PV).  One block per (16 token rows, head dimension d):
+// the rows' codes [16][64 B] and block scales [16][8 B] staged in shared
+// memory; the 16 values at d decoded without the tensor scale (exact: E2M1 x
+// E4M3) and coded by the cache's block codec with global scale 1.  Returns
+// the block's scale byte; codes in w0 (rows 0-7) and w1 (rows 8-15), row 2i in
+// the low nibble.
+__device__ __forceinline__ uint32_t token_major_block(const uint8_t* codes, const uint8_t* scales, int d,
+                                                      uint32_t& w0, uint32_t& w1) {
+  float x[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const uint32_t h2 = cvt_e2m1x2_to_f16x2(codes[t * 64 + (d >> 1)]);
+    const float e = __half2float(__ushort_as_half(static_cast<unsigned short>((d & 1) ? (h2 >> 16) : (h2 & 0xFFFFu))));
+    x[t] = e * e4m3_to_f32(scales[t * 8 + (d >> 4)]);
+  }
+  return quant_block16(x, 1.0f, w0, w1);
+}
+
+// FP4 PV repack pre-pass: each (request, kv head, KV tile) once -> one 18 KB
+// record laid out like a stage: K codes (64B-swizzled rows) | K scale atoms |
+// token-major V codes (64B-swizzled [head dim][128 keys / 2]) | their scale
+// atoms (k-step s: head dim d's four block scales at (d % 32) * 16 +
+// (d / 32) * 4).  Keys past kv_len are zeros, in K and in the V blocks.
+__global__ void __launch_bounds__(128) nvfp4_prefill_repack_fp4pv_kernel(PrefillArgs a) {
+  using L = Layout<2, true>;
+  __shared__ __align__(16) uint8_t sv[kBN * 64];  // the tile's V codes, as stored
+  __shared__ __align__(16) uint8_t ss[kBN * 8];   // and V block scales
+  const int tid = threadIdx.x;
+  const int total = a.work[1];
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    int lo = 0, hi = a.batch - 1;  // last b with tile_prefix[b] * Hkv <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.tile_prefix[mid] * a.num_kv_heads <= t) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int n_t = a.tile_prefix[b + 1] - a.tile_prefix[b];
+    const int r = t - a.tile_prefix[b] * a.num_kv_heads;
+    const int h = r / n_t, j = r - h * n_t;
+    const int kv_len = a.kv_lens[b];
+    uint8_t* rec = a.repack + static_cast<int64_t>(t) * L::kStageBytes;
+    auto row_of = [&](int key) -> int64_t {
+      const int abs_key = j * kBN + key;
+      if (abs_key >= kv_len) return -1;
+      const int pid = a.page_table[static_cast<int64_t>(b) * a.max_pages + (abs_key >> 4)];
+      if (pid < 0 || pid >= a.num_pages) {
+        set_status(a.status, kDevBadPage);
+        return -1;
+      }
+      return (static_cast<int64_t>(pid) * a.num_kv_heads + h) * kPageSize + (abs_key & 15);
+    };
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int u = tid + 128 * i, key = u >> 2, c = u & 3;
+      const int64_t row = row_of(key);
+      uint4 kw = make_uint4(0u, 0u, 0u, 0u), vw = make_uint4(0u, 0u, 0u, 0u);
+      if (row >= 0) {
+        kw = *reinterpret_cast<const uint4*>(a.k_data + row * 64 + 16 * c);
+        vw = *reinterpret_cast<const uint4*>(a.v_data + row * 64 + 16 * c);
+      }
+      *reinterpret_cast<uint4*>(rec + sw64_off(key, c)) = kw;
+      *reinterpret_cast<uint4*>(sv + key * 64 + 16 * c) = vw;
+    }
+    {
+      const int key = tid;
+      const int64_t row = row_of(key);
+      uint2 ks = make_uint2(0u, 0u), vs = make_uint2(0u, 0u);
+      if (row >= 0) {
+        ks = *reinterpret_cast<const uint2*>(a.k_scale + row * 8);
+        vs = *reinterpret_cast<const uint2*>(a.v_scale + row * 8);
+      }
+      *reinterpret_cast<uint32_t*>(rec + kKData + (key & 31) * 16 + (key >> 5) * 4) = ks.x;
+      *reinterpret_cast<uint32_t*>(rec + kKData + 512 + (key & 31) * 16 + (key >> 5) * 4) = ks.y;
+      *reinterpret_cast<uint2*>(ss + key * 8) = vs;
+    }
+    __syncthreads();
+    // thread = head dimension: eight 16-key blocks along the tile's tokens
+    const int d = tid;
+    uint8_t* vt = rec + L::kStageV;
+    uint32_t sc[2] = {0u, 0u};
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      uint32_t w0, w1;
+      const uint32_t sb = token_major_block(sv + kb * 16 * 64, ss + kb * 16 * 8, d, w0, w1);
+      *reinterpret_cast<uint2*>(vt + sw64_off(d, kb >> 1) + 8 * (kb & 1)) = make_uint2(w0, w1);
+      sc[kb >> 2] |= sb << (8 * (kb & 3));
+    }
+    *reinterpret_cast<uint32_t*>(vt + kVData + (d & 31) * 16 + (d >> 5) * 4) = sc[0];
+    *reinterpret_cast<uint32_t*>(vt + kVData + 512 + (d & 31) * 16 + (d >> 5) * 4) = sc[1];
+    __syncthreads();  // the staging buffers take the next tile
+  }
+}
+
+// The token-major blocks of whole pages, every slot as written: one CTA of
+// 128 threads (one per head dimension) per (listed page, kv head).
+__global__ void __launch_bounds__(128) nvfp4_v_token_major_kernel(TokenMajorArgs a) {
+  __shared__ __align__(16) uint8_t sv[kPageSize * 64];
+  __shared__ __align__(16) uint8_t ss[kPageSize * 8];
+  const int tid = threadIdx.x;
+  const int64_t total = static_cast<int64_t>(a.n_ids) * a.num_kv_heads;
+  for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+    const int i = static_cast<int>(w / a.num_kv_heads), h = static_cast<int>(w - static_cast<int64_t>(i) * a.num_kv_heads);
+    const int pid = a.page_ids[i];
+    const bool ok = pid >= 0 && pid < a.num_pages;
+    if (!ok && tid == 0) set_status(a.status, kDevBadPage);
+    const int64_t row0 = (static_cast<int64_t>(ok ? pid : 0) * a.num_kv_heads + h) * kPageSize;
+    if (tid < 64)
+      *reinterpret_cast<uint4*>(sv + tid * 16) =
+          ok ? *reinterpret_cast<const uint4*>(a.v_data + row0 * 64 + tid * 16) : make_uint4(0u, 0u, 0u, 0u);
+    else if (tid < 72)
+      *reinterpret_cast<uint4*>(ss + (tid - 64) * 16) =
+          ok ? *reinterpret_cast<const uint4*>(a.v_scale + row0 * 8 + (tid - 64) * 16) : make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    uint32_t w0, w1;
+    const uint32_t sb = token_major_block(sv, ss, tid, w0, w1);
+    *reinterpret_cast<uint2*>(a.codes + (w * kHeadDim + tid) * 8) = make_uint2(w0, w1);
+    a.scales[w * kHeadDim + tid] = static_cast<uint8_t>(sb);
+    __syncthreads();
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1038,7 +1287,17 @@ cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !repack) return e;
   if (variant == 0) return launch_prefill_a4q_2cta_repack(a, num_sms, s);
-  nvfp4_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a);
+  if (variant == 2) nvfp4_prefill_repack_fp4pv_kernel<<<num_sms * 8, 128, 0, s>>>(a);
+  else nvfp4_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+size_t prefill_fp4pv_record_bytes() { return Layout<2, true>::kStageBytes; }
+
+cudaError_t launch_v_token_major(const TokenMajorArgs& a, int num_sms, cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(a.n_ids) * a.num_kv_heads;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  nvfp4_v_token_major_kernel<<<static_cast<unsigned>(total < cap ? total : cap), 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -1059,6 +1318,7 @@ cudaError_t launch_prefill_merge(const PrefillArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s) {
+  if (variant == 2) return launch_main(nvfp4_prefill_a4q_fp4pv_sm103_kernel, Layout<2, true>::kAlloc, a, num_sms, s);
   if (variant == 0)
     return repack ? launch_prefill_a4q_2cta(a, num_sms, s)
                   : launch_main(nvfp4_prefill_a4q_sm103_kernel, Layout<0, false>::kAlloc, a, num_sms, s);

@@ -84,8 +84,9 @@ def test_invalid_arguments_rejected_on_host(nk):
                                             null, ws, 64, null)
     assert lib.nvfp4_paged_prefill(*args(3, 0, 16)) == -1
     assert lib.nvfp4_paged_prefill(*args(6, 0, 16)) == -1   # ratio 3 is not a power of two
-    assert lib.nvfp4_paged_prefill(*args(4, 2, 16)) == -1
+    assert lib.nvfp4_paged_prefill(*args(4, 3, 16)) == -1
     assert lib.nvfp4_paged_prefill(*args(4, 0, null)) == -3
+    assert lib.nvfp4_paged_prefill(*args(4, 2, 16)) == -3   # FP4 PV needs room for its records
     assert lib.nvfp4_paged_prefill(*args(4, 0, 16, -1.0)) == -1          # query scale must be >= 0
     assert lib.nvfp4_paged_prefill(*args(4, 0, 16, float("nan"))) == -1  # and finite
     # decode: group of 32 unsupported; workspace too small
@@ -117,6 +118,21 @@ def test_plan_run_and_noalloc_reject_bad_arguments_on_host(nk):
         16, 16, hq, ctypes.byref(d), 16, 1, 16, 16, 1, 1, 0.1, 0, 0.0, 16, null, null)
     assert noalloc(0) == -1
     assert noalloc(3) == -1
+
+
+def test_token_major_rejects_bad_arguments_on_host(nk):
+    """nvfp4_v_token_major checks its cache and buffers before any device
+    work; an empty list is a no-op."""
+    lib = nk.lib
+    null = None
+    d = nk.CacheDesc(16, 16, 32, 48, 4, 16, 2, 128, 1.0, 1.0)
+    assert lib.nvfp4_v_token_major(null, 16, 1, 16, 16, null) == -1     # no cache
+    assert lib.nvfp4_v_token_major(ctypes.byref(d), 16, -1, 16, 16, null) == -1
+    assert lib.nvfp4_v_token_major(ctypes.byref(d), 16, 0, null, null, null) == 0
+    assert lib.nvfp4_v_token_major(ctypes.byref(d), null, 1, 16, 16, null) == -1
+    assert lib.nvfp4_v_token_major(ctypes.byref(d), 16, 1, 12, 16, null) == -1   # codes not 8-byte aligned
+    bad = nk.CacheDesc(16, 16, 32, 48, 4, 16, 2, 64, 1.0, 1.0)                 # head_dim 64
+    assert lib.nvfp4_v_token_major(ctypes.byref(bad), 16, 1, 16, 16, null) == -1
 
 
 def test_header_and_library_from_plain_c(nk, tmp_path):

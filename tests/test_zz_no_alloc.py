@@ -68,3 +68,18 @@ def test_noalloc_rejects_oversized_schedule():
     torch.cuda.synchronize()
     assert nk.nvfp4kv_get_device_status() == 0
     assert np.isfinite(q.float().cpu().numpy()).all()
+
+
+def test_noalloc_refuses_the_fp4pv_variant():
+    """The FP4 PV variant reads only repacked records, which the static array
+    (a schedule only) does not hold: refused before any launch."""
+    nk = G.nk()
+    dev = G.dev()
+    inp = G.inputs("tiny")
+    cache = G.gpu_cache(inp)
+    args = (inp.q.to(dev), cache, inp.page_table.to(dev), inp.kv_lens.to(dev), inp.qo_indptr.to(dev))
+    with pytest.raises(nk.NvFp4Error) as e:
+        nk.nvfp4_paged_prefill_noalloc(*args, variant=nk.VARIANT_A4Q_FP4PV)
+    assert e.value.code == nk.NVFP4KV_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert nk.nvfp4kv_get_device_status() == 0
