@@ -136,11 +136,14 @@ def prefill_flops_split(wl: W.Workload):
     return f / 2, f / 2
 
 
-def prefill_roof_s(wl: W.Workload, peaks, a4q: bool = True) -> float:
+def prefill_roof_s(wl: W.Workload, peaks, a4q=True) -> float:
     """Tensor-roofline time of one prefill: QK at the FP4 rate and PV at the
-    16-bit rate (A4Q), or both at the 16-bit rate (dequant-ahead)."""
+    16-bit rate (A4Q, a4q True), both at the 16-bit rate (dequant-ahead, a4q
+    False), or both at the FP4 rate (a4q "fp4": the FP4 PV experiment)."""
     f_qk, f_pv = prefill_flops_split(wl)
     p16 = peaks["bf16_tflops"] * 1e12
+    if a4q == "fp4":
+        return (f_qk + f_pv) / (p16 * FP4_OVER_BF16)
     return (f_qk / (p16 * FP4_OVER_BF16) + f_pv / p16) if a4q else (f_qk + f_pv) / p16
 
 
@@ -313,6 +316,7 @@ def run_ours(args, rank, world, dev):
     dqa = nk_bench.time_fn(lambda: prefill(nk.VARIANT_DQ_AHEAD), K, 3)
     pre_ik = nk_bench.time_fn(lambda: prefill(nk.VARIANT_A4Q, "ws_min"), K, 3)
     dqa_ik = nk_bench.time_fn(lambda: prefill(nk.VARIANT_DQ_AHEAD, "ws_min"), K, 3)
+    fp4pv = nk_bench.time_fn(lambda: prefill(nk.VARIANT_A4Q_FP4PV), K, 3)
     app_bytes = APPEND_BYTES_PER_TOKEN_HEAD * wl.total_kv * wl.num_kv_heads
     comps = {
         "append": dict(gbs_entry(app, app_bytes, peaks, app_g), copy_same_bytes=copy_reference(nk_bench, app_bytes, K)),
@@ -320,6 +324,7 @@ def run_ours(args, rank, world, dev):
         "prefill_a4q_inkernel": tflops_entry(pre_ik, wl, peaks, True, "V dequantized in the kernel"),
         "prefill_dq_ahead": tflops_entry(dqa, wl, peaks, False, "K and V repacked once per KV tile"),
         "prefill_dq_ahead_inkernel": tflops_entry(dqa_ik, wl, peaks, False, "K and V dequantized in the kernel"),
+        "prefill_a4q_fp4pv": tflops_entry(fp4pv, wl, peaks, "fp4", FP4PV_MODE),
     }
     if not args.no_matrix:
         comps["shortq"] = shortq_component(nk, nk_bench, dev, K, peaks)
@@ -394,9 +399,10 @@ def tflops_entry(times, wl, peaks, a4q, mode):
     """Component entry of a prefill: mean time, TFLOP/s and the fraction of
     its tensor roofline (mixed FP4/16-bit for A4Q, 16-bit for dequant-ahead)."""
     t = statistics.mean(times)
+    roof = "FP4 QK + FP4 PV" if a4q == "fp4" else "FP4 QK + 16-bit PV" if a4q else "16-bit QK + PV"
     return {"workload": wl.name, "ms": round(t, 4), "TFLOP/s": round(wl.flops() / (t * 1e-3) / 1e12, 2),
             "frac_of_roofline": round(prefill_roof_s(wl, peaks, a4q) / (t * 1e-3), 4),
-            "roofline": "FP4 QK + 16-bit PV" if a4q else "16-bit QK + PV", "mode": mode}
+            "roofline": roof, "mode": mode}
 
 
 class PrefillCase:
@@ -428,6 +434,10 @@ class PrefillCase:
                                     sm_scale=self.inp.sm_scale, variant=variant, out=self.out, workspace=self.ws)
 
 
+FP4PV_MODE = ("experiment: A4Q QK, then P coded to NVFP4 per 16 keys and V re-coded once per 128-key tile "
+              "along tokens, PV on block-scaled FP4 MMA (one CTA per SM)")
+
+
 def shortq_component(nk, nk_bench, dev, K, peaks):
     """Batch 4 x q 128 at the end of kv 2,048, 32/8 heads, permuted pages (the
     repack comparison shape): both variants, repack mode (four q tiles per kv
@@ -436,8 +446,10 @@ def shortq_component(nk, nk_bench, dev, K, peaks):
     wl = c.inp.wl
     a = nk_bench.time_fn(lambda: c.prefill(nk.VARIANT_A4Q), K, 3)
     d = nk_bench.time_fn(lambda: c.prefill(nk.VARIANT_DQ_AHEAD), K, 3)
+    f = nk_bench.time_fn(lambda: c.prefill(nk.VARIANT_A4Q_FP4PV), K, 3)
     return {"a4q": tflops_entry(a, wl, peaks, True, "repack"),
-            "dq_ahead": tflops_entry(d, wl, peaks, False, "repack")}
+            "dq_ahead": tflops_entry(d, wl, peaks, False, "repack"),
+            "a4q_fp4pv": tflops_entry(f, wl, peaks, "fp4", FP4PV_MODE)}
 
 
 def tails_component(nk, nk_bench, dev, K, peaks):
@@ -694,9 +706,10 @@ def kernel_rows(out: torch.Tensor, inp: W.Inputs, rows):
     return {(b, i): o[int(inp.qo_indptr[b]) + i] for b, i in rows}
 
 
-def accuracy_run(nk, dev, inp, rows, schemes=("per_row",)):
+def accuracy_run(nk, dev, inp, rows, schemes=("per_row",), fp4pv=False):
     """Kernel outputs on `rows` of one workload: the BF16-query dequant-ahead
-    prefill and the A4Q prefill under each query scale scheme."""
+    prefill and the A4Q prefill under each query scale scheme (and the FP4 PV
+    experiment)."""
     c = PrefillCase(nk, dev, inp)
     res = {}
     c.prefill(nk.VARIANT_DQ_AHEAD)
@@ -707,6 +720,9 @@ def accuracy_run(nk, dev, inp, rows, schemes=("per_row",)):
                                variant=nk.VARIANT_A4Q, out=c.out, workspace=c.ws,
                                q_global_scale=q_scale_for(sch, inp.q))
         res[sch] = kernel_rows(c.out, inp, rows)
+    if fp4pv:
+        c.prefill(nk.VARIANT_A4Q_FP4PV)
+        res["fp4pv"] = kernel_rows(c.out, inp, rows)
     torch.cuda.synchronize(dev)
     st = nk.nvfp4kv_get_device_status()
     if st != 0:
@@ -726,11 +742,12 @@ def a4q_error_report(nk, dev):
                          ("prefill32k", lambda wl: W.sample_rows(wl, 3))):
         inp = inputs_of(cfg)
         rows = rows_of(inp.wl)
-        k = accuracy_run(nk, dev, inp, rows)
+        k = accuracy_run(nk, dev, inp, rows, fp4pv=True)
         ex = exact_rows(inp, rows)
         per[cfg] = {"workload": inp.wl.name, "values": inp.wl.dist, "rows": len(rows),
                     "a4q_vs_bf16q": err_stats(k["per_row"], k["bf16q"]),
-                    "a4q_vs_exact": err_stats(k["per_row"], ex), "bf16q_vs_exact": err_stats(k["bf16q"], ex)}
+                    "a4q_vs_exact": err_stats(k["per_row"], ex), "bf16q_vs_exact": err_stats(k["bf16q"], ex),
+                    "fp4pv_vs_a4q": err_stats(k["fp4pv"], k["per_row"]), "fp4pv_vs_exact": err_stats(k["fp4pv"], ex)}
     sweep = {}
     for L in (1024, 4096, 16384, 32768):
         wl = W.Workload(f"tail_q64_kv{L}_h32x8_outliers", [64], [L], 32, 8, dist="outliers", seed=L)
@@ -745,6 +762,7 @@ def a4q_error_report(nk, dev):
     return {"q_scheme": Q_SCHEMES["per_row"] + "; then one E4M3 scale per 16 values (nearest even) and E2M1 "
                                                "codes (nearest even), the cache's block codec",
             "outputs": "o_a4q: A4Q kernel; o_bf16q: dequant-ahead kernel (BF16 query) on the same NVFP4 cache; "
+                       "o_fp4pv: the FP4 PV experiment (A4Q QK, NVFP4 P, V re-coded along tokens); "
                        "o_exact: float64 attention on the unquantized bf16 Q, K, V",
             "configs": per,
             "q_scheme_x_kv_len": {"workload": "64-query tail at the end of kv_len keys, 32/8 heads, N(0,1) with "
