@@ -3,10 +3,12 @@
 // "Decode can win on fewer bytes read": decode re-reads the whole history and
 // is bandwidth-bound, so fewer bytes per token is the win).
 //
-// Split-KV: a work item is (request, kv head, split of up to 1024 tokens).  A
-// schedule kernel writes one record per item, full splits first and then the
-// shorter last splits, longest first; one persistent wave of CTAs (3 per SM)
-// claims records from a counter.  An item streams through two shared-memory
+// Split-KV: a work item is (request, kv head, split of up to S tokens), S one
+// of 1024, 2048, 4096 or 8192: the schedule kernel takes the longest that
+// still gives every attention CTA two items (each item costs a prologue, a
+// merge of the four warps and a partial result).  It writes one record per
+// item, full splits first and then the shorter last splits, longest first;
+// one persistent wave of CTAs (3 per SM) claims records from a counter.  An item streams through two shared-memory
 // stages of 256 tokens (K/V codes 1 KB + scales 128 B per page, gathered with
 // cp.async by all threads and completing on one mbarrier), so the next unit's
 // bytes are in flight while the current one is computed.  (Per-page bulk
@@ -124,18 +126,19 @@ struct DecFmt {
 constexpr int kDecCtasPerSm = 3;
 
 struct DecItem {
-  int b, h, split, n_tok, n_units;
+  int b, h, split, tok0, n_tok, n_units;
 };
 
 // The schedule lists item records (request, kv head, split, tokens): full
-// 1024-token items first, then the shorter last splits.  CTAs claim records
-// in that order from a counter (sched[1]), so the short items fill the tail.
+// S-token items first, then the shorter last splits.  CTAs claim records in
+// that order from a counter (sched[1]), so the short items fill the tail.
 template <bool FP8>
-__device__ __forceinline__ DecItem item_of(int4 r) {
+__device__ __forceinline__ DecItem item_of(int4 r, int split_len) {
   DecItem it;
   it.b = r.x;
   it.h = r.y;
   it.split = r.z;
+  it.tok0 = r.z * split_len;
   it.n_tok = r.w;
   it.n_units = (r.w + DecFmt<FP8>::kUnit - 1) / DecFmt<FP8>::kUnit;
   return it;
@@ -145,13 +148,17 @@ __device__ __forceinline__ DecItem item_of(int4 r) {
 // at most two units ahead of the compute, so at most three items are live.
 struct ClaimRing {
   int4 rec[4];
-  int n_valid;  // records claimed so far that hold an item
-  int done;     // the schedule is exhausted
+  int n_valid;    // records claimed so far that hold an item
+  int done;       // the schedule is exhausted
+  int split_len;  // S of this call (sched[2])
 };
 
-// Claim the next record (all threads call it; thread 0 takes the counter).
+// Claim the next record.  Every thread calls it, every time (its barrier
+// must be met by all threads); only thread 0 reads or writes the ring's
+// state before the barrier, and it claims nothing once the schedule is
+// exhausted.
 __device__ __forceinline__ void claim_item(const DecodeArgs& a, ClaimRing* ring) {
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && !ring->done) {
     const int idx = atomicAdd(a.sched + 1, 1);
     if (idx < a.sched[0]) {
       ring->rec[ring->n_valid & 3] = reinterpret_cast<const int4*>(a.sched + 4)[idx];
@@ -177,7 +184,7 @@ __device__ __forceinline__ int unit_page(const DecodeArgs& a, const DecItem& it,
   const int p = tid / DecFmt<FP8>::kThrPerPage;
   if (p * kPageSize >= unit_tokens<FP8>(it, u)) return -1;
   return a.page_table[static_cast<int64_t>(it.b) * a.max_pages +
-                      (it.split * kDecSplit + u * DecFmt<FP8>::kUnit) / kPageSize + p];
+                      (it.tok0 + u * DecFmt<FP8>::kUnit) / kPageSize + p];
 }
 
 // All 128 threads gather unit u of an item into `stage` with cp.async: thread
@@ -275,7 +282,7 @@ struct UnitCursor {
 template <bool FP8>
 __device__ __forceinline__ void cursor_load(ClaimRing* ring, UnitCursor& c) {
   c.has = c.ci < ring->n_valid;
-  if (c.has) c.it = item_of<FP8>(ring->rec[c.ci & 3]);
+  if (c.has) c.it = item_of<FP8>(ring->rec[c.ci & 3], ring->split_len);
 }
 template <bool FP8>
 __device__ __forceinline__ void cursor_start(const DecodeArgs& a, ClaimRing* ring, UnitCursor& c) {
@@ -289,12 +296,12 @@ __device__ __forceinline__ void cursor_next(const DecodeArgs& a, ClaimRing* ring
   if (++c.u >= c.it.n_units) {
     c.u = 0;
     ++c.ci;
-    if (!ring->done) claim_item(a, ring);  // uniform: ring->done is read after a barrier
+    claim_item(a, ring);
     cursor_load<FP8>(ring, c);
   }
 }
 
-// Persistent: CTAs claim items from the schedule.  Each item (up to 1024
+// Persistent: CTAs claim items from the schedule.  Each item (up to S
 // tokens) streams through two shared-memory stages of one unit (256 tokens
 // of NVFP4, 128 of FP8), so the copies of the next unit run while the current
 // one is computed; the four warps' partial results are merged once per item.
@@ -322,6 +329,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a) {
   __syncthreads();
   grid_dep_launch();  // the combine grid may be scheduled as CTAs finish
   grid_dep_wait();    // the schedule written by the plan kernel
+  if (tid == 0) ring.split_len = a.sched[2];  // seen by all after the first claim's barrier
   // issue cursor: two units ahead of the compute
   UnitCursor ic;
   cursor_start<FP8>(a, &ring, ic);
@@ -335,7 +343,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a) {
   bool q_ready = false;  // qr holds the query rows of the next item to compute
   uint32_t uc = 0;  // units consumed: stage uc & 1, phase (uc >> 1) & 1
   for (int k = 0; k < ring.n_valid; ++k) {
-    it = item_of<FP8>(ring.rec[k & 3]);
+    it = item_of<FP8>(ring.rec[k & 3], ring.split_len);
     const int b = it.b, h = it.h;
     if (!q_ready) load_q_raw<G>(a, it, g, t, qr);
     q_ready = false;
@@ -402,7 +410,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a) {
       // the next item's query rows once that item is claimed
       const int pid_next = ic.has ? unit_page<FP8>(a, ic.it, ic.u, tid) : -1;
       if (!q_ready && k + 1 < ring.n_valid) {
-        load_q_raw<G>(a, item_of<FP8>(ring.rec[(k + 1) & 3]), g, t, qr);
+        load_q_raw<G>(a, item_of<FP8>(ring.rec[(k + 1) & 3], ring.split_len), g, t, qr);
         q_ready = true;
       }
       const bool ok = mbar_wait(&bars[stg], (uc >> 1) & 1, a.status);
@@ -607,7 +615,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a) {
           }
         }
         __syncthreads();
-        const bool single = a.kv_lens[b] <= kDecSplit;
+        const bool single = a.kv_lens[b] <= ring.split_len;
         // per head: the combined max and sum, and each warp's weight
         // exp2(m_w - m) / L, computed once
         if (tid < G) {
@@ -700,19 +708,40 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2* warp_sums, i
   return make_int2(x.x + before.x - v.x, x.y + before.y - v.y);
 }
 
-// Schedule: one record per (request, kv head, 1024-token split).  All full
-// splits come first; then each request's shorter last split, longest first,
-// so that the items claimed last are the shortest.  Requests are taken
-// kPlanThreads at a time (one pass for the usual batch sizes); the
-// longest-first order holds within each such chunk.  Every CTA of the grid
-// computes the same prefix sums and writes its share of the records.
+// Schedule: one record per (request, kv head, S-token split).  S is the
+// longest of kDecSplit << k (k < kDecSplitSteps) whose items number at least
+// two per attention CTA, else kDecSplit.  All full splits come first; then
+// each request's shorter last split, longest first, so that the items
+// claimed last are the shortest.  Requests are taken kPlanThreads at a time
+// (one pass for the usual batch sizes); the longest-first order holds within
+// each such chunk.  Every CTA of the grid computes the same S and prefix
+// sums and writes its share of the records.
 constexpr int kPlanThreads = 256, kPlanCtas = 16;
+static_assert(kDecSplitSteps == 4, "the split choice reduces four counts");
 __global__ void __launch_bounds__(kPlanThreads) nvfp4_decode_plan_kernel(DecodeArgs a) {
   grid_dep_launch();  // the attention grid may start its prologue now
   __shared__ int2 warp_sums[32];
   __shared__ int req_len[kPlanThreads], req_first[kPlanThreads], req_fpos[kPlanThreads], req_ppos[kPlanThreads];
   int4* items = reinterpret_cast<int4*>(a.sched + 4);
   const int tid = threadIdx.x, H = a.num_kv_heads, cap = a.max_pages * kPageSize;
+  // ---- the split length S
+  int split_len = kDecSplit;
+  {
+    int c[kDecSplitSteps] = {0, 0, 0, 0};  // items per kv head for each candidate
+    for (int b = tid; b < a.batch; b += blockDim.x) {
+      const int kv = a.kv_lens[b];
+      if (kv > 0 && kv <= cap)
+#pragma unroll
+        for (int k = 0; k < kDecSplitSteps; ++k) c[k] += (kv + (kDecSplit << k) - 1) / (kDecSplit << k);
+    }
+    int2 t01, t23;
+    block_exclusive_scan2(make_int2(c[0], c[1]), warp_sums, &t01);
+    block_exclusive_scan2(make_int2(c[2], c[3]), warp_sums, &t23);
+    const int tot[kDecSplitSteps] = {t01.x, t01.y, t23.x, t23.y};
+#pragma unroll
+    for (int k = 1; k < kDecSplitSteps; ++k)
+      if (static_cast<int64_t>(tot[k]) * H >= 2 * static_cast<int64_t>(a.ctas)) split_len = kDecSplit << k;
+  }
   // total of the full items of all requests (the partial ones follow them)
   int n_full_total = 0;
   if (a.batch > static_cast<int>(blockDim.x)) {
@@ -720,7 +749,7 @@ __global__ void __launch_bounds__(kPlanThreads) nvfp4_decode_plan_kernel(DecodeA
       const int b = base + tid;
       const int kv_len = b < a.batch ? a.kv_lens[b] : 0;
       int2 tot;
-      block_exclusive_scan2(make_int2(kv_len > 0 && kv_len <= cap ? kv_len / kDecSplit : 0, 0), warp_sums, &tot);
+      block_exclusive_scan2(make_int2(kv_len > 0 && kv_len <= cap ? kv_len / split_len : 0, 0), warp_sums, &tot);
       n_full_total += tot.x * H;
     }
   }
@@ -734,7 +763,7 @@ __global__ void __launch_bounds__(kPlanThreads) nvfp4_decode_plan_kernel(DecodeA
       if (kv_len > cap) set_status(a.status, kDevBadShape);
       if (kv_len < 0 || kv_len > cap) kv_len = 0;
     }
-    const int full = kv_len / kDecSplit, plen = kv_len % kDecSplit;
+    const int full = kv_len / split_len, plen = kv_len % split_len;
     req_len[tid] = plen;
     int2 tot;
     const int2 ex = block_exclusive_scan2(make_int2(full, plen > 0 ? 1 : 0), warp_sums, &tot);
@@ -761,11 +790,11 @@ __global__ void __launch_bounds__(kPlanThreads) nvfp4_decode_plan_kernel(DecodeA
         const int mid = (lo + hi + 1) >> 1;
         if (req_first[mid] <= i) lo = mid; else hi = mid - 1;
       }
-      const int len = req_len[lo], rfull = len / kDecSplit;
+      const int len = req_len[lo], rfull = len / split_len;
       const int j = i - req_first[lo];
       const int sp = j / H, h = j - sp * H;
-      if (sp < rfull) items[req_fpos[lo] + sp * H + h] = make_int4(base + lo, h, sp, kDecSplit);
-      else items[req_ppos[lo] + h] = make_int4(base + lo, h, rfull, len - rfull * kDecSplit);
+      if (sp < rfull) items[req_fpos[lo] + sp * H + h] = make_int4(base + lo, h, sp, split_len);
+      else items[req_ppos[lo] + h] = make_int4(base + lo, h, rfull, len - rfull * split_len);
     }
     __syncthreads();
     full_carry += tot.x * H;
@@ -774,6 +803,7 @@ __global__ void __launch_bounds__(kPlanThreads) nvfp4_decode_plan_kernel(DecodeA
   if (tid == 0 && blockIdx.x == 0) {
     a.sched[0] = full_carry + part_carry;
     a.sched[1] = 0;  // claim counter of the attention kernel
+    a.sched[2] = split_len;
   }
 }
 
@@ -794,7 +824,8 @@ __global__ void __launch_bounds__(128) nvfp4_decode_combine_kernel(DecodeArgs a)
     if (a.lse && d == 0) a.lse[static_cast<int64_t>(b) * a.num_q_heads + hq] = -INFINITY;
     return;
   }
-  const int n_s = (kv_len + kDecSplit - 1) / kDecSplit;
+  const int split_len = a.sched[2];
+  const int n_s = (kv_len + split_len - 1) / split_len;
   if (n_s <= 1) return;
   const int64_t base = static_cast<int64_t>(b) * a.max_splits * a.num_q_heads + hq;
   float m = -INFINITY;
@@ -858,13 +889,15 @@ cudaError_t launch_dependent(void (*kernel)(DecodeArgs), dim3 grid, dim3 block, 
 
 template <int G, bool FP8>
 cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStream_t s) {
-  nvfp4_decode_plan_kernel<<<kPlanCtas, kPlanThreads, 0, s>>>(a);
+  DecodeArgs b = a;
+  b.ctas = num_sms * kDecCtasPerSm;
+  nvfp4_decode_plan_kernel<<<kPlanCtas, kPlanThreads, 0, s>>>(b);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   void (*kern)(DecodeArgs) = FP8 ? fp8_paged_decode_kernel<G> : nvfp4_paged_decode_kernel<G>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DecFmt<FP8>::kSmem);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(kern, dim3(num_sms * kDecCtasPerSm), dim3(128), DecFmt<FP8>::kSmem, s, a);
+  e = launch_dependent(kern, dim3(b.ctas), dim3(128), DecFmt<FP8>::kSmem, s, b);
   if (e != cudaSuccess) return e;
   const size_t wbytes = static_cast<size_t>(a.max_splits) * sizeof(float);  // split weights
   if (wbytes > 48 * 1024) {
@@ -872,7 +905,7 @@ cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStr
                              static_cast<int>(wbytes));
     if (e != cudaSuccess) return e;
   }
-  return launch_dependent(nvfp4_decode_combine_kernel, dim3(a.num_q_heads, batch), dim3(128), wbytes, s, a);
+  return launch_dependent(nvfp4_decode_combine_kernel, dim3(a.num_q_heads, batch), dim3(128), wbytes, s, b);
 }
 
 template <bool FP8>

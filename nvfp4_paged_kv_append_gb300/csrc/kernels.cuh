@@ -49,7 +49,11 @@ struct DequantArgs {
 };
 
 // ---- decode --------------------------------------------------------------------
-constexpr int kDecSplit = 1024;  // tokens per work item (one partial result)
+// Decode work items cover kDecSplit << k tokens (one partial result each),
+// k = 0 .. kDecSplitSteps - 1, chosen per call by the schedule kernel; the
+// workspace holds the partials of the shortest.
+constexpr int kDecSplit = 1024;
+constexpr int kDecSplitSteps = 4;
 constexpr int kDecUnit = 256;    // tokens per shared-memory stage (16 pages)
 constexpr int kDecWarps = 4;
 
@@ -67,7 +71,8 @@ struct DecodeArgs {
   int num_q_heads;
   int max_splits;
   int batch;
-  int* sched;         // [0] item count; item records (int4 b, h, split, n_tok) from sched + 4
+  int ctas;           // CTAs of the attention grid (the schedule sizes items for it)
+  int* sched;         // [0] item count, [1] claim counter, [2] split length; records (int4 b, h, split, n_tok) from sched + 4
   float k_g, v_g, sm_scale;
   void* o;            // bf16 [B][Hq][128]
   float* lse;         // optional [B][Hq]

@@ -12,17 +12,23 @@ from . import _gpu as G
 pytestmark = pytest.mark.gpu
 
 
-def _decode_case(wl, fill=0, sample=None):
+def _decode_case(wl, fill=0, sample=None, split_len=None):
     inp = W.make_inputs(wl)
     b = G.nk()
     cache = G.gpu_cache(inp, fill=fill)
     # the decode query of request b is its (single) query row
     q = inp.q.to(G.dev())
+    pt = inp.page_table.to(G.dev())
     lse = torch.full((wl.batch, wl.num_q_heads), float("nan"), device=G.dev())
-    o = b.nvfp4_paged_decode(q, cache, inp.page_table.to(G.dev()), inp.kv_lens.to(G.dev()), sm_scale=inp.sm_scale,
-                             lse=lse)
+    ws = torch.empty(b.nvfp4_workspace_bytes(b.OP_DECODE, wl.batch, wl.num_q_heads, wl.num_kv_heads, 0,
+                                             pt.shape[1] * 16), dtype=torch.uint8, device=G.dev())
+    o = b.nvfp4_paged_decode(q, cache, pt, inp.kv_lens.to(G.dev()), sm_scale=inp.sm_scale, lse=lse, workspace=ws)
     torch.cuda.synchronize()
     assert b.nvfp4kv_get_device_status() == 0
+    if split_len is not None:
+        # the schedule header (item count, claim counter, split length) opens
+        # the workspace: the schedule kernel chose the expected item length
+        assert int(ws[:16].view(torch.int32)[2]) == split_len
     reqs = range(wl.batch) if sample is None else sample
     rows = [(r, 0) for r in reqs if wl.kv_lens[r] > 0]
     pools = G.oracle_pools(inp)
@@ -54,7 +60,19 @@ def test_decode_full_size_all_requests():
     """32 requests with kv_len ~ U[1K, 32K], 32/8 heads, at full size (the
     benchmark's decode batch); the oracle checks every request and head."""
     wl = W.decode_batch()
-    mx, fro, lerr, _, _ = _decode_case(wl)
+    mx, fro, lerr, _, _ = _decode_case(wl, split_len=4096)
+    assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
+    assert lerr <= 1e-3
+
+
+def test_decode_split_length_2048():
+    """Enough work for 2,048-token items but not for 4,096 ones (at least two
+    items per attention CTA on 152 SMs): 20 requests of 14K-16K keys, 32/8
+    heads, every request against the oracle."""
+    rng = np.random.default_rng(33)
+    kv = [int(x) for x in rng.integers(14000, 16001, size=20)]
+    wl = W.Workload("dec_split2048", [1] * 20, kv, 32, 8, seed=33)
+    mx, fro, lerr, _, _ = _decode_case(wl, split_len=2048)
     assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
     assert lerr <= 1e-3
 
