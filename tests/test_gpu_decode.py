@@ -121,3 +121,35 @@ def test_decode_kv_len_beyond_table_flagged():
     ref = G.oracle_prefill(pools, inp, "bf16", causal=False, rows=[(0, 0), (2, 0)])
     mx, fro, _ = G.compare_rows(got, ref, inp.qo_indptr)
     assert mx <= G.MAX_ABS and fro <= G.REL_FRO, (mx, fro)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp8"])
+def test_decode_repeatable(fmt):
+    """The batch-32 decode gives the same bits on every call, whatever the
+    workspace held before: items are claimed in a different order by
+    different CTAs each time, the split merges run wherever the last split
+    finishes, and no result may depend on that."""
+    wl = W.decode_batch()
+    inp = W.make_inputs(wl)
+    b = G.nk()
+    d = G.dev()
+    if fmt == "fp8":
+        cache = b.Fp8Cache(inp.num_pages, wl.num_kv_heads, W.fp8_scale(inp.k), W.fp8_scale(inp.v), device=d)
+        b.fp8_kv_append(inp.k.to(d), inp.v.to(d), inp.slot_mapping.to(d), cache)
+        dec, wsb = b.fp8_paged_decode, b.fp8_workspace_bytes
+    else:
+        cache = G.gpu_cache(inp)
+        dec, wsb = b.nvfp4_paged_decode, b.nvfp4_workspace_bytes
+    q, pt, kvl = inp.q.to(d), inp.page_table.to(d), inp.kv_lens.to(d)
+    ws = torch.empty(wsb(b.OP_DECODE, wl.batch, wl.num_q_heads, wl.num_kv_heads, 0, pt.shape[1] * 16),
+                     dtype=torch.uint8, device=d)
+    outs = []
+    for i in range(8):
+        ws.fill_(i * 41 % 256)
+        lse = torch.empty(wl.batch, wl.num_q_heads, device=d)
+        o = dec(q, cache, pt, kvl, sm_scale=inp.sm_scale, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((o.view(torch.int16).cpu(), lse.view(torch.int32).cpu()))
+    assert b.nvfp4kv_get_device_status() == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
