@@ -76,10 +76,10 @@ constexpr int kLoaderWarp0 = 1, kLoaderWarp1 = 2;
 constexpr int kLoaderThreads = 64;
 constexpr int kTransformTid0 = 128, kSoftmaxTid0 = 256;
 
-// TMEM columns: S double buffer (fp32), O (fp32), P (FP16 pairs, one tile),
-// Q block scales, K block scales (double buffer)
-// (FP4 PV: P and V block scales, double buffered, over P's columns)
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384, kColSFA = 448, kColSFB = 456;
+// TMEM columns: S double buffer (fp32; each half's P as FP16 pairs over the
+// first 32 of its 64 columns), O (fp32), Q block scales, K block scales
+// (double buffer); FP4 PV: P and V block scales (double buffered)
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA = 448, kColSFB = 456;
 constexpr uint32_t kColSFP = 384, kColSFV = 400;
 constexpr uint32_t kTmemCols = 512;
 
@@ -264,8 +264,10 @@ __device__ void qk_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
       if constexpr (!L::kA4Q && !REPACK) {
         if (!mbar_wait(&bars.sfb_full[b], (it >> 1) & 1u, a.status)) return;
       }
-      // S buffer b held S(it-2) until the softmax loaded it
-      if (it >= 2 && !mbar_wait(&bars.s_free[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+      // S buffer b held S(it-2), and P(it-2) over it, until PV(it-2) read P
+      // (FP4 PV: P is in shared memory, so until the softmax loaded S)
+      if (it >= 2 && !mbar_wait(L::kFp4Pv ? &bars.s_free[b] : &bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status))
+        return;
       tc_fence_after();
       const uint32_t s_col = b ? kColS1 : kColS0;
       const uint32_t stage_s = smem_u32(smem + L::kOffStage + st * L::kStageBytes);
@@ -273,7 +275,7 @@ __device__ void qk_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
         // In-kernel mode the K codes and scale atoms arrived through
         // cp.async (generic proxy); the tensor core reads them next.
         if constexpr (!REPACK) fence_proxy_async_smem();
-        // SFB buffer b was last read by QK(it-2), finished before s_free(it-2).
+        // SFB buffer b was last read by QK(it-2), finished before the wait above.
         const uint32_t at_s = stage_s + kKData;
         tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b, smem_desc(at_s, 0, 128, kSwzNone));
         tc_cp_32x128b_warpx4(tbase + kColSFB + 8 * b + 4, smem_desc(at_s + 512, 0, 128, kSwzNone));
@@ -318,6 +320,7 @@ __device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
       tc_fence_after();
       const uint32_t v_s = REPACK ? smem_u32(smem + L::kOffStage + st * L::kStageBytes + L::kStageV)
                                   : smem_u32(smem + L::kOffV + b * kTile16);
+      const uint32_t s_col = b ? kColS1 : kColS0;  // P(it) is over the first half of each half's S
       if constexpr (L::kFp4Pv) {
         // P (codes and scale atoms, written by the softmax warps) and the
         // record's token-major V.  Scale buffer b was last read by PV(it-2),
@@ -336,8 +339,8 @@ __device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
       } else {
 #pragma unroll
         for (uint32_t k = 0; k < 8; ++k) {
-          mma_f16_ts(tbase + kColO, tbase + kColP + 8 * k, smem_desc(v_s + k * 2048, 16384, 1024, kSwz128), idesc_pv,
-                     (j == 0 && k == 0) ? 0u : 1u);
+          mma_f16_ts(tbase + kColO, tbase + s_col + (k < 4 ? 8 * k : 64 + 8 * (k - 4)),
+                     smem_desc(v_s + k * 2048, 16384, 1024, kSwz128), idesc_pv, (j == 0 && k == 0) ? 0u : 1u);
         }
       }
       tc_commit(&bars.pv_done[b]);
@@ -511,10 +514,14 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
       tmem_ld32(lane_base + s_col + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_ld32(lane_base + s_col + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_ld();
-      // S is in registers: the buffer may take QK(it+2)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_free[b]);
+      // FP4 PV: S is in registers and P goes to shared memory, so the
+      // buffer may take QK(it+2) (otherwise P(it) is written over it and
+      // QK(it+2) waits for PV(it))
+      if constexpr (L::kFp4Pv) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.s_free[b]);
+      }
       float* s = reinterpret_cast<float*>(sr);
       const int key0 = (item.t0 + j) * kBN + 64 * half;
       // Keys past the row's last visible one are masked (scale applied here);
@@ -617,8 +624,9 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
           if (!mbar_wait_warp(&bars.pv_done[pit & 1u], (pit >> 1) & 1u, a.status)) return;
           tc_fence_after();
         }
-      } else if (it > 0) {
-        // P and O belong to the tensor core until PV(it-1) has finished.
+      } else if (rescale_o) {
+        // O belongs to the tensor core until PV(it-1) has finished.  (P(it)
+        // goes over S(it), which no PV reads before PV(it).)
         const uint32_t pit = it - 1u;
         if (!mbar_wait_warp(&bars.pv_done[pit & 1u], (pit >> 1) & 1u, a.status)) return;
         tc_fence_after();
@@ -644,9 +652,10 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
         *reinterpret_cast<uint32_t*>(pb + 8192 + 512 * half + (r & 31) * 16 + (r >> 5) * 4) = psc;
         fence_proxy_async_smem();
       } else {
-        // P of keys 64*half.. goes to P columns 32*half..
-        tmem_st16(lane_base + kColP + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(lane_base + kColP + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        // P of keys 64*half.. over the first 32 of this half's S columns
+        // (already read into registers; the other half's are not touched)
+        tmem_st16(lane_base + s_col + 64 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(lane_base + s_col + 64 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
         tmem_wait_st();
       }
       tc_fence_before();
