@@ -809,13 +809,15 @@ __global__ void __launch_bounds__(kPlanThreads) nvfp4_decode_plan_kernel(DecodeA
 
 // Merge the split partials of requests with more than one split; write zeros
 // for empty requests.  One CTA per (q head, request), one thread per head
-// dimension: the splits' weights exp2(lse_s - m) are computed once into
-// shared memory, then each thread sums its column with independent loads.
+// dimension.  Every thread reads the splits' lse and its own column of the
+// partial O eight splits at a time, all loads of a group issued together,
+// and merges online (running max, rescaled sum and accumulator), so the
+// merge costs about one memory round trip per eight splits and needs no
+// shared memory or barrier.
+constexpr int kCombineGroup = 8;
 __global__ void __launch_bounds__(128) nvfp4_decode_combine_kernel(DecodeArgs a) {
-  extern __shared__ float wsh[];  // [max_splits] split weights
-  __shared__ float red[4];
   grid_dep_wait();  // the attention kernel's partials
-  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, warp = d >> 5;
+  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
   const int kv_len = a.kv_lens[b];
   const int64_t orow = (static_cast<int64_t>(b) * a.num_q_heads + hq) * kHeadDim;
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
@@ -827,45 +829,35 @@ __global__ void __launch_bounds__(128) nvfp4_decode_combine_kernel(DecodeArgs a)
   const int split_len = a.sched[2];
   const int n_s = (kv_len + split_len - 1) / split_len;
   if (n_s <= 1) return;
-  const int64_t base = static_cast<int64_t>(b) * a.max_splits * a.num_q_heads + hq;
-  float m = -INFINITY;
-  for (int sp = d; sp < n_s; sp += blockDim.x) {
-    const float v = a.part_lse[base + static_cast<int64_t>(sp) * a.num_q_heads];
-    wsh[sp] = v;
-    m = fmaxf(m, v);
-  }
+  const int64_t stride = static_cast<int64_t>(a.num_q_heads);
+  const float* pl = a.part_lse + static_cast<int64_t>(b) * a.max_splits * a.num_q_heads + hq;
+  const float* po = a.part_o + (static_cast<int64_t>(b) * a.max_splits * a.num_q_heads + hq) * kHeadDim + d;
+  float m = -INFINITY, L = 0.0f, acc = 0.0f;
+  for (int s0 = 0; s0 < n_s; s0 += kCombineGroup) {
+    float lv[kCombineGroup], ov[kCombineGroup];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    for (int i = 0; i < kCombineGroup; ++i) {
+      const bool in = s0 + i < n_s;
+      lv[i] = in ? pl[(s0 + i) * stride] : -INFINITY;
+      ov[i] = in ? po[(s0 + i) * stride * kHeadDim] : 0.0f;
+    }
+    float mg = m;
+#pragma unroll
+    for (int i = 0; i < kCombineGroup; ++i) mg = fmaxf(mg, lv[i]);
+    const float mu = (mg == -INFINITY) ? 0.0f : mg;
+    const float r = fast_exp2(m - mu);  // 0 while nothing is merged (m = -inf)
+    L *= r;
+    acc *= r;
+#pragma unroll
+    for (int i = 0; i < kCombineGroup; ++i) {
+      const float w = fast_exp2(lv[i] - mu);  // 0 past the last split
+      L += w;
+      acc += w * ov[i];
+    }
+    m = mg;
+  }
   const float mu = (m == -INFINITY) ? 0.0f : m;
-  __syncthreads();
-  float L = 0.0f;
-  for (int sp = d; sp < n_s; sp += blockDim.x) {
-    const float w = fast_exp2(wsh[sp] - mu);
-    wsh[sp] = w;
-    L += w;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  if (lane == 0) red[warp] = L;
-  __syncthreads();
-  L = (red[0] + red[1]) + (red[2] + red[3]);
-  float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
-  const float* po = a.part_o + base * kHeadDim + d;
-  const int64_t stride = static_cast<int64_t>(a.num_q_heads) * kHeadDim;
-  int sp = 0;
-  for (; sp + 3 < n_s; sp += 4) {
-    acc0 += wsh[sp] * po[sp * stride];
-    acc1 += wsh[sp + 1] * po[(sp + 1) * stride];
-    acc2 += wsh[sp + 2] * po[(sp + 2) * stride];
-    acc3 += wsh[sp + 3] * po[(sp + 3) * stride];
-  }
-  for (; sp < n_s; ++sp) acc0 += wsh[sp] * po[sp * stride];
-  const float acc = (acc0 + acc1) + (acc2 + acc3);
-  const float on = (L > 0.0f) ? acc / L : 0.0f;
-  o[orow + d] = __float2bfloat16_rn(on * a.v_g);
+  o[orow + d] = __float2bfloat16_rn((L > 0.0f ? acc / L : 0.0f) * a.v_g);
   if (a.lse && d == 0)
     a.lse[static_cast<int64_t>(b) * a.num_q_heads + hq] = (L > 0.0f) ? (mu + __log2f(L)) * kLn2 : -INFINITY;
 }
@@ -899,13 +891,7 @@ cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStr
   if (e != cudaSuccess) return e;
   e = launch_dependent(kern, dim3(b.ctas), dim3(128), DecFmt<FP8>::kSmem, s, b);
   if (e != cudaSuccess) return e;
-  const size_t wbytes = static_cast<size_t>(a.max_splits) * sizeof(float);  // split weights
-  if (wbytes > 48 * 1024) {
-    e = cudaFuncSetAttribute(nvfp4_decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(wbytes));
-    if (e != cudaSuccess) return e;
-  }
-  return launch_dependent(nvfp4_decode_combine_kernel, dim3(a.num_q_heads, batch), dim3(128), wbytes, s, b);
+  return launch_dependent(nvfp4_decode_combine_kernel, dim3(a.num_q_heads, batch), dim3(128), 0, s, b);
 }
 
 template <bool FP8>
