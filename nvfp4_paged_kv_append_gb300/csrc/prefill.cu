@@ -1236,24 +1236,32 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
 // lane: M = max_p m_p, w_p = 2^(m_p - M), O = sum_p w_p O_p / sum_p w_p l_p,
 // times the V tensor scale (log-sum-exp combination in the log2 domain).
 constexpr int kMergeRowsPerCta = 16;
+constexpr int kMergeGroup = 8;  // parts whose rows a lane loads at once
 __global__ void __launch_bounds__(32 * kMergeRowsPerCta) nvfp4_prefill_merge_kernel(PrefillArgs a) {
   const int u = blockIdx.x;
+  const int4 info = a.units[u];  // (grid = the most units the workspace holds)
   if (u >= a.work[2]) return;
-  const int4 info = a.units[u];
   const int parts = info.z;
   if (parts <= 1) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * kMergeRowsPerCta + warp;
   const int b = info.x, qt = info.y >> 8, kvh = info.y & 255;
   const int G = a.group, lg = a.log2_group;
-  const int q_start = a.qo_indptr[b], q_len = a.qo_indptr[b + 1] - q_start;
-  const int tok0 = qt * (kBM >> lg);
-  const int n_rows = min(kBM >> lg, q_len - tok0) << lg;
-  if (r >= n_rows) return;
   const float* base = a.part + static_cast<int64_t>(u) * a.split * kPartFloats;
-  // lane p < parts holds part p's running max and sum
+  // Loads that depend only on (unit, row) go out together: the request's
+  // bounds, each part's row max and sum (lane p < parts), and the first
+  // kMergeGroup parts' rows (r < kBM: inside the slot even for padding rows)
+  const int q_start = a.qo_indptr[b], q_end = a.qo_indptr[b + 1];
   const float mp = lane < parts ? base[lane * kPartFloats + kBM * kHeadDim + r] : -INFINITY;
   const float lp = lane < parts ? base[lane * kPartFloats + kBM * kHeadDim + kBM + r] : 0.0f;
+  float4 o4[kMergeGroup];
+#pragma unroll
+  for (int i = 0; i < kMergeGroup; ++i)
+    o4[i] = i < parts ? reinterpret_cast<const float4*>(base + i * kPartFloats + r * kHeadDim)[lane]
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int tok0 = qt * (kBM >> lg);
+  const int n_rows = min(kBM >> lg, q_end - q_start - tok0) << lg;
+  if (r >= n_rows) return;
   float m = mp;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -1263,13 +1271,21 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerCta) nvfp4_prefill_merge_ker
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int p = 0; p < parts; ++p) {
+#pragma unroll
+  for (int i = 0; i < kMergeGroup; ++i) {
+    const float w = __shfl_sync(0xffffffffu, wp, i);  // 0 for i >= parts
+    acc.x += w * o4[i].x;
+    acc.y += w * o4[i].y;
+    acc.z += w * o4[i].z;
+    acc.w += w * o4[i].w;
+  }
+  for (int p = kMergeGroup; p < parts; ++p) {
     const float w = __shfl_sync(0xffffffffu, wp, p);
-    const float4 o4 = reinterpret_cast<const float4*>(base + p * kPartFloats + r * kHeadDim)[lane];
-    acc.x += w * o4.x;
-    acc.y += w * o4.y;
-    acc.z += w * o4.z;
-    acc.w += w * o4.w;
+    const float4 v = reinterpret_cast<const float4*>(base + p * kPartFloats + r * kHeadDim)[lane];
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
   }
   const float sc = L > 0.0f ? a.v_g / L : 0.0f;
   const int tq = tok0 + (r >> lg), hq = kvh * G + (r & (G - 1));
