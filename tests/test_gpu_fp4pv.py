@@ -103,6 +103,18 @@ def test_fp4pv_prefill_groups_noncausal_junk():
         _check(got, lse, status, oracle_fp4pv(G.oracle_pools(inp), inp, causal=False), inp)
 
 
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_fp4pv_prefill_wide_groups(group):
+    """GQA ratios up to the largest the library accepts (128: one query token
+    per 128-row q tile), causal, ragged, junk-filled pools; every row."""
+    hkv = 2 if group == 32 else 1
+    wl = W.Workload(f"fp4pv_wide_g{group}", [21, 5, 1], [40, 133, 1], group * hkv, hkv, seed=group)
+    inp = W.make_inputs(wl)
+    got, lse, status = run_fp4pv(inp, G.gpu_cache(inp, fill=0xFF))
+    assert np.isfinite(got).all()
+    _check(got, lse, status, oracle_fp4pv(G.oracle_pools(inp), inp), inp)
+
+
 def test_fp4pv_prefill_shortq_sampled():
     """4 x 128 queries over 2,048 keys (the pages' repack case), sampled rows."""
     inp = G.inputs("shortq")
