@@ -225,6 +225,11 @@ size_t nvfp4_paged_prefill_noalloc_max_bytes(void);
  * tokens ("NVFP4 KV cache prefill vs decode performance", section "Decode can
  * win on fewer bytes read": decode reads the long cache for one new token and
  * is bandwidth-bound).  The query stays BF16; K and V are dequantized.
+ * Each (request, kv head) is cut into items of S tokens, S the longest of
+ * 1024, 2048, 4096 and 8192 that still gives every attention CTA two items
+ * (chosen on the device from kv_lens); the items' partial results are merged
+ * by their log-sum-exp.  The output does not depend on which CTA runs which
+ * item.
  * q, o:       bf16 [batch][num_q_heads][128].
  * lse:        optional fp32 [batch][num_q_heads].
  * workspace:  nvfp4_workspace_bytes(NVFP4KV_OP_DECODE, batch, num_q_heads,

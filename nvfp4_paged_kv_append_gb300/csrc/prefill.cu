@@ -139,7 +139,7 @@ struct Bars {
   uint64_t* kv_empty;  // [6]
   uint64_t* sfb_full;  // [2] in-kernel dequant-ahead: K tile in BF16
   uint64_t* s_full;    // [2]
-  uint64_t* s_free;    // [2] softmax has loaded S: the buffer may take the next QK
+  uint64_t* s_free;    // [2] FP4 PV: softmax has loaded S, the buffer may take the next QK
   uint64_t* p_full;    // [2]
   uint64_t* vdq_full;  // [2] in-kernel mode: V tile in FP16
   uint64_t* pv_done;   // [2]
