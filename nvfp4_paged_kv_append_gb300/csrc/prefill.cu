@@ -502,6 +502,14 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
     const float c_r = (L::kA4Q ? qscale[r] : 1.0f) * a.k_g * a.sm_scale * kLog2e;
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.qs_empty);
+    // A warp whose 32 rows all lie past the q tile's rows (a short q tile:
+    // a tail of few query tokens, a request's last tile) computes nothing:
+    // it waits for each S and arrives as if it had written its P, and its P
+    // and O rows are never read out.  (Both halves of a row agree, so the
+    // pair skips its meetings together.  QK(it+2) waits for PV(it), so such
+    // a warp cannot run ahead by a phase; FP4 PV, whose QK waits only for
+    // the S reads, keeps the full path.)
+    const bool idle = !L::kFp4Pv && 32 * quad >= (item.n_tok << lg);
     float m_run = -INFINITY;
     float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
     for (int j = 0; j < item.n_tiles; ++j) {
@@ -509,6 +517,11 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
       const uint32_t b = it & 1u;
       const uint32_t s_col = b ? kColS1 : kColS0;
       if (!mbar_wait_warp(&bars.s_full[b], (it >> 1) & 1u, a.status)) return;
+      if (idle) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full[b]);
+        continue;
+      }
       tc_fence_after();
       uint32_t sr[64];
       tmem_ld32(lane_base + s_col + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -663,6 +676,13 @@ __device__ void softmax_loop(const PrefillArgs& a, uint8_t* smem, const Bars& ba
       if (lane == 0) mbar_arrive(&bars.p_full[b]);
     }
     // ---- epilogue: combine the halves' row sums, scale this half of O ---------
+    if (idle) {
+      if (!mbar_wait_warp(bars.o_full, item_ctr & 1u, a.status)) return;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.o_empty);
+      it_ctr += item.n_tiles;
+      continue;
+    }
     const float l_half = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y) + (lacc[2].x + lacc[2].y) +
                          (lacc[3].x + lacc[3].y);
     xl[half * 128 + r] = l_half;
