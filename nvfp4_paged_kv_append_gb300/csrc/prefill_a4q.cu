@@ -24,8 +24,12 @@
 //                   tcgen05.cp of its K scale atoms, QK (kind::mxf4nvf4,
 //                   N = 64 or 48), PV (kind::f16, P from TMEM)
 //   warp 1 lane 0   one bulk copy per tile of the repacked record
-//   warps 4-7       thread = row: Q quantization at each item start, the
-//                   softmax of every half tile, the epilogue
+//   warps 2-3       Q of the CTA's next item -> NVFP4 (two rows a thread)
+//                   into the other of two Q buffers, with its block scales
+//                   in the tcgen05.cp layout and the row scales, so that an
+//                   item's first QK can run during the previous epilogue
+//   warps 4-7       thread = row: Q of the CTA's first item (the same way),
+//                   the softmax of every half tile, the epilogue
 #include "prefill_common.cuh"
 
 namespace nvfp4kv {
@@ -55,10 +59,11 @@ constexpr uint32_t kRegsIssue2 = 56, kRegsSoftmax2 = 200;
 static_assert(128 * (kRegsIssue2 + kRegsSoftmax2) <= kThreads2 * 128, "register budgets exceed the launch");
 
 // shared memory
-constexpr uint32_t kOffQ2 = 0;                                   // 8 KB FP4 Q tile
-constexpr uint32_t kOffStage2 = 8192;
-constexpr uint32_t kOffSfa2 = kOffStage2 + kStages2 * kRecord2;  // [128] uint2 Q scale words
-constexpr uint32_t kOffBar2 = kOffSfa2 + 1024;
+constexpr uint32_t kOffQ2 = 0;                                   // [2] 8 KB FP4 Q tiles
+constexpr uint32_t kOffStage2 = 16384;
+constexpr uint32_t kOffQa2 = kOffStage2 + kStages2 * kRecord2;   // [2] Q scale atoms (two k-steps x 512 B)
+constexpr uint32_t kOffQg2 = kOffQa2 + 2048;                     // [2][128] fp32 Q row scales
+constexpr uint32_t kOffBar2 = kOffQg2 + 1024;
 constexpr uint32_t kNumBars2 = 16;
 constexpr uint32_t kOffSlot2 = kOffBar2 + kNumBars2 * 8;
 constexpr uint32_t kAlloc2 = kOffSlot2 + 16 + 1024;              // + slack for 1 KB alignment
@@ -70,10 +75,9 @@ struct Bars2 {
   uint64_t* s_full;    // [half] S of the half is in TMEM
   uint64_t* p_full;    // [half] P of the half written over its S (4 softmax warps)
   uint64_t* pv_done;   // [half] PV of the half finished
-  uint64_t* q_full;    // Q tile and its scales ready (4 softmax warps)
-  uint64_t* q_empty;   // last QK of the item finished
+  uint64_t* q_full;    // [2] Q buffer b holds the item's Q tile and scales (warps 2-3)
+  uint64_t* q_empty;   // [2] the item's last QK has finished and the softmax has its row scales
   uint64_t* o_empty;   // the epilogue has read O (4 softmax warps)
-  uint64_t* sfa_ready; // the item's Q scale words are staged (4 softmax warps)
   uint64_t* drain;
 };
 
@@ -84,11 +88,10 @@ __device__ __forceinline__ Bars2 make_bars2(uint64_t* base) {
   b.s_full = base + 4;
   b.p_full = base + 6;
   b.pv_done = base + 8;
-  b.q_full = base + 10;
-  b.q_empty = base + 11;
-  b.o_empty = base + 12;
-  b.sfa_ready = base + 13;
-  b.drain = base + 14;
+  b.q_full = base + 10;   // 10, 11
+  b.q_empty = base + 12;  // 12, 13
+  b.o_empty = base + 14;
+  b.drain = base + 15;
   return b;
 }
 
@@ -114,6 +117,12 @@ __device__ __forceinline__ void qk_half(uint32_t q_s, uint32_t stage_s, uint32_t
                 s > 0 ? 1u : 0u);
 }
 
+// The item's Q block scales: two tcgen05.cp of the staged atoms (k-steps 0, 1).
+__device__ __forceinline__ void copy_q_scales(uint32_t qa_s, uint32_t tbase) {
+  tc_cp_32x128b_warpx4(tbase + kColSFA2, smem_desc(qa_s, 0, 128, kSwzNone));
+  tc_cp_32x128b_warpx4(tbase + kColSFA2 + 4, smem_desc(qa_s + 512, 0, 128, kSwzNone));
+}
+
 template <int h>
 __device__ __forceinline__ void pv_half(uint32_t stage_s, uint32_t tbase, bool first, uint32_t idesc_pv) {
   const uint32_t v_s = stage_s + kKCodes2 + kKAtoms2;
@@ -126,21 +135,24 @@ __device__ __forceinline__ void pv_half(uint32_t stage_s, uint32_t tbase, bool f
 }
 
 __device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, const Bars2& bars, uint32_t tbase) {
-  const uint32_t q_s = smem_u32(smem + kOffQ2);
   const uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 0, 1);
   uint32_t it = 0, item_ctr = 0;
   Item item;
   for (int round = 0; get_item(a, round, item); ++round, ++item_ctr) {
-    if (!mbar_wait(bars.q_full, item_ctr & 1u, a.status)) return;
-    // prologue: both halves of tile 0
+    const uint32_t qb = item_ctr & 1u;
+    const uint32_t q_s = smem_u32(smem + kOffQ2 + qb * 8192);
+    if (!mbar_wait(&bars.q_full[qb], (item_ctr >> 1) & 1u, a.status)) return;
+    // prologue: the item's Q scales, both halves of tile 0 (the previous
+    // item's QKs, issued earlier, have read the scale columns)
     uint32_t stage_s = smem_u32(smem + kOffStage2 + (it % kStages2) * kRecord2);
     if (!mbar_wait(&bars.kv_full[it % kStages2], (it / kStages2) & 1u, a.status)) return;
     tc_fence_after();
+    copy_q_scales(smem_u32(smem + kOffQa2 + qb * 1024), tbase);
     qk_half<0>(q_s, stage_s, tbase);
     tc_commit(&bars.s_full[0]);
     qk_half<1>(q_s, stage_s, tbase);
     tc_commit(&bars.s_full[1]);
-    if (item.n_tiles == 1) tc_commit(bars.q_empty);
+    if (item.n_tiles == 1) tc_commit(&bars.q_empty[qb]);
     for (int j = 0; j < item.n_tiles; ++j, ++it) {
       const uint32_t st = it % kStages2;
       const bool more = j + 1 < item.n_tiles;
@@ -167,7 +179,7 @@ __device__ __forceinline__ void mma_thread(const PrefillArgs& a, uint8_t* smem, 
       if (more) {
         qk_half<1>(q_s, next_s, tbase);
         tc_commit(&bars.s_full[1]);
-        if (j + 2 == item.n_tiles) tc_commit(bars.q_empty);
+        if (j + 2 == item.n_tiles) tc_commit(&bars.q_empty[qb]);
       }
       stage_s = next_s;
     }
@@ -187,6 +199,44 @@ __device__ __forceinline__ void load_thread(const PrefillArgs& a, uint8_t* smem,
       bulk_load(smem + kOffStage2 + st * kRecord2, a.repack + repack_index(a, item.b, item.kvh, item.t0 + j) * kRecord2,
                 kRecord2, &bars.kv_full[st]);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Q warps (warps 2-3, thread t = 0..63): the Q tile of each of the CTA's
+// items, rows t and t + 64, into Q buffer (item & 1) once the item two back
+// has released it: FP4 codes (64B-swizzled rows), the block scales in the
+// layout tcgen05.cp 32x128b.warpx4 expects (row 32 j + i at byte 16 i + 4 j
+// of each k-step's 512 B), and the row scales.
+__device__ __forceinline__ void stage_q_row(const PrefillArgs& a, uint8_t* smem, const Item& item, uint32_t qb, int r) {
+  const int G = a.group, lg = a.log2_group;
+  const int tq = item.tok0 + (r >> lg);
+  const bool valid = (r >> lg) < item.n_tok;
+  const int hq = item.kvh * G + (r & (G - 1));
+  const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) +
+                                                    (static_cast<int64_t>(item.q_start + (valid ? tq : 0)) *
+                                                         a.num_q_heads + hq) * kHeadDim);
+  float g_row;
+  const uint2 sw = quantize_q_row(src, valid, smem + kOffQ2 + qb * 8192, r, a.q_g, g_row);
+  reinterpret_cast<float*>(smem + kOffQg2)[qb * 128 + r] = g_row;
+  uint8_t* atoms = smem + kOffQa2 + qb * 1024;
+  const int off = (r & 31) * 16 + (r >> 5) * 4;
+  *reinterpret_cast<uint32_t*>(atoms + off) = sw.x;
+  *reinterpret_cast<uint32_t*>(atoms + 512 + off) = sw.y;
+}
+
+// From the second item on (the softmax warps stage the first one).
+__device__ __forceinline__ void q_warps(const PrefillArgs& a, uint8_t* smem, const Bars2& bars, int t) {
+  uint32_t item_ctr = 1;
+  Item item;
+  for (int round = 1; get_item(a, round, item); ++round, ++item_ctr) {
+    const uint32_t qb = item_ctr & 1u;
+    if (item_ctr >= 2 && !mbar_wait_warp(&bars.q_empty[qb], ((item_ctr >> 1) - 1) & 1u, a.status)) return;
+#pragma unroll 1
+    for (int r = t; r < kBM; r += 64) stage_q_row(a, smem, item, qb, r);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if ((t & 31) == 0) mbar_arrive(&bars.q_full[qb]);
   }
 }
 
@@ -283,7 +333,6 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
                                              int r) {
   const int quad = r >> 5, lane = r & 31;
   const int G = a.group, lg = a.log2_group;
-  uint2* sfa_stage = reinterpret_cast<uint2*>(smem + kOffSfa2);
   const uint32_t lane_base = tmem_addr(tbase, 32 * quad, 0);
   uint32_t it = 0, item_ctr = 0;
   Item item;
@@ -292,35 +341,21 @@ __device__ __forceinline__ void softmax_rows(const PrefillArgs& a, uint8_t* smem
     const bool valid = (r >> lg) < item.n_tok;
     const int hq = item.kvh * G + (r & (G - 1));
     const int limit = !valid ? -1 : (a.causal ? item.kv_len - item.q_len + tq : item.kv_len - 1);
-    // ---- Q tile: the previous item's last QK must have finished reading it
-    if (item_ctr > 0 && !mbar_wait_warp(bars.q_empty, (item_ctr - 1) & 1u, a.status)) return;
-    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) +
-                                                      (static_cast<int64_t>(item.q_start + tq) * a.num_q_heads + hq) *
-                                                          kHeadDim);
-    float g_row;
-    sfa_stage[r] = quantize_q_row(src, valid, smem + kOffQ2, r, a.q_g, g_row);
-    const float c_r = g_row * a.k_g * a.sm_scale * kLog2e;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars.sfa_ready);
-    if (!mbar_wait_warp(bars.sfa_ready, item_ctr & 1u, a.status)) return;
-    // Q block scales -> TMEM: lane i of each quadrant, column 4s+j holds the
-    // four scales of k-step s for row 32j+i (replicated per quadrant)
-    {
-      uint32_t va[8];
-#pragma unroll
-      for (int s2 = 0; s2 < 2; ++s2)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint2 v = sfa_stage[32 * j + lane];
-          va[4 * s2 + j] = s2 ? v.y : v.x;
-        }
-      tmem_st8(lane_base + kColSFA2, va);
-      tmem_wait_st();
+    // ---- the item's row scale from the Q warps; its Q buffer is then free
+    // as far as this warp is concerned
+    const uint32_t qb = item_ctr & 1u;
+    if (item_ctr == 0) {
+      // the first item's Q: one row per thread, all four warps, then two
+      // arrivals (as the Q warps make) once every row is staged
+      stage_q_row(a, smem, item, 0, r);
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (lane == 0 && quad < 2) mbar_arrive(&bars.q_full[0]);
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
+    if (!mbar_wait_warp(&bars.q_full[qb], (item_ctr >> 1) & 1u, a.status)) return;
+    const float c_r = reinterpret_cast<const float*>(smem + kOffQg2)[qb * 128 + r] * a.k_g * a.sm_scale * kLog2e;
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars.q_full);
+    if (lane == 0) mbar_arrive(&bars.q_empty[qb]);
 
     float m_run = -INFINITY;
     float2 lacc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
@@ -392,10 +427,11 @@ __global__ void __launch_bounds__(kThreads2, 2) nvfp4_prefill_a4q_2cta_sm103_ker
       mbar_init(&bars.p_full[h], 4);
       mbar_init(&bars.pv_done[h], 1);
     }
-    mbar_init(bars.q_full, 4);
-    mbar_init(bars.q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.q_full[b], 2);   // the two Q warps
+      mbar_init(&bars.q_empty[b], 5);  // the item's last QK (commit) + the 4 softmax warps
+    }
     mbar_init(bars.o_empty, 4);
-    mbar_init(bars.sfa_ready, 4);
     mbar_init(bars.drain, 1);
     fence_barrier_init();
   }
@@ -419,6 +455,8 @@ __global__ void __launch_bounds__(kThreads2, 2) nvfp4_prefill_a4q_2cta_sm103_ker
       tc_commit(bars.drain);  // every MMA of this thread has finished before TMEM is freed
     } else if (warp == 1 && lane == 0) {
       load_thread(a, smem, bars);
+    } else if (warp >= 2) {
+      q_warps(a, smem, bars, tid - 64);
     }
   }
   tc_fence_before();
