@@ -126,6 +126,22 @@ def test_prefill_group1_repack(variant, q_mode, mode):
     _check(inp, cache, G.oracle_pools(inp), variant, q_mode, mode=mode)
 
 
+@pytest.mark.parametrize("variant,q_mode", VARIANTS)
+def test_prefill_many_short_items(variant, q_mode):
+    """200 requests of 64 queries over 64-240 keys, 16/4 heads: 1,600 work
+    items of one to three KV tiles, about five per CTA of the two-CTA kernel,
+    in repack mode.  Each CTA stages the Q tile of its next item while it runs
+    the current one (two Q buffers, reused every other item; an item of one
+    tile releases its buffer at its first QK); every row is checked."""
+    rng = np.random.default_rng(23)
+    kv = [int(x) for x in rng.integers(64, 241, size=200)]
+    wl = W.Workload("many_short", [64] * 200, kv, 16, 4, seed=23)
+    assert G.repack_mode_expected(wl)
+    inp = W.make_inputs(wl)
+    cache = G.gpu_cache(inp, fill=0x7F)
+    _check(inp, cache, G.oracle_pools(inp), variant, q_mode)
+
+
 @pytest.mark.parametrize("mode", ["auto", "inkernel"])
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 @pytest.mark.parametrize("group", [32, 64, 128])
