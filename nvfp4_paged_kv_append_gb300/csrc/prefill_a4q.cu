@@ -20,9 +20,11 @@
 // thread owns one whole row, so no row statistics are exchanged between
 // warps.
 //
-//   warp 0 lane 0   TMEM allocation; every tensor operation: per half, the
-//                   tcgen05.cp of its K scale atoms, QK (kind::mxf4nvf4,
-//                   N = 64 or 48), PV (kind::f16, P from TMEM)
+//   warp 0 lane 0   TMEM allocation; every tensor operation: at each item
+//                   start the tcgen05.cp of the item's Q scale atoms; per
+//                   half, the tcgen05.cp of its K scale atoms, QK
+//                   (kind::mxf4nvf4, N = 64 or 48), PV (kind::f16, P from
+//                   TMEM)
 //   warp 1 lane 0   one bulk copy per tile of the repacked record
 //   warps 2-3       Q of the CTA's next item -> NVFP4 (two rows a thread)
 //                   into the other of two Q buffers, with its block scales
