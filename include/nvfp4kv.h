@@ -155,8 +155,9 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  *             are overwritten (it holds the work schedule).  Given
  *             nvfp4_workspace_bytes(..., total_q, max_pages_per_req * 16)
  *             bytes, the call may also run in repack mode:
- *             when requests average two or more q tiles (128 rows of query
- *             tokens x grouped heads) per kv head, V (and K for the
+ *             when requests average enough q tiles (128 rows of query
+ *             tokens x grouped heads) per kv head -- six for A4Q, two for
+ *             dequant-ahead -- V (and K for the
  *             dequant-ahead variant) is first dequantized once per KV
  *             tile (112 keys for A4Q, 128 for dequant-ahead) into the
  *             workspace ("NVFP4 KV cache A4Q prefill explained", section

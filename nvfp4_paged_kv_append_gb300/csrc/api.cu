@@ -315,10 +315,15 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   if (!workspace || !aligned16(workspace) || workspace_bytes < sched1) return NVFP4KV_ERR_WORKSPACE;
   // Repack mode (each V tile dequantized once, into the workspace) when the
   // workspace holds a tile for every (request, kv head, KV tile) the page
-  // table allows and requests average at least two q tiles per kv head.
+  // table allows and each record would be read by enough q tiles: requests
+  // average at least six q tiles per kv head for A4Q, two for dequant-ahead
+  // (whose in-kernel mode converts K as well).  (A4Q on GB300, whole calls:
+  // four q tiles per kv head, 4 x 128 over 2K, in-kernel 38 against 52 us;
+  // eight, 4 x 256 over 4K, repack 83 against 91 us.)
   const size_t rbytes = prefill_repack_bytes(variant, batch, c.num_kv_heads, max_kv);
   const int64_t qtiles = (total_q * (num_q_heads / c.num_kv_heads) + kBM - 1) / kBM;
-  bool repack = workspace_bytes >= sched1 + rbytes && qtiles >= 2 * static_cast<int64_t>(batch);
+  const int64_t min_qtiles = variant == NVFP4KV_VARIANT_A4Q ? 6 : 2;
+  bool repack = workspace_bytes >= sched1 + rbytes && qtiles >= min_qtiles * batch;
   if (c.fp8 || fp4pv) {  // these read only repacked records
     if (workspace_bytes < sched1 + rbytes) return NVFP4KV_ERR_WORKSPACE;
     repack = true;

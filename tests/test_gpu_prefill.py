@@ -33,8 +33,9 @@ def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None, mode="aut
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 @pytest.mark.parametrize("cfg", ["tiny", "small_ragged"])
 def test_prefill_full_parity(cfg, variant, q_mode, mode):
-    """Every row; "auto" runs the repack pre-pass (these batches average two
-    or more q tiles per kv head), "inkernel" dequantizes V in the kernel."""
+    """Every row; "auto" runs the repack pre-pass for dequant-ahead (these
+    batches average two or more q tiles per kv head) and the in-kernel mode
+    for A4Q (fewer than six), "inkernel" dequantizes V in the kernel."""
     inp = G.inputs(cfg)
     cache = G.gpu_cache(inp)
     _check(inp, cache, G.pools_for(cfg), variant, q_mode, mode=mode)
@@ -117,10 +118,10 @@ def test_prefill_long_ragged_every_tile(variant, q_mode):
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 def test_prefill_group1_repack(variant, q_mode, mode):
     """One query head per kv head (G = 1): 128 tokens per q tile.  Two
-    requests average more than two q tiles per kv head, so "auto" runs the
+    requests average seven and a half q tiles per kv head, so "auto" runs the
     repack-mode kernels (the two-CTA kernel for A4Q); every row is checked."""
-    wl = W.Workload("g1_repack", [300, 260], [420, 260], 3, 3, seed=17)
-    assert G.repack_mode_expected(wl)
+    wl = W.Workload("g1_repack", [900, 800], [1000, 800], 3, 3, seed=17)
+    assert G.repack_mode_expected(wl, variant)
     inp = W.make_inputs(wl)
     cache = G.gpu_cache(inp, fill=0x7F)
     _check(inp, cache, G.oracle_pools(inp), variant, q_mode, mode=mode)
@@ -128,15 +129,16 @@ def test_prefill_group1_repack(variant, q_mode, mode):
 
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 def test_prefill_many_short_items(variant, q_mode):
-    """200 requests of 64 queries over 64-240 keys, 16/4 heads: 1,600 work
-    items of one to three KV tiles, about five per CTA of the two-CTA kernel,
-    in repack mode.  Each CTA stages the Q tile of its next item while it runs
-    the current one (two Q buffers, reused every other item; an item of one
-    tile releases its buffer at its first QK); every row is checked."""
+    """120 requests of 128 queries over 128-240 keys, 32/4 heads (16 tokens
+    per q tile, eight q tiles per kv head): 3,840 work items of one to three
+    KV tiles, about 12 per CTA of the two-CTA kernel, in repack mode.  Each
+    CTA stages the Q tile of its next item while it runs the current one (two
+    Q buffers, reused every other item; an item of one tile releases its
+    buffer at its first QK); every row is checked."""
     rng = np.random.default_rng(23)
-    kv = [int(x) for x in rng.integers(64, 241, size=200)]
-    wl = W.Workload("many_short", [64] * 200, kv, 16, 4, seed=23)
-    assert G.repack_mode_expected(wl)
+    kv = [int(x) for x in rng.integers(128, 241, size=120)]
+    wl = W.Workload("many_short", [128] * 120, kv, 32, 4, seed=23)
+    assert G.repack_mode_expected(wl, variant)
     inp = W.make_inputs(wl)
     cache = G.gpu_cache(inp, fill=0x7F)
     _check(inp, cache, G.oracle_pools(inp), variant, q_mode)
@@ -147,9 +149,12 @@ def test_prefill_many_short_items(variant, q_mode):
 @pytest.mark.parametrize("group", [32, 64, 128])
 def test_prefill_wide_groups(group, variant, q_mode, mode):
     """GQA ratios up to the largest the library accepts (128: one query token
-    per 128-row q tile), causal, ragged; every row against the oracle."""
+    per 128-row q tile), causal, ragged; every row against the oracle.  The
+    requests average six or more q tiles per kv head, so "auto" runs repack
+    mode (the two-CTA kernel for A4Q)."""
     hkv = 2 if group == 32 else 1
-    wl = W.Workload(f"wide_g{group}", [21, 5, 1], [40, 133, 1], group * hkv, hkv, seed=group)
+    wl = W.Workload(f"wide_g{group}", [48, 20, 1], [60, 133, 1], group * hkv, hkv, seed=group)
+    assert G.repack_mode_expected(wl, variant)
     inp = W.make_inputs(wl)
     cache = G.gpu_cache(inp, fill=0x7F)
     _check(inp, cache, G.oracle_pools(inp), variant, q_mode, mode=mode)
@@ -218,16 +223,14 @@ def test_prefill_zero_query_rows_repack_mode(variant, q_mode):
     """All-zero query rows (a per-row Q scale of 0) in repack mode, on the
     causal diagonal tiles where keys are masked: the output is the mean of
     the visible V rows, never NaN."""
-    import copy
-    base = G.inputs("shortq")  # averages four q tiles per kv head: repack mode
-    inp = copy.copy(base)
-    q = base.q.clone()
-    zero_tokens = [0, 5, 127, 128 + 64, 3 * 128 + 127]
-    q[zero_tokens] = 0
-    inp.q = q
+    wl = W.Workload("zero_rows_repack", [256, 256], [2048, 1024], 32, 8, seed=31)
+    assert G.repack_mode_expected(wl, variant)  # eight q tiles per kv head
+    inp = W.make_inputs(wl)
+    zero_tokens = [0, 5, 127, 256 + 64, 256 + 255]
+    inp.q[zero_tokens] = 0
     cache = G.gpu_cache(inp)
-    rows = [(0, i) for i in range(128)] + [(1, 64), (3, 127), (2, 0), (2, 127)]
-    got, _ = _check(inp, cache, G.pools_for("shortq"), variant, q_mode, rows=rows, mode="auto")
+    rows = [(0, i) for i in range(128)] + [(1, 64), (1, 255), (0, 200), (0, 255)]
+    got, _ = _check(inp, cache, G.oracle_pools(inp), variant, q_mode, rows=rows, mode="auto")
     assert np.isfinite(got).all()
 
 
