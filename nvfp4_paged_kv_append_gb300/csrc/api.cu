@@ -30,6 +30,16 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
+// Kernels whose shared-memory attributes are set on a device.
+struct KernelAttr {
+  int dev;
+  const void* kernel;
+  int bytes;
+};
+std::mutex g_attr_mu;
+KernelAttr g_attr[256];
+int g_n_attr = 0;
+
 // Per-device set-up on first use (device current): capability check, SM
 // count, status word address.
 int device_state(DeviceState** out) {
@@ -177,6 +187,24 @@ size_t prefill_repack_bytes(int variant, int batch, int num_kv_heads, int64_t ma
   return kRepackRecordBytesDq * prefill_repack_tiles(batch, num_kv_heads, max_kv_len, kBN);
 }
 
+}  // namespace
+
+cudaError_t nvfp4kv::set_kernel_smem(const void* kernel, int bytes, bool max_carveout) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (int i = 0; i < g_n_attr; ++i)
+    if (g_attr[i].dev == dev && g_attr[i].kernel == kernel && g_attr[i].bytes == bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && max_carveout)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && g_n_attr < 256) g_attr[g_n_attr++] = {dev, kernel, bytes};
+  return e;
+}
+
+namespace {
+
 int launch_rc(cudaError_t e) { return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA; }
 
 // Decode workspace starts with the item schedule: a 16-byte header, then one
@@ -318,8 +346,9 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   // table allows and each record would be read by enough q tiles: requests
   // average at least six q tiles per kv head for A4Q, two for dequant-ahead
   // (whose in-kernel mode converts K as well).  (A4Q on GB300, whole calls:
-  // four q tiles per kv head, 4 x 128 over 2K, in-kernel 38 against 52 us;
-  // eight, 4 x 256 over 4K, repack 83 against 91 us.)
+  // four q tiles per kv head, 4 x 128 over 2K, in-kernel 36.5 against repack
+  // 57.0 us; six, 4 x 192 over 2K, 57 us in either mode; eight, 4 x 256 over
+  // 4K, repack 82.6 against 89.7 us.)
   const size_t rbytes = prefill_repack_bytes(variant, batch, c.num_kv_heads, max_kv);
   const int64_t qtiles = (total_q * (num_q_heads / c.num_kv_heads) + kBM - 1) / kBM;
   const int64_t min_qtiles = variant == NVFP4KV_VARIANT_A4Q ? 6 : 2;

@@ -887,7 +887,7 @@ cudaError_t launch_decode_g(const DecodeArgs& a, int batch, int num_sms, cudaStr
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   void (*kern)(DecodeArgs) = FP8 ? fp8_paged_decode_kernel<G> : nvfp4_paged_decode_kernel<G>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DecFmt<FP8>::kSmem);
+  e = set_kernel_smem(reinterpret_cast<const void*>(kern), DecFmt<FP8>::kSmem, false);
   if (e != cudaSuccess) return e;
   e = launch_dependent(kern, dim3(b.ctas), dim3(128), DecFmt<FP8>::kSmem, s, b);
   if (e != cudaSuccess) return e;

@@ -192,5 +192,9 @@ size_t prefill_a4q_2cta_record_bytes();
 int prefill_a4q_2cta_tile_keys();
 cudaError_t launch_prefill_a4q_2cta_repack(const PrefillArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill_a4q_2cta(const PrefillArgs& a, int num_sms, cudaStream_t s);
+// Sets a kernel's dynamic shared-memory limit (and, for the kernels that pair
+// two CTAs per SM, the largest shared-memory carveout) once per device: the
+// calls are host work that a short launch would otherwise wait on.
+cudaError_t set_kernel_smem(const void* kernel, int bytes, bool max_carveout);
 
 }  // namespace nvfp4kv

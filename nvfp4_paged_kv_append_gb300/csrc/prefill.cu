@@ -779,6 +779,11 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // The set-up above overlapped the tail of the schedule or repack kernel
+  // before this one; its results are read only after this wait.  The merge
+  // kernel, if any, may start its set-up now.
+  grid_dep_launch();
+  grid_dep_wait();
 
   if (tid >= kSoftmaxTid0) {
     softmax_loop<VARIANT, REPACK>(a, smem, bars, tbase, (tid - kSoftmaxTid0) & 127, (tid - kSoftmaxTid0) >> 7);
@@ -849,6 +854,8 @@ __global__ void __launch_bounds__(128) nvfp4_prefill_repack_fp4pv_kernel(Prefill
   using L = Layout<2, true>;
   __shared__ __align__(16) uint8_t sv[kBN * 64];  // the tile's V codes, as stored
   __shared__ __align__(16) uint8_t ss[kBN * 8];   // and V block scales
+  grid_dep_launch();
+  grid_dep_wait();  // the schedule
   const int tid = threadIdx.x;
   const int total = a.work[1];
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -951,6 +958,8 @@ __global__ void __launch_bounds__(128) nvfp4_v_token_major_kernel(TokenMajorArgs
 // written by the repack kernel of prefill_a4q.cu.)
 __global__ void __launch_bounds__(128) nvfp4_prefill_repack_kernel(PrefillArgs a) {
   using L = Layout<1, true>;
+  grid_dep_launch();
+  grid_dep_wait();  // the schedule
   const int tid = threadIdx.x;
   const int total = a.work[1];
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -1041,6 +1050,8 @@ __device__ __forceinline__ void fp8_group_to_16bit(uint4 w0, uint4 w1, bool bf16
 
 __global__ void __launch_bounds__(128) fp8_prefill_repack_kernel(PrefillArgs a) {
   using L = Layout<1, true>;
+  grid_dep_launch();
+  grid_dep_wait();  // the schedule
   const int tid = threadIdx.x;
   const int total = a.work[1];
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -1124,6 +1135,7 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* warp_sums) {
 __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
   __shared__ int hist[kMaxCostBins];
   __shared__ int warp_sums[32];
+  grid_dep_launch();  // the next kernel may start its set-up
   const int tid = threadIdx.x;
   int* prefix = a.work + 4 + 4 * a.max_items;  // [batch + 1] unit prefix (after the int4 items)
   int* tprefix = prefix + a.batch + 1;         // [batch + 1] KV-tile prefix
@@ -1259,6 +1271,7 @@ __global__ void __launch_bounds__(1024) nvfp4_prefill_plan_kernel(PlanArgs a) {
 constexpr int kMergeRowsPerCta = 16;
 constexpr int kMergeGroup = 8;  // parts whose rows a lane loads at once
 __global__ void __launch_bounds__(32 * kMergeRowsPerCta) nvfp4_prefill_merge_kernel(PrefillArgs a) {
+  grid_dep_wait();  // the attention kernel's partials
   const int u = blockIdx.x;
   const int4 info = a.units[u];  // (grid = the most units the workspace holds)
   if (u >= a.work[2]) return;
@@ -1319,10 +1332,9 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerCta) nvfp4_prefill_merge_ker
 
 template <typename K>
 cudaError_t launch_main(K kernel, uint32_t smem, const PrefillArgs& a, int num_sms, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_kernel_smem(reinterpret_cast<const void*>(kernel), smem, false);
   if (e != cudaSuccess) return e;
-  kernel<<<num_sms, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(num_sms), dim3(kThreads), smem, s, a);
 }
 
 }  // namespace
@@ -1333,9 +1345,8 @@ cudaError_t launch_prefill_plan(const PrefillArgs& a, const PlanArgs& plan, int 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !repack) return e;
   if (variant == 0) return launch_prefill_a4q_2cta_repack(a, num_sms, s);
-  if (variant == 2) nvfp4_prefill_repack_fp4pv_kernel<<<num_sms * 8, 128, 0, s>>>(a);
-  else nvfp4_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(variant == 2 ? nvfp4_prefill_repack_fp4pv_kernel : nvfp4_prefill_repack_kernel,
+                    dim3(num_sms * 8), dim3(128), 0, s, a);
 }
 
 size_t prefill_fp4pv_record_bytes() { return Layout<2, true>::kStageBytes; }
@@ -1351,16 +1362,15 @@ cudaError_t launch_prefill_fp8(const PrefillArgs& a, const PlanArgs& plan, int n
   nvfp4_prefill_plan_kernel<<<1, 1024, 0, s>>>(plan);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fp8_prefill_repack_kernel<<<num_sms * 8, 128, 0, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(fp8_prefill_repack_kernel, dim3(num_sms * 8), dim3(128), 0, s, a)) != cudaSuccess) return e;
   if ((e = launch_main(fp8_prefill_repack_sm103_kernel, Layout<1, true>::kAlloc, a, num_sms, s)) != cudaSuccess)
     return e;
   return a.split > 1 ? launch_prefill_merge(a, s) : cudaSuccess;
 }
 
 cudaError_t launch_prefill_merge(const PrefillArgs& a, cudaStream_t s) {
-  nvfp4_prefill_merge_kernel<<<dim3(a.max_units, kBM / kMergeRowsPerCta), 32 * kMergeRowsPerCta, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(nvfp4_prefill_merge_kernel, dim3(a.max_units, kBM / kMergeRowsPerCta),
+                    dim3(32 * kMergeRowsPerCta), 0, s, a);
 }
 
 cudaError_t launch_prefill_attend(const PrefillArgs& a, int variant, bool repack, int num_sms, cudaStream_t s) {

@@ -445,6 +445,10 @@ __global__ void __launch_bounds__(kThreads2, 2) nvfp4_prefill_a4q_2cta_sm103_ker
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // The set-up above overlapped the tail of the repack pre-pass (or the
+  // schedule kernel) before this one; their results are read only now.
+  grid_dep_launch();
+  grid_dep_wait();
   // Register budgets (launched with 128 per thread): warps 0-3 give up to 56,
   // the softmax warpgroup takes 200; 128 x (56 + 200) = 32,768 = 256 x 128.
   if (warp >= 4) {
@@ -478,6 +482,8 @@ __global__ void __launch_bounds__(kThreads2, 2) nvfp4_prefill_a4q_2cta_sm103_ker
 // rows zero), V as FP16 in the MN-major 128B-swizzled operand layout (two
 // chunks of 64 head dims x 112 keys).  Keys past kv_len are zeros.
 __global__ void __launch_bounds__(128) nvfp4_prefill_repack112_kernel(PrefillArgs a) {
+  grid_dep_launch();
+  grid_dep_wait();  // the schedule
   const int tid = threadIdx.x;
   const int total = a.work[1];
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -545,16 +551,13 @@ size_t prefill_a4q_2cta_record_bytes() { return kRecord2; }
 int prefill_a4q_2cta_tile_keys() { return kBN2; }
 
 cudaError_t launch_prefill_a4q_2cta_repack(const PrefillArgs& a, int num_sms, cudaStream_t s) {
-  nvfp4_prefill_repack112_kernel<<<num_sms * 8, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(nvfp4_prefill_repack112_kernel, dim3(num_sms * 8), dim3(128), 0, s, a);
 }
 
 cudaError_t launch_prefill_a4q_2cta(const PrefillArgs& a, int num_sms, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(nvfp4_prefill_a4q_2cta_sm103_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc2);
+  cudaError_t e = set_kernel_smem(reinterpret_cast<const void*>(nvfp4_prefill_a4q_2cta_sm103_kernel), kAlloc2, true);
   if (e != cudaSuccess) return e;
-  nvfp4_prefill_a4q_2cta_sm103_kernel<<<2 * num_sms, kThreads2, kAlloc2, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(nvfp4_prefill_a4q_2cta_sm103_kernel, dim3(2 * num_sms), dim3(kThreads2), kAlloc2, s, a);
 }
 
 }  // namespace nvfp4kv

@@ -4,6 +4,26 @@
 #include "kernels.cuh"
 
 namespace nvfp4kv {
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes (its set-up overlapping that
+// kernel's tail) and waits for it in grid_dep_wait before reading its results.
+template <class Args>
+inline cudaError_t launch_pdl(void (*kernel)(Args), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              const Args& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 namespace prefill_detail {
 
 constexpr float kLog2e = 1.4426950408889634f;
