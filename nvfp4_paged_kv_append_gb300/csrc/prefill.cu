@@ -176,7 +176,7 @@ __device__ __forceinline__ Bars make_bars(uint64_t* base) {
 }
 
 // ---------------------------------------------------------------------------
-// loader warps (12 and 14): t = 0..63.  In-kernel mode, thread t gathers a
+// loader warps (1 and 2): t = 0..63.  In-kernel mode, thread t gathers a
 // slice of page p = t / 8 of the tile with cp.async; a page past kv_len (or
 // with an invalid id) reads as zeros.  Repack mode: thread 0 issues the one
 // bulk copy of the tile's record.
