@@ -96,6 +96,7 @@ def _load():
         lib.orc_e4m3_encode.argtypes = [f32]
         lib.orc_e2m1_encode.restype = ctypes.c_uint
         lib.orc_e2m1_encode.argtypes = [f32]
+        lib.orc_e2m1_encode_n.argtypes = [P, i64, P]
         lib.orc_quantize_block16.argtypes = [P, f32, P, P]
         lib.orc_quantize_rows.argtypes = [P, i64, i32, i32, f32, P, P, P]
         lib.orc_dequantize_rows.argtypes = [P, P, i64, i32, P, f32, P]
@@ -155,8 +156,10 @@ def e4m3_encode_array(x) -> np.ndarray:
 
 
 def e2m1_encode_array(q) -> np.ndarray:
-    lib = _load()
-    return np.array([lib.orc_e2m1_encode(float(v)) for v in _f32(q).ravel()], dtype=np.uint8)
+    q = _f32(q).ravel()
+    codes = np.empty(q.size, dtype=np.uint8)
+    _load().orc_e2m1_encode_n(_ptr(q), q.size, _ptr(codes))
+    return codes
 
 
 # --- codec -------------------------------------------------------------------

@@ -76,6 +76,12 @@ unsigned orc_e2m1_encode(float q) {
   return (signbit(q) ? 8u : 0u) | best;
 }
 
+/* The codes of n values, one orc_e2m1_encode call each (a batch entry point
+ * for the format tests' sweeps; no arithmetic of its own). */
+void orc_e2m1_encode_n(const float* q, int64_t n, uint8_t* codes) {
+  for (int64_t i = 0; i < n; ++i) codes[i] = (uint8_t)orc_e2m1_encode(q[i]);
+}
+
 /* One block ([PD] "NVFP4 stores 4.5 bits per value before padding": one E4M3
  * scale for each group of 16 elements; packed E2M1 pairs), steps R1..R4. */
 void orc_quantize_block16(const float* x, float g, uint8_t* packed8,

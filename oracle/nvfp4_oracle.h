@@ -100,6 +100,7 @@ double orc_e2m1_value(unsigned code);   /* code in 0..15 */
 double orc_e4m3_value(unsigned byte);   /* OCP E4M3FN; NaN for 0x7F/0xFF */
 unsigned orc_e4m3_encode(float x);      /* x >= 0, finite: R1 rounding */
 unsigned orc_e2m1_encode(float q);      /* R2 rounding, returns 4-bit code */
+void orc_e2m1_encode_n(const float* q, int64_t n, uint8_t* codes); /* the same, n values */
 
 /* One 16-value block with scale g (R1..R4): writes 8 packed bytes and one
  * scale byte. */

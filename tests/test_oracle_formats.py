@@ -90,6 +90,53 @@ def test_e2m1_encode_vs_grid_rounding(orc):
     assert bad.size == 0, [(float(q[i]), int(got[i]), int(ref[i])) for i in bad[:10]]
 
 
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], np.float32)
+
+
+def e2m1_rne_grid_fast(q):
+    """The same grid rounding as e2m1_rne_grid, vectorized: every step is exact
+    in fp32 for |q| < 8 (doubling, rint, halving), and the rounded magnitude
+    is one of the eight grid values, whose index is its code."""
+    a = np.abs(q)
+    r = np.where(a < 2, np.rint(a * 2) / 2, np.where(a < 4, np.rint(a), 2 * np.rint(a / 2)))
+    r = np.minimum(r, np.float32(6.0)).astype(np.float32)
+    code = np.searchsorted(_E2M1_GRID, r).astype(np.uint8)
+    assert np.array_equal(_E2M1_GRID[code], r)
+    return code | (np.signbit(q).astype(np.uint8) << 3)
+
+
+def test_e2m1_encode_every_fp32_in_decision_range(orc):
+    """Every fp32 value in [0.125, 8), both signs (about 10^8 inputs), against
+    the grid rounding.  These binades hold every rounding threshold (0.25 ...
+    5) and the saturation point 6; below 0.125 every value is nearer to 0 than
+    to 0.5, and from 8 up every value saturates, which the sampled checks
+    below and the tie test cover."""
+    lo = int(np.float32(0.125).view(np.uint32))
+    hi = int(np.float32(8.0).view(np.uint32))
+    step = 1 << 23
+    for sign in (0, 1 << 31):
+        for start in range(lo, hi, step):
+            bits = np.arange(start, min(start + step, hi), dtype=np.uint32) | np.uint32(sign)
+            q = bits.view(np.float32)
+            got = orc.e2m1_encode_array(q)
+            ref = e2m1_rne_grid_fast(q)
+            bad = np.nonzero(got != ref)[0]
+            assert bad.size == 0, [(float(q[i]), int(got[i]), int(ref[i])) for i in bad[:10]]
+
+
+def test_e2m1_encode_outside_decision_range(orc):
+    """Below 0.125 (down to the smallest subnormal) the code is +-0; from 8 up
+    (through the largest finite value and infinity) it is +-6."""
+    rng = np.random.default_rng(2)
+    tiny = np.concatenate([np.exp2(rng.uniform(-149, -3, 200000)).astype(np.float32),
+                           np.array([0.0, np.nextafter(np.float32(0.125), np.float32(0)), 1.4e-45], np.float32)])
+    big = np.concatenate([np.exp2(rng.uniform(3, 127.9, 200000)).astype(np.float32),
+                          np.array([8.0, np.finfo(np.float32).max, np.inf], np.float32)])
+    for q, code in ((tiny, 0), (big, 7)):
+        assert np.all(orc.e2m1_encode_array(q) == code)
+        assert np.all(orc.e2m1_encode_array(-q) == (code | 8))
+
+
 def test_e2m1_tie_rules(orc):
     # ties go to the even code: .25->0, .75->1.0, 1.25->1.0, 1.75->2, 2.5->2, 3.5->4, 5->4
     expect = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6, 6.0: 7, 9.0: 7}
