@@ -68,6 +68,35 @@ def test_append_extremes_and_padding():
     _assert_same(cache, G.oracle_pools(inp))
 
 
+def test_append_scale_rounding_boundaries():
+    """Block maxima at every E4M3 rounding midpoint of the scale quotient, and
+    one bf16 step to either side.  With g = fl32(1/6), 6 g rounds to exactly
+    1, so amax / (6 g) is the block maximum itself: at a midpoint the scale
+    byte is decided by the tie rule (nearest even), next to one by the nearer
+    code, and the codes follow from that byte.  Every byte must match."""
+    wl = W.Workload("scale_ties", [1], [128], 2, 2, seed=17)
+    inp = W.make_inputs(wl, with_q=False)
+    e4 = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).float()  # 0 .. 448
+    mids = (e4[1:] + e4[:-1]) / 2
+    assert torch.equal(mids.to(torch.bfloat16).float(), mids)  # at most 5 significant bits
+    mb = mids.to(torch.bfloat16).view(torch.int16)
+    targets = torch.cat([mids, (mb - 1).view(torch.bfloat16).float(), (mb + 1).view(torch.bfloat16).float()])
+    gen = torch.Generator().manual_seed(5)
+    k = inp.k.float().view(-1, 16)                       # one row per 16-value block
+    t = targets[torch.arange(k.shape[0]) % targets.numel()]
+    k = (torch.rand(k.shape, generator=gen) * 2 - 1) * t[:, None]
+    pos = torch.arange(k.shape[0]) % 16                  # the element that carries the maximum
+    sign = torch.where(torch.arange(k.shape[0]) % 3 == 0, -1.0, 1.0)
+    k[torch.arange(k.shape[0]), pos] = sign * t
+    inp.k = k.view_as(inp.k).to(torch.bfloat16)
+    assert torch.equal(inp.k.float().view(-1, 16).abs().amax(1), t)
+    inp.k_global = float(np.float32(1.0 / 6.0))
+    assert np.float32(6.0) * np.float32(inp.k_global) == np.float32(1.0)
+    cache = G.gpu_cache(inp)
+    _assert_same(cache, G.oracle_pools(inp))
+    assert G.nk().nvfp4kv_get_device_status() == 0
+
+
 def test_append_bad_slot_flagged():
     inp = W.make_inputs(W.Workload("bad", [1], [20], 2, 2, seed=2), with_q=False)
     slots = inp.slot_mapping.clone()
