@@ -353,6 +353,41 @@ __device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
 }
 
 // ---------------------------------------------------------------------------
+// The transform warpgroup's conversion of one 128-key tile of packed codes
+// into a 128B-swizzled 16-bit operand tile: 512 units of 32 values (one key,
+// group c of its 128 head dimensions), four per thread.  src(key, c, codes,
+// scales) loads a unit's 16 code bytes and two block-scale bytes and returns
+// false for a unit that stays zero.  Thread (warp w, lane l), pass i takes
+// key 8 (4 i + w) + 4 (l >> 4) + (l & 3) and group c = bits 2-3 of l: the
+// eight lanes of a store phase hold four consecutive keys x both chunk quads
+// of one tile half, so each of their 16-byte stores lands in a different
+// bank group, and key mod 8 (hence the swizzled chunk offsets) is the same
+// in every pass.
+template <bool BF16, class Src>
+__device__ __forceinline__ void tf_convert_tile(uint8_t* tile, int tid, Src src) {
+  const int lane = tid & 31;
+  const int c = ((lane >> 2) & 1) | (((lane >> 3) & 1) << 1);
+  const int key_lo = 4 * (lane >> 4) + (lane & 3);
+  const uint32_t cc = (c & 1) * 4, kx = key_lo & 7;
+  uint8_t* dst0 = tile + (c >> 1) * 16384 + key_lo * 128;
+  const uint32_t ch0 = ((cc + 0) ^ kx) << 4, ch1 = ((cc + 1) ^ kx) << 4;
+  const uint32_t ch2 = ((cc + 2) ^ kx) << 4, ch3 = ((cc + 3) ^ kx) << 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int key8 = 8 * (4 * i + (tid >> 5));
+    uint32_t o0[4] = {0, 0, 0, 0}, o1[4] = {0, 0, 0, 0}, o2[4] = {0, 0, 0, 0}, o3[4] = {0, 0, 0, 0};
+    uint4 v;
+    uint32_t sc;
+    if (src(key8 + key_lo, c, v, sc)) dequant_unit<BF16>(v, sc, o0, o1, o2, o3);
+    uint8_t* dst = dst0 + key8 * 128;
+    *reinterpret_cast<uint4*>(dst + ch0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+    *reinterpret_cast<uint4*>(dst + ch1) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    *reinterpret_cast<uint4*>(dst + ch2) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+    *reinterpret_cast<uint4*>(dst + ch3) = make_uint4(o3[0], o3[1], o3[2], o3[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // transform warpgroup (warps 4-7): thread = Q row / TMEM lane
 template <int VARIANT, bool REPACK>
 __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, uint32_t tbase, int tid) {
@@ -423,38 +458,26 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
           // K -> BF16 (exact), K-major 128B-swizzled operand; buffer b was
           // read by QK(it-2)
           if (it >= 2 && !mbar_wait_warp(&bars.s_full[b], ((it >> 1) - 1u) & 1u, a.status)) return;
-          uint8_t* kb = smem + L::kOffK + b * kTile16;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int u = tid + 128 * i;
-            const int key = u >> 2, c = u & 3;
-            const uint4 src = *reinterpret_cast<const uint4*>(stage + sw64_off(key, c));
-            const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(stage + kKData + key * 8 + 2 * c);
-            uint32_t o0[4], o1[4], o2[4], o3[4];
-            dequant_unit<true>(src, sc01, o0, o1, o2, o3);
-            store_unit_sw128(kb, key, c, o0, o1, o2, o3);
-          }
+          tf_convert_tile<true>(smem + L::kOffK + b * kTile16, tid, [&](int key, int c, uint4& v, uint32_t& sc) {
+            v = *reinterpret_cast<const uint4*>(stage + sw64_off(key, c));
+            sc = *reinterpret_cast<const uint16_t*>(stage + kKData + key * 8 + 2 * c);
+            return true;
+          });
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars.sfb_full[b]);
         }
         // ---- V -> FP16, MN-major 128B-swizzled operand; buffer b was read by PV(it-2)
         if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
-        uint8_t* vb = smem + L::kOffV + b * kTile16;
-        const uint8_t* vd = stage + kKData + kKScale;
-        const uint8_t* vs = vd + kVData;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int u = tid + 128 * i;
-          const int key = u >> 2, c = u & 3;
-          const bool live = key_base + key < item.kv_len;  // invalid pages were loaded as zeros
-          uint32_t o0[4] = {0, 0, 0, 0}, o1[4] = {0, 0, 0, 0}, o2[4] = {0, 0, 0, 0}, o3[4] = {0, 0, 0, 0};
-          if (live) {
-            const uint4 src = *reinterpret_cast<const uint4*>(vd + key * 64 + 16 * c);
-            const uint32_t sc01 = *reinterpret_cast<const uint16_t*>(vs + key * 8 + 2 * c);
-            dequant_unit<false>(src, sc01, o0, o1, o2, o3);
-          }
-          store_unit_sw128(vb, key, c, o0, o1, o2, o3);
+        {
+          const uint8_t* vd = stage + kKData + kKScale;
+          const uint8_t* vs = vd + kVData;
+          tf_convert_tile<false>(smem + L::kOffV + b * kTile16, tid, [&](int key, int c, uint4& v, uint32_t& sc) {
+            if (key_base + key >= item.kv_len) return false;  // invalid pages were loaded as zeros
+            v = *reinterpret_cast<const uint4*>(vd + key * 64 + 16 * c);
+            sc = *reinterpret_cast<const uint16_t*>(vs + key * 8 + 2 * c);
+            return true;
+          });
         }
         fence_proxy_async_smem();
         __syncwarp();

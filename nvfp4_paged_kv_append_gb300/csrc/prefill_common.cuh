@@ -90,24 +90,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // 16-byte chunk `cc` (0..7) of row `r` in a 128B-swizzled [rows][128 B] tile.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t cc) { return r * 128u + (((cc ^ r) & 7u) << 4); }
 
-// Store the four 16-byte chunks o0..o3 of one (key, 32-value group c) unit
-// into a 128B-swizzled operand tile.  Lanes holding groups 2-3 store their
-// chunks in the order 2,3,0,1 so that every 8-lane phase of a warp-wide
-// shared-memory store hits 8 different bank groups.
-__device__ __forceinline__ void store_unit_sw128(uint8_t* tile, int key, int c, const uint32_t (&o0)[4],
-                                                 const uint32_t (&o1)[4], const uint32_t (&o2)[4],
-                                                 const uint32_t (&o3)[4]) {
-  uint8_t* dst = tile + (c >> 1) * 16384;
-  const uint32_t cc = (c & 1) * 4;
-  const bool rot = (c >> 1) != 0;
-  const uint4 a0 = make_uint4(o0[0], o0[1], o0[2], o0[3]), a1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-  const uint4 a2 = make_uint4(o2[0], o2[1], o2[2], o2[3]), a3 = make_uint4(o3[0], o3[1], o3[2], o3[3]);
-  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 2 : 0))) = rot ? a2 : a0;
-  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 3 : 1))) = rot ? a3 : a1;
-  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 0 : 2))) = rot ? a0 : a2;
-  *reinterpret_cast<uint4*>(dst + sw128_off(key, cc + (rot ? 1 : 3))) = rot ? a1 : a3;
-}
-
 // 16-byte chunk `c` (0..3) of row `r` in a 64B-swizzled [rows][64 B] tile.
 __device__ __forceinline__ uint32_t sw64_off(uint32_t r, uint32_t c) { return r * 64u + (((c ^ (r >> 1)) & 3u) << 4); }
 
