@@ -451,13 +451,19 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
       for (int j = 0; j < item.n_tiles; ++j) {
         const uint32_t it = it_ctr + j;
         const uint32_t st = it % L::kStages, b = it & 1u;
-        if (!mbar_wait_warp(&bars.kv_full[st], (it / L::kStages) & 1u, a.status)) return;
+        // A4Q: the stage and the V buffer (read by PV(it-2)) are usually both
+        // complete by now, and are tested at once so that the two round
+        // trips overlap
+        const uint32_t kv_ph = (it / L::kStages) & 1u, prev_ph = ((it >> 1) - 1u) & 1u;
+        if (L::kA4Q && it >= 2 ? !mbar_wait2_warp(&bars.kv_full[st], kv_ph, &bars.pv_done[b], prev_ph, a.status)
+                               : !mbar_wait_warp(&bars.kv_full[st], kv_ph, a.status))
+          return;
         const uint8_t* stage = smem + L::kOffStage + st * L::kStageBytes;
         const int key_base = (item.t0 + j) * kBN;
         if constexpr (!L::kA4Q) {
           // K -> BF16 (exact), K-major 128B-swizzled operand; buffer b was
           // read by QK(it-2)
-          if (it >= 2 && !mbar_wait_warp(&bars.s_full[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+          if (it >= 2 && !mbar_wait_warp(&bars.s_full[b], prev_ph, a.status)) return;
           tf_convert_tile<true>(smem + L::kOffK + b * kTile16, tid, [&](int key, int c, uint4& v, uint32_t& sc) {
             v = *reinterpret_cast<const uint4*>(stage + sw64_off(key, c));
             sc = *reinterpret_cast<const uint16_t*>(stage + kKData + key * 8 + 2 * c);
@@ -467,8 +473,9 @@ __device__ void transform_loop(const PrefillArgs& a, uint8_t* smem, const Bars& 
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars.sfb_full[b]);
         }
-        // ---- V -> FP16, MN-major 128B-swizzled operand; buffer b was read by PV(it-2)
-        if (it >= 2 && !mbar_wait_warp(&bars.pv_done[b], ((it >> 1) - 1u) & 1u, a.status)) return;
+        // ---- V -> FP16, MN-major 128B-swizzled operand; buffer b was read by
+        // PV(it-2) (A4Q: waited for above)
+        if (!L::kA4Q && it >= 2 && !mbar_wait_warp(&bars.pv_done[b], prev_ph, a.status)) return;
         {
           const uint8_t* vd = stage + kKData + kKScale;
           const uint8_t* vs = vd + kVData;

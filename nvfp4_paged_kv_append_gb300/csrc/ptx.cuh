@@ -103,6 +103,26 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, i
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// Whole-warp wait on two phases at once: both are tested before either
+// result is needed, so when both have completed (the common case of a
+// consumer that runs behind its producers) the two round trips overlap.
+// Otherwise the bounded waits above take over, first on bar0, then on bar1.
+__device__ __forceinline__ bool mbar_wait2_warp(uint64_t* bar0, uint32_t parity0, uint64_t* bar1, uint32_t parity1,
+                                                int* status) {
+  uint32_t ok0, ok1;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%2], %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%4], %5;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "selp.u32 %1, 1, 0, q;\n\t}"
+      : "=r"(ok0), "=r"(ok1)
+      : "r"(smem_u32(bar0)), "r"(parity0), "r"(smem_u32(bar1)), "r"(parity1)
+      : "memory");
+  if (__all_sync(0xffffffffu, ok0 != 0 && ok1 != 0)) return true;
+  return mbar_wait_warp(bar0, parity0, status) && mbar_wait_warp(bar1, parity1, status);
+}
+
 // ---- cp.async (LSU path) -----------------------------------------------------------
 // Copies of 16 or 4 bytes global -> shared that read only `src_bytes` bytes
 // of the source (0 or the full size) and fill the rest of the destination
