@@ -82,11 +82,6 @@ __device__ __forceinline__ void dequant8_bf16(uint32_t codes, uint32_t scale_b2,
   }
 }
 
-// Block-scale byte -> f16x2 pair (same value in both halves).
-__device__ __forceinline__ uint32_t scale_f16x2(uint32_t byte) {
-  uint32_t h = cvt_e4m3x2_to_f16x2(byte & 0xFFu);
-  return (h & 0xFFFFu) | (h << 16);
-}
 // Block-scale byte -> bf16 pair holding scale * 2^112 (exact).
 __device__ __forceinline__ uint32_t scale_bf16x2_x2p112(uint32_t byte) {
   float s = e4m3_to_f32(byte) * 5.192296858534828e33f;  // 2^112

@@ -104,7 +104,10 @@ __device__ __forceinline__ void dequant_unit(uint4 src, uint32_t sc01, uint32_t 
     dequant8_bf16(src.z, s1, o2);
     dequant8_bf16(src.w, s1, o3);
   } else {
-    const uint32_t s0 = scale_f16x2(sc01 & 0xFFu), s1 = scale_f16x2(sc01 >> 8);
+    // both scale bytes in one conversion (byte 0 -> low half), then each
+    // broadcast to a pair
+    const uint32_t h = cvt_e4m3x2_to_f16x2(sc01 & 0xFFFFu);
+    const uint32_t s0 = __byte_perm(h, 0u, 0x1010u), s1 = __byte_perm(h, 0u, 0x3232u);
     dequant8_f16(src.x, s0, o0);
     dequant8_f16(src.y, s0, o1);
     dequant8_f16(src.z, s1, o2);
