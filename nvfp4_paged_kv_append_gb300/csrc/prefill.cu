@@ -357,17 +357,17 @@ __device__ void pv_loop(const PrefillArgs& a, uint8_t* smem, const Bars& bars, u
 // into a 128B-swizzled 16-bit operand tile: 512 units of 32 values (one key,
 // group c of its 128 head dimensions), four per thread.  src(key, c, codes,
 // scales) loads a unit's 16 code bytes and two block-scale bytes and returns
-// false for a unit that stays zero.  Thread (warp w, lane l), pass i takes
-// key 8 (4 i + w) + 4 (l >> 4) + (l & 3) and group c = bits 2-3 of l: the
-// eight lanes of a store phase hold four consecutive keys x both chunk quads
-// of one tile half, so each of their 16-byte stores lands in a different
-// bank group, and key mod 8 (hence the swizzled chunk offsets) is the same
-// in every pass.
+// false for a unit that stays zero.  Thread (warp w, lane l = 8 p + j), pass
+// i takes key 8 (4 i + w) + 4 (p >> 1) + (j >> 1) and group c = (j & 1) |
+// (((j >> 2) ^ p) & 1) << 1: the eight lanes of a phase hold four consecutive
+// keys with both parities under each group, so their 16-byte code loads and
+// each of their four 16-byte stores land in eight different bank groups, and
+// key mod 8 (hence the swizzled chunk offsets) is the same in every pass.
 template <bool BF16, class Src>
 __device__ __forceinline__ void tf_convert_tile(uint8_t* tile, int tid, Src src) {
-  const int lane = tid & 31;
-  const int c = ((lane >> 2) & 1) | (((lane >> 3) & 1) << 1);
-  const int key_lo = 4 * (lane >> 4) + (lane & 3);
+  const int lane = tid & 31, j8 = lane & 7, ph = lane >> 3;
+  const int key_lo = 4 * (ph >> 1) + (j8 >> 1);
+  const int c = (j8 & 1) | ((((j8 >> 2) ^ ph) & 1) << 1);
   const uint32_t cc = (c & 1) * 4, kx = key_lo & 7;
   uint8_t* dst0 = tile + (c >> 1) * 16384 + key_lo * 128;
   const uint32_t ch0 = ((cc + 0) ^ kx) << 4, ch1 = ((cc + 1) ^ kx) << 4;
