@@ -441,7 +441,7 @@ FP4PV_MODE = ("experiment: A4Q QK, then P coded to NVFP4 per 16 keys and V re-co
 def shortq_component(nk, nk_bench, dev, K, peaks):
     """Batch 4 x q 128 at the end of kv 2,048, 32/8 heads, permuted pages (the
     repack comparison shape; four q tiles per kv head): A4Q runs the in-kernel
-    mode (repack needs six q tiles per kv head for A4Q), dequant-ahead the
+    mode (repack needs eight q tiles per kv head for A4Q), dequant-ahead the
     repack mode (two)."""
     c = PrefillCase(nk, dev, inputs_of("shortq"))
     wl = c.inp.wl

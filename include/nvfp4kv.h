@@ -156,7 +156,7 @@ int nvfp4_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  *             nvfp4_workspace_bytes(..., total_q, max_pages_per_req * 16)
  *             bytes, the call may also run in repack mode:
  *             when requests average enough q tiles (128 rows of query
- *             tokens x grouped heads) per kv head -- six for A4Q, two for
+ *             tokens x grouped heads) per kv head -- eight for A4Q, two for
  *             dequant-ahead -- V (and K for the
  *             dequant-ahead variant) is first dequantized once per KV
  *             tile (112 keys for A4Q, 128 for dequant-ahead) into the

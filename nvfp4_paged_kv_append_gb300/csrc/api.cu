@@ -344,14 +344,14 @@ int prefill_stages(int stages, const void* q, int64_t total_q, int32_t num_q_hea
   // Repack mode (each V tile dequantized once, into the workspace) when the
   // workspace holds a tile for every (request, kv head, KV tile) the page
   // table allows and each record would be read by enough q tiles: requests
-  // average at least six q tiles per kv head for A4Q, two for dequant-ahead
+  // average at least eight q tiles per kv head for A4Q, two for dequant-ahead
   // (whose in-kernel mode converts K as well).  (A4Q on GB300, whole calls:
-  // four q tiles per kv head, 4 x 128 over 2K, in-kernel 36.5 against repack
-  // 57.0 us; six, 4 x 192 over 2K, 57 us in either mode; eight, 4 x 256 over
-  // 4K, repack 82.6 against 89.7 us.)
+  // six q tiles per kv head, 4 x 192 over 2K, in-kernel 52.9 against repack
+  // 56.0 us; eight, 4 x 256 over 4K, 80.5 against 81.5 us; sixteen, 2 x 512
+  // over 8K, repack 122.5 against 131.7 us.)
   const size_t rbytes = prefill_repack_bytes(variant, batch, c.num_kv_heads, max_kv);
   const int64_t qtiles = (total_q * (num_q_heads / c.num_kv_heads) + kBM - 1) / kBM;
-  const int64_t min_qtiles = variant == NVFP4KV_VARIANT_A4Q ? 6 : 2;
+  const int64_t min_qtiles = variant == NVFP4KV_VARIANT_A4Q ? 8 : 2;
   bool repack = workspace_bytes >= sched1 + rbytes && qtiles >= min_qtiles * batch;
   if (c.fp8 || fp4pv) {  // these read only repacked records
     if (workspace_bytes < sched1 + rbytes) return NVFP4KV_ERR_WORKSPACE;

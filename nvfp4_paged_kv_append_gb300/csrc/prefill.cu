@@ -31,7 +31,7 @@
 // Repack mode follows the pages' "convert an NVFP4 tile once before repeated
 // MMA use": every q tile of a request that visits a KV tile would otherwise
 // dequantize the same V values again.  It is used when the caller's workspace
-// has room and requests have enough q tiles per kv head on average (six for
+// has room and requests have enough q tiles per kv head on average (eight for
 // A4Q, two for dequant-ahead).
 //
 // PV runs on FP16 operands: every dequantized V value (E2M1 x E4M3) is exact

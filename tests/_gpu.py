@@ -150,7 +150,7 @@ def oracle_prefill_cached(cfg, q_mode, rows, causal=True):
 
 def repack_mode_expected(wl, variant=0):
     """The library's rule for repack mode given a workspace with room for the
-    records: requests average at least six 128-row q tiles per kv head for
+    records: requests average at least eight 128-row q tiles per kv head for
     A4Q (variant 0), two for dequant-ahead."""
     qtiles = (wl.total_q * wl.group + 127) // 128
-    return qtiles >= (6 if variant == 0 else 2) * wl.batch
+    return qtiles >= (8 if variant == 0 else 2) * wl.batch

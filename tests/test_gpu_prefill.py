@@ -35,7 +35,7 @@ def _check(inp, cache, pools, variant, q_mode, causal=True, rows=None, mode="aut
 def test_prefill_full_parity(cfg, variant, q_mode, mode):
     """Every row; "auto" runs the repack pre-pass for dequant-ahead (these
     batches average two or more q tiles per kv head) and the in-kernel mode
-    for A4Q (fewer than six), "inkernel" dequantizes V in the kernel."""
+    for A4Q (fewer than eight), "inkernel" dequantizes V in the kernel."""
     inp = G.inputs(cfg)
     cache = G.gpu_cache(inp)
     _check(inp, cache, G.pools_for(cfg), variant, q_mode, mode=mode)
@@ -118,9 +118,9 @@ def test_prefill_long_ragged_every_tile(variant, q_mode):
 @pytest.mark.parametrize("variant,q_mode", VARIANTS)
 def test_prefill_group1_repack(variant, q_mode, mode):
     """One query head per kv head (G = 1): 128 tokens per q tile.  Two
-    requests average seven and a half q tiles per kv head, so "auto" runs the
+    requests average eight and a half q tiles per kv head, so "auto" runs the
     repack-mode kernels (the two-CTA kernel for A4Q); every row is checked."""
-    wl = W.Workload("g1_repack", [900, 800], [1000, 800], 3, 3, seed=17)
+    wl = W.Workload("g1_repack", [1100, 1000], [1200, 1000], 3, 3, seed=17)
     assert G.repack_mode_expected(wl, variant)
     inp = W.make_inputs(wl)
     cache = G.gpu_cache(inp, fill=0x7F)
@@ -150,10 +150,10 @@ def test_prefill_many_short_items(variant, q_mode):
 def test_prefill_wide_groups(group, variant, q_mode, mode):
     """GQA ratios up to the largest the library accepts (128: one query token
     per 128-row q tile), causal, ragged; every row against the oracle.  The
-    requests average six or more q tiles per kv head, so "auto" runs repack
+    requests average eight or more q tiles per kv head, so "auto" runs repack
     mode (the two-CTA kernel for A4Q)."""
     hkv = 2 if group == 32 else 1
-    wl = W.Workload(f"wide_g{group}", [48, 20, 1], [60, 133, 1], group * hkv, hkv, seed=group)
+    wl = W.Workload(f"wide_g{group}", [80, 20, 1], [100, 133, 1], group * hkv, hkv, seed=group)
     assert G.repack_mode_expected(wl, variant)
     inp = W.make_inputs(wl)
     cache = G.gpu_cache(inp, fill=0x7F)
