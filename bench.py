@@ -147,6 +147,25 @@ def prefill_roof_s(wl: W.Workload, peaks, a4q=True) -> float:
     return (f_qk / (p16 * FP4_OVER_BF16) + f_pv / p16) if a4q else (f_qk + f_pv) / p16
 
 
+# Issue cost of one tcgen05.mma by a single thread issuing back to back (one
+# CTA, SM clock stamps; a probe on this GB300): block-scaled FP4 at M = 128,
+# N = 128, K = 64 and f16 at M = 128, N = 128, K = 16 both take 68 cycles, so
+# at M = 128 an FP4 instruction does 4x the f16 work, not the nominal 6x.
+MMA_ISSUE_CYCLES = {"fp4_m128_n128_k64": 68, "f16_m128_n128_k16": 68}
+
+
+def fp4_issue_note(wl: W.Workload, peaks, achieved_tflops: float) -> dict:
+    """The measured M = 128 issue rate beside the nominal ratio the
+    roofline uses, and the fraction the headline would have at that rate."""
+    ratio = (64 / MMA_ISSUE_CYCLES["fp4_m128_n128_k64"]) / (16 / MMA_ISSUE_CYCLES["f16_m128_n128_k16"])
+    f_qk, f_pv = prefill_flops_split(wl)
+    p16 = peaks["bf16_tflops"] * 1e12
+    t = f_qk / (p16 * ratio) + f_pv / p16
+    return {"probe": "one thread issuing back to back, one CTA, cta_group::1 (M = 256 over a CTA pair not built)",
+            "cycles": MMA_ISSUE_CYCLES, "fp4_over_bf16_at_m128": ratio,
+            "frac_at_that_ratio": round(achieved_tflops / (wl.flops() / t / 1e12), 4)}
+
+
 def host_cores() -> int:
     """Host cores this process may run on (its affinity mask)."""
     try:
@@ -355,7 +374,8 @@ def run_ours(args, rank, world, dev):
                      "peak": round(peak_eff, 2), "unit": "TFLOP/s", "frac": round(achieved / peak_eff, 4),
                      "traffic": prefill_traffic_bytes(),
                      "peak_basis": f"t = F_QK/(bf16 x {FP4_OVER_BF16:g}) + F_PV/bf16 with bf16 = {p16} TFLOP/s "
-                                   f"({peaks['source']} burst)"},
+                                   f"({peaks['source']} burst)",
+                     "fp4_mma_issue": fp4_issue_note(wl, peaks, achieved)},
         "components": comps,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,  # append, schedule, repack pre-pass, attention

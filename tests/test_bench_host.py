@@ -64,3 +64,17 @@ def test_cache_and_append_bytes():
     assert e["GB/s"] == pytest.approx(495_127_296 / 1e-4 / 1e9, abs=0.1)
     assert e["frac_of_hbm"] == pytest.approx(e["GB/s"] / PEAKS["hbm_gbs"], abs=1e-4)
     assert math.isclose(bench.FP4_OVER_BF16, 6.0)
+
+
+def test_fp4_issue_note():
+    """At the measured M = 128 issue costs (68 cycles for FP4 K = 64 and for
+    f16 K = 16) an FP4 instruction does 4x the f16 work; the headline's
+    fraction at that ratio uses the same roofline form with 4 in place of 6."""
+    wl = W.full_prefill_16k()
+    note = bench.fp4_issue_note(wl, PEAKS, 1835.76)
+    assert note["fp4_over_bf16_at_m128"] == 4.0
+    half = wl.flops() / 2
+    p16 = PEAKS["bf16_tflops"] * 1e12
+    t4 = half / (4 * p16) + half / p16
+    assert note["frac_at_that_ratio"] == pytest.approx(1835.76e12 / (wl.flops() / t4), abs=1e-4)
+    assert note["frac_at_that_ratio"] > 1835.76e12 * bench.prefill_roof_s(wl, PEAKS) / wl.flops()
